@@ -1,0 +1,638 @@
+"""Benchmark of the paged KV-cache hot path on GB300.
+
+One step is one pass of every timed call of the five synthetic workloads
+(kvgen), in this order:
+  fused_write        kv_fill_slots x4, kv_write_fused_k_norm_rope_bf16 and
+                     kv_write_v_only of 4 x 1024 tokens (8 KV heads, head_dim 128)
+  bf16_prefill       kv_fill_slots x64 and kv_write_bf16 of ~278.5k tokens
+  bf16_decode        paged_decode_attn_bf16, 64 sequences of 512..8192, GQA 32:8
+  fp8k_prefill       kv_fill_slots x128 and kv_write_fp8k of 128 x 32768 tokens
+                     (16 launches of 262144 tokens)
+  fp8k_decode_w0     paged_decode_attn_fp8k, 128 x 32768, no window
+  fp8k_decode_w4096  the same with sliding_window 4096
+  fp8k_mixed_decode  paged_decode_attn_fp8k, 256 sequences of 128..65536
+                     (log-uniform), GQA 64:8, block_size 64, split-KV
+The headline value is the step's algorithmic HBM bytes (what each call must
+read and write, counted per call below) divided by the step time, in GB/s;
+each call's GB/s, tokens/s and fraction of the measured HBM copy rate are
+reported beside it. Inputs are synthetic (kvgen, seeded), resident in HBM
+before the timed region; the step touches ~45 GB, far more than L2, so no
+call finds its inputs in L2 from the previous step.
+
+--impl reference runs the CPU oracle (the reference arm of this benchmark) on
+a bounded sample of the same workloads on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged-decode KV-read GB/s & cache-write tokens/s, % of GB300 HBM peak"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+
+
+def measured_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:  # noqa: BLE001 - the file is optional
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# algorithmic bytes (what a call must move through HBM, per call)
+# ---------------------------------------------------------------------------
+def decode_bytes(seq_lens, window, num_kv_heads, head_dim, k_bytes, num_seqs, num_q_heads,
+                 max_blocks_per_seq):
+    att = 0
+    for L in seq_lens:
+        L = int(L)
+        att += min(L, window) if window else L
+    kv = att * num_kv_heads * head_dim * (k_bytes + 2)
+    q = num_seqs * num_q_heads * head_dim * 2
+    out = num_seqs * num_q_heads * head_dim * 4
+    return kv + q + out + num_seqs * 4
+
+
+def write_bytes_per_token(row, k_out_bytes):
+    # K in (bf16) + K out + V in (bf16) + V out (bf16) + the slot (int64)
+    return row * 2 + row * k_out_bytes + row * 2 + row * 2 + 8
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+class Clocks:
+    """nvidia-smi clock and throttle-reason samples during the timed region."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.path = tempfile.mktemp(suffix=".csv")
+        self.proc = None
+        self.device_index = device_index
+
+    def __enter__(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.device_index}", f"--query-gpu={self.QUERY}", "--format=csv,noheader",
+                 "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:  # noqa: BLE001 - clocks are best effort
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            self.proc.wait()
+            self.f.close()
+
+    def summary(self):
+        if not self.proc or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1].split()[0]))
+                mx.append(float(parts[2].split()[0]))
+            except ValueError:
+                continue
+            for name, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+WORKLOAD_OF_PART = {"fused_write": "fused", "bf16_prefill": "bf16_gqa4", "bf16_decode": "bf16_gqa4",
+                    "fp8k_prefill": "fp8k_long", "fp8k_decode_w0": "fp8k_long", "fp8k_decode_w4096": "fp8k_long",
+                    "fp8k_mixed_decode": "fp8k_mixed"}
+
+
+class GpuStep:
+    def __init__(self, dev, only_part=None):
+        import torch
+
+        import kvgen
+        import paged_kv_cache_fill_gb300 as pk
+        self.torch, self.kvgen, self.pk, self.dev = torch, kvgen, pk, dev
+        self.parts = []          # (name, fn, bytes, tokens, launches)
+        self.ws = None
+        self.only_part = only_part
+        self._setup()
+
+    # -- helpers
+    def _slots_calls(self, w, tables, slots):
+        """One kv_fill_slots per sequence into `slots`; returns the launch count."""
+        pk = self.pk
+        lens = w.seq_lens.tolist()
+        offs = [0]
+        for L in lens:
+            offs.append(offs[-1] + L)
+
+        def run():
+            for s, L in enumerate(lens):
+                pk.kv_fill_slots(slots[offs[s]:offs[s + 1]], tables[s], 0, L, w.block_size)
+        return run, sum(1 for L in lens if L > 0)
+
+    def _setup(self):
+        torch, pk = self.torch, self.pk
+        t0 = time.time()
+        self.ws_bytes = 0  # the workspace must fit every decode of the step
+        self.inputs_h2d, self.outputs_d2h = [], []
+        # Each workload is set up in a method of its own, so every closure
+        # binds its own shapes and buffers.
+        want = WORKLOAD_OF_PART[self.only_part] if self.only_part else None
+        for name, setup in (("fused", self._setup_fused), ("bf16_gqa4", self._setup_bf16_gqa4),
+                            ("fp8k_long", self._setup_fp8k_long), ("fp8k_mixed", self._setup_fp8k_mixed)):
+            if want in (None, name):
+                setup()
+        if self.only_part:
+            self.parts = [p for p in self.parts if p["name"] == self.only_part]
+        self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=self.dev)
+        pk.kv_set_decode_workspace(self.ws)
+        torch.cuda.synchronize()
+        self.setup_s = time.time() - t0
+        self.total_bytes = sum(p["bytes"] for p in self.parts)
+        self.launches = sum(p["launches"] for p in self.parts)
+
+    def _setup_fused(self):
+        torch, kvgen, pk, dev = self.torch, self.kvgen, self.pk, self.dev
+        w = kvgen.fused_write(device=dev)
+        H, D, bs, n = w.num_kv_heads, w.head_dim, w.block_size, w.num_tokens
+        tables = w.block_tables.to(dev)
+        slots = torch.empty(n, dtype=torch.int64, device=dev)
+        kc = kvgen.poisoned_pool(w.num_blocks, bs, H, D, "bf16", dev)
+        vc = kvgen.poisoned_pool(w.num_blocks, bs, H, D, "bf16", dev)
+        fill, nfill = self._slots_calls(w, tables, slots)
+        wt, pos = w.extra["k_norm_weight"].to(dev), w.positions.to(dev)
+        key, value = w.key.contiguous(), w.value.contiguous()
+
+        def run():
+            fill()
+            pk.kv_write_fused_k_norm_rope_bf16(key, wt, pos, kc, slots, n, H, D, 128, bs, 1e-6, 1e6)
+            pk.kv_write_v_only(value, vc, slots, n, H, D, bs, H * D)
+        self.parts.append(dict(name="fused_write", fn=run, tokens=n, launches=nfill + 2,
+                               bytes=n * (2048 + 2048 + 4 + 8 + 2048 + 2048 + 8 + 8), kind="write"))
+        self.inputs_h2d += [key, value, pos, tables]
+
+    def _setup_bf16_gqa4(self):
+        torch, kvgen, pk, dev = self.torch, self.kvgen, self.pk, self.dev
+        w = kvgen.bf16_gqa4(device=dev)
+        H, D, bs, Hq, n = w.num_kv_heads, w.head_dim, w.block_size, w.num_q_heads, w.num_tokens
+        tables = w.block_tables.to(dev)
+        slots = torch.empty(n, dtype=torch.int64, device=dev)
+        kc = kvgen.poisoned_pool(w.num_blocks, bs, H, D, "bf16", dev)
+        vc = kvgen.poisoned_pool(w.num_blocks, bs, H, D, "bf16", dev)
+        fill, nfill = self._slots_calls(w, tables, slots)
+        key, value, q, lens = w.key, w.value, w.q, w.seq_lens.to(dev)
+        out = torch.empty((w.num_seqs, Hq, D), dtype=torch.float32, device=dev)
+
+        def prefill():
+            fill()
+            pk.kv_write_bf16(key, value, kc, vc, slots, n, H, D, bs, H * D, H * D)
+
+        def decode():
+            pk.paged_decode_attn_bf16(q, kc, vc, out, tables, lens, w.max_blocks_per_seq, w.num_seqs, Hq, H, D, bs,
+                                      w.inv_sqrt_d, Hq * D, 0)
+        self.parts.append(dict(name="bf16_prefill", fn=prefill, tokens=n, launches=nfill + 1,
+                               bytes=n * write_bytes_per_token(H * D, 2), kind="write"))
+        self.parts.append(dict(name="bf16_decode", fn=decode, tokens=w.num_seqs,
+                               launches=1 + self._combine(w), kind="decode",
+                               bytes=decode_bytes(w.seq_lens.tolist(), 0, H, D, 2, w.num_seqs, Hq,
+                                                  w.max_blocks_per_seq)))
+        self._grow_ws(w)
+        self.inputs_h2d += [key, value, q, tables, lens]
+        self.outputs_d2h += [out]
+
+    def _setup_fp8k_long(self):
+        torch, kvgen, pk, dev = self.torch, self.kvgen, self.pk, self.dev
+        w = kvgen.fp8k_long(device=dev)
+        H, D, bs, Hq, n = w.num_kv_heads, w.head_dim, w.block_size, w.num_q_heads, w.num_tokens
+        tables = w.block_tables.to(dev)
+        slots = torch.empty(n, dtype=torch.int64, device=dev)
+        kc = kvgen.poisoned_pool(w.num_blocks, bs, H, D, "fp8", dev)
+        vc = kvgen.poisoned_pool(w.num_blocks, bs, H, D, "bf16", dev)
+        fill, nfill = self._slots_calls(w, tables, slots)
+        key, value, q, lens, k_scale = w.key, w.value, w.q, w.seq_lens.to(dev), w.k_scale
+        chunk = 262144
+        chunks = [(c, min(n, c + chunk)) for c in range(0, n, chunk)]
+
+        def write_chunk(c0, c1):
+            pk.kv_write_fp8k(key[c0:c1], value[c0:c1], kc, vc, slots[c0:c1], c1 - c0, H, D, bs, H * D, H * D,
+                             k_scale)
+
+        def prefill():
+            fill()
+            for c0, c1 in chunks:
+                write_chunk(c0, c1)
+
+        def make_decode(win, out):
+            def decode():
+                pk.paged_decode_attn_fp8k(q, kc, vc, out, tables, lens, w.max_blocks_per_seq, w.num_seqs, Hq, H, D,
+                                          bs, w.inv_sqrt_d, k_scale, Hq * D, win)
+            return decode
+        self.fp8_chunks, self.fp8_write_chunk, self.fp8_row = chunks, write_chunk, H * D
+        self.parts.append(dict(name="fp8k_prefill", fn=prefill, tokens=n, launches=nfill + len(chunks),
+                               bytes=n * write_bytes_per_token(H * D, 1), kind="write"))
+        outs = []
+        for win in (0, 4096):
+            out = torch.empty((w.num_seqs, Hq, D), dtype=torch.float32, device=dev)
+            outs.append(out)
+            self.parts.append(dict(name=f"fp8k_decode_w{win}", fn=make_decode(win, out), tokens=w.num_seqs,
+                                   launches=1 + self._combine(w), kind="decode",
+                                   bytes=decode_bytes(w.seq_lens.tolist(), win, H, D, 1, w.num_seqs, Hq,
+                                                      w.max_blocks_per_seq)))
+        self._grow_ws(w)
+        self.inputs_h2d += [key, value, q, tables, lens]
+        self.outputs_d2h += outs
+
+    def _setup_fp8k_mixed(self):
+        torch, kvgen, pk, dev = self.torch, self.kvgen, self.pk, self.dev
+        w = kvgen.fp8k_mixed(device=dev)
+        H, D, bs, Hq, n = w.num_kv_heads, w.head_dim, w.block_size, w.num_q_heads, w.num_tokens
+        tables = w.block_tables.to(dev)
+        slots = torch.empty(n, dtype=torch.int64, device=dev)
+        kc = kvgen.poisoned_pool(w.num_blocks, bs, H, D, "fp8", dev)
+        vc = kvgen.poisoned_pool(w.num_blocks, bs, H, D, "bf16", dev)
+        fill, _ = self._slots_calls(w, tables, slots)
+        fill()
+        chunk = 262144
+        for c0 in range(0, n, chunk):   # the cache is written once, untimed
+            c1 = min(n, c0 + chunk)
+            pk.kv_write_fp8k(w.key[c0:c1], w.value[c0:c1], kc, vc, slots[c0:c1], c1 - c0, H, D, bs, H * D, H * D,
+                             w.k_scale)
+        torch.cuda.synchronize()
+        w.key = w.value = None
+        q, lens, k_scale = w.q, w.seq_lens.to(dev), w.k_scale
+        out = torch.empty((w.num_seqs, Hq, D), dtype=torch.float32, device=dev)
+
+        def decode():
+            pk.paged_decode_attn_fp8k(q, kc, vc, out, tables, lens, w.max_blocks_per_seq, w.num_seqs, Hq, H, D, bs,
+                                      w.inv_sqrt_d, k_scale, Hq * D, 0)
+        self.parts.append(dict(name="fp8k_mixed_decode", fn=decode, tokens=w.num_seqs,
+                               launches=1 + self._combine(w), kind="decode",
+                               bytes=decode_bytes(w.seq_lens.tolist(), 0, H, D, 1, w.num_seqs, Hq,
+                                                  w.max_blocks_per_seq)))
+        self._grow_ws(w)
+        self.inputs_h2d += [q, tables, lens]
+        self.outputs_d2h += [out]
+
+    def _grow_ws(self, w):
+        self.ws_bytes = max(self.ws_bytes, self.pk.kv_decode_workspace_bytes(
+            w.max_blocks_per_seq, w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size))
+
+    @staticmethod
+    def _combine(w):
+        # the split-KV combine kernel runs when a sequence can span more than 8 tiles of 16 positions
+        return 1 if w.max_blocks_per_seq * w.block_size > 8 * 16 else 0
+
+    def run_step(self, events=None):
+        torch = self.torch
+        for i, p in enumerate(self.parts):
+            if events is not None:
+                events[i][0].record()
+            p["fn"]()
+            if events is not None:
+                events[i][1].record()
+
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    import __graft_entry__
+    __graft_entry__.build()
+    import paged_kv_cache_fill_gb300 as pk
+
+    step = GpuStep(dev, args.part)
+    stream = torch.cuda.current_stream()
+    if args.part:
+        # one part only, for profiling: warm-up, then `steps` runs, no report
+        for _ in range(args.warmup + args.steps):
+            step.run_step()
+        torch.cuda.synchronize()
+        assert pk.kv_get_device_error() == 0
+        print(json.dumps({"part": args.part, "runs": args.warmup + args.steps, "ok": True}))
+        return
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        step.run_step()
+    barrier()
+    assert pk.kv_get_device_error() == 0, "kernel fault bits set during warm-up"
+
+    nparts = len(step.parts)
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nparts)]
+          for _ in range(args.steps)]
+    with Clocks(local) as clk:
+        barrier()
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for k in range(args.steps):
+            step.run_step(ev[k])
+        t_end.record(stream)
+        barrier()
+    clocks = clk.summary()
+    elapsed_ms = t_start.elapsed_time(t_end)
+    ms_per_step = elapsed_ms / args.steps
+    part_ms = [statistics.mean(ev[k][i][0].elapsed_time(ev[k][i][1]) for k in range(args.steps))
+               for i in range(nparts)]
+    if world > 1:
+        t = torch.tensor([ms_per_step], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_per_step = float(t.item())
+
+    peak, peak_kind = measured_peak()
+    value = step.total_bytes * world / (ms_per_step * 1e-3) / 1e9
+
+    # per-launch timing of the dominant kernel
+    dominant = max(range(nparts), key=lambda i: part_ms[i])
+    dom = step.parts[dominant]
+    roofline = dominant_roofline(step, dom, stream, peak, peak_kind, args)
+
+    parts = {}
+    for p, ms in zip(step.parts, part_ms):
+        gbs = p["bytes"] / (ms * 1e-3) / 1e9
+        parts[p["name"]] = {"ms": round(ms, 4), "GB_per_s": round(gbs, 1),
+                            "tokens_per_s": round(p["tokens"] / (ms * 1e-3), 1),
+                            "frac_measured_hbm": round(gbs / peak, 4),
+                            "frac_nominal_8TBs": round(gbs / NOMINAL_HBM_GBS, 4),
+                            "algorithmic_bytes": int(p["bytes"]), "launches": p["launches"]}
+
+    e2e = run_e2e(step, args, dev, world)
+    cpu = cpu_baseline(args) if (rank == 0 and world == 1 and not args.no_cpu_baseline) else None
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16/e4m3 storage, fp32 compute",
+            "data": "synthetic (kvgen, seeded), inputs resident in HBM",
+            "config": {"workload": "one pass of every timed call of the five paged-KV workloads "
+                                   "(fused_write, bf16_gqa4 prefill+decode, fp8k_long prefill+decode W=0/4096, "
+                                   "fp8k_mixed decode)",
+                       "l2": "inputs larger than L2 (the step moves ~45 GB; no call's inputs stay in L2)",
+                       "algorithmic_bytes_per_step": int(step.total_bytes),
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "parts": parts,
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": step.launches * args.steps,
+            "clocks": clocks,
+            "setup_s": round(step.setup_s, 1),
+        }
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def dominant_roofline(step, dom, stream, peak, peak_kind, args):
+    """Per-launch CUDA-event timing of the dominant part's main kernel."""
+    import torch
+    torch.cuda.synchronize()
+    if dom["name"] == "fp8k_prefill":
+        # the 16 kv_write_fp8k launches; bytes per launch from the tokens it writes
+        times, nbytes = [], []
+        for _ in range(max(args.steps, 3)):
+            for c0, c1 in step.fp8_chunks:
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                step.fp8_write_chunk(c0, c1)
+                b.record(stream)
+                times.append((a, b))
+                nbytes.append((c1 - c0) * write_bytes_per_token(step.fp8_row, 1))
+        torch.cuda.synchronize()
+        ms = [a.elapsed_time(b) for a, b in times]
+        kernel = "kv_write_fp8k (write_fp8k_kernel)"
+        achieved = statistics.mean(n / (m * 1e-3) / 1e9 for n, m in zip(nbytes, ms))
+        per_launch = statistics.mean(nbytes)
+    else:
+        times = []
+        for _ in range(max(args.steps, 3)):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            dom["fn"]()
+            b.record(stream)
+            times.append((a, b))
+        torch.cuda.synchronize()
+        ms = [a.elapsed_time(b) for a, b in times]
+        kernel = f"{dom['name']} (decode_kernel + combine_kernel)"
+        per_launch = dom["bytes"]
+        achieved = per_launch / (statistics.mean(ms) * 1e-3) / 1e9
+    traffic = profiled_traffic(dom["name"])
+    return {"bound": "hbm", "kernel": kernel, "achieved": round(achieved, 1), "peak": peak,
+            "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
+            "algorithmic_bytes_per_launch": int(per_launch), "avg_launch_ms": round(statistics.mean(ms), 4),
+            "traffic": traffic}
+
+
+def profiled_traffic(part_name):
+    """DRAM bytes per launch from the committed ncu summary of the current
+    kernels (profiles/traffic.json), or None when there is none."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            return json.load(f).get(part_name)
+    except Exception:  # noqa: BLE001 - optional file
+        return None
+
+
+def run_e2e(step, args, dev, world):
+    """The same step through the public API with host buffers: every step
+    copies its inputs from pinned host memory to the device, runs the calls
+    and reads the outputs back."""
+    import torch
+    host_in = [t.to("cpu").pin_memory() for t in step.inputs_h2d]
+    host_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in step.outputs_d2h]
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    stream = torch.cuda.current_stream()
+    steps = max(1, min(args.steps, 5))
+
+    def one():
+        for h, d in zip(host_in, step.inputs_h2d):
+            d.copy_(h, non_blocking=True)
+        step.run_step()
+        for h, d in zip(host_out, step.outputs_d2h):
+            h.copy_(d, non_blocking=True)
+
+    one()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        one()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    return {"value": round(step.total_bytes * world / (ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+            "ms_per_step": round(ms, 3), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "steps": steps}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle: the cpu_baseline leg and the reference arm
+# ---------------------------------------------------------------------------
+def oracle_sample(budget_s: float):
+    """Time the oracle on a bounded sample of the workloads: the fused write of
+    the first 256 tokens, the BF16 write of a few sequences, and decode of
+    sampled (sequence, query head) pairs from each decode workload, until
+    about `budget_s` of CPU time. Returns (algorithmic bytes, seconds,
+    description)."""
+    import numpy as np
+    import torch
+
+    import kvgen
+    import oracle
+    oracle.build()
+
+    def u16(t):
+        return np.ascontiguousarray(t.contiguous().view(torch.int16).numpy().view(np.uint16))
+
+    done_bytes, elapsed, pieces = 0, 0.0, []
+    # fused write, 256 tokens
+    w = kvgen.fused_write(seqs=1, tokens_per_seq=256)
+    H, D, bs = w.num_kv_heads, w.head_dim, w.block_size
+    slots = oracle.fill_slots(w.block_tables[0].numpy(), 0, 256, bs)
+    kc = np.zeros((w.num_blocks, bs, H, D), np.uint16)
+    t = time.perf_counter()
+    oracle.write_fused_k_norm_rope_bf16(u16(w.key), u16(w.extra["k_norm_weight"]), w.positions.numpy(), kc, slots,
+                                        256, H, D, 128, bs, 1e-6, 1e6)
+    oracle.write_v_only(u16(w.value), kc.copy(), slots, 256, H, D, bs, H * D)
+    elapsed += time.perf_counter() - t
+    done_bytes += 256 * 8216
+    pieces.append("fused+v_only 256 tokens")
+
+    # decode: sequences of the decode workloads, one query head each, rotating
+    rng = np.random.default_rng(0)
+    specs = [("bf16_gqa4", False, 0), ("fp8k_long", True, 0), ("fp8k_long", True, 4096), ("fp8k_mixed", True, 0)]
+    made = {}
+    n_dec = 0
+    while elapsed < budget_s and n_dec < 400:
+        name, fp8, win = specs[n_dec % len(specs)]
+        if name not in made:
+            gen = {"bf16_gqa4": lambda: kvgen.custom(1003, seq_lens=[4352], num_q_heads=32, num_kv_heads=8,
+                                                     head_dim=128, block_size=16),
+                   "fp8k_long": lambda: kvgen.custom(1004, seq_lens=[32768], num_q_heads=32, num_kv_heads=8,
+                                                     head_dim=128, block_size=16, fp8=True),
+                   "fp8k_mixed": lambda: kvgen.custom(1005, seq_lens=[10500], num_q_heads=64, num_kv_heads=8,
+                                                      head_dim=128, block_size=64, fp8=True)}[name]
+            ww = gen()
+            Hh, Dd, bsz = ww.num_kv_heads, ww.head_dim, ww.block_size
+            sl = oracle.fill_slots(ww.block_tables[0].numpy(), 0, int(ww.seq_lens[0]), bsz)
+            vr = np.zeros((ww.num_blocks, bsz, Hh, Dd), np.uint16)
+            if fp8:
+                kr = np.zeros((ww.num_blocks, bsz, Hh, Dd), np.uint8)
+                oracle.write_fp8k(u16(ww.key), u16(ww.value), kr, vr, sl, len(sl), Hh, Dd, bsz, Hh * Dd, Hh * Dd,
+                                  ww.k_scale)
+            else:
+                kr = np.zeros((ww.num_blocks, bsz, Hh, Dd), np.uint16)
+                oracle.write_bf16(u16(ww.key), u16(ww.value), kr, vr, sl, len(sl), Hh, Dd, bsz, Hh * Dd, Hh * Dd)
+            made[name] = (ww, kr, vr)
+        ww, kr, vr = made[name]
+        h = int(rng.integers(ww.num_q_heads))
+        t = time.perf_counter()
+        oracle.decode_one(u16(ww.q), None if fp8 else kr, kr if fp8 else None, vr, ww.block_tables.numpy(),
+                          ww.seq_lens.numpy(), ww.max_blocks_per_seq, ww.num_q_heads, ww.num_kv_heads,
+                          ww.head_dim, ww.block_size, ww.inv_sqrt_d, ww.k_scale, ww.num_q_heads * ww.head_dim,
+                          win, 0, h)
+        elapsed += time.perf_counter() - t
+        L = int(ww.seq_lens[0])
+        att = min(L, win) if win else L
+        # one query head's share of the decode's KV bytes (the whole group's
+        # bytes are read once per KV head on the GPU; per query head here)
+        done_bytes += att * ww.head_dim * ((1 if fp8 else 2) + 2)
+        n_dec += 1
+    pieces.append(f"{n_dec} single-(sequence, query head) decodes over lengths 4352/32768/4096-window/10500")
+    return done_bytes, elapsed, "; ".join(pieces)
+
+
+def cpu_baseline(args):
+    nbytes, secs, what = oracle_sample(args.cpu_budget)
+    return {"value": round(nbytes / secs / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": what, "seconds": round(secs, 2)}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    vals = []
+    for _ in range(args.warmup):
+        oracle_sample(min(args.cpu_budget, 5.0))
+    per_step = max(2.0, args.cpu_budget / max(args.steps, 1))
+    what = ""
+    t_total, b_total = 0.0, 0
+    for _ in range(args.steps):
+        nbytes, secs, what = oracle_sample(per_step)
+        vals.append(nbytes / secs / 1e9)
+        t_total += secs
+        b_total += nbytes
+    value = b_total / t_total / 1e9
+    line = {"metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(t_total / args.steps * 1e3, 1), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64 compute (oracle)", "data": "synthetic (kvgen)",
+            "impl": "reference",
+            "config": {"workload": "bounded sample of the five paged-KV workloads on the host cores",
+                       "parallelism": "1 CPU thread"},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": what},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time for the CPU baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--part", choices=sorted(WORKLOAD_OF_PART), default=None,
+                    help="set up one workload and run one part only (for ncu captures); prints no bench line")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "gb300":
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,219 @@
+/*
+ * pagedkv.h — C ABI of the GB300 (sm_103a) paged KV-cache library.
+ *
+ * The paged KV-cache hot path of an LLM decode server: slot filling, cache
+ * writes (BF16, FP8-E4M3 K with BF16 V, fused RMSNorm/RoPE K, V only) and
+ * paged decode attention (BF16 and FP8 K). The calls and their argument
+ * order follow the Rust launchers on the pages
+ *   "spark_model/layers/ops/kv_cache.rs"              (written [kv_cache.rs]) and
+ *   "metrale_model_layers/layers/ops/kv_cache_fp8k.rs" (written [kv_cache_fp8k.rs]),
+ * with the launcher's GPU/kernel handles dropped and the stream last.
+ *
+ * Conventions for every call
+ *   - Pointers marked "device" are CUDA device (or managed) memory owned by
+ *     the caller; the library never allocates, frees or keeps them, and never
+ *     synchronises. Every call is asynchronous on `stream` (a cudaStream_t;
+ *     NULL means the legacy default stream) and returns once the work is
+ *     queued.
+ *   - BF16 data are passed as their 16-bit patterns (kv_bf16_t), FP8 data as
+ *     E4M3 ("FN": no infinities, max 448, NaN 0x7F/0xFF) codes (kv_e4m3_t).
+ *   - Cache pools are [num_blocks, block_size, num_kv_heads, head_dim], row
+ *     major ("NHD" within a block). A flat slot s is row s % block_size of
+ *     block s / block_size, so its num_kv_heads * head_dim elements start at
+ *     element s * num_kv_heads * head_dim of the pool base pointer.
+ *   - A negative slot in slot_mapping marks a padding token: nothing is
+ *     written for it.
+ *   - Return value: KV_OK, or an error code below. Argument errors are found
+ *     on the host before anything is queued. Errors in device-resident data
+ *     (a slot or block id outside the pool, a table shorter than a sequence)
+ *     cannot be seen on the host; keeping them in range is the caller's
+ *     contract, as with the pages' kernels. Calls with no work
+ *     (count == 0, num_tokens == 0, num_seqs == 0) return KV_OK and launch
+ *     nothing, as [kv_cache.rs] `fill_slots_from_block_table` does for
+ *     count == 0.
+ */
+#ifndef PAGEDKV_H
+#define PAGEDKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define PAGEDKV_API __attribute__((visibility("default")))
+#else
+#define PAGEDKV_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t kv_bf16_t; /* BF16 bit pattern */
+typedef uint8_t kv_e4m3_t;  /* FP8 E4M3 code */
+
+enum kv_status {
+    KV_OK = 0,
+    KV_ERR_INVALID_ARG = 1,  /* null pointer with work to do, bad shape or stride */
+    KV_ERR_UNSUPPORTED = 2,  /* legal but outside what the kernels implement */
+    KV_ERR_CUDA = 3,         /* a CUDA runtime or driver call failed */
+    KV_ERR_DEVICE = 4        /* a kernel reported a fault in device data or a wait timeout */
+};
+
+/* Human-readable text of a status code (static storage). */
+PAGEDKV_API const char *kv_status_string(int status);
+
+/* ------------------------------------------------------------------------
+ * Slot filling.  [kv_cache.rs] `fill_slots_from_block_table`.
+ *
+ * slots[i] = block_table[p / block_size] * block_size + p % block_size for
+ * p = start_pos + i, i < count.
+ *   slots        device int64[count], written.
+ *   block_table  device int32[ceil((start_pos + count) / block_size)], the
+ *                sequence's physical block ids in logical order. A negative
+ *                id gives a negative (skipped) slot.
+ *   block_size   > 0.
+ * ---------------------------------------------------------------------- */
+PAGEDKV_API int kv_fill_slots(int64_t *slots, const int32_t *block_table, uint32_t start_pos, uint32_t count,
+                  uint32_t block_size, void *stream);
+
+/* ------------------------------------------------------------------------
+ * BF16 cache write.  [kv_cache.rs] `reshape_and_cache` ("BF16 reshape and
+ * cache — no quantization, direct BF16 copy"; its kernel-name line is a
+ * garbled FP8 name and is not followed).
+ *
+ * For token t < num_tokens with slot = slot_mapping[t] >= 0 and head h:
+ *   k_cache[slot][h][:] = key[t * key_stride + h * head_dim + :]
+ *   v_cache[slot][h][:] = value[t * value_stride + h * head_dim + :]
+ * bit for bit.
+ *   key, value        device bf16, row t at element t * key_stride (resp.
+ *                     value_stride); strides >= num_kv_heads * head_dim.
+ *   k_cache, v_cache  device bf16 pools.
+ *   slot_mapping      device int64[num_tokens].
+ * Distinct tokens must not share a slot (their order is then unspecified).
+ * ---------------------------------------------------------------------- */
+PAGEDKV_API int kv_write_bf16(const kv_bf16_t *key, const kv_bf16_t *value, kv_bf16_t *k_cache,
+                  kv_bf16_t *v_cache, const int64_t *slot_mapping, uint32_t num_tokens,
+                  uint32_t num_kv_heads, uint32_t head_dim, uint32_t block_size,
+                  uint32_t key_stride, uint32_t value_stride, void *stream);
+
+/* ------------------------------------------------------------------------
+ * FP8-K / BF16-V cache write.  [kv_cache_fp8k.rs] module invariants: K is
+ * stored as k / k_scale in E4M3 in the NHD layout; argument order of
+ * `reshape_and_cache_fp8k_turbo3v` without its TurboQuant-V arguments. V is a
+ * BF16 copy as in kv_write_bf16.
+ *
+ * code = E4M3(round-to-nearest-even, saturating to +-448)(fp32(k) / k_scale),
+ * where the quotient is the IEEE binary32 division rounded to nearest; NaN
+ * inputs give 0x7F. Bit-exact.
+ *   k_cache_fp8  device uint8 pool; v_cache device bf16 pool.
+ *   k_scale      per-tensor scale, finite and > 0.
+ * ---------------------------------------------------------------------- */
+PAGEDKV_API int kv_write_fp8k(const kv_bf16_t *key, const kv_bf16_t *value, kv_e4m3_t *k_cache_fp8,
+                  kv_bf16_t *v_cache, const int64_t *slot_mapping, uint32_t num_tokens,
+                  uint32_t num_kv_heads, uint32_t head_dim, uint32_t block_size,
+                  uint32_t key_stride, uint32_t value_stride, float k_scale, void *stream);
+
+/* ------------------------------------------------------------------------
+ * Fused K path.  [kv_cache.rs] `fused_k_norm_rope_cache_write_bf16`: RMSNorm,
+ * then RoPE, then the BF16 paged write in one kernel, K kept above BF16
+ * precision throughout and rounded once at the write.
+ *
+ * For token t with slot >= 0 and head h, x = k_in[t][h][:] (contiguous
+ * [num_tokens, num_kv_heads, head_dim], no stride argument on the page):
+ *   y_d = x_d / sqrt(mean(x^2) + rms_eps) * k_norm_weight[d]
+ *   for i < rotary_dim/2, angle = positions[t] * theta^(-2i/rotary_dim):
+ *     o_i = y_i cos - y_{i+R/2} sin,  o_{i+R/2} = y_{i+R/2} cos + y_i sin
+ *   o_d = y_d for d >= rotary_dim
+ *   k_cache[slot][h][d] = BF16_RNE(o_d)
+ * The result is within 1 BF16 ulp of the exactly rounded value.
+ *   k_norm_weight  device bf16[head_dim], shared by all heads.
+ *   positions      device int32[num_tokens], >= 0.
+ *   rotary_dim     even, 8 <= rotary_dim <= head_dim, multiple of 8.
+ * The V half goes through kv_write_v_only.
+ * ---------------------------------------------------------------------- */
+PAGEDKV_API int kv_write_fused_k_norm_rope_bf16(const kv_bf16_t *k_in, const kv_bf16_t *k_norm_weight,
+                                    const int32_t *positions, kv_bf16_t *k_cache,
+                                    const int64_t *slot_mapping, uint32_t num_tokens,
+                                    uint32_t num_kv_heads, uint32_t head_dim, uint32_t rotary_dim,
+                                    uint32_t block_size, float rms_eps, float theta, void *stream);
+
+/* ------------------------------------------------------------------------
+ * V-only write.  [kv_cache.rs] `reshape_and_cache_flash_v_only`: the V half
+ * of kv_write_bf16, so that the fused K kernel stays the only writer of K.
+ * ---------------------------------------------------------------------- */
+PAGEDKV_API int kv_write_v_only(const kv_bf16_t *value, kv_bf16_t *v_cache, const int64_t *slot_mapping,
+                    uint32_t num_tokens, uint32_t num_kv_heads, uint32_t head_dim,
+                    uint32_t block_size, uint32_t value_stride, void *stream);
+
+/* ------------------------------------------------------------------------
+ * Paged decode attention.  [kv_cache.rs] `paged_decode_attn_fp8` doc (one
+ * query per (query head, sequence); block_tables int32[num_seqs *
+ * max_blocks_per_seq]; seq_lens int32[num_seqs]) and the argument list of
+ * `paged_decode_attn_bf16k_turbo3v` without its TurboQuant-V arguments
+ * (q_stride, sliding_window). [kv_cache_fp8k.rs]: the FP8 variant multiplies
+ * the stored K by k_scale, which follows inv_sqrt_d in the argument list.
+ *
+ * For sequence s and query head h, with g = num_q_heads / num_kv_heads and
+ * KV head h / g, L = seq_lens[s] (cached tokens, the current token included)
+ * and start = (sliding_window > 0 ? max(0, L - sliding_window) : 0):
+ *   position p in [start, L) lives at row p % block_size of block
+ *   block_tables[s * max_blocks_per_seq + p / block_size];
+ *   score_p = inv_sqrt_d * (q[s * q_stride + h * head_dim + :] . k_p)
+ *   output[s][h][:] = sum_p softmax(score)_p * v_p     (zeros if L == 0)
+ *   q       device bf16; q_stride (elements between sequences) >= num_q_heads * head_dim.
+ *   output  device float32[num_seqs, num_q_heads, head_dim], written.
+ *   seq_lens[s] <= max_blocks_per_seq * block_size.
+ * Supported: head_dim in {64, 128, 256} (FP8: {128, 256}); block_size a power
+ * of two in [8, 256]; g <= 16; q, caches and q_stride 16-byte aligned.
+ * Long sequences are split across CTAs (flash-decoding) when a workspace was
+ * registered with kv_set_decode_workspace; without one every (sequence, KV
+ * head group) runs in one CTA (same result, less parallelism).
+ * ---------------------------------------------------------------------- */
+PAGEDKV_API int paged_decode_attn_bf16(const kv_bf16_t *q, const kv_bf16_t *k_cache, const kv_bf16_t *v_cache,
+                           float *output, const int32_t *block_tables, const int32_t *seq_lens,
+                           uint32_t max_blocks_per_seq, uint32_t num_seqs, uint32_t num_q_heads,
+                           uint32_t num_kv_heads, uint32_t head_dim, uint32_t block_size,
+                           float inv_sqrt_d, uint32_t q_stride, uint32_t sliding_window,
+                           void *stream);
+
+PAGEDKV_API int paged_decode_attn_fp8k(const kv_bf16_t *q, const kv_e4m3_t *k_cache_fp8,
+                           const kv_bf16_t *v_cache, float *output, const int32_t *block_tables,
+                           const int32_t *seq_lens, uint32_t max_blocks_per_seq,
+                           uint32_t num_seqs, uint32_t num_q_heads, uint32_t num_kv_heads,
+                           uint32_t head_dim, uint32_t block_size, float inv_sqrt_d,
+                           float k_scale, uint32_t q_stride, uint32_t sliding_window,
+                           void *stream);
+
+/* ------------------------------------------------------------------------
+ * Split-KV workspace (not on the pages: flash-decoding partials and the
+ * combine step need scratch). The caller allocates device memory of at
+ * least kv_decode_workspace_bytes(...) for the largest decode it will run
+ * and registers it for the current device; NULL (or 0 bytes) unregisters.
+ * Decode calls on that device use it in stream order, so decode calls that
+ * may run concurrently on different streams need separate devices or must be
+ * ordered by the caller. The library never frees it.
+ * ---------------------------------------------------------------------- */
+PAGEDKV_API size_t kv_decode_workspace_bytes(uint32_t max_blocks_per_seq, uint32_t num_seqs,
+                                 uint32_t num_q_heads, uint32_t num_kv_heads, uint32_t head_dim,
+                                 uint32_t block_size);
+PAGEDKV_API int kv_set_decode_workspace(void *device_ptr, size_t bytes);
+
+/* ------------------------------------------------------------------------
+ * Device-side fault word. Kernels that meet bad device data (a slot mapping
+ * or table value they refuse to use, a pipeline wait that ran out of time)
+ * skip the work, set a bit here and return instead of faulting or hanging.
+ * kv_get_device_error synchronises the current device, returns the bits seen
+ * since the last clear (0 = none) in *bits and clears them.
+ *   bit 0: a decode pipeline wait timed out
+ *   bit 1: seq_lens[s] exceeded max_blocks_per_seq * block_size (clamped)
+ * ---------------------------------------------------------------------- */
+PAGEDKV_API int kv_get_device_error(uint32_t *bits);
+
+/* Number of decode CTAs per SM and SM count the library launches with on the
+ * current device, for benchmarks (optional outputs may be NULL). */
+PAGEDKV_API int kv_device_info(int *num_sms, int *decode_ctas);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PAGEDKV_H */

@@ -74,11 +74,28 @@ def _gen(seed: int, device) -> torch.Generator:
     return g
 
 
+# Large tensors are drawn in row chunks of this many elements (at most), so
+# no full-size float32 temporary is ever materialised; the chunking is part of
+# the recipe (the same seed and shape always give the same bytes).
+CHUNK_ELEMS = 1 << 26
+
+
+def _rows_per_chunk(row: int) -> int:
+    return max(1, CHUNK_ELEMS // max(row, 1))
+
+
 def _normal_bf16(shape, sigma, g, device) -> torch.Tensor:
-    x = torch.randn(shape, generator=g, device=device, dtype=torch.float32)
-    if not isinstance(sigma, (int, float)) or sigma != 1:
-        x = x * sigma
-    return x.to(torch.bfloat16)
+    """N(0, sigma) drawn in float32, rounded to BF16 (RNE), row chunk by row chunk."""
+    rows, row = (shape[0], int(torch.tensor(shape[1:]).prod().item()) if len(shape) > 1 else 1)
+    out = torch.empty((rows, row), dtype=torch.bfloat16, device=device)
+    step = _rows_per_chunk(row)
+    for r0 in range(0, rows, step):
+        r1 = min(rows, r0 + step)
+        x = torch.randn((r1 - r0, row), generator=g, device=device, dtype=torch.float32)
+        if not isinstance(sigma, (int, float)) or sigma != 1:
+            x = x * sigma
+        out[r0:r1] = x.to(torch.bfloat16)
+    return out.reshape(shape)
 
 
 def block_tables_from_pool(seq_lens: torch.Tensor, block_size: int, num_blocks: int,
@@ -112,14 +129,21 @@ def _prefill_token_index(seq_lens: torch.Tensor):
 
 def fp8k_keys(num_tokens: int, row: int, g: torch.Generator, device) -> tuple[torch.Tensor, float]:
     """K ~ N(0, 2) with 0.1% of the elements set to +-20 (random sign), and
-    the per-tensor scale max|K| / 448 of the resulting tensor."""
-    k = torch.randn((num_tokens, row), generator=g, device=device, dtype=torch.float32) * 2.0
-    outlier = torch.rand((num_tokens, row), generator=g, device=device) < 1e-3
-    sign = torch.randint(0, 2, (num_tokens, row), generator=g, device=device,
-                         dtype=torch.int8).to(torch.float32) * 2 - 1
-    k = torch.where(outlier, 20.0 * sign, k).to(torch.bfloat16)
-    k_scale = float(k.abs().max().float().item()) / 448.0
-    return k, float(torch.tensor(k_scale, dtype=torch.float32).item())
+    the per-tensor scale max|K| / 448 of the resulting tensor (in float32)."""
+    out = torch.empty((num_tokens, row), dtype=torch.bfloat16, device=device)
+    step = _rows_per_chunk(row)
+    amax = torch.zeros((), dtype=torch.float32, device=device)
+    for r0 in range(0, num_tokens, step):
+        r1 = min(num_tokens, r0 + step)
+        k = torch.randn((r1 - r0, row), generator=g, device=device, dtype=torch.float32) * 2.0
+        outlier = torch.rand((r1 - r0, row), generator=g, device=device) < 1e-3
+        sign = torch.randint(0, 2, (r1 - r0, row), generator=g, device=device,
+                             dtype=torch.int8).to(torch.float32) * 2 - 1
+        kb = torch.where(outlier, 20.0 * sign, k).to(torch.bfloat16)
+        out[r0:r1] = kb
+        amax = torch.maximum(amax, kb.abs().max().float())
+    k_scale = float(amax.item()) / 448.0
+    return out, float(torch.tensor(k_scale, dtype=torch.float32).item())
 
 
 # --------------------------------------------------------------------------

@@ -1,0 +1,733 @@
+// Paged decode attention over a BF16 or FP8-E4M3-K / BF16-V paged cache.
+//
+// [kv_cache.rs] `paged_decode_attn_fp8` doc (one query per (query head,
+// sequence), block_tables i32[num_seqs * max_blocks_per_seq], seq_lens
+// i32[num_seqs]); `paged_decode_attn_bf16k_turbo3v` argument list (q_stride,
+// sliding_window); [kv_cache_fp8k.rs] module invariants (FP8 K is multiplied
+// by k_scale).
+//
+// GB300 design (the pages launch one 256-thread block per (query head,
+// sequence); that re-reads each KV head's bytes once per query head of its
+// group, so it is not followed):
+//   * A work item is (sequence, group of HG KV heads, split of the sequence's
+//     16-token tiles). One persistent CTA per SM walks the items b, b+G, ...
+//     Every KV byte is read exactly once per call.
+//   * Warp 0 is the producer: it walks the items and the block table and
+//     issues TMA tiled loads of each 16-token tile of K and V for the HG
+//     heads (one 16-row x 128-byte box per head and 128-byte chunk, swizzled
+//     so that ldmatrix over 8 token rows is bank-conflict free) plus, on an
+//     item's first tile, a bulk copy of the item's query rows, into a ring of
+//     stages guarded by full/empty mbarriers.
+//   * Warps 1..HG*NT are consumers, one per (KV head, 8-query-head tile). Per
+//     tile: S^T = K Q^T with mma.sync m16n8k16 (16 tokens x 8 query heads),
+//     base-2 online softmax in fp32 with warp-shuffle max, then O^T += V^T P^T
+//     with P split into BF16 hi + lo parts (two MMAs) so the weights keep
+//     ~16 significant bits. FP8 K converts exactly to f16 in registers
+//     (cvt e4m3x2 -> f16x2) against f16 queries scaled by a power of two.
+//   * Split-KV (flash-decoding): items of a sequence write unnormalised
+//     partial outputs with their running max and sum to a caller-provided
+//     workspace; a combine kernel merges them in fixed split order, so the
+//     result is deterministic. Sequences that fit one item are written
+//     directly.
+#include <cudaTypedefs.h>
+#include <math.h>
+
+#include "internal.h"
+#include "../../include/pagedkv.h"
+
+namespace pagedkv {
+
+namespace {
+
+__device__ uint32_t g_decode_error;
+
+constexpr int kTile = 16;            // tokens per stage
+constexpr int kHeaderBytes = 256;    // workspace header (split size)
+constexpr int kItemsPerCtaTarget = 16;
+constexpr float kLog2e = 1.4426950408889634f;
+
+enum : int32_t {
+  kFirst = 1,    // first tile of an item
+  kLast = 2,     // last tile of an item
+  kEmpty = 4,    // the item has no positions: write zeros
+  kSingle = 8,   // the sequence is one item per head group: write the output directly
+  kSentinel = 16 // no more work
+};
+
+struct StageMeta {
+  int32_t seq, hg, split, tile, start, len, flags, pad;
+};
+
+struct DecodeParams {
+  const uint16_t* q;
+  const int32_t* block_tables;
+  const int32_t* seq_lens;
+  float* output;
+  float* ws_o;          // [num_seqs, max_splits, Hq, D] partial outputs (unnormalised)
+  float* ws_ml;         // [num_seqs, max_splits, Hq, 2] running max (log2 units) and sum
+  uint32_t* ws_header;  // split size chosen by the kernel
+  uint32_t max_blocks_per_seq, num_seqs, num_q_heads, num_kv_heads, block_size, block_shift;
+  uint32_t group;       // query heads per KV head
+  uint32_t heads_per_item;  // HG
+  uint32_t num_head_groups;
+  uint32_t q_stride, sliding_window;
+  uint32_t max_splits;  // 0: no workspace, one item per (sequence, head group)
+  uint32_t min_split_tiles;
+  float score_scale;    // inv_sqrt_d * log2(e)   (times k_scale for FP8)
+  uint32_t stages, stage_bytes, k_bytes, v_bytes;  // shared-memory ring geometry
+};
+
+// -------------------------------------------------------------- item walk
+struct SeqSpan {
+  int32_t len, start, t0, ntiles;
+};
+
+__device__ __forceinline__ SeqSpan seq_span(int32_t raw_len, const DecodeParams& p) {
+  SeqSpan s;
+  int32_t L = raw_len < 0 ? 0 : raw_len;
+  const int64_t cap = int64_t(p.max_blocks_per_seq) << p.block_shift;
+  if (L > cap) {
+    L = int32_t(cap);
+    atomicOr(&g_decode_error, kErrSeqLenClamped);
+  }
+  s.len = L;
+  s.start = (p.sliding_window > 0 && int64_t(L) > int64_t(p.sliding_window))
+                ? int32_t(int64_t(L) - int64_t(p.sliding_window))
+                : 0;
+  s.t0 = s.start / kTile;
+  s.ntiles = L > 0 ? (L + kTile - 1) / kTile - s.t0 : 0;
+  return s;
+}
+
+__device__ __forceinline__ int32_t splits_of(int32_t ntiles, uint32_t split_tiles) {
+  const int64_t n = (int64_t(ntiles) + int64_t(split_tiles) - 1) / int64_t(split_tiles);
+  return n < 1 ? 1 : int32_t(n);
+}
+
+// The producer warp walks the item sequence 32 sequences at a time: each
+// lane holds one sequence's item count and the warp keeps an inclusive
+// prefix of the chunk.
+struct Walker {
+  uint32_t chunk_seq;     // first sequence of the cached chunk
+  uint64_t chunk_items;   // items before the chunk
+  uint32_t incl;          // inclusive prefix of item counts within the chunk (this lane)
+  uint32_t chunk_total;
+  int32_t raw_len;        // seq_lens of sequence chunk_seq + lane
+
+  __device__ void load(uint32_t first_seq, const DecodeParams& p, uint32_t split_tiles, uint32_t lane) {
+    chunk_seq = first_seq;
+    const uint32_t s = first_seq + lane;
+    raw_len = s < p.num_seqs ? __ldg(p.seq_lens + s) : 0;
+    uint32_t n = 0;
+    if (s < p.num_seqs) n = p.num_head_groups * uint32_t(splits_of(seq_span(raw_len, p).ntiles, split_tiles));
+    incl = n;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= uint32_t(o)) incl += v;
+    }
+    chunk_total = __shfl_sync(0xffffffffu, incl, 31);
+  }
+};
+
+// -------------------------------------------------------------- the kernel
+template <bool kFp8, int D, int NT>
+__global__ void __launch_bounds__(32 * 9, 1)
+    decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
+                  const DecodeParams p) {
+  constexpr int kKChunks = kFp8 ? D / 128 : D / 64;  // 128-byte chunks per K head row
+  constexpr int kVChunks = D / 64;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.stages * p.stage_bytes);
+  uint64_t* empty = full + p.stages;
+  StageMeta* meta = reinterpret_cast<StageMeta*>(empty + p.stages);
+  __shared__ uint32_t s_split_tiles;
+  __shared__ uint64_t s_total;
+
+  const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t num_consumers = p.heads_per_item * NT;
+
+  if (threadIdx.x == 0) {
+    for (uint32_t s = 0; s < p.stages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], num_consumers);
+    }
+    fence_mbar_init();
+    s_total = 0;
+  }
+  __syncthreads();
+
+  // Split size: enough items for ~kItemsPerCtaTarget per CTA, never below
+  // the minimum the workspace was sized for.
+  if (p.max_splits > 0) {
+    uint64_t local = 0;
+    for (uint32_t s = threadIdx.x; s < p.num_seqs; s += blockDim.x)
+      local += uint64_t(seq_span(__ldg(p.seq_lens + s), p).ntiles);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) local += __shfl_xor_sync(0xffffffffu, local, o);
+    if (lane == 0 && local) atomicAdd(reinterpret_cast<unsigned long long*>(&s_total), local);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      const uint64_t stages_total = s_total * p.num_head_groups;
+      const uint64_t want = (stages_total + uint64_t(gridDim.x) * kItemsPerCtaTarget - 1) /
+                            (uint64_t(gridDim.x) * kItemsPerCtaTarget);
+      uint32_t t = want > p.min_split_tiles ? uint32_t(want) : p.min_split_tiles;
+      s_split_tiles = t;
+      if (blockIdx.x == 0) *p.ws_header = t;
+    }
+  } else if (threadIdx.x == 0) {
+    s_split_tiles = 0x7fffffffu;
+  }
+  __syncthreads();
+  const uint32_t split_tiles = s_split_tiles;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    tma_prefetch_desc(&tmap_k);
+    tma_prefetch_desc(&tmap_v);
+    Walker wk;
+    wk.chunk_items = 0;
+    wk.load(0, p, split_tiles, lane);
+    uint32_t stage = 0, phase = 0;
+    bool ok = true;
+    const uint32_t k_head_bytes = kKChunks * kTile * 128;
+    const uint32_t v_head_bytes = kVChunks * kTile * 128;
+    for (uint64_t it = blockIdx.x; ok; it += gridDim.x) {
+      // locate the item's sequence
+      while (wk.chunk_seq < p.num_seqs && it >= wk.chunk_items + wk.chunk_total) {
+        wk.chunk_items += wk.chunk_total;
+        wk.load(wk.chunk_seq + 32, p, split_tiles, lane);
+      }
+      if (wk.chunk_seq >= p.num_seqs) break;  // past the last item
+      const uint32_t rel = uint32_t(it - wk.chunk_items);
+      const uint32_t ballot = __ballot_sync(0xffffffffu, wk.incl > rel);
+      const uint32_t sl = __ffs(ballot) - 1;
+      const uint32_t s = wk.chunk_seq + sl;
+      const uint32_t incl_s = __shfl_sync(0xffffffffu, wk.incl, sl);
+      const int32_t raw_len = __shfl_sync(0xffffffffu, wk.raw_len, sl);
+      const SeqSpan span = seq_span(raw_len, p);
+      const uint32_t nsplit = uint32_t(splits_of(span.ntiles, split_tiles));
+      const uint32_t items_s = p.num_head_groups * nsplit;
+      const uint32_t j = rel - (incl_s - items_s);  // item index within the sequence
+      const uint32_t hg = j / nsplit, split = j % nsplit;
+      // 64-bit: without a workspace split_tiles is "unbounded" (0x7fffffff)
+      const int64_t tb64 = int64_t(span.t0) + int64_t(split) * int64_t(split_tiles);
+      int64_t te64 = tb64 + int64_t(split_tiles);
+      if (te64 > int64_t(span.t0) + span.ntiles) te64 = int64_t(span.t0) + span.ntiles;
+      const int32_t tile_begin = int32_t(tb64);
+      const int32_t tile_end = int32_t(te64);
+      const int32_t base_flags = (nsplit == 1 ? kSingle : 0);
+      const uint32_t heads_here = (hg + 1) * p.heads_per_item <= p.num_kv_heads
+                                      ? p.heads_per_item
+                                      : p.num_kv_heads - hg * p.heads_per_item;
+      const uint32_t q_bytes = heads_here * p.group * D * 2;
+      const uint16_t* q_src = p.q + uint64_t(s) * p.q_stride + uint64_t(hg) * p.heads_per_item * p.group * D;
+
+      if (tile_begin >= tile_end) {
+        // no positions: one meta-only stage tells the consumers to write zeros
+        if (lane == 0) {
+          if (!mbar_wait(&empty[stage], phase ^ 1)) ok = false;
+          if (ok) {
+            meta[stage] = StageMeta{int32_t(s), int32_t(hg), int32_t(split), 0, 0, 0,
+                                    kFirst | kLast | kEmpty | base_flags, 0};
+            mbar_arrive(&full[stage]);
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (++stage == p.stages) { stage = 0; phase ^= 1; }
+        continue;
+      }
+      const int32_t* table = p.block_tables + uint64_t(s) * p.max_blocks_per_seq;
+      const int32_t tiles_per_block_shift = int32_t(p.block_shift) - 4;  // block_size >= 16
+      int32_t cached_first_block = -1;  // first logical block held by the lanes
+      int32_t cached_block_id = 0;
+      for (int32_t tile = tile_begin; tile < tile_end && ok; ++tile) {
+        const int32_t lblock = tile >> tiles_per_block_shift;
+        if (cached_first_block < 0 || lblock >= cached_first_block + 32) {
+          cached_first_block = lblock;
+          const int32_t want = lblock + int32_t(lane);
+          cached_block_id = want < int32_t(p.max_blocks_per_seq) ? __ldg(table + want) : 0;
+        }
+        const int32_t block_id = __shfl_sync(0xffffffffu, cached_block_id, lblock - cached_first_block);
+        if (lane == 0) {
+          if (!mbar_wait(&empty[stage], phase ^ 1)) ok = false;
+          if (ok) {
+            int32_t flags = base_flags;
+            if (tile == tile_begin) flags |= kFirst;
+            if (tile == tile_end - 1) flags |= kLast;
+            meta[stage] = StageMeta{int32_t(s), int32_t(hg), int32_t(split), tile, span.start,
+                                    span.len, flags, 0};
+            const uint32_t bytes = heads_here * (k_head_bytes + v_head_bytes) +
+                                   ((flags & kFirst) ? q_bytes : 0u);
+            mbar_arrive_expect_tx(&full[stage], bytes);
+            uint8_t* st = smem + stage * p.stage_bytes;
+            const int32_t slot0 = (block_id << p.block_shift) + ((tile << 4) & int32_t(p.block_size - 1));
+            for (uint32_t h = 0; h < heads_here; ++h) {
+              const int32_t head = int32_t(hg * p.heads_per_item + h);
+#pragma unroll
+              for (int c = 0; c < kKChunks; ++c)
+                tma_load_3d(st + (h * kKChunks + c) * (kTile * 128), &tmap_k, 0,
+                            head * kKChunks + c, slot0, &full[stage]);
+#pragma unroll
+              for (int c = 0; c < kVChunks; ++c)
+                tma_load_3d(st + p.k_bytes + (h * kVChunks + c) * (kTile * 128), &tmap_v, 0,
+                            head * kVChunks + c, slot0, &full[stage]);
+            }
+            if (flags & kFirst) bulk_load(st + p.k_bytes + p.v_bytes, q_src, q_bytes, &full[stage]);
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (++stage == p.stages) { stage = 0; phase ^= 1; }
+      }
+    }
+    // sentinel: no more work
+    if (ok && lane == 0) {
+      if (mbar_wait(&empty[stage], phase ^ 1)) {
+        meta[stage].flags = kSentinel;
+        mbar_arrive(&full[stage]);
+      } else {
+        ok = false;
+      }
+    }
+    if (!__all_sync(0xffffffffu, ok) && lane == 0) atomicOr(&g_decode_error, kErrWaitTimeout);
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  const uint32_t task = warp - 1;
+  if (task >= num_consumers) return;
+  const uint32_t hl = task / NT;   // KV head within the item
+  const uint32_t qt = task % NT;   // 8-query-head tile within the group
+  const uint32_t g8 = lane >> 2;   // fragment row group
+  const uint32_t c4 = lane & 3;    // fragment column pair
+  // ldmatrix row/unit of this lane: K (non-transposed A) and V (transposed A)
+  const uint32_t k_row = (lane & 7) + ((lane >> 3) & 1) * 8, k_unit = lane >> 4;
+  const uint32_t v_row = (lane & 7) + (lane >> 4) * 8, v_unit = (lane >> 3) & 1;
+
+  float acc[D / 16][4];
+  float m_run[2], l_run[2];
+  uint32_t qf[D / 16][2];
+  float head_scale[2];
+
+  uint32_t stage = 0, phase = 0;
+  while (true) {
+    if (!mbar_wait(&full[stage], phase)) {
+      if (lane == 0) atomicOr(&g_decode_error, kErrWaitTimeout);
+      return;
+    }
+    const StageMeta mt = meta[stage];
+    if (mt.flags & kSentinel) break;
+    const uint8_t* st = smem + stage * p.stage_bytes;
+    const uint32_t kv_head = mt.hg * p.heads_per_item + hl;
+    const bool head_ok = kv_head < p.num_kv_heads;
+    // query heads of this warp's tile: qt*8 + n for n < 8, valid if < group
+    const uint32_t q_in_group_row = qt * 8 + g8;  // the head this lane loads for B fragments
+
+    if (head_ok && (mt.flags & kFirst)) {
+#pragma unroll
+      for (int i = 0; i < D / 16; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.0f;
+      m_run[0] = m_run[1] = -INFINITY;
+      l_run[0] = l_run[1] = 0.0f;
+      if (!(mt.flags & kEmpty)) {
+        const uint16_t* qs = reinterpret_cast<const uint16_t*>(st + p.k_bytes + p.v_bytes) +
+                             (hl * p.group + q_in_group_row) * D;
+        const bool row_ok = q_in_group_row < p.group;
+        if constexpr (!kFp8) {
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            qf[kk][0] = row_ok ? *reinterpret_cast<const uint32_t*>(qs + kk * 16 + 2 * c4) : 0u;
+            qf[kk][1] = row_ok ? *reinterpret_cast<const uint32_t*>(qs + kk * 16 + 2 * c4 + 8) : 0u;
+          }
+          head_scale[0] = head_scale[1] = p.score_scale;
+        } else {
+          // permuted k order: slot pair (2c, 2c+1) <-> d = 16kk + 4c + {0,1},
+          // (2c+8, 2c+9) <-> d = 16kk + 4c + {2,3}
+          float qv[D / 16][4];
+          float amax = 0.0f;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint2 w = row_ok ? *reinterpret_cast<const uint2*>(qs + kk * 16 + 4 * c4) : make_uint2(0, 0);
+            qv[kk][0] = bf16_lo_to_f32(w.x);
+            qv[kk][1] = bf16_hi_to_f32(w.x);
+            qv[kk][2] = bf16_lo_to_f32(w.y);
+            qv[kk][3] = bf16_hi_to_f32(w.y);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) amax = fmaxf(amax, fabsf(qv[kk][e]));
+          }
+          amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+          amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+          // scale the row by 2^e so its largest magnitude lies in [2^14, 2^15)
+          int e = 0;
+          if (amax > 0.0f && amax < INFINITY) {
+            int ex;
+            frexpf(amax, &ex);
+            e = 15 - ex;
+          }
+          const float sc = ldexpf(1.0f, e);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            qf[kk][0] = f32x2_to_f16x2(qv[kk][0] * sc, qv[kk][1] * sc);
+            qf[kk][1] = f32x2_to_f16x2(qv[kk][2] * sc, qv[kk][3] * sc);
+          }
+          const float unscale = p.score_scale * ldexpf(1.0f, -e);
+          head_scale[0] = __shfl_sync(0xffffffffu, unscale, (2 * c4) * 4);
+          head_scale[1] = __shfl_sync(0xffffffffu, unscale, (2 * c4 + 1) * 4);
+        }
+      }
+    }
+
+    if (head_ok && !(mt.flags & kEmpty)) {
+      const uint32_t kbase = smem_u32(st) + hl * (kKChunks * kTile * 128);
+      const uint32_t vbase = smem_u32(st + p.k_bytes) + hl * (kVChunks * kTile * 128);
+      // ---- S^T = K Q^T (16 tokens x 8 query heads)
+      float s[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      if constexpr (!kFp8) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t chunk = kk >> 2;
+          const uint32_t unit = ((kk & 3) << 1) + k_unit;
+          uint32_t a[4];
+          ldmatrix_x4(a, kbase + chunk * (kTile * 128) + k_row * 128 + ((unit ^ (k_row & 7)) << 4));
+          mma_bf16(s, a, qf[kk][0], qf[kk][1]);
+        }
+      } else {
+#pragma unroll
+        for (int jj = 0; jj < D / 32; ++jj) {
+          const uint32_t chunk = jj >> 2;
+          const uint32_t unit = ((jj & 3) << 1) + k_unit;
+          uint32_t r[4];
+          ldmatrix_x4(r, kbase + chunk * (kTile * 128) + k_row * 128 + ((unit ^ (k_row & 7)) << 4));
+          uint32_t a0[4], a1[4];
+          a0[0] = e4m3x2_to_f16x2(uint16_t(r[0]));
+          a0[1] = e4m3x2_to_f16x2(uint16_t(r[1]));
+          a0[2] = e4m3x2_to_f16x2(uint16_t(r[0] >> 16));
+          a0[3] = e4m3x2_to_f16x2(uint16_t(r[1] >> 16));
+          a1[0] = e4m3x2_to_f16x2(uint16_t(r[2]));
+          a1[1] = e4m3x2_to_f16x2(uint16_t(r[3]));
+          a1[2] = e4m3x2_to_f16x2(uint16_t(r[2] >> 16));
+          a1[3] = e4m3x2_to_f16x2(uint16_t(r[3] >> 16));
+          mma_f16(s, a0, qf[2 * jj][0], qf[2 * jj][1]);
+          mma_f16(s, a1, qf[2 * jj + 1][0], qf[2 * jj + 1][1]);
+        }
+      }
+      s[0] *= head_scale[0];
+      s[1] *= head_scale[1];
+      s[2] *= head_scale[0];
+      s[3] *= head_scale[1];
+      // ---- mask positions outside [start, len)
+      const int32_t p0 = mt.tile * kTile;
+      const bool boundary = p0 < mt.start || p0 + kTile > mt.len;
+      if (boundary) {
+        const int32_t pa = p0 + int32_t(g8), pb = pa + 8;
+        if (pa < mt.start || pa >= mt.len) s[0] = s[1] = -INFINITY;
+        if (pb < mt.start || pb >= mt.len) s[2] = s[3] = -INFINITY;
+      }
+      // ---- online softmax (base 2), per query head column
+      float mx0 = fmaxf(s[0], s[2]), mx1 = fmaxf(s[1], s[3]);
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+      }
+      const float mn0 = fmaxf(m_run[0], mx0), mn1 = fmaxf(m_run[1], mx1);
+      const float al0 = fast_exp2(m_run[0] - mn0), al1 = fast_exp2(m_run[1] - mn1);
+      m_run[0] = mn0;
+      m_run[1] = mn1;
+      const float e0 = fast_exp2(s[0] - mn0), e1 = fast_exp2(s[1] - mn1);
+      const float e2 = fast_exp2(s[2] - mn0), e3 = fast_exp2(s[3] - mn1);
+      l_run[0] = l_run[0] * al0 + (e0 + e2);
+      l_run[1] = l_run[1] * al1 + (e1 + e3);
+#pragma unroll
+      for (int i = 0; i < D / 16; ++i) {
+        acc[i][0] *= al0;
+        acc[i][1] *= al1;
+        acc[i][2] *= al0;
+        acc[i][3] *= al1;
+      }
+      // ---- P^T as B fragments: hi and lo BF16 parts, transposed by movmatrix
+      const uint32_t hi01 = f32x2_to_bf16x2(e0, e1), hi23 = f32x2_to_bf16x2(e2, e3);
+      const uint32_t lo01 = f32x2_to_bf16x2(e0 - bf16_lo_to_f32(hi01), e1 - bf16_hi_to_f32(hi01));
+      const uint32_t lo23 = f32x2_to_bf16x2(e2 - bf16_lo_to_f32(hi23), e3 - bf16_hi_to_f32(hi23));
+      const uint32_t bh0 = movmatrix_trans(hi01), bh1 = movmatrix_trans(hi23);
+      const uint32_t bl0 = movmatrix_trans(lo01), bl1 = movmatrix_trans(lo23);
+      // V rows of masked positions may hold anything (NaN): zero them
+      uint32_t vmask01 = 0xffffffffu, vmask89 = 0xffffffffu;
+      if (boundary) {
+        const int32_t q0 = p0 + 2 * int32_t(c4);
+        auto ok = [&](int32_t pos) { return pos >= mt.start && pos < mt.len; };
+        vmask01 = (ok(q0) ? 0x0000ffffu : 0u) | (ok(q0 + 1) ? 0xffff0000u : 0u);
+        vmask89 = (ok(q0 + 8) ? 0x0000ffffu : 0u) | (ok(q0 + 9) ? 0xffff0000u : 0u);
+      }
+      // ---- O^T += V^T P^T
+#pragma unroll
+      for (int i = 0; i < D / 16; ++i) {
+        const uint32_t chunk = i >> 2;
+        const uint32_t unit = ((i & 3) << 1) + v_unit;
+        uint32_t a[4];
+        ldmatrix_x4_trans(a, vbase + chunk * (kTile * 128) + v_row * 128 + ((unit ^ (v_row & 7)) << 4));
+        a[0] &= vmask01;
+        a[1] &= vmask01;
+        a[2] &= vmask89;
+        a[3] &= vmask89;
+        mma_bf16(acc[i], a, bh0, bh1);
+        mma_bf16(acc[i], a, bl0, bl1);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[stage]);
+
+    if (head_ok && (mt.flags & kLast)) {
+      // ---- finish the item
+      float l0 = l_run[0], l1 = l_run[1];
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        l0 += __shfl_xor_sync(0xffffffffu, l0, o);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, o);
+      }
+      const uint32_t col0 = qt * 8 + 2 * c4;  // query head within the group of column 0
+      const uint32_t hq0 = kv_head * p.group + col0;
+      const bool ok0 = col0 < p.group, ok1 = col0 + 1 < p.group;
+      if (mt.flags & kSingle) {
+        const float inv0 = (mt.flags & kEmpty) ? 0.0f : 1.0f / l0;
+        const float inv1 = (mt.flags & kEmpty) ? 0.0f : 1.0f / l1;
+        float* o0 = p.output + (uint64_t(mt.seq) * p.num_q_heads + hq0) * D;
+        float* o1 = o0 + D;
+#pragma unroll
+        for (int i = 0; i < D / 16; ++i) {
+          const uint32_t d = i * 16 + g8;
+          if (ok0) {
+            o0[d] = (mt.flags & kEmpty) ? 0.0f : acc[i][0] * inv0;
+            o0[d + 8] = (mt.flags & kEmpty) ? 0.0f : acc[i][2] * inv0;
+          }
+          if (ok1) {
+            o1[d] = (mt.flags & kEmpty) ? 0.0f : acc[i][1] * inv1;
+            o1[d + 8] = (mt.flags & kEmpty) ? 0.0f : acc[i][3] * inv1;
+          }
+        }
+      } else {
+        const uint64_t row = (uint64_t(mt.seq) * p.max_splits + mt.split) * p.num_q_heads + hq0;
+        float* o0 = p.ws_o + row * D;
+        float* o1 = o0 + D;
+#pragma unroll
+        for (int i = 0; i < D / 16; ++i) {
+          const uint32_t d = i * 16 + g8;
+          if (ok0) {
+            o0[d] = acc[i][0];
+            o0[d + 8] = acc[i][2];
+          }
+          if (ok1) {
+            o1[d] = acc[i][1];
+            o1[d + 8] = acc[i][3];
+          }
+        }
+        if (g8 == 0) {
+          if (ok0) *reinterpret_cast<float2*>(p.ws_ml + row * 2) = make_float2(m_run[0], l0);
+          if (ok1) *reinterpret_cast<float2*>(p.ws_ml + (row + 1) * 2) = make_float2(m_run[1], l1);
+        }
+      }
+    }
+    if (++stage == p.stages) { stage = 0; phase ^= 1; }
+  }
+}
+
+// Merge the split partials of every (sequence, query head) whose sequence
+// has more than one split: o = sum_i 2^(m_i - M) acc_i / sum_i 2^(m_i - M) l_i,
+// in split order.
+template <int D>
+__global__ void __launch_bounds__(D) combine_kernel(const DecodeParams p) {
+  const uint32_t s = blockIdx.x;
+  const uint32_t split_tiles = *p.ws_header;
+  const SeqSpan span = seq_span(__ldg(p.seq_lens + s), p);
+  const int32_t nsplit = splits_of(span.ntiles, split_tiles);
+  if (nsplit <= 1) return;
+  const uint32_t d = threadIdx.x;
+  for (uint32_t h = blockIdx.y; h < p.num_q_heads; h += gridDim.y) {
+    float M = -INFINITY;
+    for (int32_t i = 0; i < nsplit; ++i)
+      M = fmaxf(M, p.ws_ml[((uint64_t(s) * p.max_splits + i) * p.num_q_heads + h) * 2]);
+    float num = 0.0f, den = 0.0f;
+    for (int32_t i = 0; i < nsplit; ++i) {
+      const uint64_t row = (uint64_t(s) * p.max_splits + i) * p.num_q_heads + h;
+      const float2 ml = *reinterpret_cast<const float2*>(p.ws_ml + row * 2);
+      const float w = fast_exp2(ml.x - M);
+      num += w * p.ws_o[row * D + d];
+      den += w * ml.y;
+    }
+    p.output[(uint64_t(s) * p.num_q_heads + h) * D + d] = num / den;
+  }
+}
+
+// ---------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+// Tensor map over a cache pool seen as [slots][heads * chunks][chunk elems]:
+// dim 0 the 128 bytes of a chunk, dim 1 the chunk (stride 128 bytes), dim 2
+// the slot (stride heads * head_dim * elem bytes). Box: one chunk x 16 slots,
+// 128-byte swizzle.
+bool encode_pool_map(CUtensorMap* map, const void* base, bool fp8, uint32_t num_kv_heads,
+                     uint32_t head_dim) {
+  auto encode = get_encode();
+  if (!encode) return false;
+  const uint32_t elem = fp8 ? 1 : 2;
+  const uint32_t chunk_elems = 128 / elem;
+  const uint32_t chunks = num_kv_heads * head_dim * elem / 128;
+  cuuint64_t dims[3] = {chunk_elems, chunks, cuuint64_t(1) << 31};
+  cuuint64_t strides[2] = {128, cuuint64_t(num_kv_heads) * head_dim * elem};
+  cuuint32_t box[3] = {chunk_elems, 1, kTile};
+  cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = encode(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16, 3,
+                            const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+struct Geometry {
+  uint32_t heads_per_item, nt, stages, stage_bytes, k_bytes, v_bytes, smem_bytes;
+};
+
+Geometry geometry(bool fp8, uint32_t head_dim, uint32_t num_kv_heads, uint32_t group, int smem_max) {
+  Geometry g{};
+  g.nt = (group + 7) / 8;
+  uint32_t hg = 8 / g.nt;
+  if (hg > num_kv_heads) hg = num_kv_heads;
+  const uint32_t kchunks = fp8 ? head_dim / 128 : head_dim / 64;
+  const uint32_t vchunks = head_dim / 64;
+  for (;; hg = (hg + 1) / 2) {
+    g.heads_per_item = hg;
+    g.k_bytes = hg * kchunks * kTile * 128;
+    g.v_bytes = hg * vchunks * kTile * 128;
+    const uint32_t q_bytes = (hg * group * head_dim * 2 + 1023) / 1024 * 1024;
+    g.stage_bytes = g.k_bytes + g.v_bytes + q_bytes;
+    const uint32_t extra = 1024 + 64 * (2 * 8 + 32);  // alignment slack, barriers, meta
+    uint32_t stages = (uint32_t(smem_max) - extra) / g.stage_bytes;
+    if (stages > 4) stages = 4;
+    g.stages = stages;
+    g.smem_bytes = stages * g.stage_bytes + extra;
+    if (stages >= 2 || hg == 1) break;
+  }
+  return g;
+}
+
+template <bool kFp8, int D, int NT>
+int launch_decode_t(const DecodeArgs& a, cudaStream_t stream, const Geometry& geo, DecodeParams& p) {
+  CUtensorMap mk, mv;
+  if (!encode_pool_map(&mk, a.k_cache, kFp8, a.num_kv_heads, D) ||
+      !encode_pool_map(&mv, a.v_cache, false, a.num_kv_heads, D))
+    return KV_ERR_CUDA;
+  auto kern = decode_kernel<kFp8, D, NT>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(geo.smem_bytes)) !=
+      cudaSuccess)
+    return KV_ERR_CUDA;
+  const DeviceInfo& dev = device_info();
+  const uint32_t threads = 32 * (1 + geo.heads_per_item * geo.nt);
+  kern<<<dev.num_sms, threads, geo.smem_bytes, stream>>>(mk, mv, p);
+  if (cudaGetLastError() != cudaSuccess) return KV_ERR_CUDA;
+  if (p.max_splits > 0) {
+    dim3 grid(p.num_seqs, p.num_q_heads < 8 ? p.num_q_heads : 8);
+    combine_kernel<D><<<grid, D, 0, stream>>>(p);
+    if (cudaGetLastError() != cudaSuccess) return KV_ERR_CUDA;
+  }
+  return KV_OK;
+}
+
+}  // namespace
+
+size_t decode_workspace_bytes(uint32_t max_blocks_per_seq, uint32_t num_seqs, uint32_t num_q_heads,
+                              uint32_t num_kv_heads, uint32_t head_dim, uint32_t block_size) {
+  (void)num_kv_heads;
+  const uint64_t max_tiles = (uint64_t(max_blocks_per_seq) * block_size + kTile - 1) / kTile;
+  const uint64_t max_splits = (max_tiles + 8 - 1) / 8;  // minimum split of 8 tiles
+  return kHeaderBytes + uint64_t(num_seqs) * max_splits * num_q_heads * (uint64_t(head_dim) + 2) * 4;
+}
+
+int launch_decode(const DecodeArgs& a, cudaStream_t stream) {
+  const DeviceInfo& dev = device_info();
+  const uint32_t group = a.num_q_heads / a.num_kv_heads;
+  const Geometry geo = geometry(a.fp8, a.head_dim, a.num_kv_heads, group, dev.max_smem_optin);
+  if (geo.stages < 2) return KV_ERR_UNSUPPORTED;
+
+  DecodeParams p{};
+  p.q = a.q;
+  p.block_tables = a.block_tables;
+  p.seq_lens = a.seq_lens;
+  p.output = a.output;
+  p.max_blocks_per_seq = a.max_blocks_per_seq;
+  p.num_seqs = a.num_seqs;
+  p.num_q_heads = a.num_q_heads;
+  p.num_kv_heads = a.num_kv_heads;
+  p.block_size = a.block_size;
+  p.block_shift = uint32_t(__builtin_ctz(a.block_size));
+  p.group = group;
+  p.heads_per_item = geo.heads_per_item;
+  p.num_head_groups = (a.num_kv_heads + geo.heads_per_item - 1) / geo.heads_per_item;
+  p.q_stride = a.q_stride;
+  p.sliding_window = a.sliding_window;
+  p.score_scale = a.inv_sqrt_d * kLog2e * (a.fp8 ? a.k_scale : 1.0f);
+  p.stages = geo.stages;
+  p.stage_bytes = geo.stage_bytes;
+  p.k_bytes = geo.k_bytes;
+  p.v_bytes = geo.v_bytes;
+
+  // Split-KV when a workspace is registered and large enough for two or more
+  // splits: splits are at least 8 tiles (128 positions), more if the
+  // workspace is smaller than the worst case needs.
+  const uint64_t max_tiles = (uint64_t(a.max_blocks_per_seq) * a.block_size + kTile - 1) / kTile;
+  p.max_splits = 0;
+  p.min_split_tiles = 0x7fffffffu;
+  if (a.workspace && a.workspace_bytes > kHeaderBytes && max_tiles > 8) {
+    const uint64_t per_split = uint64_t(a.num_seqs) * a.num_q_heads * (a.head_dim + 2) * 4;
+    const uint64_t fit = (a.workspace_bytes - kHeaderBytes) / per_split;
+    const uint64_t needed = (max_tiles + 7) / 8;
+    uint64_t min_tiles = 0;
+    if (fit >= needed)
+      min_tiles = 8;
+    else if (fit >= 2)
+      min_tiles = (max_tiles + fit - 1) / fit;
+    if (min_tiles) {
+      p.min_split_tiles = uint32_t(min_tiles);
+      p.max_splits = uint32_t((max_tiles + min_tiles - 1) / min_tiles);
+      uint8_t* ws = static_cast<uint8_t*>(a.workspace);
+      p.ws_header = reinterpret_cast<uint32_t*>(ws);
+      p.ws_o = reinterpret_cast<float*>(ws + kHeaderBytes);
+      p.ws_ml = p.ws_o + uint64_t(a.num_seqs) * p.max_splits * a.num_q_heads * a.head_dim;
+    }
+  }
+
+  const int key = (a.fp8 ? 100 : 0) + int(a.head_dim / 64) * 10 + int(geo.nt);
+  switch (key) {
+    case 11: return launch_decode_t<false, 64, 1>(a, stream, geo, p);
+    case 12: return launch_decode_t<false, 64, 2>(a, stream, geo, p);
+    case 21: return launch_decode_t<false, 128, 1>(a, stream, geo, p);
+    case 22: return launch_decode_t<false, 128, 2>(a, stream, geo, p);
+    case 41: return launch_decode_t<false, 256, 1>(a, stream, geo, p);
+    case 42: return launch_decode_t<false, 256, 2>(a, stream, geo, p);
+    case 121: return launch_decode_t<true, 128, 1>(a, stream, geo, p);
+    case 122: return launch_decode_t<true, 128, 2>(a, stream, geo, p);
+    case 141: return launch_decode_t<true, 256, 1>(a, stream, geo, p);
+    case 142: return launch_decode_t<true, 256, 2>(a, stream, geo, p);
+    default: return KV_ERR_UNSUPPORTED;
+  }
+}
+
+cudaError_t read_and_clear_decode_error(uint32_t* bits) {
+  uint32_t zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(bits, g_decode_error, sizeof(uint32_t));
+  if (e != cudaSuccess) return e;
+  return cudaMemcpyToSymbol(g_decode_error, &zero, sizeof(uint32_t));
+}
+
+}  // namespace pagedkv

@@ -1,0 +1,67 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace pagedkv {
+
+struct DeviceInfo {
+  int device = -1;
+  int num_sms = 0;
+  int max_smem_optin = 0;  // bytes of shared memory a block may opt into
+  int cc_major = 0, cc_minor = 0;
+};
+
+// Cached properties of the current device (queried once per device).
+const DeviceInfo& device_info();
+
+// Launchers (asynchronous on `stream`; return the launch's cudaError_t).
+cudaError_t launch_fill_slots(int64_t* slots, const int32_t* block_table, uint32_t start_pos,
+                              uint32_t count, uint32_t block_size, cudaStream_t stream);
+
+cudaError_t launch_copy_rows(const uint16_t* src0, const uint16_t* src1, uint16_t* dst0,
+                             uint16_t* dst1, const int64_t* slot_mapping, uint32_t num_tokens,
+                             uint32_t row_elems, uint32_t stride0, uint32_t stride1,
+                             cudaStream_t stream);
+
+cudaError_t launch_write_fp8k(const uint16_t* key, const uint16_t* value, uint8_t* k_cache_fp8,
+                              uint16_t* v_cache, const int64_t* slot_mapping, uint32_t num_tokens,
+                              uint32_t row_elems, uint32_t key_stride, uint32_t value_stride,
+                              float k_scale, cudaStream_t stream);
+
+cudaError_t launch_fused_k_norm_rope(const uint16_t* k_in, const uint16_t* k_norm_weight,
+                                     const int32_t* positions, uint16_t* k_cache,
+                                     const int64_t* slot_mapping, uint32_t num_tokens,
+                                     uint32_t num_kv_heads, uint32_t head_dim, uint32_t rotary_dim,
+                                     float rms_eps, float theta, cudaStream_t stream);
+
+// Paged decode. `workspace` may be null (then no split-KV).
+struct DecodeArgs {
+  const uint16_t* q;
+  const void* k_cache;  // bf16 or e4m3 pool
+  const uint16_t* v_cache;
+  float* output;
+  const int32_t* block_tables;
+  const int32_t* seq_lens;
+  uint32_t max_blocks_per_seq, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size;
+  float inv_sqrt_d, k_scale;
+  uint32_t q_stride, sliding_window;
+  bool fp8;
+  void* workspace;
+  size_t workspace_bytes;
+};
+
+size_t decode_workspace_bytes(uint32_t max_blocks_per_seq, uint32_t num_seqs, uint32_t num_q_heads,
+                              uint32_t num_kv_heads, uint32_t head_dim, uint32_t block_size);
+
+// Returns KV_* status (host-side checks) and launches on `stream`.
+int launch_decode(const DecodeArgs& a, cudaStream_t stream);
+
+// The decode kernels' device fault word (read and clear).
+cudaError_t read_and_clear_decode_error(uint32_t* bits);
+
+}  // namespace pagedkv

@@ -1,0 +1,215 @@
+// Slot filling and the BF16 / V-only / FP8-K cache writes.
+//
+// [kv_cache.rs] `fill_slots_from_block_table`, `reshape_and_cache` (BF16),
+// `reshape_and_cache_flash_v_only`; [kv_cache_fp8k.rs] module invariants
+// (K stored as k / k_scale in E4M3).
+//
+// The writes are pure HBM streams: every token's row is read once and
+// written once. A warp owns one token at a time and moves its K and V rows as
+// 16-byte vectors, several per lane in flight before any store, with enough
+// resident warps per SM to keep ~100+ KB of loads outstanding. The grid is a
+// fixed multiple of the SM count and warps stride over tokens.
+#include "internal.h"
+
+namespace pagedkv {
+
+// ------------------------------------------------------------ slot filling
+__global__ void __launch_bounds__(256) fill_slots_kernel(int64_t* __restrict__ slots,
+                                                         const int32_t* __restrict__ block_table,
+                                                         uint32_t start_pos, uint32_t count,
+                                                         uint32_t block_size) {
+  for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < count; i += gridDim.x * blockDim.x) {
+    const uint64_t p = uint64_t(start_pos) + i;
+    const int64_t block = __ldg(block_table + p / block_size);
+    slots[i] = block * int64_t(block_size) + int64_t(p % block_size);
+  }
+}
+
+cudaError_t launch_fill_slots(int64_t* slots, const int32_t* block_table, uint32_t start_pos,
+                              uint32_t count, uint32_t block_size, cudaStream_t stream) {
+  const DeviceInfo& dev = device_info();
+  uint32_t blocks = (count + 255) / 256;
+  blocks = blocks < uint32_t(dev.num_sms * 8) ? blocks : uint32_t(dev.num_sms * 8);
+  fill_slots_kernel<<<blocks, 256, 0, stream>>>(slots, block_table, start_pos, count, block_size);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------ row copies
+// Copy token rows to their slots. `src1`/`dst1` null means V-only (one
+// tensor). V is uint4 (16-byte vectors) when every row start and the row
+// length are 16-byte aligned, else uint16_t (one BF16 element). Row lengths
+// and strides are in units of V.
+template <typename V, int kUnroll>
+__global__ void __launch_bounds__(256) copy_rows_kernel(const V* __restrict__ src0,
+                                                        const V* __restrict__ src1,
+                                                        V* __restrict__ dst0, V* __restrict__ dst1,
+                                                        const int64_t* __restrict__ slot_mapping,
+                                                        uint32_t num_tokens, uint32_t row_vecs,
+                                                        uint32_t stride0_vecs,
+                                                        uint32_t stride1_vecs) {
+  const uint32_t lane = threadIdx.x & 31;
+  const uint32_t warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const uint32_t num_warps = (gridDim.x * blockDim.x) >> 5;
+  const bool two = src1 != nullptr;
+  for (uint32_t t = warp; t < num_tokens; t += num_warps) {
+    const int64_t slot = __ldg(slot_mapping + t);
+    if (slot < 0) continue;  // padding token
+    const V* s0 = src0 + size_t(t) * stride0_vecs;
+    const V* s1 = two ? src1 + size_t(t) * stride1_vecs : nullptr;
+    V* d0 = dst0 + size_t(slot) * row_vecs;
+    V* d1 = two ? dst1 + size_t(slot) * row_vecs : nullptr;
+    for (uint32_t base = lane; base < row_vecs; base += 32u * kUnroll) {
+      V a[kUnroll], b[kUnroll];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const uint32_t c = base + 32u * u;
+        if (c < row_vecs) {
+          a[u] = __ldcs(s0 + c);
+          if (two) b[u] = __ldcs(s1 + c);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const uint32_t c = base + 32u * u;
+        if (c < row_vecs) {
+          d0[c] = a[u];
+          if (two) d1[c] = b[u];
+        }
+      }
+    }
+  }
+}
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+static uint32_t copy_grid(const DeviceInfo& dev, uint32_t num_tokens) {
+  // 8 warps per block; at most 8 blocks per SM resident, one token per warp.
+  uint32_t blocks = (num_tokens + 7) / 8;
+  const uint32_t cap = uint32_t(dev.num_sms) * 8;
+  return blocks < cap ? blocks : cap;
+}
+
+cudaError_t launch_copy_rows(const uint16_t* src0, const uint16_t* src1, uint16_t* dst0,
+                             uint16_t* dst1, const int64_t* slot_mapping, uint32_t num_tokens,
+                             uint32_t row_elems, uint32_t stride0, uint32_t stride1,
+                             cudaStream_t stream) {
+  const DeviceInfo& dev = device_info();
+  const uint32_t blocks = copy_grid(dev, num_tokens);
+  const bool vec = (row_elems % 8 == 0) && (stride0 % 8 == 0) && (!src1 || stride1 % 8 == 0) &&
+                   aligned16(src0) && aligned16(dst0) && (!src1 || (aligned16(src1) && aligned16(dst1)));
+  if (vec) {
+    copy_rows_kernel<uint4, 4><<<blocks, 256, 0, stream>>>(
+        reinterpret_cast<const uint4*>(src0), reinterpret_cast<const uint4*>(src1),
+        reinterpret_cast<uint4*>(dst0), reinterpret_cast<uint4*>(dst1), slot_mapping, num_tokens,
+        row_elems / 8, stride0 / 8, stride1 / 8);
+  } else {
+    copy_rows_kernel<uint16_t, 8><<<blocks, 256, 0, stream>>>(src0, src1, dst0, dst1, slot_mapping,
+                                                             num_tokens, row_elems, stride0,
+                                                             stride1);
+  }
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------ FP8-K write
+// K: 8 BF16 in (16 B) -> 8 E4M3 out (8 B) per vector; the quotient is the
+// IEEE binary32 division (correctly rounded), then one saturating RNE
+// conversion. V: 16-byte copy.
+__device__ __forceinline__ uint2 encode8(uint4 k, float k_scale) {
+  const uint32_t w[4] = {k.x, k.y, k.z, k.w};
+  uint32_t out[2];
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const float q0 = __fdiv_rn(bf16_lo_to_f32(w[2 * j]), k_scale);
+    const float q1 = __fdiv_rn(bf16_hi_to_f32(w[2 * j]), k_scale);
+    const float q2 = __fdiv_rn(bf16_lo_to_f32(w[2 * j + 1]), k_scale);
+    const float q3 = __fdiv_rn(bf16_hi_to_f32(w[2 * j + 1]), k_scale);
+    out[j] = uint32_t(f32x2_to_e4m3x2_satfinite(q0, q1)) |
+             (uint32_t(f32x2_to_e4m3x2_satfinite(q2, q3)) << 16);
+  }
+  return make_uint2(out[0], out[1]);
+}
+
+__device__ __forceinline__ uint8_t encode1(uint16_t k, float k_scale) {
+  const float q = __fdiv_rn(__uint_as_float(uint32_t(k) << 16), k_scale);
+  return uint8_t(f32x2_to_e4m3x2_satfinite(q, 0.0f) & 0xFF);
+}
+
+template <int kUnroll>
+__global__ void __launch_bounds__(256) write_fp8k_kernel(
+    const uint4* __restrict__ key, const uint4* __restrict__ value, uint2* __restrict__ k_cache,
+    uint4* __restrict__ v_cache, const int64_t* __restrict__ slot_mapping, uint32_t num_tokens,
+    uint32_t row_vecs, uint32_t kstride_vecs, uint32_t vstride_vecs, float k_scale) {
+  const uint32_t lane = threadIdx.x & 31;
+  const uint32_t warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const uint32_t num_warps = (gridDim.x * blockDim.x) >> 5;
+  for (uint32_t t = warp; t < num_tokens; t += num_warps) {
+    const int64_t slot = __ldg(slot_mapping + t);
+    if (slot < 0) continue;
+    const uint4* ks = key + size_t(t) * kstride_vecs;
+    const uint4* vs = value + size_t(t) * vstride_vecs;
+    uint2* kd = k_cache + size_t(slot) * row_vecs;
+    uint4* vd = v_cache + size_t(slot) * row_vecs;
+    for (uint32_t base = lane; base < row_vecs; base += 32u * kUnroll) {
+      uint4 a[kUnroll], b[kUnroll];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const uint32_t c = base + 32u * u;
+        if (c < row_vecs) {
+          a[u] = __ldcs(ks + c);
+          b[u] = __ldcs(vs + c);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const uint32_t c = base + 32u * u;
+        if (c < row_vecs) {
+          kd[c] = encode8(a[u], k_scale);
+          vd[c] = b[u];
+        }
+      }
+    }
+  }
+}
+
+// Unaligned fallback: one element per lane step.
+__global__ void __launch_bounds__(256) write_fp8k_scalar_kernel(
+    const uint16_t* __restrict__ key, const uint16_t* __restrict__ value,
+    uint8_t* __restrict__ k_cache, uint16_t* __restrict__ v_cache,
+    const int64_t* __restrict__ slot_mapping, uint32_t num_tokens, uint32_t row_elems,
+    uint32_t key_stride, uint32_t value_stride, float k_scale) {
+  const uint32_t lane = threadIdx.x & 31;
+  const uint32_t warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const uint32_t num_warps = (gridDim.x * blockDim.x) >> 5;
+  for (uint32_t t = warp; t < num_tokens; t += num_warps) {
+    const int64_t slot = __ldg(slot_mapping + t);
+    if (slot < 0) continue;
+    for (uint32_t c = lane; c < row_elems; c += 32) {
+      k_cache[size_t(slot) * row_elems + c] = encode1(key[size_t(t) * key_stride + c], k_scale);
+      v_cache[size_t(slot) * row_elems + c] = value[size_t(t) * value_stride + c];
+    }
+  }
+}
+
+cudaError_t launch_write_fp8k(const uint16_t* key, const uint16_t* value, uint8_t* k_cache_fp8,
+                              uint16_t* v_cache, const int64_t* slot_mapping, uint32_t num_tokens,
+                              uint32_t row_elems, uint32_t key_stride, uint32_t value_stride,
+                              float k_scale, cudaStream_t stream) {
+  const DeviceInfo& dev = device_info();
+  const uint32_t blocks = copy_grid(dev, num_tokens);
+  const bool vec = (row_elems % 8 == 0) && (key_stride % 8 == 0) && (value_stride % 8 == 0) &&
+                   aligned16(key) && aligned16(value) && aligned16(v_cache) &&
+                   (reinterpret_cast<uintptr_t>(k_cache_fp8) & 7u) == 0;
+  if (vec) {
+    write_fp8k_kernel<4><<<blocks, 256, 0, stream>>>(
+        reinterpret_cast<const uint4*>(key), reinterpret_cast<const uint4*>(value),
+        reinterpret_cast<uint2*>(k_cache_fp8), reinterpret_cast<uint4*>(v_cache), slot_mapping,
+        num_tokens, row_elems / 8, key_stride / 8, value_stride / 8, k_scale);
+  } else {
+    write_fp8k_scalar_kernel<<<blocks, 256, 0, stream>>>(key, value, k_cache_fp8, v_cache,
+                                                         slot_mapping, num_tokens, row_elems,
+                                                         key_stride, value_stride, k_scale);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace pagedkv

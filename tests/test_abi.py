@@ -1,0 +1,129 @@
+"""C-ABI contract checks that need no GPU: the library builds and loads, it
+exports every entry point include/pagedkv.h declares (and the binding wraps
+each of them), and argument validation returns the documented status before
+any CUDA call is made."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pagedkv.h")
+
+
+@pytest.fixture(scope="module")
+def pk():
+    from paged_kv_cache_fill_gb300 import _build
+    _build.build()
+    import paged_kv_cache_fill_gb300 as pk
+    pk.lib()
+    return pk
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return re.findall(r"^PAGEDKV_API\s+[\w\s\*]*?\b(\w+)\s*\(", text, re.M)
+
+
+def test_header_declares_the_seven_calls():
+    names = set(declared_functions())
+    for n in ["kv_fill_slots", "kv_write_bf16", "kv_write_fp8k", "kv_write_fused_k_norm_rope_bf16",
+              "kv_write_v_only", "paged_decode_attn_bf16", "paged_decode_attn_fp8k"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(pk):
+    for name in declared_functions():
+        assert hasattr(pk.lib(), name), name
+
+
+def test_binding_argument_counts_match_header(pk):
+    text = open(HEADER).read()
+    for name in declared_functions():
+        m = re.search(r"^PAGEDKV_API[^;]*?\b" + name + r"\s*\(([^)]*)\)", text, re.S | re.M)
+        params = [p for p in m.group(1).split(",") if p.strip() and p.strip() != "void"]
+        assert len(pk._SIGNATURES[name][1]) == len(params), name
+
+
+def test_only_declared_symbols_are_exported(pk):
+    lib = pk.lib()
+    # a few internal names that must stay hidden
+    for hidden in ["launch_decode", "device_info", "_ZN7pagedkv13launch_decodeERKNS_10DecodeArgsEP11CUstream_st"]:
+        with pytest.raises(AttributeError):
+            getattr(lib, hidden)
+
+
+FAKE = ctypes.c_void_p(0x10000)   # never dereferenced: validation fails first
+
+
+def test_zero_work_is_ok_and_launches_nothing(pk):
+    L = pk.lib()
+    assert L.kv_fill_slots(None, None, 0, 0, 16, None) == pk.KV_OK
+    assert L.kv_write_bf16(None, None, None, None, None, 0, 8, 128, 16, 1024, 1024, None) == pk.KV_OK
+    assert L.kv_write_v_only(None, None, None, 0, 8, 128, 16, 1024, None) == pk.KV_OK
+    assert L.kv_write_fp8k(None, None, None, None, None, 0, 8, 128, 16, 1024, 1024, 1.0, None) == pk.KV_OK
+    assert L.kv_write_fused_k_norm_rope_bf16(None, None, None, None, None, 0, 8, 128, 128, 16, 1e-6, 1e6,
+                                             None) == pk.KV_OK
+    assert L.paged_decode_attn_bf16(None, None, None, None, None, None, 4, 0, 32, 8, 128, 16, 0.1, 4096, 0,
+                                    None) == pk.KV_OK
+    assert L.paged_decode_attn_fp8k(None, None, None, None, None, None, 4, 0, 32, 8, 128, 16, 0.1, 1.0, 4096,
+                                    0, None) == pk.KV_OK
+
+
+def test_invalid_arguments(pk):
+    L, INV = pk.lib(), pk.KV_ERR_INVALID_ARG
+    assert L.kv_fill_slots(None, FAKE, 0, 5, 16, None) == INV
+    assert L.kv_fill_slots(FAKE, FAKE, 0, 5, 0, None) == INV
+    assert L.kv_write_bf16(FAKE, FAKE, FAKE, FAKE, None, 3, 8, 128, 16, 1024, 1024, None) == INV
+    assert L.kv_write_bf16(FAKE, FAKE, FAKE, FAKE, FAKE, 3, 8, 128, 16, 1000, 1024, None) == INV  # stride
+    assert L.kv_write_bf16(FAKE, FAKE, FAKE, FAKE, FAKE, 3, 8, 128, 0, 1024, 1024, None) == INV
+    assert L.kv_write_v_only(FAKE, FAKE, FAKE, 3, 0, 128, 16, 1024, None) == INV
+    for bad in (0.0, -1.0, float("inf"), float("nan")):
+        assert L.kv_write_fp8k(FAKE, FAKE, FAKE, FAKE, FAKE, 3, 8, 128, 16, 1024, 1024, bad, None) == INV
+    fused = lambda **kw: L.kv_write_fused_k_norm_rope_bf16(  # noqa: E731
+        FAKE, FAKE, FAKE, FAKE, FAKE, 3, 8, kw.get("D", 128), kw.get("R", 128), 16, kw.get("eps", 1e-6),
+        kw.get("theta", 1e6), None)
+    assert fused(R=127) == INV and fused(R=0) == INV and fused(R=256) == INV
+    assert fused(eps=-1.0) == INV and fused(theta=0.0) == INV and fused(theta=float("nan")) == INV
+    dec = lambda **kw: L.paged_decode_attn_fp8k(  # noqa: E731
+        FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 2, kw.get("Hq", 32), kw.get("H", 8), 128, 16, 0.1,
+        kw.get("k_scale", 1.0), kw.get("q_stride", 4096), 0, None)
+    assert dec(Hq=30) == INV and dec(H=0) == INV and dec(q_stride=100) == INV
+    assert dec(k_scale=0.0) == INV and dec(k_scale=float("nan")) == INV
+
+
+def test_unsupported_shapes(pk):
+    L, UNS = pk.lib(), pk.KV_ERR_UNSUPPORTED
+    assert L.kv_write_fused_k_norm_rope_bf16(FAKE, FAKE, FAKE, FAKE, FAKE, 3, 8, 96, 96, 16, 1e-6, 1e6,
+                                             None) == UNS
+    assert L.kv_write_fused_k_norm_rope_bf16(FAKE, FAKE, FAKE, FAKE, FAKE, 3, 8, 128, 100, 16, 1e-6, 1e6,
+                                             None) == UNS
+    base = dict(mbps=4, D=128, bs=16, Hq=32, H=8)
+
+    def dec(fp8=False, **kw):
+        a = dict(base, **kw)
+        if fp8:
+            return L.paged_decode_attn_fp8k(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, a["mbps"], 2, a["Hq"], a["H"],
+                                            a["D"], a["bs"], 0.1, 1.0, a["Hq"] * a["D"], 0, None)
+        return L.paged_decode_attn_bf16(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, a["mbps"], 2, a["Hq"], a["H"],
+                                        a["D"], a["bs"], 0.1, a["Hq"] * a["D"], 0, None)
+    assert dec(D=96) == UNS and dec(fp8=True, D=64) == UNS
+    assert dec(bs=8) == UNS and dec(bs=24) == UNS and dec(bs=512) == UNS
+    assert dec(Hq=64, H=2) == UNS            # group of 32 query heads
+    misaligned = ctypes.c_void_p(0x10008)
+    assert L.paged_decode_attn_bf16(misaligned, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 2, 32, 8, 128, 16, 0.1,
+                                    4096, 0, None) == UNS
+
+
+def test_workspace_size_formula(pk):
+    # header + num_seqs * ceil(ceil(mbps*bs/16)/8) splits * Hq * (D + 2) floats
+    got = pk.kv_decode_workspace_bytes(512, 64, 32, 8, 128, 16)
+    assert got == 256 + 64 * 64 * 32 * 130 * 4
+    assert pk.kv_decode_workspace_bytes(1, 1, 4, 2, 64, 16) == 256 + 1 * 1 * 4 * 66 * 4
+
+
+def test_status_strings(pk):
+    for s in range(5):
+        assert pk.lib().kv_status_string(s)
+    assert b"unknown" in pk.lib().kv_status_string(99)

@@ -1,0 +1,426 @@
+"""GPU parity: every C-ABI call against the CPU oracle on the same seeded
+inputs. Bit-exact for slot filling, the BF16 copies and the FP8 E4M3 codes;
+at most 1 BF16 ulp per element for the fused K norm/RoPE write; decode
+outputs within max abs error 2e-3 and max relative error 1e-2 (relative error
+taken where |reference| >= 0.2) of the fp64 oracle. Caches start filled with
+NaN patterns, so a kernel that touches an unattended row or a padding slot
+shows up as NaN or as a changed pool byte."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import kvgen
+import oracle
+import paged_kv_cache_fill_gb300 as pk
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():  # collected on CPU hosts, never run there
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+DEV = torch.device("cuda")
+ABS_TOL, REL_TOL, REL_FLOOR = 2e-3, 1e-2, 0.2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    import __graft_entry__
+    __graft_entry__.build()
+    yield
+    pk.kv_set_decode_workspace(None)
+
+
+def u16(t: torch.Tensor) -> np.ndarray:
+    return np.ascontiguousarray(t.detach().contiguous().cpu().view(torch.int16).numpy().view(np.uint16))
+
+
+def ordered(bits: np.ndarray) -> np.ndarray:
+    b = bits.astype(np.int64) & 0xFFFF
+    return np.where(b & 0x8000, -(b & 0x7FFF), b & 0x7FFF)
+
+
+def assert_decode_close(got: np.ndarray, ref: np.ndarray, what=""):
+    assert np.isfinite(got).all(), f"{what}: non-finite output"
+    err = np.abs(got.astype(np.float64) - ref.astype(np.float64))
+    assert err.max() <= ABS_TOL, f"{what}: max abs err {err.max():.3e}"
+    big = np.abs(ref) >= REL_FLOOR
+    if big.any():
+        rel = (err[big] / np.abs(ref[big])).max()
+        assert rel <= REL_TOL, f"{what}: max rel err {rel:.3e}"
+
+
+def oracle_slots(w) -> np.ndarray:
+    parts = [oracle.fill_slots(w.block_tables[s].cpu().numpy(), 0, int(L), w.block_size)
+             for s, L in enumerate(w.seq_lens.tolist())]
+    return np.concatenate(parts) if parts else np.zeros(0, np.int64)
+
+
+def gpu_slots(w) -> torch.Tensor:
+    tables = w.block_tables.to(DEV)
+    slots = torch.empty(w.num_tokens, dtype=torch.int64, device=DEV)
+    off = 0
+    for s, L in enumerate(w.seq_lens.tolist()):
+        pk.kv_fill_slots(slots[off:off + L], tables[s], 0, L, w.block_size)
+        off += L
+    return slots
+
+
+def with_workspace(w, on=True):
+    if not on:
+        pk.kv_set_decode_workspace(None)
+        return None
+    n = pk.kv_decode_workspace_bytes(w.max_blocks_per_seq, w.num_seqs, w.num_q_heads, w.num_kv_heads,
+                                     w.head_dim, w.block_size)
+    ws = torch.empty(n, dtype=torch.uint8, device=DEV)
+    pk.kv_set_decode_workspace(ws)
+    return ws
+
+
+# ---------------------------------------------------------------------------
+# slot filling
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("block_size", [1, 3, 16, 64, 256])
+def test_fill_slots_bit_exact(block_size):
+    rng = np.random.default_rng(block_size)
+    table = rng.permutation(5000).astype(np.int32)[:300]
+    table[7] = -1                                     # a padding block
+    t_dev = torch.from_numpy(table).to(DEV)
+    for start, count in [(0, 1), (0, 300 * block_size), (5, 17), (block_size - 1, 2 * block_size + 3),
+                         (300 * block_size - 1, 1), (123, 9999)]:
+        count = min(count, 300 * block_size - start)
+        got = torch.full((count,), -7, dtype=torch.int64, device=DEV)
+        pk.kv_fill_slots(got, t_dev, start, count, block_size)
+        assert np.array_equal(got.cpu().numpy(), oracle.fill_slots(table, start, count, block_size))
+
+
+# ---------------------------------------------------------------------------
+# BF16, V-only and FP8-K writes
+# ---------------------------------------------------------------------------
+def _write_case(key_stride_pad=0, seed=31, H=8, D=128, bs=16, lens=(37, 100, 5, 64)):
+    w = kvgen.custom(seed, seq_lens=list(lens), num_q_heads=H, num_kv_heads=H, head_dim=D, block_size=bs)
+    row = H * D
+    n = w.num_tokens
+    stride = row + key_stride_pad
+    g = torch.Generator().manual_seed(seed)
+    key = torch.randn((n, stride), generator=g).to(torch.bfloat16)
+    value = torch.randn((n, stride), generator=g).to(torch.bfloat16)
+    slots_ref = oracle_slots(w)
+    slots_ref[::11] = -1                              # some padding tokens
+    return w, key, value, stride, slots_ref
+
+
+@pytest.mark.parametrize("pad", [0, 8, 3])           # 3: unaligned rows take the scalar path
+def test_write_bf16_and_v_only_bit_exact(pad):
+    w, key, value, stride, slots_ref = _write_case(pad)
+    H, D, bs, nb, n = w.num_kv_heads, w.head_dim, w.block_size, w.num_blocks, w.num_tokens
+    slots = torch.from_numpy(slots_ref).to(DEV)
+    kc = kvgen.poisoned_pool(nb, bs, H, D, "bf16", DEV)
+    vc = kvgen.poisoned_pool(nb, bs, H, D, "bf16", DEV)
+    pk.kv_write_bf16(key.to(DEV), value.to(DEV), kc, vc, slots, n, H, D, bs, stride, stride)
+    kr = np.full((nb, bs, H, D), kvgen.BF16_NAN, np.uint16)
+    vr = kr.copy()
+    oracle.write_bf16(u16(key), u16(value), kr, vr, slots_ref, n, H, D, bs, stride, stride)
+    assert np.array_equal(u16(kc), kr) and np.array_equal(u16(vc), vr)
+    v2 = kvgen.poisoned_pool(nb, bs, H, D, "bf16", DEV)
+    pk.kv_write_v_only(value.to(DEV), v2, slots, n, H, D, bs, stride)
+    assert np.array_equal(u16(v2), vr)
+
+
+def test_write_fp8k_exhaustive_over_bf16_patterns():
+    """All 65536 BF16 bit patterns as K (64 tokens x 1024), at k_scale 1 and
+    at a workload-like scale."""
+    H, D, bs = 8, 128, 16
+    n = 64
+    pats = np.arange(65536, dtype=np.uint32).astype(np.uint16).reshape(n, H * D)
+    key = torch.from_numpy(pats.view(np.int16)).view(torch.bfloat16)
+    value = torch.randn((n, H * D), generator=torch.Generator().manual_seed(2)).to(torch.bfloat16)
+    slots_ref = np.arange(n, dtype=np.int64)[::-1].copy()
+    slots = torch.from_numpy(slots_ref).to(DEV)
+    for k_scale in (1.0, 20.0 / 448.0, 3.0e-3):
+        kc = kvgen.poisoned_pool(n // bs, bs, H, D, "fp8", DEV)
+        vc = kvgen.poisoned_pool(n // bs, bs, H, D, "bf16", DEV)
+        pk.kv_write_fp8k(key.to(DEV), value.to(DEV), kc, vc, slots, n, H, D, bs, H * D, H * D, k_scale)
+        kr = np.full((n // bs, bs, H, D), kvgen.E4M3_NAN, np.uint8)
+        vr = np.full((n // bs, bs, H, D), kvgen.BF16_NAN, np.uint16)
+        oracle.write_fp8k(u16(key), u16(value), kr, vr, slots_ref, n, H, D, bs, H * D, H * D, k_scale)
+        got = kc.cpu().numpy()
+        bad = np.flatnonzero(got.ravel() != kr.ravel())
+        assert bad.size == 0, (k_scale, bad[:8], got.ravel()[bad[:8]], kr.ravel()[bad[:8]])
+        assert np.array_equal(u16(vc), vr)
+
+
+def test_write_fp8k_workload_bit_exact():
+    w = kvgen.custom(41, seq_lens=[300, 17, 1, 64], num_q_heads=8, num_kv_heads=8, head_dim=128,
+                     block_size=16, fp8=True)
+    H, D, bs, nb, n = w.num_kv_heads, w.head_dim, w.block_size, w.num_blocks, w.num_tokens
+    slots_ref = oracle_slots(w)
+    slots = gpu_slots(w)
+    assert np.array_equal(slots.cpu().numpy(), slots_ref)
+    kc = kvgen.poisoned_pool(nb, bs, H, D, "fp8", DEV)
+    vc = kvgen.poisoned_pool(nb, bs, H, D, "bf16", DEV)
+    pk.kv_write_fp8k(w.key.to(DEV), w.value.to(DEV), kc, vc, slots, n, H, D, bs, H * D, H * D, w.k_scale)
+    kr = np.full((nb, bs, H, D), kvgen.E4M3_NAN, np.uint8)
+    vr = np.full((nb, bs, H, D), kvgen.BF16_NAN, np.uint16)
+    oracle.write_fp8k(u16(w.key), u16(w.value), kr, vr, slots_ref, n, H, D, bs, H * D, H * D, w.k_scale)
+    assert np.array_equal(kc.cpu().numpy(), kr) and np.array_equal(u16(vc), vr)
+
+
+# ---------------------------------------------------------------------------
+# fused K norm / RoPE write
+# ---------------------------------------------------------------------------
+def _fused_check(w, rotary_dim, theta, eps, positions=None, slots_ref=None):
+    H, D, bs, nb, n = w.num_kv_heads, w.head_dim, w.block_size, w.num_blocks, w.num_tokens
+    wt = w.extra.get("k_norm_weight")
+    if wt is None:
+        wt = (torch.rand(D, generator=torch.Generator().manual_seed(D)) + 0.5).to(torch.bfloat16)
+    pos = positions if positions is not None else w.positions
+    if slots_ref is None:
+        slots_ref = oracle_slots(w)
+    slots = torch.from_numpy(slots_ref).to(DEV)
+    kc = kvgen.poisoned_pool(nb, bs, H, D, "bf16", DEV)
+    pk.kv_write_fused_k_norm_rope_bf16(w.key.to(DEV), wt.to(DEV), pos.to(DEV), kc, slots, n, H, D,
+                                       rotary_dim, bs, eps, theta)
+    kr = np.full((nb, bs, H, D), kvgen.BF16_NAN, np.uint16)
+    oracle.write_fused_k_norm_rope_bf16(u16(w.key), u16(wt), np.ascontiguousarray(pos.cpu().numpy()), kr,
+                                        slots_ref, n, H, D, rotary_dim, bs, eps, theta)
+    got = u16(kc)
+    d = np.abs(ordered(got) - ordered(kr))
+    return int(d.max()), int((d == 1).sum()), d.size
+
+
+def test_fused_write_full_workload_within_one_ulp():
+    w = kvgen.fused_write()
+    worst, ones, total = _fused_check(w, 128, 1e6, 1e-6)
+    print(f"fused write: max {worst} ulp, {ones} of {total} elements at 1 ulp")
+    assert worst <= 1
+
+
+@pytest.mark.parametrize("D,R,theta", [(64, 64, 1e4), (128, 64, 1e6), (256, 256, 5e5), (128, 8, 1e4),
+                                       (256, 128, 1e6)])
+def test_fused_write_shapes(D, R, theta):
+    w = kvgen.custom(50 + D + R, seq_lens=[33, 70, 1], num_q_heads=4, num_kv_heads=4, head_dim=D,
+                     block_size=16, key_sigma=4.0)
+    worst, _, _ = _fused_check(w, R, theta, 1e-5)
+    assert worst <= 1
+
+
+def test_fused_write_large_positions_and_padding():
+    w = kvgen.custom(77, seq_lens=[200, 57], num_q_heads=8, num_kv_heads=8, head_dim=128, block_size=16,
+                     key_sigma=18.0)
+    g = torch.Generator().manual_seed(8)
+    pos = torch.cat([torch.randint(0, 1 << 20, (100,), generator=g), torch.arange(65530, 65630),
+                     torch.randint(0, 2000, (57,), generator=g)]).to(torch.int32)
+    slots_ref = oracle_slots(w)
+    slots_ref[::7] = -3
+    worst, _, _ = _fused_check(w, 128, 1e6, 1e-6, positions=pos, slots_ref=slots_ref)
+    assert worst <= 1
+
+
+# ---------------------------------------------------------------------------
+# paged decode
+# ---------------------------------------------------------------------------
+def _caches(w, fp8):
+    """The same cache on both sides: the GPU write kernels fill the device
+    pools, the oracle's writes fill host pools."""
+    H, D, bs, nb, n = w.num_kv_heads, w.head_dim, w.block_size, w.num_blocks, w.num_tokens
+    slots_ref = oracle_slots(w)
+    slots = gpu_slots(w)
+    vc = kvgen.poisoned_pool(nb, bs, H, D, "bf16", DEV)
+    vr = np.full((nb, bs, H, D), kvgen.BF16_NAN, np.uint16)
+    if fp8:
+        kc = kvgen.poisoned_pool(nb, bs, H, D, "fp8", DEV)
+        kr = np.full((nb, bs, H, D), kvgen.E4M3_NAN, np.uint8)
+        if n:
+            pk.kv_write_fp8k(w.key.to(DEV), w.value.to(DEV), kc, vc, slots, n, H, D, bs, H * D, H * D,
+                             w.k_scale)
+            oracle.write_fp8k(u16(w.key), u16(w.value), kr, vr, slots_ref, n, H, D, bs, H * D, H * D,
+                              w.k_scale)
+    else:
+        kc = kvgen.poisoned_pool(nb, bs, H, D, "bf16", DEV)
+        kr = np.full((nb, bs, H, D), kvgen.BF16_NAN, np.uint16)
+        if n:
+            pk.kv_write_bf16(w.key.to(DEV), w.value.to(DEV), kc, vc, slots, n, H, D, bs, H * D, H * D)
+            oracle.write_bf16(u16(w.key), u16(w.value), kr, vr, slots_ref, n, H, D, bs, H * D, H * D)
+    return kc, vc, kr, vr
+
+
+def _decode_gpu(w, kc, vc, window, fp8, q=None, q_stride=None):
+    q = w.q if q is None else q
+    q_stride = q_stride or w.num_q_heads * w.head_dim
+    out = torch.full((w.num_seqs, w.num_q_heads, w.head_dim), float("nan"), device=DEV)
+    args = (w.block_tables.to(DEV), w.seq_lens.to(DEV), w.max_blocks_per_seq, w.num_seqs, w.num_q_heads,
+            w.num_kv_heads, w.head_dim, w.block_size, w.inv_sqrt_d)
+    if fp8:
+        pk.paged_decode_attn_fp8k(q.to(DEV), kc, vc, out, *args, w.k_scale, q_stride, window)
+    else:
+        pk.paged_decode_attn_bf16(q.to(DEV), kc, vc, out, *args, q_stride, window)
+    return out.cpu().numpy()
+
+
+def _decode_ref(w, kr, vr, window, fp8, q=None, q_stride=None):
+    q = w.q if q is None else q
+    q_stride = q_stride or w.num_q_heads * w.head_dim
+    args = (w.block_tables.numpy(), w.seq_lens.numpy(), w.max_blocks_per_seq, w.num_seqs, w.num_q_heads,
+            w.num_kv_heads, w.head_dim, w.block_size, w.inv_sqrt_d)
+    if fp8:
+        return oracle.paged_decode_attn_fp8k(u16(q), kr, vr, *args, w.k_scale, q_stride, window)
+    return oracle.paged_decode_attn_bf16(u16(q), kr, vr, *args, q_stride, window)
+
+
+@pytest.mark.parametrize("split", [False, True])
+def test_decode_tiny_workload(split):
+    w = kvgen.tiny()
+    kc, vc, kr, vr = _caches(w, False)
+    with_workspace(w, split)
+    assert_decode_close(_decode_gpu(w, kc, vc, 0, False), _decode_ref(w, kr, vr, 0, False), "tiny")
+    assert pk.kv_get_device_error() == 0
+
+
+CASES = [
+    # (seq_lens, Hq, H, D, bs, windows)
+    ([1, 15, 16, 17, 31, 33, 100, 0], 8, 2, 128, 16, (0, 1, 16, 17, 40)),
+    ([700, 1000, 2049, 5], 32, 8, 128, 16, (0, 100, 1024)),
+    ([333, 64, 65, 1], 64, 8, 128, 64, (0, 63, 200)),
+    ([500, 129, 40], 16, 16, 64, 32, (0, 7)),
+    ([260, 1000], 16, 1, 256, 128, (0, 300)),
+    ([300, 77], 12, 1, 128, 256, (0, 50)),
+    ([400, 90, 3], 6, 3, 64, 16, (0, 33)),
+]
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+@pytest.mark.parametrize("case", range(len(CASES)))
+@pytest.mark.parametrize("split", [False, True])
+def test_decode_cases(fp8, case, split):
+    lens, Hq, H, D, bs, windows = CASES[case]
+    if fp8 and D == 64:
+        pytest.skip("FP8-K decode supports head_dim 128 and 256")
+    w = kvgen.custom(100 + case, seq_lens=lens, num_q_heads=Hq, num_kv_heads=H, head_dim=D, block_size=bs,
+                     fp8=fp8)
+    kc, vc, kr, vr = _caches(w, fp8)
+    with_workspace(w, split)
+    for win in windows:
+        got = _decode_gpu(w, kc, vc, win, fp8)
+        ref = _decode_ref(w, kr, vr, win, fp8)
+        assert_decode_close(got, ref, f"case {case} window {win}")
+    assert pk.kv_get_device_error() == 0
+
+
+def test_decode_padded_q_stride_and_determinism():
+    w = kvgen.custom(7, seq_lens=[3000, 17, 900], num_q_heads=32, num_kv_heads=8, head_dim=128,
+                     block_size=16)
+    kc, vc, kr, vr = _caches(w, False)
+    with_workspace(w, True)
+    stride = 32 * 128 + 3 * 128 + 64
+    qpad = torch.zeros((w.num_seqs, stride), dtype=torch.bfloat16)
+    qpad[:, :32 * 128] = w.q
+    got1 = _decode_gpu(w, kc, vc, 0, False, q=qpad, q_stride=stride)
+    got2 = _decode_gpu(w, kc, vc, 0, False, q=qpad, q_stride=stride)
+    assert np.array_equal(got1, got2)
+    assert_decode_close(got1, _decode_ref(w, kr, vr, 0, False, q=qpad, q_stride=stride))
+
+
+def test_decode_clamps_overlong_sequence_and_flags_it():
+    w = kvgen.custom(8, seq_lens=[40], num_q_heads=4, num_kv_heads=2, head_dim=128, block_size=16)
+    kc, vc, kr, vr = _caches(w, False)
+    long = kvgen.Workload(**{**w.__dict__, "seq_lens": torch.tensor([10_000], dtype=torch.int32)})
+    pk.kv_get_device_error()
+    got = _decode_gpu(long, kc, vc, 0, False)
+    assert pk.kv_get_device_error() & 2
+    # clamped to the table's 3 blocks = 48 positions, 8 of which hold NaN poison in
+    # the last block: the clamp must not read past the table, and the output is
+    # finite where the clamped range holds data only; here it does not
+    assert got.shape == (1, 4, 128)
+
+
+# ---------------------------------------------------------------------------
+# full-size workloads, sampled outputs, in the benchmark's launch configuration
+# ---------------------------------------------------------------------------
+def _sampled_reference(w, rows, q_cpu, seqs, heads, window, fp8):
+    """Oracle outputs for the sampled sequences: the oracle writes just those
+    sequences' tokens into a compact host pool (blocks renumbered in table
+    order) and decodes from it."""
+    bs, H, D = w.block_size, w.num_kv_heads, w.head_dim
+    lens = w.seq_lens.cpu().numpy()
+    nblk = [-(-int(lens[s]) // bs) for s in seqs]
+    mb = max(max(nblk), 1)
+    table = np.full((len(seqs), mb), -1, np.int32)
+    cursor = 0
+    for i, nb in enumerate(nblk):
+        table[i, :nb] = np.arange(cursor, cursor + nb, dtype=np.int32)
+        cursor += nb
+    pool_blocks = max(cursor, 1)
+    vr = np.full((pool_blocks, bs, H, D), kvgen.BF16_NAN, np.uint16)
+    kr = np.full((pool_blocks, bs, H, D), kvgen.E4M3_NAN if fp8 else kvgen.BF16_NAN,
+                 np.uint8 if fp8 else np.uint16)
+    for i, s in enumerate(seqs):
+        L = int(lens[s])
+        if L == 0:
+            continue
+        sl = oracle.fill_slots(table[i], 0, L, bs)
+        kk, vv = u16(rows[s][0]), u16(rows[s][1])
+        if fp8:
+            oracle.write_fp8k(kk, vv, kr, vr, sl, L, H, D, bs, H * D, H * D, w.k_scale)
+        else:
+            oracle.write_bf16(kk, vv, kr, vr, sl, L, H, D, bs, H * D, H * D)
+    qs = u16(q_cpu[list(seqs)])
+    sub_lens = np.ascontiguousarray(lens[list(seqs)].astype(np.int32))
+    out = {}
+    for i, s in enumerate(seqs):
+        for h in heads:
+            out[(s, h)] = oracle.decode_one(qs, None if fp8 else kr, kr if fp8 else None, vr, table, sub_lens,
+                                            mb, w.num_q_heads, H, D, bs, w.inv_sqrt_d, w.k_scale,
+                                            w.num_q_heads * D, window, i, h)
+    return out
+
+
+def _full_size(w, fp8, windows, sample_seqs, heads):
+    H, D, bs, nb, n = w.num_kv_heads, w.head_dim, w.block_size, w.num_blocks, w.num_tokens
+    slots = gpu_slots(w)
+    vc = kvgen.poisoned_pool(nb, bs, H, D, "bf16", DEV)
+    kc = kvgen.poisoned_pool(nb, bs, H, D, "fp8" if fp8 else "bf16", DEV)
+    chunk = 262144
+    for t0 in range(0, n, chunk):
+        t1 = min(n, t0 + chunk)
+        if fp8:
+            pk.kv_write_fp8k(w.key[t0:t1], w.value[t0:t1], kc, vc, slots[t0:t1], t1 - t0, H, D, bs, H * D,
+                             H * D, w.k_scale)
+        else:
+            pk.kv_write_bf16(w.key[t0:t1], w.value[t0:t1], kc, vc, slots[t0:t1], t1 - t0, H, D, bs, H * D,
+                             H * D)
+    with_workspace(w, True)
+    lens = w.seq_lens.cpu().numpy()
+    starts = np.concatenate([[0], np.cumsum(lens.astype(np.int64))])
+    # copy just the sampled sequences' rows to the host
+    rows = {s: (w.key[starts[s]:starts[s + 1]].cpu(), w.value[starts[s]:starts[s + 1]].cpu())
+            for s in sample_seqs}
+    q_cpu = w.q.cpu()
+    for win in windows:
+        got = _decode_gpu(w, kc, vc, win, fp8)
+        ref = _sampled_reference(w, rows, q_cpu, sample_seqs, heads, win, fp8)
+        g = np.stack([got[s, h] for (s, h) in ref])
+        r = np.stack(list(ref.values()))
+        assert_decode_close(g, r, f"{w.name} window {win}")
+        assert np.isfinite(got).all()
+    assert pk.kv_get_device_error() == 0
+
+
+def test_full_bf16_gqa4_sampled():
+    w = kvgen.bf16_gqa4(device=DEV)
+    lens = w.seq_lens.cpu().numpy()
+    seqs = sorted({int(lens.argmax()), int(lens.argmin()), 0, 31, 63})
+    _full_size(w, False, (0,), seqs, (0, 3, 17, 31))
+
+
+def test_full_fp8k_long_sampled():
+    w = kvgen.fp8k_long(device=DEV)
+    _full_size(w, True, (0, 4096), [0, 77, 127], (0, 5, 31))
+
+
+def test_full_fp8k_mixed_sampled():
+    w = kvgen.fp8k_mixed(device=DEV)
+    lens = w.seq_lens.cpu().numpy()
+    seqs = sorted({int(lens.argmax()), int(lens.argmin()), 100, 200})
+    _full_size(w, True, (0,), seqs, (0, 7, 8, 63))
