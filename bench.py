@@ -131,7 +131,11 @@ WORKLOAD_OF_PART = {"fused_write": "fused", "bf16_prefill": "bf16_gqa4", "bf16_d
 
 
 class GpuStep:
-    def __init__(self, dev, only_part=None):
+    # workload sizes for --small (profiling captures): fewer sequences, the
+    # same shapes otherwise; every input still exceeds L2
+    SMALL = {"bf16_gqa4": dict(num_seqs=16), "fp8k_long": dict(num_seqs=4), "fp8k_mixed": dict(num_seqs=32)}
+
+    def __init__(self, dev, only_part=None, small=False):
         import torch
 
         import kvgen
@@ -140,21 +144,31 @@ class GpuStep:
         self.parts = []          # (name, fn, bytes, tokens, launches)
         self.ws = None
         self.only_part = only_part
+        self.small = small
         self._setup()
 
     # -- helpers
     def _slots_calls(self, w, tables, slots):
-        """One kv_fill_slots per sequence into `slots`; returns the launch count."""
+        """One kv_fill_slots per sequence into `slots`: returns a callable that
+        runs them all, the launch count, and the per-sequence callables (the
+        graph capture spreads these over parallel branches)."""
         pk = self.pk
         lens = w.seq_lens.tolist()
         offs = [0]
         for L in lens:
             offs.append(offs[-1] + L)
 
+        def one(s):
+            def f():
+                pk.kv_fill_slots(slots[offs[s]:offs[s + 1]], tables[s], 0, lens[s], w.block_size)
+            return f
+        each = [one(s) for s, L in enumerate(lens) if L > 0]
+
         def run():
-            for s, L in enumerate(lens):
-                pk.kv_fill_slots(slots[offs[s]:offs[s + 1]], tables[s], 0, L, w.block_size)
-        return run, sum(1 for L in lens if L > 0)
+            for f in each:
+                f()
+        run.each = each
+        return run, len(each)
 
     def _setup(self):
         torch, pk = self.torch, self.pk
@@ -189,17 +203,21 @@ class GpuStep:
         wt, pos = w.extra["k_norm_weight"].to(dev), w.positions.to(dev)
         key, value = w.key.contiguous(), w.value.contiguous()
 
-        def run():
-            fill()
+        def main():
             pk.kv_write_fused_k_norm_rope_bf16(key, wt, pos, kc, slots, n, H, D, 128, bs, 1e-6, 1e6)
             pk.kv_write_v_only(value, vc, slots, n, H, D, bs, H * D)
-        self.parts.append(dict(name="fused_write", fn=run, tokens=n, launches=nfill + 2,
+
+        def run():
+            fill()
+            main()
+        self.parts.append(dict(name="fused_write", fn=run, fills=fill.each, main=main, tokens=n,
+                               launches=nfill + 2,
                                bytes=n * (2048 + 2048 + 4 + 8 + 2048 + 2048 + 8 + 8), kind="write"))
         self.inputs_h2d += [key, value, pos, tables]
 
     def _setup_bf16_gqa4(self):
         torch, kvgen, pk, dev = self.torch, self.kvgen, self.pk, self.dev
-        w = kvgen.bf16_gqa4(device=dev)
+        w = kvgen.bf16_gqa4(device=dev, **(self.SMALL['bf16_gqa4'] if self.small else {}))
         H, D, bs, Hq, n = w.num_kv_heads, w.head_dim, w.block_size, w.num_q_heads, w.num_tokens
         tables = w.block_tables.to(dev)
         slots = torch.empty(n, dtype=torch.int64, device=dev)
@@ -209,14 +227,18 @@ class GpuStep:
         key, value, q, lens = w.key, w.value, w.q, w.seq_lens.to(dev)
         out = torch.empty((w.num_seqs, Hq, D), dtype=torch.float32, device=dev)
 
+        def prefill_main():
+            pk.kv_write_bf16(key, value, kc, vc, slots, n, H, D, bs, H * D, H * D)
+
         def prefill():
             fill()
-            pk.kv_write_bf16(key, value, kc, vc, slots, n, H, D, bs, H * D, H * D)
+            prefill_main()
 
         def decode():
             pk.paged_decode_attn_bf16(q, kc, vc, out, tables, lens, w.max_blocks_per_seq, w.num_seqs, Hq, H, D, bs,
                                       w.inv_sqrt_d, Hq * D, 0)
-        self.parts.append(dict(name="bf16_prefill", fn=prefill, tokens=n, launches=nfill + 1,
+        self.parts.append(dict(name="bf16_prefill", fn=prefill, fills=fill.each, main=prefill_main, tokens=n,
+                               launches=nfill + 1,
                                bytes=n * write_bytes_per_token(H * D, 2), kind="write"))
         self.parts.append(dict(name="bf16_decode", fn=decode, tokens=w.num_seqs,
                                launches=1 + self._combine(w), kind="decode",
@@ -228,7 +250,7 @@ class GpuStep:
 
     def _setup_fp8k_long(self):
         torch, kvgen, pk, dev = self.torch, self.kvgen, self.pk, self.dev
-        w = kvgen.fp8k_long(device=dev)
+        w = kvgen.fp8k_long(device=dev, **(self.SMALL['fp8k_long'] if self.small else {}))
         H, D, bs, Hq, n = w.num_kv_heads, w.head_dim, w.block_size, w.num_q_heads, w.num_tokens
         tables = w.block_tables.to(dev)
         slots = torch.empty(n, dtype=torch.int64, device=dev)
@@ -243,10 +265,13 @@ class GpuStep:
             pk.kv_write_fp8k(key[c0:c1], value[c0:c1], kc, vc, slots[c0:c1], c1 - c0, H, D, bs, H * D, H * D,
                              k_scale)
 
-        def prefill():
-            fill()
+        def prefill_main():
             for c0, c1 in chunks:
                 write_chunk(c0, c1)
+
+        def prefill():
+            fill()
+            prefill_main()
 
         def make_decode(win, out):
             def decode():
@@ -254,7 +279,8 @@ class GpuStep:
                                           bs, w.inv_sqrt_d, k_scale, Hq * D, win)
             return decode
         self.fp8_chunks, self.fp8_write_chunk, self.fp8_row = chunks, write_chunk, H * D
-        self.parts.append(dict(name="fp8k_prefill", fn=prefill, tokens=n, launches=nfill + len(chunks),
+        self.parts.append(dict(name="fp8k_prefill", fn=prefill, fills=fill.each, main=prefill_main, tokens=n,
+                               launches=nfill + len(chunks),
                                bytes=n * write_bytes_per_token(H * D, 1), kind="write"))
         outs = []
         for win in (0, 4096):
@@ -270,7 +296,7 @@ class GpuStep:
 
     def _setup_fp8k_mixed(self):
         torch, kvgen, pk, dev = self.torch, self.kvgen, self.pk, self.dev
-        w = kvgen.fp8k_mixed(device=dev)
+        w = kvgen.fp8k_mixed(device=dev, **(self.SMALL['fp8k_mixed'] if self.small else {}))
         H, D, bs, Hq, n = w.num_kv_heads, w.head_dim, w.block_size, w.num_q_heads, w.num_tokens
         tables = w.block_tables.to(dev)
         slots = torch.empty(n, dtype=torch.int64, device=dev)
@@ -308,6 +334,35 @@ class GpuStep:
         # the split-KV combine kernel runs when a sequence can span more than 8 tiles of 16 positions
         return 1 if w.max_blocks_per_seq * w.block_size > 8 * 16 else 0
 
+    def capture(self, branches: int = 8):
+        """Capture one step into a CUDA graph. Each part's per-sequence slot
+        fills run on `branches` parallel side streams (independent kernels),
+        joined before the part's write; everything else is in stream order."""
+        torch = self.torch
+        self.graph = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream()
+        side = [torch.cuda.Stream() for _ in range(branches)]
+        cap.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.graph(self.graph, stream=cap):
+            for p in self.parts:
+                fills = p.get("fills")
+                if fills:
+                    for i, st in enumerate(side):
+                        st.wait_stream(cap)
+                        with torch.cuda.stream(st):
+                            for f in fills[i::branches]:
+                                f()
+                    for st in side:
+                        cap.wait_stream(st)
+                    p["main"]()
+                else:
+                    p["fn"]()
+        torch.cuda.current_stream().wait_stream(cap)
+        torch.cuda.synchronize()
+
+    def replay(self):
+        self.graph.replay()
+
     def run_step(self, events=None):
         torch = self.torch
         for i, p in enumerate(self.parts):
@@ -333,7 +388,7 @@ def run_gpu(args):
     __graft_entry__.build()
     import paged_kv_cache_fill_gb300 as pk
 
-    step = GpuStep(dev, args.part)
+    step = GpuStep(dev, args.part, args.small)
     stream = torch.cuda.current_stream()
     if args.part:
         # one part only, for profiling: warm-up, then `steps` runs, no report
@@ -353,19 +408,28 @@ def run_gpu(args):
         step.run_step()
     barrier()
     assert pk.kv_get_device_error() == 0, "kernel fault bits set during warm-up"
+    step.capture()
+    for _ in range(args.warmup):
+        step.replay()
+    barrier()
 
-    nparts = len(step.parts)
-    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nparts)]
-          for _ in range(args.steps)]
     with Clocks(local) as clk:
         barrier()
         t_start = torch.cuda.Event(enable_timing=True)
         t_end = torch.cuda.Event(enable_timing=True)
         t_start.record(stream)
-        for k in range(args.steps):
-            step.run_step(ev[k])
+        for _ in range(args.steps):
+            step.replay()
         t_end.record(stream)
         barrier()
+    assert pk.kv_get_device_error() == 0, "kernel fault bits set during the timed steps"
+    # per-call times: the same calls launched eagerly, CUDA events around each part
+    nparts = len(step.parts)
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nparts)]
+          for _ in range(args.steps)]
+    for k in range(args.steps):
+        step.run_step(ev[k])
+    torch.cuda.synchronize()
     clocks = clk.summary()
     elapsed_ms = t_start.elapsed_time(t_end)
     ms_per_step = elapsed_ms / args.steps
@@ -408,6 +472,8 @@ def run_gpu(args):
                        "l2": "inputs larger than L2 (the step moves ~45 GB; no call's inputs stay in L2)",
                        "algorithmic_bytes_per_step": int(step.total_bytes),
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "step_mode": "one CUDA-graph replay per step (the per-sequence slot fills run as 8 parallel graph "
+                         "branches); per-call 'parts' timed from eager launches with CUDA events",
             "parts": parts,
             "roofline": roofline,
             "cpu_baseline": cpu,
@@ -486,7 +552,7 @@ def run_e2e(step, args, dev, world):
     def one():
         for h, d in zip(host_in, step.inputs_h2d):
             d.copy_(h, non_blocking=True)
-        step.run_step()
+        step.replay()
         for h, d in zip(host_out, step.outputs_d2h):
             h.copy_(d, non_blocking=True)
 
@@ -623,6 +689,7 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time for the CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--small", action="store_true", help="with --part: fewer sequences (profiling captures)")
     ap.add_argument("--part", choices=sorted(WORKLOAD_OF_PART), default=None,
                     help="set up one workload and run one part only (for ncu captures); prints no bench line")
     args = ap.parse_args()

@@ -18,6 +18,7 @@ std::mutex g_mutex;
 DeviceInfo g_devices[kMaxDevices];
 void* g_ws_ptr[kMaxDevices];
 size_t g_ws_bytes[kMaxDevices];
+bool g_ws_fresh[kMaxDevices];
 
 int current_device() {
   int d = 0;
@@ -189,8 +190,16 @@ static int decode_common(const kv_bf16_t* q, const void* k_cache, const kv_bf16_
     std::lock_guard<std::mutex> lock(g_mutex);
     a.workspace = g_ws_ptr[dev.device];
     a.workspace_bytes = g_ws_bytes[dev.device];
+    a.workspace_fresh = g_ws_fresh[dev.device];
   }
-  return launch_decode(a, as_stream(stream));
+  const int status = launch_decode(a, as_stream(stream));
+  if (status == KV_OK && a.workspace_fresh) {
+    // the work counters were zeroed on this call's stream; the kernels keep
+    // them at zero from here on
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (g_ws_ptr[dev.device] == a.workspace) g_ws_fresh[dev.device] = false;
+  }
+  return status;
 }
 
 int paged_decode_attn_bf16(const kv_bf16_t* q, const kv_bf16_t* k_cache, const kv_bf16_t* v_cache,
@@ -225,6 +234,7 @@ int kv_set_decode_workspace(void* device_ptr, size_t bytes) {
   std::lock_guard<std::mutex> lock(g_mutex);
   g_ws_ptr[d] = bytes ? device_ptr : nullptr;
   g_ws_bytes[d] = device_ptr ? bytes : 0;
+  g_ws_fresh[d] = g_ws_ptr[d] != nullptr;
   return KV_OK;
 }
 

@@ -43,7 +43,8 @@ __device__ uint32_t g_decode_error;
 
 constexpr int kTile = 16;            // tokens per stage
 constexpr int kHeaderBytes = 256;    // workspace header (split size)
-constexpr int kItemsPerCtaTarget = 16;
+constexpr int kItemsPerCtaTarget = 24;  // items per CTA the split size aims for
+constexpr int kMinSplitTiles = 16;      // smallest split: 256 positions
 constexpr float kLog2e = 1.4426950408889634f;
 
 enum : int32_t {
@@ -65,7 +66,7 @@ struct DecodeParams {
   float* output;
   float* ws_o;          // [num_seqs, max_splits, Hq, D] partial outputs (unnormalised)
   float* ws_ml;         // [num_seqs, max_splits, Hq, 2] running max (log2 units) and sum
-  uint32_t* ws_header;  // split size chosen by the kernel
+  uint32_t* ws_header;  // [0] split size chosen by the kernel, [1] work counter, [2] done counter
   uint32_t max_blocks_per_seq, num_seqs, num_q_heads, num_kv_heads, block_size, block_shift;
   uint32_t group;       // query heads per KV head
   uint32_t heads_per_item;  // HG
@@ -160,7 +161,7 @@ __global__ void __launch_bounds__(32 * 9, 1)
   __syncthreads();
 
   // Split size: enough items for ~kItemsPerCtaTarget per CTA, never below
-  // the minimum the workspace was sized for.
+  // the minimum split (or the larger minimum a small workspace imposes).
   if (p.max_splits > 0) {
     uint64_t local = 0;
     for (uint32_t s = threadIdx.x; s < p.num_seqs; s += blockDim.x)
@@ -194,7 +195,17 @@ __global__ void __launch_bounds__(32 * 9, 1)
     bool ok = true;
     const uint32_t k_head_bytes = kKChunks * kTile * 128;
     const uint32_t v_head_bytes = kVChunks * kTile * 128;
-    for (uint64_t it = blockIdx.x; ok; it += gridDim.x) {
+    // Items are handed out by an atomic counter in the workspace (each CTA
+    // keeps the next item id in hand and asks for the one after while it
+    // issues the current item), or statically without a workspace.
+    const bool dynamic = p.max_splits > 0;
+    uint32_t* const work = dynamic ? p.ws_header + 1 : nullptr;
+    auto grab = [&]() -> uint32_t { return lane == 0 ? atomicAdd(work, 1u) : 0u; };
+    uint64_t it = dynamic ? __shfl_sync(0xffffffffu, grab(), 0) : blockIdx.x;
+    uint64_t next = dynamic ? __shfl_sync(0xffffffffu, grab(), 0) : it + gridDim.x;
+    uint32_t pending = 0;
+    for (; ok; it = next, next = dynamic ? __shfl_sync(0xffffffffu, pending, 0) : next + gridDim.x) {
+      if (dynamic) pending = grab();  // consumed at the end of this iteration
       // locate the item's sequence
       while (wk.chunk_seq < p.num_seqs && it >= wk.chunk_items + wk.chunk_total) {
         wk.chunk_items += wk.chunk_total;
@@ -292,6 +303,14 @@ __global__ void __launch_bounds__(32 * 9, 1)
       }
     }
     if (!__all_sync(0xffffffffu, ok) && lane == 0) atomicOr(&g_decode_error, kErrWaitTimeout);
+    // The last CTA to finish resets the counters for the next launch.
+    if (dynamic && lane == 0) {
+      __threadfence();
+      if (atomicAdd(p.ws_header + 2, 1u) == gridDim.x - 1) {
+        atomicExch(p.ws_header + 1, 0u);
+        atomicExch(p.ws_header + 2, 0u);
+      }
+    }
     return;
   }
 
@@ -534,29 +553,71 @@ __global__ void __launch_bounds__(32 * 9, 1)
 
 // Merge the split partials of every (sequence, query head) whose sequence
 // has more than one split: o = sum_i 2^(m_i - M) acc_i / sum_i 2^(m_i - M) l_i,
-// in split order.
+// in split order. One CTA of D threads per (sequence, query head): the
+// splits' (m, l) are reduced across the threads, then each thread sums its
+// output element over the splits with independent (overlapping) loads.
+constexpr int kCombineMaxSplits = 1024;  // per pass through shared memory
+
 template <int D>
 __global__ void __launch_bounds__(D) combine_kernel(const DecodeParams p) {
-  const uint32_t s = blockIdx.x;
+  __shared__ float s_w[kCombineMaxSplits];
+  __shared__ float s_red[D / 32];
+  __shared__ float s_bcast;
+  const uint32_t s = blockIdx.x, h = blockIdx.y;
   const uint32_t split_tiles = *p.ws_header;
   const SeqSpan span = seq_span(__ldg(p.seq_lens + s), p);
   const int32_t nsplit = splits_of(span.ntiles, split_tiles);
   if (nsplit <= 1) return;
-  const uint32_t d = threadIdx.x;
-  for (uint32_t h = blockIdx.y; h < p.num_q_heads; h += gridDim.y) {
-    float M = -INFINITY;
-    for (int32_t i = 0; i < nsplit; ++i)
-      M = fmaxf(M, p.ws_ml[((uint64_t(s) * p.max_splits + i) * p.num_q_heads + h) * 2]);
-    float num = 0.0f, den = 0.0f;
-    for (int32_t i = 0; i < nsplit; ++i) {
-      const uint64_t row = (uint64_t(s) * p.max_splits + i) * p.num_q_heads + h;
-      const float2 ml = *reinterpret_cast<const float2*>(p.ws_ml + row * 2);
-      const float w = fast_exp2(ml.x - M);
-      num += w * p.ws_o[row * D + d];
-      den += w * ml.y;
+  const uint32_t t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const uint64_t row0 = uint64_t(s) * p.max_splits * p.num_q_heads + h;  // split i at row0 + i*Hq
+  auto block_reduce = [&](float v, bool is_max) -> float {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float u = __shfl_xor_sync(0xffffffffu, v, o);
+      v = is_max ? fmaxf(v, u) : v + u;
     }
-    p.output[(uint64_t(s) * p.num_q_heads + h) * D + d] = num / den;
+    if (lane == 0) s_red[warp] = v;
+    __syncthreads();
+    if (t == 0) {
+      float r = s_red[0];
+      for (int w = 1; w < D / 32; ++w) r = is_max ? fmaxf(r, s_red[w]) : r + s_red[w];
+      s_bcast = r;
+    }
+    __syncthreads();
+    const float r = s_bcast;
+    __syncthreads();
+    return r;
+  };
+  // global max of the splits' running maxima
+  float m = -INFINITY;
+  for (int32_t i = t; i < nsplit; i += D)
+    m = fmaxf(m, p.ws_ml[(row0 + uint64_t(i) * p.num_q_heads) * 2]);
+  const float M = block_reduce(m, true);
+  float num = 0.0f, den_part = 0.0f;
+  for (int32_t base = 0; base < nsplit; base += kCombineMaxSplits) {
+    const int32_t n = nsplit - base < kCombineMaxSplits ? nsplit - base : kCombineMaxSplits;
+    for (int32_t i = t; i < n; i += D) {
+      const float2 ml = *reinterpret_cast<const float2*>(p.ws_ml + (row0 + uint64_t(base + i) * p.num_q_heads) * 2);
+      const float w = fast_exp2(ml.x - M);
+      s_w[i] = w;
+      den_part += w * ml.y;
+    }
+    __syncthreads();
+    const float* src = p.ws_o + (row0 + uint64_t(base) * p.num_q_heads) * D + t;
+    const uint64_t step = uint64_t(p.num_q_heads) * D;
+    int32_t i = 0;
+    for (; i + 8 <= n; i += 8) {
+      float v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) v[u] = src[uint64_t(i + u) * step];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) num += s_w[i + u] * v[u];
+    }
+    for (; i < n; ++i) num += s_w[i] * src[uint64_t(i) * step];
+    __syncthreads();
   }
+  const float den = block_reduce(den_part, false);
+  p.output[(uint64_t(s) * p.num_q_heads + h) * D + t] = num / den;
 }
 
 // ---------------------------------------------------------------- host side
@@ -629,15 +690,24 @@ int launch_decode_t(const DecodeArgs& a, cudaStream_t stream, const Geometry& ge
       !encode_pool_map(&mv, a.v_cache, false, a.num_kv_heads, D))
     return KV_ERR_CUDA;
   auto kern = decode_kernel<kFp8, D, NT>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(geo.smem_bytes)) !=
-      cudaSuccess)
-    return KV_ERR_CUDA;
+  // The dynamic shared-memory opt-in is set once per device and size (so
+  // that calls made while a stream is being captured into a CUDA graph after
+  // a first eager call issue no attribute change).
+  static int set_bytes[64] = {0};
+  const int dev_id = device_info().device;
+  if (dev_id < 0 || dev_id >= 64) return KV_ERR_CUDA;
+  if (set_bytes[dev_id] < int(geo.smem_bytes)) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(geo.smem_bytes)) !=
+        cudaSuccess)
+      return KV_ERR_CUDA;
+    set_bytes[dev_id] = int(geo.smem_bytes);
+  }
   const DeviceInfo& dev = device_info();
   const uint32_t threads = 32 * (1 + geo.heads_per_item * geo.nt);
   kern<<<dev.num_sms, threads, geo.smem_bytes, stream>>>(mk, mv, p);
   if (cudaGetLastError() != cudaSuccess) return KV_ERR_CUDA;
   if (p.max_splits > 0) {
-    dim3 grid(p.num_seqs, p.num_q_heads < 8 ? p.num_q_heads : 8);
+    dim3 grid(p.num_seqs, p.num_q_heads);
     combine_kernel<D><<<grid, D, 0, stream>>>(p);
     if (cudaGetLastError() != cudaSuccess) return KV_ERR_CUDA;
   }
@@ -650,7 +720,7 @@ size_t decode_workspace_bytes(uint32_t max_blocks_per_seq, uint32_t num_seqs, ui
                               uint32_t num_kv_heads, uint32_t head_dim, uint32_t block_size) {
   (void)num_kv_heads;
   const uint64_t max_tiles = (uint64_t(max_blocks_per_seq) * block_size + kTile - 1) / kTile;
-  const uint64_t max_splits = (max_tiles + 8 - 1) / 8;  // minimum split of 8 tiles
+  const uint64_t max_splits = (max_tiles + kMinSplitTiles - 1) / kMinSplitTiles;
   return kHeaderBytes + uint64_t(num_seqs) * max_splits * num_q_heads * (uint64_t(head_dim) + 2) * 4;
 }
 
@@ -683,21 +753,24 @@ int launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   p.v_bytes = geo.v_bytes;
 
   // Split-KV when a workspace is registered and large enough for two or more
-  // splits: splits are at least 8 tiles (128 positions), more if the
-  // workspace is smaller than the worst case needs.
+  // splits: splits are at least kMinSplitTiles tiles, more if the workspace
+  // is smaller than the worst case needs.
   const uint64_t max_tiles = (uint64_t(a.max_blocks_per_seq) * a.block_size + kTile - 1) / kTile;
   p.max_splits = 0;
   p.min_split_tiles = 0x7fffffffu;
-  if (a.workspace && a.workspace_bytes > kHeaderBytes && max_tiles > 8) {
+  if (a.workspace && a.workspace_bytes > kHeaderBytes && max_tiles > kMinSplitTiles) {
     const uint64_t per_split = uint64_t(a.num_seqs) * a.num_q_heads * (a.head_dim + 2) * 4;
     const uint64_t fit = (a.workspace_bytes - kHeaderBytes) / per_split;
-    const uint64_t needed = (max_tiles + 7) / 8;
+    const uint64_t needed = (max_tiles + kMinSplitTiles - 1) / kMinSplitTiles;
     uint64_t min_tiles = 0;
     if (fit >= needed)
-      min_tiles = 8;
+      min_tiles = kMinSplitTiles;
     else if (fit >= 2)
       min_tiles = (max_tiles + fit - 1) / fit;
     if (min_tiles) {
+      if (a.workspace_fresh &&
+          cudaMemsetAsync(a.workspace, 0, kHeaderBytes, stream) != cudaSuccess)
+        return KV_ERR_CUDA;
       p.min_split_tiles = uint32_t(min_tiles);
       p.max_splits = uint32_t((max_tiles + min_tiles - 1) / min_tiles);
       uint8_t* ws = static_cast<uint8_t*>(a.workspace);

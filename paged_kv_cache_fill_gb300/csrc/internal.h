@@ -53,6 +53,7 @@ struct DecodeArgs {
   bool fp8;
   void* workspace;
   size_t workspace_bytes;
+  bool workspace_fresh;  // registered since the last decode: its counters must be zeroed first
 };
 
 size_t decode_workspace_bytes(uint32_t max_blocks_per_seq, uint32_t num_seqs, uint32_t num_q_heads,

@@ -117,9 +117,9 @@ def test_unsupported_shapes(pk):
 
 
 def test_workspace_size_formula(pk):
-    # header + num_seqs * ceil(ceil(mbps*bs/16)/8) splits * Hq * (D + 2) floats
+    # header + num_seqs * ceil(ceil(mbps*bs/16)/16) splits * Hq * (D + 2) floats
     got = pk.kv_decode_workspace_bytes(512, 64, 32, 8, 128, 16)
-    assert got == 256 + 64 * 64 * 32 * 130 * 4
+    assert got == 256 + 64 * 32 * 32 * 130 * 4
     assert pk.kv_decode_workspace_bytes(1, 1, 4, 2, 64, 16) == 256 + 1 * 1 * 4 * 66 * 4
 
 
