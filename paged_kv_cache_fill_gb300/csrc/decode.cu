@@ -193,8 +193,6 @@ __global__ void __launch_bounds__(32 * 9, 1)
     wk.load(0, p, split_tiles, lane);
     uint32_t stage = 0, phase = 0;
     bool ok = true;
-    const uint32_t k_head_bytes = kKChunks * kTile * 128;
-    const uint32_t v_head_bytes = kVChunks * kTile * 128;
     // Items are handed out by an atomic counter in the workspace (each CTA
     // keeps the next item id in hand and asks for the one after while it
     // issues the current item), or statically without a workspace.
@@ -270,22 +268,15 @@ __global__ void __launch_bounds__(32 * 9, 1)
             if (tile == tile_end - 1) flags |= kLast;
             meta[stage] = StageMeta{int32_t(s), int32_t(hg), int32_t(split), tile, span.start,
                                     span.len, flags, 0};
-            const uint32_t bytes = heads_here * (k_head_bytes + v_head_bytes) +
-                                   ((flags & kFirst) ? q_bytes : 0u);
+            // one box per tensor covers all heads of the item (chunks past the
+            // last head are zero-filled and still counted in the box bytes)
+            const uint32_t bytes = p.k_bytes + p.v_bytes + ((flags & kFirst) ? q_bytes : 0u);
             mbar_arrive_expect_tx(&full[stage], bytes);
             uint8_t* st = smem + stage * p.stage_bytes;
             const int32_t slot0 = (block_id << p.block_shift) + ((tile << 4) & int32_t(p.block_size - 1));
-            for (uint32_t h = 0; h < heads_here; ++h) {
-              const int32_t head = int32_t(hg * p.heads_per_item + h);
-#pragma unroll
-              for (int c = 0; c < kKChunks; ++c)
-                tma_load_3d(st + (h * kKChunks + c) * (kTile * 128), &tmap_k, 0,
-                            head * kKChunks + c, slot0, &full[stage]);
-#pragma unroll
-              for (int c = 0; c < kVChunks; ++c)
-                tma_load_3d(st + p.k_bytes + (h * kVChunks + c) * (kTile * 128), &tmap_v, 0,
-                            head * kVChunks + c, slot0, &full[stage]);
-            }
+            const int32_t head0 = int32_t(hg * p.heads_per_item);
+            tma_load_3d(st, &tmap_k, 0, slot0, head0 * kKChunks, &full[stage]);
+            tma_load_3d(st + p.k_bytes, &tmap_v, 0, slot0, head0 * kVChunks, &full[stage]);
             if (flags & kFirst) bulk_load(st + p.k_bytes + p.v_bytes, q_src, q_bytes, &full[stage]);
           }
         }
@@ -634,20 +625,23 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
   return fn;
 }
 
-// Tensor map over a cache pool seen as [slots][heads * chunks][chunk elems]:
-// dim 0 the 128 bytes of a chunk, dim 1 the chunk (stride 128 bytes), dim 2
-// the slot (stride heads * head_dim * elem bytes). Box: one chunk x 16 slots,
-// 128-byte swizzle.
+// Tensor map over a cache pool for one TMA box per 16-position tile and
+// item: dim 0 the elements of a 128-byte chunk, dim 1 the slot (stride
+// heads * head_dim * elem bytes), dim 2 the 128-byte chunk of a slot's row
+// (stride 128 bytes; a head owns head_dim * elem / 128 consecutive chunks).
+// Box: one chunk x 16 slots x (heads per item * chunks per head), so the
+// shared-memory tile is [chunk][slot][128 bytes], 128-byte swizzled by slot
+// row. (Dim 1's stride exceeds dim 2's; the encoder accepts any order.)
 bool encode_pool_map(CUtensorMap* map, const void* base, bool fp8, uint32_t num_kv_heads,
-                     uint32_t head_dim) {
+                     uint32_t head_dim, uint32_t heads_per_item) {
   auto encode = get_encode();
   if (!encode) return false;
   const uint32_t elem = fp8 ? 1 : 2;
   const uint32_t chunk_elems = 128 / elem;
-  const uint32_t chunks = num_kv_heads * head_dim * elem / 128;
-  cuuint64_t dims[3] = {chunk_elems, chunks, cuuint64_t(1) << 31};
-  cuuint64_t strides[2] = {128, cuuint64_t(num_kv_heads) * head_dim * elem};
-  cuuint32_t box[3] = {chunk_elems, 1, kTile};
+  const uint32_t chunks_per_head = head_dim * elem / 128;
+  cuuint64_t dims[3] = {chunk_elems, cuuint64_t(1) << 31, cuuint64_t(num_kv_heads) * chunks_per_head};
+  cuuint64_t strides[2] = {cuuint64_t(num_kv_heads) * head_dim * elem, 128};
+  cuuint32_t box[3] = {chunk_elems, kTile, heads_per_item * chunks_per_head};
   cuuint32_t estr[3] = {1, 1, 1};
   const CUresult r = encode(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16, 3,
                             const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -686,8 +680,8 @@ Geometry geometry(bool fp8, uint32_t head_dim, uint32_t num_kv_heads, uint32_t g
 template <bool kFp8, int D, int NT>
 int launch_decode_t(const DecodeArgs& a, cudaStream_t stream, const Geometry& geo, DecodeParams& p) {
   CUtensorMap mk, mv;
-  if (!encode_pool_map(&mk, a.k_cache, kFp8, a.num_kv_heads, D) ||
-      !encode_pool_map(&mv, a.v_cache, false, a.num_kv_heads, D))
+  if (!encode_pool_map(&mk, a.k_cache, kFp8, a.num_kv_heads, D, geo.heads_per_item) ||
+      !encode_pool_map(&mv, a.v_cache, false, a.num_kv_heads, D, geo.heads_per_item))
     return KV_ERR_CUDA;
   auto kern = decode_kernel<kFp8, D, NT>;
   // The dynamic shared-memory opt-in is set once per device and size (so
