@@ -185,6 +185,35 @@ PAGEDKV_API int paged_decode_attn_fp8k(const kv_bf16_t *q, const kv_e4m3_t *k_ca
                            void *stream);
 
 /* ------------------------------------------------------------------------
+ * FP8-K paged decode without any caller-provided memory. The source pages
+ * have no counterpart of this call; it exists for callers that cannot give
+ * the library a device allocation: host code running in a callback enqueued
+ * with cudaLaunchHostFunc may not call the CUDA API (so it cannot
+ * cudaMalloc a workspace), and applications whose device memory belongs to
+ * another allocator (a framework memory pool, a serving engine with a fixed
+ * memory budget) cannot set a raw buffer aside for a library.
+ *
+ * Same arguments, results and limits as paged_decode_attn_fp8k; the
+ * split-KV scratch comes from a fixed 64 MiB array in the library's own
+ * device memory, which every GPU that loads the library keeps until the
+ * process exits. The call allocates and frees nothing. It returns
+ * KV_ERR_UNSUPPORTED when the shape's worst-case scratch
+ * (kv_decode_workspace_bytes of the same arguments) exceeds 64 MiB.
+ * The first call on a device, with that device current, looks up the
+ * array's device address (cudaGetSymbolAddress) and caches it: make that
+ * first call before any stream capture. All calls share the one array,
+ * which keeps the previous call's contents; each call clears the counters
+ * that must start at zero on its own stream first. Calls whose work may
+ * overlap on the GPU (different streams, other devices' calls aside) race on
+ * the array: order them.
+ * ---------------------------------------------------------------------- */
+PAGEDKV_API int paged_decode_attn_fp8k_static_scratch(
+    const kv_bf16_t *q, const kv_e4m3_t *k_cache_fp8, const kv_bf16_t *v_cache, float *output,
+    const int32_t *block_tables, const int32_t *seq_lens, uint32_t max_blocks_per_seq, uint32_t num_seqs,
+    uint32_t num_q_heads, uint32_t num_kv_heads, uint32_t head_dim, uint32_t block_size, float inv_sqrt_d,
+    float k_scale, uint32_t q_stride, uint32_t sliding_window, void *stream);
+
+/* ------------------------------------------------------------------------
  * Split-KV workspace (not on the pages: flash-decoding partials and the
  * combine step need scratch). The caller allocates device memory of at
  * least kv_decode_workspace_bytes(...) for the largest decode it will run
