@@ -203,14 +203,18 @@ class GpuStep:
         wt, pos = w.extra["k_norm_weight"].to(dev), w.positions.to(dev)
         key, value = w.key.contiguous(), w.value.contiguous()
 
-        def main():
+        def k_write():
             pk.kv_write_fused_k_norm_rope_bf16(key, wt, pos, kc, slots, n, H, D, 128, bs, 1e-6, 1e6)
+
+        def v_write():
             pk.kv_write_v_only(value, vc, slots, n, H, D, bs, H * D)
 
         def run():
             fill()
-            main()
-        self.parts.append(dict(name="fused_write", fn=run, fills=fill.each, main=main, tokens=n,
+            k_write()
+            v_write()
+        # the K and V writes touch different pools: the graph runs them side by side
+        self.parts.append(dict(name="fused_write", fn=run, fills=fill.each, mains=[k_write, v_write], tokens=n,
                                launches=nfill + 2,
                                bytes=n * (2048 + 2048 + 4 + 8 + 2048 + 2048 + 8 + 8), kind="write"))
         self.inputs_h2d += [key, value, pos, tables]
@@ -354,7 +358,14 @@ class GpuStep:
                                 f()
                     for st in side:
                         cap.wait_stream(st)
-                    p["main"]()
+                    mains = p.get("mains") or [p["main"]]
+                    for i, f in enumerate(mains):
+                        st = side[i]
+                        st.wait_stream(cap)
+                        with torch.cuda.stream(st):
+                            f()
+                    for st in side[:len(mains)]:
+                        cap.wait_stream(st)
                 else:
                     p["fn"]()
         torch.cuda.current_stream().wait_stream(cap)
@@ -373,15 +384,51 @@ class GpuStep:
                 events[i][1].record()
 
 
+class Ranks:
+    """One process per GPU (torchrun sets RANK / WORLD_SIZE / LOCAL_RANK).
+    Each rank runs its own replica of the step (weak scaling: the work per
+    GPU is fixed); the only collectives are the barriers around the timed
+    region and the max of the per-rank step times, never the data path."""
+
+    def __init__(self, backend: str | None = None):
+        import torch
+        import torch.distributed as dist
+        self.dist = dist
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        if self.world > 1 and not dist.is_initialized():
+            dist.init_process_group(backend or ("nccl" if torch.cuda.is_available() else "gloo"))
+        self.device = torch.device("cuda", self.local) if torch.cuda.is_available() else torch.device("cpu")
+
+    def barrier(self):
+        import torch
+        if self.world > 1:
+            self.dist.barrier()
+        if torch.cuda.is_available():
+            torch.cuda.synchronize()
+
+    def max(self, value: float) -> float:
+        """The largest of the ranks' values (every rank gets it)."""
+        if self.world == 1:
+            return float(value)
+        import torch
+        t = torch.tensor([float(value)], dtype=torch.float64,
+                         device=self.device if self.device.type == "cuda" and
+                         self.dist.get_backend() == "nccl" else "cpu")
+        self.dist.all_reduce(t, op=self.dist.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.world > 1 and self.dist.is_initialized():
+            self.dist.destroy_process_group()
+
+
 def run_gpu(args):
     import torch
-    import torch.distributed as dist
 
-    rank = int(os.environ.get("RANK", "0"))
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    if world > 1:
-        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    ranks = Ranks()
+    rank, world, local = ranks.rank, ranks.world, ranks.local
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     import __graft_entry__
@@ -399,10 +446,7 @@ def run_gpu(args):
         print(json.dumps({"part": args.part, "runs": args.warmup + args.steps, "ok": True}))
         return
 
-    def barrier():
-        if world > 1:
-            dist.barrier()
-        torch.cuda.synchronize()
+    barrier = ranks.barrier
 
     for _ in range(args.warmup):
         step.run_step()
@@ -435,10 +479,7 @@ def run_gpu(args):
     ms_per_step = elapsed_ms / args.steps
     part_ms = [statistics.mean(ev[k][i][0].elapsed_time(ev[k][i][1]) for k in range(args.steps))
                for i in range(nparts)]
-    if world > 1:
-        t = torch.tensor([ms_per_step], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_per_step = float(t.item())
+    ms_per_step = ranks.max(ms_per_step)  # the job is as slow as its slowest rank
 
     peak, peak_kind = measured_peak()
     value = step.total_bytes * world / (ms_per_step * 1e-3) / 1e9
@@ -473,7 +514,8 @@ def run_gpu(args):
                        "algorithmic_bytes_per_step": int(step.total_bytes),
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "step_mode": "one CUDA-graph replay per step (the per-sequence slot fills run as 8 parallel graph "
-                         "branches); per-call 'parts' timed from eager launches with CUDA events",
+                         "branches, the fused K and V-only writes side by side); per-call 'parts' timed "
+                         "from eager launches with CUDA events",
             "parts": parts,
             "roofline": roofline,
             "cpu_baseline": cpu,
@@ -483,48 +525,44 @@ def run_gpu(args):
             "setup_s": round(step.setup_s, 1),
         }
         print(json.dumps(line))
-    if world > 1:
-        dist.destroy_process_group()
+    ranks.close()
 
 
 def dominant_roofline(step, dom, stream, peak, peak_kind, args):
-    """Per-launch CUDA-event timing of the dominant part's main kernel."""
+    """Average launch duration of the dominant part's main kernel: CUDA events
+    on the launching stream around back-to-back launches, divided by the
+    number of launches."""
     import torch
     torch.cuda.synchronize()
+    reps = max(args.steps, 3)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if dom["name"] == "fp8k_prefill":
-        # the 16 kv_write_fp8k launches; bytes per launch from the tokens it writes
-        times, nbytes = [], []
-        for _ in range(max(args.steps, 3)):
+        # the 16 kv_write_fp8k launches of 262144 tokens each
+        a.record(stream)
+        for _ in range(reps):
             for c0, c1 in step.fp8_chunks:
-                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                a.record(stream)
                 step.fp8_write_chunk(c0, c1)
-                b.record(stream)
-                times.append((a, b))
-                nbytes.append((c1 - c0) * write_bytes_per_token(step.fp8_row, 1))
+        b.record(stream)
         torch.cuda.synchronize()
-        ms = [a.elapsed_time(b) for a, b in times]
+        launches = reps * len(step.fp8_chunks)
+        per_launch = statistics.mean((c1 - c0) * write_bytes_per_token(step.fp8_row, 1) for c0, c1 in step.fp8_chunks)
         kernel = "kv_write_fp8k (write_fp8k_kernel)"
-        achieved = statistics.mean(n / (m * 1e-3) / 1e9 for n, m in zip(nbytes, ms))
-        per_launch = statistics.mean(nbytes)
     else:
-        times = []
-        for _ in range(max(args.steps, 3)):
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            dom["fn"]()
-            b.record(stream)
-            times.append((a, b))
+        a.record(stream)
+        for _ in range(reps):
+            (dom.get("main") or dom["fn"])()
+        b.record(stream)
         torch.cuda.synchronize()
-        ms = [a.elapsed_time(b) for a, b in times]
-        kernel = f"{dom['name']} (decode_kernel + combine_kernel)"
+        launches = reps
         per_launch = dom["bytes"]
-        achieved = per_launch / (statistics.mean(ms) * 1e-3) / 1e9
+        kernel = f"{dom['name']} (decode_kernel + combine_kernel)"
+    avg_ms = a.elapsed_time(b) / launches
+    achieved = per_launch / (avg_ms * 1e-3) / 1e9
     traffic = profiled_traffic(dom["name"])
     return {"bound": "hbm", "kernel": kernel, "achieved": round(achieved, 1), "peak": peak,
             "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
-            "algorithmic_bytes_per_launch": int(per_launch), "avg_launch_ms": round(statistics.mean(ms), 4),
-            "traffic": traffic}
+            "algorithmic_bytes_per_launch": int(per_launch), "avg_launch_ms": round(avg_ms, 4),
+            "launches_timed": launches, "traffic": traffic}
 
 
 def profiled_traffic(part_name):

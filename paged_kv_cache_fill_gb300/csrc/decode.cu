@@ -672,6 +672,9 @@ Geometry geometry(bool fp8, uint32_t head_dim, uint32_t num_kv_heads, uint32_t g
     if (stages > 4) stages = 4;
     g.stages = stages;
     g.smem_bytes = stages * g.stage_bytes + extra;
+    // Keep all heads of a group in one item (8 consumer warps per CTA) even
+    // at 3 stages: 4 heads per item with a 6-stage ring measured slower (the
+    // per-tile MMA/softmax work of 4 warps becomes the limit).
     if (stages >= 2 || hg == 1) break;
   }
   return g;

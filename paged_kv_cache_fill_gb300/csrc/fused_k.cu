@@ -16,16 +16,20 @@
 //     remainder (|r| <= pi/64) by short Taylor series in double-binary32
 //     arithmetic, combined with a table of sin/cos(m pi/32) held as (hi, lo)
 //     pairs (rope_tables.h): about 2^-44 absolute error;
-//   - forms u_i cos - u_j sin with exact product error terms (FMA), so the
+//   - forms u_i cos - u_j sin inside one FMA against the rounded second
+//     product, adding that product's exact error (FMA) afterwards, so the
 //     cancellation is exact and the result is accurate to ~2^-23 of itself.
 // The error-free transforms use __fmul_rn / __fadd_rn so that the compiler
 // cannot fuse them into FMAs.
 //
-// Work split: a CTA handles 256 / (head_dim / 8) rows (token, head) per
-// step, head_dim / 8 lanes per row and 8 elements per lane: lane l < R/8
-// holds the rotation pairs (4l..4l+3, R/2+4l..R/2+4l+3), the other lanes 8
-// pass-through elements. The sin/cos of a token are computed once per token
-// into shared memory and shared by all its heads.
+// Work split: one 512-thread CTA per SM takes passes of up to
+// tokens_per_pass() tokens (all their heads); head_dim / 8 lanes per row and
+// 8 elements per lane: lane l < R/8 holds the rotation pairs (4l..4l+3,
+// R/2+4l..R/2+4l+3), the other lanes 8 pass-through elements; a thread keeps
+// up to 4 rows. Each pass
+// first issues every row load, then all threads build the pass's sin/cos
+// table in shared memory (once per token, shared by its heads) while the
+// loads are in flight, then normalises, rotates and stores every row.
 #include <math.h>
 
 #include "internal.h"
@@ -65,7 +69,7 @@ struct Freq {
 
 // sin and cos of the remainder r = rh + rl (|r| <= ~pi/64), combined with
 // the table entry m: returns (sin, cos) of m*pi/32 + r as (hi, lo) pairs.
-__device__ __forceinline__ float4 sincos_from_remainder(float rh, float rl, int m) {
+__device__ __forceinline__ float4 sincos_from_remainder(float rh, float rl, int m, const float4* tab) {
   // z = r^2
   const float zh = __fmul_rn(rh, rh);
   const float zl = fmaf(rh, rh, -zh) + 2.0f * rh * rl;
@@ -82,7 +86,7 @@ __device__ __forceinline__ float4 sincos_from_remainder(float rh, float rl, int 
   // cos r = 1 + d, d = -z/2 + z^2/24 - z^3/720
   const float dh = -0.5f * zh;
   const float dl = -0.5f * zl + (zh * zh) * (1.0f / 24.0f - zh * (1.0f / 720.0f));
-  const float4 t = kSinCosPio32[m & 63];  // {sin_hi, sin_lo, cos_hi, cos_lo}
+  const float4 t = tab[m & 63];  // {sin_hi, sin_lo, cos_hi, cos_lo} of m*pi/32
   // X + X*d + sign * Y*sin r
   auto combine = [&](float xh, float xl, float yh, float yl, float sign) -> Dd {
     const Dd t1 = two_prod(xh, dh);
@@ -101,7 +105,7 @@ __device__ __forceinline__ float4 sincos_from_remainder(float rh, float rl, int 
 }
 
 // sin and cos of pos * freq as (hi, lo) pairs.
-__device__ __forceinline__ float4 rope_sincos(int32_t pos, const Freq& f) {
+__device__ __forceinline__ float4 rope_sincos(int32_t pos, const Freq& f, const float4* tab) {
   if (pos > -65536 && pos < 65536) {
     const float pf = float(pos);  // exact
     const Dd a1 = two_prod(pf, f.h);
@@ -118,7 +122,7 @@ __device__ __forceinline__ float4 rope_sincos(int32_t pos, const Freq& f) {
     Dd s4 = two_sum(s3.hi, -q2.hi);
     const float lo = ((s1.lo + s2.lo) + (s3.lo + s4.lo)) + ((a2.lo + a3) - (q2.lo + q3));
     const Dd r = fast_two_sum(s4.hi, lo);
-    return sincos_from_remainder(r.hi, r.lo, int(k));
+    return sincos_from_remainder(r.hi, r.lo, int(k), tab);
   }
   // Large positions: reduce in binary64.
   const double a = double(pos) * f.d;
@@ -128,16 +132,19 @@ __device__ __forceinline__ float4 rope_sincos(int32_t pos, const Freq& f) {
   const float rh = float(r);
   const float rl = float(r - double(rh));
   const long long km = (long long)k;
-  return sincos_from_remainder(rh, rl, int(km & 63));
+  return sincos_from_remainder(rh, rl, int(km & 63), tab);
 }
 
-// Compensated u_a * c + sign * u_b * s with c = (ch, cl), s = (sh, sl).
+// u_a * c + sign * u_b * s with c = (ch, cl), s = (sh, sl), accurate to about
+// 2^-23 of the result even when the two products cancel: p2 = RN(u_b * sh)
+// with its exact error e2 (FMA); u_a * ch - p2 is formed exactly inside one
+// FMA and rounded once; the small terms are added last.
 __device__ __forceinline__ float rotate(float ua, float ub, float ch, float cl, float sh, float sl,
                                         float sign) {
-  const Dd p1 = two_prod(ua, ch);
-  const Dd p2 = two_prod(ub, sh);
-  const Dd s = two_sum(p1.hi, sign * p2.hi);
-  return s.hi + (s.lo + ((p1.lo + sign * p2.lo) + (ua * cl + sign * (ub * sl))));
+  const float p2 = __fmul_rn(ub, sh);
+  const float e2 = fmaf(ub, sh, -p2);
+  const float t0 = fmaf(ua, ch, sign * p2);  // ua*ch + sign*p2, one rounding
+  return t0 + (sign * e2 + (ua * cl + sign * (ub * sl)));
 }
 
 __device__ __forceinline__ void unpack8(const uint32_t (&w)[4], float (&x)[8]) {
@@ -148,38 +155,37 @@ __device__ __forceinline__ void unpack8(const uint32_t (&w)[4], float (&x)[8]) {
   }
 }
 
-constexpr int kThreads = 256;
-constexpr int kMaxRows = 32;        // rows per step for head_dim 64
-constexpr int kMaxTableEntries = 1024;  // tokens per step x rotary_dim/2
+constexpr int kThreads = 512;
+constexpr int kMaxRowsPerThread = 4;
+constexpr int kTableEntries = 2048;  // sin/cos entries per pass: tokens x rotary_dim/2
+
+// Tokens per pass for a head_dim/rotary/heads shape: bounded by the table and
+// by 16 rows per thread.
+__host__ __device__ inline uint32_t tokens_per_pass(uint32_t head_dim, uint32_t rotary_dim, uint32_t num_kv_heads) {
+  const uint32_t rows_per_pass = (kThreads / (head_dim / 8)) * kMaxRowsPerThread;
+  uint32_t t = kTableEntries / (rotary_dim / 2);
+  const uint32_t by_rows = rows_per_pass / num_kv_heads;
+  if (by_rows < t) t = by_rows;
+  return t < 1 ? 1 : t;
+}
 
 template <int D>
-__global__ void __launch_bounds__(kThreads) fused_k_norm_rope_kernel(
+__global__ void __launch_bounds__(kThreads, 1) fused_k_norm_rope_kernel(
     const uint16_t* __restrict__ k_in, const uint16_t* __restrict__ k_norm_weight,
     const int32_t* __restrict__ positions, uint16_t* __restrict__ k_cache,
     const int64_t* __restrict__ slot_mapping, uint32_t num_tokens, uint32_t num_kv_heads,
-    uint32_t rotary_dim, float rms_eps, float theta) {
-  constexpr int kLanes = D / 8;                 // lanes per row
-  constexpr int kRows = kThreads / kLanes;      // rows per step
-  static_assert(kRows <= kMaxRows, "rows per step");
+    uint32_t rotary_dim, float rms_eps, float theta, uint32_t tok_pass) {
+  constexpr int kLanes = D / 8;              // lanes per row
+  constexpr int kRows = kThreads / kLanes;   // rows per sweep of the CTA
   __shared__ Freq freq[128];
-  __shared__ float4 table[2][kMaxTableEntries];
+  __shared__ float4 table[kTableEntries];
+  __shared__ float4 sincos_pio32[64];  // lanes index it by position: shared, not constant, memory
+  if (threadIdx.x < 64) sincos_pio32[threadIdx.x] = kSinCosPio32[threadIdx.x];
 
   const uint32_t half = rotary_dim / 2;
-  // Frequencies theta^(-2i/R) in binary64, split into three binary32 parts.
-  if (threadIdx.x < half) {
-    const double c = -2.0 * log2(double(theta)) / double(rotary_dim);
-    const double f = exp2(c * double(threadIdx.x));
-    Freq e;
-    e.h = float(f);
-    e.m = float(f - double(e.h));
-    e.l = float(f - double(e.h) - double(e.m));
-    e.pad = 0.0f;
-    e.d = f;
-    freq[threadIdx.x] = e;
-  }
 
   const uint32_t lane = threadIdx.x % kLanes;
-  const uint32_t row_in_step = threadIdx.x / kLanes;
+  const uint32_t row_in_sweep = threadIdx.x / kLanes;
   const uint32_t pair_lanes = rotary_dim / 8;
   const bool is_pair = lane < pair_lanes;
   // element offsets of this lane's two groups of four (pair lanes) or one
@@ -194,76 +200,101 @@ __global__ void __launch_bounds__(kThreads) fused_k_norm_rope_kernel(
     const uint32_t ww[4] = {wa.x, wa.y, wb.x, wb.y};
     unpack8(ww, w);
   }
-  __syncthreads();
 
-  const uint64_t total_rows = uint64_t(num_tokens) * num_kv_heads;
-  const uint64_t steps = (total_rows + kRows - 1) / kRows;
-  uint32_t parity = 0;
-  for (uint64_t step = blockIdx.x; step < steps; step += gridDim.x, parity ^= 1) {
-    const uint64_t row0 = step * kRows;
-    const uint64_t row = row0 + row_in_step;
-    const bool active = row < total_rows;
-    const uint32_t t_first = uint32_t(row0 / num_kv_heads);
-    // rows past the end idle on the step's first token (in-bounds table reads)
-    const uint32_t t = active ? uint32_t(row / num_kv_heads) : t_first;
-    const uint32_t h = active ? uint32_t(row % num_kv_heads) : 0;
-    uint64_t last_row = row0 + kRows - 1;
-    if (last_row >= total_rows) last_row = total_rows - 1;
-    const uint32_t ntok = uint32_t(last_row / num_kv_heads) - t_first + 1;
+  const uint32_t passes = (num_tokens + tok_pass - 1) / tok_pass;
+  for (uint32_t pass = blockIdx.x; pass < passes; pass += gridDim.x) {
+    const uint32_t t0 = pass * tok_pass;
+    const uint32_t ntok = num_tokens - t0 < tok_pass ? num_tokens - t0 : tok_pass;
+    const uint32_t nrows = ntok * num_kv_heads;
 
-    // issue this row's loads first
-    int64_t slot = -1;
-    uint2 xa = make_uint2(0, 0), xb = make_uint2(0, 0);
-    if (active) {
-      slot = __ldg(slot_mapping + t);
-      const uint16_t* src = k_in + (uint64_t(t) * num_kv_heads + h) * D;
-      xa = __ldcs(reinterpret_cast<const uint2*>(src + off_a));
-      xb = __ldcs(reinterpret_cast<const uint2*>(src + off_b));
+    // 1. every load of the pass first: this thread's rows and their slots
+    uint2 xa[kMaxRowsPerThread], xb[kMaxRowsPerThread];
+    int64_t slot[kMaxRowsPerThread];
+    uint32_t tok_of[kMaxRowsPerThread], head_of[kMaxRowsPerThread];  // token in the pass, head
+#pragma unroll
+    for (int k = 0; k < kMaxRowsPerThread; ++k) {
+      const uint32_t row = row_in_sweep + k * kRows;
+      xa[k] = xb[k] = make_uint2(0, 0);
+      slot[k] = -1;
+      tok_of[k] = row / num_kv_heads;
+      head_of[k] = row - tok_of[k] * num_kv_heads;
+      if (row < nrows) {
+        const uint32_t t = t0 + tok_of[k], h = head_of[k];
+        const uint16_t* src = k_in + (uint64_t(t) * num_kv_heads + h) * D;
+        xa[k] = __ldcs(reinterpret_cast<const uint2*>(src + off_a));
+        xb[k] = __ldcs(reinterpret_cast<const uint2*>(src + off_b));
+        slot[k] = __ldg(slot_mapping + t);
+      }
     }
-    // sin/cos of every (token of this step, frequency)
+    if (pass == blockIdx.x) {
+      // Frequencies theta^(-2i/R) in binary64, split into three binary32
+      // parts; once per CTA, while the first pass's loads are in flight.
+      if (threadIdx.x < half) {
+        const double c = -2.0 * log2(double(theta)) / double(rotary_dim);
+        const double f = exp2(c * double(threadIdx.x));
+        Freq e;
+        e.h = float(f);
+        e.m = float(f - double(e.h));
+        e.l = float(f - double(e.h) - double(e.m));
+        e.pad = 0.0f;
+        e.d = f;
+        freq[threadIdx.x] = e;
+      }
+      __syncthreads();
+    }
+    // 2. sin/cos of every (token of the pass, frequency), by all threads
     for (uint32_t e = threadIdx.x; e < ntok * half; e += kThreads) {
       const uint32_t j = e / half, i = e % half;
-      table[parity][j * half + i] = rope_sincos(__ldg(positions + t_first + j), freq[i]);
+      table[j * half + i] = rope_sincos(__ldg(positions + t0 + j), freq[i], sincos_pio32);
     }
     __syncthreads();
 
-    float x[8];
-    {
-      const uint32_t xw[4] = {xa.x, xa.y, xb.x, xb.y};
-      unpack8(xw, x);
-    }
-    float ss = 0.0f;
+    // 3. normalise, rotate, round once and store every row
 #pragma unroll
-    for (int j = 0; j < 8; ++j) ss = fmaf(x[j], x[j], ss);  // x^2 is exact in binary32
-#pragma unroll
-    for (int o = kLanes / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    const float r = 1.0f / sqrtf(__fadd_rn(ss / float(D), rms_eps));
-
-    float u[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) u[j] = __fmul_rn(x[j], w[j]);  // exact
-    float out[8];
-    if (is_pair && active) {
-      const float4* tb = &table[parity][(t - t_first) * half + 4 * lane];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float4 sc = tb[q];  // {sin_hi, sin_lo, cos_hi, cos_lo}
-        out[q] = rotate(u[q], u[4 + q], sc.z, sc.w, sc.x, sc.y, -1.0f);
-        out[4 + q] = rotate(u[4 + q], u[q], sc.z, sc.w, sc.x, sc.y, 1.0f);
+    for (int k = 0; k < kMaxRowsPerThread; ++k) {
+      const uint32_t row = row_in_sweep + k * kRows;
+      if (k * kRows >= nrows) break;  // uniform across the CTA
+      const bool active = row < nrows;
+      float x[8];
+      {
+        const uint32_t xw[4] = {xa[k].x, xa[k].y, xb[k].x, xb[k].y};
+        unpack8(xw, x);
       }
-    } else {
+      float ss = 0.0f;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) out[j] = u[j];
-    }
-    if (active && slot >= 0) {
-      uint32_t packed[4];
+      for (int j = 0; j < 8; ++j) ss = fmaf(x[j], x[j], ss);  // x^2 is exact in binary32
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
-        packed[j] = f32x2_to_bf16x2(__fmul_rn(out[2 * j], r), __fmul_rn(out[2 * j + 1], r));
-      uint16_t* dst = k_cache + (uint64_t(slot) * num_kv_heads + h) * D;
-      *reinterpret_cast<uint2*>(dst + off_a) = make_uint2(packed[0], packed[1]);
-      *reinterpret_cast<uint2*>(dst + off_b) = make_uint2(packed[2], packed[3]);
+      for (int o = kLanes / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+      // 1/sqrt(mean + eps): a few-ulp binary32 factor, a relative error on the
+      // whole row far below half a BF16 ulp
+      const float r = rsqrtf(__fadd_rn(ss * (1.0f / float(D)), rms_eps));
+      float u[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) u[j] = __fmul_rn(x[j], w[j]);  // exact
+      float out[8];
+      if (is_pair && active) {
+        const float4* tb = &table[tok_of[k] * half + 4 * lane];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float4 sc = tb[q];  // {sin_hi, sin_lo, cos_hi, cos_lo}
+          out[q] = rotate(u[q], u[4 + q], sc.z, sc.w, sc.x, sc.y, -1.0f);
+          out[4 + q] = rotate(u[4 + q], u[q], sc.z, sc.w, sc.x, sc.y, 1.0f);
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) out[j] = u[j];
+      }
+      if (active && slot[k] >= 0) {
+        uint32_t packed[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          packed[j] = f32x2_to_bf16x2(__fmul_rn(out[2 * j], r), __fmul_rn(out[2 * j + 1], r));
+        uint16_t* dst = k_cache + (uint64_t(slot[k]) * num_kv_heads + head_of[k]) * D;
+        *reinterpret_cast<uint2*>(dst + off_a) = make_uint2(packed[0], packed[1]);
+        *reinterpret_cast<uint2*>(dst + off_b) = make_uint2(packed[2], packed[3]);
+      }
     }
+    __syncthreads();  // the next pass rewrites the table
   }
 }
 
@@ -275,25 +306,25 @@ cudaError_t launch_fused_k_norm_rope(const uint16_t* k_in, const uint16_t* k_nor
                                      uint32_t num_kv_heads, uint32_t head_dim, uint32_t rotary_dim,
                                      float rms_eps, float theta, cudaStream_t stream) {
   const DeviceInfo& dev = device_info();
-  const uint32_t rows_per_step = kThreads / (head_dim / 8);
-  const uint64_t steps = (uint64_t(num_tokens) * num_kv_heads + rows_per_step - 1) / rows_per_step;
-  uint64_t blocks = uint64_t(dev.num_sms) * 4;
-  if (steps < blocks) blocks = steps;
+  const uint32_t tok_pass = tokens_per_pass(head_dim, rotary_dim, num_kv_heads);
+  const uint64_t passes = (uint64_t(num_tokens) + tok_pass - 1) / tok_pass;
+  uint64_t blocks = uint64_t(dev.num_sms);  // persistent: the frequency set-up runs once per SM
+  if (passes < blocks) blocks = passes;
   switch (head_dim) {
     case 64:
       fused_k_norm_rope_kernel<64><<<unsigned(blocks), kThreads, 0, stream>>>(
           k_in, k_norm_weight, positions, k_cache, slot_mapping, num_tokens, num_kv_heads,
-          rotary_dim, rms_eps, theta);
+          rotary_dim, rms_eps, theta, tok_pass);
       break;
     case 128:
       fused_k_norm_rope_kernel<128><<<unsigned(blocks), kThreads, 0, stream>>>(
           k_in, k_norm_weight, positions, k_cache, slot_mapping, num_tokens, num_kv_heads,
-          rotary_dim, rms_eps, theta);
+          rotary_dim, rms_eps, theta, tok_pass);
       break;
     case 256:
       fused_k_norm_rope_kernel<256><<<unsigned(blocks), kThreads, 0, stream>>>(
           k_in, k_norm_weight, positions, k_cache, slot_mapping, num_tokens, num_kv_heads,
-          rotary_dim, rms_eps, theta);
+          rotary_dim, rms_eps, theta, tok_pass);
       break;
     default:
       return cudaErrorInvalidValue;
