@@ -111,6 +111,13 @@ def e4m3_encode(x: np.ndarray) -> np.ndarray:
     return out
 
 
+def e4m3_encode_f64(x: np.ndarray) -> np.ndarray:
+    x = _check(np.asarray(x, np.float64), np.float64, "x")
+    out = np.empty(x.shape, np.uint8)
+    lib().oracle_e4m3_encode_f64_array(_ptr(x), _ptr(out), ctypes.c_int64(x.size))
+    return out
+
+
 # --------------------------------------------------------------------------
 # the seven calls
 # --------------------------------------------------------------------------
@@ -170,6 +177,55 @@ def write_fused_k_norm_rope_bf16(k_in, k_norm_weight, positions, k_cache, slot_m
         _ptr(k_in), _ptr(k_norm_weight), _ptr(positions), _ptr(k_cache), _ptr(slot_mapping),
         _u32(num_tokens), _u32(num_kv_heads), _u32(head_dim), _u32(rotary_dim),
         _u32(block_size), _f32(rms_eps), _f32(theta))
+
+
+def write_fused_k_norm_rope_bf16_mrope(k_in, k_norm_weight, pos_t, pos_h, pos_w, k_cache,
+                                       slot_mapping, num_tokens, num_kv_heads, head_dim, rotary_dim,
+                                       block_size, rms_eps, theta) -> None:
+    _check(k_in, np.uint16, "k_in")
+    _check(k_norm_weight, np.uint16, "k_norm_weight")
+    for a, n in ((pos_t, "pos_t"), (pos_h, "pos_h"), (pos_w, "pos_w")):
+        _check(a, np.int32, n)
+    _check(k_cache, np.uint16, "k_cache")
+    _check(slot_mapping, np.int64, "slot_mapping")
+    lib().oracle_write_fused_k_norm_rope_bf16_mrope(
+        _ptr(k_in), _ptr(k_norm_weight), _ptr(pos_t), _ptr(pos_h), _ptr(pos_w), _ptr(k_cache),
+        _ptr(slot_mapping), _u32(num_tokens), _u32(num_kv_heads), _u32(head_dim), _u32(rotary_dim),
+        _u32(block_size), _f32(rms_eps), _f32(theta))
+
+
+def write_fused_k_norm_rope_fp8(k_in, k_norm_weight, positions, k_cache_fp8, slot_mapping, num_tokens,
+                                num_kv_heads, head_dim, rotary_dim, block_size, rms_eps, theta,
+                                inv_scale) -> None:
+    _check(k_in, np.uint16, "k_in")
+    _check(k_norm_weight, np.uint16, "k_norm_weight")
+    _check(positions, np.int32, "positions")
+    _check(k_cache_fp8, np.uint8, "k_cache_fp8")
+    _check(slot_mapping, np.int64, "slot_mapping")
+    lib().oracle_write_fused_k_norm_rope_fp8(
+        _ptr(k_in), _ptr(k_norm_weight), _ptr(positions), _ptr(k_cache_fp8), _ptr(slot_mapping),
+        _u32(num_tokens), _u32(num_kv_heads), _u32(head_dim), _u32(rotary_dim), _u32(block_size),
+        _f32(rms_eps), _f32(theta), _f32(inv_scale))
+
+
+def rope_row_mrope(y: np.ndarray, rotary_dim: int, pos3, theta: float) -> np.ndarray:
+    y = _check(np.asarray(y, np.float64), np.float64, "y")
+    p3 = np.ascontiguousarray(np.asarray(pos3, np.float64))
+    out = np.empty_like(y)
+    lib().oracle_rope_row_mrope(_ptr(y), _u32(y.size), _u32(rotary_dim), _ptr(p3), ctypes.c_double(theta),
+                                _ptr(out))
+    return out
+
+
+def fused_k_row_f64_mrope(k_in, k_norm_weight, pos_t, pos_h, pos_w, t, h, num_kv_heads, head_dim,
+                          rotary_dim, rms_eps, theta) -> np.ndarray:
+    out = np.empty(int(head_dim), np.float64)
+    lib().oracle_fused_k_row_f64_mrope(
+        _ptr(_check(k_in, np.uint16, "k_in")), _ptr(_check(k_norm_weight, np.uint16, "w")),
+        _ptr(_check(pos_t, np.int32, "pos_t")), _ptr(_check(pos_h, np.int32, "pos_h")),
+        _ptr(_check(pos_w, np.int32, "pos_w")), _u32(t), _u32(h), _u32(num_kv_heads), _u32(head_dim),
+        _u32(rotary_dim), _f32(rms_eps), _f32(theta), _ptr(out))
+    return out
 
 
 def rmsnorm_row(x: np.ndarray, w: np.ndarray, eps: float) -> np.ndarray:

@@ -87,11 +87,10 @@ double oracle_e4m3_to_f64(uint8_t code) {
     return s ? -v : v;
 }
 
-/* Encode a binary32 value to E4M3 with round-to-nearest-even and saturation
+/* Encode a binary64 value to E4M3 with round-to-nearest-even and saturation
  * to the largest finite magnitude (448) for |x| >= 448 and for infinities.
  * NaN encodes as the canonical NaN 0x7F. */
-uint8_t oracle_e4m3_encode(float xf) {
-    double x = (double)xf;
+uint8_t oracle_e4m3_encode_f64(double x) {
     uint8_t sign = signbit(x) ? 0x80u : 0u;
     if (isnan(x)) return 0x7Fu;
     double ax = fabs(x);
@@ -111,6 +110,9 @@ uint8_t oracle_e4m3_encode(float xf) {
     int mant = (int)((y / ldexp(1.0, yexp) - 1.0) * 8.0);
     return (uint8_t)(sign | (uint8_t)(((yexp + 7) << 3) | mant));
 }
+
+/* The same rule for a binary32 input (exactly representable in binary64). */
+uint8_t oracle_e4m3_encode(float xf) { return oracle_e4m3_encode_f64((double)xf); }
 
 /* ------------------------------------------------------------------------
  * Slot mapping.  [kv_cache.rs] `fill_slots_from_block_table`: for i < count,
@@ -209,20 +211,33 @@ void oracle_rmsnorm_row(const double *x, const double *w, uint32_t head_dim, dou
     for (uint32_t d = 0; d < head_dim; ++d) y[d] = x[d] * inv_rms * w[d];
 }
 
-/* Rotary embedding of one head row at integer position pos, rotate-half
- * pairing: for i < rotary_dim / 2 the pair (i, i + rotary_dim / 2) turns by
- * the angle pos * theta^(-2i / rotary_dim); dims >= rotary_dim pass through. */
-void oracle_rope_row(const double *y, uint32_t head_dim, uint32_t rotary_dim, double pos,
-                     double theta, double *out) {
+/* Rotary embedding of one head row, rotate-half pairing: for
+ * i < rotary_dim / 2 the pair (i, i + rotary_dim / 2) turns by the angle
+ * p_i * theta^(-2i / rotary_dim); dims >= rotary_dim pass through.
+ * [kv_cache.rs] `fused_k_norm_rope_cache_write_bf16_mrope`: the MRoPE
+ * variant takes one position per rotation pair, chosen from the three
+ * position streams by pair index mod 3, p_i = pos3[i % 3] (pos3[0] = t,
+ * pos3[1] = h, pos3[2] = w). */
+void oracle_rope_row_mrope(const double *y, uint32_t head_dim, uint32_t rotary_dim,
+                           const double *pos3, double theta, double *out) {
     uint32_t half = rotary_dim / 2;
     for (uint32_t d = 0; d < head_dim; ++d) out[d] = y[d];
     for (uint32_t i = 0; i < half; ++i) {
         double inv_freq = pow(theta, -2.0 * (double)i / (double)rotary_dim);
-        double angle = pos * inv_freq;
+        double angle = pos3[i % 3] * inv_freq;
         double c = cos(angle), s = sin(angle);
         out[i] = y[i] * c - y[i + half] * s;
         out[i + half] = y[i + half] * c + y[i] * s;
     }
+}
+
+/* Plain RoPE at one integer position pos: every pair turns by
+ * pos * theta^(-2i / rotary_dim), i.e. the rule above with three equal
+ * positions. */
+void oracle_rope_row(const double *y, uint32_t head_dim, uint32_t rotary_dim, double pos,
+                     double theta, double *out) {
+    const double pos3[3] = {pos, pos, pos};
+    oracle_rope_row_mrope(y, head_dim, rotary_dim, pos3, theta, out);
 }
 
 /* The fused call's result before its single rounding, for one (token, head):
@@ -256,6 +271,66 @@ void oracle_write_fused_k_norm_rope_bf16(const uint16_t *k_in, const uint16_t *k
             for (uint32_t d = 0; d < head_dim; ++d)
                 k_cache[pool_index(slot, block_size, num_kv_heads, head_dim, h, d)] =
                     oracle_f64_to_bf16(out[d]);
+        }
+    }
+}
+
+/* The MRoPE variant's result before its rounding, for one (token, head). */
+void oracle_fused_k_row_f64_mrope(const uint16_t *k_in, const uint16_t *k_norm_weight,
+                                  const int32_t *pos_t, const int32_t *pos_h, const int32_t *pos_w,
+                                  uint32_t t, uint32_t h, uint32_t num_kv_heads, uint32_t head_dim,
+                                  uint32_t rotary_dim, float rms_eps, float theta, double *out) {
+    double x[1024], w[1024], y[1024];
+    double pos3[3] = {(double)pos_t[t], (double)pos_h[t], (double)pos_w[t]};
+    for (uint32_t d = 0; d < head_dim; ++d) {
+        x[d] = oracle_bf16_to_f64(k_in[((int64_t)t * num_kv_heads + h) * head_dim + d]);
+        w[d] = oracle_bf16_to_f64(k_norm_weight[d]);
+    }
+    oracle_rmsnorm_row(x, w, head_dim, (double)rms_eps, y);
+    oracle_rope_row_mrope(y, head_dim, rotary_dim, pos3, (double)theta, out);
+}
+
+void oracle_write_fused_k_norm_rope_bf16_mrope(const uint16_t *k_in, const uint16_t *k_norm_weight,
+                                               const int32_t *pos_t, const int32_t *pos_h,
+                                               const int32_t *pos_w, uint16_t *k_cache,
+                                               const int64_t *slot_mapping, uint32_t num_tokens,
+                                               uint32_t num_kv_heads, uint32_t head_dim,
+                                               uint32_t rotary_dim, uint32_t block_size,
+                                               float rms_eps, float theta) {
+    double out[1024];
+    for (uint32_t t = 0; t < num_tokens; ++t) {
+        int64_t slot = slot_mapping[t];
+        if (slot < 0) continue;
+        for (uint32_t h = 0; h < num_kv_heads; ++h) {
+            oracle_fused_k_row_f64_mrope(k_in, k_norm_weight, pos_t, pos_h, pos_w, t, h, num_kv_heads,
+                                         head_dim, rotary_dim, rms_eps, theta, out);
+            for (uint32_t d = 0; d < head_dim; ++d)
+                k_cache[pool_index(slot, block_size, num_kv_heads, head_dim, h, d)] =
+                    oracle_f64_to_bf16(out[d]);
+        }
+    }
+}
+
+/* [kv_cache.rs] `fused_k_norm_rope_cache_write_fp8`: the FP8-output
+ * sibling of the fused write. Same RMSNorm and RoPE; the result, without
+ * any BF16 rounding, is multiplied by inv_scale and cast to E4M3 with
+ * saturation (round to nearest even). */
+void oracle_write_fused_k_norm_rope_fp8(const uint16_t *k_in, const uint16_t *k_norm_weight,
+                                        const int32_t *positions, uint8_t *k_cache_fp8,
+                                        const int64_t *slot_mapping, uint32_t num_tokens,
+                                        uint32_t num_kv_heads, uint32_t head_dim,
+                                        uint32_t rotary_dim, uint32_t block_size, float rms_eps,
+                                        float theta, float inv_scale) {
+    double out[1024];
+    for (uint32_t t = 0; t < num_tokens; ++t) {
+        int64_t slot = slot_mapping[t];
+        if (slot < 0) continue;
+        for (uint32_t h = 0; h < num_kv_heads; ++h) {
+            oracle_fused_k_row_f64(k_in, k_norm_weight, positions, t, h, num_kv_heads, head_dim,
+                                   rotary_dim, rms_eps, theta, out);
+            for (uint32_t d = 0; d < head_dim; ++d)
+                k_cache_fp8[pool_index(slot, block_size, num_kv_heads, head_dim, h, d)] =
+                    oracle_e4m3_encode_f64(out[d] * (double)inv_scale);
         }
     }
 }
@@ -399,4 +474,7 @@ void oracle_e4m3_to_f64_array(const uint8_t *in, double *out, int64_t n) {
 }
 void oracle_e4m3_encode_array(const float *in, uint8_t *out, int64_t n) {
     for (int64_t i = 0; i < n; ++i) out[i] = oracle_e4m3_encode(in[i]);
+}
+void oracle_e4m3_encode_f64_array(const double *in, uint8_t *out, int64_t n) {
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_e4m3_encode_f64(in[i]);
 }

@@ -34,6 +34,9 @@ MUTANTS = {
                         "return ((block * (int64_t)num_kv_heads + head) * block_size + offset) * (int64_t)head_dim + d;"),
     "value_row_of_key": ("acc[d] += e * oracle_bf16_to_f64(v_cache[",
                          "acc[d] += e * oracle_bf16_to_f64((k_cache_bf16 ? k_cache_bf16 : v_cache)["),
+    "mrope_index": ("double angle = pos3[i % 3] * inv_freq;", "double angle = pos3[(i / 3) % 3] * inv_freq;"),
+    "fp8_fused_no_scale": ("oracle_e4m3_encode_f64(out[d] * (double)inv_scale);",
+                           "oracle_e4m3_encode_f64(out[d]);"),
     "softmax_unnormalised": ("for (uint32_t d = 0; d < head_dim; ++d) out[d] = acc[d] / denom;",
                              "for (uint32_t d = 0; d < head_dim; ++d) out[d] = acc[d];"),
 }

@@ -460,3 +460,79 @@ def test_decode_block_permutation_invariance(oracle_lib):
     bt2 = np.where(bt >= 0, perm[np.clip(bt, 0, None)], bt).astype(np.int32)
     moved = oracle_lib.paged_decode_attn_fp8k(q, kc2, vc2, *args(bt2))
     assert np.array_equal(base, moved)
+
+
+# ---------------------------------------------------------------------------
+# next rows: MRoPE-interleaved fused write and the FP8-output fused write
+# (kv_cache.rs, fused_k_norm_rope_cache_write_bf16_mrope / _fp8)
+# ---------------------------------------------------------------------------
+def test_mrope_with_equal_positions_is_the_scalar_rope(oracle_lib):
+    y = np.random.default_rng(9).standard_normal(128)
+    for pos in (0, 5, 1023, 77777):
+        assert np.array_equal(oracle_lib.rope_row_mrope(y, 128, [pos, pos, pos], 1e6),
+                              oracle_lib.rope_row(y, 128, pos, 1e6))
+
+
+def test_mrope_pair_uses_position_of_its_index_mod_3(oracle_lib):
+    rng = np.random.default_rng(10)
+    y = rng.standard_normal(128)
+    pos3 = (1, 2, 3)                         # small: no angle wraps
+    out = oracle_lib.rope_row_mrope(y, 128, pos3, 1e6)
+    z_in = y[:64] + 1j * y[64:]
+    z_out = out[:64] + 1j * out[64:]
+    np.testing.assert_allclose(np.abs(z_out), np.abs(z_in), rtol=1e-13)
+    ang = np.angle(z_out / z_in)
+    per_pos = ang / np.array([pos3[i % 3] for i in range(64)])   # the frequency ladder alone
+    np.testing.assert_allclose(per_pos[0], 1.0, rtol=1e-12)
+    np.testing.assert_allclose(per_pos[1:] / per_pos[:-1], 1e6 ** (-2 / 128), rtol=1e-9)
+
+
+def test_mrope_fused_row_equals_torch_rmsnorm_then_complex_rotation(oracle_lib):
+    w = kvgen.fused_write(seqs=1, tokens_per_seq=16)
+    H, D = w.num_kv_heads, w.head_dim
+    k_in, wt = _rows(w.key), _rows(w.extra["k_norm_weight"].reshape(1, -1)).ravel()
+    rng = np.random.default_rng(11)
+    pt, ph, pw = (np.ascontiguousarray(rng.integers(0, 5000, 16).astype(np.int32)) for _ in range(3))
+    wt64 = torch.from_numpy(wt.view(np.int16)).view(torch.bfloat16).to(torch.float64)
+    inv_freq = 1e6 ** (-np.arange(0, D, 2) / D)
+    for t in (0, 7, 15):
+        pos = np.array([(pt, ph, pw)[i % 3][t] for i in range(D // 2)], np.float64)
+        for h in (0, H - 1):
+            x = w.key[t].view(H, D)[h].to(torch.float64)
+            y = torch.nn.functional.rms_norm(x, (D,), wt64, eps=float(np.float32(1e-6))).numpy()
+            z = (y[:D // 2] + 1j * y[D // 2:]) * np.exp(1j * pos * inv_freq)
+            ref = np.concatenate([z.real, z.imag])
+            got = oracle_lib.fused_k_row_f64_mrope(k_in, wt, pt, ph, pw, t, h, H, D, D, 1e-6, 1e6)
+            np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-12 * np.abs(ref).max())
+
+
+def test_e4m3_encode_f64_agrees_with_binary32_encode_and_brute_force(oracle_lib):
+    x32 = torch.from_numpy(ALL_BF16.view(np.int16)).view(torch.bfloat16).to(torch.float32).numpy()
+    with np.errstate(invalid="ignore"):       # the NaN patterns
+        assert np.array_equal(oracle_lib.e4m3_encode_f64(x32.astype(np.float64)), oracle_lib.e4m3_encode(x32))
+    rng = np.random.default_rng(12)
+    xs = rng.standard_normal(4000) * 10.0 ** rng.uniform(-4, 3, 4000)
+    got = oracle_lib.e4m3_encode_f64(xs)
+    want = np.array([_e4m3_brute_force(float(v)) for v in xs], np.uint8)
+    assert np.array_equal(got, want)
+
+
+def test_fp8_fused_write_codes_are_nearest_to_scaled_exact_rows(oracle_lib):
+    w = kvgen.fused_write(seqs=1, tokens_per_seq=32)
+    H, D, bs, nb = w.num_kv_heads, w.head_dim, w.block_size, w.num_blocks
+    k_in, wt = _rows(w.key), _rows(w.extra["k_norm_weight"].reshape(1, -1)).ravel()
+    pos = np.ascontiguousarray(w.positions.numpy())
+    slots = oracle_lib.fill_slots(w.block_tables[0].numpy(), 0, 32, bs)
+    inv_scale = np.float32(448.0 / 30.0)
+    kc = np.full((nb, bs, H, D), kvgen.E4M3_NAN, np.uint8)
+    oracle_lib.write_fused_k_norm_rope_fp8(k_in, wt, pos, kc, slots, 32, H, D, D, bs, 1e-6, 1e6, inv_scale)
+    wt64 = torch.from_numpy(wt.view(np.int16)).view(torch.bfloat16).to(torch.float64)
+    inv_freq = 1e6 ** (-np.arange(0, D, 2) / D)
+    for t in (0, 31):
+        for h in (0, 5):
+            x = w.key[t].view(H, D)[h].to(torch.float64)
+            y = torch.nn.functional.rms_norm(x, (D,), wt64, eps=float(np.float32(1e-6))).numpy()
+            z = (y[:D // 2] + 1j * y[D // 2:]) * np.exp(1j * pos[t] * inv_freq)
+            v = np.concatenate([z.real, z.imag]) * float(inv_scale)
+            want = np.array([_e4m3_brute_force(float(a)) for a in v], np.uint8)
+            assert np.array_equal(kc[slots[t] // bs, slots[t] % bs, h], want)
