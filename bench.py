@@ -12,11 +12,14 @@ One step is one pass of every timed call of the five synthetic workloads
   fp8k_decode_w4096  the same with sliding_window 4096
   fp8k_mixed_decode  paged_decode_attn_fp8k, 256 sequences of 128..65536
                      (log-uniform), GQA 64:8, block_size 64, split-KV
+Beside the step, and not in it, the FP8-output and the MRoPE variants of the
+fused K write are timed on the fused_write tokens ("next_rows"), with L2
+flushed before each launch.
 The headline value is the step's algorithmic HBM bytes (what each call must
 read and write, counted per call below) divided by the step time, in GB/s;
 each call's GB/s, tokens/s and fraction of the measured HBM copy rate are
 reported beside it. Inputs are synthetic (kvgen, seeded), resident in HBM
-before the timed region; the step touches ~45 GB, far more than L2, so no
+before the timed region; the step moves ~57 GB, far more than L2, so no
 call finds its inputs in L2 from the previous step.
 
 --impl reference runs the CPU oracle (the reference arm of this benchmark) on
@@ -168,6 +171,10 @@ class GpuStep:
             for f in each:
                 f()
         run.each = each
+        # what the fills move: an int64 slot per token written, an int32
+        # table entry per block read
+        run.bytes = sum(8 * L + 4 * (-(-L // w.block_size)) for L in lens)
+        run.tokens = sum(lens)
         return run, len(each)
 
     def _setup(self):
@@ -175,6 +182,7 @@ class GpuStep:
         t0 = time.time()
         self.ws_bytes = 0  # the workspace must fit every decode of the step
         self.inputs_h2d, self.outputs_d2h = [], []
+        self.extras = []  # calls timed beside the step, not in it
         # Each workload is set up in a method of its own, so every closure
         # binds its own shapes and buffers.
         want = WORKLOAD_OF_PART[self.only_part] if self.only_part else None
@@ -188,7 +196,10 @@ class GpuStep:
         pk.kv_set_decode_workspace(self.ws)
         torch.cuda.synchronize()
         self.setup_s = time.time() - t0
-        self.total_bytes = sum(p["bytes"] for p in self.parts)
+        self.fill_bytes = sum(p["fill_fn"].bytes for p in self.parts if "fill_fn" in p)
+        self.fill_tokens = sum(p["fill_fn"].tokens for p in self.parts if "fill_fn" in p)
+        self.fill_launches = sum(len(p["fills"]) for p in self.parts if "fills" in p)
+        self.total_bytes = sum(p["bytes"] for p in self.parts) + self.fill_bytes
         self.launches = sum(p["launches"] for p in self.parts)
 
     def _setup_fused(self):
@@ -214,10 +225,31 @@ class GpuStep:
             k_write()
             v_write()
         # the K and V writes touch different pools: the graph runs them side by side
-        self.parts.append(dict(name="fused_write", fn=run, fills=fill.each, mains=[k_write, v_write], tokens=n,
+        self.parts.append(dict(name="fused_write", fn=run, fills=fill.each, fill_fn=fill, mains=[k_write, v_write],
+                               tokens=n,
                                launches=nfill + 2,
-                               bytes=n * (2048 + 2048 + 4 + 8 + 2048 + 2048 + 8 + 8), kind="write"))
+                               bytes=n * (2048 + 2048 + 4 + 8 + 2048 + 2048 + 8), kind="write"))
         self.inputs_h2d += [key, value, pos, tables]
+
+        # the two siblings of the fused K write, timed on the same tokens
+        # outside the step: the FP8-output write (E4M3 pool, inv_scale as the
+        # FP8-K decode's 1/k_scale) and the MRoPE write (t/h/w position streams)
+        kc8 = kvgen.poisoned_pool(w.num_blocks, bs, H, D, "fp8", dev)
+        g = torch.Generator().manual_seed(2024)
+        pos_h = torch.randint(0, 1 << 17, (n,), generator=g).to(torch.int32).to(dev)
+        pos_w = torch.randint(0, 512, (n,), generator=g).to(torch.int32).to(dev)
+
+        def k_write_fp8():
+            pk.kv_write_fused_k_norm_rope_fp8(key, wt, pos, kc8, slots, n, H, D, 128, bs, 1e-6, 1e6, 448.0 / 6.0)
+
+        def k_write_mrope():
+            pk.kv_write_fused_k_norm_rope_bf16_mrope(key, wt, pos, pos_h, pos_w, kc, slots, n, H, D, 128, bs,
+                                                     1e-6, 1e6)
+        # per token: K read 2048, K write (1024 as E4M3, 2048 as BF16),
+        # positions (4, or 3 x 4) and the slot (8)
+        self.extras += [dict(name="fused_k_write_fp8", fn=k_write_fp8, tokens=n, bytes=n * (2048 + 1024 + 4 + 8)),
+                        dict(name="fused_k_write_mrope", fn=k_write_mrope, tokens=n,
+                             bytes=n * (2048 + 2048 + 12 + 8))]
 
     def _setup_bf16_gqa4(self):
         torch, kvgen, pk, dev = self.torch, self.kvgen, self.pk, self.dev
@@ -241,7 +273,8 @@ class GpuStep:
         def decode():
             pk.paged_decode_attn_bf16(q, kc, vc, out, tables, lens, w.max_blocks_per_seq, w.num_seqs, Hq, H, D, bs,
                                       w.inv_sqrt_d, Hq * D, 0)
-        self.parts.append(dict(name="bf16_prefill", fn=prefill, fills=fill.each, main=prefill_main, tokens=n,
+        self.parts.append(dict(name="bf16_prefill", fn=prefill, fills=fill.each, fill_fn=fill, main=prefill_main,
+                               tokens=n,
                                launches=nfill + 1,
                                bytes=n * write_bytes_per_token(H * D, 2), kind="write"))
         self.parts.append(dict(name="bf16_decode", fn=decode, tokens=w.num_seqs,
@@ -283,7 +316,8 @@ class GpuStep:
                                           bs, w.inv_sqrt_d, k_scale, Hq * D, win)
             return decode
         self.fp8_chunks, self.fp8_write_chunk, self.fp8_row = chunks, write_chunk, H * D
-        self.parts.append(dict(name="fp8k_prefill", fn=prefill, fills=fill.each, main=prefill_main, tokens=n,
+        self.parts.append(dict(name="fp8k_prefill", fn=prefill, fills=fill.each, fill_fn=fill, main=prefill_main,
+                               tokens=n,
                                launches=nfill + len(chunks),
                                bytes=n * write_bytes_per_token(H * D, 1), kind="write"))
         outs = []
@@ -374,14 +408,62 @@ class GpuStep:
     def replay(self):
         self.graph.replay()
 
-    def run_step(self, events=None):
-        torch = self.torch
-        for i, p in enumerate(self.parts):
-            if events is not None:
-                events[i][0].record()
+    def run_step(self):
+        for p in self.parts:
             p["fn"]()
-            if events is not None:
-                events[i][1].record()
+
+    def time_calls(self, reps: int) -> dict:
+        """Eager launches with CUDA events: each part's writes or decode, and
+        the per-sequence slot fills of all parts together ("slot_fill")."""
+        torch = self.torch
+        ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+        rec = []
+        for _ in range(reps):
+            for p in self.parts:
+                if "fill_fn" in p:
+                    a, b, c = ev(), ev(), ev()
+                    a.record()
+                    p["fill_fn"]()
+                    b.record()
+                    for f in (p.get("mains") or [p["main"]]):
+                        f()
+                    c.record()
+                    rec.append(("slot_fill", a, b))
+                    rec.append((p["name"], b, c))
+                else:
+                    a, b = ev(), ev()
+                    a.record()
+                    p["fn"]()
+                    b.record()
+                    rec.append((p["name"], a, b))
+        torch.cuda.synchronize()
+        out = {}
+        for name, a, b in rec:
+            out[name] = out.get(name, 0.0) + a.elapsed_time(b) / reps
+        return out
+
+
+    def time_extras(self, reps: int) -> dict:
+        """Eager launches of the calls outside the step, CUDA events around
+        each; a call's first run is untimed. Their inputs fit in L2, so a
+        256 MiB buffer is rewritten before every timed launch (outside the
+        events) to flush it."""
+        torch = self.torch
+        scrub = torch.empty(256 << 20, dtype=torch.uint8, device=self.dev)
+        out = {}
+        for x in self.extras:
+            x["fn"]()
+            evs = []
+            for i in range(reps):
+                scrub.fill_(i & 0xFF)
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                x["fn"]()
+                b.record()
+                evs.append((a, b))
+            torch.cuda.synchronize()
+            out[x["name"]] = sum(a.elapsed_time(b) for a, b in evs) / reps
+        return out
 
 
 class Ranks:
@@ -467,36 +549,41 @@ def run_gpu(args):
         t_end.record(stream)
         barrier()
     assert pk.kv_get_device_error() == 0, "kernel fault bits set during the timed steps"
-    # per-call times: the same calls launched eagerly, CUDA events around each part
-    nparts = len(step.parts)
-    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nparts)]
-          for _ in range(args.steps)]
-    for k in range(args.steps):
-        step.run_step(ev[k])
-    torch.cuda.synchronize()
+    # per-call times: the same calls launched eagerly, CUDA events around each
     clocks = clk.summary()
     elapsed_ms = t_start.elapsed_time(t_end)
     ms_per_step = elapsed_ms / args.steps
-    part_ms = [statistics.mean(ev[k][i][0].elapsed_time(ev[k][i][1]) for k in range(args.steps))
-               for i in range(nparts)]
+    call_ms = step.time_calls(args.steps)
     ms_per_step = ranks.max(ms_per_step)  # the job is as slow as its slowest rank
 
     peak, peak_kind = measured_peak()
     value = step.total_bytes * world / (ms_per_step * 1e-3) / 1e9
 
     # per-launch timing of the dominant kernel
-    dominant = max(range(nparts), key=lambda i: part_ms[i])
-    dom = step.parts[dominant]
+    dom = max(step.parts, key=lambda p: call_ms[p["name"]])
     roofline = dominant_roofline(step, dom, stream, peak, peak_kind, args)
 
+    entries = [(p["name"], p["bytes"], p["tokens"], p["launches"] - len(p.get("fills", ())))
+               for p in step.parts]
+    entries.insert(0, ("slot_fill", step.fill_bytes, step.fill_tokens, step.fill_launches))
     parts = {}
-    for p, ms in zip(step.parts, part_ms):
-        gbs = p["bytes"] / (ms * 1e-3) / 1e9
-        parts[p["name"]] = {"ms": round(ms, 4), "GB_per_s": round(gbs, 1),
-                            "tokens_per_s": round(p["tokens"] / (ms * 1e-3), 1),
-                            "frac_measured_hbm": round(gbs / peak, 4),
-                            "frac_nominal_8TBs": round(gbs / NOMINAL_HBM_GBS, 4),
-                            "algorithmic_bytes": int(p["bytes"]), "launches": p["launches"]}
+    for name, nbytes, tokens, launches in entries:
+        ms = call_ms[name]
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        parts[name] = {"ms": round(ms, 4), "GB_per_s": round(gbs, 1),
+                       "tokens_per_s": round(tokens / (ms * 1e-3), 1),
+                       "frac_measured_hbm": round(gbs / peak, 4),
+                       "frac_nominal_8TBs": round(gbs / NOMINAL_HBM_GBS, 4),
+                       "algorithmic_bytes": int(nbytes), "launches": launches}
+
+    extra_ms = step.time_extras(args.steps)
+    next_rows = {}
+    for x in step.extras:
+        ms = extra_ms[x["name"]]
+        gbs = x["bytes"] / (ms * 1e-3) / 1e9
+        next_rows[x["name"]] = {"ms": round(ms, 4), "GB_per_s": round(gbs, 1),
+                                "tokens_per_s": round(x["tokens"] / (ms * 1e-3), 1),
+                                "frac_measured_hbm": round(gbs / peak, 4), "algorithmic_bytes": int(x["bytes"])}
 
     e2e = run_e2e(step, args, dev, world)
     cpu = cpu_baseline(args) if (rank == 0 and world == 1 and not args.no_cpu_baseline) else None
@@ -510,13 +597,16 @@ def run_gpu(args):
             "config": {"workload": "one pass of every timed call of the five paged-KV workloads "
                                    "(fused_write, bf16_gqa4 prefill+decode, fp8k_long prefill+decode W=0/4096, "
                                    "fp8k_mixed decode)",
-                       "l2": "inputs larger than L2 (the step moves ~45 GB; no call's inputs stay in L2)",
+                       "l2": f"inputs larger than L2 (the step moves {step.total_bytes / 1e9:.0f} GB; "
+                             "no call's inputs stay in L2)",
                        "algorithmic_bytes_per_step": int(step.total_bytes),
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "step_mode": "one CUDA-graph replay per step (the per-sequence slot fills run as 8 parallel graph "
                          "branches, the fused K and V-only writes side by side); per-call 'parts' timed "
-                         "from eager launches with CUDA events",
+                         "from eager launches with CUDA events, the 196 per-sequence kv_fill_slots launches "
+                         "together as slot_fill",
             "parts": parts,
+            "next_rows": next_rows,
             "roofline": roofline,
             "cpu_baseline": cpu,
             "e2e": e2e,

@@ -138,6 +138,38 @@ PAGEDKV_API int kv_write_fused_k_norm_rope_bf16(const kv_bf16_t *k_in, const kv_
                                     uint32_t block_size, float rms_eps, float theta, void *stream);
 
 /* ------------------------------------------------------------------------
+ * MRoPE-interleaved fused K path. [kv_cache.rs]
+ * `fused_k_norm_rope_cache_write_bf16_mrope`: as
+ * kv_write_fused_k_norm_rope_bf16, but rotation pair i of token t turns by
+ * pos * theta^(-2i/rotary_dim) with pos = (pos_t, pos_h, pos_w)[i % 3][t].
+ * With pos_t == pos_h == pos_w the result is bit-identical to
+ * kv_write_fused_k_norm_rope_bf16.
+ *   pos_t, pos_h, pos_w  device int32[num_tokens] each.
+ * ---------------------------------------------------------------------- */
+PAGEDKV_API int kv_write_fused_k_norm_rope_bf16_mrope(
+    const kv_bf16_t *k_in, const kv_bf16_t *k_norm_weight, const int32_t *pos_t, const int32_t *pos_h,
+    const int32_t *pos_w, kv_bf16_t *k_cache, const int64_t *slot_mapping, uint32_t num_tokens,
+    uint32_t num_kv_heads, uint32_t head_dim, uint32_t rotary_dim, uint32_t block_size, float rms_eps,
+    float theta, void *stream);
+
+/* ------------------------------------------------------------------------
+ * FP8-output fused K path. [kv_cache.rs] `fused_k_norm_rope_cache_write_fp8`:
+ * the same RMSNorm and RoPE with no BF16 rounding; the result times
+ * inv_scale (finite, > 0; inv_scale = 1 / k_scale of the FP8-K decode) is
+ * cast once to E4M3, round to nearest even, saturating to +-448. The code
+ * equals the correctly rounded one except where the exact scaled value lies
+ * within ~2^-19 (relative) of the midpoint between two codes; there either
+ * neighbour may be stored.
+ *   k_cache_fp8  device uint8 pool [num_blocks, block_size, num_kv_heads, head_dim].
+ * ---------------------------------------------------------------------- */
+PAGEDKV_API int kv_write_fused_k_norm_rope_fp8(const kv_bf16_t *k_in, const kv_bf16_t *k_norm_weight,
+                                               const int32_t *positions, kv_e4m3_t *k_cache_fp8,
+                                               const int64_t *slot_mapping, uint32_t num_tokens,
+                                               uint32_t num_kv_heads, uint32_t head_dim, uint32_t rotary_dim,
+                                               uint32_t block_size, float rms_eps, float theta, float inv_scale,
+                                               void *stream);
+
+/* ------------------------------------------------------------------------
  * V-only write.  [kv_cache.rs] `reshape_and_cache_flash_v_only`: the V half
  * of kv_write_bf16, so that the fused K kernel stays the only writer of K.
  * ---------------------------------------------------------------------- */

@@ -20,7 +20,8 @@ import torch
 
 __all__ = [
     "PagedKVError", "library_path", "kv_fill_slots", "kv_write_bf16", "kv_write_fp8k",
-    "kv_write_fused_k_norm_rope_bf16", "kv_write_v_only", "paged_decode_attn_bf16",
+    "kv_write_fused_k_norm_rope_bf16", "kv_write_fused_k_norm_rope_bf16_mrope",
+    "kv_write_fused_k_norm_rope_fp8", "kv_write_v_only", "paged_decode_attn_bf16",
     "paged_decode_attn_fp8k", "paged_decode_attn_fp8k_static_scratch", "kv_decode_workspace_bytes",
     "kv_set_decode_workspace", "kv_get_device_error", "kv_device_info", "KV_OK", "KV_ERR_INVALID_ARG",
     "KV_ERR_UNSUPPORTED", "KV_ERR_CUDA", "KV_ERR_DEVICE",
@@ -41,6 +42,10 @@ _SIGNATURES = {
     "kv_write_fp8k": (ctypes.c_int, [_P, _P, _P, _P, _P, _U32, _U32, _U32, _U32, _U32, _U32, _F32, _P]),
     "kv_write_fused_k_norm_rope_bf16": (
         ctypes.c_int, [_P, _P, _P, _P, _P, _U32, _U32, _U32, _U32, _U32, _F32, _F32, _P]),
+    "kv_write_fused_k_norm_rope_bf16_mrope": (
+        ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _U32, _U32, _U32, _U32, _U32, _F32, _F32, _P]),
+    "kv_write_fused_k_norm_rope_fp8": (
+        ctypes.c_int, [_P, _P, _P, _P, _P, _U32, _U32, _U32, _U32, _U32, _F32, _F32, _F32, _P]),
     "kv_write_v_only": (ctypes.c_int, [_P, _P, _P, _U32, _U32, _U32, _U32, _U32, _P]),
     "paged_decode_attn_bf16": (
         ctypes.c_int, [_P, _P, _P, _P, _P, _P, _U32, _U32, _U32, _U32, _U32, _U32, _F32, _U32, _U32, _P]),
@@ -134,6 +139,23 @@ def kv_write_fused_k_norm_rope_bf16(k_in, k_norm_weight, positions, k_cache, slo
     _check("kv_write_fused_k_norm_rope_bf16", lib().kv_write_fused_k_norm_rope_bf16(
         _ptr(k_in), _ptr(k_norm_weight), _ptr(positions), _ptr(k_cache), _ptr(slot_mapping),
         num_tokens, num_kv_heads, head_dim, rotary_dim, block_size, rms_eps, theta, _stream(stream)))
+
+
+def kv_write_fused_k_norm_rope_bf16_mrope(k_in, k_norm_weight, pos_t, pos_h, pos_w, k_cache, slot_mapping,
+                                          num_tokens, num_kv_heads, head_dim, rotary_dim, block_size, rms_eps,
+                                          theta, stream=None):
+    _check("kv_write_fused_k_norm_rope_bf16_mrope", lib().kv_write_fused_k_norm_rope_bf16_mrope(
+        _ptr(k_in), _ptr(k_norm_weight), _ptr(pos_t), _ptr(pos_h), _ptr(pos_w), _ptr(k_cache),
+        _ptr(slot_mapping), num_tokens, num_kv_heads, head_dim, rotary_dim, block_size, rms_eps, theta,
+        _stream(stream)))
+
+
+def kv_write_fused_k_norm_rope_fp8(k_in, k_norm_weight, positions, k_cache_fp8, slot_mapping, num_tokens,
+                                   num_kv_heads, head_dim, rotary_dim, block_size, rms_eps, theta, inv_scale,
+                                   stream=None):
+    _check("kv_write_fused_k_norm_rope_fp8", lib().kv_write_fused_k_norm_rope_fp8(
+        _ptr(k_in), _ptr(k_norm_weight), _ptr(positions), _ptr(k_cache_fp8), _ptr(slot_mapping), num_tokens,
+        num_kv_heads, head_dim, rotary_dim, block_size, rms_eps, theta, inv_scale, _stream(stream)))
 
 
 def kv_write_v_only(value, v_cache, slot_mapping, num_tokens, num_kv_heads, head_dim, block_size,

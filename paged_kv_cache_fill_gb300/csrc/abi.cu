@@ -125,23 +125,54 @@ int kv_write_fp8k(const kv_bf16_t* key, const kv_bf16_t* value, kv_e4m3_t* k_cac
                                      key_stride, value_stride, k_scale, as_stream(stream)));
 }
 
+static int fused_common(const kv_bf16_t* k_in, const kv_bf16_t* k_norm_weight, const int32_t* positions,
+                        const int32_t* pos_h, const int32_t* pos_w, bool mrope, void* k_cache, bool fp8_out,
+                        float inv_scale, const int64_t* slot_mapping, uint32_t num_tokens, uint32_t num_kv_heads,
+                        uint32_t head_dim, uint32_t rotary_dim, uint32_t block_size, float rms_eps, float theta,
+                        void* stream) {
+  if (num_tokens == 0) return KV_OK;
+  if (!k_in || !k_norm_weight || !positions || !k_cache || !slot_mapping) return KV_ERR_INVALID_ARG;
+  if (mrope && (!pos_h || !pos_w)) return KV_ERR_INVALID_ARG;
+  if (num_kv_heads == 0 || head_dim == 0 || block_size == 0) return KV_ERR_INVALID_ARG;
+  if (rotary_dim == 0 || rotary_dim % 2 || rotary_dim > head_dim) return KV_ERR_INVALID_ARG;
+  if (!(rms_eps >= 0.0f) || !isfinite(rms_eps) || !(theta > 0.0f) || !isfinite(theta))
+    return KV_ERR_INVALID_ARG;
+  if (fp8_out && (!(inv_scale > 0.0f) || !isfinite(inv_scale))) return KV_ERR_INVALID_ARG;
+  if (head_dim != 64 && head_dim != 128 && head_dim != 256) return KV_ERR_UNSUPPORTED;
+  if (rotary_dim % 8) return KV_ERR_UNSUPPORTED;
+  if (!aligned(k_in, 16) || !aligned(k_norm_weight, 16) || !aligned(k_cache, 16)) return KV_ERR_UNSUPPORTED;
+  return from_cuda(launch_fused_k_norm_rope(k_in, k_norm_weight, positions, mrope ? pos_h : nullptr,
+                                            mrope ? pos_w : nullptr, k_cache, fp8_out, inv_scale, slot_mapping,
+                                            num_tokens, num_kv_heads, head_dim, rotary_dim, rms_eps, theta,
+                                            as_stream(stream)));
+}
+
 int kv_write_fused_k_norm_rope_bf16(const kv_bf16_t* k_in, const kv_bf16_t* k_norm_weight,
                                     const int32_t* positions, kv_bf16_t* k_cache,
                                     const int64_t* slot_mapping, uint32_t num_tokens,
                                     uint32_t num_kv_heads, uint32_t head_dim, uint32_t rotary_dim,
                                     uint32_t block_size, float rms_eps, float theta, void* stream) {
-  if (num_tokens == 0) return KV_OK;
-  if (!k_in || !k_norm_weight || !positions || !k_cache || !slot_mapping) return KV_ERR_INVALID_ARG;
-  if (num_kv_heads == 0 || head_dim == 0 || block_size == 0) return KV_ERR_INVALID_ARG;
-  if (rotary_dim == 0 || rotary_dim % 2 || rotary_dim > head_dim) return KV_ERR_INVALID_ARG;
-  if (!(rms_eps >= 0.0f) || !isfinite(rms_eps) || !(theta > 0.0f) || !isfinite(theta))
-    return KV_ERR_INVALID_ARG;
-  if (head_dim != 64 && head_dim != 128 && head_dim != 256) return KV_ERR_UNSUPPORTED;
-  if (rotary_dim % 8) return KV_ERR_UNSUPPORTED;
-  if (!aligned(k_in, 16) || !aligned(k_norm_weight, 16) || !aligned(k_cache, 16)) return KV_ERR_UNSUPPORTED;
-  return from_cuda(launch_fused_k_norm_rope(k_in, k_norm_weight, positions, k_cache, slot_mapping, num_tokens,
-                                            num_kv_heads, head_dim, rotary_dim, rms_eps, theta,
-                                            as_stream(stream)));
+  return fused_common(k_in, k_norm_weight, positions, nullptr, nullptr, false, k_cache, false, 1.0f, slot_mapping,
+                      num_tokens, num_kv_heads, head_dim, rotary_dim, block_size, rms_eps, theta, stream);
+}
+
+int kv_write_fused_k_norm_rope_bf16_mrope(const kv_bf16_t* k_in, const kv_bf16_t* k_norm_weight,
+                                          const int32_t* pos_t, const int32_t* pos_h, const int32_t* pos_w,
+                                          kv_bf16_t* k_cache, const int64_t* slot_mapping, uint32_t num_tokens,
+                                          uint32_t num_kv_heads, uint32_t head_dim, uint32_t rotary_dim,
+                                          uint32_t block_size, float rms_eps, float theta, void* stream) {
+  return fused_common(k_in, k_norm_weight, pos_t, pos_h, pos_w, true, k_cache, false, 1.0f, slot_mapping,
+                      num_tokens, num_kv_heads, head_dim, rotary_dim, block_size, rms_eps, theta, stream);
+}
+
+int kv_write_fused_k_norm_rope_fp8(const kv_bf16_t* k_in, const kv_bf16_t* k_norm_weight,
+                                   const int32_t* positions, kv_e4m3_t* k_cache_fp8,
+                                   const int64_t* slot_mapping, uint32_t num_tokens, uint32_t num_kv_heads,
+                                   uint32_t head_dim, uint32_t rotary_dim, uint32_t block_size, float rms_eps,
+                                   float theta, float inv_scale, void* stream) {
+  return fused_common(k_in, k_norm_weight, positions, nullptr, nullptr, false, k_cache_fp8, true, inv_scale,
+                      slot_mapping, num_tokens, num_kv_heads, head_dim, rotary_dim, block_size, rms_eps, theta,
+                      stream);
 }
 
 static int decode_common(const kv_bf16_t* q, const void* k_cache, const kv_bf16_t* v_cache, float* output,

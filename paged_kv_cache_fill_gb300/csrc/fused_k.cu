@@ -169,12 +169,15 @@ __host__ __device__ inline uint32_t tokens_per_pass(uint32_t head_dim, uint32_t 
   return t < 1 ? 1 : t;
 }
 
-template <int D>
+// kFp8Out: store E4M3(o * inv_scale) (saturating, RNE) instead of BF16(o).
+// kMrope: pair i takes its position from positions / pos_h / pos_w by i % 3.
+template <int D, bool kFp8Out, bool kMrope>
 __global__ void __launch_bounds__(kThreads, 1) fused_k_norm_rope_kernel(
     const uint16_t* __restrict__ k_in, const uint16_t* __restrict__ k_norm_weight,
-    const int32_t* __restrict__ positions, uint16_t* __restrict__ k_cache,
+    const int32_t* __restrict__ positions, const int32_t* __restrict__ pos_h,
+    const int32_t* __restrict__ pos_w, void* __restrict__ k_cache,
     const int64_t* __restrict__ slot_mapping, uint32_t num_tokens, uint32_t num_kv_heads,
-    uint32_t rotary_dim, float rms_eps, float theta, uint32_t tok_pass) {
+    uint32_t rotary_dim, float rms_eps, float theta, float inv_scale, uint32_t tok_pass) {
   constexpr int kLanes = D / 8;              // lanes per row
   constexpr int kRows = kThreads / kLanes;   // rows per sweep of the CTA
   __shared__ Freq freq[128];
@@ -245,7 +248,9 @@ __global__ void __launch_bounds__(kThreads, 1) fused_k_norm_rope_kernel(
     // 2. sin/cos of every (token of the pass, frequency), by all threads
     for (uint32_t e = threadIdx.x; e < ntok * half; e += kThreads) {
       const uint32_t j = e / half, i = e % half;
-      table[j * half + i] = rope_sincos(__ldg(positions + t0 + j), freq[i], sincos_pio32);
+      const int32_t* pos_src = positions;
+      if (kMrope) pos_src = (i % 3 == 0) ? positions : (i % 3 == 1 ? pos_h : pos_w);
+      table[j * half + i] = rope_sincos(__ldg(pos_src + t0 + j), freq[i], sincos_pio32);
     }
     __syncthreads();
 
@@ -285,13 +290,27 @@ __global__ void __launch_bounds__(kThreads, 1) fused_k_norm_rope_kernel(
         for (int j = 0; j < 8; ++j) out[j] = u[j];
       }
       if (active && slot[k] >= 0) {
-        uint32_t packed[4];
+        if constexpr (kFp8Out) {
+          // no BF16 rounding: the binary32 result times inv_scale, cast once
+          const float rs = __fmul_rn(r, inv_scale);
+          uint32_t codes[2];
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-          packed[j] = f32x2_to_bf16x2(__fmul_rn(out[2 * j], r), __fmul_rn(out[2 * j + 1], r));
-        uint16_t* dst = k_cache + (uint64_t(slot[k]) * num_kv_heads + head_of[k]) * D;
-        *reinterpret_cast<uint2*>(dst + off_a) = make_uint2(packed[0], packed[1]);
-        *reinterpret_cast<uint2*>(dst + off_b) = make_uint2(packed[2], packed[3]);
+          for (int j = 0; j < 2; ++j)
+            codes[j] = uint32_t(f32x2_to_e4m3x2_satfinite(__fmul_rn(out[4 * j], rs), __fmul_rn(out[4 * j + 1], rs))) |
+                       (uint32_t(f32x2_to_e4m3x2_satfinite(__fmul_rn(out[4 * j + 2], rs),
+                                                           __fmul_rn(out[4 * j + 3], rs))) << 16);
+          uint8_t* dst = static_cast<uint8_t*>(k_cache) + (uint64_t(slot[k]) * num_kv_heads + head_of[k]) * D;
+          *reinterpret_cast<uint32_t*>(dst + off_a) = codes[0];
+          *reinterpret_cast<uint32_t*>(dst + off_b) = codes[1];
+        } else {
+          uint32_t packed[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            packed[j] = f32x2_to_bf16x2(__fmul_rn(out[2 * j], r), __fmul_rn(out[2 * j + 1], r));
+          uint16_t* dst = static_cast<uint16_t*>(k_cache) + (uint64_t(slot[k]) * num_kv_heads + head_of[k]) * D;
+          *reinterpret_cast<uint2*>(dst + off_a) = make_uint2(packed[0], packed[1]);
+          *reinterpret_cast<uint2*>(dst + off_b) = make_uint2(packed[2], packed[3]);
+        }
       }
     }
     __syncthreads();  // the next pass rewrites the table
@@ -300,8 +319,25 @@ __global__ void __launch_bounds__(kThreads, 1) fused_k_norm_rope_kernel(
 
 }  // namespace
 
+template <int D>
+static void launch_d(bool fp8_out, bool mrope, unsigned blocks, cudaStream_t stream, const uint16_t* k_in,
+                     const uint16_t* w, const int32_t* pos, const int32_t* pos_h, const int32_t* pos_w, void* cache,
+                     const int64_t* slots, uint32_t n, uint32_t H, uint32_t R, float eps, float theta, float inv_scale,
+                     uint32_t tok_pass) {
+  if (fp8_out)
+    fused_k_norm_rope_kernel<D, true, false><<<blocks, kThreads, 0, stream>>>(
+        k_in, w, pos, pos_h, pos_w, cache, slots, n, H, R, eps, theta, inv_scale, tok_pass);
+  else if (mrope)
+    fused_k_norm_rope_kernel<D, false, true><<<blocks, kThreads, 0, stream>>>(
+        k_in, w, pos, pos_h, pos_w, cache, slots, n, H, R, eps, theta, inv_scale, tok_pass);
+  else
+    fused_k_norm_rope_kernel<D, false, false><<<blocks, kThreads, 0, stream>>>(
+        k_in, w, pos, pos_h, pos_w, cache, slots, n, H, R, eps, theta, inv_scale, tok_pass);
+}
+
 cudaError_t launch_fused_k_norm_rope(const uint16_t* k_in, const uint16_t* k_norm_weight,
-                                     const int32_t* positions, uint16_t* k_cache,
+                                     const int32_t* positions, const int32_t* pos_h, const int32_t* pos_w,
+                                     void* k_cache, bool fp8_out, float inv_scale,
                                      const int64_t* slot_mapping, uint32_t num_tokens,
                                      uint32_t num_kv_heads, uint32_t head_dim, uint32_t rotary_dim,
                                      float rms_eps, float theta, cudaStream_t stream) {
@@ -310,21 +346,19 @@ cudaError_t launch_fused_k_norm_rope(const uint16_t* k_in, const uint16_t* k_nor
   const uint64_t passes = (uint64_t(num_tokens) + tok_pass - 1) / tok_pass;
   uint64_t blocks = uint64_t(dev.num_sms);  // persistent: the frequency set-up runs once per SM
   if (passes < blocks) blocks = passes;
+  const bool mrope = pos_h != nullptr;
   switch (head_dim) {
     case 64:
-      fused_k_norm_rope_kernel<64><<<unsigned(blocks), kThreads, 0, stream>>>(
-          k_in, k_norm_weight, positions, k_cache, slot_mapping, num_tokens, num_kv_heads,
-          rotary_dim, rms_eps, theta, tok_pass);
+      launch_d<64>(fp8_out, mrope, unsigned(blocks), stream, k_in, k_norm_weight, positions, pos_h, pos_w, k_cache,
+                   slot_mapping, num_tokens, num_kv_heads, rotary_dim, rms_eps, theta, inv_scale, tok_pass);
       break;
     case 128:
-      fused_k_norm_rope_kernel<128><<<unsigned(blocks), kThreads, 0, stream>>>(
-          k_in, k_norm_weight, positions, k_cache, slot_mapping, num_tokens, num_kv_heads,
-          rotary_dim, rms_eps, theta, tok_pass);
+      launch_d<128>(fp8_out, mrope, unsigned(blocks), stream, k_in, k_norm_weight, positions, pos_h, pos_w, k_cache,
+                    slot_mapping, num_tokens, num_kv_heads, rotary_dim, rms_eps, theta, inv_scale, tok_pass);
       break;
     case 256:
-      fused_k_norm_rope_kernel<256><<<unsigned(blocks), kThreads, 0, stream>>>(
-          k_in, k_norm_weight, positions, k_cache, slot_mapping, num_tokens, num_kv_heads,
-          rotary_dim, rms_eps, theta, tok_pass);
+      launch_d<256>(fp8_out, mrope, unsigned(blocks), stream, k_in, k_norm_weight, positions, pos_h, pos_w, k_cache,
+                    slot_mapping, num_tokens, num_kv_heads, rotary_dim, rms_eps, theta, inv_scale, tok_pass);
       break;
     default:
       return cudaErrorInvalidValue;

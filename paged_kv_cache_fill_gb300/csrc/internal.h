@@ -33,8 +33,12 @@ cudaError_t launch_write_fp8k(const uint16_t* key, const uint16_t* value, uint8_
                               uint32_t row_elems, uint32_t key_stride, uint32_t value_stride,
                               float k_scale, cudaStream_t stream);
 
+// Fused RMSNorm/RoPE K write. pos_h/pos_w non-null selects the MRoPE
+// variant (position of pair i from positions/pos_h/pos_w by i % 3); fp8_out
+// stores E4M3(o * inv_scale) into a uint8 pool instead of BF16(o).
 cudaError_t launch_fused_k_norm_rope(const uint16_t* k_in, const uint16_t* k_norm_weight,
-                                     const int32_t* positions, uint16_t* k_cache,
+                                     const int32_t* positions, const int32_t* pos_h, const int32_t* pos_w,
+                                     void* k_cache, bool fp8_out, float inv_scale,
                                      const int64_t* slot_mapping, uint32_t num_tokens,
                                      uint32_t num_kv_heads, uint32_t head_dim, uint32_t rotary_dim,
                                      float rms_eps, float theta, cudaStream_t stream);

@@ -218,6 +218,111 @@ def test_fused_write_large_positions_and_padding():
     assert worst <= 1
 
 
+def _norm_weight(D):
+    return (torch.rand(D, generator=torch.Generator().manual_seed(D)) + 0.5).to(torch.bfloat16)
+
+
+def _mrope_check(w, rotary_dim, theta, eps, pos3):
+    H, D, bs, nb, n = w.num_kv_heads, w.head_dim, w.block_size, w.num_blocks, w.num_tokens
+    wt = _norm_weight(D)
+    slots_ref = oracle_slots(w)
+    slots = torch.from_numpy(slots_ref).to(DEV)
+    kc = kvgen.poisoned_pool(nb, bs, H, D, "bf16", DEV)
+    pt, ph, pw = (p.to(DEV) for p in pos3)
+    pk.kv_write_fused_k_norm_rope_bf16_mrope(w.key.to(DEV), wt.to(DEV), pt, ph, pw, kc, slots, n, H, D,
+                                             rotary_dim, bs, eps, theta)
+    kr = np.full((nb, bs, H, D), kvgen.BF16_NAN, np.uint16)
+    oracle.write_fused_k_norm_rope_bf16_mrope(u16(w.key), u16(wt), *(np.ascontiguousarray(p.numpy()) for p in pos3),
+                                              kr, slots_ref, n, H, D, rotary_dim, bs, eps, theta)
+    got = u16(kc)
+    return int(np.abs(ordered(got) - ordered(kr)).max()), got
+
+
+@pytest.mark.parametrize("D,R,theta", [(128, 128, 1e6), (128, 64, 1e4), (64, 48, 1e4), (256, 256, 5e5)])
+def test_mrope_write_within_one_ulp(D, R, theta):
+    w = kvgen.custom(90 + D + R, seq_lens=[300, 41, 1], num_q_heads=8, num_kv_heads=4, head_dim=D,
+                     block_size=16, key_sigma=4.0)
+    g = torch.Generator().manual_seed(R)
+    n = w.num_tokens
+    # text-like runs (t = h = w) next to image-like tokens with spread h/w and
+    # a few positions past 2^16
+    pt = torch.randint(0, 4096, (n,), generator=g).to(torch.int32)
+    ph = torch.where(torch.arange(n) % 3 == 0, pt, torch.randint(0, 1 << 17, (n,), generator=g).to(torch.int32))
+    pw = torch.randint(0, 512, (n,), generator=g).to(torch.int32)
+    worst, _ = _mrope_check(w, R, theta, 1e-6, (pt, ph, pw))
+    assert worst <= 1
+
+
+def test_mrope_with_equal_positions_is_bit_identical_to_plain_fused_write():
+    w = kvgen.custom(4242, seq_lens=[500, 12], num_q_heads=8, num_kv_heads=8, head_dim=128, block_size=16,
+                     key_sigma=6.0)
+    H, D, bs, nb, n = w.num_kv_heads, w.head_dim, w.block_size, w.num_blocks, w.num_tokens
+    pos = torch.randint(0, 1 << 20, (n,), generator=torch.Generator().manual_seed(5)).to(torch.int32)
+    _, got = _mrope_check(w, 128, 1e6, 1e-6, (pos, pos, pos))
+    wt = _norm_weight(D).to(DEV)
+    kc = kvgen.poisoned_pool(nb, bs, H, D, "bf16", DEV)
+    pk.kv_write_fused_k_norm_rope_bf16(w.key.to(DEV), wt, pos.to(DEV), kc, torch.from_numpy(oracle_slots(w)).to(DEV),
+                                       n, H, D, 128, bs, 1e-6, 1e6)
+    assert np.array_equal(got, u16(kc))
+
+
+def _fp8_fused_check(w, rotary_dim, theta, eps, inv_scale, slots_ref=None):
+    """Codes must equal the oracle's, except where the exact scaled value lies
+    within a relative 2^-19 of the midpoint between the two codes (the kernel
+    works in binary32 and its reciprocal square root is not correctly
+    rounded); there the other neighbour is accepted. Returns the number of
+    such accepted differences."""
+    H, D, bs, nb, n = w.num_kv_heads, w.head_dim, w.block_size, w.num_blocks, w.num_tokens
+    wt = _norm_weight(D)
+    if slots_ref is None:
+        slots_ref = oracle_slots(w)
+    kc = kvgen.poisoned_pool(nb, bs, H, D, "fp8", DEV)
+    pk.kv_write_fused_k_norm_rope_fp8(w.key.to(DEV), wt.to(DEV), w.positions.to(DEV), kc,
+                                      torch.from_numpy(slots_ref).to(DEV), n, H, D, rotary_dim, bs, eps, theta,
+                                      inv_scale)
+    kr = np.full((nb, bs, H, D), kvgen.E4M3_NAN, np.uint8)
+    k16, w16, pos = u16(w.key), u16(wt), np.ascontiguousarray(w.positions.numpy())
+    oracle.write_fused_k_norm_rope_fp8(k16, w16, pos, kr, slots_ref, n, H, D, rotary_dim, bs, eps, theta,
+                                       inv_scale)
+    got = kc.cpu().numpy()
+    bad = np.argwhere(got != kr)
+    if len(bad) == 0:
+        return 0
+    token_of_slot = {int(s): t for t, s in enumerate(slots_ref) if s >= 0}
+    exact_rows = {}
+    for blk, off, h, d in bad:
+        t = token_of_slot.get(int(blk) * bs + int(off))
+        assert t is not None, "a slot no token maps to was written"
+        if (t, h) not in exact_rows:
+            exact_rows[(t, h)] = oracle.fused_k_row_f64(k16, w16, pos, t, h, H, D, rotary_dim, eps, theta)
+        v = exact_rows[(t, h)][d] * np.float64(np.float32(inv_scale))
+        a, b = oracle.e4m3_to_f64(np.array([got[blk, off, h, d], kr[blk, off, h, d]], np.uint8))
+        mid = 0.5 * (a + b)
+        assert abs(int(got[blk, off, h, d] & 0x7F) - int(kr[blk, off, h, d] & 0x7F)) == 1, (v, a, b)
+        assert abs(v - mid) <= abs(mid) * 2.0 ** -19, (v, a, b)
+    return len(bad)
+
+
+def test_fp8_fused_write_full_workload():
+    w = kvgen.fused_write()
+    # the FP8-K decode's scale rule: the largest |K| after norm and rotation
+    # maps near the top of the E4M3 range
+    ties = _fp8_fused_check(w, 128, 1e6, 1e-6, inv_scale=448.0 / 6.0)
+    print(f"fused FP8 write: {ties} codes at a rounding midpoint")
+    assert ties <= w.num_tokens * w.num_kv_heads * w.head_dim * 1e-4
+
+
+@pytest.mark.parametrize("D,R,inv_scale", [(64, 64, 30.0), (128, 32, 100.0), (256, 256, 1.0), (128, 128, 1e4)])
+def test_fp8_fused_write_shapes_scales_and_saturation(D, R, inv_scale):
+    # inv_scale 1e4 drives most codes into saturation (+-448); 1.0 leaves many
+    # in the subnormal range
+    w = kvgen.custom(60 + D + R, seq_lens=[65, 3], num_q_heads=4, num_kv_heads=2, head_dim=D, block_size=16,
+                     key_sigma=3.0)
+    slots_ref = oracle_slots(w)
+    slots_ref[5::9] = -1
+    _fp8_fused_check(w, R, 1e4, 1e-5, inv_scale, slots_ref=slots_ref)
+
+
 # ---------------------------------------------------------------------------
 # paged decode
 # ---------------------------------------------------------------------------
