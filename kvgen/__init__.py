@@ -56,6 +56,7 @@ class Workload:
     token_seq: torch.Tensor | None  # int32 [num_tokens], sequence of each prefill token
     inv_sqrt_d: float = 0.0
     k_scale: float = 1.0
+    v_scale: float = 1.0
     sliding_windows: tuple = (0,)
     extra: dict = field(default_factory=dict)
 
@@ -252,7 +253,8 @@ def custom(seed: int, device="cpu", *, seq_lens, num_q_heads, num_kv_heads, head
            num_blocks=None, max_blocks_per_seq=None, key_sigma=1.0, fp8=False, q_rows=None) -> Workload:
     """A small workload of any shape, for edge-case tests: given lengths, a
     permuted pool with spare blocks, N(0, key_sigma) K (or fp8k_keys when
-    fp8), N(0, 1) V and Q."""
+    fp8), N(0, 1) V and Q. v_scale is max|V| / 448 (float32), the scale an
+    E4M3 V cache of these rows would use."""
     g = _gen(seed, device)
     seq_lens = torch.as_tensor(seq_lens, dtype=torch.int32).to(device)
     need = [-(-int(L) // block_size) for L in seq_lens.tolist()]
@@ -272,7 +274,16 @@ def custom(seed: int, device="cpu", *, seq_lens, num_q_heads, num_kv_heads, head
     token_seq, positions = _prefill_token_index(seq_lens)
     return Workload("custom", len(seq_lens), num_q_heads, num_kv_heads, head_dim, block_size, nb,
                     mbps, seq_lens, tables, key, value, q, positions, token_seq,
-                    inv_sqrt_d=1.0 / math.sqrt(head_dim), k_scale=k_scale)
+                    inv_sqrt_d=1.0 / math.sqrt(head_dim), k_scale=k_scale, v_scale=amax_scale(value))
+
+
+def amax_scale(x: torch.Tensor) -> float:
+    """Per-tensor E4M3 scale max|x| / 448, in float32 (1.0 for an empty or
+    all-zero tensor)."""
+    if x.numel() == 0:
+        return 1.0
+    amax = float(x.abs().max().float().item())
+    return float(torch.tensor(amax / 448.0, dtype=torch.float32).item()) if amax > 0 else 1.0
 
 
 def poisoned_pool(num_blocks: int, block_size: int, num_kv_heads: int, head_dim: int,

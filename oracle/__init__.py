@@ -1,7 +1,7 @@
 """CPU oracle for the paged KV-cache path (test infrastructure only).
 
-A plain, slow, single-threaded C restatement (``oracle.c``) of the seven
-library calls, loaded with ctypes. Only the tests, ``__graft_entry__.smoke()``
+A plain, slow, single-threaded C restatement (``oracle.c``) of the library's
+calls, loaded with ctypes. Only the tests, ``__graft_entry__.smoke()``
 and the benchmark's CPU-baseline leg may import this package; the product
 path (``paged_kv_cache_fill_gb300``) never does, and the two share no code.
 
@@ -163,6 +163,19 @@ def write_fp8k(key, value, k_cache_fp8, v_cache, slot_mapping, num_tokens, num_k
                             _u32(value_stride), _f32(k_scale))
 
 
+def write_fp8(key, value, k_cache_fp8, v_cache_fp8, slot_mapping, num_tokens, num_kv_heads, head_dim,
+              block_size, k_scale, v_scale, key_stride, value_stride) -> None:
+    _check(key, np.uint16, "key")
+    _check(value, np.uint16, "value")
+    _check(k_cache_fp8, np.uint8, "k_cache_fp8")
+    _check(v_cache_fp8, np.uint8, "v_cache_fp8")
+    _check(slot_mapping, np.int64, "slot_mapping")
+    lib().oracle_write_fp8(_ptr(key), _ptr(value), _ptr(k_cache_fp8), _ptr(v_cache_fp8),
+                           _ptr(slot_mapping), _u32(num_tokens), _u32(num_kv_heads),
+                           _u32(head_dim), _u32(block_size), _f32(k_scale), _f32(v_scale),
+                           _u32(key_stride), _u32(value_stride))
+
+
 def write_fused_k_norm_rope_bf16(k_in, k_norm_weight, positions, k_cache, slot_mapping,
                                  num_tokens, num_kv_heads, head_dim, rotary_dim, block_size,
                                  rms_eps, theta) -> None:
@@ -257,11 +270,16 @@ def fused_k_row_f64(k_in, k_norm_weight, positions, t, h, num_kv_heads, head_dim
 
 def decode_one(q, k_cache_bf16, k_cache_fp8, v_cache, block_tables, seq_lens, max_blocks_per_seq,
                num_q_heads, num_kv_heads, head_dim, block_size, inv_sqrt_d, k_scale, q_stride,
-               sliding_window, s, h, want_weights=False):
+               sliding_window, s, h, want_weights=False, v_cache_fp8=None, v_scale=1.0):
     """Output (float64[head_dim]) and optionally the softmax weights by position
-    for one (sequence, query head)."""
+    for one (sequence, query head). v_cache_fp8 (with v_scale) in place of
+    v_cache selects an E4M3 V cache."""
     _check(q, np.uint16, "q")
-    _check(v_cache, np.uint16, "v_cache")
+    if v_cache_fp8 is None:
+        _check(v_cache, np.uint16, "v_cache")
+    else:
+        _check(v_cache_fp8, np.uint8, "v_cache_fp8")
+        v_cache = None
     _check(block_tables, np.int32, "block_tables")
     _check(seq_lens, np.int32, "seq_lens")
     if head_dim > 1024:
@@ -269,10 +287,11 @@ def decode_one(q, k_cache_bf16, k_cache_fp8, v_cache, block_tables, seq_lens, ma
     out = np.empty(int(head_dim), np.float64)
     weights = np.empty(max(int(seq_lens[s]), 1), np.float64) if want_weights else None
     lib().oracle_decode_one(
-        _ptr(q), _ptr(k_cache_bf16), _ptr(k_cache_fp8), _ptr(v_cache), _ptr(block_tables),
-        _ptr(seq_lens), _u32(max_blocks_per_seq), _u32(num_q_heads), _u32(num_kv_heads),
-        _u32(head_dim), _u32(block_size), _f32(inv_sqrt_d), _f32(k_scale), _u32(q_stride),
-        _u32(sliding_window), _u32(s), _u32(h), _ptr(out), _ptr(weights))
+        _ptr(q), _ptr(k_cache_bf16), _ptr(k_cache_fp8), _ptr(v_cache), _ptr(v_cache_fp8),
+        _ptr(block_tables), _ptr(seq_lens), _u32(max_blocks_per_seq), _u32(num_q_heads),
+        _u32(num_kv_heads), _u32(head_dim), _u32(block_size), _f32(inv_sqrt_d), _f32(k_scale),
+        _f32(v_scale), _u32(q_stride), _u32(sliding_window), _u32(s), _u32(h), _ptr(out),
+        _ptr(weights))
     if want_weights:
         return out, weights[: int(seq_lens[s])]
     return out
@@ -307,4 +326,21 @@ def paged_decode_attn_fp8k(q, k_cache_fp8, v_cache, block_tables, seq_lens, max_
         _u32(max_blocks_per_seq), _u32(num_seqs), _u32(num_q_heads), _u32(num_kv_heads),
         _u32(head_dim), _u32(block_size), _f32(inv_sqrt_d), _f32(k_scale), _u32(q_stride),
         _u32(sliding_window))
+    return out
+
+
+def paged_decode_attn_fp8(q, k_cache_fp8, v_cache_fp8, block_tables, seq_lens, max_blocks_per_seq,
+                          num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, inv_sqrt_d,
+                          k_scale, v_scale, q_stride, sliding_window) -> np.ndarray:
+    _check(q, np.uint16, "q")
+    _check(k_cache_fp8, np.uint8, "k_cache_fp8")
+    _check(v_cache_fp8, np.uint8, "v_cache_fp8")
+    _check(block_tables, np.int32, "block_tables")
+    _check(seq_lens, np.int32, "seq_lens")
+    out = np.empty((int(num_seqs), int(num_q_heads), int(head_dim)), np.float32)
+    lib().oracle_paged_decode_attn_fp8(
+        _ptr(q), _ptr(k_cache_fp8), _ptr(v_cache_fp8), _ptr(out), _ptr(block_tables), _ptr(seq_lens),
+        _u32(max_blocks_per_seq), _u32(num_seqs), _u32(num_q_heads), _u32(num_kv_heads),
+        _u32(head_dim), _u32(block_size), _f32(inv_sqrt_d), _f32(k_scale), _f32(v_scale),
+        _u32(q_stride), _u32(sliding_window))
     return out

@@ -169,6 +169,27 @@ void oracle_write_bf16(const uint16_t *key, const uint16_t *value, uint16_t *k_c
                         block_size, value_stride);
 }
 
+/* Quantised paged write of one tensor: element x of token t, head h is stored
+ * as the E4M3 code of the binary32 quotient (float)x / scale, rounded to
+ * nearest. */
+static void write_rows_e4m3(const uint16_t *src, uint32_t src_stride, uint8_t *cache,
+                            const int64_t *slot_mapping, uint32_t num_tokens,
+                            uint32_t num_kv_heads, uint32_t head_dim, uint32_t block_size,
+                            float scale) {
+    for (uint32_t t = 0; t < num_tokens; ++t) {
+        int64_t slot = slot_mapping[t];
+        if (slot < 0) continue;
+        for (uint32_t h = 0; h < num_kv_heads; ++h)
+            for (uint32_t d = 0; d < head_dim; ++d) {
+                float x = (float)oracle_bf16_to_f64(
+                    src[(int64_t)t * src_stride + (int64_t)h * head_dim + d]);
+                float quotient = x / scale; /* binary32 division, round to nearest */
+                cache[pool_index(slot, block_size, num_kv_heads, head_dim, h, d)] =
+                    oracle_e4m3_encode(quotient);
+            }
+    }
+}
+
 /* ------------------------------------------------------------------------
  * [kv_cache_fp8k.rs] module invariants: the write stores k / k_scale as
  * E4M3 in the [num_blocks, block_size, num_kv_heads, head_dim] layout; the
@@ -179,20 +200,26 @@ void oracle_write_fp8k(const uint16_t *key, const uint16_t *value, uint8_t *k_ca
                        uint16_t *v_cache, const int64_t *slot_mapping, uint32_t num_tokens,
                        uint32_t num_kv_heads, uint32_t head_dim, uint32_t block_size,
                        uint32_t key_stride, uint32_t value_stride, float k_scale) {
-    for (uint32_t t = 0; t < num_tokens; ++t) {
-        int64_t slot = slot_mapping[t];
-        if (slot < 0) continue;
-        for (uint32_t h = 0; h < num_kv_heads; ++h)
-            for (uint32_t d = 0; d < head_dim; ++d) {
-                float k = (float)oracle_bf16_to_f64(
-                    key[(int64_t)t * key_stride + (int64_t)h * head_dim + d]);
-                float quotient = k / k_scale; /* binary32 division, round to nearest */
-                k_cache_fp8[pool_index(slot, block_size, num_kv_heads, head_dim, h, d)] =
-                    oracle_e4m3_encode(quotient);
-            }
-    }
+    write_rows_e4m3(key, key_stride, k_cache_fp8, slot_mapping, num_tokens, num_kv_heads,
+                    head_dim, block_size, k_scale);
     oracle_write_v_only(value, v_cache, slot_mapping, num_tokens, num_kv_heads, head_dim,
                         block_size, value_stride);
+}
+
+/* ------------------------------------------------------------------------
+ * [kv_cache.rs] `reshape_and_cache_fp8`: K and V both stored as E4M3, K as
+ * k / k_scale and V as v / v_scale, each with the rule above, into two
+ * pools of the same layout. Argument order as the launcher's (k_scale,
+ * v_scale before the strides); its cache_stride is implied by the layout.
+ * ---------------------------------------------------------------------- */
+void oracle_write_fp8(const uint16_t *key, const uint16_t *value, uint8_t *k_cache_fp8,
+                      uint8_t *v_cache_fp8, const int64_t *slot_mapping, uint32_t num_tokens,
+                      uint32_t num_kv_heads, uint32_t head_dim, uint32_t block_size,
+                      float k_scale, float v_scale, uint32_t key_stride, uint32_t value_stride) {
+    write_rows_e4m3(key, key_stride, k_cache_fp8, slot_mapping, num_tokens, num_kv_heads,
+                    head_dim, block_size, k_scale);
+    write_rows_e4m3(value, value_stride, v_cache_fp8, slot_mapping, num_tokens, num_kv_heads,
+                    head_dim, block_size, v_scale);
 }
 
 /* ------------------------------------------------------------------------
@@ -360,17 +387,27 @@ static double key_at(const uint16_t *k_cache_bf16, const uint8_t *k_cache_fp8, i
     return oracle_bf16_to_f64(k_cache_bf16[idx]);
 }
 
-/* k_cache_fp8 != NULL selects the FP8-K cache (k_cache_bf16 is then unused).
+/* Value element d of position p's row: BF16 widened exactly, or, for the
+ * FP8 K+V cache ([kv_cache.rs] `paged_decode_attn_fp8`, which takes
+ * v_scale), the E4M3 code's value times v_scale. */
+static double value_at(const uint16_t *v_cache_bf16, const uint8_t *v_cache_fp8, int64_t idx,
+                       float v_scale) {
+    if (v_cache_fp8) return oracle_e4m3_to_f64(v_cache_fp8[idx]) * (double)v_scale;
+    return oracle_bf16_to_f64(v_cache_bf16[idx]);
+}
+
+/* k_cache_fp8 != NULL selects the FP8-K cache (k_cache_bf16 is then unused);
+ * v_cache_fp8 != NULL likewise selects an FP8 V cache (v_cache unused).
  * out receives head_dim values. weights, when not NULL, has room for
  * seq_lens[s] values and receives the softmax weight of each position
  * (0 for positions outside the window). head_dim is at most 1024. */
 void oracle_decode_one(const uint16_t *q, const uint16_t *k_cache_bf16, const uint8_t *k_cache_fp8,
-                       const uint16_t *v_cache, const int32_t *block_tables,
-                       const int32_t *seq_lens, uint32_t max_blocks_per_seq,
-                       uint32_t num_q_heads, uint32_t num_kv_heads, uint32_t head_dim,
-                       uint32_t block_size, float inv_sqrt_d, float k_scale, uint32_t q_stride,
-                       uint32_t sliding_window, uint32_t s, uint32_t h, double *out,
-                       double *weights) {
+                       const uint16_t *v_cache, const uint8_t *v_cache_fp8,
+                       const int32_t *block_tables, const int32_t *seq_lens,
+                       uint32_t max_blocks_per_seq, uint32_t num_q_heads, uint32_t num_kv_heads,
+                       uint32_t head_dim, uint32_t block_size, float inv_sqrt_d, float k_scale,
+                       float v_scale, uint32_t q_stride, uint32_t sliding_window, uint32_t s,
+                       uint32_t h, double *out, double *weights) {
     uint32_t group = num_q_heads / num_kv_heads;
     uint32_t kv_head = h / group;
     int64_t L = seq_lens[s];
@@ -410,8 +447,10 @@ void oracle_decode_one(const uint16_t *q, const uint16_t *k_cache_bf16, const ui
         scores[p - start] = e;
         denom += e;
         for (uint32_t d = 0; d < head_dim; ++d)
-            acc[d] += e * oracle_bf16_to_f64(v_cache[pool_index(slots[p - start], block_size,
-                                                                num_kv_heads, head_dim, kv_head, d)]);
+            acc[d] += e * value_at(v_cache, v_cache_fp8,
+                                   pool_index(slots[p - start], block_size, num_kv_heads,
+                                              head_dim, kv_head, d),
+                                   v_scale);
     }
     for (uint32_t d = 0; d < head_dim; ++d) out[d] = acc[d] / denom;
     for (int64_t p = start; weights && p < L; ++p) weights[p] = scores[p - start] / denom;
@@ -420,17 +459,19 @@ void oracle_decode_one(const uint16_t *q, const uint16_t *k_cache_bf16, const ui
 }
 
 static void decode_all(const uint16_t *q, const uint16_t *k_cache_bf16, const uint8_t *k_cache_fp8,
-                       const uint16_t *v_cache, float *output, const int32_t *block_tables,
-                       const int32_t *seq_lens, uint32_t max_blocks_per_seq, uint32_t num_seqs,
-                       uint32_t num_q_heads, uint32_t num_kv_heads, uint32_t head_dim,
-                       uint32_t block_size, float inv_sqrt_d, float k_scale, uint32_t q_stride,
+                       const uint16_t *v_cache, const uint8_t *v_cache_fp8, float *output,
+                       const int32_t *block_tables, const int32_t *seq_lens,
+                       uint32_t max_blocks_per_seq, uint32_t num_seqs, uint32_t num_q_heads,
+                       uint32_t num_kv_heads, uint32_t head_dim, uint32_t block_size,
+                       float inv_sqrt_d, float k_scale, float v_scale, uint32_t q_stride,
                        uint32_t sliding_window) {
     double out[1024];
     for (uint32_t s = 0; s < num_seqs; ++s)
         for (uint32_t h = 0; h < num_q_heads; ++h) {
-            oracle_decode_one(q, k_cache_bf16, k_cache_fp8, v_cache, block_tables, seq_lens,
-                              max_blocks_per_seq, num_q_heads, num_kv_heads, head_dim, block_size,
-                              inv_sqrt_d, k_scale, q_stride, sliding_window, s, h, out, 0);
+            oracle_decode_one(q, k_cache_bf16, k_cache_fp8, v_cache, v_cache_fp8, block_tables,
+                              seq_lens, max_blocks_per_seq, num_q_heads, num_kv_heads, head_dim,
+                              block_size, inv_sqrt_d, k_scale, v_scale, q_stride, sliding_window,
+                              s, h, out, 0);
             for (uint32_t d = 0; d < head_dim; ++d)
                 output[((int64_t)s * num_q_heads + h) * head_dim + d] = (float)out[d];
         }
@@ -443,8 +484,8 @@ void oracle_paged_decode_attn_bf16(const uint16_t *q, const uint16_t *k_cache,
                                    uint32_t num_q_heads, uint32_t num_kv_heads, uint32_t head_dim,
                                    uint32_t block_size, float inv_sqrt_d, uint32_t q_stride,
                                    uint32_t sliding_window) {
-    decode_all(q, k_cache, 0, v_cache, output, block_tables, seq_lens, max_blocks_per_seq,
-               num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, inv_sqrt_d, 1.0f,
+    decode_all(q, k_cache, 0, v_cache, 0, output, block_tables, seq_lens, max_blocks_per_seq,
+               num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, inv_sqrt_d, 1.0f, 1.0f,
                q_stride, sliding_window);
 }
 
@@ -455,9 +496,23 @@ void oracle_paged_decode_attn_fp8k(const uint16_t *q, const uint8_t *k_cache_fp8
                                    uint32_t num_q_heads, uint32_t num_kv_heads, uint32_t head_dim,
                                    uint32_t block_size, float inv_sqrt_d, float k_scale,
                                    uint32_t q_stride, uint32_t sliding_window) {
-    decode_all(q, 0, k_cache_fp8, v_cache, output, block_tables, seq_lens, max_blocks_per_seq,
-               num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, inv_sqrt_d, k_scale,
+    decode_all(q, 0, k_cache_fp8, v_cache, 0, output, block_tables, seq_lens, max_blocks_per_seq,
+               num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, inv_sqrt_d, k_scale, 1.0f,
                q_stride, sliding_window);
+}
+
+/* [kv_cache.rs] `paged_decode_attn_fp8`: K and V both E4M3, dequantised by
+ * k_scale and v_scale. */
+void oracle_paged_decode_attn_fp8(const uint16_t *q, const uint8_t *k_cache_fp8,
+                                  const uint8_t *v_cache_fp8, float *output,
+                                  const int32_t *block_tables, const int32_t *seq_lens,
+                                  uint32_t max_blocks_per_seq, uint32_t num_seqs,
+                                  uint32_t num_q_heads, uint32_t num_kv_heads, uint32_t head_dim,
+                                  uint32_t block_size, float inv_sqrt_d, float k_scale,
+                                  float v_scale, uint32_t q_stride, uint32_t sliding_window) {
+    decode_all(q, 0, k_cache_fp8, 0, v_cache_fp8, output, block_tables, seq_lens,
+               max_blocks_per_seq, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+               inv_sqrt_d, k_scale, v_scale, q_stride, sliding_window);
 }
 
 /* ------------------------------------------------------------------------

@@ -32,8 +32,12 @@ MUTANTS = {
                  "slots[i] = physical_block * (int64_t)block_size + (int64_t)(i % block_size);"),
     "pool_head_major": ("return ((block * (int64_t)block_size + offset) * num_kv_heads + head) * (int64_t)head_dim + d;",
                         "return ((block * (int64_t)num_kv_heads + head) * block_size + offset) * (int64_t)head_dim + d;"),
-    "value_row_of_key": ("acc[d] += e * oracle_bf16_to_f64(v_cache[",
-                         "acc[d] += e * oracle_bf16_to_f64((k_cache_bf16 ? k_cache_bf16 : v_cache)["),
+    "value_row_of_key": ("acc[d] += e * value_at(v_cache, v_cache_fp8,",
+                         "acc[d] += e * value_at(k_cache_bf16 ? k_cache_bf16 : v_cache, v_cache_fp8,"),
+    "v_scale_dropped": ("return oracle_e4m3_to_f64(v_cache_fp8[idx]) * (double)v_scale;",
+                        "return oracle_e4m3_to_f64(v_cache_fp8[idx]);"),
+    "fp8_v_written_with_k_scale": ("head_dim, block_size, v_scale);", "head_dim, block_size, k_scale);"),
+    "fp8_v_rows_at_key_stride": ("write_rows_e4m3(value, value_stride,", "write_rows_e4m3(value, key_stride,"),
     "mrope_index": ("double angle = pos3[i % 3] * inv_freq;", "double angle = pos3[(i / 3) % 3] * inv_freq;"),
     "fp8_fused_no_scale": ("oracle_e4m3_encode_f64(out[d] * (double)inv_scale);",
                            "oracle_e4m3_encode_f64(out[d]);"),

@@ -362,7 +362,7 @@ def _oracle_cache(oracle_lib, w, fp8=False):
     return kc, vc
 
 
-def _dense_reference(w, kc, vc, s, window, fp8=False):
+def _dense_reference(w, kc, vc, s, window, fp8=False, fp8_v=False):
     """Gather the sequence's rows by fancy indexing on the pool viewed as
     [num_blocks, block_size, H, D], then torch's own scaled-dot-product
     attention in float64 with the window as a boolean mask."""
@@ -374,7 +374,10 @@ def _dense_reference(w, kc, vc, s, window, fp8=False):
         k = torch.from_numpy(kc[blocks, p % bs]).view(torch.float8_e4m3fn).to(torch.float64) * w.k_scale
     else:
         k = torch.from_numpy(kc[blocks, p % bs].view(np.int16)).view(torch.bfloat16).to(torch.float64)
-    v = torch.from_numpy(vc[blocks, p % bs].view(np.int16)).view(torch.bfloat16).to(torch.float64)
+    if fp8_v:
+        v = torch.from_numpy(vc[blocks, p % bs]).view(torch.float8_e4m3fn).to(torch.float64) * w.v_scale
+    else:
+        v = torch.from_numpy(vc[blocks, p % bs].view(np.int16)).view(torch.bfloat16).to(torch.float64)
     q = w.q[s].view(Hq, D).to(torch.float64)
     g = Hq // H
     k = k.permute(1, 0, 2).repeat_interleave(g, 0)          # [Hq, L, D]
@@ -460,6 +463,101 @@ def test_decode_block_permutation_invariance(oracle_lib):
     bt2 = np.where(bt >= 0, perm[np.clip(bt, 0, None)], bt).astype(np.int32)
     moved = oracle_lib.paged_decode_attn_fp8k(q, kc2, vc2, *args(bt2))
     assert np.array_equal(base, moved)
+
+
+# ---------------------------------------------------------------------------
+# FP8 K and V (kv_cache.rs, reshape_and_cache_fp8 / paged_decode_attn_fp8)
+# ---------------------------------------------------------------------------
+def _oracle_cache_fp8(oracle_lib, w):
+    nb, bs, H, D = w.num_blocks, w.block_size, w.num_kv_heads, w.head_dim
+    slots = np.concatenate([oracle_lib.fill_slots(w.block_tables[s].numpy(), 0, int(L), bs)
+                            for s, L in enumerate(w.seq_lens.tolist())] or [np.zeros(0, np.int64)])
+    kc = np.full((nb, bs, H, D), kvgen.E4M3_NAN, np.uint8)
+    vc = np.full((nb, bs, H, D), kvgen.E4M3_NAN, np.uint8)
+    oracle_lib.write_fp8(_rows(w.key), _rows(w.value), kc, vc, slots, len(slots), H, D, bs, w.k_scale,
+                         w.v_scale, H * D, H * D)
+    return kc, vc
+
+
+def test_write_fp8_codes_are_rounded_quotients_of_k_and_v(oracle_lib):
+    H, D, bs, nb = 2, 32, 16, 7
+    n = 40
+    ks, vs = H * D + 16, H * D + 48          # rows padded differently, as in fused QKV buffers
+    g = torch.Generator().manual_seed(12)
+    key = (torch.randn(n, ks, generator=g) * 3).to(torch.bfloat16)
+    value = (torch.randn(n, vs, generator=g) * 0.7).to(torch.bfloat16)
+    k_scale, v_scale = np.float32(0.021), np.float32(0.0037)
+    slots = np.random.default_rng(3).permutation(nb * bs)[:n].astype(np.int64)
+    slots[[4, 19]] = -1
+    kc = np.full((nb, bs, H, D), kvgen.E4M3_NAN, np.uint8)
+    vc = np.full((nb, bs, H, D), kvgen.E4M3_NAN, np.uint8)
+    oracle_lib.write_fp8(_rows(key), _rows(value), kc, vc, slots, n, H, D, bs, k_scale, v_scale, ks, vs)
+    flat_k, flat_v = kc.reshape(nb * bs, H * D), vc.reshape(nb * bs, H * D)
+    for src, scale, flat in ((key, k_scale, flat_k), (value, v_scale, flat_v)):
+        quot = src[:, :H * D].to(torch.float32).numpy() / scale    # numpy's own binary32 division
+        assert quot.dtype == np.float32
+        for t in range(n):
+            if slots[t] >= 0:
+                want = [_e4m3_brute_force(float(x)) for x in quot[t]]
+                assert np.array_equal(flat[slots[t]], np.array(want, np.uint8)), t
+        untouched = np.ones(nb * bs, bool)
+        untouched[slots[slots >= 0]] = False
+        assert (flat[untouched] == kvgen.E4M3_NAN).all()
+
+
+@pytest.mark.parametrize("window", [0, 1, 50])
+def test_fp8_decode_equals_dense_attention(oracle_lib, window):
+    w = kvgen.custom(25, seq_lens=[37, 100, 1, 16, 17], num_q_heads=8, num_kv_heads=2, head_dim=64,
+                     block_size=16, fp8=True)
+    kc, vc = _oracle_cache_fp8(oracle_lib, w)
+    q = _rows(w.q)
+    out = oracle_lib.paged_decode_attn_fp8(q, kc, vc, w.block_tables.numpy(), w.seq_lens.numpy(),
+                                           w.max_blocks_per_seq, w.num_seqs, w.num_q_heads, w.num_kv_heads,
+                                           w.head_dim, w.block_size, w.inv_sqrt_d, w.k_scale, w.v_scale,
+                                           w.num_q_heads * w.head_dim, window)
+    for s in range(w.num_seqs):
+        ref = _dense_reference(w, kc, vc, s, window, fp8=True, fp8_v=True)
+        np.testing.assert_allclose(out[s], ref, rtol=2.0 ** -24, atol=1e-30)
+        one = oracle_lib.decode_one(q, None, kc, None, w.block_tables.numpy(), w.seq_lens.numpy(),
+                                    w.max_blocks_per_seq, w.num_q_heads, w.num_kv_heads, w.head_dim,
+                                    w.block_size, w.inv_sqrt_d, w.k_scale, w.num_q_heads * w.head_dim,
+                                    window, s, 3, v_cache_fp8=vc, v_scale=w.v_scale)
+        np.testing.assert_allclose(one, ref[3], rtol=1e-12, atol=1e-12)
+
+
+def test_fp8_decode_single_position_and_v_scale_linearity(oracle_lib):
+    w = kvgen.custom(26, seq_lens=[1, 90], num_q_heads=4, num_kv_heads=2, head_dim=32, block_size=16,
+                     fp8=True)
+    kc, vc = _oracle_cache_fp8(oracle_lib, w)
+    q = _rows(w.q)
+    args = lambda vs: (w.block_tables.numpy(), w.seq_lens.numpy(), w.max_blocks_per_seq, w.num_seqs,  # noqa: E731
+                       w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size, w.inv_sqrt_d, w.k_scale, vs,
+                       w.num_q_heads * w.head_dim, 0)
+    out = oracle_lib.paged_decode_attn_fp8(q, kc, vc, *args(w.v_scale))
+    # one position: every query head of a KV head returns that row's codes times v_scale
+    b0 = w.block_tables[0, 0].item()
+    for h in range(w.num_q_heads):
+        row = oracle_lib.e4m3_to_f64(np.ascontiguousarray(vc[b0, 0, h // 2])) * np.float64(np.float32(w.v_scale))
+        assert np.array_equal(out[0, h], row.astype(np.float32))
+    # the output is linear in v_scale: doubling it doubles every value exactly
+    out2 = oracle_lib.paged_decode_attn_fp8(q, kc, vc, *args(2 * w.v_scale))
+    assert np.array_equal(out2, 2 * out)
+
+
+def test_fp8_v_decode_equals_bf16_v_decode_of_the_dequantised_rows(oracle_lib):
+    # with v_scale a power of two, code * v_scale is a BF16 value: the FP8-V
+    # decode must equal the FP8-K / BF16-V decode of those rows
+    w = kvgen.custom(27, seq_lens=[70, 33], num_q_heads=8, num_kv_heads=2, head_dim=32, block_size=16,
+                     fp8=True)
+    w.v_scale = 2.0 ** -6
+    kc, vc = _oracle_cache_fp8(oracle_lib, w)
+    deq = oracle_lib.e4m3_to_f64(vc.ravel()) * w.v_scale
+    vbf = oracle_lib.f64_to_bf16(np.nan_to_num(deq)).reshape(vc.shape)
+    args = (w.block_tables.numpy(), w.seq_lens.numpy(), w.max_blocks_per_seq, w.num_seqs, w.num_q_heads,
+            w.num_kv_heads, w.head_dim, w.block_size, w.inv_sqrt_d, w.k_scale)
+    a = oracle_lib.paged_decode_attn_fp8(_rows(w.q), kc, vc, *args, w.v_scale, 8 * 32, 0)
+    b = oracle_lib.paged_decode_attn_fp8k(_rows(w.q), kc, vbf, *args, 8 * 32, 0)
+    assert np.array_equal(a, b)
 
 
 # ---------------------------------------------------------------------------
