@@ -12,9 +12,10 @@ One step is one pass of every timed call of the five synthetic workloads
   fp8k_decode_w4096  the same with sliding_window 4096
   fp8k_mixed_decode  paged_decode_attn_fp8k, 256 sequences of 128..65536
                      (log-uniform), GQA 64:8, block_size 64, split-KV
-Beside the step, and not in it, the FP8-output and the MRoPE variants of the
-fused K write are timed on the fused_write tokens ("next_rows"), with L2
-flushed before each launch.
+Beside the step, and not in it ("next_rows"), with L2 flushed before each
+launch: the FP8-output and the MRoPE variants of the fused K write on the
+fused_write tokens, and the FP8 K+V cache (kv_write_fp8 of the fp8k_long
+tokens, paged_decode_attn_fp8 of fp8k_long at W = 0 and of fp8k_mixed).
 The headline value is the step's algorithmic HBM bytes (what each call must
 read and write, counted per call below) divided by the step time, in GB/s;
 each call's GB/s, tokens/s and fraction of the measured HBM copy rate are
@@ -57,20 +58,20 @@ def measured_peak():
 # algorithmic bytes (what a call must move through HBM, per call)
 # ---------------------------------------------------------------------------
 def decode_bytes(seq_lens, window, num_kv_heads, head_dim, k_bytes, num_seqs, num_q_heads,
-                 max_blocks_per_seq):
+                 max_blocks_per_seq, v_bytes=2):
     att = 0
     for L in seq_lens:
         L = int(L)
         att += min(L, window) if window else L
-    kv = att * num_kv_heads * head_dim * (k_bytes + 2)
+    kv = att * num_kv_heads * head_dim * (k_bytes + v_bytes)
     q = num_seqs * num_q_heads * head_dim * 2
     out = num_seqs * num_q_heads * head_dim * 4
     return kv + q + out + num_seqs * 4
 
 
-def write_bytes_per_token(row, k_out_bytes):
-    # K in (bf16) + K out + V in (bf16) + V out (bf16) + the slot (int64)
-    return row * 2 + row * k_out_bytes + row * 2 + row * 2 + 8
+def write_bytes_per_token(row, k_out_bytes, v_out_bytes=2):
+    # K in (bf16) + K out + V in (bf16) + V out + the slot (int64)
+    return row * 2 + row * k_out_bytes + row * 2 + row * v_out_bytes + 8
 
 
 # ---------------------------------------------------------------------------
@@ -130,7 +131,11 @@ class Clocks:
 
 WORKLOAD_OF_PART = {"fused_write": "fused", "bf16_prefill": "bf16_gqa4", "bf16_decode": "bf16_gqa4",
                     "fp8k_prefill": "fp8k_long", "fp8k_decode_w0": "fp8k_long", "fp8k_decode_w4096": "fp8k_long",
-                    "fp8k_mixed_decode": "fp8k_mixed"}
+                    "fp8k_mixed_decode": "fp8k_mixed",
+                    # calls timed beside the step
+                    "fused_k_write_fp8": "fused", "fused_k_write_mrope": "fused",
+                    "fp8_kv_prefill": "fp8k_long", "fp8_kv_decode_w0": "fp8k_long",
+                    "fp8_kv_mixed_decode": "fp8k_mixed"}
 
 
 class GpuStep:
@@ -191,7 +196,13 @@ class GpuStep:
             if want in (None, name):
                 setup()
         if self.only_part:
-            self.parts = [p for p in self.parts if p["name"] == self.only_part]
+            # a call beside the step keeps its workload's parts (they fill the
+            # slots and caches it reads)
+            if any(x["name"] == self.only_part for x in self.extras):
+                self.extras = [x for x in self.extras if x["name"] == self.only_part]
+            else:
+                self.parts = [p for p in self.parts if p["name"] == self.only_part]
+                self.extras = []
         self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=self.dev)
         pk.kv_set_decode_workspace(self.ws)
         torch.cuda.synchronize()
@@ -332,6 +343,26 @@ class GpuStep:
         self.inputs_h2d += [key, value, q, tables, lens]
         self.outputs_d2h += outs
 
+        # FP8 K and V, timed beside the step: the same tokens written with
+        # kv_write_fp8 (the K codes are the ones above), then decoded (W = 0)
+        vc8 = kvgen.poisoned_pool(w.num_blocks, bs, H, D, "fp8", dev)
+        v_scale = w.v_scale
+
+        def fp8kv_prefill():
+            for c0, c1 in chunks:
+                pk.kv_write_fp8(key[c0:c1], value[c0:c1], kc, vc8, slots[c0:c1], c1 - c0, H, D, bs, k_scale,
+                                v_scale, H * D, H * D)
+        out8 = torch.empty((w.num_seqs, Hq, D), dtype=torch.float32, device=dev)
+
+        def fp8kv_decode():
+            pk.paged_decode_attn_fp8(q, kc, vc8, out8, tables, lens, w.max_blocks_per_seq, w.num_seqs, Hq, H, D, bs,
+                                     w.inv_sqrt_d, k_scale, v_scale, Hq * D, 0)
+        self.extras += [dict(name="fp8_kv_prefill", fn=fp8kv_prefill, tokens=n,
+                             bytes=n * write_bytes_per_token(H * D, 1, 1)),
+                        dict(name="fp8_kv_decode_w0", fn=fp8kv_decode, tokens=w.num_seqs,
+                             bytes=decode_bytes(w.seq_lens.tolist(), 0, H, D, 1, w.num_seqs, Hq,
+                                                w.max_blocks_per_seq, v_bytes=1))]
+
     def _setup_fp8k_mixed(self):
         torch, kvgen, pk, dev = self.torch, self.kvgen, self.pk, self.dev
         w = kvgen.fp8k_mixed(device=dev, **(self.SMALL['fp8k_mixed'] if self.small else {}))
@@ -340,13 +371,16 @@ class GpuStep:
         slots = torch.empty(n, dtype=torch.int64, device=dev)
         kc = kvgen.poisoned_pool(w.num_blocks, bs, H, D, "fp8", dev)
         vc = kvgen.poisoned_pool(w.num_blocks, bs, H, D, "bf16", dev)
+        vc8 = kvgen.poisoned_pool(w.num_blocks, bs, H, D, "fp8", dev)   # FP8 V, for the FP8 K+V decode
         fill, _ = self._slots_calls(w, tables, slots)
         fill()
         chunk = 262144
-        for c0 in range(0, n, chunk):   # the cache is written once, untimed
+        for c0 in range(0, n, chunk):   # the caches are written once, untimed
             c1 = min(n, c0 + chunk)
             pk.kv_write_fp8k(w.key[c0:c1], w.value[c0:c1], kc, vc, slots[c0:c1], c1 - c0, H, D, bs, H * D, H * D,
                              w.k_scale)
+            pk.kv_write_fp8(w.key[c0:c1], w.value[c0:c1], kc, vc8, slots[c0:c1], c1 - c0, H, D, bs, w.k_scale,
+                            w.v_scale, H * D, H * D)
         torch.cuda.synchronize()
         w.key = w.value = None
         q, lens, k_scale = w.q, w.seq_lens.to(dev), w.k_scale
@@ -362,6 +396,15 @@ class GpuStep:
         self._grow_ws(w)
         self.inputs_h2d += [q, tables, lens]
         self.outputs_d2h += [out]
+        out8 = torch.empty((w.num_seqs, Hq, D), dtype=torch.float32, device=dev)
+        v_scale = w.v_scale
+
+        def fp8kv_decode():
+            pk.paged_decode_attn_fp8(q, kc, vc8, out8, tables, lens, w.max_blocks_per_seq, w.num_seqs, Hq, H, D, bs,
+                                     w.inv_sqrt_d, k_scale, v_scale, Hq * D, 0)
+        self.extras.append(dict(name="fp8_kv_mixed_decode", fn=fp8kv_decode, tokens=w.num_seqs,
+                                bytes=decode_bytes(w.seq_lens.tolist(), 0, H, D, 1, w.num_seqs, Hq,
+                                                   w.max_blocks_per_seq, v_bytes=1)))
 
     def _grow_ws(self, w):
         self.ws_bytes = max(self.ws_bytes, self.pk.kv_decode_workspace_bytes(
@@ -520,9 +563,15 @@ def run_gpu(args):
     step = GpuStep(dev, args.part, args.small)
     stream = torch.cuda.current_stream()
     if args.part:
-        # one part only, for profiling: warm-up, then `steps` runs, no report
-        for _ in range(args.warmup + args.steps):
+        # one part only, for profiling: warm-up, then `steps` runs, no report.
+        # A call beside the step runs after one pass of its workload's parts.
+        runs = [step.run_step]
+        if step.extras:
             step.run_step()
+            runs = [x["fn"] for x in step.extras]
+        for _ in range(args.warmup + args.steps):
+            for f in runs:
+                f()
         torch.cuda.synchronize()
         assert pk.kv_get_device_error() == 0
         print(json.dumps({"part": args.part, "runs": args.warmup + args.steps, "ok": True}))
@@ -636,7 +685,7 @@ def dominant_roofline(step, dom, stream, peak, peak_kind, args):
         torch.cuda.synchronize()
         launches = reps * len(step.fp8_chunks)
         per_launch = statistics.mean((c1 - c0) * write_bytes_per_token(step.fp8_row, 1) for c0, c1 in step.fp8_chunks)
-        kernel = "kv_write_fp8k (write_fp8k_kernel)"
+        kernel = "kv_write_fp8k (write_fp8_kernel<4, false>)"
     else:
         a.record(stream)
         for _ in range(reps):

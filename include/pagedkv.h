@@ -114,6 +114,19 @@ PAGEDKV_API int kv_write_fp8k(const kv_bf16_t *key, const kv_bf16_t *value, kv_e
                   uint32_t key_stride, uint32_t value_stride, float k_scale, void *stream);
 
 /* ------------------------------------------------------------------------
+ * FP8 K and V cache write.  [kv_cache.rs] `reshape_and_cache_fp8`: K stored
+ * as k / k_scale and V as v / v_scale, both E4M3 with the rule of
+ * kv_write_fp8k, into two uint8 pools of the NHD layout. Argument order of
+ * that launcher (scales before strides); its cache_stride is implied by the
+ * layout and dropped. Bit-exact.
+ *   k_scale, v_scale  per-tensor scales, finite and > 0.
+ * ---------------------------------------------------------------------- */
+PAGEDKV_API int kv_write_fp8(const kv_bf16_t *key, const kv_bf16_t *value, kv_e4m3_t *k_cache_fp8,
+                             kv_e4m3_t *v_cache_fp8, const int64_t *slot_mapping, uint32_t num_tokens,
+                             uint32_t num_kv_heads, uint32_t head_dim, uint32_t block_size, float k_scale,
+                             float v_scale, uint32_t key_stride, uint32_t value_stride, void *stream);
+
+/* ------------------------------------------------------------------------
  * Fused K path.  [kv_cache.rs] `fused_k_norm_rope_cache_write_bf16`: RMSNorm,
  * then RoPE, then the BF16 paged write in one kernel, K kept above BF16
  * precision throughout and rounded once at the write.
@@ -215,6 +228,20 @@ PAGEDKV_API int paged_decode_attn_fp8k(const kv_bf16_t *q, const kv_e4m3_t *k_ca
                            uint32_t head_dim, uint32_t block_size, float inv_sqrt_d,
                            float k_scale, uint32_t q_stride, uint32_t sliding_window,
                            void *stream);
+
+/* ------------------------------------------------------------------------
+ * FP8 K and V paged decode.  [kv_cache.rs] `paged_decode_attn_fp8` (its
+ * argument order, with num_seqs, q_stride and sliding_window as in the
+ * calls above and cache_stride dropped): as paged_decode_attn_fp8k, with
+ * v_p = E4M3 code * v_scale (v_scale finite and > 0) read from a uint8 V
+ * pool. Supported head_dim: {128, 256}.
+ * ---------------------------------------------------------------------- */
+PAGEDKV_API int paged_decode_attn_fp8(const kv_bf16_t *q, const kv_e4m3_t *k_cache_fp8,
+                                      const kv_e4m3_t *v_cache_fp8, float *output, const int32_t *block_tables,
+                                      const int32_t *seq_lens, uint32_t max_blocks_per_seq, uint32_t num_seqs,
+                                      uint32_t num_q_heads, uint32_t num_kv_heads, uint32_t head_dim,
+                                      uint32_t block_size, float inv_sqrt_d, float k_scale, float v_scale,
+                                      uint32_t q_stride, uint32_t sliding_window, void *stream);
 
 /* ------------------------------------------------------------------------
  * FP8-K paged decode without any caller-provided memory. The source pages

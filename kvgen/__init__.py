@@ -217,6 +217,7 @@ def fp8k_long(seed: int = 1004, device="cpu", num_seqs: int = 128, seq_len: int 
     token_seq, positions = _prefill_token_index(seq_lens)
     return Workload("fp8k_long", num_seqs, Hq, H, D, bs, nb, mbps, seq_lens, tables, key, value, q,
                     positions, token_seq, inv_sqrt_d=1.0 / math.sqrt(D), k_scale=k_scale,
+                    v_scale=amax_scale(value),
                     sliding_windows=(0, 4096))
 
 
@@ -237,7 +238,8 @@ def fp8k_mixed(seed: int = 1005, device="cpu", num_seqs: int = 256, min_len: int
     q = _normal_bf16((num_seqs, Hq * D), 1.0, g, device)
     token_seq, positions = _prefill_token_index(seq_lens)
     return Workload("fp8k_mixed", num_seqs, Hq, H, D, bs, nb, mbps, seq_lens, tables, key, value, q,
-                    positions, token_seq, inv_sqrt_d=1.0 / math.sqrt(D), k_scale=k_scale)
+                    positions, token_seq, inv_sqrt_d=1.0 / math.sqrt(D), k_scale=k_scale,
+                    v_scale=amax_scale(value))
 
 
 WORKLOADS = {
@@ -279,10 +281,14 @@ def custom(seed: int, device="cpu", *, seq_lens, num_q_heads, num_kv_heads, head
 
 def amax_scale(x: torch.Tensor) -> float:
     """Per-tensor E4M3 scale max|x| / 448, in float32 (1.0 for an empty or
-    all-zero tensor)."""
+    all-zero tensor). Rows are scanned in chunks, so no full-size temporary
+    is made."""
     if x.numel() == 0:
         return 1.0
-    amax = float(x.abs().max().float().item())
+    step = _rows_per_chunk(x.shape[-1]) if x.dim() == 2 else x.shape[0]
+    amax = 0.0
+    for r0 in range(0, x.shape[0], step):
+        amax = max(amax, float(x[r0:r0 + step].abs().max().float().item()))
     return float(torch.tensor(amax / 448.0, dtype=torch.float32).item()) if amax > 0 else 1.0
 
 

@@ -19,10 +19,11 @@ import os
 import torch
 
 __all__ = [
-    "PagedKVError", "library_path", "kv_fill_slots", "kv_write_bf16", "kv_write_fp8k",
+    "PagedKVError", "library_path", "kv_fill_slots", "kv_write_bf16", "kv_write_fp8k", "kv_write_fp8",
     "kv_write_fused_k_norm_rope_bf16", "kv_write_fused_k_norm_rope_bf16_mrope",
     "kv_write_fused_k_norm_rope_fp8", "kv_write_v_only", "paged_decode_attn_bf16",
-    "paged_decode_attn_fp8k", "paged_decode_attn_fp8k_static_scratch", "kv_decode_workspace_bytes",
+    "paged_decode_attn_fp8k", "paged_decode_attn_fp8", "paged_decode_attn_fp8k_static_scratch",
+    "kv_decode_workspace_bytes",
     "kv_set_decode_workspace", "kv_get_device_error", "kv_device_info", "KV_OK", "KV_ERR_INVALID_ARG",
     "KV_ERR_UNSUPPORTED", "KV_ERR_CUDA", "KV_ERR_DEVICE",
 ]
@@ -40,6 +41,7 @@ _SIGNATURES = {
     "kv_fill_slots": (ctypes.c_int, [_P, _P, _U32, _U32, _U32, _P]),
     "kv_write_bf16": (ctypes.c_int, [_P, _P, _P, _P, _P, _U32, _U32, _U32, _U32, _U32, _U32, _P]),
     "kv_write_fp8k": (ctypes.c_int, [_P, _P, _P, _P, _P, _U32, _U32, _U32, _U32, _U32, _U32, _F32, _P]),
+    "kv_write_fp8": (ctypes.c_int, [_P, _P, _P, _P, _P, _U32, _U32, _U32, _U32, _F32, _F32, _U32, _U32, _P]),
     "kv_write_fused_k_norm_rope_bf16": (
         ctypes.c_int, [_P, _P, _P, _P, _P, _U32, _U32, _U32, _U32, _U32, _F32, _F32, _P]),
     "kv_write_fused_k_norm_rope_bf16_mrope": (
@@ -52,6 +54,9 @@ _SIGNATURES = {
     "paged_decode_attn_fp8k": (
         ctypes.c_int,
         [_P, _P, _P, _P, _P, _P, _U32, _U32, _U32, _U32, _U32, _U32, _F32, _F32, _U32, _U32, _P]),
+    "paged_decode_attn_fp8": (
+        ctypes.c_int,
+        [_P, _P, _P, _P, _P, _P, _U32, _U32, _U32, _U32, _U32, _U32, _F32, _F32, _F32, _U32, _U32, _P]),
     "paged_decode_attn_fp8k_static_scratch": (
         ctypes.c_int,
         [_P, _P, _P, _P, _P, _P, _U32, _U32, _U32, _U32, _U32, _U32, _F32, _F32, _U32, _U32, _P]),
@@ -133,6 +138,13 @@ def kv_write_fp8k(key, value, k_cache_fp8, v_cache, slot_mapping, num_tokens, nu
         num_kv_heads, head_dim, block_size, key_stride, value_stride, k_scale, _stream(stream)))
 
 
+def kv_write_fp8(key, value, k_cache_fp8, v_cache_fp8, slot_mapping, num_tokens, num_kv_heads, head_dim,
+                 block_size, k_scale, v_scale, key_stride, value_stride, stream=None):
+    _check("kv_write_fp8", lib().kv_write_fp8(
+        _ptr(key), _ptr(value), _ptr(k_cache_fp8), _ptr(v_cache_fp8), _ptr(slot_mapping), num_tokens,
+        num_kv_heads, head_dim, block_size, k_scale, v_scale, key_stride, value_stride, _stream(stream)))
+
+
 def kv_write_fused_k_norm_rope_bf16(k_in, k_norm_weight, positions, k_cache, slot_mapping, num_tokens,
                                     num_kv_heads, head_dim, rotary_dim, block_size, rms_eps, theta,
                                     stream=None):
@@ -181,6 +193,15 @@ def paged_decode_attn_fp8k(q, k_cache_fp8, v_cache, output, block_tables, seq_le
         _ptr(q), _ptr(k_cache_fp8), _ptr(v_cache), _ptr(output), _ptr(block_tables), _ptr(seq_lens),
         max_blocks_per_seq, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, inv_sqrt_d,
         k_scale, q_stride, sliding_window, _stream(stream)))
+
+
+def paged_decode_attn_fp8(q, k_cache_fp8, v_cache_fp8, output, block_tables, seq_lens, max_blocks_per_seq,
+                          num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, inv_sqrt_d, k_scale, v_scale,
+                          q_stride, sliding_window, stream=None):
+    _check("paged_decode_attn_fp8", lib().paged_decode_attn_fp8(
+        _ptr(q), _ptr(k_cache_fp8), _ptr(v_cache_fp8), _ptr(output), _ptr(block_tables), _ptr(seq_lens),
+        max_blocks_per_seq, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, inv_sqrt_d,
+        k_scale, v_scale, q_stride, sliding_window, _stream(stream)))
 
 
 def paged_decode_attn_fp8k_static_scratch(q, k_cache_fp8, v_cache, output, block_tables, seq_lens,

@@ -121,8 +121,23 @@ int kv_write_fp8k(const kv_bf16_t* key, const kv_bf16_t* value, kv_e4m3_t* k_cac
   const uint32_t row = num_kv_heads * head_dim;
   if (key_stride < row || value_stride < row) return KV_ERR_INVALID_ARG;
   if (!(k_scale > 0.0f) || !isfinite(k_scale)) return KV_ERR_INVALID_ARG;
-  return from_cuda(launch_write_fp8k(key, value, k_cache_fp8, v_cache, slot_mapping, num_tokens, row,
-                                     key_stride, value_stride, k_scale, as_stream(stream)));
+  return from_cuda(launch_write_fp8(key, value, k_cache_fp8, v_cache, false, slot_mapping, num_tokens, row,
+                                    key_stride, value_stride, k_scale, 1.0f, as_stream(stream)));
+}
+
+int kv_write_fp8(const kv_bf16_t* key, const kv_bf16_t* value, kv_e4m3_t* k_cache_fp8, kv_e4m3_t* v_cache_fp8,
+                 const int64_t* slot_mapping, uint32_t num_tokens, uint32_t num_kv_heads, uint32_t head_dim,
+                 uint32_t block_size, float k_scale, float v_scale, uint32_t key_stride, uint32_t value_stride,
+                 void* stream) {
+  if (num_tokens == 0) return KV_OK;
+  if (!key || !value || !k_cache_fp8 || !v_cache_fp8 || !slot_mapping) return KV_ERR_INVALID_ARG;
+  if (int r = check_rows(num_kv_heads, head_dim, block_size)) return r;
+  const uint32_t row = num_kv_heads * head_dim;
+  if (key_stride < row || value_stride < row) return KV_ERR_INVALID_ARG;
+  if (!(k_scale > 0.0f) || !isfinite(k_scale) || !(v_scale > 0.0f) || !isfinite(v_scale))
+    return KV_ERR_INVALID_ARG;
+  return from_cuda(launch_write_fp8(key, value, k_cache_fp8, v_cache_fp8, true, slot_mapping, num_tokens, row,
+                                    key_stride, value_stride, k_scale, v_scale, as_stream(stream)));
 }
 
 static int fused_common(const kv_bf16_t* k_in, const kv_bf16_t* k_norm_weight, const int32_t* positions,
@@ -175,11 +190,11 @@ int kv_write_fused_k_norm_rope_fp8(const kv_bf16_t* k_in, const kv_bf16_t* k_nor
                       stream);
 }
 
-static int decode_common(const kv_bf16_t* q, const void* k_cache, const kv_bf16_t* v_cache, float* output,
+static int decode_common(const kv_bf16_t* q, const void* k_cache, const void* v_cache, float* output,
                          const int32_t* block_tables, const int32_t* seq_lens, uint32_t max_blocks_per_seq,
                          uint32_t num_seqs, uint32_t num_q_heads, uint32_t num_kv_heads, uint32_t head_dim,
                          uint32_t block_size, float inv_sqrt_d, float k_scale, uint32_t q_stride,
-                         uint32_t sliding_window, bool fp8, void* stream) {
+                         uint32_t sliding_window, bool fp8, bool fp8_v, float v_scale, void* stream) {
   if (num_seqs == 0) return KV_OK;
   if (!q || !k_cache || !v_cache || !output || !block_tables || !seq_lens) return KV_ERR_INVALID_ARG;
   if (num_kv_heads == 0 || num_q_heads == 0 || num_q_heads % num_kv_heads) return KV_ERR_INVALID_ARG;
@@ -187,6 +202,7 @@ static int decode_common(const kv_bf16_t* q, const void* k_cache, const kv_bf16_
   if (uint64_t(q_stride) < uint64_t(num_q_heads) * head_dim) return KV_ERR_INVALID_ARG;
   if (!isfinite(inv_sqrt_d)) return KV_ERR_INVALID_ARG;
   if (fp8 && (!(k_scale > 0.0f) || !isfinite(k_scale))) return KV_ERR_INVALID_ARG;
+  if (fp8_v && (!(v_scale > 0.0f) || !isfinite(v_scale))) return KV_ERR_INVALID_ARG;
   if (fp8 ? (head_dim != 128 && head_dim != 256) : (head_dim != 64 && head_dim != 128 && head_dim != 256))
     return KV_ERR_UNSUPPORTED;
   if (!is_pow2(block_size) || block_size < 16 || block_size > 256) return KV_ERR_UNSUPPORTED;
@@ -217,6 +233,8 @@ static int decode_common(const kv_bf16_t* q, const void* k_cache, const kv_bf16_
   a.q_stride = q_stride;
   a.sliding_window = sliding_window;
   a.fp8 = fp8;
+  a.fp8_v = fp8_v;
+  a.v_scale = v_scale;
   {
     std::lock_guard<std::mutex> lock(g_mutex);
     a.workspace = g_ws_ptr[dev.device];
@@ -240,7 +258,7 @@ int paged_decode_attn_bf16(const kv_bf16_t* q, const kv_bf16_t* k_cache, const k
                            uint32_t q_stride, uint32_t sliding_window, void* stream) {
   return decode_common(q, k_cache, v_cache, output, block_tables, seq_lens, max_blocks_per_seq, num_seqs,
                        num_q_heads, num_kv_heads, head_dim, block_size, inv_sqrt_d, 1.0f, q_stride,
-                       sliding_window, false, stream);
+                       sliding_window, false, false, 1.0f, stream);
 }
 
 int paged_decode_attn_fp8k(const kv_bf16_t* q, const kv_e4m3_t* k_cache_fp8, const kv_bf16_t* v_cache,
@@ -250,7 +268,18 @@ int paged_decode_attn_fp8k(const kv_bf16_t* q, const kv_e4m3_t* k_cache_fp8, con
                            float k_scale, uint32_t q_stride, uint32_t sliding_window, void* stream) {
   return decode_common(q, k_cache_fp8, v_cache, output, block_tables, seq_lens, max_blocks_per_seq, num_seqs,
                        num_q_heads, num_kv_heads, head_dim, block_size, inv_sqrt_d, k_scale, q_stride,
-                       sliding_window, true, stream);
+                       sliding_window, true, false, 1.0f, stream);
+}
+
+int paged_decode_attn_fp8(const kv_bf16_t* q, const kv_e4m3_t* k_cache_fp8, const kv_e4m3_t* v_cache_fp8,
+                          float* output, const int32_t* block_tables, const int32_t* seq_lens,
+                          uint32_t max_blocks_per_seq, uint32_t num_seqs, uint32_t num_q_heads,
+                          uint32_t num_kv_heads, uint32_t head_dim, uint32_t block_size, float inv_sqrt_d,
+                          float k_scale, float v_scale, uint32_t q_stride, uint32_t sliding_window,
+                          void* stream) {
+  return decode_common(q, k_cache_fp8, v_cache_fp8, output, block_tables, seq_lens, max_blocks_per_seq,
+                       num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, inv_sqrt_d, k_scale, q_stride,
+                       sliding_window, true, true, v_scale, stream);
 }
 
 size_t kv_decode_workspace_bytes(uint32_t max_blocks_per_seq, uint32_t num_seqs, uint32_t num_q_heads,

@@ -161,6 +161,18 @@ __device__ __forceinline__ float bf16_hi_to_f32(uint32_t v) {
   return __uint_as_float(v & 0xFFFF0000u);
 }
 
+// Halves of an f16x2 -> f32 (exact).
+__device__ __forceinline__ float f16_lo_to_f32(uint32_t v) {
+  float f;
+  asm("cvt.f32.f16 %0, %1;" : "=f"(f) : "h"(uint16_t(v & 0xffffu)));
+  return f;
+}
+__device__ __forceinline__ float f16_hi_to_f32(uint32_t v) {
+  float f;
+  asm("cvt.f32.f16 %0, %1;" : "=f"(f) : "h"(uint16_t(v >> 16)));
+  return f;
+}
+
 // Two floats -> f16x2 (round to nearest even), `lo` in the low half.
 __device__ __forceinline__ uint32_t f32x2_to_f16x2(float lo, float hi) {
   uint32_t d;

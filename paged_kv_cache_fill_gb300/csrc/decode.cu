@@ -1,8 +1,10 @@
-// Paged decode attention over a BF16 or FP8-E4M3-K / BF16-V paged cache.
+// Paged decode attention over a BF16, FP8-E4M3-K / BF16-V or FP8 K+V paged
+// cache.
 //
 // [kv_cache.rs] `paged_decode_attn_fp8` doc (one query per (query head,
 // sequence), block_tables i32[num_seqs * max_blocks_per_seq], seq_lens
-// i32[num_seqs]); `paged_decode_attn_bf16k_turbo3v` argument list (q_stride,
+// i32[num_seqs]; K and V scaled by k_scale and v_scale);
+// `paged_decode_attn_bf16k_turbo3v` argument list (q_stride,
 // sliding_window); [kv_cache_fp8k.rs] module invariants (FP8 K is multiplied
 // by k_scale).
 //
@@ -24,6 +26,10 @@
 //     with P split into BF16 hi + lo parts (two MMAs) so the weights keep
 //     ~16 significant bits. FP8 K converts exactly to f16 in registers
 //     (cvt e4m3x2 -> f16x2) against f16 queries scaled by a power of two.
+//     FP8 V converts exactly to f16 too, after a transposing ldmatrix that
+//     gives each lane two tokens of two adjacent dims; P then enters as f16
+//     hi + lo parts scaled by 2^8 (keeping small weights out of the f16
+//     subnormal range), and v_scale / 2^8 is applied at the end.
 //   * Split-KV (flash-decoding): items of a sequence write unnormalised
 //     partial outputs with their running max and sum to a caller-provided
 //     workspace; a combine kernel merges them in fixed split order, so the
@@ -75,6 +81,7 @@ struct DecodeParams {
   uint32_t max_splits;  // 0: no workspace, one item per (sequence, head group)
   uint32_t min_split_tiles;
   float score_scale;    // inv_sqrt_d * log2(e)   (times k_scale for FP8)
+  float out_scale;      // FP8 V: v_scale / 2^8 (P enters the MMA scaled by 2^8)
   uint32_t stages, stage_bytes, k_bytes, v_bytes;  // shared-memory ring geometry
 };
 
@@ -132,12 +139,13 @@ struct Walker {
 };
 
 // -------------------------------------------------------------- the kernel
-template <bool kFp8, int D, int NT>
+template <bool kFp8, bool kFp8V, int D, int NT>
 __global__ void __launch_bounds__(32 * 9, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                   const DecodeParams p) {
   constexpr int kKChunks = kFp8 ? D / 128 : D / 64;  // 128-byte chunks per K head row
-  constexpr int kVChunks = D / 64;
+  constexpr int kVChunks = kFp8V ? D / 128 : D / 64;
+  static_assert(kFp8 || !kFp8V, "an FP8 V cache comes with an FP8 K cache");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -456,12 +464,6 @@ __global__ void __launch_bounds__(32 * 9, 1)
         acc[i][2] *= al0;
         acc[i][3] *= al1;
       }
-      // ---- P^T as B fragments: hi and lo BF16 parts, transposed by movmatrix
-      const uint32_t hi01 = f32x2_to_bf16x2(e0, e1), hi23 = f32x2_to_bf16x2(e2, e3);
-      const uint32_t lo01 = f32x2_to_bf16x2(e0 - bf16_lo_to_f32(hi01), e1 - bf16_hi_to_f32(hi01));
-      const uint32_t lo23 = f32x2_to_bf16x2(e2 - bf16_lo_to_f32(hi23), e3 - bf16_hi_to_f32(hi23));
-      const uint32_t bh0 = movmatrix_trans(hi01), bh1 = movmatrix_trans(hi23);
-      const uint32_t bl0 = movmatrix_trans(lo01), bl1 = movmatrix_trans(lo23);
       // V rows of masked positions may hold anything (NaN): zero them
       uint32_t vmask01 = 0xffffffffu, vmask89 = 0xffffffffu;
       if (boundary) {
@@ -470,19 +472,60 @@ __global__ void __launch_bounds__(32 * 9, 1)
         vmask01 = (ok(q0) ? 0x0000ffffu : 0u) | (ok(q0 + 1) ? 0xffff0000u : 0u);
         vmask89 = (ok(q0 + 8) ? 0x0000ffffu : 0u) | (ok(q0 + 9) ? 0xffff0000u : 0u);
       }
-      // ---- O^T += V^T P^T
+      if constexpr (!kFp8V) {
+        // ---- P^T as B fragments: hi and lo BF16 parts, transposed by movmatrix
+        const uint32_t hi01 = f32x2_to_bf16x2(e0, e1), hi23 = f32x2_to_bf16x2(e2, e3);
+        const uint32_t lo01 = f32x2_to_bf16x2(e0 - bf16_lo_to_f32(hi01), e1 - bf16_hi_to_f32(hi01));
+        const uint32_t lo23 = f32x2_to_bf16x2(e2 - bf16_lo_to_f32(hi23), e3 - bf16_hi_to_f32(hi23));
+        const uint32_t bh0 = movmatrix_trans(hi01), bh1 = movmatrix_trans(hi23);
+        const uint32_t bl0 = movmatrix_trans(lo01), bl1 = movmatrix_trans(lo23);
+        // ---- O^T += V^T P^T
 #pragma unroll
-      for (int i = 0; i < D / 16; ++i) {
-        const uint32_t chunk = i >> 2;
-        const uint32_t unit = ((i & 3) << 1) + v_unit;
-        uint32_t a[4];
-        ldmatrix_x4_trans(a, vbase + chunk * (kTile * 128) + v_row * 128 + ((unit ^ (v_row & 7)) << 4));
-        a[0] &= vmask01;
-        a[1] &= vmask01;
-        a[2] &= vmask89;
-        a[3] &= vmask89;
-        mma_bf16(acc[i], a, bh0, bh1);
-        mma_bf16(acc[i], a, bl0, bl1);
+        for (int i = 0; i < D / 16; ++i) {
+          const uint32_t chunk = i >> 2;
+          const uint32_t unit = ((i & 3) << 1) + v_unit;
+          uint32_t a[4];
+          ldmatrix_x4_trans(a, vbase + chunk * (kTile * 128) + v_row * 128 + ((unit ^ (v_row & 7)) << 4));
+          a[0] &= vmask01;
+          a[1] &= vmask01;
+          a[2] &= vmask89;
+          a[3] &= vmask89;
+          mma_bf16(acc[i], a, bh0, bh1);
+          mma_bf16(acc[i], a, bl0, bl1);
+        }
+      } else {
+        // ---- P^T as f16 hi + lo parts of 2^8 * P
+        const float f0 = e0 * 256.0f, f1 = e1 * 256.0f, f2 = e2 * 256.0f, f3 = e3 * 256.0f;
+        const uint32_t hi01 = f32x2_to_f16x2(f0, f1), hi23 = f32x2_to_f16x2(f2, f3);
+        const uint32_t lo01 = f32x2_to_f16x2(f0 - f16_lo_to_f32(hi01), f1 - f16_hi_to_f32(hi01));
+        const uint32_t lo23 = f32x2_to_f16x2(f2 - f16_lo_to_f32(hi23), f3 - f16_hi_to_f32(hi23));
+        const uint32_t bh0 = movmatrix_trans(hi01), bh1 = movmatrix_trans(hi23);
+        const uint32_t bl0 = movmatrix_trans(lo01), bl1 = movmatrix_trans(lo23);
+        // ---- O^T += V^T P^T. One transposing ldmatrix covers 32 dims x 16
+        // tokens: matrix m holds tokens 8(m&1).. of 16-byte unit 2(jj&3)+(m>>1)
+        // and gives this lane the byte pairs (dims 2g8, 2g8+1) of tokens 2c4
+        // and 2c4+1. A-row g8 is dim 2g8 and A-row g8+8 is dim 2g8+1 of the
+        // 16-dim block, so the accumulator rows come out in that order too.
+#pragma unroll
+        for (int jj = 0; jj < D / 32; ++jj) {
+          const uint32_t chunk = jj >> 2;
+          const uint32_t unit = ((jj & 3) << 1) + k_unit;
+          uint32_t r[4];
+          ldmatrix_x4_trans(r, vbase + chunk * (kTile * 128) + k_row * 128 + ((unit ^ (k_row & 7)) << 4));
+          uint32_t a0[4], a1[4];
+          a0[0] = e4m3x2_to_f16x2(uint16_t(__byte_perm(r[0], 0u, 0x0020u))) & vmask01;
+          a0[1] = e4m3x2_to_f16x2(uint16_t(__byte_perm(r[0], 0u, 0x0031u))) & vmask01;
+          a0[2] = e4m3x2_to_f16x2(uint16_t(__byte_perm(r[1], 0u, 0x0020u))) & vmask89;
+          a0[3] = e4m3x2_to_f16x2(uint16_t(__byte_perm(r[1], 0u, 0x0031u))) & vmask89;
+          a1[0] = e4m3x2_to_f16x2(uint16_t(__byte_perm(r[2], 0u, 0x0020u))) & vmask01;
+          a1[1] = e4m3x2_to_f16x2(uint16_t(__byte_perm(r[2], 0u, 0x0031u))) & vmask01;
+          a1[2] = e4m3x2_to_f16x2(uint16_t(__byte_perm(r[3], 0u, 0x0020u))) & vmask89;
+          a1[3] = e4m3x2_to_f16x2(uint16_t(__byte_perm(r[3], 0u, 0x0031u))) & vmask89;
+          mma_f16(acc[2 * jj], a0, bh0, bh1);
+          mma_f16(acc[2 * jj], a0, bl0, bl1);
+          mma_f16(acc[2 * jj + 1], a1, bh0, bh1);
+          mma_f16(acc[2 * jj + 1], a1, bl0, bl1);
+        }
       }
     }
     __syncwarp();
@@ -500,20 +543,28 @@ __global__ void __launch_bounds__(32 * 9, 1)
       const uint32_t hq0 = kv_head * p.group + col0;
       const bool ok0 = col0 < p.group, ok1 = col0 + 1 < p.group;
       if (mt.flags & kSingle) {
-        const float inv0 = (mt.flags & kEmpty) ? 0.0f : 1.0f / l0;
-        const float inv1 = (mt.flags & kEmpty) ? 0.0f : 1.0f / l1;
+        const float sc = kFp8V ? p.out_scale : 1.0f;
+        const float inv0 = (mt.flags & kEmpty) ? 0.0f : sc / l0;
+        const float inv1 = (mt.flags & kEmpty) ? 0.0f : sc / l1;
         float* o0 = p.output + (uint64_t(mt.seq) * p.num_q_heads + hq0) * D;
         float* o1 = o0 + D;
 #pragma unroll
         for (int i = 0; i < D / 16; ++i) {
-          const uint32_t d = i * 16 + g8;
-          if (ok0) {
-            o0[d] = (mt.flags & kEmpty) ? 0.0f : acc[i][0] * inv0;
-            o0[d + 8] = (mt.flags & kEmpty) ? 0.0f : acc[i][2] * inv0;
-          }
-          if (ok1) {
-            o1[d] = (mt.flags & kEmpty) ? 0.0f : acc[i][1] * inv1;
-            o1[d + 8] = (mt.flags & kEmpty) ? 0.0f : acc[i][3] * inv1;
+          if constexpr (kFp8V) {
+            // accumulator rows g8 / g8+8 are dims 2g8 / 2g8+1
+            const uint32_t d = i * 16 + 2 * g8;
+            if (ok0) *reinterpret_cast<float2*>(o0 + d) = make_float2(acc[i][0] * inv0, acc[i][2] * inv0);
+            if (ok1) *reinterpret_cast<float2*>(o1 + d) = make_float2(acc[i][1] * inv1, acc[i][3] * inv1);
+          } else {
+            const uint32_t d = i * 16 + g8;
+            if (ok0) {
+              o0[d] = (mt.flags & kEmpty) ? 0.0f : acc[i][0] * inv0;
+              o0[d + 8] = (mt.flags & kEmpty) ? 0.0f : acc[i][2] * inv0;
+            }
+            if (ok1) {
+              o1[d] = (mt.flags & kEmpty) ? 0.0f : acc[i][1] * inv1;
+              o1[d + 8] = (mt.flags & kEmpty) ? 0.0f : acc[i][3] * inv1;
+            }
           }
         }
       } else {
@@ -522,14 +573,21 @@ __global__ void __launch_bounds__(32 * 9, 1)
         float* o1 = o0 + D;
 #pragma unroll
         for (int i = 0; i < D / 16; ++i) {
-          const uint32_t d = i * 16 + g8;
-          if (ok0) {
-            o0[d] = acc[i][0];
-            o0[d + 8] = acc[i][2];
-          }
-          if (ok1) {
-            o1[d] = acc[i][1];
-            o1[d + 8] = acc[i][3];
+          if constexpr (kFp8V) {
+            const uint32_t d = i * 16 + 2 * g8;
+            const float sc = p.out_scale;
+            if (ok0) *reinterpret_cast<float2*>(o0 + d) = make_float2(acc[i][0] * sc, acc[i][2] * sc);
+            if (ok1) *reinterpret_cast<float2*>(o1 + d) = make_float2(acc[i][1] * sc, acc[i][3] * sc);
+          } else {
+            const uint32_t d = i * 16 + g8;
+            if (ok0) {
+              o0[d] = acc[i][0];
+              o0[d + 8] = acc[i][2];
+            }
+            if (ok1) {
+              o1[d] = acc[i][1];
+              o1[d + 8] = acc[i][3];
+            }
           }
         }
         if (g8 == 0) {
@@ -654,13 +712,13 @@ struct Geometry {
   uint32_t heads_per_item, nt, stages, stage_bytes, k_bytes, v_bytes, smem_bytes;
 };
 
-Geometry geometry(bool fp8, uint32_t head_dim, uint32_t num_kv_heads, uint32_t group, int smem_max) {
+Geometry geometry(bool fp8, bool fp8_v, uint32_t head_dim, uint32_t num_kv_heads, uint32_t group, int smem_max) {
   Geometry g{};
   g.nt = (group + 7) / 8;
   uint32_t hg = 8 / g.nt;
   if (hg > num_kv_heads) hg = num_kv_heads;
   const uint32_t kchunks = fp8 ? head_dim / 128 : head_dim / 64;
-  const uint32_t vchunks = head_dim / 64;
+  const uint32_t vchunks = fp8_v ? head_dim / 128 : head_dim / 64;
   for (;; hg = (hg + 1) / 2) {
     g.heads_per_item = hg;
     g.k_bytes = hg * kchunks * kTile * 128;
@@ -680,13 +738,13 @@ Geometry geometry(bool fp8, uint32_t head_dim, uint32_t num_kv_heads, uint32_t g
   return g;
 }
 
-template <bool kFp8, int D, int NT>
+template <bool kFp8, bool kFp8V, int D, int NT>
 int launch_decode_t(const DecodeArgs& a, cudaStream_t stream, const Geometry& geo, DecodeParams& p) {
   CUtensorMap mk, mv;
   if (!encode_pool_map(&mk, a.k_cache, kFp8, a.num_kv_heads, D, geo.heads_per_item) ||
-      !encode_pool_map(&mv, a.v_cache, false, a.num_kv_heads, D, geo.heads_per_item))
+      !encode_pool_map(&mv, a.v_cache, kFp8V, a.num_kv_heads, D, geo.heads_per_item))
     return KV_ERR_CUDA;
-  auto kern = decode_kernel<kFp8, D, NT>;
+  auto kern = decode_kernel<kFp8, kFp8V, D, NT>;
   // The dynamic shared-memory opt-in is set once per device and size (so
   // that calls made while a stream is being captured into a CUDA graph after
   // a first eager call issue no attribute change).
@@ -724,7 +782,8 @@ size_t decode_workspace_bytes(uint32_t max_blocks_per_seq, uint32_t num_seqs, ui
 int launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   const DeviceInfo& dev = device_info();
   const uint32_t group = a.num_q_heads / a.num_kv_heads;
-  const Geometry geo = geometry(a.fp8, a.head_dim, a.num_kv_heads, group, dev.max_smem_optin);
+  const bool fp8_v = a.fp8 && a.fp8_v;
+  const Geometry geo = geometry(a.fp8, fp8_v, a.head_dim, a.num_kv_heads, group, dev.max_smem_optin);
   if (geo.stages < 2) return KV_ERR_UNSUPPORTED;
 
   DecodeParams p{};
@@ -744,6 +803,7 @@ int launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   p.q_stride = a.q_stride;
   p.sliding_window = a.sliding_window;
   p.score_scale = a.inv_sqrt_d * kLog2e * (a.fp8 ? a.k_scale : 1.0f);
+  p.out_scale = fp8_v ? a.v_scale * (1.0f / 256.0f) : 1.0f;
   p.stages = geo.stages;
   p.stage_bytes = geo.stage_bytes;
   p.k_bytes = geo.k_bytes;
@@ -777,18 +837,22 @@ int launch_decode(const DecodeArgs& a, cudaStream_t stream) {
     }
   }
 
-  const int key = (a.fp8 ? 100 : 0) + int(a.head_dim / 64) * 10 + int(geo.nt);
+  const int key = (fp8_v ? 200 : a.fp8 ? 100 : 0) + int(a.head_dim / 64) * 10 + int(geo.nt);
   switch (key) {
-    case 11: return launch_decode_t<false, 64, 1>(a, stream, geo, p);
-    case 12: return launch_decode_t<false, 64, 2>(a, stream, geo, p);
-    case 21: return launch_decode_t<false, 128, 1>(a, stream, geo, p);
-    case 22: return launch_decode_t<false, 128, 2>(a, stream, geo, p);
-    case 41: return launch_decode_t<false, 256, 1>(a, stream, geo, p);
-    case 42: return launch_decode_t<false, 256, 2>(a, stream, geo, p);
-    case 121: return launch_decode_t<true, 128, 1>(a, stream, geo, p);
-    case 122: return launch_decode_t<true, 128, 2>(a, stream, geo, p);
-    case 141: return launch_decode_t<true, 256, 1>(a, stream, geo, p);
-    case 142: return launch_decode_t<true, 256, 2>(a, stream, geo, p);
+    case 11: return launch_decode_t<false, false, 64, 1>(a, stream, geo, p);
+    case 12: return launch_decode_t<false, false, 64, 2>(a, stream, geo, p);
+    case 21: return launch_decode_t<false, false, 128, 1>(a, stream, geo, p);
+    case 22: return launch_decode_t<false, false, 128, 2>(a, stream, geo, p);
+    case 41: return launch_decode_t<false, false, 256, 1>(a, stream, geo, p);
+    case 42: return launch_decode_t<false, false, 256, 2>(a, stream, geo, p);
+    case 121: return launch_decode_t<true, false, 128, 1>(a, stream, geo, p);
+    case 122: return launch_decode_t<true, false, 128, 2>(a, stream, geo, p);
+    case 141: return launch_decode_t<true, false, 256, 1>(a, stream, geo, p);
+    case 142: return launch_decode_t<true, false, 256, 2>(a, stream, geo, p);
+    case 221: return launch_decode_t<true, true, 128, 1>(a, stream, geo, p);
+    case 222: return launch_decode_t<true, true, 128, 2>(a, stream, geo, p);
+    case 241: return launch_decode_t<true, true, 256, 1>(a, stream, geo, p);
+    case 242: return launch_decode_t<true, true, 256, 2>(a, stream, geo, p);
     default: return KV_ERR_UNSUPPORTED;
   }
 }

@@ -28,10 +28,11 @@ cudaError_t launch_copy_rows(const uint16_t* src0, const uint16_t* src1, uint16_
                              uint32_t row_elems, uint32_t stride0, uint32_t stride1,
                              cudaStream_t stream);
 
-cudaError_t launch_write_fp8k(const uint16_t* key, const uint16_t* value, uint8_t* k_cache_fp8,
-                              uint16_t* v_cache, const int64_t* slot_mapping, uint32_t num_tokens,
-                              uint32_t row_elems, uint32_t key_stride, uint32_t value_stride,
-                              float k_scale, cudaStream_t stream);
+// FP8 K write; V is copied as BF16 (fp8_v false) or quantised by v_scale.
+cudaError_t launch_write_fp8(const uint16_t* key, const uint16_t* value, uint8_t* k_cache_fp8, void* v_cache,
+                             bool fp8_v, const int64_t* slot_mapping, uint32_t num_tokens, uint32_t row_elems,
+                             uint32_t key_stride, uint32_t value_stride, float k_scale, float v_scale,
+                             cudaStream_t stream);
 
 // Fused RMSNorm/RoPE K write. pos_h/pos_w non-null selects the MRoPE
 // variant (position of pair i from positions/pos_h/pos_w by i % 3); fp8_out
@@ -47,7 +48,7 @@ cudaError_t launch_fused_k_norm_rope(const uint16_t* k_in, const uint16_t* k_nor
 struct DecodeArgs {
   const uint16_t* q;
   const void* k_cache;  // bf16 or e4m3 pool
-  const uint16_t* v_cache;
+  const void* v_cache;  // bf16 pool, or e4m3 when fp8_v
   float* output;
   const int32_t* block_tables;
   const int32_t* seq_lens;
@@ -55,6 +56,8 @@ struct DecodeArgs {
   float inv_sqrt_d, k_scale;
   uint32_t q_stride, sliding_window;
   bool fp8;
+  bool fp8_v;     // V is E4M3 too (requires fp8), dequantised by v_scale
+  float v_scale;
   void* workspace;
   size_t workspace_bytes;
   bool workspace_fresh;  // registered since the last decode: its counters must be zeroed first

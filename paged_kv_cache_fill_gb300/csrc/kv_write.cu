@@ -1,8 +1,9 @@
-// Slot filling and the BF16 / V-only / FP8-K cache writes.
+// Slot filling and the BF16 / V-only / FP8-K / FP8 K+V cache writes.
 //
 // [kv_cache.rs] `fill_slots_from_block_table`, `reshape_and_cache` (BF16),
-// `reshape_and_cache_flash_v_only`; [kv_cache_fp8k.rs] module invariants
-// (K stored as k / k_scale in E4M3).
+// `reshape_and_cache_flash_v_only`, `reshape_and_cache_fp8` (K and V as
+// k / k_scale and v / v_scale in E4M3); [kv_cache_fp8k.rs] module
+// invariants (K stored as k / k_scale in E4M3).
 //
 // The writes are pure HBM streams: every token's row is read once and
 // written once. A warp owns one token at a time and moves its K and V rows as
@@ -110,10 +111,10 @@ cudaError_t launch_copy_rows(const uint16_t* src0, const uint16_t* src1, uint16_
   return cudaGetLastError();
 }
 
-// ------------------------------------------------------------ FP8-K write
-// K: 8 BF16 in (16 B) -> 8 E4M3 out (8 B) per vector; the quotient is the
-// IEEE binary32 division (correctly rounded), then one saturating RNE
-// conversion. V: 16-byte copy.
+// ------------------------------------------------------------ FP8 writes
+// K (and V when it is FP8 too): 8 BF16 in (16 B) -> 8 E4M3 out (8 B) per
+// vector; the quotient is the IEEE binary32 division (correctly rounded),
+// then one saturating RNE conversion. A BF16 V is a 16-byte copy.
 __device__ __forceinline__ uint2 encode8(uint4 k, float k_scale) {
   const uint32_t w[4] = {k.x, k.y, k.z, k.w};
   uint32_t out[2];
@@ -134,11 +135,13 @@ __device__ __forceinline__ uint8_t encode1(uint16_t k, float k_scale) {
   return uint8_t(f32x2_to_e4m3x2_satfinite(q, 0.0f) & 0xFF);
 }
 
-template <int kUnroll>
-__global__ void __launch_bounds__(256) write_fp8k_kernel(
+// kFp8V: V is quantised like K (v / v_scale, 16 B in -> 8 B out) instead of
+// copied.
+template <int kUnroll, bool kFp8V>
+__global__ void __launch_bounds__(256) write_fp8_kernel(
     const uint4* __restrict__ key, const uint4* __restrict__ value, uint2* __restrict__ k_cache,
-    uint4* __restrict__ v_cache, const int64_t* __restrict__ slot_mapping, uint32_t num_tokens,
-    uint32_t row_vecs, uint32_t kstride_vecs, uint32_t vstride_vecs, float k_scale) {
+    void* __restrict__ v_cache, const int64_t* __restrict__ slot_mapping, uint32_t num_tokens,
+    uint32_t row_vecs, uint32_t kstride_vecs, uint32_t vstride_vecs, float k_scale, float v_scale) {
   const uint32_t lane = threadIdx.x & 31;
   const uint32_t warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const uint32_t num_warps = (gridDim.x * blockDim.x) >> 5;
@@ -148,7 +151,6 @@ __global__ void __launch_bounds__(256) write_fp8k_kernel(
     const uint4* ks = key + size_t(t) * kstride_vecs;
     const uint4* vs = value + size_t(t) * vstride_vecs;
     uint2* kd = k_cache + size_t(slot) * row_vecs;
-    uint4* vd = v_cache + size_t(slot) * row_vecs;
     for (uint32_t base = lane; base < row_vecs; base += 32u * kUnroll) {
       uint4 a[kUnroll], b[kUnroll];
 #pragma unroll
@@ -164,7 +166,10 @@ __global__ void __launch_bounds__(256) write_fp8k_kernel(
         const uint32_t c = base + 32u * u;
         if (c < row_vecs) {
           kd[c] = encode8(a[u], k_scale);
-          vd[c] = b[u];
+          if constexpr (kFp8V)
+            static_cast<uint2*>(v_cache)[size_t(slot) * row_vecs + c] = encode8(b[u], v_scale);
+          else
+            static_cast<uint4*>(v_cache)[size_t(slot) * row_vecs + c] = b[u];
         }
       }
     }
@@ -172,11 +177,12 @@ __global__ void __launch_bounds__(256) write_fp8k_kernel(
 }
 
 // Unaligned fallback: one element per lane step.
-__global__ void __launch_bounds__(256) write_fp8k_scalar_kernel(
+template <bool kFp8V>
+__global__ void __launch_bounds__(256) write_fp8_scalar_kernel(
     const uint16_t* __restrict__ key, const uint16_t* __restrict__ value,
-    uint8_t* __restrict__ k_cache, uint16_t* __restrict__ v_cache,
+    uint8_t* __restrict__ k_cache, void* __restrict__ v_cache,
     const int64_t* __restrict__ slot_mapping, uint32_t num_tokens, uint32_t row_elems,
-    uint32_t key_stride, uint32_t value_stride, float k_scale) {
+    uint32_t key_stride, uint32_t value_stride, float k_scale, float v_scale) {
   const uint32_t lane = threadIdx.x & 31;
   const uint32_t warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const uint32_t num_warps = (gridDim.x * blockDim.x) >> 5;
@@ -184,31 +190,49 @@ __global__ void __launch_bounds__(256) write_fp8k_scalar_kernel(
     const int64_t slot = __ldg(slot_mapping + t);
     if (slot < 0) continue;
     for (uint32_t c = lane; c < row_elems; c += 32) {
-      k_cache[size_t(slot) * row_elems + c] = encode1(key[size_t(t) * key_stride + c], k_scale);
-      v_cache[size_t(slot) * row_elems + c] = value[size_t(t) * value_stride + c];
+      const size_t dst = size_t(slot) * row_elems + c;
+      k_cache[dst] = encode1(key[size_t(t) * key_stride + c], k_scale);
+      const uint16_t v = value[size_t(t) * value_stride + c];
+      if constexpr (kFp8V)
+        static_cast<uint8_t*>(v_cache)[dst] = encode1(v, v_scale);
+      else
+        static_cast<uint16_t*>(v_cache)[dst] = v;
     }
   }
 }
 
-cudaError_t launch_write_fp8k(const uint16_t* key, const uint16_t* value, uint8_t* k_cache_fp8,
-                              uint16_t* v_cache, const int64_t* slot_mapping, uint32_t num_tokens,
-                              uint32_t row_elems, uint32_t key_stride, uint32_t value_stride,
-                              float k_scale, cudaStream_t stream) {
+template <bool kFp8V>
+static void launch_write_fp8_t(bool vec, uint32_t blocks, cudaStream_t stream, const uint16_t* key,
+                               const uint16_t* value, uint8_t* k_cache_fp8, void* v_cache,
+                               const int64_t* slot_mapping, uint32_t num_tokens, uint32_t row_elems,
+                               uint32_t key_stride, uint32_t value_stride, float k_scale, float v_scale) {
+  if (vec)
+    write_fp8_kernel<4, kFp8V><<<blocks, 256, 0, stream>>>(
+        reinterpret_cast<const uint4*>(key), reinterpret_cast<const uint4*>(value),
+        reinterpret_cast<uint2*>(k_cache_fp8), v_cache, slot_mapping, num_tokens, row_elems / 8, key_stride / 8,
+        value_stride / 8, k_scale, v_scale);
+  else
+    write_fp8_scalar_kernel<kFp8V><<<blocks, 256, 0, stream>>>(key, value, k_cache_fp8, v_cache, slot_mapping,
+                                                               num_tokens, row_elems, key_stride, value_stride,
+                                                               k_scale, v_scale);
+}
+
+cudaError_t launch_write_fp8(const uint16_t* key, const uint16_t* value, uint8_t* k_cache_fp8, void* v_cache,
+                             bool fp8_v, const int64_t* slot_mapping, uint32_t num_tokens, uint32_t row_elems,
+                             uint32_t key_stride, uint32_t value_stride, float k_scale, float v_scale,
+                             cudaStream_t stream) {
   const DeviceInfo& dev = device_info();
   const uint32_t blocks = copy_grid(dev, num_tokens);
+  const uintptr_t v_align = fp8_v ? 7u : 15u;
   const bool vec = (row_elems % 8 == 0) && (key_stride % 8 == 0) && (value_stride % 8 == 0) &&
-                   aligned16(key) && aligned16(value) && aligned16(v_cache) &&
+                   aligned16(key) && aligned16(value) && (reinterpret_cast<uintptr_t>(v_cache) & v_align) == 0 &&
                    (reinterpret_cast<uintptr_t>(k_cache_fp8) & 7u) == 0;
-  if (vec) {
-    write_fp8k_kernel<4><<<blocks, 256, 0, stream>>>(
-        reinterpret_cast<const uint4*>(key), reinterpret_cast<const uint4*>(value),
-        reinterpret_cast<uint2*>(k_cache_fp8), reinterpret_cast<uint4*>(v_cache), slot_mapping,
-        num_tokens, row_elems / 8, key_stride / 8, value_stride / 8, k_scale);
-  } else {
-    write_fp8k_scalar_kernel<<<blocks, 256, 0, stream>>>(key, value, k_cache_fp8, v_cache,
-                                                         slot_mapping, num_tokens, row_elems,
-                                                         key_stride, value_stride, k_scale);
-  }
+  if (fp8_v)
+    launch_write_fp8_t<true>(vec, blocks, stream, key, value, k_cache_fp8, v_cache, slot_mapping, num_tokens,
+                             row_elems, key_stride, value_stride, k_scale, v_scale);
+  else
+    launch_write_fp8_t<false>(vec, blocks, stream, key, value, k_cache_fp8, v_cache, slot_mapping, num_tokens,
+                              row_elems, key_stride, value_stride, k_scale, v_scale);
   return cudaGetLastError();
 }
 

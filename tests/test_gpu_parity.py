@@ -151,6 +151,24 @@ def test_write_fp8k_exhaustive_over_bf16_patterns():
         assert np.array_equal(u16(vc), vr)
 
 
+@pytest.mark.parametrize("pad", [0, 8, 3])           # 3: unaligned rows take the scalar path
+def test_write_fp8_k_and_v_bit_exact(pad):
+    w, key, value, stride, slots_ref = _write_case(pad, seed=33)
+    H, D, bs, nb, n = w.num_kv_heads, w.head_dim, w.block_size, w.num_blocks, w.num_tokens
+    vstride = stride + (8 if pad != 3 else 5)         # K and V rows at different strides
+    value = torch.cat([value, torch.randn((n, vstride - stride), generator=torch.Generator().manual_seed(4))
+                       .to(torch.bfloat16)], 1).contiguous()
+    slots = torch.from_numpy(slots_ref).to(DEV)
+    for k_scale, v_scale in ((20.0 / 448.0, 4.5 / 448.0), (1.0, 1.0), (3.0e-3, 0.5)):
+        kc = kvgen.poisoned_pool(nb, bs, H, D, "fp8", DEV)
+        vc = kvgen.poisoned_pool(nb, bs, H, D, "fp8", DEV)
+        pk.kv_write_fp8(key.to(DEV), value.to(DEV), kc, vc, slots, n, H, D, bs, k_scale, v_scale, stride, vstride)
+        kr = np.full((nb, bs, H, D), kvgen.E4M3_NAN, np.uint8)
+        vr = kr.copy()
+        oracle.write_fp8(u16(key), u16(value), kr, vr, slots_ref, n, H, D, bs, k_scale, v_scale, stride, vstride)
+        assert np.array_equal(kc.cpu().numpy(), kr) and np.array_equal(vc.cpu().numpy(), vr), (k_scale, v_scale)
+
+
 def test_write_fp8k_workload_bit_exact():
     w = kvgen.custom(41, seq_lens=[300, 17, 1, 64], num_q_heads=8, num_kv_heads=8, head_dim=128,
                      block_size=16, fp8=True)
@@ -328,10 +346,21 @@ def test_fp8_fused_write_shapes_scales_and_saturation(D, R, inv_scale):
 # ---------------------------------------------------------------------------
 def _caches(w, fp8):
     """The same cache on both sides: the GPU write kernels fill the device
-    pools, the oracle's writes fill host pools."""
+    pools, the oracle's writes fill host pools. fp8: False (BF16 K and V),
+    True (FP8 K, BF16 V) or "kv" (FP8 K and V)."""
     H, D, bs, nb, n = w.num_kv_heads, w.head_dim, w.block_size, w.num_blocks, w.num_tokens
     slots_ref = oracle_slots(w)
     slots = gpu_slots(w)
+    if fp8 == "kv":
+        kc, vc = (kvgen.poisoned_pool(nb, bs, H, D, "fp8", DEV) for _ in range(2))
+        kr, vr = (np.full((nb, bs, H, D), kvgen.E4M3_NAN, np.uint8) for _ in range(2))
+        if n:
+            pk.kv_write_fp8(w.key.to(DEV), w.value.to(DEV), kc, vc, slots, n, H, D, bs, w.k_scale, w.v_scale,
+                            H * D, H * D)
+            oracle.write_fp8(u16(w.key), u16(w.value), kr, vr, slots_ref, n, H, D, bs, w.k_scale, w.v_scale,
+                             H * D, H * D)
+            assert np.array_equal(kc.cpu().numpy(), kr) and np.array_equal(vc.cpu().numpy(), vr)
+        return kc, vc, kr, vr
     vc = kvgen.poisoned_pool(nb, bs, H, D, "bf16", DEV)
     vr = np.full((nb, bs, H, D), kvgen.BF16_NAN, np.uint16)
     if fp8:
@@ -357,7 +386,9 @@ def _decode_gpu(w, kc, vc, window, fp8, q=None, q_stride=None):
     out = torch.full((w.num_seqs, w.num_q_heads, w.head_dim), float("nan"), device=DEV)
     args = (w.block_tables.to(DEV), w.seq_lens.to(DEV), w.max_blocks_per_seq, w.num_seqs, w.num_q_heads,
             w.num_kv_heads, w.head_dim, w.block_size, w.inv_sqrt_d)
-    if fp8:
+    if fp8 == "kv":
+        pk.paged_decode_attn_fp8(q.to(DEV), kc, vc, out, *args, w.k_scale, w.v_scale, q_stride, window)
+    elif fp8:
         pk.paged_decode_attn_fp8k(q.to(DEV), kc, vc, out, *args, w.k_scale, q_stride, window)
     else:
         pk.paged_decode_attn_bf16(q.to(DEV), kc, vc, out, *args, q_stride, window)
@@ -369,6 +400,8 @@ def _decode_ref(w, kr, vr, window, fp8, q=None, q_stride=None):
     q_stride = q_stride or w.num_q_heads * w.head_dim
     args = (w.block_tables.numpy(), w.seq_lens.numpy(), w.max_blocks_per_seq, w.num_seqs, w.num_q_heads,
             w.num_kv_heads, w.head_dim, w.block_size, w.inv_sqrt_d)
+    if fp8 == "kv":
+        return oracle.paged_decode_attn_fp8(u16(q), kr, vr, *args, w.k_scale, w.v_scale, q_stride, window)
     if fp8:
         return oracle.paged_decode_attn_fp8k(u16(q), kr, vr, *args, w.k_scale, q_stride, window)
     return oracle.paged_decode_attn_bf16(u16(q), kr, vr, *args, q_stride, window)
@@ -395,15 +428,15 @@ CASES = [
 ]
 
 
-@pytest.mark.parametrize("fp8", [False, True])
+@pytest.mark.parametrize("fp8", [False, True, "kv"])
 @pytest.mark.parametrize("case", range(len(CASES)))
 @pytest.mark.parametrize("split", [False, True])
 def test_decode_cases(fp8, case, split):
     lens, Hq, H, D, bs, windows = CASES[case]
     if fp8 and D == 64:
-        pytest.skip("FP8-K decode supports head_dim 128 and 256")
+        pytest.skip("the FP8 decodes support head_dim 128 and 256")
     w = kvgen.custom(100 + case, seq_lens=lens, num_q_heads=Hq, num_kv_heads=H, head_dim=D, block_size=bs,
-                     fp8=fp8)
+                     fp8=bool(fp8))
     kc, vc, kr, vr = _caches(w, fp8)
     with_workspace(w, split)
     for win in windows:
@@ -457,7 +490,10 @@ def _sampled_reference(w, rows, q_cpu, seqs, heads, window, fp8):
         table[i, :nb] = np.arange(cursor, cursor + nb, dtype=np.int32)
         cursor += nb
     pool_blocks = max(cursor, 1)
-    vr = np.full((pool_blocks, bs, H, D), kvgen.BF16_NAN, np.uint16)
+    if fp8 == "kv":
+        vr = np.full((pool_blocks, bs, H, D), kvgen.E4M3_NAN, np.uint8)
+    else:
+        vr = np.full((pool_blocks, bs, H, D), kvgen.BF16_NAN, np.uint16)
     kr = np.full((pool_blocks, bs, H, D), kvgen.E4M3_NAN if fp8 else kvgen.BF16_NAN,
                  np.uint8 if fp8 else np.uint16)
     for i, s in enumerate(seqs):
@@ -466,7 +502,9 @@ def _sampled_reference(w, rows, q_cpu, seqs, heads, window, fp8):
             continue
         sl = oracle.fill_slots(table[i], 0, L, bs)
         kk, vv = u16(rows[s][0]), u16(rows[s][1])
-        if fp8:
+        if fp8 == "kv":
+            oracle.write_fp8(kk, vv, kr, vr, sl, L, H, D, bs, w.k_scale, w.v_scale, H * D, H * D)
+        elif fp8:
             oracle.write_fp8k(kk, vv, kr, vr, sl, L, H, D, bs, H * D, H * D, w.k_scale)
         else:
             oracle.write_bf16(kk, vv, kr, vr, sl, L, H, D, bs, H * D, H * D)
@@ -475,21 +513,27 @@ def _sampled_reference(w, rows, q_cpu, seqs, heads, window, fp8):
     out = {}
     for i, s in enumerate(seqs):
         for h in heads:
-            out[(s, h)] = oracle.decode_one(qs, None if fp8 else kr, kr if fp8 else None, vr, table, sub_lens,
+            fp8_v = fp8 == "kv"
+            out[(s, h)] = oracle.decode_one(qs, None if fp8 else kr, kr if fp8 else None,
+                                            None if fp8_v else vr, table, sub_lens,
                                             mb, w.num_q_heads, H, D, bs, w.inv_sqrt_d, w.k_scale,
-                                            w.num_q_heads * D, window, i, h)
+                                            w.num_q_heads * D, window, i, h,
+                                            v_cache_fp8=vr if fp8_v else None, v_scale=w.v_scale)
     return out
 
 
 def _full_size(w, fp8, windows, sample_seqs, heads):
     H, D, bs, nb, n = w.num_kv_heads, w.head_dim, w.block_size, w.num_blocks, w.num_tokens
     slots = gpu_slots(w)
-    vc = kvgen.poisoned_pool(nb, bs, H, D, "bf16", DEV)
+    vc = kvgen.poisoned_pool(nb, bs, H, D, "fp8" if fp8 == "kv" else "bf16", DEV)
     kc = kvgen.poisoned_pool(nb, bs, H, D, "fp8" if fp8 else "bf16", DEV)
     chunk = 262144
     for t0 in range(0, n, chunk):
         t1 = min(n, t0 + chunk)
-        if fp8:
+        if fp8 == "kv":
+            pk.kv_write_fp8(w.key[t0:t1], w.value[t0:t1], kc, vc, slots[t0:t1], t1 - t0, H, D, bs, w.k_scale,
+                            w.v_scale, H * D, H * D)
+        elif fp8:
             pk.kv_write_fp8k(w.key[t0:t1], w.value[t0:t1], kc, vc, slots[t0:t1], t1 - t0, H, D, bs, H * D,
                              H * D, w.k_scale)
         else:
@@ -529,3 +573,15 @@ def test_full_fp8k_mixed_sampled():
     lens = w.seq_lens.cpu().numpy()
     seqs = sorted({int(lens.argmax()), int(lens.argmin()), 100, 200})
     _full_size(w, True, (0,), seqs, (0, 7, 8, 63))
+
+
+def test_full_fp8_kv_long_sampled():
+    w = kvgen.fp8k_long(device=DEV)
+    _full_size(w, "kv", (0, 4096), [0, 77, 127], (0, 5, 31))
+
+
+def test_full_fp8_kv_mixed_sampled():
+    w = kvgen.fp8k_mixed(device=DEV)
+    lens = w.seq_lens.cpu().numpy()
+    seqs = sorted({int(lens.argmax()), int(lens.argmin()), 100, 200})
+    _full_size(w, "kv", (0,), seqs, (0, 7, 8, 63))
