@@ -685,7 +685,7 @@ def dominant_roofline(step, dom, stream, peak, peak_kind, args):
         torch.cuda.synchronize()
         launches = reps * len(step.fp8_chunks)
         per_launch = statistics.mean((c1 - c0) * write_bytes_per_token(step.fp8_row, 1) for c0, c1 in step.fp8_chunks)
-        kernel = "kv_write_fp8k (write_fp8_kernel<4, false>)"
+        kernel = "kv_write_fp8k (write_fp8_kernel<4, false, true>)"
     else:
         a.record(stream)
         for _ in range(reps):

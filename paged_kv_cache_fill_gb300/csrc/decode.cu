@@ -138,6 +138,71 @@ struct Walker {
   }
 };
 
+// -------------------------------------------------------------- O^T += V^T P^T
+// One 16-token tile of the PV product for one warp: acc[i] holds the 16-dim
+// block i of O^T (8 query-head columns). B fragments (bh*, bl*) are the hi and
+// lo parts of P^T; kMask zeroes the V values of masked positions (their rows
+// may hold NaN), with vmask01 / vmask89 covering this lane's tokens 2c4, 2c4+1
+// and 2c4+8, 2c4+9.
+//   BF16 V: per 16-dim block one transposing ldmatrix (rows: 16 tokens).
+//   FP8 V: one transposing ldmatrix covers 32 dims x 16 tokens: matrix m holds
+//     tokens 8(m&1).. of 16-byte unit 2(jj&3)+(m>>1) and gives this lane the
+//     byte pairs (dims 2g8, 2g8+1) of tokens 2c4 and 2c4+1; one byte
+//     permutation regroups them by dim and each pair converts exactly to f16.
+//     A-row g8 is dim 2g8 and A-row g8+8 dim 2g8+1 of the 16-dim block, so
+//     the accumulator rows come out in that order too.
+template <bool kFp8V, int D, bool kMask>
+__device__ __forceinline__ void pv_tile(float (&acc)[D / 16][4], uint32_t vbase, uint32_t row, uint32_t unit_lo,
+                                        uint32_t bh0, uint32_t bh1, uint32_t bl0, uint32_t bl1, uint32_t vmask01,
+                                        uint32_t vmask89) {
+  if constexpr (!kFp8V) {
+#pragma unroll
+    for (int i = 0; i < D / 16; ++i) {
+      const uint32_t chunk = i >> 2;
+      const uint32_t unit = ((i & 3) << 1) + unit_lo;
+      uint32_t a[4];
+      ldmatrix_x4_trans(a, vbase + chunk * (kTile * 128) + row * 128 + ((unit ^ (row & 7)) << 4));
+      if constexpr (kMask) {
+        a[0] &= vmask01;
+        a[1] &= vmask01;
+        a[2] &= vmask89;
+        a[3] &= vmask89;
+      }
+      mma_bf16(acc[i], a, bh0, bh1);
+      mma_bf16(acc[i], a, bl0, bl1);
+    }
+  } else {
+#pragma unroll
+    for (int jj = 0; jj < D / 32; ++jj) {
+      const uint32_t chunk = jj >> 2;
+      const uint32_t unit = ((jj & 3) << 1) + unit_lo;
+      uint32_t r[4];
+      ldmatrix_x4_trans(r, vbase + chunk * (kTile * 128) + row * 128 + ((unit ^ (row & 7)) << 4));
+      uint32_t a[2][4];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        // bytes [t0 d0, t0 d1, t1 d0, t1 d1] -> [t0 d0, t1 d0, t0 d1, t1 d1]
+        const uint32_t w0 = __byte_perm(r[2 * h], 0u, 0x3120u);
+        const uint32_t w1 = __byte_perm(r[2 * h + 1], 0u, 0x3120u);
+        a[h][0] = e4m3x2_to_f16x2(uint16_t(w0));
+        a[h][1] = e4m3x2_to_f16x2(uint16_t(w0 >> 16));
+        a[h][2] = e4m3x2_to_f16x2(uint16_t(w1));
+        a[h][3] = e4m3x2_to_f16x2(uint16_t(w1 >> 16));
+        if constexpr (kMask) {
+          a[h][0] &= vmask01;
+          a[h][1] &= vmask01;
+          a[h][2] &= vmask89;
+          a[h][3] &= vmask89;
+        }
+      }
+      mma_f16(acc[2 * jj], a[0], bh0, bh1);
+      mma_f16(acc[2 * jj], a[0], bl0, bl1);
+      mma_f16(acc[2 * jj + 1], a[1], bh0, bh1);
+      mma_f16(acc[2 * jj + 1], a[1], bl0, bl1);
+    }
+  }
+}
+
 // -------------------------------------------------------------- the kernel
 template <bool kFp8, bool kFp8V, int D, int NT>
 __global__ void __launch_bounds__(32 * 9, 1)
@@ -450,20 +515,26 @@ __global__ void __launch_bounds__(32 * 9, 1)
         mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
       }
       const float mn0 = fmaxf(m_run[0], mx0), mn1 = fmaxf(m_run[1], mx1);
-      const float al0 = fast_exp2(m_run[0] - mn0), al1 = fast_exp2(m_run[1] - mn1);
+      // Rescale only when some column's running max moved (rare after the
+      // first tiles); with the max unchanged the factor would be exactly 1.
+      if (__any_sync(0xffffffffu, mn0 != m_run[0] || mn1 != m_run[1])) {
+        const float al0 = fast_exp2(m_run[0] - mn0), al1 = fast_exp2(m_run[1] - mn1);
+        l_run[0] *= al0;
+        l_run[1] *= al1;
+#pragma unroll
+        for (int i = 0; i < D / 16; ++i) {
+          acc[i][0] *= al0;
+          acc[i][1] *= al1;
+          acc[i][2] *= al0;
+          acc[i][3] *= al1;
+        }
+      }
       m_run[0] = mn0;
       m_run[1] = mn1;
       const float e0 = fast_exp2(s[0] - mn0), e1 = fast_exp2(s[1] - mn1);
       const float e2 = fast_exp2(s[2] - mn0), e3 = fast_exp2(s[3] - mn1);
-      l_run[0] = l_run[0] * al0 + (e0 + e2);
-      l_run[1] = l_run[1] * al1 + (e1 + e3);
-#pragma unroll
-      for (int i = 0; i < D / 16; ++i) {
-        acc[i][0] *= al0;
-        acc[i][1] *= al1;
-        acc[i][2] *= al0;
-        acc[i][3] *= al1;
-      }
+      l_run[0] += e0 + e2;
+      l_run[1] += e1 + e3;
       // V rows of masked positions may hold anything (NaN): zero them
       uint32_t vmask01 = 0xffffffffu, vmask89 = 0xffffffffu;
       if (boundary) {
@@ -472,61 +543,29 @@ __global__ void __launch_bounds__(32 * 9, 1)
         vmask01 = (ok(q0) ? 0x0000ffffu : 0u) | (ok(q0 + 1) ? 0xffff0000u : 0u);
         vmask89 = (ok(q0 + 8) ? 0x0000ffffu : 0u) | (ok(q0 + 9) ? 0xffff0000u : 0u);
       }
+      uint32_t bh0, bh1, bl0, bl1;
       if constexpr (!kFp8V) {
         // ---- P^T as B fragments: hi and lo BF16 parts, transposed by movmatrix
         const uint32_t hi01 = f32x2_to_bf16x2(e0, e1), hi23 = f32x2_to_bf16x2(e2, e3);
         const uint32_t lo01 = f32x2_to_bf16x2(e0 - bf16_lo_to_f32(hi01), e1 - bf16_hi_to_f32(hi01));
         const uint32_t lo23 = f32x2_to_bf16x2(e2 - bf16_lo_to_f32(hi23), e3 - bf16_hi_to_f32(hi23));
-        const uint32_t bh0 = movmatrix_trans(hi01), bh1 = movmatrix_trans(hi23);
-        const uint32_t bl0 = movmatrix_trans(lo01), bl1 = movmatrix_trans(lo23);
-        // ---- O^T += V^T P^T
-#pragma unroll
-        for (int i = 0; i < D / 16; ++i) {
-          const uint32_t chunk = i >> 2;
-          const uint32_t unit = ((i & 3) << 1) + v_unit;
-          uint32_t a[4];
-          ldmatrix_x4_trans(a, vbase + chunk * (kTile * 128) + v_row * 128 + ((unit ^ (v_row & 7)) << 4));
-          a[0] &= vmask01;
-          a[1] &= vmask01;
-          a[2] &= vmask89;
-          a[3] &= vmask89;
-          mma_bf16(acc[i], a, bh0, bh1);
-          mma_bf16(acc[i], a, bl0, bl1);
-        }
+        bh0 = movmatrix_trans(hi01), bh1 = movmatrix_trans(hi23);
+        bl0 = movmatrix_trans(lo01), bl1 = movmatrix_trans(lo23);
       } else {
         // ---- P^T as f16 hi + lo parts of 2^8 * P
         const float f0 = e0 * 256.0f, f1 = e1 * 256.0f, f2 = e2 * 256.0f, f3 = e3 * 256.0f;
         const uint32_t hi01 = f32x2_to_f16x2(f0, f1), hi23 = f32x2_to_f16x2(f2, f3);
         const uint32_t lo01 = f32x2_to_f16x2(f0 - f16_lo_to_f32(hi01), f1 - f16_hi_to_f32(hi01));
         const uint32_t lo23 = f32x2_to_f16x2(f2 - f16_lo_to_f32(hi23), f3 - f16_hi_to_f32(hi23));
-        const uint32_t bh0 = movmatrix_trans(hi01), bh1 = movmatrix_trans(hi23);
-        const uint32_t bl0 = movmatrix_trans(lo01), bl1 = movmatrix_trans(lo23);
-        // ---- O^T += V^T P^T. One transposing ldmatrix covers 32 dims x 16
-        // tokens: matrix m holds tokens 8(m&1).. of 16-byte unit 2(jj&3)+(m>>1)
-        // and gives this lane the byte pairs (dims 2g8, 2g8+1) of tokens 2c4
-        // and 2c4+1. A-row g8 is dim 2g8 and A-row g8+8 is dim 2g8+1 of the
-        // 16-dim block, so the accumulator rows come out in that order too.
-#pragma unroll
-        for (int jj = 0; jj < D / 32; ++jj) {
-          const uint32_t chunk = jj >> 2;
-          const uint32_t unit = ((jj & 3) << 1) + k_unit;
-          uint32_t r[4];
-          ldmatrix_x4_trans(r, vbase + chunk * (kTile * 128) + k_row * 128 + ((unit ^ (k_row & 7)) << 4));
-          uint32_t a0[4], a1[4];
-          a0[0] = e4m3x2_to_f16x2(uint16_t(__byte_perm(r[0], 0u, 0x0020u))) & vmask01;
-          a0[1] = e4m3x2_to_f16x2(uint16_t(__byte_perm(r[0], 0u, 0x0031u))) & vmask01;
-          a0[2] = e4m3x2_to_f16x2(uint16_t(__byte_perm(r[1], 0u, 0x0020u))) & vmask89;
-          a0[3] = e4m3x2_to_f16x2(uint16_t(__byte_perm(r[1], 0u, 0x0031u))) & vmask89;
-          a1[0] = e4m3x2_to_f16x2(uint16_t(__byte_perm(r[2], 0u, 0x0020u))) & vmask01;
-          a1[1] = e4m3x2_to_f16x2(uint16_t(__byte_perm(r[2], 0u, 0x0031u))) & vmask01;
-          a1[2] = e4m3x2_to_f16x2(uint16_t(__byte_perm(r[3], 0u, 0x0020u))) & vmask89;
-          a1[3] = e4m3x2_to_f16x2(uint16_t(__byte_perm(r[3], 0u, 0x0031u))) & vmask89;
-          mma_f16(acc[2 * jj], a0, bh0, bh1);
-          mma_f16(acc[2 * jj], a0, bl0, bl1);
-          mma_f16(acc[2 * jj + 1], a1, bh0, bh1);
-          mma_f16(acc[2 * jj + 1], a1, bl0, bl1);
-        }
+        bh0 = movmatrix_trans(hi01), bh1 = movmatrix_trans(hi23);
+        bl0 = movmatrix_trans(lo01), bl1 = movmatrix_trans(lo23);
       }
+      // ---- O^T += V^T P^T; only a tile with masked positions pays for the masks
+      const uint32_t vrow = kFp8V ? k_row : v_row, vunit = kFp8V ? k_unit : v_unit;
+      if (boundary)
+        pv_tile<kFp8V, D, true>(acc, vbase, vrow, vunit, bh0, bh1, bl0, bl1, vmask01, vmask89);
+      else
+        pv_tile<kFp8V, D, false>(acc, vbase, vrow, vunit, bh0, bh1, bl0, bl1, 0u, 0u);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[stage]);

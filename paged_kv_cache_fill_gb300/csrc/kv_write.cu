@@ -115,15 +115,50 @@ cudaError_t launch_copy_rows(const uint16_t* src0, const uint16_t* src1, uint16_
 // K (and V when it is FP8 too): 8 BF16 in (16 B) -> 8 E4M3 out (8 B) per
 // vector; the quotient is the IEEE binary32 division (correctly rounded),
 // then one saturating RNE conversion. A BF16 V is a 16-byte copy.
-__device__ __forceinline__ uint2 encode8(uint4 k, float k_scale) {
+//
+// The correctly rounded quotient comes from one of two routes. The exact
+// division __fdiv_rn works for any scale. The division-free route is for
+// scales s in [2^-60, 2^60]. It takes y = RN(1/s) once per thread
+// (__frcp_rn), q0 = RN(x*y), and two residual corrections
+// q' = RN(q + RN(x - s*q)*y); each residual is exact by FMA.
+// The first correction leaves q1 within one ulp of x/s, since its error
+// before rounding is |q0 - x/s| * |1 - s*y| <= 2^-24 |q0 - x/s|. From q1,
+// Markstein's theorem gives RN(x/s) exactly, provided no intermediate
+// underflows or overflows (P. Markstein, "Computation of elementary functions
+// on the IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990;
+// J.-M. Muller et al., Handbook of Floating-Point Arithmetic, division with
+// an FMA). That holds while |q0| lies in [2^-20, 2^20] and s in
+// [2^-60, 2^60]. Outside that range of |q0| the quotient is below 2^-10 or
+// above 448, so q0 gives the same E4M3 code (+-0, or +-448 when
+// saturated), as do NaN and infinite inputs.
+constexpr float kFastScaleMin = 0x1p-60f, kFastScaleMax = 0x1p60f;
+
+__device__ __forceinline__ float quotient_rn(float x, float s, float y) {
+  const float q0 = __fmul_rn(x, y);
+  const float q1 = __fmaf_rn(__fmaf_rn(-q0, s, x), y, q0);
+  const float q2 = __fmaf_rn(__fmaf_rn(-q1, s, x), y, q1);
+  const float a = fabsf(q0);
+  return (a >= 0x1p-20f && a <= 0x1p20f) ? q2 : q0;
+}
+
+template <bool kFast>
+__device__ __forceinline__ float quotient(float x, float s, float y) {
+  if constexpr (kFast)
+    return quotient_rn(x, s, y);
+  else
+    return __fdiv_rn(x, s);
+}
+
+template <bool kFast>
+__device__ __forceinline__ uint2 encode8(uint4 k, float scale, float recip) {
   const uint32_t w[4] = {k.x, k.y, k.z, k.w};
   uint32_t out[2];
 #pragma unroll
   for (int j = 0; j < 2; ++j) {
-    const float q0 = __fdiv_rn(bf16_lo_to_f32(w[2 * j]), k_scale);
-    const float q1 = __fdiv_rn(bf16_hi_to_f32(w[2 * j]), k_scale);
-    const float q2 = __fdiv_rn(bf16_lo_to_f32(w[2 * j + 1]), k_scale);
-    const float q3 = __fdiv_rn(bf16_hi_to_f32(w[2 * j + 1]), k_scale);
+    const float q0 = quotient<kFast>(bf16_lo_to_f32(w[2 * j]), scale, recip);
+    const float q1 = quotient<kFast>(bf16_hi_to_f32(w[2 * j]), scale, recip);
+    const float q2 = quotient<kFast>(bf16_lo_to_f32(w[2 * j + 1]), scale, recip);
+    const float q3 = quotient<kFast>(bf16_hi_to_f32(w[2 * j + 1]), scale, recip);
     out[j] = uint32_t(f32x2_to_e4m3x2_satfinite(q0, q1)) |
              (uint32_t(f32x2_to_e4m3x2_satfinite(q2, q3)) << 16);
   }
@@ -136,12 +171,14 @@ __device__ __forceinline__ uint8_t encode1(uint16_t k, float k_scale) {
 }
 
 // kFp8V: V is quantised like K (v / v_scale, 16 B in -> 8 B out) instead of
-// copied.
-template <int kUnroll, bool kFp8V>
+// copied. kFast: the division-free quotient (both scales in its range).
+template <int kUnroll, bool kFp8V, bool kFast>
 __global__ void __launch_bounds__(256) write_fp8_kernel(
     const uint4* __restrict__ key, const uint4* __restrict__ value, uint2* __restrict__ k_cache,
     void* __restrict__ v_cache, const int64_t* __restrict__ slot_mapping, uint32_t num_tokens,
     uint32_t row_vecs, uint32_t kstride_vecs, uint32_t vstride_vecs, float k_scale, float v_scale) {
+  const float k_recip = kFast ? __frcp_rn(k_scale) : 0.0f;
+  const float v_recip = kFast ? __frcp_rn(v_scale) : 0.0f;
   const uint32_t lane = threadIdx.x & 31;
   const uint32_t warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const uint32_t num_warps = (gridDim.x * blockDim.x) >> 5;
@@ -165,9 +202,9 @@ __global__ void __launch_bounds__(256) write_fp8_kernel(
       for (int u = 0; u < kUnroll; ++u) {
         const uint32_t c = base + 32u * u;
         if (c < row_vecs) {
-          kd[c] = encode8(a[u], k_scale);
+          kd[c] = encode8<kFast>(a[u], k_scale, k_recip);
           if constexpr (kFp8V)
-            static_cast<uint2*>(v_cache)[size_t(slot) * row_vecs + c] = encode8(b[u], v_scale);
+            static_cast<uint2*>(v_cache)[size_t(slot) * row_vecs + c] = encode8<kFast>(b[u], v_scale, v_recip);
           else
             static_cast<uint4*>(v_cache)[size_t(slot) * row_vecs + c] = b[u];
         }
@@ -206,8 +243,15 @@ static void launch_write_fp8_t(bool vec, uint32_t blocks, cudaStream_t stream, c
                                const uint16_t* value, uint8_t* k_cache_fp8, void* v_cache,
                                const int64_t* slot_mapping, uint32_t num_tokens, uint32_t row_elems,
                                uint32_t key_stride, uint32_t value_stride, float k_scale, float v_scale) {
-  if (vec)
-    write_fp8_kernel<4, kFp8V><<<blocks, 256, 0, stream>>>(
+  auto in_fast_range = [](float sc) { return sc >= kFastScaleMin && sc <= kFastScaleMax; };
+  const bool fast = in_fast_range(k_scale) && (!kFp8V || in_fast_range(v_scale));
+  if (vec && fast)
+    write_fp8_kernel<4, kFp8V, true><<<blocks, 256, 0, stream>>>(
+        reinterpret_cast<const uint4*>(key), reinterpret_cast<const uint4*>(value),
+        reinterpret_cast<uint2*>(k_cache_fp8), v_cache, slot_mapping, num_tokens, row_elems / 8, key_stride / 8,
+        value_stride / 8, k_scale, v_scale);
+  else if (vec)
+    write_fp8_kernel<4, kFp8V, false><<<blocks, 256, 0, stream>>>(
         reinterpret_cast<const uint4*>(key), reinterpret_cast<const uint4*>(value),
         reinterpret_cast<uint2*>(k_cache_fp8), v_cache, slot_mapping, num_tokens, row_elems / 8, key_stride / 8,
         value_stride / 8, k_scale, v_scale);

@@ -128,9 +128,23 @@ def test_write_bf16_and_v_only_bit_exact(pad):
     assert np.array_equal(u16(v2), vr)
 
 
+def _scales_to_sweep():
+    """Scales for the exhaustive FP8 tests: workload-like ones, 48 seeded
+    log-uniform ones over [2^-60, 2^60] (the division-free quotient's range),
+    significands of all ones and of 1 + 2^-23 (the hardest reciprocals), the
+    range ends, and scales outside it (the exact-division route)."""
+    rng = np.random.default_rng(77)
+    sweep = [1.0, 20.0 / 448.0, 3.0e-3, 5.5 / 448.0]
+    sweep += list(2.0 ** rng.uniform(-60, 60, 48))
+    for e in (-60, -31, -7, 0, 9, 59):
+        sweep += [np.nextafter(np.float32(2.0 ** (e + 1)), np.float32(0)), np.float32(2.0 ** e) * np.float32(1 + 2**-23)]
+    sweep += [2.0 ** -60, 2.0 ** 60, 2.0 ** -61, 2.0 ** 61, 1e-30, 3e25, 1e-40]
+    return [float(np.float32(x)) for x in sweep]
+
+
 def test_write_fp8k_exhaustive_over_bf16_patterns():
-    """All 65536 BF16 bit patterns as K (64 tokens x 1024), at k_scale 1 and
-    at a workload-like scale."""
+    """All 65536 BF16 bit patterns as K (64 tokens x 1024), over the scale
+    sweep: bit-exact codes on both quotient routes."""
     H, D, bs = 8, 128, 16
     n = 64
     pats = np.arange(65536, dtype=np.uint32).astype(np.uint16).reshape(n, H * D)
@@ -138,7 +152,7 @@ def test_write_fp8k_exhaustive_over_bf16_patterns():
     value = torch.randn((n, H * D), generator=torch.Generator().manual_seed(2)).to(torch.bfloat16)
     slots_ref = np.arange(n, dtype=np.int64)[::-1].copy()
     slots = torch.from_numpy(slots_ref).to(DEV)
-    for k_scale in (1.0, 20.0 / 448.0, 3.0e-3):
+    for k_scale in _scales_to_sweep():
         kc = kvgen.poisoned_pool(n // bs, bs, H, D, "fp8", DEV)
         vc = kvgen.poisoned_pool(n // bs, bs, H, D, "bf16", DEV)
         pk.kv_write_fp8k(key.to(DEV), value.to(DEV), kc, vc, slots, n, H, D, bs, H * D, H * D, k_scale)
@@ -167,6 +181,28 @@ def test_write_fp8_k_and_v_bit_exact(pad):
         vr = kr.copy()
         oracle.write_fp8(u16(key), u16(value), kr, vr, slots_ref, n, H, D, bs, k_scale, v_scale, stride, vstride)
         assert np.array_equal(kc.cpu().numpy(), kr) and np.array_equal(vc.cpu().numpy(), vr), (k_scale, v_scale)
+
+
+def test_write_fp8_v_exhaustive_over_bf16_patterns():
+    """All 65536 BF16 bit patterns as V of the FP8 K+V write, with K and V
+    scales from the sweep (paired so that some calls mix the two routes)."""
+    H, D, bs = 8, 128, 16
+    n = 64
+    pats = np.arange(65536, dtype=np.uint32).astype(np.uint16).reshape(n, H * D)
+    value = torch.from_numpy(pats.view(np.int16)).view(torch.bfloat16)
+    key = torch.from_numpy(np.ascontiguousarray(pats[::-1]).view(np.int16)).view(torch.bfloat16)
+    slots_ref = np.arange(n, dtype=np.int64)
+    slots = torch.from_numpy(slots_ref).to(DEV)
+    sweep = _scales_to_sweep()
+    for k_scale, v_scale in zip(sweep, sweep[7:] + sweep[:7]):
+        kc = kvgen.poisoned_pool(n // bs, bs, H, D, "fp8", DEV)
+        vc = kvgen.poisoned_pool(n // bs, bs, H, D, "fp8", DEV)
+        pk.kv_write_fp8(key.to(DEV), value.to(DEV), kc, vc, slots, n, H, D, bs, k_scale, v_scale, H * D, H * D)
+        kr = np.full((n // bs, bs, H, D), kvgen.E4M3_NAN, np.uint8)
+        vr = kr.copy()
+        oracle.write_fp8(u16(key), u16(value), kr, vr, slots_ref, n, H, D, bs, k_scale, v_scale, H * D, H * D)
+        assert np.array_equal(kc.cpu().numpy(), kr), (k_scale, v_scale)
+        assert np.array_equal(vc.cpu().numpy(), vr), (k_scale, v_scale)
 
 
 def test_write_fp8k_workload_bit_exact():
