@@ -396,21 +396,19 @@ static double value_at(const uint16_t *v_cache_bf16, const uint8_t *v_cache_fp8,
     return oracle_bf16_to_f64(v_cache_bf16[idx]);
 }
 
-/* k_cache_fp8 != NULL selects the FP8-K cache (k_cache_bf16 is then unused);
- * v_cache_fp8 != NULL likewise selects an FP8 V cache (v_cache unused).
- * out receives head_dim values. weights, when not NULL, has room for
- * seq_lens[s] values and receives the softmax weight of each position
- * (0 for positions outside the window). head_dim is at most 1024. */
-void oracle_decode_one(const uint16_t *q, const uint16_t *k_cache_bf16, const uint8_t *k_cache_fp8,
-                       const uint16_t *v_cache, const uint8_t *v_cache_fp8,
-                       const int32_t *block_tables, const int32_t *seq_lens,
-                       uint32_t max_blocks_per_seq, uint32_t num_q_heads, uint32_t num_kv_heads,
-                       uint32_t head_dim, uint32_t block_size, float inv_sqrt_d, float k_scale,
-                       float v_scale, uint32_t q_stride, uint32_t sliding_window, uint32_t s,
-                       uint32_t h, double *out, double *weights) {
-    uint32_t group = num_q_heads / num_kv_heads;
-    uint32_t kv_head = h / group;
-    int64_t L = seq_lens[s];
+/* The attention of one query row over positions [start, L) of one sequence,
+ * start = max(0, L - sliding_window) when sliding_window > 0, else 0:
+ * q_row is the query head's head_dim BF16 values and table the sequence's
+ * block-table row. k_cache_fp8 != NULL selects the FP8-K cache (k_cache_bf16
+ * is then unused); v_cache_fp8 != NULL likewise selects an FP8 V cache
+ * (v_cache unused). out receives head_dim values. weights, when not NULL,
+ * has room for L values and receives the softmax weight of each position (0
+ * for positions outside the window). head_dim is at most 1024. */
+static void attend(const uint16_t *q_row, const uint16_t *k_cache_bf16, const uint8_t *k_cache_fp8,
+                   const uint16_t *v_cache, const uint8_t *v_cache_fp8, const int32_t *table,
+                   int64_t L, uint32_t num_kv_heads, uint32_t kv_head, uint32_t head_dim,
+                   uint32_t block_size, float inv_sqrt_d, float k_scale, float v_scale,
+                   uint32_t sliding_window, double *out, double *weights) {
     int64_t start = 0;
     if (sliding_window > 0 && L > (int64_t)sliding_window) start = L - sliding_window;
     for (uint32_t d = 0; d < head_dim; ++d) out[d] = 0.0;
@@ -419,7 +417,7 @@ void oracle_decode_one(const uint16_t *q, const uint16_t *k_cache_bf16, const ui
 
     double qv[1024], acc[1024];
     for (uint32_t d = 0; d < head_dim; ++d) {
-        qv[d] = oracle_bf16_to_f64(q[(int64_t)s * q_stride + (int64_t)h * head_dim + d]);
+        qv[d] = oracle_bf16_to_f64(q_row[d]);
         acc[d] = 0.0;
     }
     double *scores = (double *)malloc((size_t)(L - start) * sizeof(double));
@@ -428,7 +426,7 @@ void oracle_decode_one(const uint16_t *q, const uint16_t *k_cache_bf16, const ui
     /* pass 1: walk the block table and score every attended position */
     double max_score = -INFINITY;
     for (int64_t p = start; p < L; ++p) {
-        int64_t block = block_tables[(int64_t)s * max_blocks_per_seq + p / block_size];
+        int64_t block = table[p / block_size];
         int64_t slot = block * (int64_t)block_size + p % block_size;
         double dot = 0.0;
         for (uint32_t d = 0; d < head_dim; ++d)
@@ -456,6 +454,23 @@ void oracle_decode_one(const uint16_t *q, const uint16_t *k_cache_bf16, const ui
     for (int64_t p = start; weights && p < L; ++p) weights[p] = scores[p - start] / denom;
     free(scores);
     free(slots);
+}
+
+/* Decode: the one query of sequence s (at position seq_lens[s] - 1) for
+ * query head h, whose KV head is h / (num_q_heads / num_kv_heads). */
+void oracle_decode_one(const uint16_t *q, const uint16_t *k_cache_bf16, const uint8_t *k_cache_fp8,
+                       const uint16_t *v_cache, const uint8_t *v_cache_fp8,
+                       const int32_t *block_tables, const int32_t *seq_lens,
+                       uint32_t max_blocks_per_seq, uint32_t num_q_heads, uint32_t num_kv_heads,
+                       uint32_t head_dim, uint32_t block_size, float inv_sqrt_d, float k_scale,
+                       float v_scale, uint32_t q_stride, uint32_t sliding_window, uint32_t s,
+                       uint32_t h, double *out, double *weights) {
+    uint32_t group = num_q_heads / num_kv_heads;
+    uint32_t kv_head = h / group;
+    attend(q + (int64_t)s * q_stride + (int64_t)h * head_dim, k_cache_bf16, k_cache_fp8, v_cache,
+           v_cache_fp8, block_tables + (int64_t)s * max_blocks_per_seq, seq_lens[s], num_kv_heads,
+           kv_head, head_dim, block_size, inv_sqrt_d, k_scale, v_scale, sliding_window, out,
+           weights);
 }
 
 static void decode_all(const uint16_t *q, const uint16_t *k_cache_bf16, const uint8_t *k_cache_fp8,
@@ -513,6 +528,45 @@ void oracle_paged_decode_attn_fp8(const uint16_t *q, const uint8_t *k_cache_fp8,
     decode_all(q, 0, k_cache_fp8, 0, v_cache_fp8, output, block_tables, seq_lens,
                max_blocks_per_seq, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
                inv_sqrt_d, k_scale, v_scale, q_stride, sliding_window);
+}
+
+/* ------------------------------------------------------------------------
+ * Multi-token (chunked-prefill) paged attention. [kv_cache.rs] "Batched
+ * prefill variants (N tokens)" (a heading only): sequence s brings
+ * n_s = query_start_loc[s + 1] - query_start_loc[s] query tokens, the last n_s
+ * of its seq_lens[s] cached positions. Query j (row query_start_loc[s] + j of
+ * q, at position P = seq_lens[s] - n_s + j) attends causally: positions
+ * [start, P] with start = max(0, P + 1 - sliding_window) when
+ * sliding_window > 0, else 0 -- exactly what a decode of that sequence
+ * truncated to length P + 1 attends. A query with P < 0 (n_s > seq_lens[s])
+ * attends nothing and gives zeros. Output float32
+ * [num_q_tokens, num_q_heads, head_dim]. k_cache_fp8 != NULL selects the
+ * FP8-K cache (k_scale as in the FP8-K decode).
+ * ---------------------------------------------------------------------- */
+void oracle_paged_prefill_attn(const uint16_t *q, const uint16_t *k_cache_bf16,
+                               const uint8_t *k_cache_fp8, const uint16_t *v_cache, float *output,
+                               const int32_t *block_tables, const int32_t *seq_lens,
+                               const int32_t *query_start_loc, uint32_t max_blocks_per_seq,
+                               uint32_t num_seqs, uint32_t num_q_heads, uint32_t num_kv_heads,
+                               uint32_t head_dim, uint32_t block_size, float inv_sqrt_d,
+                               float k_scale, uint32_t q_stride, uint32_t sliding_window) {
+    double out[1024];
+    uint32_t group = num_q_heads / num_kv_heads;
+    for (uint32_t s = 0; s < num_seqs; ++s) {
+        int64_t n = (int64_t)query_start_loc[s + 1] - query_start_loc[s];
+        for (int64_t j = 0; j < n; ++j) {
+            int64_t row = query_start_loc[s] + j;
+            int64_t position = (int64_t)seq_lens[s] - n + j;
+            for (uint32_t h = 0; h < num_q_heads; ++h) {
+                attend(q + row * q_stride + (int64_t)h * head_dim, k_cache_bf16, k_cache_fp8,
+                       v_cache, 0, block_tables + (int64_t)s * max_blocks_per_seq, position + 1,
+                       num_kv_heads, h / group, head_dim, block_size, inv_sqrt_d, k_scale, 1.0f,
+                       sliding_window, out, 0);
+                for (uint32_t d = 0; d < head_dim; ++d)
+                    output[(row * num_q_heads + h) * head_dim + d] = (float)out[d];
+            }
+        }
+    }
 }
 
 /* ------------------------------------------------------------------------

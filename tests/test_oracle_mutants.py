@@ -41,6 +41,9 @@ MUTANTS = {
     "mrope_index": ("double angle = pos3[i % 3] * inv_freq;", "double angle = pos3[(i / 3) % 3] * inv_freq;"),
     "fp8_fused_no_scale": ("oracle_e4m3_encode_f64(out[d] * (double)inv_scale);",
                            "oracle_e4m3_encode_f64(out[d]);"),
+    "prefill_position_off_by_one": ("int64_t position = (int64_t)seq_lens[s] - n + j;",
+                                    "int64_t position = (int64_t)seq_lens[s] - n + j + 1;"),
+    "prefill_not_causal": ("max_blocks_per_seq, position + 1,", "max_blocks_per_seq, (int64_t)seq_lens[s],"),
     "softmax_unnormalised": ("for (uint32_t d = 0; d < head_dim; ++d) out[d] = acc[d] / denom;",
                              "for (uint32_t d = 0; d < head_dim; ++d) out[d] = acc[d];"),
 }

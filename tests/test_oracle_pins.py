@@ -561,6 +561,106 @@ def test_fp8_v_decode_equals_bf16_v_decode_of_the_dequantised_rows(oracle_lib):
 
 
 # ---------------------------------------------------------------------------
+# multi-token (chunked-prefill) paged attention (kv_cache.rs, "Batched prefill
+# variants (N tokens)")
+# ---------------------------------------------------------------------------
+def _prefill_case(seed, lens, qlens, fp8, Hq=8, H=2, D=32, bs=16):
+    w = kvgen.custom(seed, seq_lens=lens, num_q_heads=Hq, num_kv_heads=H, head_dim=D, block_size=bs, fp8=fp8,
+                     q_rows=max(sum(qlens), 1))
+    qsl = np.concatenate([[0], np.cumsum(qlens)]).astype(np.int32)
+    return w, qsl
+
+
+def _prefill(oracle_lib, w, kc, vc, qsl, window, fp8, seq_lens=None, q=None):
+    seq_lens = w.seq_lens.numpy() if seq_lens is None else seq_lens
+    q = _rows(w.q) if q is None else q
+    return oracle_lib.paged_prefill_attn(q, None if fp8 else kc, kc if fp8 else None, vc, w.block_tables.numpy(),
+                                         np.ascontiguousarray(seq_lens, dtype=np.int32), qsl, w.max_blocks_per_seq,
+                                         w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size,
+                                         w.inv_sqrt_d, w.k_scale, w.num_q_heads * w.head_dim, window)
+
+
+def _dense_causal(w, kc, vc, qsl, s, window, fp8):
+    """torch's scaled_dot_product_attention in float64 over the sequence's
+    gathered rows, with the causal window as an explicit boolean mask."""
+    L = int(w.seq_lens[s])
+    n = int(qsl[s + 1] - qsl[s])
+    bs, H, D, Hq = w.block_size, w.num_kv_heads, w.head_dim, w.num_q_heads
+    p = np.arange(L)
+    blocks = w.block_tables[s].numpy()[p // bs]
+    if fp8:
+        k = torch.from_numpy(kc[blocks, p % bs]).view(torch.float8_e4m3fn).to(torch.float64) * w.k_scale
+    else:
+        k = torch.from_numpy(kc[blocks, p % bs].view(np.int16)).view(torch.bfloat16).to(torch.float64)
+    v = torch.from_numpy(vc[blocks, p % bs].view(np.int16)).view(torch.bfloat16).to(torch.float64)
+    q = w.q[int(qsl[s]):int(qsl[s + 1])].view(n, Hq, D).permute(1, 0, 2).to(torch.float64)   # [Hq, n, D]
+    g = Hq // H
+    k = k.permute(1, 0, 2).repeat_interleave(g, 0)
+    v = v.permute(1, 0, 2).repeat_interleave(g, 0)
+    pos = torch.arange(L - n, L)[:, None]
+    keys = torch.arange(L)[None, :]
+    mask = keys <= pos
+    if window:
+        mask &= keys > pos - window
+    o = torch.nn.functional.scaled_dot_product_attention(q, k, v, attn_mask=mask[None],
+                                                         scale=float(np.float32(w.inv_sqrt_d)))
+    return o.permute(1, 0, 2).numpy()                                                      # [n, Hq, D]
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+@pytest.mark.parametrize("window", [0, 1, 7, 50])
+def test_prefill_equals_dense_causal_attention(oracle_lib, fp8, window):
+    lens, qlens = [37, 100, 1, 16, 64], [5, 37, 1, 16, 1]
+    w, qsl = _prefill_case(31, lens, qlens, fp8)
+    kc, vc = _oracle_cache(oracle_lib, w, fp8)
+    out = _prefill(oracle_lib, w, kc, vc, qsl, window, fp8)
+    for s in range(w.num_seqs):
+        ref = _dense_causal(w, kc, vc, qsl, s, window, fp8)
+        np.testing.assert_allclose(out[qsl[s]:qsl[s + 1]], ref, rtol=2.0 ** -24, atol=1e-30)
+
+
+def test_prefill_last_query_is_the_decode_of_its_row(oracle_lib):
+    lens, qlens = [37, 100, 16], [4, 9, 16]
+    w, qsl = _prefill_case(32, lens, qlens, False)
+    kc, vc = _oracle_cache(oracle_lib, w)
+    out = _prefill(oracle_lib, w, kc, vc, qsl, 0, False)
+    q = _rows(w.q)
+    for s in range(w.num_seqs):
+        last = q[qsl[s + 1] - 1][None].repeat(w.num_seqs, 0)       # that row as every sequence's query
+        dec = oracle_lib.paged_decode_attn_bf16(np.ascontiguousarray(last), kc, vc, w.block_tables.numpy(),
+                                                w.seq_lens.numpy(), w.max_blocks_per_seq, w.num_seqs,
+                                                w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size,
+                                                w.inv_sqrt_d, w.num_q_heads * w.head_dim, 0)
+        assert np.array_equal(out[qsl[s + 1] - 1], dec[s])
+
+
+def test_prefill_chunk_split_in_two_calls_gives_the_same_rows(oracle_lib):
+    # causal attention: query j's output depends only on positions <= its own,
+    # so the first part of a chunk, run with the cache length cut back to its
+    # last position, reproduces those rows exactly
+    lens, qlens = [90, 40], [30, 17]
+    w, qsl = _prefill_case(33, lens, qlens, True)
+    kc, vc = _oracle_cache(oracle_lib, w, True)
+    full = _prefill(oracle_lib, w, kc, vc, qsl, 20, True)
+    first = [12, 5]
+    q = _rows(w.q)
+    q1 = np.ascontiguousarray(np.concatenate([q[qsl[s]:qsl[s] + first[s]] for s in range(2)]))
+    qsl1 = np.array([0, first[0], first[0] + first[1]], np.int32)
+    lens1 = np.array([lens[s] - qlens[s] + first[s] for s in range(2)], np.int32)
+    part = _prefill(oracle_lib, w, kc, vc, qsl1, 20, True, seq_lens=lens1, q=q1)
+    want = np.concatenate([full[qsl[s]:qsl[s] + first[s]] for s in range(2)])
+    assert np.array_equal(part, want)
+
+
+def test_prefill_queries_before_position_zero_give_zeros(oracle_lib):
+    lens, qlens = [3, 10], [5, 2]                # sequence 0 has more queries than positions
+    w, qsl = _prefill_case(34, lens, qlens, False)
+    kc, vc = _oracle_cache(oracle_lib, w)
+    out = _prefill(oracle_lib, w, kc, vc, qsl, 0, False)
+    assert not out[:2].any() and np.isfinite(out).all() and out[2:5].any()
+
+
+# ---------------------------------------------------------------------------
 # next rows: MRoPE-interleaved fused write and the FP8-output fused write
 # (kv_cache.rs, fused_k_norm_rope_cache_write_bf16_mrope / _fp8)
 # ---------------------------------------------------------------------------
