@@ -14,8 +14,12 @@ One step is one pass of every timed call of the five synthetic workloads
                      (log-uniform), GQA 64:8, block_size 64, split-KV
 Beside the step, and not in it ("next_rows"), with L2 flushed before each
 launch: the FP8-output and the MRoPE variants of the fused K write on the
-fused_write tokens, and the FP8 K+V cache (kv_write_fp8 of the fp8k_long
-tokens, paged_decode_attn_fp8 of fp8k_long at W = 0 and of fp8k_mixed).
+fused_write tokens; the FP8 K+V cache (kv_write_fp8 of the fp8k_long tokens,
+paged_decode_attn_fp8 of fp8k_long at W = 0 and of fp8k_mixed); and chunked
+prefill attention (paged_prefill_attn_bf16 over the bf16_gqa4 cache and
+paged_prefill_attn_fp8k over the first 32 fp8k_mixed sequences, the last
+min(256, L) positions of each sequence as causal queries), reported in
+TFLOP/s against the measured BF16 tensor peak.
 The headline value is the step's algorithmic HBM bytes (what each call must
 read and write, counted per call below) divided by the step time, in GB/s;
 each call's GB/s, tokens/s and fraction of the measured HBM copy rate are
@@ -29,6 +33,7 @@ a bounded sample of the same workloads on the host cores.
 from __future__ import annotations
 
 import argparse
+import itertools
 import json
 import math
 import os
@@ -43,6 +48,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "paged-decode KV-read GB/s & cache-write tokens/s, % of GB300 HBM peak"
 NOMINAL_HBM_GBS = 8000.0
+FALLBACK_BF16_TFLOPS = 1900.0  # one earlier GB300 measurement (burst)
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -52,6 +58,27 @@ def measured_peak():
             return float(json.load(f)["hbm_gbs"]), "measured"
     except Exception:  # noqa: BLE001 - the file is optional
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def measured_bf16_tflops():
+    """Dense BF16 tensor peak (burst: the prefill calls are timed alone)."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:  # noqa: BLE001 - the file is optional
+        return FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def prefill_flops(seq_lens, q_lens, window, num_q_heads, head_dim):
+    """4 * Hq * D per attended (query, key) pair: QK^T and PV, 2 flops per MAC."""
+    pairs = 0
+    for L, n in zip(seq_lens, q_lens):
+        for j in range(int(n)):
+            P = int(L) - int(n) + j
+            if P < 0:
+                continue
+            pairs += min(P + 1, window) if window else P + 1
+    return 4 * num_q_heads * head_dim * pairs
 
 
 # ---------------------------------------------------------------------------
@@ -135,7 +162,8 @@ WORKLOAD_OF_PART = {"fused_write": "fused", "bf16_prefill": "bf16_gqa4", "bf16_d
                     # calls timed beside the step
                     "fused_k_write_fp8": "fused", "fused_k_write_mrope": "fused",
                     "fp8_kv_prefill": "fp8k_long", "fp8_kv_decode_w0": "fp8k_long",
-                    "fp8_kv_mixed_decode": "fp8k_mixed"}
+                    "fp8_kv_mixed_decode": "fp8k_mixed", "bf16_chunked_prefill": "bf16_gqa4",
+                    "fp8k_chunked_prefill": "fp8k_mixed"}
 
 
 class GpuStep:
@@ -296,6 +324,22 @@ class GpuStep:
         self.inputs_h2d += [key, value, q, tables, lens]
         self.outputs_d2h += [out]
 
+        # chunked prefill over the same cache, timed beside the step: each
+        # sequence's last min(256, L) positions are its query tokens (causal)
+        q_lens = [min(256, int(L)) for L in w.seq_lens.tolist()]
+        qsl = torch.tensor([0] + list(itertools.accumulate(q_lens)), dtype=torch.int32, device=dev)
+        n_q = sum(q_lens)
+        g = torch.Generator(device="cpu").manual_seed(2025)
+        qp = torch.randn((n_q, Hq * D), generator=g).to(torch.bfloat16).to(dev)
+        outp = torch.empty((n_q, Hq, D), dtype=torch.float32, device=dev)
+
+        def prefill_attn():
+            pk.paged_prefill_attn_bf16(qp, kc, vc, outp, tables, lens, qsl, w.max_blocks_per_seq, w.num_seqs, n_q,
+                                       Hq, H, D, bs, w.inv_sqrt_d, Hq * D, 0)
+        self.extras.append(dict(name="bf16_chunked_prefill", fn=prefill_attn, tokens=n_q,
+                                flops=prefill_flops(w.seq_lens.tolist(), q_lens, 0, Hq, D),
+                                bytes=sum(int(L) for L in w.seq_lens.tolist()) * H * D * 4 + n_q * Hq * D * (2 + 4)))
+
     def _setup_fp8k_long(self):
         torch, kvgen, pk, dev = self.torch, self.kvgen, self.pk, self.dev
         w = kvgen.fp8k_long(device=dev, **(self.SMALL['fp8k_long'] if self.small else {}))
@@ -405,6 +449,26 @@ class GpuStep:
         self.extras.append(dict(name="fp8_kv_mixed_decode", fn=fp8kv_decode, tokens=w.num_seqs,
                                 bytes=decode_bytes(w.seq_lens.tolist(), 0, H, D, 1, w.num_seqs, Hq,
                                                    w.max_blocks_per_seq, v_bytes=1)))
+
+        # chunked prefill over the FP8-K cache of the first 32 sequences: the
+        # last min(256, L) positions of each are its query tokens (causal)
+        ns = min(32, w.num_seqs)
+        q_lens = [min(256, int(L)) for L in w.seq_lens[:ns].tolist()]
+        qsl = torch.tensor([0] + list(itertools.accumulate(q_lens)), dtype=torch.int32, device=dev)
+        n_q = sum(q_lens)
+        g = torch.Generator(device="cpu").manual_seed(2026)
+        qp = torch.randn((n_q, Hq * D), generator=g).to(torch.bfloat16).to(dev)
+        outp = torch.empty((n_q, Hq, D), dtype=torch.float32, device=dev)
+        lens_p = lens[:ns].contiguous()
+        tables_p = tables[:ns].contiguous()
+
+        def prefill_attn():
+            pk.paged_prefill_attn_fp8k(qp, kc, vc, outp, tables_p, lens_p, qsl, w.max_blocks_per_seq, ns, n_q, Hq,
+                                       H, D, bs, w.inv_sqrt_d, k_scale, Hq * D, 0)
+        self.extras.append(dict(name="fp8k_chunked_prefill", fn=prefill_attn, tokens=n_q,
+                                flops=prefill_flops(w.seq_lens[:ns].tolist(), q_lens, 0, Hq, D),
+                                bytes=sum(int(L) for L in w.seq_lens[:ns].tolist()) * H * D * 3
+                                + n_q * Hq * D * (2 + 4)))
 
     def _grow_ws(self, w):
         self.ws_bytes = max(self.ws_bytes, self.pk.kv_decode_workspace_bytes(
@@ -627,12 +691,20 @@ def run_gpu(args):
 
     extra_ms = step.time_extras(args.steps)
     next_rows = {}
+    tf_peak, tf_kind = measured_bf16_tflops()
     for x in step.extras:
         ms = extra_ms[x["name"]]
         gbs = x["bytes"] / (ms * 1e-3) / 1e9
         next_rows[x["name"]] = {"ms": round(ms, 4), "GB_per_s": round(gbs, 1),
                                 "tokens_per_s": round(x["tokens"] / (ms * 1e-3), 1),
                                 "frac_measured_hbm": round(gbs / peak, 4), "algorithmic_bytes": int(x["bytes"])}
+        if "flops" in x:
+            # a contraction: its roofline is the tensor pipe, not HBM
+            tfs = x["flops"] / (ms * 1e-3) / 1e12
+            next_rows[x["name"]].update({"bound": "tensor", "TFLOP_per_s": round(tfs, 1),
+                                         "frac_of_bf16_peak": round(tfs / tf_peak, 4),
+                                         "bf16_peak": tf_peak, "peak_kind": tf_kind,
+                                         "algorithmic_flops": int(x["flops"])})
 
     e2e = run_e2e(step, args, dev, world)
     cpu = cpu_baseline(args) if (rank == 0 and world == 1 and not args.no_cpu_baseline) else None

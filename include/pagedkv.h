@@ -244,6 +244,42 @@ PAGEDKV_API int paged_decode_attn_fp8(const kv_bf16_t *q, const kv_e4m3_t *k_cac
                                       uint32_t q_stride, uint32_t sliding_window, void *stream);
 
 /* ------------------------------------------------------------------------
+ * Multi-token (chunked-prefill) paged attention.  [kv_cache.rs] "Batched
+ * prefill variants (N tokens)" gives only the heading; the reading here:
+ * sequence s brings n_s = query_start_loc[s+1] - query_start_loc[s] query
+ * tokens, the last n_s of its seq_lens[s] cached positions (their K/V
+ * already written). Query j of s (row query_start_loc[s] + j of q, at
+ * position P = seq_lens[s] - n_s + j) attends causally, over positions
+ * [start, P] with start = (sliding_window > 0 ? max(0, P + 1 -
+ * sliding_window) : 0): exactly what the paged decode attends for that
+ * sequence cut to length P + 1. A query with P < 0 gives zeros. GQA,
+ * inv_sqrt_d, the block tables and (FP8) k_scale are as in the decode calls.
+ *   q                bf16 rows [num_q_tokens], row stride q_stride elements,
+ *                    head h at +h * head_dim.
+ *   query_start_loc  device int32[num_seqs + 1], non-decreasing, from 0 to
+ *                    num_q_tokens (a violation sets bit 2 of the device
+ *                    fault word and that sequence's rows are skipped).
+ *   output           device float32[num_q_tokens, num_q_heads, head_dim].
+ * Supported: head_dim 64 or 128 (FP8: 128); block_size a power of two in
+ * [16, 256]; q, caches and q_stride 16-byte aligned. No workspace is used.
+ * ---------------------------------------------------------------------- */
+PAGEDKV_API int paged_prefill_attn_bf16(const kv_bf16_t *q, const kv_bf16_t *k_cache, const kv_bf16_t *v_cache,
+                                        float *output, const int32_t *block_tables, const int32_t *seq_lens,
+                                        const int32_t *query_start_loc, uint32_t max_blocks_per_seq,
+                                        uint32_t num_seqs, uint32_t num_q_tokens, uint32_t num_q_heads,
+                                        uint32_t num_kv_heads, uint32_t head_dim, uint32_t block_size,
+                                        float inv_sqrt_d, uint32_t q_stride, uint32_t sliding_window,
+                                        void *stream);
+
+PAGEDKV_API int paged_prefill_attn_fp8k(const kv_bf16_t *q, const kv_e4m3_t *k_cache_fp8,
+                                        const kv_bf16_t *v_cache, float *output, const int32_t *block_tables,
+                                        const int32_t *seq_lens, const int32_t *query_start_loc,
+                                        uint32_t max_blocks_per_seq, uint32_t num_seqs, uint32_t num_q_tokens,
+                                        uint32_t num_q_heads, uint32_t num_kv_heads, uint32_t head_dim,
+                                        uint32_t block_size, float inv_sqrt_d, float k_scale, uint32_t q_stride,
+                                        uint32_t sliding_window, void *stream);
+
+/* ------------------------------------------------------------------------
  * FP8-K paged decode without any caller-provided memory. The source pages
  * have no counterpart of this call; it exists for callers that cannot give
  * the library a device allocation: host code running in a callback enqueued
@@ -294,6 +330,9 @@ PAGEDKV_API int kv_set_decode_workspace(void *device_ptr, size_t bytes);
  * since the last clear (0 = none) in *bits and clears them.
  *   bit 0: a decode pipeline wait timed out
  *   bit 1: seq_lens[s] exceeded max_blocks_per_seq * block_size (clamped)
+ *   bit 2: a prefill query_start_loc was decreasing, negative or past
+ *          num_q_tokens (that sequence skipped)
+ *   (bit 0 also covers the prefill pipeline)
  * ---------------------------------------------------------------------- */
 PAGEDKV_API int kv_get_device_error(uint32_t *bits);
 

@@ -15,7 +15,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(CSRC, "_build")
 LIB = os.path.join(HERE, "libpagedkv.so")
-SOURCES = ["abi.cu", "kv_write.cu", "fused_k.cu", "decode.cu", "static_scratch.cu"]
+SOURCES = ["abi.cu", "kv_write.cu", "fused_k.cu", "decode.cu", "prefill.cu", "static_scratch.cu"]
 HEADERS = ["common.cuh", "internal.h", "rope_tables.h", os.path.join("..", "..", "include", "pagedkv.h")]
 
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")

@@ -282,6 +282,74 @@ int paged_decode_attn_fp8(const kv_bf16_t* q, const kv_e4m3_t* k_cache_fp8, cons
                        sliding_window, true, true, v_scale, stream);
 }
 
+static int prefill_common(const kv_bf16_t* q, const void* k_cache, const kv_bf16_t* v_cache, float* output,
+                          const int32_t* block_tables, const int32_t* seq_lens, const int32_t* query_start_loc,
+                          uint32_t max_blocks_per_seq, uint32_t num_seqs, uint32_t num_q_tokens,
+                          uint32_t num_q_heads, uint32_t num_kv_heads, uint32_t head_dim, uint32_t block_size,
+                          float inv_sqrt_d, float k_scale, uint32_t q_stride, uint32_t sliding_window, bool fp8,
+                          void* stream) {
+  if (num_seqs == 0 || num_q_tokens == 0) return KV_OK;
+  if (!q || !k_cache || !v_cache || !output || !block_tables || !seq_lens || !query_start_loc)
+    return KV_ERR_INVALID_ARG;
+  if (num_kv_heads == 0 || num_q_heads == 0 || num_q_heads % num_kv_heads) return KV_ERR_INVALID_ARG;
+  if (head_dim == 0 || block_size == 0) return KV_ERR_INVALID_ARG;
+  if (uint64_t(q_stride) < uint64_t(num_q_heads) * head_dim) return KV_ERR_INVALID_ARG;
+  if (!isfinite(inv_sqrt_d)) return KV_ERR_INVALID_ARG;
+  if (fp8 && (!(k_scale > 0.0f) || !isfinite(k_scale))) return KV_ERR_INVALID_ARG;
+  if (fp8 ? head_dim != 128 : (head_dim != 64 && head_dim != 128)) return KV_ERR_UNSUPPORTED;
+  if (!is_pow2(block_size) || block_size < 16 || block_size > 256) return KV_ERR_UNSUPPORTED;
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || (q_stride * 2u) % 16)
+    return KV_ERR_UNSUPPORTED;
+  if (!aligned(output, 8)) return KV_ERR_UNSUPPORTED;
+  if (uint64_t(max_blocks_per_seq) * block_size >= (1ull << 31)) return KV_ERR_UNSUPPORTED;
+  if (uint64_t(num_q_tokens) * num_q_heads >= (1ull << 31)) return KV_ERR_UNSUPPORTED;
+  const DeviceInfo& dev = device_info();
+  if (dev.device < 0) return KV_ERR_CUDA;
+  if (dev.cc_major < 10) return KV_ERR_UNSUPPORTED;
+  PrefillArgs a{};
+  a.q = q;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.output = output;
+  a.block_tables = block_tables;
+  a.seq_lens = seq_lens;
+  a.query_start_loc = query_start_loc;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.num_seqs = num_seqs;
+  a.num_q_tokens = num_q_tokens;
+  a.num_q_heads = num_q_heads;
+  a.num_kv_heads = num_kv_heads;
+  a.head_dim = head_dim;
+  a.block_size = block_size;
+  a.inv_sqrt_d = inv_sqrt_d;
+  a.k_scale = k_scale;
+  a.q_stride = q_stride;
+  a.sliding_window = sliding_window;
+  a.fp8 = fp8;
+  return launch_prefill(a, as_stream(stream));
+}
+
+int paged_prefill_attn_bf16(const kv_bf16_t* q, const kv_bf16_t* k_cache, const kv_bf16_t* v_cache, float* output,
+                            const int32_t* block_tables, const int32_t* seq_lens, const int32_t* query_start_loc,
+                            uint32_t max_blocks_per_seq, uint32_t num_seqs, uint32_t num_q_tokens,
+                            uint32_t num_q_heads, uint32_t num_kv_heads, uint32_t head_dim, uint32_t block_size,
+                            float inv_sqrt_d, uint32_t q_stride, uint32_t sliding_window, void* stream) {
+  return prefill_common(q, k_cache, v_cache, output, block_tables, seq_lens, query_start_loc, max_blocks_per_seq,
+                        num_seqs, num_q_tokens, num_q_heads, num_kv_heads, head_dim, block_size, inv_sqrt_d, 1.0f,
+                        q_stride, sliding_window, false, stream);
+}
+
+int paged_prefill_attn_fp8k(const kv_bf16_t* q, const kv_e4m3_t* k_cache_fp8, const kv_bf16_t* v_cache,
+                            float* output, const int32_t* block_tables, const int32_t* seq_lens,
+                            const int32_t* query_start_loc, uint32_t max_blocks_per_seq, uint32_t num_seqs,
+                            uint32_t num_q_tokens, uint32_t num_q_heads, uint32_t num_kv_heads, uint32_t head_dim,
+                            uint32_t block_size, float inv_sqrt_d, float k_scale, uint32_t q_stride,
+                            uint32_t sliding_window, void* stream) {
+  return prefill_common(q, k_cache_fp8, v_cache, output, block_tables, seq_lens, query_start_loc,
+                        max_blocks_per_seq, num_seqs, num_q_tokens, num_q_heads, num_kv_heads, head_dim, block_size,
+                        inv_sqrt_d, k_scale, q_stride, sliding_window, true, stream);
+}
+
 size_t kv_decode_workspace_bytes(uint32_t max_blocks_per_seq, uint32_t num_seqs, uint32_t num_q_heads,
                                  uint32_t num_kv_heads, uint32_t head_dim, uint32_t block_size) {
   return decode_workspace_bytes(max_blocks_per_seq, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size);
@@ -301,7 +369,12 @@ int kv_set_decode_workspace(void* device_ptr, size_t bytes) {
 int kv_get_device_error(uint32_t* bits) {
   if (!bits) return KV_ERR_INVALID_ARG;
   if (cudaDeviceSynchronize() != cudaSuccess) return KV_ERR_CUDA;
-  return from_cuda(read_and_clear_decode_error(bits));
+  uint32_t decode_bits = 0, prefill_bits = 0;
+  if (read_and_clear_decode_error(&decode_bits) != cudaSuccess ||
+      read_and_clear_prefill_error(&prefill_bits) != cudaSuccess)
+    return KV_ERR_CUDA;
+  *bits = decode_bits | prefill_bits;
+  return KV_OK;
 }
 
 int kv_device_info(int* num_sms, int* decode_ctas) {

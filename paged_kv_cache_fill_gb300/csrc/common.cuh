@@ -14,6 +14,7 @@ namespace pagedkv {
 enum : uint32_t {
   kErrWaitTimeout = 1u << 0,
   kErrSeqLenClamped = 1u << 1,
+  kErrQueryLayout = 1u << 2,
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

@@ -709,7 +709,9 @@ __global__ void __launch_bounds__(D) combine_kernel(const DecodeParams p) {
 }
 
 // ---------------------------------------------------------------- host side
-PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+}  // namespace
+
+static PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   if (!fn) {
     void* ptr = nullptr;
@@ -746,6 +748,8 @@ bool encode_pool_map(CUtensorMap* map, const void* base, bool fp8, uint32_t num_
                             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
+
+namespace {
 
 struct Geometry {
   uint32_t heads_per_item, nt, stages, stage_bytes, k_bytes, v_bytes, smem_bytes;

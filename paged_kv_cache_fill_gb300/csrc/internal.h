@@ -44,6 +44,30 @@ cudaError_t launch_fused_k_norm_rope(const uint16_t* k_in, const uint16_t* k_nor
                                      uint32_t num_kv_heads, uint32_t head_dim, uint32_t rotary_dim,
                                      float rms_eps, float theta, cudaStream_t stream);
 
+// Tensor map over a cache pool [num_blocks, block_size, num_kv_heads,
+// head_dim] (bf16, or e4m3 when fp8) whose box is one 128-byte chunk x 16
+// slots x (heads_per_item x chunks per head): the shared-memory tile is
+// [chunk][slot][128 B], 128-byte swizzled by slot row.
+bool encode_pool_map(CUtensorMap* map, const void* base, bool fp8, uint32_t num_kv_heads, uint32_t head_dim,
+                     uint32_t heads_per_item);
+
+// Multi-token (chunked-prefill) paged attention; returns a KV_* status.
+struct PrefillArgs {
+  const uint16_t* q;
+  const void* k_cache;  // bf16 or e4m3 pool
+  const uint16_t* v_cache;
+  float* output;
+  const int32_t* block_tables;
+  const int32_t* seq_lens;
+  const int32_t* query_start_loc;
+  uint32_t max_blocks_per_seq, num_seqs, num_q_tokens, num_q_heads, num_kv_heads, head_dim, block_size;
+  float inv_sqrt_d, k_scale;
+  uint32_t q_stride, sliding_window;
+  bool fp8;
+};
+int launch_prefill(const PrefillArgs& a, cudaStream_t stream);
+cudaError_t read_and_clear_prefill_error(uint32_t* bits);
+
 // Paged decode. `workspace` may be null (then no split-KV).
 struct DecodeArgs {
   const uint16_t* q;

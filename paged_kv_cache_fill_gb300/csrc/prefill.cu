@@ -1,0 +1,499 @@
+// Multi-token (chunked-prefill) paged attention over a BF16 or FP8-E4M3-K /
+// BF16-V paged cache.
+//
+// [kv_cache.rs] "Batched prefill variants (N tokens)" (a heading only), read
+// as: sequence s brings n_s = query_start_loc[s+1] - query_start_loc[s]
+// query tokens, the last n_s of its seq_lens[s] cached positions; query j
+// (row query_start_loc[s] + j, position P = seq_lens[s] - n_s + j) attends
+// positions [start, P], start = max(0, P + 1 - sliding_window) when
+// sliding_window > 0, else 0 -- what the paged decode ([kv_cache.rs]
+// `paged_decode_attn_fp8`) attends for a sequence of length P + 1. GQA as in
+// the decode: query head h reads KV head h / (num_q_heads / num_kv_heads).
+//
+// GB300 design. Rows are (query token, query head of the KV head's group)
+// pairs, token-major, so one CTA's 64 rows share every K/V tile it loads.
+// A CTA owns one (sequence, KV head, block of 64 rows) item; items are laid
+// out longest key range first within a sequence, and the grid holds an upper
+// bound of the item count (CTAs past the last item exit at once).
+//   * Warp 0 produces: TMA tiled loads (cp.async.bulk.tensor.3d) of 16-slot
+//     boxes of K and V (one physical block run each, 128-byte swizzle) into
+//     a 3-stage ring of 64-key tiles guarded by full/empty mbarriers.
+//   * Warps 1..4 consume, 16 rows each, FlashAttention-2 style with
+//     mma.sync m16n8k16: S = Q K^T with Q held in registers (BF16; or f16
+//     scaled by a power of two per row against FP8 K converted exactly to
+//     f16, in the permuted k order the byte layout of ldmatrix gives), base-2
+//     online softmax per row, then O += P V with P split into BF16 hi + lo
+//     parts (two MMAs) taken straight from the S accumulators, V through
+//     transposing ldmatrix. Only tiles that cross a row's causal or window
+//     edge, or the end of the loaded keys, pay for masks.
+#include <math.h>
+
+#include "../../include/pagedkv.h"
+#include "internal.h"
+
+namespace pagedkv {
+
+__device__ uint32_t g_prefill_error;
+
+namespace {
+
+constexpr int kBM = 64;                 // rows per CTA
+constexpr int kBN = 64;                 // keys per stage
+constexpr int kSub = 16;                // keys per TMA box
+constexpr int kStages = 3;
+constexpr int kConsumers = kBM / 16;    // one warp per 16 rows
+constexpr int kThreads = 32 * (1 + kConsumers);
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct PrefillParams {
+  const uint16_t* q;
+  const int32_t* block_tables;
+  const int32_t* seq_lens;
+  const int32_t* qsl;  // query_start_loc
+  float* output;
+  uint32_t max_blocks_per_seq, num_seqs, num_q_tokens, num_q_heads, num_kv_heads, group;
+  uint32_t block_size, block_shift, q_stride, sliding_window;
+  float score_scale;  // inv_sqrt_d * log2(e) (times k_scale for FP8)
+  uint32_t k_box_bytes, v_box_bytes, stage_bytes;
+};
+
+struct Item {
+  int32_t seq, kv_head, row0, rows;  // rows [row0, row0 + rows) of the sequence's n * group
+  int32_t n, qstart, len;            // query tokens, their first row in q, cached positions
+};
+
+__device__ __forceinline__ uint32_t row_blocks(int64_t n, uint32_t group) {
+  return uint32_t((n * group + kBM - 1) / kBM);
+}
+
+// The item of CTA `target` (seq < 0: none). Run by one warp.
+__device__ Item locate(uint32_t target, const PrefillParams& p, uint32_t lane) {
+  Item it{};
+  it.seq = -1;
+  uint64_t base = 0;
+  for (uint32_t s0 = 0; s0 < p.num_seqs; s0 += 32) {
+    const uint32_t s = s0 + lane;
+    int64_t n = 0;
+    if (s < p.num_seqs) {
+      const int32_t a = __ldg(p.qsl + s), b = __ldg(p.qsl + s + 1);
+      n = int64_t(b) - a;
+      if (a < 0 || n < 0 || uint32_t(b) > p.num_q_tokens) {
+        atomicOr(&g_prefill_error, kErrQueryLayout);
+        n = 0;
+      }
+    }
+    const uint32_t items = row_blocks(n, p.group) * p.num_kv_heads;
+    uint32_t incl = items;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= uint32_t(o)) incl += v;
+    }
+    const uint32_t total = __shfl_sync(0xffffffffu, incl, 31);
+    if (uint64_t(target) < base + total) {
+      const uint32_t rel = uint32_t(target - base);
+      const uint32_t sl = __ffs(__ballot_sync(0xffffffffu, incl > rel)) - 1;
+      const uint32_t local = rel - (__shfl_sync(0xffffffffu, incl, sl) - __shfl_sync(0xffffffffu, items, sl));
+      const int64_t ns = __shfl_sync(0xffffffffu, n, sl);
+      const uint32_t nblk = row_blocks(ns, p.group);
+      const uint32_t blk = nblk - 1 - local / p.num_kv_heads;  // longest key range first
+      it.seq = int32_t(s0 + sl);
+      it.kv_head = int32_t(local % p.num_kv_heads);
+      it.row0 = int32_t(blk * kBM);
+      const int64_t rows_total = ns * p.group;
+      it.rows = int32_t(rows_total - it.row0 < kBM ? rows_total - it.row0 : kBM);
+      it.n = int32_t(ns);
+      it.qstart = __ldg(p.qsl + it.seq);
+      int32_t L = __ldg(p.seq_lens + it.seq);
+      if (L < 0) L = 0;
+      const int64_t cap = int64_t(p.max_blocks_per_seq) << p.block_shift;
+      if (L > cap) {
+        L = int32_t(cap);
+        if (lane == 0 && it.kv_head == 0) atomicOr(&g_prefill_error, kErrSeqLenClamped);
+      }
+      it.len = L;
+      return it;
+    }
+    base += total;
+  }
+  return it;
+}
+
+template <bool kFp8, int D>
+__global__ void __launch_bounds__(kThreads)
+    prefill_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
+                   const PrefillParams p) {
+  constexpr int kKChunks = kFp8 ? D / 128 : D / 64;  // 128-byte chunks per K head row
+  constexpr int kVChunks = D / 64;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+  __shared__ uint64_t full[kStages], empty[kStages];
+  __shared__ Item s_item;
+
+  const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kConsumers);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    const Item it = locate(blockIdx.x, p, lane);
+    if (lane == 0) s_item = it;
+  }
+  __syncthreads();
+  const Item it = s_item;
+  if (it.seq < 0) return;
+
+  // key range of the item: positions of its first and last rows' tokens
+  const int32_t g = int32_t(p.group);
+  const int32_t pos_first = it.len - it.n + it.row0 / g;
+  const int32_t pos_last = it.len - it.n + (it.row0 + it.rows - 1) / g;
+  const int32_t k_hi = pos_last + 1;  // keys [k_lo, k_hi)
+  const int32_t W = int32_t(p.sliding_window);
+  int32_t k_lo = 0;
+  if (W > 0 && pos_first + 1 - W > 0) k_lo = pos_first + 1 - W;
+  const int32_t t_begin = k_lo / kBN;
+  const int32_t t_end = k_hi > 0 ? (k_hi + kBN - 1) / kBN : t_begin;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    tma_prefetch_desc(&tmap_k);
+    tma_prefetch_desc(&tmap_v);
+    const int32_t* table = p.block_tables + uint64_t(it.seq) * p.max_blocks_per_seq;
+    uint32_t stage = 0, phase = 0;
+    bool ok = true;
+    for (int32_t tile = t_begin; tile < t_end && ok; ++tile) {
+      // block ids of the tile's 16-key boxes (keys below k_hi only)
+      int32_t block_id = 0;
+      const int32_t key0 = tile * kBN + int32_t(lane) * kSub;
+      if (lane < uint32_t(kBN / kSub) && key0 < k_hi) block_id = __ldg(table + (key0 >> p.block_shift));
+      if (lane == 0) {
+        if (!mbar_wait(&empty[stage], phase ^ 1)) ok = false;
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      const uint32_t loaded = __popc(__ballot_sync(0xffffffffu, lane < uint32_t(kBN / kSub) && key0 < k_hi));
+      if (lane == 0) mbar_arrive_expect_tx(&full[stage], loaded * (p.k_box_bytes + p.v_box_bytes));
+      __syncwarp();
+      if (lane < loaded) {
+        uint8_t* st = smem + stage * p.stage_bytes;
+        const int32_t slot0 = (block_id << p.block_shift) + (key0 & int32_t(p.block_size - 1));
+        tma_load_3d(st + lane * p.k_box_bytes, &tmap_k, 0, slot0, it.kv_head * kKChunks, &full[stage]);
+        tma_load_3d(st + (kBN / kSub) * p.k_box_bytes + lane * p.v_box_bytes, &tmap_v, 0, slot0,
+                    it.kv_head * kVChunks, &full[stage]);
+      }
+      if (++stage == kStages) { stage = 0; phase ^= 1; }
+    }
+    if (!ok && lane == 0) atomicOr(&g_prefill_error, kErrWaitTimeout);
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  const uint32_t cw = warp - 1;        // rows cw*16 .. cw*16+15 of the item
+  const uint32_t g8 = lane >> 2, c4 = lane & 3;
+  // this lane's two rows (g8, g8 + 8): token position, valid key range
+  int32_t pos[2], lo[2];
+  const uint16_t* qrow[2];
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const int32_t row = int32_t(cw * 16 + g8 + 8 * r);
+    const int32_t grow = it.row0 + row;
+    const bool valid = row < it.rows;
+    const int32_t t = grow / g, hh = grow % g;
+    pos[r] = valid ? it.len - it.n + t : -1;  // -1: attends nothing
+    lo[r] = (W > 0) ? pos[r] + 1 - W : INT32_MIN;
+    qrow[r] = valid ? p.q + uint64_t(it.qstart + t) * p.q_stride + uint64_t(it.kv_head * g + hh) * D : nullptr;
+  }
+
+  // Q fragments (A operand), D / 16 k-steps of 4 registers
+  uint32_t qf[D / 16][4];
+  float row_scale[2];
+  if constexpr (!kFp8) {
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        qf[kk][r] = qrow[r] ? *reinterpret_cast<const uint32_t*>(qrow[r] + kk * 16 + 2 * c4) : 0u;
+        qf[kk][2 + r] = qrow[r] ? *reinterpret_cast<const uint32_t*>(qrow[r] + kk * 16 + 8 + 2 * c4) : 0u;
+      }
+    }
+    row_scale[0] = row_scale[1] = p.score_scale;
+  } else {
+    // k order permuted to the byte layout of ldmatrix on FP8 rows: MMA k pair
+    // (2c, 2c+1) <-> dims 16kk + 4c + {0,1}, (2c+8, 2c+9) <-> 16kk + 4c + {2,3}
+    float qv[2][D / 16][4];
+    float amax[2] = {0.0f, 0.0f};
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint2 w = qrow[r] ? *reinterpret_cast<const uint2*>(qrow[r] + kk * 16 + 4 * c4) : make_uint2(0, 0);
+        qv[r][kk][0] = bf16_lo_to_f32(w.x);
+        qv[r][kk][1] = bf16_hi_to_f32(w.x);
+        qv[r][kk][2] = bf16_lo_to_f32(w.y);
+        qv[r][kk][3] = bf16_hi_to_f32(w.y);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) amax[r] = fmaxf(amax[r], fabsf(qv[r][kk][e]));
+      }
+      amax[r] = fmaxf(amax[r], __shfl_xor_sync(0xffffffffu, amax[r], 1));
+      amax[r] = fmaxf(amax[r], __shfl_xor_sync(0xffffffffu, amax[r], 2));
+      // scale the row by 2^e so that its largest magnitude lies in [2^14, 2^15)
+      int e = 0;
+      if (amax[r] > 0.0f && amax[r] < INFINITY) {
+        int ex;
+        frexpf(amax[r], &ex);
+        e = 15 - ex;
+      }
+      const float sc = ldexpf(1.0f, e);
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        qf[kk][r] = f32x2_to_f16x2(qv[r][kk][0] * sc, qv[r][kk][1] * sc);
+        qf[kk][2 + r] = f32x2_to_f16x2(qv[r][kk][2] * sc, qv[r][kk][3] * sc);
+      }
+      row_scale[r] = p.score_scale * ldexpf(1.0f, -e);
+    }
+  }
+
+  float acc[D / 8][4];
+#pragma unroll
+  for (int i = 0; i < D / 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.0f;
+  float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.0f, 0.0f};
+  // ldmatrix lane roles: K (non-transposed B: two n8 key groups x two 16-byte
+  // units) and V (transposed B: two 8-key halves x two 16-byte units)
+  const uint32_t k_row = (lane & 7) + ((lane >> 4) & 1) * 8, k_unit = (lane >> 3) & 1;
+  const uint32_t v_row = (lane & 7) + ((lane >> 3) & 1) * 8, v_unit = lane >> 4;
+  const int32_t lo_max = lo[0] > lo[1] ? lo[0] : lo[1];
+  const int32_t pos_min = pos[0] < pos[1] ? pos[0] : pos[1];
+
+  uint32_t stage = 0, phase = 0;
+  for (int32_t tile = t_begin; tile < t_end; ++tile) {
+    if (!mbar_wait(&full[stage], phase)) {
+      if (lane == 0) atomicOr(&g_prefill_error, kErrWaitTimeout);
+      return;
+    }
+    const uint32_t kbase = smem_u32(smem + stage * p.stage_bytes);
+    const uint32_t vbase = kbase + (kBN / kSub) * p.k_box_bytes;
+    const int32_t key_base = tile * kBN;
+
+    // ---- S = Q K^T: 16 rows x 64 keys (8 n8 groups)
+    float s[kBN / 8][4];
+#pragma unroll
+    for (int j = 0; j < kBN / 8; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.0f;
+#pragma unroll
+    for (int jp = 0; jp < kBN / 16; ++jp) {  // box jp = keys 16jp..16jp+15 = n8 groups 2jp, 2jp+1
+      const uint32_t box = kbase + jp * p.k_box_bytes;
+      if constexpr (!kFp8) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t chunk = kk >> 2, unit = ((kk & 3) << 1) + k_unit;
+          uint32_t b[4];
+          ldmatrix_x4(b, box + chunk * (kSub * 128) + k_row * 128 + ((unit ^ (k_row & 7)) << 4));
+          mma_bf16(s[2 * jp], qf[kk], b[0], b[1]);
+          mma_bf16(s[2 * jp + 1], qf[kk], b[2], b[3]);
+        }
+      } else {
+#pragma unroll
+        for (int up = 0; up < D / 32; ++up) {  // 16-byte units 2up, 2up+1 = k-steps 2up, 2up+1
+          const uint32_t chunk = up >> 2, unit = ((up & 3) << 1) + k_unit;
+          uint32_t r[4];
+          ldmatrix_x4(r, box + chunk * (kSub * 128) + k_row * 128 + ((unit ^ (k_row & 7)) << 4));
+          // r[0]: keys 16jp+0..7, unit 2up; r[1]: same keys, unit 2up+1;
+          // r[2], r[3]: keys 16jp+8..15
+          mma_f16(s[2 * jp], qf[2 * up], e4m3x2_to_f16x2(uint16_t(r[0])), e4m3x2_to_f16x2(uint16_t(r[0] >> 16)));
+          mma_f16(s[2 * jp], qf[2 * up + 1], e4m3x2_to_f16x2(uint16_t(r[1])),
+                  e4m3x2_to_f16x2(uint16_t(r[1] >> 16)));
+          mma_f16(s[2 * jp + 1], qf[2 * up], e4m3x2_to_f16x2(uint16_t(r[2])),
+                  e4m3x2_to_f16x2(uint16_t(r[2] >> 16)));
+          mma_f16(s[2 * jp + 1], qf[2 * up + 1], e4m3x2_to_f16x2(uint16_t(r[3])),
+                  e4m3x2_to_f16x2(uint16_t(r[3] >> 16)));
+        }
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kBN / 8; ++j) {
+      s[j][0] *= row_scale[0];
+      s[j][1] *= row_scale[0];
+      s[j][2] *= row_scale[1];
+      s[j][3] *= row_scale[1];
+    }
+    // ---- masks: only a tile that crosses a row's causal or window edge
+    const bool edge = key_base + kBN - 1 > pos_min || key_base < lo_max;
+    if (edge) {
+#pragma unroll
+      for (int j = 0; j < kBN / 8; ++j) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int32_t key = key_base + 8 * j + 2 * int32_t(c4) + (e & 1);
+          const int r = e >> 1;
+          if (key > pos[r] || key < lo[r]) s[j][e] = -INFINITY;
+        }
+      }
+    }
+    // ---- online softmax (base 2), rows g8 and g8 + 8
+    float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+    for (int j = 0; j < kBN / 8; ++j) {
+      mx[0] = fmaxf(mx[0], fmaxf(s[j][0], s[j][1]));
+      mx[1] = fmaxf(mx[1], fmaxf(s[j][2], s[j][3]));
+    }
+    float mb[2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
+      mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
+      mx[r] = fmaxf(mx[r], m_run[r]);
+      mb[r] = mx[r] == -INFINITY ? 0.0f : mx[r];  // a row with nothing attended yet stays at zero
+    }
+    if (__any_sync(0xffffffffu, mx[0] != m_run[0] || mx[1] != m_run[1])) {
+      const float al0 = fast_exp2(m_run[0] - mb[0]), al1 = fast_exp2(m_run[1] - mb[1]);
+      l_run[0] *= al0;
+      l_run[1] *= al1;
+#pragma unroll
+      for (int i = 0; i < D / 8; ++i) {
+        acc[i][0] *= al0;
+        acc[i][1] *= al0;
+        acc[i][2] *= al1;
+        acc[i][3] *= al1;
+      }
+    }
+    m_run[0] = mx[0];
+    m_run[1] = mx[1];
+#pragma unroll
+    for (int j = 0; j < kBN / 8; ++j) {
+      s[j][0] = fast_exp2(s[j][0] - mb[0]);
+      s[j][1] = fast_exp2(s[j][1] - mb[0]);
+      s[j][2] = fast_exp2(s[j][2] - mb[1]);
+      s[j][3] = fast_exp2(s[j][3] - mb[1]);
+      l_run[0] += s[j][0] + s[j][1];
+      l_run[1] += s[j][2] + s[j][3];
+    }
+    // ---- O += P V, P as BF16 hi + lo A fragments straight from S
+    const bool tail = key_base + kBN > k_hi;  // keys >= k_hi: not loaded or past the end: zero their V
+#pragma unroll
+    for (int kk = 0; kk < kBN / 16; ++kk) {
+      uint32_t ph[4], pl[4];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {  // h: n8 group 2kk + h = A columns 8h..8h+7
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const float x0 = s[2 * kk + h][2 * r], x1 = s[2 * kk + h][2 * r + 1];
+          const uint32_t hi = f32x2_to_bf16x2(x0, x1);
+          ph[2 * h + r] = hi;
+          pl[2 * h + r] = f32x2_to_bf16x2(x0 - bf16_lo_to_f32(hi), x1 - bf16_hi_to_f32(hi));
+        }
+      }
+      uint32_t m01 = 0xffffffffu, m89 = 0xffffffffu;
+      if (tail) {
+        const int32_t k0 = key_base + 16 * kk + 2 * int32_t(c4);
+        m01 = (k0 < k_hi ? 0x0000ffffu : 0u) | (k0 + 1 < k_hi ? 0xffff0000u : 0u);
+        m89 = (k0 + 8 < k_hi ? 0x0000ffffu : 0u) | (k0 + 9 < k_hi ? 0xffff0000u : 0u);
+      }
+      const uint32_t box = vbase + kk * p.v_box_bytes;
+#pragma unroll
+      for (int dp = 0; dp < D / 16; ++dp) {  // n8 dim groups 2dp, 2dp+1
+        const uint32_t chunk = dp >> 2, unit = ((dp & 3) << 1) + v_unit;
+        uint32_t b[4];
+        ldmatrix_x4_trans(b, box + chunk * (kSub * 128) + v_row * 128 + ((unit ^ (v_row & 7)) << 4));
+        b[0] &= m01;
+        b[1] &= m89;
+        b[2] &= m01;
+        b[3] &= m89;
+        mma_bf16(acc[2 * dp], ph, b[0], b[1]);
+        mma_bf16(acc[2 * dp], pl, b[0], b[1]);
+        mma_bf16(acc[2 * dp + 1], ph, b[2], b[3]);
+        mma_bf16(acc[2 * dp + 1], pl, b[2], b[3]);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[stage]);
+    if (++stage == kStages) { stage = 0; phase ^= 1; }
+  }
+
+  // ---- normalise and store: row r's dims 8i + 2c4, +1
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    float l = l_run[r];
+    l += __shfl_xor_sync(0xffffffffu, l, 1);
+    l += __shfl_xor_sync(0xffffffffu, l, 2);
+    if (!qrow[r]) continue;
+    const int32_t row = int32_t(cw * 16 + g8 + 8 * r), grow = it.row0 + row;
+    const int32_t t = grow / g, hh = grow % g;
+    const float inv = l > 0.0f ? 1.0f / l : 0.0f;
+    float* o = p.output + (uint64_t(it.qstart + t) * p.num_q_heads + uint64_t(it.kv_head * g + hh)) * D;
+#pragma unroll
+    for (int i = 0; i < D / 8; ++i)
+      *reinterpret_cast<float2*>(o + 8 * i + 2 * c4) = make_float2(acc[i][2 * r] * inv, acc[i][2 * r + 1] * inv);
+  }
+}
+
+template <bool kFp8, int D>
+int launch_prefill_t(const PrefillArgs& a, cudaStream_t stream, PrefillParams& p, uint64_t grid) {
+  CUtensorMap mk, mv;
+  if (!encode_pool_map(&mk, a.k_cache, kFp8, a.num_kv_heads, D, 1) ||
+      !encode_pool_map(&mv, a.v_cache, false, a.num_kv_heads, D, 1))
+    return KV_ERR_CUDA;
+  constexpr uint32_t kKChunks = kFp8 ? D / 128 : D / 64, kVChunks = D / 64;
+  p.k_box_bytes = kKChunks * kSub * 128;
+  p.v_box_bytes = kVChunks * kSub * 128;
+  p.stage_bytes = (kBN / kSub) * (p.k_box_bytes + p.v_box_bytes);
+  const int smem = int(1024 + kStages * p.stage_bytes);
+  auto kern = prefill_kernel<kFp8, D>;
+  // the dynamic shared-memory opt-in is set once per device and size
+  static int set_bytes[64] = {0};
+  const int dev_id = device_info().device;
+  if (dev_id < 0 || dev_id >= 64) return KV_ERR_CUDA;
+  if (set_bytes[dev_id] < smem) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+      return KV_ERR_CUDA;
+    set_bytes[dev_id] = smem;
+  }
+  kern<<<unsigned(grid), kThreads, smem, stream>>>(mk, mv, p);
+  return cudaGetLastError() == cudaSuccess ? KV_OK : KV_ERR_CUDA;
+}
+
+}  // namespace
+
+int launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
+  PrefillParams p{};
+  p.q = a.q;
+  p.block_tables = a.block_tables;
+  p.seq_lens = a.seq_lens;
+  p.qsl = a.query_start_loc;
+  p.output = a.output;
+  p.max_blocks_per_seq = a.max_blocks_per_seq;
+  p.num_seqs = a.num_seqs;
+  p.num_q_tokens = a.num_q_tokens;
+  p.num_q_heads = a.num_q_heads;
+  p.num_kv_heads = a.num_kv_heads;
+  p.group = a.num_q_heads / a.num_kv_heads;
+  p.block_size = a.block_size;
+  p.block_shift = uint32_t(__builtin_ctz(a.block_size));
+  p.q_stride = a.q_stride;
+  p.sliding_window = a.sliding_window;
+  p.score_scale = a.inv_sqrt_d * kLog2e * (a.fp8 ? a.k_scale : 1.0f);
+  // an upper bound of the item count: sum over sequences of
+  // ceil(n_s * group / 64) <= num_q_tokens * group / 64 + num_seqs
+  const uint64_t grid =
+      uint64_t(a.num_kv_heads) * ((uint64_t(a.num_q_tokens) * p.group + kBM - 1) / kBM + a.num_seqs);
+  if (grid == 0) return KV_OK;
+  if (grid > 0x7fffffffull) return KV_ERR_UNSUPPORTED;
+  const int key = (a.fp8 ? 100 : 0) + int(a.head_dim);
+  switch (key) {
+    case 64: return launch_prefill_t<false, 64>(a, stream, p, grid);
+    case 128: return launch_prefill_t<false, 128>(a, stream, p, grid);
+    case 228: return launch_prefill_t<true, 128>(a, stream, p, grid);
+    default: return KV_ERR_UNSUPPORTED;
+  }
+}
+
+cudaError_t read_and_clear_prefill_error(uint32_t* bits) {
+  uint32_t zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(bits, g_prefill_error, sizeof(uint32_t));
+  if (e != cudaSuccess) return e;
+  return cudaMemcpyToSymbol(g_prefill_error, &zero, sizeof(uint32_t));
+}
+
+}  // namespace pagedkv

@@ -30,6 +30,7 @@ def built():
     __graft_entry__.build()
     yield
     pk.kv_set_decode_workspace(None)
+    _WORKSPACE.clear()
 
 
 def u16(t: torch.Tensor) -> np.ndarray:
@@ -67,7 +68,11 @@ def gpu_slots(w) -> torch.Tensor:
     return slots
 
 
+_WORKSPACE = []  # the registered workspace stays alive until the next registration
+
+
 def with_workspace(w, on=True):
+    _WORKSPACE.clear()
     if not on:
         pk.kv_set_decode_workspace(None)
         return None
@@ -75,6 +80,7 @@ def with_workspace(w, on=True):
                                      w.head_dim, w.block_size)
     ws = torch.empty(n, dtype=torch.uint8, device=DEV)
     pk.kv_set_decode_workspace(ws)
+    _WORKSPACE.append(ws)
     return ws
 
 
@@ -507,6 +513,84 @@ def test_decode_clamps_overlong_sequence_and_flags_it():
     # the last block: the clamp must not read past the table, and the output is
     # finite where the clamped range holds data only; here it does not
     assert got.shape == (1, 4, 128)
+
+
+# ---------------------------------------------------------------------------
+# multi-token (chunked-prefill) paged attention
+# ---------------------------------------------------------------------------
+def _prefill_gpu(w, kc, vc, qsl, window, fp8, q_stride=None):
+    n_q = int(qsl[-1])
+    q_stride = q_stride or w.num_q_heads * w.head_dim
+    out = torch.full((max(n_q, 1), w.num_q_heads, w.head_dim), float("nan"), device=DEV)
+    args = (w.block_tables.to(DEV), w.seq_lens.to(DEV), torch.from_numpy(qsl).to(DEV), w.max_blocks_per_seq,
+            w.num_seqs, n_q, w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size, w.inv_sqrt_d)
+    q = w.q.to(DEV)
+    if fp8:
+        pk.paged_prefill_attn_fp8k(q, kc, vc, out, *args, w.k_scale, q_stride, window)
+    else:
+        pk.paged_prefill_attn_bf16(q, kc, vc, out, *args, q_stride, window)
+    return out[:n_q].cpu().numpy()
+
+
+def _prefill_ref(w, kr, vr, qsl, window, fp8):
+    return oracle.paged_prefill_attn(u16(w.q), None if fp8 else kr, kr if fp8 else None, vr,
+                                     w.block_tables.numpy(), w.seq_lens.numpy(), qsl, w.max_blocks_per_seq,
+                                     w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size,
+                                     w.inv_sqrt_d, w.k_scale, w.num_q_heads * w.head_dim, window)
+
+
+PREFILL_CASES = [
+    # (seq_lens, query tokens per sequence, Hq, H, D, bs, windows)
+    ([37, 100, 1, 16, 300, 65], [37, 20, 1, 16, 129, 1], 8, 2, 128, 16, (0, 1, 17, 100)),
+    ([700, 1000, 2049, 5], [700, 64, 333, 5], 32, 8, 128, 16, (0, 256)),
+    ([333, 64, 129], [100, 64, 3], 64, 8, 128, 64, (0, 63)),
+    ([500, 129, 40], [77, 129, 40], 16, 16, 64, 32, (0, 7)),
+    ([260, 1000], [260, 50], 16, 1, 128, 128, (0, 300)),
+    ([300, 77, 90], [31, 77, 90], 12, 4, 64, 256, (0, 50)),
+    ([3, 10, 0, 50], [5, 2, 0, 50], 8, 2, 128, 16, (0, 4)),      # more queries than positions; an empty sequence
+]
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+@pytest.mark.parametrize("case", range(len(PREFILL_CASES)))
+def test_prefill_cases(fp8, case):
+    lens, qlens, Hq, H, D, bs, windows = PREFILL_CASES[case]
+    if fp8 and D != 128:
+        pytest.skip("the FP8-K prefill supports head_dim 128")
+    w = kvgen.custom(200 + case, seq_lens=lens, num_q_heads=Hq, num_kv_heads=H, head_dim=D, block_size=bs,
+                     fp8=fp8, q_rows=max(sum(qlens), 1))
+    kc, vc, kr, vr = _caches(w, fp8)
+    qsl = np.concatenate([[0], np.cumsum(qlens)]).astype(np.int32)
+    for win in windows:
+        got = _prefill_gpu(w, kc, vc, qsl, win, fp8)
+        ref = _prefill_ref(w, kr, vr, qsl, win, fp8)
+        assert_decode_close(got, ref, f"prefill case {case} window {win}")
+    assert pk.kv_get_device_error() == 0
+
+
+def test_prefill_one_query_per_sequence_matches_the_decode():
+    w = kvgen.custom(230, seq_lens=[4000, 17, 900, 1], num_q_heads=32, num_kv_heads=8, head_dim=128, block_size=16)
+    kc, vc, kr, vr = _caches(w, False)
+    qsl = np.arange(w.num_seqs + 1, dtype=np.int32)
+    with_workspace(w, True)
+    dec = _decode_gpu(w, kc, vc, 0, False)
+    pre = _prefill_gpu(w, kc, vc, qsl, 0, False)
+    assert_decode_close(pre, dec, "prefill of one token vs decode")
+    assert_decode_close(pre, _decode_ref(w, kr, vr, 0, False), "prefill of one token vs oracle decode")
+
+
+def test_prefill_flags_a_decreasing_query_layout():
+    w = kvgen.custom(231, seq_lens=[40, 40], num_q_heads=4, num_kv_heads=2, head_dim=128, block_size=16,
+                     q_rows=10)
+    kc, vc, _, _ = _caches(w, False)
+    pk.kv_get_device_error()
+    qsl = np.array([0, 8, 4], np.int32)          # the second sequence would have -4 queries
+    out = torch.zeros((10, 4, 128), device=DEV)
+    pk.paged_prefill_attn_bf16(w.q.to(DEV), kc, vc, out, w.block_tables.to(DEV), w.seq_lens.to(DEV),
+                               torch.from_numpy(qsl).to(DEV), w.max_blocks_per_seq, 2, 10, 4, 2, 128, 16,
+                               w.inv_sqrt_d, 4 * 128, 0)
+    assert pk.kv_get_device_error() & 4
+    assert torch.isfinite(out).all()
 
 
 # ---------------------------------------------------------------------------
