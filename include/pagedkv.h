@@ -261,7 +261,8 @@ PAGEDKV_API int paged_decode_attn_fp8(const kv_bf16_t *q, const kv_e4m3_t *k_cac
  *                    fault word and that sequence's rows are skipped).
  *   output           device float32[num_q_tokens, num_q_heads, head_dim].
  * Supported: head_dim 64 or 128 (FP8: 128); block_size a power of two in
- * [16, 256]; q, caches and q_stride 16-byte aligned. No workspace is used.
+ * [16, 256]; q, caches, q_stride and output 16-byte aligned. No workspace
+ * is used.
  * ---------------------------------------------------------------------- */
 PAGEDKV_API int paged_prefill_attn_bf16(const kv_bf16_t *q, const kv_bf16_t *k_cache, const kv_bf16_t *v_cache,
                                         float *output, const int32_t *block_tables, const int32_t *seq_lens,

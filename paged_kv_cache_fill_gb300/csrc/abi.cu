@@ -300,7 +300,7 @@ static int prefill_common(const kv_bf16_t* q, const void* k_cache, const kv_bf16
   if (!is_pow2(block_size) || block_size < 16 || block_size > 256) return KV_ERR_UNSUPPORTED;
   if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || (q_stride * 2u) % 16)
     return KV_ERR_UNSUPPORTED;
-  if (!aligned(output, 8)) return KV_ERR_UNSUPPORTED;
+  if (!aligned(output, 16)) return KV_ERR_UNSUPPORTED;
   if (uint64_t(max_blocks_per_seq) * block_size >= (1ull << 31)) return KV_ERR_UNSUPPORTED;
   if (uint64_t(num_q_tokens) * num_q_heads >= (1ull << 31)) return KV_ERR_UNSUPPORTED;
   const DeviceInfo& dev = device_info();

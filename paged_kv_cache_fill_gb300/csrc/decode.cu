@@ -732,7 +732,7 @@ static PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
 // shared-memory tile is [chunk][slot][128 bytes], 128-byte swizzled by slot
 // row. (Dim 1's stride exceeds dim 2's; the encoder accepts any order.)
 bool encode_pool_map(CUtensorMap* map, const void* base, bool fp8, uint32_t num_kv_heads,
-                     uint32_t head_dim, uint32_t heads_per_item) {
+                     uint32_t head_dim, uint32_t heads_per_item, uint32_t box_chunks) {
   auto encode = get_encode();
   if (!encode) return false;
   const uint32_t elem = fp8 ? 1 : 2;
@@ -740,7 +740,7 @@ bool encode_pool_map(CUtensorMap* map, const void* base, bool fp8, uint32_t num_
   const uint32_t chunks_per_head = head_dim * elem / 128;
   cuuint64_t dims[3] = {chunk_elems, cuuint64_t(1) << 31, cuuint64_t(num_kv_heads) * chunks_per_head};
   cuuint64_t strides[2] = {cuuint64_t(num_kv_heads) * head_dim * elem, 128};
-  cuuint32_t box[3] = {chunk_elems, kTile, heads_per_item * chunks_per_head};
+  cuuint32_t box[3] = {chunk_elems, kTile, box_chunks ? box_chunks : heads_per_item * chunks_per_head};
   cuuint32_t estr[3] = {1, 1, 1};
   const CUresult r = encode(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16, 3,
                             const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,

@@ -46,10 +46,11 @@ cudaError_t launch_fused_k_norm_rope(const uint16_t* k_in, const uint16_t* k_nor
 
 // Tensor map over a cache pool [num_blocks, block_size, num_kv_heads,
 // head_dim] (bf16, or e4m3 when fp8) whose box is one 128-byte chunk x 16
-// slots x (heads_per_item x chunks per head): the shared-memory tile is
-// [chunk][slot][128 B], 128-byte swizzled by slot row.
+// slots x (heads_per_item x chunks per head, or box_chunks when nonzero):
+// the shared-memory tile is [chunk][slot][128 B], 128-byte swizzled by slot
+// row.
 bool encode_pool_map(CUtensorMap* map, const void* base, bool fp8, uint32_t num_kv_heads, uint32_t head_dim,
-                     uint32_t heads_per_item);
+                     uint32_t heads_per_item, uint32_t box_chunks = 0);
 
 // Multi-token (chunked-prefill) paged attention; returns a KV_* status.
 struct PrefillArgs {

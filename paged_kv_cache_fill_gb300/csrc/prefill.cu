@@ -62,11 +62,13 @@ struct Item {
   int32_t n, qstart, len;            // query tokens, their first row in q, cached positions
 };
 
+template <int BM>
 __device__ __forceinline__ uint32_t row_blocks(int64_t n, uint32_t group) {
-  return uint32_t((n * group + kBM - 1) / kBM);
+  return uint32_t((n * group + BM - 1) / BM);
 }
 
-// The item of CTA `target` (seq < 0: none). Run by one warp.
+// The item of CTA `target` (seq < 0: none), items of BM rows. Run by one warp.
+template <int BM>
 __device__ Item locate(uint32_t target, const PrefillParams& p, uint32_t lane) {
   Item it{};
   it.seq = -1;
@@ -82,7 +84,7 @@ __device__ Item locate(uint32_t target, const PrefillParams& p, uint32_t lane) {
         n = 0;
       }
     }
-    const uint32_t items = row_blocks(n, p.group) * p.num_kv_heads;
+    const uint32_t items = row_blocks<BM>(n, p.group) * p.num_kv_heads;
     uint32_t incl = items;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -95,13 +97,13 @@ __device__ Item locate(uint32_t target, const PrefillParams& p, uint32_t lane) {
       const uint32_t sl = __ffs(__ballot_sync(0xffffffffu, incl > rel)) - 1;
       const uint32_t local = rel - (__shfl_sync(0xffffffffu, incl, sl) - __shfl_sync(0xffffffffu, items, sl));
       const int64_t ns = __shfl_sync(0xffffffffu, n, sl);
-      const uint32_t nblk = row_blocks(ns, p.group);
+      const uint32_t nblk = row_blocks<BM>(ns, p.group);
       const uint32_t blk = nblk - 1 - local / p.num_kv_heads;  // longest key range first
       it.seq = int32_t(s0 + sl);
       it.kv_head = int32_t(local % p.num_kv_heads);
-      it.row0 = int32_t(blk * kBM);
+      it.row0 = int32_t(blk * BM);
       const int64_t rows_total = ns * p.group;
-      it.rows = int32_t(rows_total - it.row0 < kBM ? rows_total - it.row0 : kBM);
+      it.rows = int32_t(rows_total - it.row0 < BM ? rows_total - it.row0 : BM);
       it.n = int32_t(ns);
       it.qstart = __ldg(p.qsl + it.seq);
       int32_t L = __ldg(p.seq_lens + it.seq);
@@ -140,7 +142,7 @@ __global__ void __launch_bounds__(kThreads)
     fence_mbar_init();
   }
   if (warp == 0) {
-    const Item it = locate(blockIdx.x, p, lane);
+    const Item it = locate<kBM>(blockIdx.x, p, lane);
     if (lane == 0) s_item = it;
   }
   __syncthreads();
@@ -429,6 +431,338 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
+// ---------------------------------------------------------------- tcgen05 path (BF16 cache)
+// One CTA per (sequence, KV head, block of 128 rows), 192 threads:
+//   warp 0      TMA producer: 64-key K and V tiles, each [chunk][key][128 B]
+//               (one box per 16-slot block run and 64-element chunk), 3 stages;
+//   warp 1      owns TMEM and issues every tcgen05.mma from one thread:
+//               S = Q K^T (M 128, N 64, K = head_dim) into one of two TMEM
+//               S buffers, then O += P_hi V + P_lo V (M 128, N = head_dim,
+//               K 64) into TMEM O, V read as the MN-major operand;
+//   warps 2..5  softmax, one thread per row = TMEM lane (warp w owns lanes
+//               32 (w % 4) ..): Q rows into shared memory, then per tile
+//               S row via tcgen05.ld, masks, base-2 online softmax, O row
+//               rescale in TMEM when the row max moved, P hi / lo rows into
+//               shared memory, and at the end O / l to the output.
+// S of tile i + 1 is computed while the softmax works on tile i.
+constexpr int kTcBM = 128, kTcBN = 64, kTcStages = 3, kTcThreads = 192;
+
+template <int D>
+struct TcLayout {  // byte offsets from the 1024-aligned shared base
+  static constexpr uint32_t kChunks = D / 64;
+  static constexpr uint32_t kQ = 0;                           // [chunk][128 rows][128 B]
+  static constexpr uint32_t kPHi = kChunks * kTcBM * 128;     // [128 rows][128 B] (64 keys)
+  static constexpr uint32_t kPLo = kPHi + kTcBM * 128;
+  static constexpr uint32_t kStage0 = kPLo + kTcBM * 128;
+  static constexpr uint32_t kKBytes = kChunks * kTcBN * 128;  // [chunk][64 keys][128 B]
+  static constexpr uint32_t kStageBytes = 2 * kKBytes;        // K, then V
+  static constexpr uint32_t kBytes = kStage0 + kTcStages * kStageBytes;
+  static constexpr uint32_t kTmemCols = 256;                  // S buffers [0, 64), [64, 128); O [128, 128 + D)
+  static constexpr uint32_t kOCol = 128;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
+                      const PrefillParams p) {
+  using Lay = TcLayout<D>;
+  constexpr uint32_t kChunks = Lay::kChunks;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+  const uint32_t sbase = smem_u32(smem);
+  __shared__ uint64_t kv_full[kTcStages], kv_empty[kTcStages], s_full[2], s_free[2];
+  __shared__ uint64_t p_full, o_full, q_full, mma_done;
+  __shared__ uint32_t tmem_base_s;
+  __shared__ Item s_item;
+
+  const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kTcStages; ++s) {
+      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&s_full[b], 1);
+      mbar_init(&s_free[b], 128);
+    }
+    mbar_init(&p_full, 128);
+    mbar_init(&o_full, 1);
+    mbar_init(&q_full, 128);
+    mbar_init(&mma_done, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    const Item it = locate<kTcBM>(blockIdx.x, p, lane);
+    if (lane == 0) s_item = it;
+  }
+  __syncthreads();
+  const Item it = s_item;
+  if (it.seq < 0) return;
+  if (warp == 1) tmem_alloc(&tmem_base_s, Lay::kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_s;
+
+  const int32_t g = int32_t(p.group);
+  const int32_t pos_first = it.len - it.n + it.row0 / g;
+  const int32_t pos_last = it.len - it.n + (it.row0 + it.rows - 1) / g;
+  const int32_t k_hi = pos_last + 1;  // keys [k_lo, k_hi)
+  const int32_t W = int32_t(p.sliding_window);
+  int32_t k_lo = 0;
+  if (W > 0 && pos_first + 1 - W > 0) k_lo = pos_first + 1 - W;
+  const int32_t t_begin = k_lo / kTcBN;
+  const int32_t t_end = k_hi > 0 ? (k_hi + kTcBN - 1) / kTcBN : t_begin;
+  const int32_t T = t_end - t_begin;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    tma_prefetch_desc(&tmap_k);
+    tma_prefetch_desc(&tmap_v);
+    const int32_t* table = p.block_tables + uint64_t(it.seq) * p.max_blocks_per_seq;
+    bool ok = true;
+    for (int32_t i = 0; i < T && ok; ++i) {
+      const uint32_t st = uint32_t(i) % kTcStages;
+      const int32_t key0 = (t_begin + i) * kTcBN + int32_t(lane) * kSub;
+      const bool mine = lane < uint32_t(kTcBN / kSub) && key0 < k_hi;
+      const int32_t block_id = mine ? __ldg(table + (key0 >> p.block_shift)) : 0;
+      if (lane == 0 && i >= kTcStages && !mbar_wait(&kv_empty[st], ((i / kTcStages) - 1) & 1)) ok = false;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      const uint32_t loaded = __popc(__ballot_sync(0xffffffffu, mine));
+      if (lane == 0) mbar_arrive_expect_tx(&kv_full[st], loaded * 2u * kChunks * (kSub * 128));
+      __syncwarp();
+      if (mine) {
+        const int32_t slot0 = (block_id << p.block_shift) + (key0 & int32_t(p.block_size - 1));
+        uint8_t* kdst = smem + Lay::kStage0 + st * Lay::kStageBytes + lane * (kSub * 128);
+#pragma unroll
+        for (uint32_t c = 0; c < kChunks; ++c) {
+          tma_load_3d(kdst + c * (kTcBN * 128), &tmap_k, 0, slot0, it.kv_head * kChunks + c, &kv_full[st]);
+          tma_load_3d(kdst + Lay::kKBytes + c * (kTcBN * 128), &tmap_v, 0, slot0, it.kv_head * kChunks + c,
+                      &kv_full[st]);
+        }
+      }
+    }
+    if (!ok && lane == 0) atomicOr(&g_prefill_error, kErrWaitTimeout);
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issue
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = umma_idesc_bf16(kTcBM, kTcBN, false);
+      constexpr uint32_t idesc_o = umma_idesc_bf16(kTcBM, D, true);
+      bool ok = mbar_wait(&q_full, 0);
+      tc_fence_after();
+      auto issue_s = [&](int32_t i) -> bool {
+        const uint32_t st = uint32_t(i) % kTcStages, b = uint32_t(i) & 1;
+        if (!mbar_wait(&kv_full[st], (i / kTcStages) & 1)) return false;
+        if (i >= 2 && !mbar_wait(&s_free[b], ((i - 2) >> 1) & 1)) return false;
+        tc_fence_after();
+        const uint32_t kb = sbase + Lay::kStage0 + st * Lay::kStageBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t c = kk >> 2, off = (kk & 3) * 32;
+          umma_bf16(tmem + b * kTcBN, umma_desc_sw128(sbase + Lay::kQ + c * (kTcBM * 128) + off, 16, 1024),
+                    umma_desc_sw128(kb + c * (kTcBN * 128) + off, 16, 1024), idesc_s, kk > 0);
+        }
+        umma_commit(&s_full[b]);
+        return true;
+      };
+      if (ok && T > 0) ok = issue_s(0);
+      for (int32_t i = 0; i < T && ok; ++i) {
+        if (i + 1 < T && !issue_s(i + 1)) {
+          ok = false;
+          break;
+        }
+        if (!mbar_wait(&p_full, uint32_t(i) & 1)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t st = uint32_t(i) % kTcStages;
+        const uint32_t vb = sbase + Lay::kStage0 + st * Lay::kStageBytes + Lay::kKBytes;
+#pragma unroll
+        for (int kk = 0; kk < kTcBN / 16; ++kk) {
+          const uint64_t vd = umma_desc_sw128(vb + kk * (16 * 128), kTcBN * 128, 1024);
+          umma_bf16(tmem + Lay::kOCol, umma_desc_sw128(sbase + Lay::kPHi + kk * 32, 16, 1024), vd, idesc_o,
+                    i > 0 || kk > 0);
+          umma_bf16(tmem + Lay::kOCol, umma_desc_sw128(sbase + Lay::kPLo + kk * 32, 16, 1024), vd, idesc_o, true);
+        }
+        umma_commit(&o_full);
+        umma_commit(&kv_empty[st]);
+      }
+      if (!ok) atomicOr(&g_prefill_error, kErrWaitTimeout);
+      // every issued MMA has finished before TMEM is released
+      umma_commit(&mma_done);
+      mbar_wait(&mma_done, 0);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax
+    const uint32_t quad = warp & 3;             // TMEM lanes 32 quad .. 32 quad + 31
+    const uint32_t row = quad * 32 + lane;      // the item's row = TMEM lane
+    const uint32_t lane_addr = (quad * 32u) << 16;
+    const bool valid = int32_t(row) < it.rows;
+    const int32_t grow = it.row0 + int32_t(row);
+    const int32_t t = grow / g, hh = grow % g;
+    const int32_t pos = valid ? it.len - it.n + t : -1;  // -1: attends nothing
+    const int32_t lo = W > 0 ? pos + 1 - W : INT32_MIN;
+    // Q row, 128-byte swizzled, zeros for rows past the item
+    const uint16_t* qr = valid ? p.q + uint64_t(it.qstart + t) * p.q_stride + uint64_t(it.kv_head * g + hh) * D
+                               : nullptr;
+#pragma unroll
+    for (uint32_t u = 0; u < D / 8; ++u) {
+      const uint4 v = qr ? *reinterpret_cast<const uint4*>(qr + 8 * u) : make_uint4(0, 0, 0, 0);
+      const uint32_t c = u >> 3, uu = u & 7;
+      *reinterpret_cast<uint4*>(smem + Lay::kQ + c * (kTcBM * 128) + row * 128 + ((uu ^ (row & 7)) << 4)) = v;
+    }
+    fence_async_smem();
+    mbar_arrive(&q_full);
+
+    float m_run = -INFINITY, l_run = 0.0f;
+    bool ok = true;
+    for (int32_t i = 0; i < T; ++i) {
+      const uint32_t b = uint32_t(i) & 1, st = uint32_t(i) % kTcStages;
+      ok = __all_sync(0xffffffffu, mbar_wait(&s_full[b], (uint32_t(i) >> 1) & 1));
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t sv[kTcBN];
+      tmem_ld32(tmem + lane_addr + b * kTcBN, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+      tmem_ld32(tmem + lane_addr + b * kTcBN + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(&s_free[b]);
+      float x[kTcBN];
+#pragma unroll
+      for (int j = 0; j < kTcBN; ++j) x[j] = __uint_as_float(sv[j]) * p.score_scale;
+      const int32_t key_base = (t_begin + i) * kTcBN;
+      if (key_base + kTcBN - 1 > pos || key_base < lo) {
+#pragma unroll
+        for (int j = 0; j < kTcBN; ++j)
+          if (key_base + j > pos || key_base + j < lo) x[j] = -INFINITY;
+      }
+      float mx = m_run;
+#pragma unroll
+      for (int j = 0; j < kTcBN; ++j) mx = fmaxf(mx, x[j]);
+      const float mb = mx == -INFINITY ? 0.0f : mx;  // a row with nothing attended yet stays at zero
+      float sum = 0.0f;
+#pragma unroll
+      for (int j = 0; j < kTcBN; ++j) {
+        x[j] = fast_exp2(x[j] - mb);
+        sum += x[j];
+      }
+      // PV of the previous tile done: O is stable and the P buffers are free
+      if (i > 0) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&o_full, uint32_t(i - 1) & 1));
+        if (!ok) break;
+        tc_fence_after();
+      }
+      const float al = fast_exp2(m_run - mb);  // 1 when the max did not move, 0 before the first key
+      if (i > 0 && __any_sync(0xffffffffu, mx != m_run)) {
+#pragma unroll
+        for (uint32_t c0 = 0; c0 < D; c0 += 32) {
+          uint32_t ov[32];
+          tmem_ld32(tmem + lane_addr + Lay::kOCol + c0, ov);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * al);
+          tmem_st32(tmem + lane_addr + Lay::kOCol + c0, ov);
+        }
+        tmem_wait_st();
+      }
+      l_run = l_run * al + sum;
+      m_run = mx;
+      // the last tile's V rows at or past k_hi were not loaded, or hold
+      // positions past every query: zero them for the PV product
+      if (key_base + kTcBN > k_hi) {
+        mbar_wait(&kv_full[st], (uint32_t(i) / kTcStages) & 1);  // already complete: orders after the TMA
+        const int32_t z0 = k_hi - key_base > 0 ? k_hi - key_base : 0;
+        uint8_t* vb = smem + Lay::kStage0 + st * Lay::kStageBytes + Lay::kKBytes;
+        const uint32_t units = uint32_t(kTcBN - z0) * kChunks * 8;
+        for (uint32_t e = threadIdx.x - 64; e < units; e += 128) {
+          const uint32_t r = uint32_t(z0) + e / (kChunks * 8), rest = e % (kChunks * 8);
+          *reinterpret_cast<uint4*>(vb + (rest >> 3) * (kTcBN * 128) + r * 128 + ((rest & 7) << 4)) =
+              make_uint4(0, 0, 0, 0);
+        }
+      }
+      // P hi / lo rows, 128-byte swizzled
+#pragma unroll
+      for (uint32_t u = 0; u < kTcBN / 8; ++u) {
+        uint32_t hi[4], lw[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float x0 = x[8 * u + 2 * q], x1 = x[8 * u + 2 * q + 1];
+          hi[q] = f32x2_to_bf16x2(x0, x1);
+          lw[q] = f32x2_to_bf16x2(x0 - bf16_lo_to_f32(hi[q]), x1 - bf16_hi_to_f32(hi[q]));
+        }
+        const uint32_t off = row * 128 + ((u ^ (row & 7)) << 4);
+        *reinterpret_cast<uint4*>(smem + Lay::kPHi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4*>(smem + Lay::kPLo + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+      }
+      fence_async_smem();
+      tc_fence_before();
+      mbar_arrive(&p_full);
+    }
+    if (!ok && lane == 0) atomicOr(&g_prefill_error, kErrWaitTimeout);
+    // ---- O / l to the output row
+    if (ok && T > 0) {
+      ok = __all_sync(0xffffffffu, mbar_wait(&o_full, uint32_t(T - 1) & 1));
+      tc_fence_after();
+    }
+    const float inv = l_run > 0.0f ? 1.0f / l_run : 0.0f;
+    float* o = valid ? p.output + (uint64_t(it.qstart + t) * p.num_q_heads + uint64_t(it.kv_head * g + hh)) * D
+                     : nullptr;
+#pragma unroll
+    for (uint32_t c0 = 0; c0 < D; c0 += 32) {
+      uint32_t ov[32];
+      if (ok && T > 0) {
+        tmem_ld32(tmem + lane_addr + Lay::kOCol + c0, ov);
+        tmem_wait_ld();
+      }
+      if (o && ok) {
+#pragma unroll
+        for (int j = 0; j < 32; j += 4) {
+          const float4 w4 = T > 0 ? make_float4(__uint_as_float(ov[j]) * inv, __uint_as_float(ov[j + 1]) * inv,
+                                                __uint_as_float(ov[j + 2]) * inv, __uint_as_float(ov[j + 3]) * inv)
+                                  : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+          *reinterpret_cast<float4*>(o + c0 + j) = w4;
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, Lay::kTmemCols);
+  }
+}
+
+template <int D>
+int launch_prefill_tc(const PrefillArgs& a, cudaStream_t stream, PrefillParams& p) {
+  CUtensorMap mk, mv;
+  // one 64-element chunk per box: each box lands in its chunk's [64 keys] tile
+  if (!encode_pool_map(&mk, a.k_cache, false, a.num_kv_heads, D, 1, 1) ||
+      !encode_pool_map(&mv, a.v_cache, false, a.num_kv_heads, D, 1, 1))
+    return KV_ERR_CUDA;
+  // grid: an upper bound of the item count, as for the mma.sync path
+  const uint64_t grid =
+      uint64_t(a.num_kv_heads) * ((uint64_t(a.num_q_tokens) * p.group + kTcBM - 1) / kTcBM + a.num_seqs);
+  if (grid == 0) return KV_OK;
+  if (grid > 0x7fffffffull) return KV_ERR_UNSUPPORTED;
+  const int smem = int(1024 + TcLayout<D>::kBytes);
+  auto kern = prefill_tc_kernel<D>;
+  static int set_bytes[64] = {0};
+  const int dev_id = device_info().device;
+  if (dev_id < 0 || dev_id >= 64) return KV_ERR_CUDA;
+  if (set_bytes[dev_id] < smem) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+      return KV_ERR_CUDA;
+    set_bytes[dev_id] = smem;
+  }
+  kern<<<unsigned(grid), kTcThreads, smem, stream>>>(mk, mv, p);
+  return cudaGetLastError() == cudaSuccess ? KV_OK : KV_ERR_CUDA;
+}
+
 template <bool kFp8, int D>
 int launch_prefill_t(const PrefillArgs& a, cudaStream_t stream, PrefillParams& p, uint64_t grid) {
   CUtensorMap mk, mv;
@@ -482,9 +816,9 @@ int launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   if (grid > 0x7fffffffull) return KV_ERR_UNSUPPORTED;
   const int key = (a.fp8 ? 100 : 0) + int(a.head_dim);
   switch (key) {
-    case 64: return launch_prefill_t<false, 64>(a, stream, p, grid);
-    case 128: return launch_prefill_t<false, 128>(a, stream, p, grid);
-    case 228: return launch_prefill_t<true, 128>(a, stream, p, grid);
+    case 64: return launch_prefill_tc<64>(a, stream, p);     // BF16: tcgen05 / TMEM
+    case 128: return launch_prefill_tc<128>(a, stream, p);
+    case 228: return launch_prefill_t<true, 128>(a, stream, p, grid);  // FP8 K: mma.sync
     default: return KV_ERR_UNSUPPORTED;
   }
 }
