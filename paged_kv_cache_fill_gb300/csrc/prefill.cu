@@ -432,33 +432,42 @@ __global__ void __launch_bounds__(kThreads)
 }
 
 // ---------------------------------------------------------------- tcgen05 path (BF16 cache)
-// One CTA per (sequence, KV head, block of 128 rows), 192 threads:
-//   warp 0      TMA producer: 64-key K and V tiles, each [chunk][key][128 B]
-//               (one box per 16-slot block run and 64-element chunk), 3 stages;
+// One CTA per (sequence, KV head, block of 128 rows), 352 threads:
+//   warps 0, 10 TMA producers of 128-key K and V tiles, each [chunk][key][128 B]
+//               (one box per 16-slot block run and 64-element chunk), in two
+//               2-stage rings: a K stage is free once its S is done, a V stage
+//               once its PV is;
 //   warp 1      owns TMEM and issues every tcgen05.mma from one thread:
-//               S = Q K^T (M 128, N 64, K = head_dim) into one of two TMEM
+//               S = Q K^T (M 128, N 128, K = head_dim) into one of two TMEM
 //               S buffers, then O += P_hi V + P_lo V (M 128, N = head_dim,
-//               K 64) into TMEM O, V read as the MN-major operand;
-//   warps 2..5  softmax, one thread per row = TMEM lane (warp w owns lanes
-//               32 (w % 4) ..): Q rows into shared memory, then per tile
-//               S row via tcgen05.ld, masks, base-2 online softmax, O row
-//               rescale in TMEM when the row max moved, P hi / lo rows into
-//               shared memory, and at the end O / l to the output.
+//               K 128) into TMEM O, P from TMEM (written over its S buffer),
+//               V read as the MN-major shared-memory operand;
+//   warps 2..9  softmax, two threads per row = TMEM lane (warp w owns lanes
+//               32 (w % 4) ..; warps 2..5 the first half of a tile's keys and
+//               of O's columns, warps 6..9 the second): Q rows into shared
+//               memory, then per tile S via tcgen05.ld, masks, base-2 online
+//               softmax (the pair swaps partial row maxima), O rescale in
+//               TMEM when a row max moved, P hi / lo into TMEM (the PV MMA
+//               reads its A operand from tensor memory, sparing shared memory
+//               bandwidth), and at the end O / l to the output.
 // S of tile i + 1 is computed while the softmax works on tile i.
-constexpr int kTcBM = 128, kTcBN = 64, kTcStages = 3, kTcThreads = 192;
+constexpr int kTcBM = 128, kTcBN = 128, kTcStages = 2, kTcWarps = 11, kTcThreads = 32 * kTcWarps;
+constexpr float kRescaleLog2 = 8.0f;  // reference-max slack of the online softmax (base 2)
 
 template <int D>
 struct TcLayout {  // byte offsets from the 1024-aligned shared base
   static constexpr uint32_t kChunks = D / 64;
   static constexpr uint32_t kQ = 0;                           // [chunk][128 rows][128 B]
-  static constexpr uint32_t kPHi = kChunks * kTcBM * 128;     // [128 rows][128 B] (64 keys)
-  static constexpr uint32_t kPLo = kPHi + kTcBM * 128;
-  static constexpr uint32_t kStage0 = kPLo + kTcBM * 128;
-  static constexpr uint32_t kKBytes = kChunks * kTcBN * 128;  // [chunk][64 keys][128 B]
+  static constexpr uint32_t kStage0 = kChunks * kTcBM * 128;
+  static constexpr uint32_t kKBytes = kChunks * kTcBN * 128;  // [chunk][128 keys][128 B]
   static constexpr uint32_t kStageBytes = 2 * kKBytes;        // K, then V
   static constexpr uint32_t kBytes = kStage0 + kTcStages * kStageBytes;
-  static constexpr uint32_t kTmemCols = 256;                  // S buffers [0, 64), [64, 128); O [128, 128 + D)
-  static constexpr uint32_t kOCol = 128;
+  // TMEM columns: three S buffers [0, 128), [128, 256), [256, 384), each
+  // overwritten by its tile's P once read (hi [+0, +64), lo [+64, +128): 128
+  // keys, 2 per column); O [384, 384 + D)
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kOCol = 384;
+  static constexpr uint32_t kSBufs = 3;
 };
 
 template <int D>
@@ -471,24 +480,31 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
   const uint32_t sbase = smem_u32(smem);
-  __shared__ uint64_t kv_full[kTcStages], kv_empty[kTcStages], s_full[2], s_free[2];
-  __shared__ uint64_t p_full, o_full, q_full, mma_done;
+  __shared__ uint64_t k_full[kTcStages], v_full[kTcStages];
+  __shared__ uint64_t s_full[3], p_full[3], o_full[3], q_full, mma_done;  // per S/P buffer
   __shared__ uint32_t tmem_base_s;
   __shared__ Item s_item;
+  __shared__ float s_xchg[2][2][kTcBM];  // [tile parity][half][row] partial row maxima
+  __shared__ float s_lsum[2][kTcBM];     // [half][row] partial row sums, at the end
+  __shared__ uint64_t xchg_bar[4][2], lsum_bar[4];  // per TMEM lane quarter: the pair of warps
 
   const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kTcStages; ++s) {
-      mbar_init(&kv_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
+      mbar_init(&k_full[s], 1);
+      mbar_init(&v_full[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < 3; ++b) {
       mbar_init(&s_full[b], 1);
-      mbar_init(&s_free[b], 128);
+      mbar_init(&p_full[b], 256);
+      mbar_init(&o_full[b], 1);
     }
-    mbar_init(&p_full, 128);
-    mbar_init(&o_full, 1);
-    mbar_init(&q_full, 128);
+    mbar_init(&q_full, 256);
+    for (int qd = 0; qd < 4; ++qd) {
+      mbar_init(&xchg_bar[qd][0], 64);
+      mbar_init(&xchg_bar[qd][1], 64);
+      mbar_init(&lsum_bar[qd], 64);
+    }
     mbar_init(&mma_done, 1);
     fence_mbar_init();
   }
@@ -516,10 +532,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int32_t t_end = k_hi > 0 ? (k_hi + kTcBN - 1) / kTcBN : t_begin;
   const int32_t T = t_end - t_begin;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    tma_prefetch_desc(&tmap_k);
-    tma_prefetch_desc(&tmap_v);
+  if (warp == 0 || warp == kTcWarps - 1) {
+    // ------------------------------------------------------------ producers
+    // warp 0 loads K, the last warp V, each into its own ring: a K stage is
+    // free again once its S product is done, a V stage once its PV is
+    // a K stage is free once the S product two tiles back is done (s_full),
+    // a V stage once that tile's PV is done (o_full): the MMA thread commits
+    // nothing extra for the producers, and loads are in order, so those
+    // barriers cannot have moved on to a later tile of the same buffer yet
+    const bool is_k = warp == 0;
+    const CUtensorMap* map = is_k ? &tmap_k : &tmap_v;
+    uint64_t* full = is_k ? k_full : v_full;
+    uint64_t* done_bar = is_k ? s_full : o_full;
+    static_assert(kTcStages == 2, "stage reuse waits on tile i - 2");
+    tma_prefetch_desc(map);
     const int32_t* table = p.block_tables + uint64_t(it.seq) * p.max_blocks_per_seq;
     bool ok = true;
     for (int32_t i = 0; i < T && ok; ++i) {
@@ -527,21 +553,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int32_t key0 = (t_begin + i) * kTcBN + int32_t(lane) * kSub;
       const bool mine = lane < uint32_t(kTcBN / kSub) && key0 < k_hi;
       const int32_t block_id = mine ? __ldg(table + (key0 >> p.block_shift)) : 0;
-      if (lane == 0 && i >= kTcStages && !mbar_wait(&kv_empty[st], ((i / kTcStages) - 1) & 1)) ok = false;
+      if (lane == 0 && i >= kTcStages &&
+          !mbar_wait(&done_bar[(i - kTcStages) % Lay::kSBufs], uint32_t((i - kTcStages) / Lay::kSBufs) & 1))
+        ok = false;
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       const uint32_t loaded = __popc(__ballot_sync(0xffffffffu, mine));
-      if (lane == 0) mbar_arrive_expect_tx(&kv_full[st], loaded * 2u * kChunks * (kSub * 128));
+      if (lane == 0) mbar_arrive_expect_tx(&full[st], loaded * kChunks * (kSub * 128));
       __syncwarp();
       if (mine) {
         const int32_t slot0 = (block_id << p.block_shift) + (key0 & int32_t(p.block_size - 1));
-        uint8_t* kdst = smem + Lay::kStage0 + st * Lay::kStageBytes + lane * (kSub * 128);
+        uint8_t* dst = smem + Lay::kStage0 + st * Lay::kStageBytes + (is_k ? 0u : Lay::kKBytes) + lane * (kSub * 128);
 #pragma unroll
-        for (uint32_t c = 0; c < kChunks; ++c) {
-          tma_load_3d(kdst + c * (kTcBN * 128), &tmap_k, 0, slot0, it.kv_head * kChunks + c, &kv_full[st]);
-          tma_load_3d(kdst + Lay::kKBytes + c * (kTcBN * 128), &tmap_v, 0, slot0, it.kv_head * kChunks + c,
-                      &kv_full[st]);
-        }
+        for (uint32_t c = 0; c < kChunks; ++c)
+          tma_load_3d(dst + c * (kTcBN * 128), map, 0, slot0, it.kv_head * kChunks + c, &full[st]);
       }
     }
     if (!ok && lane == 0) atomicOr(&g_prefill_error, kErrWaitTimeout);
@@ -550,19 +575,31 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idesc_s = umma_idesc_bf16(kTcBM, kTcBN, false);
       constexpr uint32_t idesc_o = umma_idesc_bf16(kTcBM, D, true);
+      // Descriptors are built once: a k-step or a stage moves only the start
+      // address field (bits 0-13, in 16-byte units), so each MMA adds a small
+      // constant. One thread issues every MMA, so its instruction count per
+      // MMA sets the issue rate.
+      const uint64_t q_desc = umma_desc_sw128(sbase + Lay::kQ, 16, 1024);
+      const uint64_t k_desc0 = umma_desc_sw128(sbase + Lay::kStage0, 16, 1024);
+      const uint64_t v_desc0 = umma_desc_sw128(sbase + Lay::kStage0 + Lay::kKBytes, kTcBN * 128, 1024);
+      constexpr uint64_t kStageStep = Lay::kStageBytes >> 4;
+      const uint32_t tmem_o = tmem + Lay::kOCol;
       bool ok = mbar_wait(&q_full, 0);
       tc_fence_after();
       auto issue_s = [&](int32_t i) -> bool {
-        const uint32_t st = uint32_t(i) % kTcStages, b = uint32_t(i) & 1;
-        if (!mbar_wait(&kv_full[st], (i / kTcStages) & 1)) return false;
-        if (i >= 2 && !mbar_wait(&s_free[b], ((i - 2) >> 1) & 1)) return false;
+        const uint32_t st = uint32_t(i) % kTcStages, b = uint32_t(i) % Lay::kSBufs;
+        if (!mbar_wait(&k_full[st], (i / kTcStages) & 1)) return false;
+        // buffer b holds tile i - 3's P until its PV is done
+        if (i >= 3 && !mbar_wait(&o_full[b], uint32_t((i - 3) / 3) & 1)) return false;
         tc_fence_after();
-        const uint32_t kb = sbase + Lay::kStage0 + st * Lay::kStageBytes;
+        const uint64_t kd = k_desc0 + st * kStageStep;
+        const uint32_t tmem_s = tmem + b * kTcBN;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t c = kk >> 2, off = (kk & 3) * 32;
-          umma_bf16(tmem + b * kTcBN, umma_desc_sw128(sbase + Lay::kQ + c * (kTcBM * 128) + off, 16, 1024),
-                    umma_desc_sw128(kb + c * (kTcBN * 128) + off, 16, 1024), idesc_s, kk > 0);
+          // chunk kk / 4 of Q is kTcBM rows of 128 B further, of K kTcBN rows
+          const uint64_t off_q = uint64_t((kk >> 2) * (kTcBM * 128) + (kk & 3) * 32) >> 4;
+          const uint64_t off_k = uint64_t((kk >> 2) * (kTcBN * 128) + (kk & 3) * 32) >> 4;
+          umma_bf16(tmem_s, q_desc + off_q, kd + off_k, idesc_s, kk > 0);
         }
         umma_commit(&s_full[b]);
         return true;
@@ -573,22 +610,27 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           ok = false;
           break;
         }
-        if (!mbar_wait(&p_full, uint32_t(i) & 1)) {
+        // per-buffer: the softmax cannot get a phase ahead on buffer i % 3
+        // before PV i, which reads it, has been issued
+        if (!mbar_wait(&p_full[i % 3], uint32_t(i / 3) & 1)) {
+          ok = false;
+          break;
+        }
+        const uint32_t st = uint32_t(i) % kTcStages, pb = uint32_t(i) % Lay::kSBufs;
+        if (!mbar_wait(&v_full[st], (i / kTcStages) & 1)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t st = uint32_t(i) % kTcStages;
-        const uint32_t vb = sbase + Lay::kStage0 + st * Lay::kStageBytes + Lay::kKBytes;
+        const uint64_t vd = v_desc0 + st * kStageStep;
+        const uint32_t pt = tmem + pb * kTcBN;  // P of this tile, in its S buffer: hi, then lo
 #pragma unroll
         for (int kk = 0; kk < kTcBN / 16; ++kk) {
-          const uint64_t vd = umma_desc_sw128(vb + kk * (16 * 128), kTcBN * 128, 1024);
-          umma_bf16(tmem + Lay::kOCol, umma_desc_sw128(sbase + Lay::kPHi + kk * 32, 16, 1024), vd, idesc_o,
-                    i > 0 || kk > 0);
-          umma_bf16(tmem + Lay::kOCol, umma_desc_sw128(sbase + Lay::kPLo + kk * 32, 16, 1024), vd, idesc_o, true);
+          const uint64_t v_k = vd + uint64_t(kk * (16 * 128) >> 4);
+          umma_bf16_tmem_a(tmem_o, pt + 8 * kk, v_k, idesc_o, i > 0 || kk > 0);
+          umma_bf16_tmem_a(tmem_o, pt + kTcBN / 2 + 8 * kk, v_k, idesc_o, true);
         }
-        umma_commit(&o_full);
-        umma_commit(&kv_empty[st]);
+        umma_commit(&o_full[pb]);
       }
       if (!ok) atomicOr(&g_prefill_error, kErrWaitTimeout);
       // every issued MMA has finished before TMEM is released
@@ -598,7 +640,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax
+    // two threads per row: warps 2..5 take keys 0..31 of each tile and O
+    // columns [0, D/2), warps 6..9 keys 32..63 and [D/2, D); the two warps
+    // of a TMEM lane quarter swap their partial row max (and, at the end,
+    // their partial sums) through shared memory and a 64-arrival mbarrier
+    constexpr int kHalfKeys = kTcBN / 2;
+    constexpr uint32_t kHalfD = D / 2;
     const uint32_t quad = warp & 3;             // TMEM lanes 32 quad .. 32 quad + 31
+    const uint32_t half = (warp - 2) >> 2;      // 0: warps 2..5, 1: warps 6..9
     const uint32_t row = quad * 32 + lane;      // the item's row = TMEM lane
     const uint32_t lane_addr = (quad * 32u) << 16;
     const bool valid = int32_t(row) < it.rows;
@@ -606,11 +655,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int32_t t = grow / g, hh = grow % g;
     const int32_t pos = valid ? it.len - it.n + t : -1;  // -1: attends nothing
     const int32_t lo = W > 0 ? pos + 1 - W : INT32_MIN;
-    // Q row, 128-byte swizzled, zeros for rows past the item
+    // this thread's half of the Q row, 128-byte swizzled, zeros past the item
     const uint16_t* qr = valid ? p.q + uint64_t(it.qstart + t) * p.q_stride + uint64_t(it.kv_head * g + hh) * D
                                : nullptr;
 #pragma unroll
-    for (uint32_t u = 0; u < D / 8; ++u) {
+    for (uint32_t uh = 0; uh < D / 16; ++uh) {
+      const uint32_t u = half * (D / 16) + uh;
       const uint4 v = qr ? *reinterpret_cast<const uint4*>(qr + 8 * u) : make_uint4(0, 0, 0, 0);
       const uint32_t c = u >> 3, uu = u & 7;
       *reinterpret_cast<uint4*>(smem + Lay::kQ + c * (kTcBM * 128) + row * 128 + ((uu ^ (row & 7)) << 4)) = v;
@@ -621,51 +671,73 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     float m_run = -INFINITY, l_run = 0.0f;
     bool ok = true;
     for (int32_t i = 0; i < T; ++i) {
-      const uint32_t b = uint32_t(i) & 1, st = uint32_t(i) % kTcStages;
-      ok = __all_sync(0xffffffffu, mbar_wait(&s_full[b], (uint32_t(i) >> 1) & 1));
+      const uint32_t b = uint32_t(i) % Lay::kSBufs, st = uint32_t(i) % kTcStages, xb = uint32_t(i) & 1;
+      ok = __all_sync(0xffffffffu, mbar_wait(&s_full[b], uint32_t(i / 3) & 1));
       if (!ok) break;
       tc_fence_after();
-      uint32_t sv[kTcBN];
-      tmem_ld32(tmem + lane_addr + b * kTcBN, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
-      tmem_ld32(tmem + lane_addr + b * kTcBN + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+      uint32_t sv[kHalfKeys];
+#pragma unroll
+      for (int c = 0; c < kHalfKeys / 32; ++c)
+        tmem_ld32(tmem + lane_addr + b * kTcBN + half * kHalfKeys + 32 * c,
+                  *reinterpret_cast<uint32_t(*)[32]>(&sv[32 * c]));
       tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(&s_free[b]);
-      float x[kTcBN];
+      // raw scores; max and exponent work on s * score_scale (score_scale > 0)
+      float x[kHalfKeys];
 #pragma unroll
-      for (int j = 0; j < kTcBN; ++j) x[j] = __uint_as_float(sv[j]) * p.score_scale;
-      const int32_t key_base = (t_begin + i) * kTcBN;
-      if (key_base + kTcBN - 1 > pos || key_base < lo) {
+      for (int j = 0; j < kHalfKeys; ++j) x[j] = __uint_as_float(sv[j]);
+      const int32_t key_base = (t_begin + i) * kTcBN + int32_t(half) * kHalfKeys;
+      if (key_base + kHalfKeys - 1 > pos || key_base < lo) {
 #pragma unroll
-        for (int j = 0; j < kTcBN; ++j)
+        for (int j = 0; j < kHalfKeys; ++j)
           if (key_base + j > pos || key_base + j < lo) x[j] = -INFINITY;
       }
-      float mx = m_run;
+      float xm8[8];
 #pragma unroll
-      for (int j = 0; j < kTcBN; ++j) mx = fmaxf(mx, x[j]);
+      for (int q = 0; q < 8; ++q) xm8[q] = x[q];
+#pragma unroll
+      for (int j = 8; j < kHalfKeys; ++j) xm8[j & 7] = fmaxf(xm8[j & 7], x[j]);
+      float xm = fmaxf(fmaxf(fmaxf(xm8[0], xm8[1]), fmaxf(xm8[2], xm8[3])),
+                       fmaxf(fmaxf(xm8[4], xm8[5]), fmaxf(xm8[6], xm8[7])));
+      // the row's other half: partial maxima swap through a per-tile-parity
+      // slot and the quarter's mbarrier (bounded wait)
+      s_xchg[xb][half][row] = xm;
+      mbar_arrive(&xchg_bar[quad][xb]);
+      ok = __all_sync(0xffffffffu, mbar_wait(&xchg_bar[quad][xb], (uint32_t(i) >> 1) & 1));
+      if (!ok) break;
+      xm = fmaxf(xm, s_xchg[xb][half ^ 1][row]);
+      // The row's reference max moves only when the tile max exceeds it by
+      // more than kRescaleLog2 (or on its first finite score): softmax does
+      // not depend on the reference, the weights stay below 2^kRescaleLog2,
+      // and the O rescale -- which must wait for the previous PV -- is rare.
+      const float tile_max = xm * p.score_scale;
+      const float mx = (m_run == -INFINITY || tile_max > m_run + kRescaleLog2) ? fmaxf(m_run, tile_max) : m_run;
       const float mb = mx == -INFINITY ? 0.0f : mx;  // a row with nothing attended yet stays at zero
-      float sum = 0.0f;
+      float sum8[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-      for (int j = 0; j < kTcBN; ++j) {
-        x[j] = fast_exp2(x[j] - mb);
-        sum += x[j];
+      for (int j = 0; j < kHalfKeys; ++j) {
+        x[j] = fast_exp2(fmaf(x[j], p.score_scale, -mb));
+        sum8[j & 7] += x[j];
       }
-      // PV of the previous tile done: O is stable and the P buffers are free
-      if (i > 0) {
-        ok = __all_sync(0xffffffffu, mbar_wait(&o_full, uint32_t(i - 1) & 1));
+      const float sum = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
+      const float al = fast_exp2(m_run - mb);  // 1 when the max did not move, 0 before the first key
+      // both warps of a quarter see the same rows and maxima: the same choice
+      const bool rescale = i > 0 && __any_sync(0xffffffffu, mx != m_run);
+      // O changes only when every PV so far is done (tile i - 1's)
+      if (rescale) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&o_full[(i - 1) % 3], uint32_t((i - 1) / 3) & 1));
         if (!ok) break;
         tc_fence_after();
       }
-      const float al = fast_exp2(m_run - mb);  // 1 when the max did not move, 0 before the first key
-      if (i > 0 && __any_sync(0xffffffffu, mx != m_run)) {
+      if (rescale) {
 #pragma unroll
-        for (uint32_t c0 = 0; c0 < D; c0 += 32) {
+        for (uint32_t c0 = 0; c0 < kHalfD; c0 += 32) {
           uint32_t ov[32];
-          tmem_ld32(tmem + lane_addr + Lay::kOCol + c0, ov);
+          const uint32_t col = tmem + lane_addr + Lay::kOCol + half * kHalfD + c0;
+          tmem_ld32(col, ov);
           tmem_wait_ld();
 #pragma unroll
           for (int j = 0; j < 32; ++j) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * al);
-          tmem_st32(tmem + lane_addr + Lay::kOCol + c0, ov);
+          tmem_st32(col, ov);
         }
         tmem_wait_st();
       }
@@ -673,52 +745,68 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       m_run = mx;
       // the last tile's V rows at or past k_hi were not loaded, or hold
       // positions past every query: zero them for the PV product
-      if (key_base + kTcBN > k_hi) {
-        mbar_wait(&kv_full[st], (uint32_t(i) / kTcStages) & 1);  // already complete: orders after the TMA
-        const int32_t z0 = k_hi - key_base > 0 ? k_hi - key_base : 0;
+      const int32_t tile_base = (t_begin + i) * kTcBN;
+      if (tile_base + kTcBN > k_hi) {
+        // V of this tile must have landed before its tail rows are zeroed
+        ok = __all_sync(0xffffffffu, mbar_wait(&v_full[st], (uint32_t(i) / kTcStages) & 1));
+        if (!ok) break;
+        const int32_t z0 = k_hi - tile_base > 0 ? k_hi - tile_base : 0;
         uint8_t* vb = smem + Lay::kStage0 + st * Lay::kStageBytes + Lay::kKBytes;
         const uint32_t units = uint32_t(kTcBN - z0) * kChunks * 8;
-        for (uint32_t e = threadIdx.x - 64; e < units; e += 128) {
+        for (uint32_t e = threadIdx.x - 64; e < units; e += 256) {
           const uint32_t r = uint32_t(z0) + e / (kChunks * 8), rest = e % (kChunks * 8);
           *reinterpret_cast<uint4*>(vb + (rest >> 3) * (kTcBN * 128) + r * 128 + ((rest & 7) << 4)) =
               make_uint4(0, 0, 0, 0);
         }
       }
-      // P hi / lo rows, 128-byte swizzled
+      // this thread's keys of the P hi / lo rows, into the tile's S buffer in
+      // TMEM (two keys per column; both halves of the row have read their S
+      // values before either passed the max swap). hi is the weight's top 16
+      // bits and lo the top 16 bits of the (exact) remainder: both
+      // truncations, so |P - hi - lo| < 2^-15 P
 #pragma unroll
-      for (uint32_t u = 0; u < kTcBN / 8; ++u) {
-        uint32_t hi[4], lw[4];
+      for (int c = 0; c < kHalfKeys / 64; ++c) {
+        uint32_t hi[32], lw[32];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float x0 = x[8 * u + 2 * q], x1 = x[8 * u + 2 * q + 1];
-          hi[q] = f32x2_to_bf16x2(x0, x1);
-          lw[q] = f32x2_to_bf16x2(x0 - bf16_lo_to_f32(hi[q]), x1 - bf16_hi_to_f32(hi[q]));
+        for (int q = 0; q < 32; ++q) {
+          const float x0 = x[64 * c + 2 * q], x1 = x[64 * c + 2 * q + 1];
+          const uint32_t b0 = __float_as_uint(x0), b1 = __float_as_uint(x1);
+          hi[q] = __byte_perm(b0, b1, 0x7632u);
+          const float r0 = x0 - __uint_as_float(b0 & 0xffff0000u);
+          const float r1 = x1 - __uint_as_float(b1 & 0xffff0000u);
+          lw[q] = __byte_perm(__float_as_uint(r0), __float_as_uint(r1), 0x7632u);
         }
-        const uint32_t off = row * 128 + ((u ^ (row & 7)) << 4);
-        *reinterpret_cast<uint4*>(smem + Lay::kPHi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        *reinterpret_cast<uint4*>(smem + Lay::kPLo + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+        const uint32_t pt = tmem + lane_addr + b * kTcBN + half * (kHalfKeys / 2) + 32 * c;
+        tmem_st32(pt, hi);
+        tmem_st32(pt + kTcBN / 2, lw);
       }
-      fence_async_smem();
+      tmem_wait_st();
+      if (tile_base + kTcBN > k_hi) fence_async_smem();  // the zeroed V rows, for the MMA
       tc_fence_before();
-      mbar_arrive(&p_full);
+      mbar_arrive(&p_full[b]);
     }
     if (!ok && lane == 0) atomicOr(&g_prefill_error, kErrWaitTimeout);
-    // ---- O / l to the output row
-    if (ok && T > 0) {
-      ok = __all_sync(0xffffffffu, mbar_wait(&o_full, uint32_t(T - 1) & 1));
+    // ---- O / l to the output row (each thread its half of the columns)
+    s_lsum[half][row] = l_run;
+    mbar_arrive(&lsum_bar[quad]);
+    bool done = __all_sync(0xffffffffu, ok && mbar_wait(&lsum_bar[quad], 0));
+    const float l_row = l_run + s_lsum[half ^ 1][row];
+    if (done && T > 0) {
+      done = __all_sync(0xffffffffu, mbar_wait(&o_full[(T - 1) % 3], uint32_t((T - 1) / 3) & 1));
       tc_fence_after();
     }
-    const float inv = l_run > 0.0f ? 1.0f / l_run : 0.0f;
-    float* o = valid ? p.output + (uint64_t(it.qstart + t) * p.num_q_heads + uint64_t(it.kv_head * g + hh)) * D
+    const float inv = l_row > 0.0f ? 1.0f / l_row : 0.0f;
+    float* o = valid ? p.output + (uint64_t(it.qstart + t) * p.num_q_heads + uint64_t(it.kv_head * g + hh)) * D +
+                           half * kHalfD
                      : nullptr;
 #pragma unroll
-    for (uint32_t c0 = 0; c0 < D; c0 += 32) {
+    for (uint32_t c0 = 0; c0 < kHalfD; c0 += 32) {
       uint32_t ov[32];
-      if (ok && T > 0) {
-        tmem_ld32(tmem + lane_addr + Lay::kOCol + c0, ov);
+      if (done && T > 0) {
+        tmem_ld32(tmem + lane_addr + Lay::kOCol + half * kHalfD + c0, ov);
         tmem_wait_ld();
       }
-      if (o && ok) {
+      if (o && done) {
 #pragma unroll
         for (int j = 0; j < 32; j += 4) {
           const float4 w4 = T > 0 ? make_float4(__uint_as_float(ov[j]) * inv, __uint_as_float(ov[j + 1]) * inv,
@@ -749,7 +837,9 @@ int launch_prefill_tc(const PrefillArgs& a, cudaStream_t stream, PrefillParams& 
       uint64_t(a.num_kv_heads) * ((uint64_t(a.num_q_tokens) * p.group + kTcBM - 1) / kTcBM + a.num_seqs);
   if (grid == 0) return KV_OK;
   if (grid > 0x7fffffffull) return KV_ERR_UNSUPPORTED;
-  const int smem = int(1024 + TcLayout<D>::kBytes);
+  // The kernel takes all 512 TMEM columns: ask for enough shared memory that
+  // no second CTA of it is resident on an SM (it would wait in tcgen05.alloc)
+  const int smem = int(1024 + TcLayout<D>::kBytes) > 120 * 1024 ? int(1024 + TcLayout<D>::kBytes) : 120 * 1024;
   auto kern = prefill_tc_kernel<D>;
   static int set_bytes[64] = {0};
   const int dev_id = device_info().device;
