@@ -10,22 +10,13 @@
 // `paged_decode_attn_fp8`) attends for a sequence of length P + 1. GQA as in
 // the decode: query head h reads KV head h / (num_q_heads / num_kv_heads).
 //
-// GB300 design. Rows are (query token, query head of the KV head's group)
-// pairs, token-major, so one CTA's 64 rows share every K/V tile it loads.
-// A CTA owns one (sequence, KV head, block of 64 rows) item; items are laid
-// out longest key range first within a sequence, and the grid holds an upper
-// bound of the item count (CTAs past the last item exit at once).
-//   * Warp 0 produces: TMA tiled loads (cp.async.bulk.tensor.3d) of 16-slot
-//     boxes of K and V (one physical block run each, 128-byte swizzle) into
-//     a 3-stage ring of 64-key tiles guarded by full/empty mbarriers.
-//   * Warps 1..4 consume, 16 rows each, FlashAttention-2 style with
-//     mma.sync m16n8k16: S = Q K^T with Q held in registers (BF16; or f16
-//     scaled by a power of two per row against FP8 K converted exactly to
-//     f16, in the permuted k order the byte layout of ldmatrix gives), base-2
-//     online softmax per row, then O += P V with P split into BF16 hi + lo
-//     parts (two MMAs) taken straight from the S accumulators, V through
-//     transposing ldmatrix. Only tiles that cross a row's causal or window
-//     edge, or the end of the loaded keys, pay for masks.
+// GB300 design (tcgen05 / TMEM). Rows are (query token, query head of the
+// KV head's group) pairs, token-major, so one CTA's 128 rows -- the M of one
+// tcgen05.mma -- share every K/V tile it loads. A CTA owns one (sequence, KV
+// head, block of 128 rows) item; items are laid out longest key range first
+// within a sequence, and the grid holds an upper bound of the item count
+// (CTAs past the last item exit at once). The kernel's own comment gives the
+// warp roles, the TMEM map and the barriers.
 #include <math.h>
 
 #include "../../include/pagedkv.h"
@@ -37,12 +28,7 @@ __device__ uint32_t g_prefill_error;
 
 namespace {
 
-constexpr int kBM = 64;                 // rows per CTA
-constexpr int kBN = 64;                 // keys per stage
 constexpr int kSub = 16;                // keys per TMA box
-constexpr int kStages = 3;
-constexpr int kConsumers = kBM / 16;    // one warp per 16 rows
-constexpr int kThreads = 32 * (1 + kConsumers);
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct PrefillParams {
@@ -121,347 +107,48 @@ __device__ Item locate(uint32_t target, const PrefillParams& p, uint32_t lane) {
   return it;
 }
 
-template <bool kFp8, int D>
-__global__ void __launch_bounds__(kThreads)
-    prefill_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
-                   const PrefillParams p) {
-  constexpr int kKChunks = kFp8 ? D / 128 : D / 64;  // 128-byte chunks per K head row
-  constexpr int kVChunks = D / 64;
-  extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw_addr = smem_u32(smem_raw);
-  uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
-  __shared__ uint64_t full[kStages], empty[kStages];
-  __shared__ Item s_item;
-
-  const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kConsumers);
-    }
-    fence_mbar_init();
-  }
-  if (warp == 0) {
-    const Item it = locate<kBM>(blockIdx.x, p, lane);
-    if (lane == 0) s_item = it;
-  }
-  __syncthreads();
-  const Item it = s_item;
-  if (it.seq < 0) return;
-
-  // key range of the item: positions of its first and last rows' tokens
-  const int32_t g = int32_t(p.group);
-  const int32_t pos_first = it.len - it.n + it.row0 / g;
-  const int32_t pos_last = it.len - it.n + (it.row0 + it.rows - 1) / g;
-  const int32_t k_hi = pos_last + 1;  // keys [k_lo, k_hi)
-  const int32_t W = int32_t(p.sliding_window);
-  int32_t k_lo = 0;
-  if (W > 0 && pos_first + 1 - W > 0) k_lo = pos_first + 1 - W;
-  const int32_t t_begin = k_lo / kBN;
-  const int32_t t_end = k_hi > 0 ? (k_hi + kBN - 1) / kBN : t_begin;
-
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    tma_prefetch_desc(&tmap_k);
-    tma_prefetch_desc(&tmap_v);
-    const int32_t* table = p.block_tables + uint64_t(it.seq) * p.max_blocks_per_seq;
-    uint32_t stage = 0, phase = 0;
-    bool ok = true;
-    for (int32_t tile = t_begin; tile < t_end && ok; ++tile) {
-      // block ids of the tile's 16-key boxes (keys below k_hi only)
-      int32_t block_id = 0;
-      const int32_t key0 = tile * kBN + int32_t(lane) * kSub;
-      if (lane < uint32_t(kBN / kSub) && key0 < k_hi) block_id = __ldg(table + (key0 >> p.block_shift));
-      if (lane == 0) {
-        if (!mbar_wait(&empty[stage], phase ^ 1)) ok = false;
-      }
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
-      const uint32_t loaded = __popc(__ballot_sync(0xffffffffu, lane < uint32_t(kBN / kSub) && key0 < k_hi));
-      if (lane == 0) mbar_arrive_expect_tx(&full[stage], loaded * (p.k_box_bytes + p.v_box_bytes));
-      __syncwarp();
-      if (lane < loaded) {
-        uint8_t* st = smem + stage * p.stage_bytes;
-        const int32_t slot0 = (block_id << p.block_shift) + (key0 & int32_t(p.block_size - 1));
-        tma_load_3d(st + lane * p.k_box_bytes, &tmap_k, 0, slot0, it.kv_head * kKChunks, &full[stage]);
-        tma_load_3d(st + (kBN / kSub) * p.k_box_bytes + lane * p.v_box_bytes, &tmap_v, 0, slot0,
-                    it.kv_head * kVChunks, &full[stage]);
-      }
-      if (++stage == kStages) { stage = 0; phase ^= 1; }
-    }
-    if (!ok && lane == 0) atomicOr(&g_prefill_error, kErrWaitTimeout);
-    return;
-  }
-
-  // -------------------------------------------------------------- consumers
-  const uint32_t cw = warp - 1;        // rows cw*16 .. cw*16+15 of the item
-  const uint32_t g8 = lane >> 2, c4 = lane & 3;
-  // this lane's two rows (g8, g8 + 8): token position, valid key range
-  int32_t pos[2], lo[2];
-  const uint16_t* qrow[2];
-#pragma unroll
-  for (int r = 0; r < 2; ++r) {
-    const int32_t row = int32_t(cw * 16 + g8 + 8 * r);
-    const int32_t grow = it.row0 + row;
-    const bool valid = row < it.rows;
-    const int32_t t = grow / g, hh = grow % g;
-    pos[r] = valid ? it.len - it.n + t : -1;  // -1: attends nothing
-    lo[r] = (W > 0) ? pos[r] + 1 - W : INT32_MIN;
-    qrow[r] = valid ? p.q + uint64_t(it.qstart + t) * p.q_stride + uint64_t(it.kv_head * g + hh) * D : nullptr;
-  }
-
-  // Q fragments (A operand), D / 16 k-steps of 4 registers
-  uint32_t qf[D / 16][4];
-  float row_scale[2];
-  if constexpr (!kFp8) {
-#pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
-#pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        qf[kk][r] = qrow[r] ? *reinterpret_cast<const uint32_t*>(qrow[r] + kk * 16 + 2 * c4) : 0u;
-        qf[kk][2 + r] = qrow[r] ? *reinterpret_cast<const uint32_t*>(qrow[r] + kk * 16 + 8 + 2 * c4) : 0u;
-      }
-    }
-    row_scale[0] = row_scale[1] = p.score_scale;
-  } else {
-    // k order permuted to the byte layout of ldmatrix on FP8 rows: MMA k pair
-    // (2c, 2c+1) <-> dims 16kk + 4c + {0,1}, (2c+8, 2c+9) <-> 16kk + 4c + {2,3}
-    float qv[2][D / 16][4];
-    float amax[2] = {0.0f, 0.0f};
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint2 w = qrow[r] ? *reinterpret_cast<const uint2*>(qrow[r] + kk * 16 + 4 * c4) : make_uint2(0, 0);
-        qv[r][kk][0] = bf16_lo_to_f32(w.x);
-        qv[r][kk][1] = bf16_hi_to_f32(w.x);
-        qv[r][kk][2] = bf16_lo_to_f32(w.y);
-        qv[r][kk][3] = bf16_hi_to_f32(w.y);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) amax[r] = fmaxf(amax[r], fabsf(qv[r][kk][e]));
-      }
-      amax[r] = fmaxf(amax[r], __shfl_xor_sync(0xffffffffu, amax[r], 1));
-      amax[r] = fmaxf(amax[r], __shfl_xor_sync(0xffffffffu, amax[r], 2));
-      // scale the row by 2^e so that its largest magnitude lies in [2^14, 2^15)
-      int e = 0;
-      if (amax[r] > 0.0f && amax[r] < INFINITY) {
-        int ex;
-        frexpf(amax[r], &ex);
-        e = 15 - ex;
-      }
-      const float sc = ldexpf(1.0f, e);
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        qf[kk][r] = f32x2_to_f16x2(qv[r][kk][0] * sc, qv[r][kk][1] * sc);
-        qf[kk][2 + r] = f32x2_to_f16x2(qv[r][kk][2] * sc, qv[r][kk][3] * sc);
-      }
-      row_scale[r] = p.score_scale * ldexpf(1.0f, -e);
-    }
-  }
-
-  float acc[D / 8][4];
-#pragma unroll
-  for (int i = 0; i < D / 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.0f;
-  float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.0f, 0.0f};
-  // ldmatrix lane roles: K (non-transposed B: two n8 key groups x two 16-byte
-  // units) and V (transposed B: two 8-key halves x two 16-byte units)
-  const uint32_t k_row = (lane & 7) + ((lane >> 4) & 1) * 8, k_unit = (lane >> 3) & 1;
-  const uint32_t v_row = (lane & 7) + ((lane >> 3) & 1) * 8, v_unit = lane >> 4;
-  const int32_t lo_max = lo[0] > lo[1] ? lo[0] : lo[1];
-  const int32_t pos_min = pos[0] < pos[1] ? pos[0] : pos[1];
-
-  uint32_t stage = 0, phase = 0;
-  for (int32_t tile = t_begin; tile < t_end; ++tile) {
-    if (!mbar_wait(&full[stage], phase)) {
-      if (lane == 0) atomicOr(&g_prefill_error, kErrWaitTimeout);
-      return;
-    }
-    const uint32_t kbase = smem_u32(smem + stage * p.stage_bytes);
-    const uint32_t vbase = kbase + (kBN / kSub) * p.k_box_bytes;
-    const int32_t key_base = tile * kBN;
-
-    // ---- S = Q K^T: 16 rows x 64 keys (8 n8 groups)
-    float s[kBN / 8][4];
-#pragma unroll
-    for (int j = 0; j < kBN / 8; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.0f;
-#pragma unroll
-    for (int jp = 0; jp < kBN / 16; ++jp) {  // box jp = keys 16jp..16jp+15 = n8 groups 2jp, 2jp+1
-      const uint32_t box = kbase + jp * p.k_box_bytes;
-      if constexpr (!kFp8) {
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t chunk = kk >> 2, unit = ((kk & 3) << 1) + k_unit;
-          uint32_t b[4];
-          ldmatrix_x4(b, box + chunk * (kSub * 128) + k_row * 128 + ((unit ^ (k_row & 7)) << 4));
-          mma_bf16(s[2 * jp], qf[kk], b[0], b[1]);
-          mma_bf16(s[2 * jp + 1], qf[kk], b[2], b[3]);
-        }
-      } else {
-#pragma unroll
-        for (int up = 0; up < D / 32; ++up) {  // 16-byte units 2up, 2up+1 = k-steps 2up, 2up+1
-          const uint32_t chunk = up >> 2, unit = ((up & 3) << 1) + k_unit;
-          uint32_t r[4];
-          ldmatrix_x4(r, box + chunk * (kSub * 128) + k_row * 128 + ((unit ^ (k_row & 7)) << 4));
-          // r[0]: keys 16jp+0..7, unit 2up; r[1]: same keys, unit 2up+1;
-          // r[2], r[3]: keys 16jp+8..15
-          mma_f16(s[2 * jp], qf[2 * up], e4m3x2_to_f16x2(uint16_t(r[0])), e4m3x2_to_f16x2(uint16_t(r[0] >> 16)));
-          mma_f16(s[2 * jp], qf[2 * up + 1], e4m3x2_to_f16x2(uint16_t(r[1])),
-                  e4m3x2_to_f16x2(uint16_t(r[1] >> 16)));
-          mma_f16(s[2 * jp + 1], qf[2 * up], e4m3x2_to_f16x2(uint16_t(r[2])),
-                  e4m3x2_to_f16x2(uint16_t(r[2] >> 16)));
-          mma_f16(s[2 * jp + 1], qf[2 * up + 1], e4m3x2_to_f16x2(uint16_t(r[3])),
-                  e4m3x2_to_f16x2(uint16_t(r[3] >> 16)));
-        }
-      }
-    }
-#pragma unroll
-    for (int j = 0; j < kBN / 8; ++j) {
-      s[j][0] *= row_scale[0];
-      s[j][1] *= row_scale[0];
-      s[j][2] *= row_scale[1];
-      s[j][3] *= row_scale[1];
-    }
-    // ---- masks: only a tile that crosses a row's causal or window edge
-    const bool edge = key_base + kBN - 1 > pos_min || key_base < lo_max;
-    if (edge) {
-#pragma unroll
-      for (int j = 0; j < kBN / 8; ++j) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int32_t key = key_base + 8 * j + 2 * int32_t(c4) + (e & 1);
-          const int r = e >> 1;
-          if (key > pos[r] || key < lo[r]) s[j][e] = -INFINITY;
-        }
-      }
-    }
-    // ---- online softmax (base 2), rows g8 and g8 + 8
-    float mx[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-    for (int j = 0; j < kBN / 8; ++j) {
-      mx[0] = fmaxf(mx[0], fmaxf(s[j][0], s[j][1]));
-      mx[1] = fmaxf(mx[1], fmaxf(s[j][2], s[j][3]));
-    }
-    float mb[2];
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
-      mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
-      mx[r] = fmaxf(mx[r], m_run[r]);
-      mb[r] = mx[r] == -INFINITY ? 0.0f : mx[r];  // a row with nothing attended yet stays at zero
-    }
-    if (__any_sync(0xffffffffu, mx[0] != m_run[0] || mx[1] != m_run[1])) {
-      const float al0 = fast_exp2(m_run[0] - mb[0]), al1 = fast_exp2(m_run[1] - mb[1]);
-      l_run[0] *= al0;
-      l_run[1] *= al1;
-#pragma unroll
-      for (int i = 0; i < D / 8; ++i) {
-        acc[i][0] *= al0;
-        acc[i][1] *= al0;
-        acc[i][2] *= al1;
-        acc[i][3] *= al1;
-      }
-    }
-    m_run[0] = mx[0];
-    m_run[1] = mx[1];
-#pragma unroll
-    for (int j = 0; j < kBN / 8; ++j) {
-      s[j][0] = fast_exp2(s[j][0] - mb[0]);
-      s[j][1] = fast_exp2(s[j][1] - mb[0]);
-      s[j][2] = fast_exp2(s[j][2] - mb[1]);
-      s[j][3] = fast_exp2(s[j][3] - mb[1]);
-      l_run[0] += s[j][0] + s[j][1];
-      l_run[1] += s[j][2] + s[j][3];
-    }
-    // ---- O += P V, P as BF16 hi + lo A fragments straight from S
-    const bool tail = key_base + kBN > k_hi;  // keys >= k_hi: not loaded or past the end: zero their V
-#pragma unroll
-    for (int kk = 0; kk < kBN / 16; ++kk) {
-      uint32_t ph[4], pl[4];
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {  // h: n8 group 2kk + h = A columns 8h..8h+7
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          const float x0 = s[2 * kk + h][2 * r], x1 = s[2 * kk + h][2 * r + 1];
-          const uint32_t hi = f32x2_to_bf16x2(x0, x1);
-          ph[2 * h + r] = hi;
-          pl[2 * h + r] = f32x2_to_bf16x2(x0 - bf16_lo_to_f32(hi), x1 - bf16_hi_to_f32(hi));
-        }
-      }
-      uint32_t m01 = 0xffffffffu, m89 = 0xffffffffu;
-      if (tail) {
-        const int32_t k0 = key_base + 16 * kk + 2 * int32_t(c4);
-        m01 = (k0 < k_hi ? 0x0000ffffu : 0u) | (k0 + 1 < k_hi ? 0xffff0000u : 0u);
-        m89 = (k0 + 8 < k_hi ? 0x0000ffffu : 0u) | (k0 + 9 < k_hi ? 0xffff0000u : 0u);
-      }
-      const uint32_t box = vbase + kk * p.v_box_bytes;
-#pragma unroll
-      for (int dp = 0; dp < D / 16; ++dp) {  // n8 dim groups 2dp, 2dp+1
-        const uint32_t chunk = dp >> 2, unit = ((dp & 3) << 1) + v_unit;
-        uint32_t b[4];
-        ldmatrix_x4_trans(b, box + chunk * (kSub * 128) + v_row * 128 + ((unit ^ (v_row & 7)) << 4));
-        b[0] &= m01;
-        b[1] &= m89;
-        b[2] &= m01;
-        b[3] &= m89;
-        mma_bf16(acc[2 * dp], ph, b[0], b[1]);
-        mma_bf16(acc[2 * dp], pl, b[0], b[1]);
-        mma_bf16(acc[2 * dp + 1], ph, b[2], b[3]);
-        mma_bf16(acc[2 * dp + 1], pl, b[2], b[3]);
-      }
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[stage]);
-    if (++stage == kStages) { stage = 0; phase ^= 1; }
-  }
-
-  // ---- normalise and store: row r's dims 8i + 2c4, +1
-#pragma unroll
-  for (int r = 0; r < 2; ++r) {
-    float l = l_run[r];
-    l += __shfl_xor_sync(0xffffffffu, l, 1);
-    l += __shfl_xor_sync(0xffffffffu, l, 2);
-    if (!qrow[r]) continue;
-    const int32_t row = int32_t(cw * 16 + g8 + 8 * r), grow = it.row0 + row;
-    const int32_t t = grow / g, hh = grow % g;
-    const float inv = l > 0.0f ? 1.0f / l : 0.0f;
-    float* o = p.output + (uint64_t(it.qstart + t) * p.num_q_heads + uint64_t(it.kv_head * g + hh)) * D;
-#pragma unroll
-    for (int i = 0; i < D / 8; ++i)
-      *reinterpret_cast<float2*>(o + 8 * i + 2 * c4) = make_float2(acc[i][2 * r] * inv, acc[i][2 * r + 1] * inv);
-  }
-}
-
-// ---------------------------------------------------------------- tcgen05 path (BF16 cache)
-// One CTA per (sequence, KV head, block of 128 rows), 352 threads:
+// ---------------------------------------------------------------- the kernel
+// One CTA per (sequence, KV head, block of 128 rows), 352 threads (384 for
+// an FP8-K cache):
 //   warps 0, 10 TMA producers of 128-key K and V tiles, each [chunk][key][128 B]
-//               (one box per 16-slot block run and 64-element chunk), in two
-//               2-stage rings: a K stage is free once its S is done, a V stage
-//               once its PV is;
+//               (one box per 16-slot block run and 128-byte chunk), in two
+//               2-stage rings: a K stage is free once the S two tiles back is
+//               done, a V stage once that tile's PV is;
+//   warp 11     (FP8 K only) converts each E4M3 K tile, loaded into its own
+//               ring, into the f16 K tile (exact);
 //   warp 1      owns TMEM and issues every tcgen05.mma from one thread:
-//               S = Q K^T (M 128, N 128, K = head_dim) into one of two TMEM
-//               S buffers, then O += P_hi V + P_lo V (M 128, N = head_dim,
-//               K 128) into TMEM O, P from TMEM (written over its S buffer),
-//               V read as the MN-major shared-memory operand;
+//               S = Q K^T (M 128, N 128, K = head_dim; BF16, or f16 Q scaled
+//               by a power of two per row against the f16 K) into one of
+//               three TMEM S buffers, then O += P_hi V + P_lo V (M 128,
+//               N = head_dim, K 128) into TMEM O, P from TMEM (written over
+//               its S buffer), V read as the MN-major shared-memory operand;
 //   warps 2..9  softmax, two threads per row = TMEM lane (warp w owns lanes
 //               32 (w % 4) ..; warps 2..5 the first half of a tile's keys and
 //               of O's columns, warps 6..9 the second): Q rows into shared
 //               memory, then per tile S via tcgen05.ld, masks, base-2 online
 //               softmax (the pair swaps partial row maxima), O rescale in
-//               TMEM when a row max moved, P hi / lo into TMEM (the PV MMA
-//               reads its A operand from tensor memory, sparing shared memory
-//               bandwidth), and at the end O / l to the output.
+//               TMEM when a row's reference max moved, P hi / lo into TMEM
+//               (the PV MMA reads its A operand from tensor memory, sparing
+//               shared-memory bandwidth), and at the end O / l to the output.
 // S of tile i + 1 is computed while the softmax works on tile i.
-constexpr int kTcBM = 128, kTcBN = 128, kTcStages = 2, kTcWarps = 11, kTcThreads = 32 * kTcWarps;
+constexpr int kTcBM = 128, kTcBN = 128, kTcStages = 2;
+constexpr uint32_t kVWarp = 10, kConvWarp = 11;  // V producer; FP8 K converter
+template <bool kFp8>
+constexpr int tc_threads() { return 32 * (kFp8 ? 12 : 11); }
 constexpr float kRescaleLog2 = 8.0f;  // reference-max slack of the online softmax (base 2)
 
-template <int D>
+template <int D, bool kFp8>
 struct TcLayout {  // byte offsets from the 1024-aligned shared base
   static constexpr uint32_t kChunks = D / 64;
   static constexpr uint32_t kQ = 0;                           // [chunk][128 rows][128 B]
   static constexpr uint32_t kStage0 = kChunks * kTcBM * 128;
   static constexpr uint32_t kKBytes = kChunks * kTcBN * 128;  // [chunk][128 keys][128 B]
-  static constexpr uint32_t kStageBytes = 2 * kKBytes;        // K, then V
-  static constexpr uint32_t kBytes = kStage0 + kTcStages * kStageBytes;
+  static constexpr uint32_t kStageBytes = 2 * kKBytes;        // K (f16 when FP8: converted), then V
+  // FP8 K as loaded: [chunk of 128 dims][128 keys][128 B], one ring of stages
+  static constexpr uint32_t kK8Chunks = D / 128;
+  static constexpr uint32_t kK8Bytes = kFp8 ? kK8Chunks * kTcBN * 128 : 0;
+  static constexpr uint32_t kK80 = kStage0 + kTcStages * kStageBytes;
+  static constexpr uint32_t kBytes = kK80 + kTcStages * kK8Bytes;
   // TMEM columns: three S buffers [0, 128), [128, 256), [256, 384), each
   // overwritten by its tile's P once read (hi [+0, +64), lo [+64, +128): 128
   // keys, 2 per column); O [384, 384 + D)
@@ -470,17 +157,20 @@ struct TcLayout {  // byte offsets from the 1024-aligned shared base
   static constexpr uint32_t kSBufs = 3;
 };
 
-template <int D>
-__global__ void __launch_bounds__(kTcThreads, 1)
+template <int D, bool kFp8>
+__global__ void __launch_bounds__(tc_threads<kFp8>(), 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                       const PrefillParams p) {
-  using Lay = TcLayout<D>;
+  using Lay = TcLayout<D, kFp8>;
   constexpr uint32_t kChunks = Lay::kChunks;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
   const uint32_t sbase = smem_u32(smem);
   __shared__ uint64_t k_full[kTcStages], v_full[kTcStages];
+  __shared__ uint64_t k8_full[kTcStages], k8_empty[kTcStages];  // FP8 K: loaded, converted
+  __shared__ float s_qamax[2][kTcBM];                           // FP8: [half][row] partial max |q|
+  __shared__ uint64_t qamax_bar[4];
   __shared__ uint64_t s_full[3], p_full[3], o_full[3], q_full, mma_done;  // per S/P buffer
   __shared__ uint32_t tmem_base_s;
   __shared__ Item s_item;
@@ -491,8 +181,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kTcStages; ++s) {
-      mbar_init(&k_full[s], 1);
+      mbar_init(&k_full[s], kFp8 ? 32 : 1);  // FP8: the converter warp's arrivals
       mbar_init(&v_full[s], 1);
+      mbar_init(&k8_full[s], 1);
+      mbar_init(&k8_empty[s], 32);
     }
     for (int b = 0; b < 3; ++b) {
       mbar_init(&s_full[b], 1);
@@ -504,6 +196,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(&xchg_bar[qd][0], 64);
       mbar_init(&xchg_bar[qd][1], 64);
       mbar_init(&lsum_bar[qd], 64);
+      mbar_init(&qamax_bar[qd], 64);
     }
     mbar_init(&mma_done, 1);
     fence_mbar_init();
@@ -532,7 +225,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int32_t t_end = k_hi > 0 ? (k_hi + kTcBN - 1) / kTcBN : t_begin;
   const int32_t T = t_end - t_begin;
 
-  if (warp == 0 || warp == kTcWarps - 1) {
+  if (warp == 0 || warp == kVWarp) {
     // ------------------------------------------------------------ producers
     // warp 0 loads K, the last warp V, each into its own ring: a K stage is
     // free again once its S product is done, a V stage once its PV is
@@ -540,10 +233,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // a V stage once that tile's PV is done (o_full): the MMA thread commits
     // nothing extra for the producers, and loads are in order, so those
     // barriers cannot have moved on to a later tile of the same buffer yet
+    // (FP8: K lands in its own ring, free once the converters have read it)
     const bool is_k = warp == 0;
     const CUtensorMap* map = is_k ? &tmap_k : &tmap_v;
-    uint64_t* full = is_k ? k_full : v_full;
-    uint64_t* done_bar = is_k ? s_full : o_full;
+    uint64_t* full = is_k ? (kFp8 ? k8_full : k_full) : v_full;
     static_assert(kTcStages == 2, "stage reuse waits on tile i - 2");
     tma_prefetch_desc(map);
     const int32_t* table = p.block_tables + uint64_t(it.seq) * p.max_blocks_per_seq;
@@ -553,27 +246,35 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int32_t key0 = (t_begin + i) * kTcBN + int32_t(lane) * kSub;
       const bool mine = lane < uint32_t(kTcBN / kSub) && key0 < k_hi;
       const int32_t block_id = mine ? __ldg(table + (key0 >> p.block_shift)) : 0;
-      if (lane == 0 && i >= kTcStages &&
-          !mbar_wait(&done_bar[(i - kTcStages) % Lay::kSBufs], uint32_t((i - kTcStages) / Lay::kSBufs) & 1))
-        ok = false;
+      if (lane == 0 && i >= kTcStages) {
+        const int32_t j = i - kTcStages;
+        const bool freed = (is_k && kFp8) ? mbar_wait(&k8_empty[st], uint32_t(j / kTcStages) & 1)
+                                          : mbar_wait(&(is_k ? s_full : o_full)[j % Lay::kSBufs],
+                                                      uint32_t(j / Lay::kSBufs) & 1);
+        if (!freed) ok = false;
+      }
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       const uint32_t loaded = __popc(__ballot_sync(0xffffffffu, mine));
-      if (lane == 0) mbar_arrive_expect_tx(&full[st], loaded * kChunks * (kSub * 128));
+      const uint32_t chunks = (is_k && kFp8) ? Lay::kK8Chunks : kChunks;
+      if (lane == 0) mbar_arrive_expect_tx(&full[st], loaded * chunks * (kSub * 128));
       __syncwarp();
       if (mine) {
         const int32_t slot0 = (block_id << p.block_shift) + (key0 & int32_t(p.block_size - 1));
-        uint8_t* dst = smem + Lay::kStage0 + st * Lay::kStageBytes + (is_k ? 0u : Lay::kKBytes) + lane * (kSub * 128);
-#pragma unroll
-        for (uint32_t c = 0; c < kChunks; ++c)
-          tma_load_3d(dst + c * (kTcBN * 128), map, 0, slot0, it.kv_head * kChunks + c, &full[st]);
+        uint8_t* dst = smem + ((is_k && kFp8) ? Lay::kK80 + st * Lay::kK8Bytes
+                                              : Lay::kStage0 + st * Lay::kStageBytes + (is_k ? 0u : Lay::kKBytes)) +
+                       lane * (kSub * 128);
+        for (uint32_t c = 0; c < chunks; ++c)
+          tma_load_3d(dst + c * (kTcBN * 128), map, 0, slot0, it.kv_head * chunks + c, &full[st]);
       }
     }
     if (!ok && lane == 0) atomicOr(&g_prefill_error, kErrWaitTimeout);
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issue
     if (lane == 0) {
-      constexpr uint32_t idesc_s = umma_idesc_bf16(kTcBM, kTcBN, false);
+      // S: BF16 Q and K, or (FP8 cache) f16 Q scaled per row against K converted exactly to f16
+      constexpr uint32_t idesc_s =
+          kFp8 ? umma_idesc_f16(kTcBM, kTcBN, false) : umma_idesc_bf16(kTcBM, kTcBN, false);
       constexpr uint32_t idesc_o = umma_idesc_bf16(kTcBM, D, true);
       // Descriptors are built once: a k-step or a stage moves only the start
       // address field (bits 0-13, in 16-byte units), so each MMA adds a small
@@ -638,6 +339,49 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_wait(&mma_done, 0);
     }
     __syncwarp();
+  } else if (kFp8 && warp == kConvWarp) {
+    // ------------------------------------------------------------ FP8 K -> f16
+    // One warp turns each loaded E4M3 K tile into the f16 [chunk][key][128 B]
+    // tile the S product reads (exact: every E4M3 value is an f16 value),
+    // each lane four key rows. The f16 stage is free once the S product two
+    // tiles back is done; the E4M3 stage once the rows are read.
+    const uint32_t ct = lane;
+    bool ok = true;
+    for (int32_t i = 0; i < T && ok; ++i) {
+      const uint32_t st = uint32_t(i) % kTcStages;
+      ok = __all_sync(0xffffffffu, mbar_wait(&k8_full[st], uint32_t(i / kTcStages) & 1));
+      if (ok && i >= kTcStages)
+        ok = __all_sync(0xffffffffu, mbar_wait(&s_full[(i - kTcStages) % Lay::kSBufs],
+                                               uint32_t((i - kTcStages) / Lay::kSBufs) & 1));
+      if (!ok) break;
+      const uint8_t* src = smem + Lay::kK80 + st * Lay::kK8Bytes;
+      uint8_t* dst = smem + Lay::kStage0 + st * Lay::kStageBytes;
+      for (uint32_t r = ct; r < uint32_t(kTcBN); r += 32) {
+#pragma unroll
+        for (uint32_t c8 = 0; c8 < (kFp8 ? Lay::kK8Chunks : 1u); ++c8) {
+#pragma unroll
+          for (uint32_t u = 0; u < 8; ++u) {  // 16 dims per 16-byte unit
+            const uint4 w = *reinterpret_cast<const uint4*>(src + c8 * (kTcBN * 128) + r * 128 + ((u ^ (r & 7)) << 4));
+            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+            uint32_t h[8];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              h[2 * j] = e4m3x2_to_f16x2(uint16_t(ws[j]));
+              h[2 * j + 1] = e4m3x2_to_f16x2(uint16_t(ws[j] >> 16));
+            }
+            // dims 128 c8 + 16 u .. + 15: f16 chunk 2 c8 + u / 4, units 2 (u % 4) and + 1
+            const uint32_t c = 2 * c8 + (u >> 2), u0 = 2 * (u & 3);
+            uint8_t* drow = dst + c * (kTcBN * 128) + r * 128;
+            *reinterpret_cast<uint4*>(drow + ((u0 ^ (r & 7)) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
+            *reinterpret_cast<uint4*>(drow + (((u0 + 1) ^ (r & 7)) << 4)) = make_uint4(h[4], h[5], h[6], h[7]);
+          }
+        }
+      }
+      fence_async_smem();
+      mbar_arrive(&k8_empty[st]);
+      mbar_arrive(&k_full[st]);
+    }
+    if (!ok && lane == 0) atomicOr(&g_prefill_error, kErrWaitTimeout);
   } else {
     // ------------------------------------------------------------ softmax
     // two threads per row: warps 2..5 take keys 0..31 of each tile and O
@@ -658,19 +402,60 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // this thread's half of the Q row, 128-byte swizzled, zeros past the item
     const uint16_t* qr = valid ? p.q + uint64_t(it.qstart + t) * p.q_stride + uint64_t(it.kv_head * g + hh) * D
                                : nullptr;
+    float rs = p.score_scale;  // the row's score scale (FP8: the row's power-of-two Q scale undone)
+    bool ok = true;
+    if constexpr (!kFp8) {
 #pragma unroll
-    for (uint32_t uh = 0; uh < D / 16; ++uh) {
-      const uint32_t u = half * (D / 16) + uh;
-      const uint4 v = qr ? *reinterpret_cast<const uint4*>(qr + 8 * u) : make_uint4(0, 0, 0, 0);
-      const uint32_t c = u >> 3, uu = u & 7;
-      *reinterpret_cast<uint4*>(smem + Lay::kQ + c * (kTcBM * 128) + row * 128 + ((uu ^ (row & 7)) << 4)) = v;
+      for (uint32_t uh = 0; uh < D / 16; ++uh) {
+        const uint32_t u = half * (D / 16) + uh;
+        const uint4 v = qr ? *reinterpret_cast<const uint4*>(qr + 8 * u) : make_uint4(0, 0, 0, 0);
+        const uint32_t c = u >> 3, uu = u & 7;
+        *reinterpret_cast<uint4*>(smem + Lay::kQ + c * (kTcBM * 128) + row * 128 + ((uu ^ (row & 7)) << 4)) = v;
+      }
+    } else {
+      // f16 Q for the f16 S product: the row times 2^e, e chosen so that its
+      // largest magnitude lies in [2^14, 2^15) (the two halves swap maxima)
+      float qv[D / 2];
+      float amax = 0.0f;
+#pragma unroll
+      for (uint32_t uh = 0; uh < D / 16; ++uh) {
+        const uint4 v = qr ? *reinterpret_cast<const uint4*>(qr + 8 * (half * (D / 16) + uh)) : make_uint4(0, 0, 0, 0);
+        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          qv[8 * uh + 2 * j] = bf16_lo_to_f32(w4[j]);
+          qv[8 * uh + 2 * j + 1] = bf16_hi_to_f32(w4[j]);
+          amax = fmaxf(amax, fmaxf(fabsf(qv[8 * uh + 2 * j]), fabsf(qv[8 * uh + 2 * j + 1])));
+        }
+      }
+      s_qamax[half][row] = amax;
+      mbar_arrive(&qamax_bar[quad]);
+      ok = __all_sync(0xffffffffu, mbar_wait(&qamax_bar[quad], 0));
+      amax = fmaxf(amax, s_qamax[half ^ 1][row]);
+      int e = 0;
+      if (amax > 0.0f && amax < INFINITY) {
+        int ex;
+        frexpf(amax, &ex);
+        e = 15 - ex;
+      }
+      const float sc = ldexpf(1.0f, e);
+      rs = p.score_scale * ldexpf(1.0f, -e);
+#pragma unroll
+      for (uint32_t uh = 0; uh < D / 16; ++uh) {
+        const uint32_t u = half * (D / 16) + uh;
+        uint32_t f[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) f[j] = f32x2_to_f16x2(qv[8 * uh + 2 * j] * sc, qv[8 * uh + 2 * j + 1] * sc);
+        const uint32_t c = u >> 3, uu = u & 7;
+        *reinterpret_cast<uint4*>(smem + Lay::kQ + c * (kTcBM * 128) + row * 128 + ((uu ^ (row & 7)) << 4)) =
+            make_uint4(f[0], f[1], f[2], f[3]);
+      }
     }
     fence_async_smem();
     mbar_arrive(&q_full);
 
     float m_run = -INFINITY, l_run = 0.0f;
-    bool ok = true;
-    for (int32_t i = 0; i < T; ++i) {
+    for (int32_t i = 0; i < T && ok; ++i) {
       const uint32_t b = uint32_t(i) % Lay::kSBufs, st = uint32_t(i) % kTcStages, xb = uint32_t(i) & 1;
       ok = __all_sync(0xffffffffu, mbar_wait(&s_full[b], uint32_t(i / 3) & 1));
       if (!ok) break;
@@ -709,13 +494,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // more than kRescaleLog2 (or on its first finite score): softmax does
       // not depend on the reference, the weights stay below 2^kRescaleLog2,
       // and the O rescale -- which must wait for the previous PV -- is rare.
-      const float tile_max = xm * p.score_scale;
+      const float tile_max = xm * rs;
       const float mx = (m_run == -INFINITY || tile_max > m_run + kRescaleLog2) ? fmaxf(m_run, tile_max) : m_run;
       const float mb = mx == -INFINITY ? 0.0f : mx;  // a row with nothing attended yet stays at zero
       float sum8[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
       for (int j = 0; j < kHalfKeys; ++j) {
-        x[j] = fast_exp2(fmaf(x[j], p.score_scale, -mb));
+        x[j] = fast_exp2(fmaf(x[j], rs, -mb));
         sum8[j & 7] += x[j];
       }
       const float sum = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
@@ -825,22 +610,24 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
 }
 
-template <int D>
+template <int D, bool kFp8>
 int launch_prefill_tc(const PrefillArgs& a, cudaStream_t stream, PrefillParams& p) {
   CUtensorMap mk, mv;
-  // one 64-element chunk per box: each box lands in its chunk's [64 keys] tile
-  if (!encode_pool_map(&mk, a.k_cache, false, a.num_kv_heads, D, 1, 1) ||
+  // one 128-byte chunk per box: each box lands in its chunk's [128 keys] tile
+  if (!encode_pool_map(&mk, a.k_cache, kFp8, a.num_kv_heads, D, 1, 1) ||
       !encode_pool_map(&mv, a.v_cache, false, a.num_kv_heads, D, 1, 1))
     return KV_ERR_CUDA;
-  // grid: an upper bound of the item count, as for the mma.sync path
+  // grid: an upper bound of the item count, sum over sequences of
+  // ceil(n_s * group / 128) <= num_q_tokens * group / 128 + num_seqs
   const uint64_t grid =
       uint64_t(a.num_kv_heads) * ((uint64_t(a.num_q_tokens) * p.group + kTcBM - 1) / kTcBM + a.num_seqs);
   if (grid == 0) return KV_OK;
   if (grid > 0x7fffffffull) return KV_ERR_UNSUPPORTED;
   // The kernel takes all 512 TMEM columns: ask for enough shared memory that
   // no second CTA of it is resident on an SM (it would wait in tcgen05.alloc)
-  const int smem = int(1024 + TcLayout<D>::kBytes) > 120 * 1024 ? int(1024 + TcLayout<D>::kBytes) : 120 * 1024;
-  auto kern = prefill_tc_kernel<D>;
+  constexpr int kNeed = int(1024 + TcLayout<D, kFp8>::kBytes);
+  const int smem = kNeed > 120 * 1024 ? kNeed : 120 * 1024;
+  auto kern = prefill_tc_kernel<D, kFp8>;
   static int set_bytes[64] = {0};
   const int dev_id = device_info().device;
   if (dev_id < 0 || dev_id >= 64) return KV_ERR_CUDA;
@@ -849,32 +636,7 @@ int launch_prefill_tc(const PrefillArgs& a, cudaStream_t stream, PrefillParams& 
       return KV_ERR_CUDA;
     set_bytes[dev_id] = smem;
   }
-  kern<<<unsigned(grid), kTcThreads, smem, stream>>>(mk, mv, p);
-  return cudaGetLastError() == cudaSuccess ? KV_OK : KV_ERR_CUDA;
-}
-
-template <bool kFp8, int D>
-int launch_prefill_t(const PrefillArgs& a, cudaStream_t stream, PrefillParams& p, uint64_t grid) {
-  CUtensorMap mk, mv;
-  if (!encode_pool_map(&mk, a.k_cache, kFp8, a.num_kv_heads, D, 1) ||
-      !encode_pool_map(&mv, a.v_cache, false, a.num_kv_heads, D, 1))
-    return KV_ERR_CUDA;
-  constexpr uint32_t kKChunks = kFp8 ? D / 128 : D / 64, kVChunks = D / 64;
-  p.k_box_bytes = kKChunks * kSub * 128;
-  p.v_box_bytes = kVChunks * kSub * 128;
-  p.stage_bytes = (kBN / kSub) * (p.k_box_bytes + p.v_box_bytes);
-  const int smem = int(1024 + kStages * p.stage_bytes);
-  auto kern = prefill_kernel<kFp8, D>;
-  // the dynamic shared-memory opt-in is set once per device and size
-  static int set_bytes[64] = {0};
-  const int dev_id = device_info().device;
-  if (dev_id < 0 || dev_id >= 64) return KV_ERR_CUDA;
-  if (set_bytes[dev_id] < smem) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-      return KV_ERR_CUDA;
-    set_bytes[dev_id] = smem;
-  }
-  kern<<<unsigned(grid), kThreads, smem, stream>>>(mk, mv, p);
+  kern<<<unsigned(grid), tc_threads<kFp8>(), smem, stream>>>(mk, mv, p);
   return cudaGetLastError() == cudaSuccess ? KV_OK : KV_ERR_CUDA;
 }
 
@@ -898,17 +660,11 @@ int launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   p.q_stride = a.q_stride;
   p.sliding_window = a.sliding_window;
   p.score_scale = a.inv_sqrt_d * kLog2e * (a.fp8 ? a.k_scale : 1.0f);
-  // an upper bound of the item count: sum over sequences of
-  // ceil(n_s * group / 64) <= num_q_tokens * group / 64 + num_seqs
-  const uint64_t grid =
-      uint64_t(a.num_kv_heads) * ((uint64_t(a.num_q_tokens) * p.group + kBM - 1) / kBM + a.num_seqs);
-  if (grid == 0) return KV_OK;
-  if (grid > 0x7fffffffull) return KV_ERR_UNSUPPORTED;
   const int key = (a.fp8 ? 100 : 0) + int(a.head_dim);
   switch (key) {
-    case 64: return launch_prefill_tc<64>(a, stream, p);     // BF16: tcgen05 / TMEM
-    case 128: return launch_prefill_tc<128>(a, stream, p);
-    case 228: return launch_prefill_t<true, 128>(a, stream, p, grid);  // FP8 K: mma.sync
+    case 64: return launch_prefill_tc<64, false>(a, stream, p);  // tcgen05 / TMEM
+    case 128: return launch_prefill_tc<128, false>(a, stream, p);
+    case 228: return launch_prefill_tc<128, true>(a, stream, p);
     default: return KV_ERR_UNSUPPORTED;
   }
 }
