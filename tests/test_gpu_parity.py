@@ -705,3 +705,72 @@ def test_full_fp8_kv_mixed_sampled():
     lens = w.seq_lens.cpu().numpy()
     seqs = sorted({int(lens.argmax()), int(lens.argmin()), 100, 200})
     _full_size(w, "kv", (0,), seqs, (0, 7, 8, 63))
+
+
+def _full_prefill_sampled(w, fp8, chunk, seqs, rows_per_seq=3):
+    """The benchmark's chunked prefill (the last min(chunk, L) positions of
+    every sequence as causal queries) over the full-size cache, on the GPU;
+    for each sampled sequence, its first, middle and last query rows from the
+    oracle, which runs just those queries over the same sequence (cache rows
+    written by the oracle's own write into a compact host pool)."""
+    H, D, bs, Hq, nb, n = w.num_kv_heads, w.head_dim, w.block_size, w.num_q_heads, w.num_blocks, w.num_tokens
+    slots = gpu_slots(w)
+    vc = kvgen.poisoned_pool(nb, bs, H, D, "bf16", DEV)
+    kc = kvgen.poisoned_pool(nb, bs, H, D, "fp8" if fp8 else "bf16", DEV)
+    for t0 in range(0, n, 262144):
+        t1 = min(n, t0 + 262144)
+        if fp8:
+            pk.kv_write_fp8k(w.key[t0:t1], w.value[t0:t1], kc, vc, slots[t0:t1], t1 - t0, H, D, bs, H * D, H * D,
+                             w.k_scale)
+        else:
+            pk.kv_write_bf16(w.key[t0:t1], w.value[t0:t1], kc, vc, slots[t0:t1], t1 - t0, H, D, bs, H * D, H * D)
+    lens = w.seq_lens.cpu().numpy()
+    q_lens = [min(chunk, int(L)) for L in lens]
+    qsl = np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32)
+    n_q = int(qsl[-1])
+    q = torch.randn((n_q, Hq * D), generator=torch.Generator().manual_seed(77)).to(torch.bfloat16)
+    out = torch.full((n_q, Hq, D), float("nan"), device=DEV)
+    args = (w.block_tables.to(DEV), w.seq_lens.to(DEV), torch.from_numpy(qsl).to(DEV), w.max_blocks_per_seq,
+            w.num_seqs, n_q, Hq, H, D, bs, w.inv_sqrt_d)
+    if fp8:
+        pk.paged_prefill_attn_fp8k(q.to(DEV), kc, vc, out, *args, w.k_scale, Hq * D, 0)
+    else:
+        pk.paged_prefill_attn_bf16(q.to(DEV), kc, vc, out, *args, Hq * D, 0)
+    got = out.cpu().numpy()
+    assert np.isfinite(got).all()
+    starts = np.concatenate([[0], np.cumsum(lens.astype(np.int64))])
+    for s in seqs:
+        L = int(lens[s])
+        nq = q_lens[s]
+        js = sorted({0, nq // 2, nq - 1})[:rows_per_seq]
+        # compact host cache of sequence s
+        nblk = -(-L // bs)
+        table = np.arange(nblk, dtype=np.int32)[None]
+        kr = np.full((nblk, bs, H, D), kvgen.E4M3_NAN if fp8 else kvgen.BF16_NAN, np.uint8 if fp8 else np.uint16)
+        vr = np.full((nblk, bs, H, D), kvgen.BF16_NAN, np.uint16)
+        sl = oracle.fill_slots(table[0], 0, L, bs)
+        kk, vv = u16(w.key[starts[s]:starts[s + 1]].cpu()), u16(w.value[starts[s]:starts[s + 1]].cpu())
+        if fp8:
+            oracle.write_fp8k(kk, vv, kr, vr, sl, L, H, D, bs, H * D, H * D, w.k_scale)
+        else:
+            oracle.write_bf16(kk, vv, kr, vr, sl, L, H, D, bs, H * D, H * D)
+        for j in js:
+            # one query at position L - nq + j: a sequence cut to that length + 1
+            qrow = np.ascontiguousarray(u16(q[qsl[s] + j][None]))
+            ref = oracle.paged_prefill_attn(qrow, None if fp8 else kr, kr if fp8 else None, vr, table,
+                                            np.array([L - nq + j + 1], np.int32), np.array([0, 1], np.int32), nblk,
+                                            1, Hq, H, D, bs, w.inv_sqrt_d, w.k_scale, Hq * D, 0)
+            assert_decode_close(got[qsl[s] + j][None], ref, f"{w.name} seq {s} query {j}")
+    assert pk.kv_get_device_error() == 0
+
+
+def test_full_bf16_chunked_prefill_sampled():
+    w = kvgen.bf16_gqa4(device=DEV)
+    lens = w.seq_lens.cpu().numpy()
+    _full_prefill_sampled(w, False, 256, sorted({int(lens.argmax()), int(lens.argmin()), 0, 63}))
+
+
+def test_full_fp8k_chunked_prefill_sampled():
+    w = kvgen.fp8k_mixed(device=DEV)
+    lens = w.seq_lens.cpu().numpy()[:32]
+    _full_prefill_sampled(w, True, 256, sorted({int(lens.argmax()), int(lens.argmin()), 5}))
