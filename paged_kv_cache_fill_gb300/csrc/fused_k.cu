@@ -22,8 +22,9 @@
 // The error-free transforms use __fmul_rn / __fadd_rn so that the compiler
 // cannot fuse them into FMAs.
 //
-// Work split: one 512-thread CTA per SM takes passes of up to
-// tokens_per_pass() tokens (all their heads); head_dim / 8 lanes per row and
+// Work split: two 256-thread CTAs per SM (their phases interleave) take
+// passes of up to tokens_per_pass() tokens (all their heads); the frequency
+// ladder comes from the host with the launch. head_dim / 8 lanes per row and
 // 8 elements per lane: lane l < R/8 holds the rotation pairs (4l..4l+3,
 // R/2+4l..R/2+4l+3), the other lanes 8 pass-through elements; a thread keeps
 // up to 4 rows. Each pass
@@ -65,6 +66,12 @@ struct Freq {
   float h, m, l;  // h + m + l = the binary64 frequency
   float pad;
   double d;
+};
+
+// theta^(-2i/R) for every rotation pair i < R/2 (R <= 256), computed on the
+// host per call (binary64 exp2/log2 are slow on this GPU) and passed by value.
+struct FreqTable {
+  Freq f[128];
 };
 
 // sin and cos of the remainder r = rh + rl (|r| <= ~pi/64), combined with
@@ -155,7 +162,8 @@ __device__ __forceinline__ void unpack8(const uint32_t (&w)[4], float (&x)[8]) {
   }
 }
 
-constexpr int kThreads = 512;
+constexpr int kThreads = 256;
+constexpr int kCtasPerSm = 2;  // two CTAs per SM interleave their load / table / row phases
 constexpr int kMaxRowsPerThread = 4;
 constexpr int kTableEntries = 2048;  // sin/cos entries per pass: tokens x rotary_dim/2
 
@@ -172,12 +180,12 @@ __host__ __device__ inline uint32_t tokens_per_pass(uint32_t head_dim, uint32_t 
 // kFp8Out: store E4M3(o * inv_scale) (saturating, RNE) instead of BF16(o).
 // kMrope: pair i takes its position from positions / pos_h / pos_w by i % 3.
 template <int D, bool kFp8Out, bool kMrope>
-__global__ void __launch_bounds__(kThreads, 1) fused_k_norm_rope_kernel(
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) fused_k_norm_rope_kernel(
     const uint16_t* __restrict__ k_in, const uint16_t* __restrict__ k_norm_weight,
     const int32_t* __restrict__ positions, const int32_t* __restrict__ pos_h,
     const int32_t* __restrict__ pos_w, void* __restrict__ k_cache,
     const int64_t* __restrict__ slot_mapping, uint32_t num_tokens, uint32_t num_kv_heads,
-    uint32_t rotary_dim, float rms_eps, float theta, float inv_scale, uint32_t tok_pass) {
+    uint32_t rotary_dim, float rms_eps, const __grid_constant__ FreqTable ft, float inv_scale, uint32_t tok_pass) {
   constexpr int kLanes = D / 8;              // lanes per row
   constexpr int kRows = kThreads / kLanes;   // rows per sweep of the CTA
   __shared__ Freq freq[128];
@@ -186,6 +194,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_k_norm_rope_kernel(
   if (threadIdx.x < 64) sincos_pio32[threadIdx.x] = kSinCosPio32[threadIdx.x];
 
   const uint32_t half = rotary_dim / 2;
+  if (threadIdx.x < half) freq[threadIdx.x] = ft.f[threadIdx.x];  // visible after the pass's first barrier
 
   const uint32_t lane = threadIdx.x % kLanes;
   const uint32_t row_in_sweep = threadIdx.x / kLanes;
@@ -229,22 +238,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_k_norm_rope_kernel(
         slot[k] = __ldg(slot_mapping + t);
       }
     }
-    if (pass == blockIdx.x) {
-      // Frequencies theta^(-2i/R) in binary64, split into three binary32
-      // parts; once per CTA, while the first pass's loads are in flight.
-      if (threadIdx.x < half) {
-        const double c = -2.0 * log2(double(theta)) / double(rotary_dim);
-        const double f = exp2(c * double(threadIdx.x));
-        Freq e;
-        e.h = float(f);
-        e.m = float(f - double(e.h));
-        e.l = float(f - double(e.h) - double(e.m));
-        e.pad = 0.0f;
-        e.d = f;
-        freq[threadIdx.x] = e;
-      }
-      __syncthreads();
-    }
+    if (pass == blockIdx.x) __syncthreads();  // freq and sincos_pio32 written
     // 2. sin/cos of every (token of the pass, frequency), by all threads
     for (uint32_t e = threadIdx.x; e < ntok * half; e += kThreads) {
       const uint32_t j = e / half, i = e % half;
@@ -322,17 +316,17 @@ __global__ void __launch_bounds__(kThreads, 1) fused_k_norm_rope_kernel(
 template <int D>
 static void launch_d(bool fp8_out, bool mrope, unsigned blocks, cudaStream_t stream, const uint16_t* k_in,
                      const uint16_t* w, const int32_t* pos, const int32_t* pos_h, const int32_t* pos_w, void* cache,
-                     const int64_t* slots, uint32_t n, uint32_t H, uint32_t R, float eps, float theta, float inv_scale,
-                     uint32_t tok_pass) {
+                     const int64_t* slots, uint32_t n, uint32_t H, uint32_t R, float eps, const FreqTable& ft,
+                     float inv_scale, uint32_t tok_pass) {
   if (fp8_out)
     fused_k_norm_rope_kernel<D, true, false><<<blocks, kThreads, 0, stream>>>(
-        k_in, w, pos, pos_h, pos_w, cache, slots, n, H, R, eps, theta, inv_scale, tok_pass);
+        k_in, w, pos, pos_h, pos_w, cache, slots, n, H, R, eps, ft, inv_scale, tok_pass);
   else if (mrope)
     fused_k_norm_rope_kernel<D, false, true><<<blocks, kThreads, 0, stream>>>(
-        k_in, w, pos, pos_h, pos_w, cache, slots, n, H, R, eps, theta, inv_scale, tok_pass);
+        k_in, w, pos, pos_h, pos_w, cache, slots, n, H, R, eps, ft, inv_scale, tok_pass);
   else
     fused_k_norm_rope_kernel<D, false, false><<<blocks, kThreads, 0, stream>>>(
-        k_in, w, pos, pos_h, pos_w, cache, slots, n, H, R, eps, theta, inv_scale, tok_pass);
+        k_in, w, pos, pos_h, pos_w, cache, slots, n, H, R, eps, ft, inv_scale, tok_pass);
 }
 
 cudaError_t launch_fused_k_norm_rope(const uint16_t* k_in, const uint16_t* k_norm_weight,
@@ -344,21 +338,33 @@ cudaError_t launch_fused_k_norm_rope(const uint16_t* k_in, const uint16_t* k_nor
   const DeviceInfo& dev = device_info();
   const uint32_t tok_pass = tokens_per_pass(head_dim, rotary_dim, num_kv_heads);
   const uint64_t passes = (uint64_t(num_tokens) + tok_pass - 1) / tok_pass;
-  uint64_t blocks = uint64_t(dev.num_sms);  // persistent: the frequency set-up runs once per SM
+  uint64_t blocks = uint64_t(dev.num_sms) * kCtasPerSm;  // persistent
   if (passes < blocks) blocks = passes;
   const bool mrope = pos_h != nullptr;
+  // theta^(-2i/R) in binary64, split into three binary32 parts
+  FreqTable ft{};
+  const double c = -2.0 * log2(double(theta)) / double(rotary_dim);
+  for (uint32_t i = 0; i < rotary_dim / 2 && i < 128; ++i) {
+    const double f = exp2(c * double(i));
+    Freq& e = ft.f[i];
+    e.h = float(f);
+    e.m = float(f - double(e.h));
+    e.l = float(f - double(e.h) - double(e.m));
+    e.pad = 0.0f;
+    e.d = f;
+  }
   switch (head_dim) {
     case 64:
       launch_d<64>(fp8_out, mrope, unsigned(blocks), stream, k_in, k_norm_weight, positions, pos_h, pos_w, k_cache,
-                   slot_mapping, num_tokens, num_kv_heads, rotary_dim, rms_eps, theta, inv_scale, tok_pass);
+                   slot_mapping, num_tokens, num_kv_heads, rotary_dim, rms_eps, ft, inv_scale, tok_pass);
       break;
     case 128:
       launch_d<128>(fp8_out, mrope, unsigned(blocks), stream, k_in, k_norm_weight, positions, pos_h, pos_w, k_cache,
-                    slot_mapping, num_tokens, num_kv_heads, rotary_dim, rms_eps, theta, inv_scale, tok_pass);
+                    slot_mapping, num_tokens, num_kv_heads, rotary_dim, rms_eps, ft, inv_scale, tok_pass);
       break;
     case 256:
       launch_d<256>(fp8_out, mrope, unsigned(blocks), stream, k_in, k_norm_weight, positions, pos_h, pos_w, k_cache,
-                    slot_mapping, num_tokens, num_kv_heads, rotary_dim, rms_eps, theta, inv_scale, tok_pass);
+                    slot_mapping, num_tokens, num_kv_heads, rotary_dim, rms_eps, ft, inv_scale, tok_pass);
       break;
     default:
       return cudaErrorInvalidValue;
