@@ -633,12 +633,21 @@ def run_gpu(args):
         if step.extras:
             step.run_step()
             runs = [x["fn"] for x in step.extras]
-        for _ in range(args.warmup + args.steps):
+        times = []
+        for it in range(args.warmup + args.steps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
             for f in runs:
                 f()
+            b.record(stream)
+            if it >= args.warmup:
+                times.append((a, b))
         torch.cuda.synchronize()
         assert pk.kv_get_device_error() == 0
-        print(json.dumps({"part": args.part, "runs": args.warmup + args.steps, "ok": True}))
+        ms = sorted(a.elapsed_time(b) for a, b in times)
+        # back-to-back runs, L2 not flushed: a quick look, not a bench figure
+        print(json.dumps({"part": args.part, "runs": args.warmup + args.steps, "ok": True,
+                          "ms_median_unflushed": round(ms[len(ms) // 2], 4) if ms else None}))
         return
 
     barrier = ranks.barrier
@@ -814,9 +823,37 @@ def run_e2e(step, args, dev, world):
     b.record(stream)
     torch.cuda.synchronize()
     ms = a.elapsed_time(b) / steps
-    return {"value": round(step.total_bytes * world / (ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+    link = host_link_gbs(stream)
+    # the step cannot end before its inputs have crossed the host link and
+    # its outputs have come back: that time bounds the end-to-end rate
+    link_ms = 1e3 * (h2d / (link["h2d_gbs"] * 1e9) + d2h / (link["d2h_gbs"] * 1e9))
+    bound = step.total_bytes * world / (link_ms * 1e-3) / 1e9
+    value = step.total_bytes * world / (ms * 1e-3) / 1e9
+    return {"value": round(value, 1), "unit": "GB/s",
             "ms_per_step": round(ms, 3), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-            "steps": steps}
+            "steps": steps,
+            "host_link": dict(link, bound_value=round(bound, 1), frac_of_bound=round(value / bound, 4))}
+
+
+def host_link_gbs(stream, nbytes=1 << 30, reps=3):
+    """Pinned host <-> device copy rate of this machine, one 1 GiB copy each way
+    (best of `reps`): the link every end-to-end step's inputs cross."""
+    import torch
+    h = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    d = torch.empty(nbytes, dtype=torch.uint8, device=torch.cuda.current_device())
+    out = {}
+    for name, dst, src in (("h2d_gbs", d, h), ("d2h_gbs", h, d)):
+        best = float("inf")
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            dst.copy_(src, non_blocking=True)
+            b.record(stream)
+            b.synchronize()
+            best = min(best, a.elapsed_time(b))
+        out[name] = round(nbytes / (best * 1e-3) / 1e9, 1)
+    del h, d
+    return out
 
 
 # ---------------------------------------------------------------------------

@@ -119,12 +119,15 @@ __device__ Item locate(uint32_t target, const PrefillParams& p, uint32_t lane) {
 //   warp 1      owns TMEM and issues every tcgen05.mma from one thread:
 //               S = Q K^T (M 128, N 128, K = head_dim; BF16, or f16 Q scaled
 //               by a power of two per row against the f16 K) into one of
-//               three TMEM S buffers, then O += P_hi V + P_lo V (M 128,
-//               N = head_dim, K 128) into TMEM O, P from TMEM (written over
-//               its S buffer), V read as the MN-major shared-memory operand;
+//               two TMEM S buffers, Q read from tensor memory, then
+//               O += P_hi V + P_lo V (M 128, N = head_dim, K 128) into TMEM
+//               O, P from TMEM (written over its S buffer), V read as the
+//               MN-major shared-memory operand. Only K and V tiles are read
+//               from shared memory: the kernel's time follows its
+//               shared-memory traffic per tile;
 //   warps 2..9  softmax, two threads per row = TMEM lane (warp w owns lanes
 //               32 (w % 4) ..; warps 2..5 the first half of a tile's keys and
-//               of O's columns, warps 6..9 the second): Q rows into shared
+//               of O's columns, warps 6..9 the second): Q rows into tensor
 //               memory, then per tile S via tcgen05.ld, masks, base-2 online
 //               softmax (the pair swaps partial row maxima), O rescale in
 //               TMEM when a row's reference max moved, P hi / lo into TMEM
@@ -140,8 +143,7 @@ constexpr float kRescaleLog2 = 8.0f;  // reference-max slack of the online softm
 template <int D, bool kFp8>
 struct TcLayout {  // byte offsets from the 1024-aligned shared base
   static constexpr uint32_t kChunks = D / 64;
-  static constexpr uint32_t kQ = 0;                           // [chunk][128 rows][128 B]
-  static constexpr uint32_t kStage0 = kChunks * kTcBM * 128;
+  static constexpr uint32_t kStage0 = 0;
   static constexpr uint32_t kKBytes = kChunks * kTcBN * 128;  // [chunk][128 keys][128 B]
   static constexpr uint32_t kStageBytes = 2 * kKBytes;        // K (f16 when FP8: converted), then V
   // FP8 K as loaded: [chunk of 128 dims][128 keys][128 B], one ring of stages
@@ -149,12 +151,14 @@ struct TcLayout {  // byte offsets from the 1024-aligned shared base
   static constexpr uint32_t kK8Bytes = kFp8 ? kK8Chunks * kTcBN * 128 : 0;
   static constexpr uint32_t kK80 = kStage0 + kTcStages * kStageBytes;
   static constexpr uint32_t kBytes = kK80 + kTcStages * kK8Bytes;
-  // TMEM columns: three S buffers [0, 128), [128, 256), [256, 384), each
-  // overwritten by its tile's P once read (hi [+0, +64), lo [+64, +128): 128
-  // keys, 2 per column); O [384, 384 + D)
+  // TMEM columns: two S buffers [0, 128), [128, 256), each overwritten by
+  // its tile's P once read (hi [+0, +64), lo [+64, +128): 128 keys, 2 per
+  // column); Q [256, 256 + D / 2) (the S product's A operand, 2 dims per
+  // column); O [384, 384 + D)
   static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kQCol = 256;
   static constexpr uint32_t kOCol = 384;
-  static constexpr uint32_t kSBufs = 3;
+  static constexpr uint32_t kSBufs = 2;
 };
 
 template <int D, bool kFp8>
@@ -171,7 +175,8 @@ __global__ void __launch_bounds__(tc_threads<kFp8>(), 1)
   __shared__ uint64_t k8_full[kTcStages], k8_empty[kTcStages];  // FP8 K: loaded, converted
   __shared__ float s_qamax[2][kTcBM];                           // FP8: [half][row] partial max |q|
   __shared__ uint64_t qamax_bar[4];
-  __shared__ uint64_t s_full[3], p_full[3], o_full[3], q_full, mma_done;  // per S/P buffer
+  __shared__ uint64_t s_full[Lay::kSBufs], p_full[Lay::kSBufs], o_full[Lay::kSBufs];  // per S/P buffer
+  __shared__ uint64_t q_full, mma_done;
   __shared__ uint32_t tmem_base_s;
   __shared__ Item s_item;
   __shared__ float s_xchg[2][2][kTcBM];  // [tile parity][half][row] partial row maxima
@@ -186,7 +191,7 @@ __global__ void __launch_bounds__(tc_threads<kFp8>(), 1)
       mbar_init(&k8_full[s], 1);
       mbar_init(&k8_empty[s], 32);
     }
-    for (int b = 0; b < 3; ++b) {
+    for (uint32_t b = 0; b < Lay::kSBufs; ++b) {
       mbar_init(&s_full[b], 1);
       mbar_init(&p_full[b], 256);
       mbar_init(&o_full[b], 1);
@@ -280,7 +285,6 @@ __global__ void __launch_bounds__(tc_threads<kFp8>(), 1)
       // address field (bits 0-13, in 16-byte units), so each MMA adds a small
       // constant. One thread issues every MMA, so its instruction count per
       // MMA sets the issue rate.
-      const uint64_t q_desc = umma_desc_sw128(sbase + Lay::kQ, 16, 1024);
       const uint64_t k_desc0 = umma_desc_sw128(sbase + Lay::kStage0, 16, 1024);
       const uint64_t v_desc0 = umma_desc_sw128(sbase + Lay::kStage0 + Lay::kKBytes, kTcBN * 128, 1024);
       constexpr uint64_t kStageStep = Lay::kStageBytes >> 4;
@@ -290,17 +294,17 @@ __global__ void __launch_bounds__(tc_threads<kFp8>(), 1)
       auto issue_s = [&](int32_t i) -> bool {
         const uint32_t st = uint32_t(i) % kTcStages, b = uint32_t(i) % Lay::kSBufs;
         if (!mbar_wait(&k_full[st], (i / kTcStages) & 1)) return false;
-        // buffer b holds tile i - 3's P until its PV is done
-        if (i >= 3 && !mbar_wait(&o_full[b], uint32_t((i - 3) / 3) & 1)) return false;
+        // buffer b holds tile i - 2's P until its PV is done
+        if (i >= int32_t(Lay::kSBufs) && !mbar_wait(&o_full[b], uint32_t((i - Lay::kSBufs) / Lay::kSBufs) & 1))
+          return false;
         tc_fence_after();
         const uint64_t kd = k_desc0 + st * kStageStep;
         const uint32_t tmem_s = tmem + b * kTcBN;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          // chunk kk / 4 of Q is kTcBM rows of 128 B further, of K kTcBN rows
-          const uint64_t off_q = uint64_t((kk >> 2) * (kTcBM * 128) + (kk & 3) * 32) >> 4;
+          // Q: 8 TMEM columns per 16 dims; K: chunk kk / 4 is kTcBN rows of 128 B further
           const uint64_t off_k = uint64_t((kk >> 2) * (kTcBN * 128) + (kk & 3) * 32) >> 4;
-          umma_bf16(tmem_s, q_desc + off_q, kd + off_k, idesc_s, kk > 0);
+          umma_bf16_tmem_a(tmem_s, tmem + Lay::kQCol + 8 * kk, kd + off_k, idesc_s, kk > 0);
         }
         umma_commit(&s_full[b]);
         return true;
@@ -311,9 +315,9 @@ __global__ void __launch_bounds__(tc_threads<kFp8>(), 1)
           ok = false;
           break;
         }
-        // per-buffer: the softmax cannot get a phase ahead on buffer i % 3
+        // per-buffer: the softmax cannot get a phase ahead on buffer i % 2
         // before PV i, which reads it, has been issued
-        if (!mbar_wait(&p_full[i % 3], uint32_t(i / 3) & 1)) {
+        if (!mbar_wait(&p_full[i % Lay::kSBufs], uint32_t(i / Lay::kSBufs) & 1)) {
           ok = false;
           break;
         }
@@ -399,18 +403,22 @@ __global__ void __launch_bounds__(tc_threads<kFp8>(), 1)
     const int32_t t = grow / g, hh = grow % g;
     const int32_t pos = valid ? it.len - it.n + t : -1;  // -1: attends nothing
     const int32_t lo = W > 0 ? pos + 1 - W : INT32_MIN;
-    // this thread's half of the Q row, 128-byte swizzled, zeros past the item
+    // this thread's half of the Q row into its TMEM lane (dims 2c and 2c + 1
+    // in column c, the lower in the low half: a bf16 pair of the row as it
+    // lies in memory), zeros past the item
     const uint16_t* qr = valid ? p.q + uint64_t(it.qstart + t) * p.q_stride + uint64_t(it.kv_head * g + hh) * D
                                : nullptr;
     float rs = p.score_scale;  // the row's score scale (FP8: the row's power-of-two Q scale undone)
     bool ok = true;
+    uint32_t qw[D / 4];        // this half's D / 2 dims, two per word
     if constexpr (!kFp8) {
 #pragma unroll
       for (uint32_t uh = 0; uh < D / 16; ++uh) {
-        const uint32_t u = half * (D / 16) + uh;
-        const uint4 v = qr ? *reinterpret_cast<const uint4*>(qr + 8 * u) : make_uint4(0, 0, 0, 0);
-        const uint32_t c = u >> 3, uu = u & 7;
-        *reinterpret_cast<uint4*>(smem + Lay::kQ + c * (kTcBM * 128) + row * 128 + ((uu ^ (row & 7)) << 4)) = v;
+        const uint4 v = qr ? *reinterpret_cast<const uint4*>(qr + 8 * (half * (D / 16) + uh)) : make_uint4(0, 0, 0, 0);
+        qw[4 * uh] = v.x;
+        qw[4 * uh + 1] = v.y;
+        qw[4 * uh + 2] = v.z;
+        qw[4 * uh + 3] = v.w;
       }
     } else {
       // f16 Q for the f16 S product: the row times 2^e, e chosen so that its
@@ -441,23 +449,23 @@ __global__ void __launch_bounds__(tc_threads<kFp8>(), 1)
       const float sc = ldexpf(1.0f, e);
       rs = p.score_scale * ldexpf(1.0f, -e);
 #pragma unroll
-      for (uint32_t uh = 0; uh < D / 16; ++uh) {
-        const uint32_t u = half * (D / 16) + uh;
-        uint32_t f[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) f[j] = f32x2_to_f16x2(qv[8 * uh + 2 * j] * sc, qv[8 * uh + 2 * j + 1] * sc);
-        const uint32_t c = u >> 3, uu = u & 7;
-        *reinterpret_cast<uint4*>(smem + Lay::kQ + c * (kTcBM * 128) + row * 128 + ((uu ^ (row & 7)) << 4)) =
-            make_uint4(f[0], f[1], f[2], f[3]);
-      }
+      for (uint32_t w = 0; w < D / 4; ++w) qw[w] = f32x2_to_f16x2(qv[2 * w] * sc, qv[2 * w + 1] * sc);
     }
-    fence_async_smem();
+    const uint32_t q_col = tmem + lane_addr + Lay::kQCol + half * (D / 4);
+    if constexpr (D == 128) {
+      tmem_st32(q_col, qw);
+    } else {
+      static_assert(D == 64, "head_dim 64 or 128");
+      tmem_st16(q_col, qw);
+    }
+    tmem_wait_st();
+    tc_fence_before();
     mbar_arrive(&q_full);
 
     float m_run = -INFINITY, l_run = 0.0f;
     for (int32_t i = 0; i < T && ok; ++i) {
       const uint32_t b = uint32_t(i) % Lay::kSBufs, st = uint32_t(i) % kTcStages, xb = uint32_t(i) & 1;
-      ok = __all_sync(0xffffffffu, mbar_wait(&s_full[b], uint32_t(i / 3) & 1));
+      ok = __all_sync(0xffffffffu, mbar_wait(&s_full[b], uint32_t(i / Lay::kSBufs) & 1));
       if (!ok) break;
       tc_fence_after();
       uint32_t sv[kHalfKeys];
@@ -509,7 +517,8 @@ __global__ void __launch_bounds__(tc_threads<kFp8>(), 1)
       const bool rescale = i > 0 && __any_sync(0xffffffffu, mx != m_run);
       // O changes only when every PV so far is done (tile i - 1's)
       if (rescale) {
-        ok = __all_sync(0xffffffffu, mbar_wait(&o_full[(i - 1) % 3], uint32_t((i - 1) / 3) & 1));
+        ok = __all_sync(0xffffffffu,
+                        mbar_wait(&o_full[(i - 1) % Lay::kSBufs], uint32_t((i - 1) / Lay::kSBufs) & 1));
         if (!ok) break;
         tc_fence_after();
       }
@@ -577,7 +586,8 @@ __global__ void __launch_bounds__(tc_threads<kFp8>(), 1)
     bool done = __all_sync(0xffffffffu, ok && mbar_wait(&lsum_bar[quad], 0));
     const float l_row = l_run + s_lsum[half ^ 1][row];
     if (done && T > 0) {
-      done = __all_sync(0xffffffffu, mbar_wait(&o_full[(T - 1) % 3], uint32_t((T - 1) / 3) & 1));
+      done = __all_sync(0xffffffffu,
+                        mbar_wait(&o_full[(T - 1) % Lay::kSBufs], uint32_t((T - 1) / Lay::kSBufs) & 1));
       tc_fence_after();
     }
     const float inv = l_row > 0.0f ? 1.0f / l_row : 0.0f;
