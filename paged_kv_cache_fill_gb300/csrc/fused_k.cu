@@ -239,12 +239,15 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) fused_k_norm_rope_kernel
       }
     }
     if (pass == blockIdx.x) __syncthreads();  // freq and sincos_pio32 written
-    // 2. sin/cos of every (token of the pass, frequency), by all threads
+    // 2. sin/cos of every (token of the pass, frequency), by all threads.
+    // Pair i = 4 l + q (lane l, group q) sits at [token][q][l], so the 16
+    // lanes of a row read 16 consecutive entries (no bank conflicts).
+    const uint32_t quarter = half >> 2;  // rotary_dim is a multiple of 8
     for (uint32_t e = threadIdx.x; e < ntok * half; e += kThreads) {
       const uint32_t j = e / half, i = e % half;
       const int32_t* pos_src = positions;
       if (kMrope) pos_src = (i % 3 == 0) ? positions : (i % 3 == 1 ? pos_h : pos_w);
-      table[j * half + i] = rope_sincos(__ldg(pos_src + t0 + j), freq[i], sincos_pio32);
+      table[j * half + (i & 3) * quarter + (i >> 2)] = rope_sincos(__ldg(pos_src + t0 + j), freq[i], sincos_pio32);
     }
     __syncthreads();
 
@@ -272,10 +275,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) fused_k_norm_rope_kernel
       for (int j = 0; j < 8; ++j) u[j] = __fmul_rn(x[j], w[j]);  // exact
       float out[8];
       if (is_pair && active) {
-        const float4* tb = &table[tok_of[k] * half + 4 * lane];
+        const float4* tb = &table[tok_of[k] * half + lane];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          const float4 sc = tb[q];  // {sin_hi, sin_lo, cos_hi, cos_lo}
+          const float4 sc = tb[q * quarter];  // pair 4 lane + q: {sin_hi, sin_lo, cos_hi, cos_lo}
           out[q] = rotate(u[q], u[4 + q], sc.z, sc.w, sc.x, sc.y, -1.0f);
           out[4 + q] = rotate(u[4 + q], u[q], sc.z, sc.w, sc.x, sc.y, 1.0f);
         }
