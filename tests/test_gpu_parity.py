@@ -6,6 +6,8 @@ taken where |reference| >= 0.2) of the fp64 oracle. Caches start filled with
 NaN patterns, so a kernel that touches an unattended row or a padding slot
 shows up as NaN or as a changed pool byte."""
 import math
+import os
+from concurrent.futures import ThreadPoolExecutor
 
 import numpy as np
 import pytest
@@ -630,16 +632,67 @@ def _sampled_reference(w, rows, q_cpu, seqs, heads, window, fp8):
             oracle.write_bf16(kk, vv, kr, vr, sl, L, H, D, bs, H * D, H * D)
     qs = u16(q_cpu[list(seqs)])
     sub_lens = np.ascontiguousarray(lens[list(seqs)].astype(np.int32))
-    out = {}
-    for i, s in enumerate(seqs):
-        for h in heads:
-            fp8_v = fp8 == "kv"
-            out[(s, h)] = oracle.decode_one(qs, None if fp8 else kr, kr if fp8 else None,
-                                            None if fp8_v else vr, table, sub_lens,
-                                            mb, w.num_q_heads, H, D, bs, w.inv_sqrt_d, w.k_scale,
-                                            w.num_q_heads * D, window, i, h,
-                                            v_cache_fp8=vr if fp8_v else None, v_scale=w.v_scale)
-    return out
+    fp8_v = fp8 == "kv"
+
+    def one(job):
+        i, h = job
+        return oracle.decode_one(qs, None if fp8 else kr, kr if fp8 else None, None if fp8_v else vr, table,
+                                 sub_lens, mb, w.num_q_heads, H, D, bs, w.inv_sqrt_d, w.k_scale,
+                                 w.num_q_heads * D, window, i, h, v_cache_fp8=vr if fp8_v else None,
+                                 v_scale=w.v_scale)
+    # the oracle's C calls release the GIL and share no state: threads run
+    # them side by side (no process is forked after the GPU calls)
+    jobs = [(i, h) for i in range(len(seqs)) for h in heads]
+    with ThreadPoolExecutor(max_workers=os.cpu_count() or 1) as pool:
+        results = list(pool.map(one, jobs))
+    return {(seqs[i], h): r for (i, h), r in zip(jobs, results)}
+
+
+def _check_pool_sample(w, fp8, kc, vc, lens, starts):
+    """The written pools on a seeded stratified sample of tokens: every
+    sequence's first and last token and every 97th (offset by the sequence
+    index), bit-exact against the oracle's encoding of the same rows at the
+    slots the oracle computes from the block tables."""
+    H, D, bs = w.num_kv_heads, w.head_dim, w.block_size
+    toks, slot_rows = [], []
+    tables = w.block_tables.cpu().numpy()
+    for s in range(w.num_seqs):
+        L = int(lens[s])
+        if L == 0:
+            continue
+        js = sorted({0, L - 1} | set(range(s % 97, L, 97)))
+        sl = oracle.fill_slots(tables[s], 0, L, bs)
+        toks += [int(starts[s]) + j for j in js]
+        slot_rows += [int(sl[j]) for j in js]
+    toks_t = torch.tensor(toks, dtype=torch.int64, device=DEV)
+    rows_t = torch.tensor(slot_rows, dtype=torch.int64, device=DEV)
+    m = len(toks)
+    key, value = u16(w.key[toks_t]), u16(w.value[toks_t])
+    k8, v8 = bool(fp8), fp8 == "kv"
+    kr = np.full((m, 1, H, D), kvgen.E4M3_NAN if k8 else kvgen.BF16_NAN, np.uint8 if k8 else np.uint16)
+    vr = np.full((m, 1, H, D), kvgen.E4M3_NAN if v8 else kvgen.BF16_NAN, np.uint8 if v8 else np.uint16)
+    compact = np.arange(m, dtype=np.int64)
+    if v8:
+        oracle.write_fp8(key, value, kr, vr, compact, m, H, D, 1, w.k_scale, w.v_scale, H * D, H * D)
+    elif k8:
+        oracle.write_fp8k(key, value, kr, vr, compact, m, H, D, 1, H * D, H * D, w.k_scale)
+    else:
+        oracle.write_bf16(key, value, kr, vr, compact, m, H, D, 1, H * D, H * D)
+
+    def gathered(pool):
+        flat = pool.view(-1, H * D)[rows_t]
+        return flat.cpu().numpy() if pool.dtype == torch.uint8 else u16(flat)
+    assert np.array_equal(gathered(kc), kr.reshape(m, H * D)), f"{w.name}: K pool sample differs"
+    assert np.array_equal(gathered(vc), vr.reshape(m, H * D)), f"{w.name}: V pool sample differs"
+
+
+def _stratified(lens, k, seed):
+    """k sequences: the longest, the shortest and a seeded spread of the rest."""
+    rng = np.random.default_rng(seed)
+    pick = {int(lens.argmax()), int(lens.argmin())}
+    rest = [s for s in range(len(lens)) if s not in pick]
+    pick |= set(int(x) for x in rng.choice(rest, size=min(k - len(pick), len(rest)), replace=False))
+    return sorted(pick)
 
 
 def _full_size(w, fp8, windows, sample_seqs, heads):
@@ -662,6 +715,7 @@ def _full_size(w, fp8, windows, sample_seqs, heads):
     with_workspace(w, True)
     lens = w.seq_lens.cpu().numpy()
     starts = np.concatenate([[0], np.cumsum(lens.astype(np.int64))])
+    _check_pool_sample(w, fp8, kc, vc, lens, starts)
     # copy just the sampled sequences' rows to the host
     rows = {s: (w.key[starts[s]:starts[s + 1]].cpu(), w.value[starts[s]:starts[s + 1]].cpu())
             for s in sample_seqs}
@@ -676,35 +730,32 @@ def _full_size(w, fp8, windows, sample_seqs, heads):
     assert pk.kv_get_device_error() == 0
 
 
-def test_full_bf16_gqa4_sampled():
+def test_full_bf16_gqa4_every_output():
+    """The BF16 decode workload in full: every (sequence, query head)."""
     w = kvgen.bf16_gqa4(device=DEV)
-    lens = w.seq_lens.cpu().numpy()
-    seqs = sorted({int(lens.argmax()), int(lens.argmin()), 0, 31, 63})
-    _full_size(w, False, (0,), seqs, (0, 3, 17, 31))
+    _full_size(w, False, (0,), list(range(w.num_seqs)), tuple(range(w.num_q_heads)))
 
 
 def test_full_fp8k_long_sampled():
+    """Every query head of 16 stratified sequences, W = 0 and 4096."""
     w = kvgen.fp8k_long(device=DEV)
-    _full_size(w, True, (0, 4096), [0, 77, 127], (0, 5, 31))
+    _full_size(w, True, (0, 4096), _stratified(w.seq_lens.cpu().numpy(), 16, 4),
+               tuple(range(w.num_q_heads)))
 
 
 def test_full_fp8k_mixed_sampled():
     w = kvgen.fp8k_mixed(device=DEV)
-    lens = w.seq_lens.cpu().numpy()
-    seqs = sorted({int(lens.argmax()), int(lens.argmin()), 100, 200})
-    _full_size(w, True, (0,), seqs, (0, 7, 8, 63))
+    _full_size(w, True, (0,), _stratified(w.seq_lens.cpu().numpy(), 16, 5), tuple(range(w.num_q_heads)))
 
 
 def test_full_fp8_kv_long_sampled():
     w = kvgen.fp8k_long(device=DEV)
-    _full_size(w, "kv", (0, 4096), [0, 77, 127], (0, 5, 31))
+    _full_size(w, "kv", (0, 4096), _stratified(w.seq_lens.cpu().numpy(), 16, 6), tuple(range(w.num_q_heads)))
 
 
 def test_full_fp8_kv_mixed_sampled():
     w = kvgen.fp8k_mixed(device=DEV)
-    lens = w.seq_lens.cpu().numpy()
-    seqs = sorted({int(lens.argmax()), int(lens.argmin()), 100, 200})
-    _full_size(w, "kv", (0,), seqs, (0, 7, 8, 63))
+    _full_size(w, "kv", (0,), _stratified(w.seq_lens.cpu().numpy(), 16, 7), tuple(range(w.num_q_heads)))
 
 
 def _full_prefill_sampled(w, fp8, chunk, seqs, rows_per_seq=3):
