@@ -209,7 +209,8 @@ PAGEDKV_API int kv_write_v_only(const kv_bf16_t *value, kv_bf16_t *v_cache, cons
  *   output  device float32[num_seqs, num_q_heads, head_dim], written.
  *   seq_lens[s] <= max_blocks_per_seq * block_size.
  * Supported: head_dim in {64, 128, 256} (FP8: {128, 256}); block_size a power
- * of two in [8, 256]; g <= 16; q, caches and q_stride 16-byte aligned.
+ * of two in [16, 256]; g <= 16; q, caches and q_stride 16-byte aligned;
+ * output 8-byte aligned. Anything else returns KV_ERR_UNSUPPORTED.
  * Long sequences are split across CTAs (flash-decoding) when a workspace was
  * registered with kv_set_decode_workspace; without one every (sequence, KV
  * head group) runs in one CTA (same result, less parallelism).

@@ -469,6 +469,7 @@ CASES = [
     ([260, 1000], 16, 1, 256, 128, (0, 300)),
     ([300, 77], 12, 1, 128, 256, (0, 50)),
     ([400, 90, 3], 6, 3, 64, 16, (0, 33)),
+    ([129, 1500, 16], 32, 2, 128, 16, (0, 200)),     # the largest group (16): two 8-head tiles per KV head
 ]
 
 
@@ -728,6 +729,17 @@ def _full_size(w, fp8, windows, sample_seqs, heads):
         assert_decode_close(g, r, f"{w.name} window {win}")
         assert np.isfinite(got).all()
     assert pk.kv_get_device_error() == 0
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_decode_one_very_long_sequence_every_head(fp8):
+    """A 262,144-position sequence beside a one-position one: ~1,000
+    split-KV partials for one (sequence, query head), the pool written in the
+    benchmark's 262,144-token chunks; every query head, with and without a
+    window."""
+    w = kvgen.custom(240, device=DEV, seq_lens=[262144, 1], num_q_heads=32, num_kv_heads=8, head_dim=128,
+                     block_size=16, fp8=fp8)
+    _full_size(w, fp8, (0, 5000), [0, 1], tuple(range(32)))
 
 
 def test_full_bf16_gqa4_every_output():
