@@ -6,7 +6,8 @@ raises PagedKVError on a non-zero status. All work runs in the library's
 CUDA kernels; there is no other implementation to fall back on, so a missing
 library is an error.
 
-Tensors must live on the current CUDA device. BF16 data are torch.bfloat16
+Tensors must be contiguous and live on the current CUDA device (checked
+here; the C entry points take raw pointers). BF16 data are torch.bfloat16
 (or int16/uint16 bit patterns), FP8 caches torch.uint8 or
 torch.float8_e4m3fn. `stream` is a torch.cuda.Stream, a raw cudaStream_t
 integer, or None for torch's current stream.
@@ -113,8 +114,14 @@ def _ptr(t: torch.Tensor | None):
         return None
     if not isinstance(t, torch.Tensor):
         raise TypeError("expected a torch.Tensor")
-    if t.numel() and not t.is_cuda:
-        raise ValueError("tensor must be on a CUDA device")
+    if t.numel():
+        if not t.is_cuda:
+            raise ValueError("tensor must be on a CUDA device")
+        if t.get_device() != torch.cuda.current_device():
+            raise ValueError(f"tensor is on cuda:{t.get_device()}, the current device is "
+                             f"cuda:{torch.cuda.current_device()}")
+        if not t.is_contiguous():
+            raise ValueError("tensor must be contiguous (the library reads rows at the strides it is given)")
     return t.data_ptr() or None
 
 

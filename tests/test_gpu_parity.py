@@ -86,6 +86,17 @@ def with_workspace(w, on=True):
     return ws
 
 
+def test_binding_refuses_host_and_strided_tensors():
+    """The C entry points take raw pointers: the binding refuses a host
+    tensor and a non-contiguous view before any launch."""
+    table = torch.arange(8, dtype=torch.int32, device=DEV)
+    slots = torch.empty(16, dtype=torch.int64, device=DEV)
+    with pytest.raises(ValueError, match="CUDA device"):
+        pk.kv_fill_slots(slots, table.cpu(), 0, 16, 2)
+    with pytest.raises(ValueError, match="contiguous"):
+        pk.kv_fill_slots(torch.empty(32, dtype=torch.int64, device=DEV)[::2], table, 0, 16, 2)
+
+
 # ---------------------------------------------------------------------------
 # slot filling
 # ---------------------------------------------------------------------------
