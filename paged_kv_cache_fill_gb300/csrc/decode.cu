@@ -156,21 +156,23 @@ __device__ __forceinline__ void pv_tile(float (&acc)[D / 16][4], uint32_t vbase,
                                         uint32_t bh0, uint32_t bh1, uint32_t bl0, uint32_t bl1, uint32_t vmask01,
                                         uint32_t vmask89) {
   if constexpr (!kFp8V) {
+    uint32_t a[D / 16][4];
 #pragma unroll
     for (int i = 0; i < D / 16; ++i) {
       const uint32_t chunk = i >> 2;
       const uint32_t unit = ((i & 3) << 1) + unit_lo;
-      uint32_t a[4];
-      ldmatrix_x4_trans(a, vbase + chunk * (kTile * 128) + row * 128 + ((unit ^ (row & 7)) << 4));
+      ldmatrix_x4_trans(a[i], vbase + chunk * (kTile * 128) + row * 128 + ((unit ^ (row & 7)) << 4));
       if constexpr (kMask) {
-        a[0] &= vmask01;
-        a[1] &= vmask01;
-        a[2] &= vmask89;
-        a[3] &= vmask89;
+        a[i][0] &= vmask01;
+        a[i][1] &= vmask01;
+        a[i][2] &= vmask89;
+        a[i][3] &= vmask89;
       }
-      mma_bf16(acc[i], a, bh0, bh1);
-      mma_bf16(acc[i], a, bl0, bl1);
+      mma_bf16(acc[i], a[i], bh0, bh1);
     }
+    // the lo parts after every hi part: no MMA waits on the one before
+#pragma unroll
+    for (int i = 0; i < D / 16; ++i) mma_bf16(acc[i], a[i], bl0, bl1);
   } else {
 #pragma unroll
     for (int jj = 0; jj < D / 32; ++jj) {
@@ -195,9 +197,10 @@ __device__ __forceinline__ void pv_tile(float (&acc)[D / 16][4], uint32_t vbase,
           a[h][3] &= vmask89;
         }
       }
+      // hi, hi, lo, lo: no MMA waits on the accumulator of the one before
       mma_f16(acc[2 * jj], a[0], bh0, bh1);
-      mma_f16(acc[2 * jj], a[0], bl0, bl1);
       mma_f16(acc[2 * jj + 1], a[1], bh0, bh1);
+      mma_f16(acc[2 * jj], a[0], bl0, bl1);
       mma_f16(acc[2 * jj + 1], a[1], bl0, bl1);
     }
   }
@@ -464,8 +467,9 @@ __global__ void __launch_bounds__(32 * 9, 1)
     if (head_ok && !(mt.flags & kEmpty)) {
       const uint32_t kbase = smem_u32(st) + hl * (kKChunks * kTile * 128);
       const uint32_t vbase = smem_u32(st + p.k_bytes) + hl * (kVChunks * kTile * 128);
-      // ---- S^T = K Q^T (16 tokens x 8 query heads)
-      float s[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      // ---- S^T = K Q^T (16 tokens x 8 query heads), even and odd k-steps in
+      // two accumulators so that consecutive MMAs do not wait on each other
+      float s[4] = {0.0f, 0.0f, 0.0f, 0.0f}, s2[4] = {0.0f, 0.0f, 0.0f, 0.0f};
       if constexpr (!kFp8) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
@@ -473,7 +477,8 @@ __global__ void __launch_bounds__(32 * 9, 1)
           const uint32_t unit = ((kk & 3) << 1) + k_unit;
           uint32_t a[4];
           ldmatrix_x4(a, kbase + chunk * (kTile * 128) + k_row * 128 + ((unit ^ (k_row & 7)) << 4));
-          mma_bf16(s, a, qf[kk][0], qf[kk][1]);
+          if (kk & 1) mma_bf16(s2, a, qf[kk][0], qf[kk][1]);
+          else mma_bf16(s, a, qf[kk][0], qf[kk][1]);
         }
       } else {
 #pragma unroll
@@ -492,9 +497,13 @@ __global__ void __launch_bounds__(32 * 9, 1)
           a1[2] = e4m3x2_to_f16x2(uint16_t(r[2] >> 16));
           a1[3] = e4m3x2_to_f16x2(uint16_t(r[3] >> 16));
           mma_f16(s, a0, qf[2 * jj][0], qf[2 * jj][1]);
-          mma_f16(s, a1, qf[2 * jj + 1][0], qf[2 * jj + 1][1]);
+          mma_f16(s2, a1, qf[2 * jj + 1][0], qf[2 * jj + 1][1]);
         }
       }
+      s[0] += s2[0];
+      s[1] += s2[1];
+      s[2] += s2[2];
+      s[3] += s2[3];
       s[0] *= head_scale[0];
       s[1] *= head_scale[1];
       s[2] *= head_scale[0];
