@@ -876,13 +876,33 @@ def run_e2e(step, args, dev, world):
         torch.cuda.synchronize()
         return start.elapsed_time(end)
 
+    def copies_alone():
+        # the step's own pinned buffers, copied with no kernel running: the
+        # floor of a step's time on this host (placement of the pinned pages
+        # and other traffic on the host included)
+        t = []
+        for src, dst in ((host_in, dev_in[0]), (dev_out[0], host_out[0])):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(h2d_s)
+            with torch.cuda.stream(h2d_s):
+                for x, y in zip(src, dst):
+                    y.copy_(x, non_blocking=True)
+            b.record(h2d_s)
+            b.synchronize()
+            t.append(a.elapsed_time(b))
+        return t
+
     run(2)  # warm-up: both graphs and both buffer sets
     ms = run(steps) / steps
+    alone = [copies_alone() for _ in range(2)]
+    h2d_ms, d2h_ms = min(t[0] for t in alone), min(t[1] for t in alone)
     del twin_graph, twins
     link = host_link_gbs(compute)
+    link.update(step_h2d_gbs=round(h2d / (h2d_ms * 1e-3) / 1e9, 1), step_d2h_gbs=round(d2h / (d2h_ms * 1e-3) / 1e9, 1))
     # the step cannot end before its inputs have crossed the host link and
-    # its outputs have come back: that time bounds the end-to-end rate
-    link_ms = 1e3 * (h2d / (link["h2d_gbs"] * 1e9) + d2h / (link["d2h_gbs"] * 1e9))
+    # its outputs have come back: the step's own copies, timed alone, bound
+    # the end-to-end rate
+    link_ms = h2d_ms + d2h_ms
     bound = step.total_bytes * world / (link_ms * 1e-3) / 1e9
     value = step.total_bytes * world / (ms * 1e-3) / 1e9
     return {"value": round(value, 1), "unit": "GB/s",
