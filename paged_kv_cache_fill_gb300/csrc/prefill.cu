@@ -112,8 +112,8 @@ __device__ Item locate(uint32_t target, const PrefillParams& p, uint32_t lane) {
 // an FP8-K cache):
 //   warps 0, 10 TMA producers of 128-key K and V tiles, each [chunk][key][128 B]
 //               (one box per 16-slot block run and 128-byte chunk), in two
-//               2-stage rings: a K stage is free once the S two tiles back is
-//               done, a V stage once that tile's PV is;
+//               2-stage rings: a K stage is free once the S product of the
+//               tile two back is done, a V stage once that tile's PV is;
 //   warp 11     (FP8 K only) converts each E4M3 K tile, loaded into its own
 //               ring, into the f16 K tile (exact);
 //   warp 1      owns TMEM and issues every tcgen05.mma from one thread:
@@ -122,9 +122,9 @@ __device__ Item locate(uint32_t target, const PrefillParams& p, uint32_t lane) {
 //               two TMEM S buffers, Q read from tensor memory, then
 //               O += P_hi V + P_lo V (M 128, N = head_dim, K 128) into TMEM
 //               O, P from TMEM (written over its S buffer), V read as the
-//               MN-major shared-memory operand. Only K and V tiles are read
-//               from shared memory: the kernel's time follows its
-//               shared-memory traffic per tile;
+//               MN-major shared-memory operand (only K and V tiles are
+//               read from shared memory); this thread's issue-and-wait loop
+//               is the kernel's serial path;
 //   warps 2..9  softmax, two threads per row = TMEM lane (warp w owns lanes
 //               32 (w % 4) ..; warps 2..5 the first half of a tile's keys and
 //               of O's columns, warps 6..9 the second): Q rows into tensor
@@ -232,13 +232,13 @@ __global__ void __launch_bounds__(tc_threads<kFp8>(), 1)
 
   if (warp == 0 || warp == kVWarp) {
     // ------------------------------------------------------------ producers
-    // warp 0 loads K, the last warp V, each into its own ring: a K stage is
-    // free again once its S product is done, a V stage once its PV is
-    // a K stage is free once the S product two tiles back is done (s_full),
-    // a V stage once that tile's PV is done (o_full): the MMA thread commits
-    // nothing extra for the producers, and loads are in order, so those
-    // barriers cannot have moved on to a later tile of the same buffer yet
-    // (FP8: K lands in its own ring, free once the converters have read it)
+    // warp 0 loads K, warp 10 V, each into its own 2-stage ring. A K stage
+    // is free once the S product of the tile two back is done (s_full of its
+    // S buffer), a V stage once that tile's PV product is done (o_full): the
+    // MMA thread commits nothing extra for the producers. With two S buffers
+    // the same barrier completes next for tile i itself, which needs this
+    // load first, so the parity of the wait is unambiguous. FP8 K lands in a
+    // ring of its own, free once the converter warp has read it.
     const bool is_k = warp == 0;
     const CUtensorMap* map = is_k ? &tmap_k : &tmap_v;
     uint64_t* full = is_k ? (kFp8 ? k8_full : k_full) : v_full;
