@@ -163,7 +163,7 @@ WORKLOAD_OF_PART = {"fused_write": "fused", "bf16_prefill": "bf16_gqa4", "bf16_d
                     "fused_k_write_fp8": "fused", "fused_k_write_mrope": "fused",
                     "fp8_kv_prefill": "fp8k_long", "fp8_kv_decode_w0": "fp8k_long",
                     "fp8_kv_mixed_decode": "fp8k_mixed", "bf16_chunked_prefill": "bf16_gqa4",
-                    "fp8k_chunked_prefill": "fp8k_mixed"}
+                    "fp8k_chunked_prefill": "fp8k_mixed", "fp8_kv_chunked_prefill": "fp8k_mixed"}
 
 
 class GpuStep:
@@ -468,6 +468,17 @@ class GpuStep:
         self.extras.append(dict(name="fp8k_chunked_prefill", fn=prefill_attn, tokens=n_q,
                                 flops=prefill_flops(w.seq_lens[:ns].tolist(), q_lens, 0, Hq, D),
                                 bytes=sum(int(L) for L in w.seq_lens[:ns].tolist()) * H * D * 3
+                                + n_q * Hq * D * (2 + 4)))
+
+        # the same queries over the FP8 K and V cache
+        outpq = torch.empty((n_q, Hq, D), dtype=torch.float32, device=dev)
+
+        def fp8kv_prefill_attn():
+            pk.paged_prefill_attn_fp8(qp, kc, vc8, outpq, tables_p, lens_p, qsl, w.max_blocks_per_seq, ns, n_q, Hq,
+                                      H, D, bs, w.inv_sqrt_d, k_scale, v_scale, Hq * D, 0)
+        self.extras.append(dict(name="fp8_kv_chunked_prefill", fn=fp8kv_prefill_attn, tokens=n_q,
+                                flops=prefill_flops(w.seq_lens[:ns].tolist(), q_lens, 0, Hq, D),
+                                bytes=sum(int(L) for L in w.seq_lens[:ns].tolist()) * H * D * 2
                                 + n_q * Hq * D * (2 + 4)))
 
     def _grow_ws(self, w):

@@ -281,6 +281,18 @@ PAGEDKV_API int paged_prefill_attn_fp8k(const kv_bf16_t *q, const kv_e4m3_t *k_c
                                         uint32_t block_size, float inv_sqrt_d, float k_scale, uint32_t q_stride,
                                         uint32_t sliding_window, void *stream);
 
+/* Multi-token paged attention over an FP8 K and V cache (the cache that
+ * kv_write_fp8 fills and paged_decode_attn_fp8 reads): as
+ * paged_prefill_attn_fp8k, with v_p = E4M3 code * v_scale (v_scale finite and
+ * > 0) read from a uint8 V pool. head_dim 128. */
+PAGEDKV_API int paged_prefill_attn_fp8(const kv_bf16_t *q, const kv_e4m3_t *k_cache_fp8,
+                                       const kv_e4m3_t *v_cache_fp8, float *output, const int32_t *block_tables,
+                                       const int32_t *seq_lens, const int32_t *query_start_loc,
+                                       uint32_t max_blocks_per_seq, uint32_t num_seqs, uint32_t num_q_tokens,
+                                       uint32_t num_q_heads, uint32_t num_kv_heads, uint32_t head_dim,
+                                       uint32_t block_size, float inv_sqrt_d, float k_scale, float v_scale,
+                                       uint32_t q_stride, uint32_t sliding_window, void *stream);
+
 /* ------------------------------------------------------------------------
  * FP8-K paged decode without any caller-provided memory. The source pages
  * have no counterpart of this call; it exists for callers that cannot give

@@ -348,23 +348,29 @@ def paged_decode_attn_fp8(q, k_cache_fp8, v_cache_fp8, block_tables, seq_lens, m
 
 def paged_prefill_attn(q, k_cache_bf16, k_cache_fp8, v_cache, block_tables, seq_lens, query_start_loc,
                        max_blocks_per_seq, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
-                       inv_sqrt_d, k_scale, q_stride, sliding_window) -> np.ndarray:
+                       inv_sqrt_d, k_scale, q_stride, sliding_window, v_cache_fp8=None,
+                       v_scale=1.0) -> np.ndarray:
     """Multi-token paged attention; pass k_cache_fp8 (and k_scale) or
-    k_cache_bf16, the other None. Returns float32 [num_q_tokens, Hq, D]."""
+    k_cache_bf16, the other None; v_cache_fp8 (with v_scale) in place of
+    v_cache selects an E4M3 V cache. Returns float32 [num_q_tokens, Hq, D]."""
     _check(q, np.uint16, "q")
     if k_cache_fp8 is None:
         _check(k_cache_bf16, np.uint16, "k_cache_bf16")
     else:
         _check(k_cache_fp8, np.uint8, "k_cache_fp8")
-    _check(v_cache, np.uint16, "v_cache")
+    if v_cache_fp8 is None:
+        _check(v_cache, np.uint16, "v_cache")
+    else:
+        _check(v_cache_fp8, np.uint8, "v_cache_fp8")
+        v_cache = None
     _check(block_tables, np.int32, "block_tables")
     _check(seq_lens, np.int32, "seq_lens")
     _check(query_start_loc, np.int32, "query_start_loc")
     n_q = int(query_start_loc[int(num_seqs)])
     out = np.empty((n_q, int(num_q_heads), int(head_dim)), np.float32)
     lib().oracle_paged_prefill_attn(
-        _ptr(q), _ptr(k_cache_bf16), _ptr(k_cache_fp8), _ptr(v_cache), _ptr(out), _ptr(block_tables),
-        _ptr(seq_lens), _ptr(query_start_loc), _u32(max_blocks_per_seq), _u32(num_seqs), _u32(num_q_heads),
-        _u32(num_kv_heads), _u32(head_dim), _u32(block_size), _f32(inv_sqrt_d), _f32(k_scale), _u32(q_stride),
-        _u32(sliding_window))
+        _ptr(q), _ptr(k_cache_bf16), _ptr(k_cache_fp8), _ptr(v_cache), _ptr(v_cache_fp8), _ptr(out),
+        _ptr(block_tables), _ptr(seq_lens), _ptr(query_start_loc), _u32(max_blocks_per_seq), _u32(num_seqs),
+        _u32(num_q_heads), _u32(num_kv_heads), _u32(head_dim), _u32(block_size), _f32(inv_sqrt_d), _f32(k_scale),
+        _f32(v_scale), _u32(q_stride), _u32(sliding_window))
     return out

@@ -544,12 +544,14 @@ void oracle_paged_decode_attn_fp8(const uint16_t *q, const uint8_t *k_cache_fp8,
  * FP8-K cache (k_scale as in the FP8-K decode).
  * ---------------------------------------------------------------------- */
 void oracle_paged_prefill_attn(const uint16_t *q, const uint16_t *k_cache_bf16,
-                               const uint8_t *k_cache_fp8, const uint16_t *v_cache, float *output,
+                               const uint8_t *k_cache_fp8, const uint16_t *v_cache,
+                               const uint8_t *v_cache_fp8, float *output,
                                const int32_t *block_tables, const int32_t *seq_lens,
                                const int32_t *query_start_loc, uint32_t max_blocks_per_seq,
                                uint32_t num_seqs, uint32_t num_q_heads, uint32_t num_kv_heads,
                                uint32_t head_dim, uint32_t block_size, float inv_sqrt_d,
-                               float k_scale, uint32_t q_stride, uint32_t sliding_window) {
+                               float k_scale, float v_scale, uint32_t q_stride,
+                               uint32_t sliding_window) {
     double out[1024];
     uint32_t group = num_q_heads / num_kv_heads;
     for (uint32_t s = 0; s < num_seqs; ++s) {
@@ -559,8 +561,8 @@ void oracle_paged_prefill_attn(const uint16_t *q, const uint16_t *k_cache_bf16,
             int64_t position = (int64_t)seq_lens[s] - n + j;
             for (uint32_t h = 0; h < num_q_heads; ++h) {
                 attend(q + row * q_stride + (int64_t)h * head_dim, k_cache_bf16, k_cache_fp8,
-                       v_cache, 0, block_tables + (int64_t)s * max_blocks_per_seq, position + 1,
-                       num_kv_heads, h / group, head_dim, block_size, inv_sqrt_d, k_scale, 1.0f,
+                       v_cache, v_cache_fp8, block_tables + (int64_t)s * max_blocks_per_seq, position + 1,
+                       num_kv_heads, h / group, head_dim, block_size, inv_sqrt_d, k_scale, v_scale,
                        sliding_window, out, 0);
                 for (uint32_t d = 0; d < head_dim; ++d)
                     output[(row * num_q_heads + h) * head_dim + d] = (float)out[d];

@@ -24,7 +24,7 @@ __all__ = [
     "kv_write_fused_k_norm_rope_bf16", "kv_write_fused_k_norm_rope_bf16_mrope",
     "kv_write_fused_k_norm_rope_fp8", "kv_write_v_only", "paged_decode_attn_bf16",
     "paged_decode_attn_fp8k", "paged_decode_attn_fp8", "paged_prefill_attn_bf16", "paged_prefill_attn_fp8k",
-    "paged_decode_attn_fp8k_static_scratch",
+    "paged_prefill_attn_fp8", "paged_decode_attn_fp8k_static_scratch",
     "kv_decode_workspace_bytes",
     "kv_set_decode_workspace", "kv_get_device_error", "kv_device_info", "KV_OK", "KV_ERR_INVALID_ARG",
     "KV_ERR_UNSUPPORTED", "KV_ERR_CUDA", "KV_ERR_DEVICE",
@@ -65,6 +65,9 @@ _SIGNATURES = {
     "paged_prefill_attn_fp8k": (
         ctypes.c_int,
         [_P, _P, _P, _P, _P, _P, _P, _U32, _U32, _U32, _U32, _U32, _U32, _U32, _F32, _F32, _U32, _U32, _P]),
+    "paged_prefill_attn_fp8": (
+        ctypes.c_int,
+        [_P, _P, _P, _P, _P, _P, _P, _U32, _U32, _U32, _U32, _U32, _U32, _U32, _F32, _F32, _F32, _U32, _U32, _P]),
     "paged_decode_attn_fp8k_static_scratch": (
         ctypes.c_int,
         [_P, _P, _P, _P, _P, _P, _U32, _U32, _U32, _U32, _U32, _U32, _F32, _F32, _U32, _U32, _P]),
@@ -234,6 +237,15 @@ def paged_prefill_attn_fp8k(q, k_cache_fp8, v_cache, output, block_tables, seq_l
         _ptr(q), _ptr(k_cache_fp8), _ptr(v_cache), _ptr(output), _ptr(block_tables), _ptr(seq_lens),
         _ptr(query_start_loc), max_blocks_per_seq, num_seqs, num_q_tokens, num_q_heads, num_kv_heads, head_dim,
         block_size, inv_sqrt_d, k_scale, q_stride, sliding_window, _stream(stream)))
+
+
+def paged_prefill_attn_fp8(q, k_cache_fp8, v_cache_fp8, output, block_tables, seq_lens, query_start_loc,
+                           max_blocks_per_seq, num_seqs, num_q_tokens, num_q_heads, num_kv_heads, head_dim,
+                           block_size, inv_sqrt_d, k_scale, v_scale, q_stride, sliding_window, stream=None):
+    _check("paged_prefill_attn_fp8", lib().paged_prefill_attn_fp8(
+        _ptr(q), _ptr(k_cache_fp8), _ptr(v_cache_fp8), _ptr(output), _ptr(block_tables), _ptr(seq_lens),
+        _ptr(query_start_loc), max_blocks_per_seq, num_seqs, num_q_tokens, num_q_heads, num_kv_heads, head_dim,
+        block_size, inv_sqrt_d, k_scale, v_scale, q_stride, sliding_window, _stream(stream)))
 
 
 def paged_decode_attn_fp8k_static_scratch(q, k_cache_fp8, v_cache, output, block_tables, seq_lens,

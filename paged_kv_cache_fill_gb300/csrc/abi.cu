@@ -282,12 +282,12 @@ int paged_decode_attn_fp8(const kv_bf16_t* q, const kv_e4m3_t* k_cache_fp8, cons
                        sliding_window, true, true, v_scale, stream);
 }
 
-static int prefill_common(const kv_bf16_t* q, const void* k_cache, const kv_bf16_t* v_cache, float* output,
+static int prefill_common(const kv_bf16_t* q, const void* k_cache, const void* v_cache, float* output,
                           const int32_t* block_tables, const int32_t* seq_lens, const int32_t* query_start_loc,
                           uint32_t max_blocks_per_seq, uint32_t num_seqs, uint32_t num_q_tokens,
                           uint32_t num_q_heads, uint32_t num_kv_heads, uint32_t head_dim, uint32_t block_size,
-                          float inv_sqrt_d, float k_scale, uint32_t q_stride, uint32_t sliding_window, bool fp8,
-                          void* stream) {
+                          float inv_sqrt_d, float k_scale, float v_scale, uint32_t q_stride,
+                          uint32_t sliding_window, bool fp8, bool fp8_v, void* stream) {
   if (num_seqs == 0 || num_q_tokens == 0) return KV_OK;
   if (!q || !k_cache || !v_cache || !output || !block_tables || !seq_lens || !query_start_loc)
     return KV_ERR_INVALID_ARG;
@@ -296,6 +296,7 @@ static int prefill_common(const kv_bf16_t* q, const void* k_cache, const kv_bf16
   if (uint64_t(q_stride) < uint64_t(num_q_heads) * head_dim) return KV_ERR_INVALID_ARG;
   if (!isfinite(inv_sqrt_d)) return KV_ERR_INVALID_ARG;
   if (fp8 && (!(k_scale > 0.0f) || !isfinite(k_scale))) return KV_ERR_INVALID_ARG;
+  if (fp8_v && (!(v_scale > 0.0f) || !isfinite(v_scale))) return KV_ERR_INVALID_ARG;
   if (fp8 ? head_dim != 128 : (head_dim != 64 && head_dim != 128)) return KV_ERR_UNSUPPORTED;
   if (!is_pow2(block_size) || block_size < 16 || block_size > 256) return KV_ERR_UNSUPPORTED;
   if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || (q_stride * 2u) % 16)
@@ -323,9 +324,11 @@ static int prefill_common(const kv_bf16_t* q, const void* k_cache, const kv_bf16
   a.block_size = block_size;
   a.inv_sqrt_d = inv_sqrt_d;
   a.k_scale = k_scale;
+  a.v_scale = v_scale;
   a.q_stride = q_stride;
   a.sliding_window = sliding_window;
   a.fp8 = fp8;
+  a.fp8_v = fp8_v;
   return launch_prefill(a, as_stream(stream));
 }
 
@@ -336,7 +339,7 @@ int paged_prefill_attn_bf16(const kv_bf16_t* q, const kv_bf16_t* k_cache, const 
                             float inv_sqrt_d, uint32_t q_stride, uint32_t sliding_window, void* stream) {
   return prefill_common(q, k_cache, v_cache, output, block_tables, seq_lens, query_start_loc, max_blocks_per_seq,
                         num_seqs, num_q_tokens, num_q_heads, num_kv_heads, head_dim, block_size, inv_sqrt_d, 1.0f,
-                        q_stride, sliding_window, false, stream);
+                        1.0f, q_stride, sliding_window, false, false, stream);
 }
 
 int paged_prefill_attn_fp8k(const kv_bf16_t* q, const kv_e4m3_t* k_cache_fp8, const kv_bf16_t* v_cache,
@@ -347,7 +350,18 @@ int paged_prefill_attn_fp8k(const kv_bf16_t* q, const kv_e4m3_t* k_cache_fp8, co
                             uint32_t sliding_window, void* stream) {
   return prefill_common(q, k_cache_fp8, v_cache, output, block_tables, seq_lens, query_start_loc,
                         max_blocks_per_seq, num_seqs, num_q_tokens, num_q_heads, num_kv_heads, head_dim, block_size,
-                        inv_sqrt_d, k_scale, q_stride, sliding_window, true, stream);
+                        inv_sqrt_d, k_scale, 1.0f, q_stride, sliding_window, true, false, stream);
+}
+
+int paged_prefill_attn_fp8(const kv_bf16_t* q, const kv_e4m3_t* k_cache_fp8, const kv_e4m3_t* v_cache_fp8,
+                           float* output, const int32_t* block_tables, const int32_t* seq_lens,
+                           const int32_t* query_start_loc, uint32_t max_blocks_per_seq, uint32_t num_seqs,
+                           uint32_t num_q_tokens, uint32_t num_q_heads, uint32_t num_kv_heads, uint32_t head_dim,
+                           uint32_t block_size, float inv_sqrt_d, float k_scale, float v_scale, uint32_t q_stride,
+                           uint32_t sliding_window, void* stream) {
+  return prefill_common(q, k_cache_fp8, v_cache_fp8, output, block_tables, seq_lens, query_start_loc,
+                        max_blocks_per_seq, num_seqs, num_q_tokens, num_q_heads, num_kv_heads, head_dim, block_size,
+                        inv_sqrt_d, k_scale, v_scale, q_stride, sliding_window, true, true, stream);
 }
 
 size_t kv_decode_workspace_bytes(uint32_t max_blocks_per_seq, uint32_t num_seqs, uint32_t num_q_heads,

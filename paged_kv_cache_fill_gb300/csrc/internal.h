@@ -56,15 +56,15 @@ bool encode_pool_map(CUtensorMap* map, const void* base, bool fp8, uint32_t num_
 struct PrefillArgs {
   const uint16_t* q;
   const void* k_cache;  // bf16 or e4m3 pool
-  const uint16_t* v_cache;
+  const void* v_cache;  // bf16 or (fp8_v) e4m3 pool
   float* output;
   const int32_t* block_tables;
   const int32_t* seq_lens;
   const int32_t* query_start_loc;
   uint32_t max_blocks_per_seq, num_seqs, num_q_tokens, num_q_heads, num_kv_heads, head_dim, block_size;
-  float inv_sqrt_d, k_scale;
+  float inv_sqrt_d, k_scale, v_scale;
   uint32_t q_stride, sliding_window;
-  bool fp8;
+  bool fp8, fp8_v;  // fp8_v implies fp8
 };
 int launch_prefill(const PrefillArgs& a, cudaStream_t stream);
 cudaError_t read_and_clear_prefill_error(uint32_t* bits);

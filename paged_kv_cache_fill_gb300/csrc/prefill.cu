@@ -40,8 +40,59 @@ struct PrefillParams {
   uint32_t max_blocks_per_seq, num_seqs, num_q_tokens, num_q_heads, num_kv_heads, group;
   uint32_t block_size, block_shift, q_stride, sliding_window;
   float score_scale;  // inv_sqrt_d * log2(e) (times k_scale for FP8)
+  float out_scale;    // E4M3 V: v_scale (the V codes enter the PV product as they are)
   uint32_t k_box_bytes, v_box_bytes, stage_bytes;
 };
+
+// An E4M3 tile [chunk of 128 dims][128 keys][128 B] -> the f16 tile [chunk of
+// 64 dims][128 keys][128 B], both 128-byte swizzled; rows at or past `live`
+// become zeros. Exact (every E4M3 value is an f16 value). Lane l takes keys
+// l, l + 32 (first pass) and l + 64, l + 96 (second). Each pass loads its
+// two rows (16 x 16 B) before any store: the stores could alias the loads as
+// far as the compiler knows, so interleaving them would serialise every
+// load behind the previous unit's stores. A dead row's codes are replaced by
+// zeros as loaded (E4M3 0 is f16 0), which costs far fewer instructions than
+// selecting every converted word.
+template <int D>
+__device__ __forceinline__ void e4m3_tile_to_f16(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst,
+                                                 int32_t live, uint32_t lane) {
+#pragma unroll
+  for (uint32_t r0 = 0; r0 < 128u; r0 += 64) {
+#pragma unroll
+    for (uint32_t c8 = 0; c8 < uint32_t(D / 128); ++c8) {
+      uint4 w[2][8];
+#pragma unroll
+      for (uint32_t k = 0; k < 2; ++k) {
+        const uint32_t r = r0 + 32 * k + lane;
+        const bool keep = int32_t(r) < live;
+#pragma unroll
+        for (uint32_t u = 0; u < 8; ++u) {
+          w[k][u] = *reinterpret_cast<const uint4*>(src + c8 * (128 * 128) + r * 128 + ((u ^ (r & 7)) << 4));
+          if (!keep) w[k][u] = make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+#pragma unroll
+      for (uint32_t k = 0; k < 2; ++k) {
+        const uint32_t r = r0 + 32 * k + lane;
+#pragma unroll
+        for (uint32_t u = 0; u < 8; ++u) {  // 16 dims per 16-byte unit
+          const uint32_t ws[4] = {w[k][u].x, w[k][u].y, w[k][u].z, w[k][u].w};
+          uint32_t h[8];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            h[2 * j] = e4m3x2_to_f16x2(uint16_t(ws[j]));
+            h[2 * j + 1] = e4m3x2_to_f16x2(uint16_t(ws[j] >> 16));
+          }
+          // dims 128 c8 + 16 u .. + 15: f16 chunk 2 c8 + u / 4, units 2 (u % 4) and + 1
+          const uint32_t c = 2 * c8 + (u >> 2), u0 = 2 * (u & 3);
+          uint8_t* drow = dst + c * (128 * 128) + r * 128;
+          *reinterpret_cast<uint4*>(drow + ((u0 ^ (r & 7)) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
+          *reinterpret_cast<uint4*>(drow + (((u0 + 1) ^ (r & 7)) << 4)) = make_uint4(h[4], h[5], h[6], h[7]);
+        }
+      }
+    }
+  }
+}
 
 struct Item {
   int32_t seq, kv_head, row0, rows;  // rows [row0, row0 + rows) of the sequence's n * group
@@ -115,7 +166,9 @@ __device__ Item locate(uint32_t target, const PrefillParams& p, uint32_t lane) {
 //               2-stage rings: a K stage is free once the S product of the
 //               tile two back is done, a V stage once that tile's PV is;
 //   warp 11     (FP8 K only) converts each E4M3 K tile, loaded into its own
-//               ring, into the f16 K tile (exact);
+//               ring, into the f16 K tile (exact); with an E4M3 V cache,
+//               warp 10 likewise converts each V tile it loaded, one tile
+//               behind its loads;
 //   warp 1      owns TMEM and issues every tcgen05.mma from one thread:
 //               S = Q K^T (M 128, N 128, K = head_dim; BF16, or f16 Q scaled
 //               by a power of two per row against the f16 K) into one of
@@ -135,12 +188,12 @@ __device__ Item locate(uint32_t target, const PrefillParams& p, uint32_t lane) {
 //               shared-memory bandwidth), and at the end O / l to the output.
 // S of tile i + 1 is computed while the softmax works on tile i.
 constexpr int kTcBM = 128, kTcBN = 128, kTcStages = 2;
-constexpr uint32_t kVWarp = 10, kConvWarp = 11;  // V producer; FP8 K converter
+constexpr uint32_t kVWarp = 10, kConvWarp = 11;  // V producer (and E4M3 V converter); FP8 K converter
 template <bool kFp8>
 constexpr int tc_threads() { return 32 * (kFp8 ? 12 : 11); }
 constexpr float kRescaleLog2 = 8.0f;  // reference-max slack of the online softmax (base 2)
 
-template <int D, bool kFp8>
+template <int D, bool kFp8, bool kFp8V = false>
 struct TcLayout {  // byte offsets from the 1024-aligned shared base
   static constexpr uint32_t kChunks = D / 64;
   static constexpr uint32_t kStage0 = 0;
@@ -150,7 +203,10 @@ struct TcLayout {  // byte offsets from the 1024-aligned shared base
   static constexpr uint32_t kK8Chunks = D / 128;
   static constexpr uint32_t kK8Bytes = kFp8 ? kK8Chunks * kTcBN * 128 : 0;
   static constexpr uint32_t kK80 = kStage0 + kTcStages * kStageBytes;
-  static constexpr uint32_t kBytes = kK80 + kTcStages * kK8Bytes;
+  // E4M3 V as loaded (same shape as the E4M3 K), one ring of stages
+  static constexpr uint32_t kV8Bytes = kFp8V ? kK8Chunks * kTcBN * 128 : 0;
+  static constexpr uint32_t kV80 = kK80 + kTcStages * kK8Bytes;
+  static constexpr uint32_t kBytes = kV80 + kTcStages * kV8Bytes;
   // TMEM columns: two S buffers [0, 128), [128, 256), each overwritten by
   // its tile's P once read (hi [+0, +64), lo [+64, +128): 128 keys, 2 per
   // column); Q [256, 256 + D / 2) (the S product's A operand, 2 dims per
@@ -161,11 +217,12 @@ struct TcLayout {  // byte offsets from the 1024-aligned shared base
   static constexpr uint32_t kSBufs = 2;
 };
 
-template <int D, bool kFp8>
+template <int D, bool kFp8, bool kFp8V>
 __global__ void __launch_bounds__(tc_threads<kFp8>(), 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                       const PrefillParams p) {
-  using Lay = TcLayout<D, kFp8>;
+  static_assert(kFp8 || !kFp8V, "an E4M3 V cache comes with an E4M3 K cache");
+  using Lay = TcLayout<D, kFp8, kFp8V>;
   constexpr uint32_t kChunks = Lay::kChunks;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -173,6 +230,7 @@ __global__ void __launch_bounds__(tc_threads<kFp8>(), 1)
   const uint32_t sbase = smem_u32(smem);
   __shared__ uint64_t k_full[kTcStages], v_full[kTcStages];
   __shared__ uint64_t k8_full[kTcStages], k8_empty[kTcStages];  // FP8 K: loaded, converted
+  __shared__ uint64_t v8_full[kTcStages];                       // FP8 V: loaded
   __shared__ float s_qamax[2][kTcBM];                           // FP8: [half][row] partial max |q|
   __shared__ uint64_t qamax_bar[4];
   __shared__ uint64_t s_full[Lay::kSBufs], p_full[Lay::kSBufs], o_full[Lay::kSBufs];  // per S/P buffer
@@ -187,9 +245,10 @@ __global__ void __launch_bounds__(tc_threads<kFp8>(), 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kTcStages; ++s) {
       mbar_init(&k_full[s], kFp8 ? 32 : 1);  // FP8: the converter warp's arrivals
-      mbar_init(&v_full[s], 1);
+      mbar_init(&v_full[s], kFp8V ? 32 : 1);  // FP8 V: warp 10's arrivals once converted
       mbar_init(&k8_full[s], 1);
       mbar_init(&k8_empty[s], 32);
+      mbar_init(&v8_full[s], 1);
     }
     for (uint32_t b = 0; b < Lay::kSBufs; ++b) {
       mbar_init(&s_full[b], 1);
@@ -237,42 +296,71 @@ __global__ void __launch_bounds__(tc_threads<kFp8>(), 1)
     // S buffer), a V stage once that tile's PV product is done (o_full): the
     // MMA thread commits nothing extra for the producers. With two S buffers
     // the same barrier completes next for tile i itself, which needs this
-    // load first, so the parity of the wait is unambiguous. FP8 K lands in a
-    // ring of its own, free once the converter warp has read it.
+    // load first, so the parity of the wait is unambiguous. FP8 K lands in
+    // a ring of its own, free once the converter warp has read it. E4M3 V
+    // lands in a ring of its own too, which warp 10 converts itself one tile
+    // behind its loads: a stage of it is free again by the time warp 10
+    // loads into it, the f16 V stage once the PV product two tiles back is
+    // done.
     const bool is_k = warp == 0;
+    const bool e4m3 = is_k ? kFp8 : kFp8V;  // this tensor's cache holds E4M3 codes
     const CUtensorMap* map = is_k ? &tmap_k : &tmap_v;
-    uint64_t* full = is_k ? (kFp8 ? k8_full : k_full) : v_full;
+    uint64_t* full = is_k ? (kFp8 ? k8_full : k_full) : (kFp8V ? v8_full : v_full);
     static_assert(kTcStages == 2, "stage reuse waits on tile i - 2");
     tma_prefetch_desc(map);
     const int32_t* table = p.block_tables + uint64_t(it.seq) * p.max_blocks_per_seq;
+    // E4M3 V tile j -> the f16 V stage the PV product reads; rows past the
+    // item's last key (not loaded, or positions past every query) as zeros
+    auto convert_v = [&](int32_t j) -> bool {
+      if constexpr (kFp8V) {
+        const uint32_t sj = uint32_t(j) % kTcStages;
+        bool good = __all_sync(0xffffffffu, mbar_wait(&v8_full[sj], uint32_t(j / kTcStages) & 1));
+        if (good && j >= kTcStages)
+          good = __all_sync(0xffffffffu, mbar_wait(&o_full[(j - kTcStages) % Lay::kSBufs],
+                                                   uint32_t((j - kTcStages) / Lay::kSBufs) & 1));
+        if (!good) return false;
+        const int32_t left = k_hi - (t_begin + j) * kTcBN;
+        e4m3_tile_to_f16<D>(smem + Lay::kV80 + sj * Lay::kV8Bytes,
+                            smem + Lay::kStage0 + sj * Lay::kStageBytes + Lay::kKBytes,
+                            left < 0 ? 0 : (left > kTcBN ? kTcBN : left), lane);
+        fence_async_smem();
+        mbar_arrive(&v_full[sj]);
+        return true;
+      } else {
+        return j < 0;  // not reached: only an E4M3 V cache converts
+      }
+    };
+    const bool self_converts = kFp8V && !is_k;
     bool ok = true;
     for (int32_t i = 0; i < T && ok; ++i) {
       const uint32_t st = uint32_t(i) % kTcStages;
       const int32_t key0 = (t_begin + i) * kTcBN + int32_t(lane) * kSub;
       const bool mine = lane < uint32_t(kTcBN / kSub) && key0 < k_hi;
       const int32_t block_id = mine ? __ldg(table + (key0 >> p.block_shift)) : 0;
-      if (lane == 0 && i >= kTcStages) {
+      if (lane == 0 && i >= kTcStages && !self_converts) {
         const int32_t j = i - kTcStages;
-        const bool freed = (is_k && kFp8) ? mbar_wait(&k8_empty[st], uint32_t(j / kTcStages) & 1)
-                                          : mbar_wait(&(is_k ? s_full : o_full)[j % Lay::kSBufs],
-                                                      uint32_t(j / Lay::kSBufs) & 1);
+        const bool freed = e4m3 ? mbar_wait(&k8_empty[st], uint32_t(j / kTcStages) & 1)
+                                : mbar_wait(&(is_k ? s_full : o_full)[j % Lay::kSBufs],
+                                            uint32_t(j / Lay::kSBufs) & 1);
         if (!freed) ok = false;
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       const uint32_t loaded = __popc(__ballot_sync(0xffffffffu, mine));
-      const uint32_t chunks = (is_k && kFp8) ? Lay::kK8Chunks : kChunks;
+      const uint32_t chunks = e4m3 ? Lay::kK8Chunks : kChunks;
       if (lane == 0) mbar_arrive_expect_tx(&full[st], loaded * chunks * (kSub * 128));
       __syncwarp();
       if (mine) {
         const int32_t slot0 = (block_id << p.block_shift) + (key0 & int32_t(p.block_size - 1));
-        uint8_t* dst = smem + ((is_k && kFp8) ? Lay::kK80 + st * Lay::kK8Bytes
-                                              : Lay::kStage0 + st * Lay::kStageBytes + (is_k ? 0u : Lay::kKBytes)) +
+        uint8_t* dst = smem + (e4m3 ? (is_k ? Lay::kK80 + st * Lay::kK8Bytes : Lay::kV80 + st * Lay::kV8Bytes)
+                                    : Lay::kStage0 + st * Lay::kStageBytes + (is_k ? 0u : Lay::kKBytes)) +
                        lane * (kSub * 128);
         for (uint32_t c = 0; c < chunks; ++c)
           tma_load_3d(dst + c * (kTcBN * 128), map, 0, slot0, it.kv_head * chunks + c, &full[st]);
       }
+      if (self_converts && i >= 1) ok = convert_v(i - 1);
     }
+    if (self_converts && ok && T > 0) ok = convert_v(T - 1);
     if (!ok && lane == 0) atomicOr(&g_prefill_error, kErrWaitTimeout);
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issue
@@ -280,7 +368,8 @@ __global__ void __launch_bounds__(tc_threads<kFp8>(), 1)
       // S: BF16 Q and K, or (FP8 cache) f16 Q scaled per row against K converted exactly to f16
       constexpr uint32_t idesc_s =
           kFp8 ? umma_idesc_f16(kTcBM, kTcBN, false) : umma_idesc_bf16(kTcBM, kTcBN, false);
-      constexpr uint32_t idesc_o = umma_idesc_bf16(kTcBM, D, true);
+      // PV: BF16 P parts x BF16 V, or (E4M3 V) f16 P parts x V converted exactly to f16
+      constexpr uint32_t idesc_o = kFp8V ? umma_idesc_f16(kTcBM, D, true) : umma_idesc_bf16(kTcBM, D, true);
       // Descriptors are built once: a k-step or a stage moves only the start
       // address field (bits 0-13, in 16-byte units), so each MMA adds a small
       // constant. One thread issues every MMA, so its instruction count per
@@ -344,12 +433,12 @@ __global__ void __launch_bounds__(tc_threads<kFp8>(), 1)
     }
     __syncwarp();
   } else if (kFp8 && warp == kConvWarp) {
-    // ------------------------------------------------------------ FP8 K -> f16
+   if constexpr (kFp8) {  // (warp 11 exists only with an E4M3 K cache)
+    // ------------------------------------------------------------ E4M3 -> f16
     // One warp turns each loaded E4M3 K tile into the f16 [chunk][key][128 B]
-    // tile the S product reads (exact: every E4M3 value is an f16 value),
-    // each lane four key rows. The f16 stage is free once the S product two
-    // tiles back is done; the E4M3 stage once the rows are read.
-    const uint32_t ct = lane;
+    // tile the S product reads. Exact: every E4M3 value is an f16 value. A
+    // f16 K stage is free once the S product two tiles back is done; an E4M3
+    // stage once its rows are read.
     bool ok = true;
     for (int32_t i = 0; i < T && ok; ++i) {
       const uint32_t st = uint32_t(i) % kTcStages;
@@ -358,34 +447,14 @@ __global__ void __launch_bounds__(tc_threads<kFp8>(), 1)
         ok = __all_sync(0xffffffffu, mbar_wait(&s_full[(i - kTcStages) % Lay::kSBufs],
                                                uint32_t((i - kTcStages) / Lay::kSBufs) & 1));
       if (!ok) break;
-      const uint8_t* src = smem + Lay::kK80 + st * Lay::kK8Bytes;
-      uint8_t* dst = smem + Lay::kStage0 + st * Lay::kStageBytes;
-      for (uint32_t r = ct; r < uint32_t(kTcBN); r += 32) {
-#pragma unroll
-        for (uint32_t c8 = 0; c8 < (kFp8 ? Lay::kK8Chunks : 1u); ++c8) {
-#pragma unroll
-          for (uint32_t u = 0; u < 8; ++u) {  // 16 dims per 16-byte unit
-            const uint4 w = *reinterpret_cast<const uint4*>(src + c8 * (kTcBN * 128) + r * 128 + ((u ^ (r & 7)) << 4));
-            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-            uint32_t h[8];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              h[2 * j] = e4m3x2_to_f16x2(uint16_t(ws[j]));
-              h[2 * j + 1] = e4m3x2_to_f16x2(uint16_t(ws[j] >> 16));
-            }
-            // dims 128 c8 + 16 u .. + 15: f16 chunk 2 c8 + u / 4, units 2 (u % 4) and + 1
-            const uint32_t c = 2 * c8 + (u >> 2), u0 = 2 * (u & 3);
-            uint8_t* drow = dst + c * (kTcBN * 128) + r * 128;
-            *reinterpret_cast<uint4*>(drow + ((u0 ^ (r & 7)) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
-            *reinterpret_cast<uint4*>(drow + (((u0 + 1) ^ (r & 7)) << 4)) = make_uint4(h[4], h[5], h[6], h[7]);
-          }
-        }
-      }
+      e4m3_tile_to_f16<D>(smem + Lay::kK80 + st * Lay::kK8Bytes, smem + Lay::kStage0 + st * Lay::kStageBytes,
+                          kTcBN, lane);
       fence_async_smem();
       mbar_arrive(&k8_empty[st]);
       mbar_arrive(&k_full[st]);
     }
     if (!ok && lane == 0) atomicOr(&g_prefill_error, kErrWaitTimeout);
+   }
   } else {
     // ------------------------------------------------------------ softmax
     // two threads per row: warps 2..5 take keys 0..31 of each tile and O
@@ -505,10 +574,14 @@ __global__ void __launch_bounds__(tc_threads<kFp8>(), 1)
       const float tile_max = xm * rs;
       const float mx = (m_run == -INFINITY || tile_max > m_run + kRescaleLog2) ? fmaxf(m_run, tile_max) : m_run;
       const float mb = mx == -INFINITY ? 0.0f : mx;  // a row with nothing attended yet stays at zero
+      // E4M3 V: the weights are formed as 2^7 P (<= 2^15), so that their f16
+      // parts stay above the f16 subnormal range down to P = 2^-21; the sum l
+      // takes the same factor
+      const float mbp = kFp8V ? mb - 7.0f : mb;
       float sum8[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
       for (int j = 0; j < kHalfKeys; ++j) {
-        x[j] = fast_exp2(fmaf(x[j], rs, -mb));
+        x[j] = fast_exp2(fmaf(x[j], rs, -mbp));
         sum8[j & 7] += x[j];
       }
       const float sum = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
@@ -540,7 +613,9 @@ __global__ void __launch_bounds__(tc_threads<kFp8>(), 1)
       // the last tile's V rows at or past k_hi were not loaded, or hold
       // positions past every query: zero them for the PV product
       const int32_t tile_base = (t_begin + i) * kTcBN;
-      if (tile_base + kTcBN > k_hi) {
+      // (E4M3 V: the converter warp zeroes those rows as it converts)
+      const bool zero_v = !kFp8V && tile_base + kTcBN > k_hi;
+      if (zero_v) {
         // V of this tile must have landed before its tail rows are zeroed
         ok = __all_sync(0xffffffffu, mbar_wait(&v_full[st], (uint32_t(i) / kTcStages) & 1));
         if (!ok) break;
@@ -555,27 +630,37 @@ __global__ void __launch_bounds__(tc_threads<kFp8>(), 1)
       }
       // this thread's keys of the P hi / lo rows, into the tile's S buffer in
       // TMEM (two keys per column; both halves of the row have read their S
-      // values before either passed the max swap). hi is the weight's top 16
-      // bits and lo the top 16 bits of the (exact) remainder: both
-      // truncations, so |P - hi - lo| < 2^-15 P
+      // values before either passed the max swap). BF16 V: hi is the
+      // weight's top 16 bits and lo the top 16 bits of the (exact) remainder,
+      // both truncations, so |P - hi - lo| < 2^-15 P. E4M3 V: f16 parts, hi
+      // the weight truncated to 11 significant bits and lo the exact
+      // remainder rounded to f16, so |P - hi - lo| <= 2^-21 P (weights in
+      // f16's subnormal range, below 2^-14, to within 2^-25)
 #pragma unroll
       for (int c = 0; c < kHalfKeys / 64; ++c) {
         uint32_t hi[32], lw[32];
 #pragma unroll
         for (int q = 0; q < 32; ++q) {
           const float x0 = x[64 * c + 2 * q], x1 = x[64 * c + 2 * q + 1];
-          const uint32_t b0 = __float_as_uint(x0), b1 = __float_as_uint(x1);
-          hi[q] = __byte_perm(b0, b1, 0x7632u);
-          const float r0 = x0 - __uint_as_float(b0 & 0xffff0000u);
-          const float r1 = x1 - __uint_as_float(b1 & 0xffff0000u);
-          lw[q] = __byte_perm(__float_as_uint(r0), __float_as_uint(r1), 0x7632u);
+          if constexpr (kFp8V) {
+            const float h0 = __uint_as_float(__float_as_uint(x0) & 0xffffe000u);
+            const float h1 = __uint_as_float(__float_as_uint(x1) & 0xffffe000u);
+            hi[q] = f32x2_to_f16x2(h0, h1);
+            lw[q] = f32x2_to_f16x2(x0 - h0, x1 - h1);
+          } else {
+            const uint32_t b0 = __float_as_uint(x0), b1 = __float_as_uint(x1);
+            hi[q] = __byte_perm(b0, b1, 0x7632u);
+            const float r0 = x0 - __uint_as_float(b0 & 0xffff0000u);
+            const float r1 = x1 - __uint_as_float(b1 & 0xffff0000u);
+            lw[q] = __byte_perm(__float_as_uint(r0), __float_as_uint(r1), 0x7632u);
+          }
         }
         const uint32_t pt = tmem + lane_addr + b * kTcBN + half * (kHalfKeys / 2) + 32 * c;
         tmem_st32(pt, hi);
         tmem_st32(pt + kTcBN / 2, lw);
       }
       tmem_wait_st();
-      if (tile_base + kTcBN > k_hi) fence_async_smem();  // the zeroed V rows, for the MMA
+      if (zero_v) fence_async_smem();  // the zeroed V rows, for the MMA
       tc_fence_before();
       mbar_arrive(&p_full[b]);
     }
@@ -590,7 +675,8 @@ __global__ void __launch_bounds__(tc_threads<kFp8>(), 1)
                         mbar_wait(&o_full[(T - 1) % Lay::kSBufs], uint32_t((T - 1) / Lay::kSBufs) & 1));
       tc_fence_after();
     }
-    const float inv = l_row > 0.0f ? 1.0f / l_row : 0.0f;
+    // (E4M3 V: the PV product summed codes; v_scale dequantises them)
+    const float inv = l_row > 0.0f ? (kFp8V ? p.out_scale : 1.0f) / l_row : 0.0f;
     float* o = valid ? p.output + (uint64_t(it.qstart + t) * p.num_q_heads + uint64_t(it.kv_head * g + hh)) * D +
                            half * kHalfD
                      : nullptr;
@@ -620,12 +706,12 @@ __global__ void __launch_bounds__(tc_threads<kFp8>(), 1)
   }
 }
 
-template <int D, bool kFp8>
+template <int D, bool kFp8, bool kFp8V>
 int launch_prefill_tc(const PrefillArgs& a, cudaStream_t stream, PrefillParams& p) {
   CUtensorMap mk, mv;
   // one 128-byte chunk per box: each box lands in its chunk's [128 keys] tile
   if (!encode_pool_map(&mk, a.k_cache, kFp8, a.num_kv_heads, D, 1, 1) ||
-      !encode_pool_map(&mv, a.v_cache, false, a.num_kv_heads, D, 1, 1))
+      !encode_pool_map(&mv, a.v_cache, kFp8V, a.num_kv_heads, D, 1, 1))
     return KV_ERR_CUDA;
   // grid: an upper bound of the item count, sum over sequences of
   // ceil(n_s * group / 128) <= num_q_tokens * group / 128 + num_seqs
@@ -635,9 +721,9 @@ int launch_prefill_tc(const PrefillArgs& a, cudaStream_t stream, PrefillParams& 
   if (grid > 0x7fffffffull) return KV_ERR_UNSUPPORTED;
   // The kernel takes all 512 TMEM columns: ask for enough shared memory that
   // no second CTA of it is resident on an SM (it would wait in tcgen05.alloc)
-  constexpr int kNeed = int(1024 + TcLayout<D, kFp8>::kBytes);
+  constexpr int kNeed = int(1024 + TcLayout<D, kFp8, kFp8V>::kBytes);
   const int smem = kNeed > 120 * 1024 ? kNeed : 120 * 1024;
-  auto kern = prefill_tc_kernel<D, kFp8>;
+  auto kern = prefill_tc_kernel<D, kFp8, kFp8V>;
   static int set_bytes[64] = {0};
   const int dev_id = device_info().device;
   if (dev_id < 0 || dev_id >= 64) return KV_ERR_CUDA;
@@ -670,11 +756,13 @@ int launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   p.q_stride = a.q_stride;
   p.sliding_window = a.sliding_window;
   p.score_scale = a.inv_sqrt_d * kLog2e * (a.fp8 ? a.k_scale : 1.0f);
-  const int key = (a.fp8 ? 100 : 0) + int(a.head_dim);
+  p.out_scale = a.fp8_v ? a.v_scale : 1.0f;
+  const int key = (a.fp8_v ? 200 : a.fp8 ? 100 : 0) + int(a.head_dim);
   switch (key) {
-    case 64: return launch_prefill_tc<64, false>(a, stream, p);  // tcgen05 / TMEM
-    case 128: return launch_prefill_tc<128, false>(a, stream, p);
-    case 228: return launch_prefill_tc<128, true>(a, stream, p);
+    case 64: return launch_prefill_tc<64, false, false>(a, stream, p);  // tcgen05 / TMEM
+    case 128: return launch_prefill_tc<128, false, false>(a, stream, p);
+    case 228: return launch_prefill_tc<128, true, false>(a, stream, p);
+    case 328: return launch_prefill_tc<128, true, true>(a, stream, p);
     default: return KV_ERR_UNSUPPORTED;
   }
 }

@@ -539,7 +539,9 @@ def _prefill_gpu(w, kc, vc, qsl, window, fp8, q_stride=None):
     args = (w.block_tables.to(DEV), w.seq_lens.to(DEV), torch.from_numpy(qsl).to(DEV), w.max_blocks_per_seq,
             w.num_seqs, n_q, w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size, w.inv_sqrt_d)
     q = w.q.to(DEV)
-    if fp8:
+    if fp8 == "kv":
+        pk.paged_prefill_attn_fp8(q, kc, vc, out, *args, w.k_scale, w.v_scale, q_stride, window)
+    elif fp8:
         pk.paged_prefill_attn_fp8k(q, kc, vc, out, *args, w.k_scale, q_stride, window)
     else:
         pk.paged_prefill_attn_bf16(q, kc, vc, out, *args, q_stride, window)
@@ -547,10 +549,12 @@ def _prefill_gpu(w, kc, vc, qsl, window, fp8, q_stride=None):
 
 
 def _prefill_ref(w, kr, vr, qsl, window, fp8):
-    return oracle.paged_prefill_attn(u16(w.q), None if fp8 else kr, kr if fp8 else None, vr,
+    kv = fp8 == "kv"
+    return oracle.paged_prefill_attn(u16(w.q), None if fp8 else kr, kr if fp8 else None, None if kv else vr,
                                      w.block_tables.numpy(), w.seq_lens.numpy(), qsl, w.max_blocks_per_seq,
                                      w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size,
-                                     w.inv_sqrt_d, w.k_scale, w.num_q_heads * w.head_dim, window)
+                                     w.inv_sqrt_d, w.k_scale, w.num_q_heads * w.head_dim, window,
+                                     v_cache_fp8=vr if kv else None, v_scale=w.v_scale)
 
 
 PREFILL_CASES = [
@@ -565,12 +569,12 @@ PREFILL_CASES = [
 ]
 
 
-@pytest.mark.parametrize("fp8", [False, True])
+@pytest.mark.parametrize("fp8", [False, True, "kv"])
 @pytest.mark.parametrize("case", range(len(PREFILL_CASES)))
 def test_prefill_cases(fp8, case):
     lens, qlens, Hq, H, D, bs, windows = PREFILL_CASES[case]
     if fp8 and D != 128:
-        pytest.skip("the FP8-K prefill supports head_dim 128")
+        pytest.skip("the FP8 prefills support head_dim 128")
     w = kvgen.custom(200 + case, seq_lens=lens, num_q_heads=Hq, num_kv_heads=H, head_dim=D, block_size=bs,
                      fp8=fp8, q_rows=max(sum(qlens), 1))
     kc, vc, kr, vr = _caches(w, fp8)
@@ -788,12 +792,16 @@ def _full_prefill_sampled(w, fp8, chunk, seqs, rows_per_seq=3):
     oracle, which runs just those queries over the same sequence (cache rows
     written by the oracle's own write into a compact host pool)."""
     H, D, bs, Hq, nb, n = w.num_kv_heads, w.head_dim, w.block_size, w.num_q_heads, w.num_blocks, w.num_tokens
+    kv = fp8 == "kv"
     slots = gpu_slots(w)
-    vc = kvgen.poisoned_pool(nb, bs, H, D, "bf16", DEV)
+    vc = kvgen.poisoned_pool(nb, bs, H, D, "fp8" if kv else "bf16", DEV)
     kc = kvgen.poisoned_pool(nb, bs, H, D, "fp8" if fp8 else "bf16", DEV)
     for t0 in range(0, n, 262144):
         t1 = min(n, t0 + 262144)
-        if fp8:
+        if kv:
+            pk.kv_write_fp8(w.key[t0:t1], w.value[t0:t1], kc, vc, slots[t0:t1], t1 - t0, H, D, bs, w.k_scale,
+                            w.v_scale, H * D, H * D)
+        elif fp8:
             pk.kv_write_fp8k(w.key[t0:t1], w.value[t0:t1], kc, vc, slots[t0:t1], t1 - t0, H, D, bs, H * D, H * D,
                              w.k_scale)
         else:
@@ -806,7 +814,9 @@ def _full_prefill_sampled(w, fp8, chunk, seqs, rows_per_seq=3):
     out = torch.full((n_q, Hq, D), float("nan"), device=DEV)
     args = (w.block_tables.to(DEV), w.seq_lens.to(DEV), torch.from_numpy(qsl).to(DEV), w.max_blocks_per_seq,
             w.num_seqs, n_q, Hq, H, D, bs, w.inv_sqrt_d)
-    if fp8:
+    if kv:
+        pk.paged_prefill_attn_fp8(q.to(DEV), kc, vc, out, *args, w.k_scale, w.v_scale, Hq * D, 0)
+    elif fp8:
         pk.paged_prefill_attn_fp8k(q.to(DEV), kc, vc, out, *args, w.k_scale, Hq * D, 0)
     else:
         pk.paged_prefill_attn_bf16(q.to(DEV), kc, vc, out, *args, Hq * D, 0)
@@ -821,19 +831,23 @@ def _full_prefill_sampled(w, fp8, chunk, seqs, rows_per_seq=3):
         nblk = -(-L // bs)
         table = np.arange(nblk, dtype=np.int32)[None]
         kr = np.full((nblk, bs, H, D), kvgen.E4M3_NAN if fp8 else kvgen.BF16_NAN, np.uint8 if fp8 else np.uint16)
-        vr = np.full((nblk, bs, H, D), kvgen.BF16_NAN, np.uint16)
+        vr = (np.full((nblk, bs, H, D), kvgen.E4M3_NAN, np.uint8) if kv
+              else np.full((nblk, bs, H, D), kvgen.BF16_NAN, np.uint16))
         sl = oracle.fill_slots(table[0], 0, L, bs)
         kk, vv = u16(w.key[starts[s]:starts[s + 1]].cpu()), u16(w.value[starts[s]:starts[s + 1]].cpu())
-        if fp8:
+        if kv:
+            oracle.write_fp8(kk, vv, kr, vr, sl, L, H, D, bs, w.k_scale, w.v_scale, H * D, H * D)
+        elif fp8:
             oracle.write_fp8k(kk, vv, kr, vr, sl, L, H, D, bs, H * D, H * D, w.k_scale)
         else:
             oracle.write_bf16(kk, vv, kr, vr, sl, L, H, D, bs, H * D, H * D)
         for j in js:
             # one query at position L - nq + j: a sequence cut to that length + 1
             qrow = np.ascontiguousarray(u16(q[qsl[s] + j][None]))
-            ref = oracle.paged_prefill_attn(qrow, None if fp8 else kr, kr if fp8 else None, vr, table,
-                                            np.array([L - nq + j + 1], np.int32), np.array([0, 1], np.int32), nblk,
-                                            1, Hq, H, D, bs, w.inv_sqrt_d, w.k_scale, Hq * D, 0)
+            ref = oracle.paged_prefill_attn(qrow, None if fp8 else kr, kr if fp8 else None, None if kv else vr,
+                                            table, np.array([L - nq + j + 1], np.int32), np.array([0, 1], np.int32),
+                                            nblk, 1, Hq, H, D, bs, w.inv_sqrt_d, w.k_scale, Hq * D, 0,
+                                            v_cache_fp8=vr if kv else None, v_scale=w.v_scale)
             assert_decode_close(got[qsl[s] + j][None], ref, f"{w.name} seq {s} query {j}")
     assert pk.kv_get_device_error() == 0
 
@@ -848,3 +862,9 @@ def test_full_fp8k_chunked_prefill_sampled():
     w = kvgen.fp8k_mixed(device=DEV)
     lens = w.seq_lens.cpu().numpy()[:32]
     _full_prefill_sampled(w, True, 256, sorted({int(lens.argmax()), int(lens.argmin()), 5}))
+
+
+def test_full_fp8_kv_chunked_prefill_sampled():
+    w = kvgen.fp8k_mixed(device=DEV)
+    lens = w.seq_lens.cpu().numpy()
+    _full_prefill_sampled(w, "kv", 256, sorted({int(lens.argmax()), int(lens.argmin()), 11, len(lens) - 1}))

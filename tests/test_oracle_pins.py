@@ -652,6 +652,42 @@ def test_prefill_chunk_split_in_two_calls_gives_the_same_rows(oracle_lib):
     assert np.array_equal(part, want)
 
 
+@pytest.mark.parametrize("window", [0, 9])
+def test_fp8_v_prefill_equals_bf16_v_prefill_of_the_dequantised_rows(oracle_lib, window):
+    # with v_scale a power of two, code * v_scale is a BF16 value: the FP8 K+V
+    # prefill must equal the FP8-K / BF16-V prefill of those rows
+    lens, qlens = [70, 33, 5], [9, 33, 2]
+    w, qsl = _prefill_case(35, lens, qlens, True)
+    w.v_scale = 2.0 ** -6
+    kc, vc = _oracle_cache_fp8(oracle_lib, w)
+    deq = oracle_lib.e4m3_to_f64(vc.ravel()) * w.v_scale
+    vbf = oracle_lib.f64_to_bf16(np.nan_to_num(deq)).reshape(vc.shape)
+    a = oracle_lib.paged_prefill_attn(_rows(w.q), None, kc, None, w.block_tables.numpy(), w.seq_lens.numpy(), qsl,
+                                      w.max_blocks_per_seq, w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim,
+                                      w.block_size, w.inv_sqrt_d, w.k_scale, w.num_q_heads * w.head_dim, window,
+                                      v_cache_fp8=vc, v_scale=w.v_scale)
+    b = _prefill(oracle_lib, w, kc, vbf, qsl, window, True)
+    assert np.array_equal(a, b)
+
+
+def test_fp8_kv_prefill_last_query_is_the_fp8_decode_of_its_row(oracle_lib):
+    lens, qlens = [37, 100, 16], [4, 9, 16]
+    w, qsl = _prefill_case(36, lens, qlens, True)
+    kc, vc = _oracle_cache_fp8(oracle_lib, w)
+    out = oracle_lib.paged_prefill_attn(_rows(w.q), None, kc, None, w.block_tables.numpy(), w.seq_lens.numpy(),
+                                        qsl, w.max_blocks_per_seq, w.num_seqs, w.num_q_heads, w.num_kv_heads,
+                                        w.head_dim, w.block_size, w.inv_sqrt_d, w.k_scale,
+                                        w.num_q_heads * w.head_dim, 0, v_cache_fp8=vc, v_scale=w.v_scale)
+    q = _rows(w.q)
+    for s in range(w.num_seqs):
+        last = np.ascontiguousarray(q[qsl[s + 1] - 1][None].repeat(w.num_seqs, 0))
+        dec = oracle_lib.paged_decode_attn_fp8(last, kc, vc, w.block_tables.numpy(), w.seq_lens.numpy(),
+                                               w.max_blocks_per_seq, w.num_seqs, w.num_q_heads, w.num_kv_heads,
+                                               w.head_dim, w.block_size, w.inv_sqrt_d, w.k_scale, w.v_scale,
+                                               w.num_q_heads * w.head_dim, 0)
+        assert np.array_equal(out[qsl[s + 1] - 1], dec[s])
+
+
 def test_prefill_queries_before_position_zero_give_zeros(oracle_lib):
     lens, qlens = [3, 10], [5, 2]                # sequence 0 has more queries than positions
     w, qsl = _prefill_case(34, lens, qlens, False)
