@@ -52,11 +52,13 @@ struct PrefillParams {
 // far as the compiler knows, so interleaving them would serialise every
 // load behind the previous unit's stores. A dead row's codes are replaced by
 // zeros as loaded (E4M3 0 is f16 0), which costs far fewer instructions than
-// selecting every converted word.
+// selecting every converted word. Not inlined and the passes not unrolled:
+// the K and V converting warps then run one short body, where two inlined,
+// unrolled copies left the kernel's warps stalled on instruction fetch.
 template <int D>
-__device__ __forceinline__ void e4m3_tile_to_f16(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst,
-                                                 int32_t live, uint32_t lane) {
-#pragma unroll
+__device__ __noinline__ void e4m3_tile_to_f16(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst,
+                                              int32_t live, uint32_t lane) {
+#pragma unroll 1
   for (uint32_t r0 = 0; r0 < 128u; r0 += 64) {
 #pragma unroll
     for (uint32_t c8 = 0; c8 < uint32_t(D / 128); ++c8) {
