@@ -161,8 +161,8 @@ __device__ Item locate(uint32_t target, const PrefillParams& p, uint32_t lane) {
 }
 
 // ---------------------------------------------------------------- the kernel
-// One CTA per (sequence, KV head, block of 128 rows), 352 threads (384 for
-// an FP8-K cache):
+// One CTA per (sequence, KV head, block of 128 rows), 352 threads (384 with
+// an E4M3 K cache):
 //   warps 0, 10 TMA producers of 128-key K and V tiles, each [chunk][key][128 B]
 //               (one box per 16-slot block run and 128-byte chunk), in two
 //               2-stage rings: a K stage is free once the S product of the
