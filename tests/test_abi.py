@@ -116,6 +116,53 @@ def test_unsupported_shapes(pk):
                                     4096, 0, None) == UNS
 
 
+def _prefill(L, kind, **kw):
+    """One prefill call of `kind` ("bf16", "fp8k", "fp8") on fake pointers;
+    every case below must fail validation before any device work."""
+    a = dict(q=FAKE, k=FAKE, v=FAKE, out=FAKE, mbps=4, ns=2, nq=10, Hq=32, H=8, D=128, bs=16, isd=0.1,
+             k_scale=1.0, v_scale=1.0, q_stride=4096, win=0)
+    a.update(kw)
+    head = (a["q"], a["k"], a["v"], a["out"], FAKE, FAKE, FAKE, a["mbps"], a["ns"], a["nq"], a["Hq"], a["H"],
+            a["D"], a["bs"], a["isd"])
+    if kind == "bf16":
+        return L.paged_prefill_attn_bf16(*head, a["q_stride"], a["win"], None)
+    if kind == "fp8k":
+        return L.paged_prefill_attn_fp8k(*head, a["k_scale"], a["q_stride"], a["win"], None)
+    return L.paged_prefill_attn_fp8(*head, a["k_scale"], a["v_scale"], a["q_stride"], a["win"], None)
+
+
+@pytest.mark.parametrize("kind", ["bf16", "fp8k", "fp8"])
+def test_prefill_zero_work_and_invalid_arguments(pk, kind):
+    L, INV = pk.lib(), pk.KV_ERR_INVALID_ARG
+    none = dict(q=None, k=None, v=None, out=None)
+    assert _prefill(L, kind, ns=0, **none) == pk.KV_OK
+    assert _prefill(L, kind, nq=0, **none) == pk.KV_OK
+    assert _prefill(L, kind, out=None) == INV and _prefill(L, kind, v=None) == INV
+    assert _prefill(L, kind, Hq=30) == INV and _prefill(L, kind, H=0) == INV
+    assert _prefill(L, kind, q_stride=100) == INV and _prefill(L, kind, isd=float("nan")) == INV
+    assert _prefill(L, kind, bs=0) == INV and _prefill(L, kind, D=0) == INV
+    if kind != "bf16":
+        for bad in (0.0, -1.0, float("inf"), float("nan")):
+            assert _prefill(L, kind, k_scale=bad) == INV
+    if kind == "fp8":
+        for bad in (0.0, -1.0, float("inf"), float("nan")):
+            assert _prefill(L, kind, v_scale=bad) == INV
+
+
+@pytest.mark.parametrize("kind", ["bf16", "fp8k", "fp8"])
+def test_prefill_unsupported_shapes(pk, kind):
+    L, UNS = pk.lib(), pk.KV_ERR_UNSUPPORTED
+    assert _prefill(L, kind, D=96, q_stride=32 * 96) == UNS
+    if kind != "bf16":
+        assert _prefill(L, kind, D=64, q_stride=32 * 64) == UNS   # the FP8 prefills take head_dim 128
+    assert _prefill(L, kind, bs=8) == UNS and _prefill(L, kind, bs=24) == UNS and _prefill(L, kind, bs=512) == UNS
+    misaligned = ctypes.c_void_p(0x10008)
+    assert _prefill(L, kind, q=misaligned) == UNS and _prefill(L, kind, out=misaligned) == UNS
+    assert _prefill(L, kind, v=misaligned) == UNS
+    assert _prefill(L, kind, q_stride=4097) == UNS                 # q rows must start on 16 bytes
+    assert _prefill(L, kind, mbps=1 << 27, bs=16) == UNS           # 2^31 positions per sequence
+
+
 def test_workspace_size_formula(pk):
     # header + num_seqs * ceil(ceil(mbps*bs/16)/16) splits * Hq * (D + 2) floats
     got = pk.kv_decode_workspace_bytes(512, 64, 32, 8, 128, 16)
