@@ -334,6 +334,7 @@ __global__ void __launch_bounds__(tc_threads<kFp8>(), 1)
     };
     const bool self_converts = kFp8V && !is_k;
     bool ok = true;
+    int32_t issued = 0;  // tiles whose loads this warp has issued
     for (int32_t i = 0; i < T && ok; ++i) {
       const uint32_t st = uint32_t(i) % kTcStages;
       const int32_t key0 = (t_begin + i) * kTcBN + int32_t(lane) * kSub;
@@ -360,10 +361,18 @@ __global__ void __launch_bounds__(tc_threads<kFp8>(), 1)
         for (uint32_t c = 0; c < chunks; ++c)
           tma_load_3d(dst + c * (kTcBN * 128), map, 0, slot0, it.kv_head * chunks + c, &full[st]);
       }
+      issued = i + 1;
       if (self_converts && i >= 1) ok = convert_v(i - 1);
     }
     if (self_converts && ok && T > 0) ok = convert_v(T - 1);
-    if (!ok && lane == 0) atomicOr(&g_prefill_error, kErrWaitTimeout);
+    if (!ok) {
+      // a wait gave up: let this warp's loads still in flight (at most the
+      // last two tiles, one per stage) land, bounded, before the CTA can
+      // exit, so no copy writes into shared memory the CTA has released
+      if (lane == 0) atomicOr(&g_prefill_error, kErrWaitTimeout);
+      for (int32_t j = issued > kTcStages ? issued - kTcStages : 0; j < issued; ++j)
+        mbar_wait(&full[uint32_t(j) % kTcStages], uint32_t(j / kTcStages) & 1);
+    }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issue
     if (lane == 0) {
