@@ -283,7 +283,8 @@ def kv_set_decode_workspace(workspace: torch.Tensor | None) -> None:
 def kv_get_device_error() -> int:
     """Synchronise the current device and return (and clear) the kernels'
     fault bits: 1 = a pipeline wait timed out, 2 = a sequence length was
-    clamped to its block table."""
+    clamped to its block table, 4 = a prefill's query_start_loc was
+    decreasing, negative or past num_q_tokens (that sequence skipped)."""
     bits = ctypes.c_uint32(0)
     _check("kv_get_device_error", lib().kv_get_device_error(ctypes.byref(bits)))
     return int(bits.value)

@@ -163,6 +163,27 @@ def test_prefill_unsupported_shapes(pk, kind):
     assert _prefill(L, kind, mbps=1 << 27, bs=16) == UNS           # 2^31 positions per sequence
 
 
+def test_readme_example_calls_match_the_binding(pk):
+    """The README's call sequence cannot run without a GPU; parse it instead
+    and bind every pk.* call to the binding's signature."""
+    import ast
+    import inspect
+    text = open(os.path.join(ROOT, "README.md")).read()
+    blocks = re.findall(r"```python\n(.*?)```", text, re.S)
+    assert blocks, "README has no python example"
+    tree = ast.parse(blocks[0])
+    calls = [n for n in ast.walk(tree) if isinstance(n, ast.Call) and isinstance(n.func, ast.Attribute)
+             and isinstance(n.func.value, ast.Name) and n.func.value.id == "pk"]
+    assert len(calls) >= 5
+    for c in calls:
+        name = c.func.attr
+        assert name in pk.__all__, name
+        sig = inspect.signature(getattr(pk, name))
+        sig.bind(*[None] * len(c.args), **{k.arg: None for k in c.keywords})
+        required = [q for q in sig.parameters.values() if q.default is inspect.Parameter.empty]
+        assert len(c.args) == len(required), f"{name}: {len(c.args)} positional, {len(required)} required"
+
+
 def test_workspace_size_formula(pk):
     # header + num_seqs * ceil(ceil(mbps*bs/16)/16) splits * Hq * (D + 2) floats
     got = pk.kv_decode_workspace_bytes(512, 64, 32, 8, 128, 16)
