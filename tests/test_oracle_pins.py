@@ -582,7 +582,8 @@ def _prefill(oracle_lib, w, kc, vc, qsl, window, fp8, seq_lens=None, q=None):
 
 def _dense_causal(w, kc, vc, qsl, s, window, fp8):
     """torch's scaled_dot_product_attention in float64 over the sequence's
-    gathered rows, with the causal window as an explicit boolean mask."""
+    gathered rows, with the causal window as an explicit boolean mask.
+    fp8: False (BF16 K and V), True (E4M3 K) or "kv" (E4M3 K and V)."""
     L = int(w.seq_lens[s])
     n = int(qsl[s + 1] - qsl[s])
     bs, H, D, Hq = w.block_size, w.num_kv_heads, w.head_dim, w.num_q_heads
@@ -592,7 +593,10 @@ def _dense_causal(w, kc, vc, qsl, s, window, fp8):
         k = torch.from_numpy(kc[blocks, p % bs]).view(torch.float8_e4m3fn).to(torch.float64) * w.k_scale
     else:
         k = torch.from_numpy(kc[blocks, p % bs].view(np.int16)).view(torch.bfloat16).to(torch.float64)
-    v = torch.from_numpy(vc[blocks, p % bs].view(np.int16)).view(torch.bfloat16).to(torch.float64)
+    if fp8 == "kv":
+        v = torch.from_numpy(vc[blocks, p % bs]).view(torch.float8_e4m3fn).to(torch.float64) * w.v_scale
+    else:
+        v = torch.from_numpy(vc[blocks, p % bs].view(np.int16)).view(torch.bfloat16).to(torch.float64)
     q = w.q[int(qsl[s]):int(qsl[s + 1])].view(n, Hq, D).permute(1, 0, 2).to(torch.float64)   # [Hq, n, D]
     g = Hq // H
     k = k.permute(1, 0, 2).repeat_interleave(g, 0)
@@ -607,13 +611,20 @@ def _dense_causal(w, kc, vc, qsl, s, window, fp8):
     return o.permute(1, 0, 2).numpy()                                                      # [n, Hq, D]
 
 
-@pytest.mark.parametrize("fp8", [False, True])
+@pytest.mark.parametrize("fp8", [False, True, "kv"])
 @pytest.mark.parametrize("window", [0, 1, 7, 50])
 def test_prefill_equals_dense_causal_attention(oracle_lib, fp8, window):
     lens, qlens = [37, 100, 1, 16, 64], [5, 37, 1, 16, 1]
     w, qsl = _prefill_case(31, lens, qlens, fp8)
-    kc, vc = _oracle_cache(oracle_lib, w, fp8)
-    out = _prefill(oracle_lib, w, kc, vc, qsl, window, fp8)
+    if fp8 == "kv":
+        kc, vc = _oracle_cache_fp8(oracle_lib, w)
+        out = oracle_lib.paged_prefill_attn(_rows(w.q), None, kc, None, w.block_tables.numpy(), w.seq_lens.numpy(),
+                                            qsl, w.max_blocks_per_seq, w.num_seqs, w.num_q_heads, w.num_kv_heads,
+                                            w.head_dim, w.block_size, w.inv_sqrt_d, w.k_scale,
+                                            w.num_q_heads * w.head_dim, window, v_cache_fp8=vc, v_scale=w.v_scale)
+    else:
+        kc, vc = _oracle_cache(oracle_lib, w, fp8)
+        out = _prefill(oracle_lib, w, kc, vc, qsl, window, fp8)
     for s in range(w.num_seqs):
         ref = _dense_causal(w, kc, vc, qsl, s, window, fp8)
         np.testing.assert_allclose(out[qsl[s]:qsl[s + 1]], ref, rtol=2.0 ** -24, atol=1e-30)
