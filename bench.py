@@ -762,13 +762,8 @@ def run_gpu(args):
             "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16/e4m3 storage, fp32 compute",
             "data": "synthetic (kvgen, seeded), inputs resident in HBM",
-            "config": {"workload": "one pass of every timed call of the five paged-KV workloads "
-                                   "(fused_write, bf16_gqa4 prefill+decode, fp8k_long prefill+decode W=0/4096, "
-                                   "fp8k_mixed decode)",
-                       "l2": f"inputs larger than L2 (the step moves {step.total_bytes / 1e9:.0f} GB; "
-                             "no call's inputs stay in L2)",
-                       "algorithmic_bytes_per_step": int(step.total_bytes),
-                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "config": bench_config(world),
+            "algorithmic_bytes_per_step": int(step.total_bytes),
             "step_mode": "one CUDA-graph replay per step (the per-sequence slot fills run as 8 parallel graph "
                          "branches, the fused K and V-only writes side by side); per-call 'parts' timed "
                          "from eager launches with CUDA events, the 196 per-sequence kv_fill_slots launches "
@@ -1026,6 +1021,17 @@ def cpu_baseline(args):
             "sample": what, "seconds": round(secs, 2)}
 
 
+def bench_config(world: int) -> dict:
+    """The workload both arms report: the GPU arm times it whole, the
+    reference arm (the oracle) a bounded sample of it, named in its
+    cpu_baseline."""
+    return {"workload": "one pass of every timed call of the five paged-KV workloads "
+                        "(fused_write, bf16_gqa4 prefill+decode, fp8k_long prefill+decode W=0/4096, "
+                        "fp8k_mixed decode)",
+            "l2": "inputs larger than L2 (129 MB): the step moves ~57 GB and no call's inputs stay in L2",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+
+
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -1042,14 +1048,14 @@ def run_reference(args):
         t_total += secs
         b_total += nbytes
     value = b_total / t_total / 1e9
-    line = {"metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    line = {"metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(t_total / args.steps * 1e3, 1), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64 compute (oracle)", "data": "synthetic (kvgen)",
             "impl": "reference",
-            "config": {"workload": "bounded sample of the five paged-KV workloads on the host cores",
-                       "parallelism": "1 CPU thread"},
+            "config": bench_config(world),
             "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                             "sample": what},
+                             "sample": f"rank 0 only, 1 CPU thread, per step: {what}"},
             "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
 
