@@ -645,8 +645,10 @@ __global__ void __launch_bounds__(tc_threads<kFp8>(), 1)
       // weight's top 16 bits and lo the top 16 bits of the (exact) remainder,
       // both truncations, so |P - hi - lo| < 2^-15 P. E4M3 V: f16 parts, hi
       // the weight truncated to 11 significant bits and lo the exact
-      // remainder rounded to f16, so |P - hi - lo| <= 2^-21 P (weights in
-      // f16's subnormal range, below 2^-14, to within 2^-25)
+      // remainder rounded to f16, so |P - hi - lo| <= max(2^-21 P, 2^-24)
+      // (the absolute term where lo or hi falls into f16's subnormals); the
+      // row's largest weight is at least 2^7, so either is far below the
+      // row sum's rounding
 #pragma unroll
       for (int c = 0; c < kHalfKeys / 64; ++c) {
         uint32_t hi[32], lw[32];
