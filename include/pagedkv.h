@@ -346,9 +346,25 @@ PAGEDKV_API int kv_set_decode_workspace(void *device_ptr, size_t bytes);
  *   bit 1: seq_lens[s] exceeded max_blocks_per_seq * block_size (clamped)
  *   bit 2: a prefill query_start_loc was decreasing, negative or past
  *          num_q_tokens (that sequence skipped)
+ *   bit 3: (bounds-checking build only) a slot or block id outside the pool
+ *          set by kv_debug_set_pool
  *   (bit 0 also covers the prefill pipeline)
  * ---------------------------------------------------------------------- */
 PAGEDKV_API int kv_get_device_error(uint32_t *bits);
+
+/* ------------------------------------------------------------------------
+ * Bounds checking (a separate build of this library, compiled with
+ * PAGEDKV_DEBUG_BOUNDS: libpagedkv_debug.so). Device data that index the
+ * pools (slot mappings, block tables) are the caller's contract and go
+ * unchecked in the product build. In the bounds-checking build every kernel
+ * checks each slot against num_blocks * block_size and each block id
+ * against num_blocks, as set here for the current device (num_blocks 0:
+ * unchecked, the initial state). A write skips a row whose slot is out of
+ * the pool; an attention call reads block 0 in place of a block id out of
+ * the pool; either sets bit 3 of the fault word. Nothing traps. The call
+ * synchronises. The product build returns KV_ERR_UNSUPPORTED.
+ * ---------------------------------------------------------------------- */
+PAGEDKV_API int kv_debug_set_pool(uint32_t num_blocks, uint32_t block_size);
 
 /* Number of decode CTAs per SM and SM count the library launches with on the
  * current device, for benchmarks (optional outputs may be NULL). */

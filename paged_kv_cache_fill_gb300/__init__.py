@@ -26,7 +26,8 @@ __all__ = [
     "paged_decode_attn_fp8k", "paged_decode_attn_fp8", "paged_prefill_attn_bf16", "paged_prefill_attn_fp8k",
     "paged_prefill_attn_fp8", "paged_decode_attn_fp8k_static_scratch",
     "kv_decode_workspace_bytes",
-    "kv_set_decode_workspace", "kv_get_device_error", "kv_device_info", "KV_OK", "KV_ERR_INVALID_ARG",
+    "kv_set_decode_workspace", "kv_get_device_error", "kv_device_info", "kv_debug_set_pool", "use_library",
+    "KV_OK", "KV_ERR_INVALID_ARG",
     "KV_ERR_UNSUPPORTED", "KV_ERR_CUDA", "KV_ERR_DEVICE",
 ]
 
@@ -75,6 +76,7 @@ _SIGNATURES = {
     "kv_set_decode_workspace": (ctypes.c_int, [_P, _SZ]),
     "kv_get_device_error": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32)]),
     "kv_device_info": (ctypes.c_int, [ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)]),
+    "kv_debug_set_pool": (ctypes.c_int, [_U32, _U32]),
 }
 
 
@@ -82,6 +84,16 @@ class PagedKVError(RuntimeError):
     def __init__(self, name: str, status: int):
         self.status = status
         super().__init__(f"{name}: status {status} ({_status_text(status)})")
+
+
+def use_library(path: str) -> None:
+    """Load the library from `path` instead of the default build, e.g. the
+    bounds-checking libpagedkv_debug.so (`_build.build(debug=True)`). Only
+    before the first call: the library in use cannot be swapped."""
+    global library_path
+    if _lib is not None:
+        raise RuntimeError(f"{library_path} is already loaded")
+    library_path = os.path.abspath(path)
 
 
 def lib() -> ctypes.CDLL:
@@ -280,11 +292,21 @@ def kv_set_decode_workspace(workspace: torch.Tensor | None) -> None:
     _workspace_keepalive[dev] = workspace
 
 
+def kv_debug_set_pool(num_blocks: int, block_size: int) -> None:
+    """Bounds-checking build only: check every slot and block id against a
+    pool of num_blocks blocks of block_size slots (0 blocks: unchecked) on
+    the current device; an index outside it sets bit 8 of
+    kv_get_device_error. Raises PagedKVError (KV_ERR_UNSUPPORTED) on the
+    product build."""
+    _check("kv_debug_set_pool", lib().kv_debug_set_pool(num_blocks, block_size))
+
+
 def kv_get_device_error() -> int:
     """Synchronise the current device and return (and clear) the kernels'
     fault bits: 1 = a pipeline wait timed out, 2 = a sequence length was
     clamped to its block table, 4 = a prefill's query_start_loc was
-    decreasing, negative or past num_q_tokens (that sequence skipped)."""
+    decreasing, negative or past num_q_tokens (that sequence skipped),
+    8 = (bounds-checking build) a slot or block id outside the pool."""
     bits = ctypes.c_uint32(0)
     _check("kv_get_device_error", lib().kv_get_device_error(ctypes.byref(bits)))
     return int(bits.value)

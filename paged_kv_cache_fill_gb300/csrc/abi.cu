@@ -388,7 +388,31 @@ int kv_get_device_error(uint32_t* bits) {
       read_and_clear_prefill_error(&prefill_bits) != cudaSuccess)
     return KV_ERR_CUDA;
   *bits = decode_bits | prefill_bits;
+#ifdef PAGEDKV_DEBUG_BOUNDS
+  uint32_t d[4] = {0, 0, 0, 0};
+  if (debug_read_and_clear_kv_write(&d[0]) != cudaSuccess || debug_read_and_clear_fused_k(&d[1]) != cudaSuccess ||
+      debug_read_and_clear_decode(&d[2]) != cudaSuccess || debug_read_and_clear_prefill(&d[3]) != cudaSuccess)
+    return KV_ERR_CUDA;
+  *bits |= d[0] | d[1] | d[2] | d[3];
+#endif
   return KV_OK;
+}
+
+int kv_debug_set_pool(uint32_t num_blocks, uint32_t block_size) {
+#ifdef PAGEDKV_DEBUG_BOUNDS
+  if (num_blocks && !block_size) return KV_ERR_INVALID_ARG;
+  if (device_info().device < 0) return KV_ERR_CUDA;
+  if (debug_set_pool_kv_write(num_blocks, block_size) != cudaSuccess ||
+      debug_set_pool_fused_k(num_blocks, block_size) != cudaSuccess ||
+      debug_set_pool_decode(num_blocks, block_size) != cudaSuccess ||
+      debug_set_pool_prefill(num_blocks, block_size) != cudaSuccess)
+    return KV_ERR_CUDA;
+  return KV_OK;
+#else
+  (void)num_blocks;
+  (void)block_size;
+  return KV_ERR_UNSUPPORTED;  // only the bounds-checking build checks indices
+#endif
 }
 
 int kv_device_info(int* num_sms, int* decode_ctas) {

@@ -15,7 +15,49 @@ enum : uint32_t {
   kErrWaitTimeout = 1u << 0,
   kErrSeqLenClamped = 1u << 1,
   kErrQueryLayout = 1u << 2,
+  kErrIndexOutOfPool = 1u << 3,  // bounds-checking build only
 };
+
+#ifdef PAGEDKV_DEBUG_BOUNDS
+// Bounds-checking build. Each translation unit holds the pool size the
+// caller set (kv_debug_set_pool; 0 blocks = unchecked) and its own fault
+// word. A slot or block id outside the pool sets kErrIndexOutOfPool there;
+// the caller of the check then skips the row (writes) or reads block 0
+// instead (attention), so no access leaves the pool and nothing traps.
+static __device__ uint32_t g_dbg_pool_blocks;
+static __device__ uint64_t g_dbg_pool_slots;
+static __device__ uint32_t g_dbg_error;
+
+__device__ __forceinline__ bool dbg_block_ok(int64_t block) {
+  const uint32_t n = g_dbg_pool_blocks;
+  if (n == 0 || (block >= 0 && block < int64_t(n))) return true;
+  atomicOr(&g_dbg_error, kErrIndexOutOfPool);
+  return false;
+}
+
+// slot >= 0 (a negative slot is padding and never reaches the check)
+__device__ __forceinline__ bool dbg_slot_ok(int64_t slot) {
+  const uint64_t n = g_dbg_pool_slots;
+  if (n == 0 || uint64_t(slot) < n) return true;
+  atomicOr(&g_dbg_error, kErrIndexOutOfPool);
+  return false;
+}
+
+// The unit's host accessors, named after the unit: debug_set_pool_<unit>
+// and debug_read_and_clear_<unit> (current device; they synchronise).
+#define PAGEDKV_DEBUG_UNIT(unit)                                                       \
+  cudaError_t debug_set_pool_##unit(uint32_t num_blocks, uint32_t block_size) {        \
+    const uint64_t slots = uint64_t(num_blocks) * block_size;                          \
+    cudaError_t e = cudaMemcpyToSymbol(g_dbg_pool_blocks, &num_blocks, sizeof(num_blocks)); \
+    return e != cudaSuccess ? e : cudaMemcpyToSymbol(g_dbg_pool_slots, &slots, sizeof(slots)); \
+  }                                                                                    \
+  cudaError_t debug_read_and_clear_##unit(uint32_t* bits) {                            \
+    cudaError_t e = cudaMemcpyFromSymbol(bits, g_dbg_error, sizeof(uint32_t));         \
+    if (e != cudaSuccess) return e;                                                    \
+    const uint32_t zero = 0;                                                           \
+    return cudaMemcpyToSymbol(g_dbg_error, &zero, sizeof(zero));                       \
+  }
+#endif
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

@@ -349,7 +349,13 @@ __global__ void __launch_bounds__(32 * 9, 1)
             const uint32_t bytes = p.k_bytes + p.v_bytes + ((flags & kFirst) ? q_bytes : 0u);
             mbar_arrive_expect_tx(&full[stage], bytes);
             uint8_t* st = smem + stage * p.stage_bytes;
+#ifdef PAGEDKV_DEBUG_BOUNDS
+            // a block id outside the pool is flagged and block 0 read instead
+            const int32_t slot0 =
+                ((dbg_block_ok(block_id) ? block_id : 0) << p.block_shift) + ((tile << 4) & int32_t(p.block_size - 1));
+#else
             const int32_t slot0 = (block_id << p.block_shift) + ((tile << 4) & int32_t(p.block_size - 1));
+#endif
             const int32_t head0 = int32_t(hg * p.heads_per_item);
             tma_load_3d(st, &tmap_k, 0, slot0, head0 * kKChunks, &full[stage]);
             tma_load_3d(st + p.k_bytes, &tmap_v, 0, slot0, head0 * kVChunks, &full[stage]);
@@ -915,5 +921,9 @@ cudaError_t read_and_clear_decode_error(uint32_t* bits) {
   if (e != cudaSuccess) return e;
   return cudaMemcpyToSymbol(g_decode_error, &zero, sizeof(uint32_t));
 }
+
+#ifdef PAGEDKV_DEBUG_BOUNDS
+PAGEDKV_DEBUG_UNIT(decode)
+#endif
 
 }  // namespace pagedkv

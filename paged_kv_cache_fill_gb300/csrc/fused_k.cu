@@ -236,6 +236,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) fused_k_norm_rope_kernel
         xa[k] = __ldcs(reinterpret_cast<const uint2*>(src + off_a));
         xb[k] = __ldcs(reinterpret_cast<const uint2*>(src + off_b));
         slot[k] = __ldg(slot_mapping + t);
+#ifdef PAGEDKV_DEBUG_BOUNDS
+        if (slot[k] >= 0 && !dbg_slot_ok(slot[k])) slot[k] = -1;  // skipped like padding
+#endif
       }
     }
     if (pass == blockIdx.x) __syncthreads();  // freq and sincos_pio32 written
@@ -374,5 +377,9 @@ cudaError_t launch_fused_k_norm_rope(const uint16_t* k_in, const uint16_t* k_nor
   }
   return cudaGetLastError();
 }
+
+#ifdef PAGEDKV_DEBUG_BOUNDS
+PAGEDKV_DEBUG_UNIT(fused_k)
+#endif
 
 }  // namespace pagedkv

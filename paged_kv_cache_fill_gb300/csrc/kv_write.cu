@@ -22,6 +22,9 @@ __global__ void __launch_bounds__(256) fill_slots_kernel(int64_t* __restrict__ s
   for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < count; i += gridDim.x * blockDim.x) {
     const uint64_t p = uint64_t(start_pos) + i;
     const int64_t block = __ldg(block_table + p / block_size);
+#ifdef PAGEDKV_DEBUG_BOUNDS
+    if (block >= 0) dbg_block_ok(block);  // flagged here; the write skips the slot it gives
+#endif
     slots[i] = block * int64_t(block_size) + int64_t(p % block_size);
   }
 }
@@ -55,6 +58,9 @@ __global__ void __launch_bounds__(256) copy_rows_kernel(const V* __restrict__ sr
   for (uint32_t t = warp; t < num_tokens; t += num_warps) {
     const int64_t slot = __ldg(slot_mapping + t);
     if (slot < 0) continue;  // padding token
+#ifdef PAGEDKV_DEBUG_BOUNDS
+    if (!dbg_slot_ok(slot)) continue;
+#endif
     const V* s0 = src0 + size_t(t) * stride0_vecs;
     const V* s1 = two ? src1 + size_t(t) * stride1_vecs : nullptr;
     V* d0 = dst0 + size_t(slot) * row_vecs;
@@ -185,6 +191,9 @@ __global__ void __launch_bounds__(256) write_fp8_kernel(
   for (uint32_t t = warp; t < num_tokens; t += num_warps) {
     const int64_t slot = __ldg(slot_mapping + t);
     if (slot < 0) continue;
+#ifdef PAGEDKV_DEBUG_BOUNDS
+    if (!dbg_slot_ok(slot)) continue;
+#endif
     const uint4* ks = key + size_t(t) * kstride_vecs;
     const uint4* vs = value + size_t(t) * vstride_vecs;
     uint2* kd = k_cache + size_t(slot) * row_vecs;
@@ -226,6 +235,9 @@ __global__ void __launch_bounds__(256) write_fp8_scalar_kernel(
   for (uint32_t t = warp; t < num_tokens; t += num_warps) {
     const int64_t slot = __ldg(slot_mapping + t);
     if (slot < 0) continue;
+#ifdef PAGEDKV_DEBUG_BOUNDS
+    if (!dbg_slot_ok(slot)) continue;
+#endif
     for (uint32_t c = lane; c < row_elems; c += 32) {
       const size_t dst = size_t(slot) * row_elems + c;
       k_cache[dst] = encode1(key[size_t(t) * key_stride + c], k_scale);
@@ -279,5 +291,9 @@ cudaError_t launch_write_fp8(const uint16_t* key, const uint16_t* value, uint8_t
                               row_elems, key_stride, value_stride, k_scale, v_scale);
   return cudaGetLastError();
 }
+
+#ifdef PAGEDKV_DEBUG_BOUNDS
+PAGEDKV_DEBUG_UNIT(kv_write)
+#endif
 
 }  // namespace pagedkv

@@ -354,7 +354,13 @@ __global__ void __launch_bounds__(tc_threads<kFp8>(), 1)
       if (lane == 0) mbar_arrive_expect_tx(&full[st], loaded * chunks * (kSub * 128));
       __syncwarp();
       if (mine) {
+#ifdef PAGEDKV_DEBUG_BOUNDS
+        // a block id outside the pool is flagged and block 0 read instead
+        const int32_t slot0 =
+            ((dbg_block_ok(block_id) ? block_id : 0) << p.block_shift) + (key0 & int32_t(p.block_size - 1));
+#else
         const int32_t slot0 = (block_id << p.block_shift) + (key0 & int32_t(p.block_size - 1));
+#endif
         uint8_t* dst = smem + (e4m3 ? (is_k ? Lay::kK80 + st * Lay::kK8Bytes : Lay::kV80 + st * Lay::kV8Bytes)
                                     : Lay::kStage0 + st * Lay::kStageBytes + (is_k ? 0u : Lay::kKBytes)) +
                        lane * (kSub * 128);
@@ -786,5 +792,9 @@ cudaError_t read_and_clear_prefill_error(uint32_t* bits) {
   if (e != cudaSuccess) return e;
   return cudaMemcpyToSymbol(g_prefill_error, &zero, sizeof(uint32_t));
 }
+
+#ifdef PAGEDKV_DEBUG_BOUNDS
+PAGEDKV_DEBUG_UNIT(prefill)
+#endif
 
 }  // namespace pagedkv

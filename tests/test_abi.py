@@ -184,6 +184,35 @@ def test_readme_example_calls_match_the_binding(pk):
         assert len(c.args) == len(required), f"{name}: {len(c.args)} positional, {len(required)} required"
 
 
+def test_product_build_has_no_bounds_checks(pk):
+    assert pk.lib().kv_debug_set_pool(16, 16) == pk.KV_ERR_UNSUPPORTED
+
+
+def test_bounds_checking_build(pk):
+    """The PAGEDKV_DEBUG_BOUNDS build compiles, exports exactly the header's
+    calls, and takes kv_debug_set_pool (checked in a child process, which
+    loads that library alone)."""
+    import subprocess
+    import sys
+    sys.path.insert(0, os.path.join(ROOT, "paged_kv_cache_fill_gb300"))
+    import _build
+    path = _build.build(debug=True)
+    out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True, text=True).stdout
+    exported = {ln.split()[-1] for ln in out.splitlines() if " T " in ln}
+    assert exported == set(declared_functions())
+    code = (
+        "import ctypes, sys\n"
+        "L = ctypes.CDLL(sys.argv[1])\n"
+        "f = L.kv_debug_set_pool\n"
+        "f.restype, f.argtypes = ctypes.c_int, [ctypes.c_uint32, ctypes.c_uint32]\n"
+        "print(f(16, 0), f(16, 16))\n")
+    r = subprocess.run([sys.executable, "-c", code, path], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stderr
+    bad_block_size, ok_or_no_device = map(int, r.stdout.split())
+    assert bad_block_size == pk.KV_ERR_INVALID_ARG
+    assert ok_or_no_device in (pk.KV_OK, pk.KV_ERR_CUDA)   # KV_OK where a GPU is present
+
+
 def test_workspace_size_formula(pk):
     # header + num_seqs * ceil(ceil(mbps*bs/16)/16) splits * Hq * (D + 2) floats
     got = pk.kv_decode_workspace_bytes(512, 64, 32, 8, 128, 16)
