@@ -295,9 +295,8 @@ def kv_set_decode_workspace(workspace: torch.Tensor | None) -> None:
 def kv_debug_set_pool(num_blocks: int, block_size: int) -> None:
     """Bounds-checking build only: check every slot and block id against a
     pool of num_blocks blocks of block_size slots (0 blocks: unchecked) on
-    the current device; an index outside it sets bit 8 of
-    kv_get_device_error. Raises PagedKVError (KV_ERR_UNSUPPORTED) on the
-    product build."""
+    the current device; an index outside it sets 8 in kv_get_device_error's
+    bits. Raises PagedKVError (KV_ERR_UNSUPPORTED) on the product build."""
     _check("kv_debug_set_pool", lib().kv_debug_set_pool(num_blocks, block_size))
 
 
