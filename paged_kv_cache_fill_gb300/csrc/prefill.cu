@@ -410,7 +410,7 @@ __global__ void __launch_bounds__(tc_threads<kFp8>(), 1)
         for (int kk = 0; kk < D / 16; ++kk) {
           // Q: 8 TMEM columns per 16 dims; K: chunk kk / 4 is kTcBN rows of 128 B further
           const uint64_t off_k = uint64_t((kk >> 2) * (kTcBN * 128) + (kk & 3) * 32) >> 4;
-          umma_bf16_tmem_a(tmem_s, tmem + Lay::kQCol + 8 * kk, kd + off_k, idesc_s, kk > 0);
+          umma_f16kind_tmem_a(tmem_s, tmem + Lay::kQCol + 8 * kk, kd + off_k, idesc_s, kk > 0);
         }
         umma_commit(&s_full[b]);
         return true;
@@ -438,8 +438,8 @@ __global__ void __launch_bounds__(tc_threads<kFp8>(), 1)
 #pragma unroll
         for (int kk = 0; kk < kTcBN / 16; ++kk) {
           const uint64_t v_k = vd + uint64_t(kk * (16 * 128) >> 4);
-          umma_bf16_tmem_a(tmem_o, pt + 8 * kk, v_k, idesc_o, i > 0 || kk > 0);
-          umma_bf16_tmem_a(tmem_o, pt + kTcBN / 2 + 8 * kk, v_k, idesc_o, true);
+          umma_f16kind_tmem_a(tmem_o, pt + 8 * kk, v_k, idesc_o, i > 0 || kk > 0);
+          umma_f16kind_tmem_a(tmem_o, pt + kTcBN / 2 + 8 * kk, v_k, idesc_o, true);
         }
         umma_commit(&o_full[pb]);
       }
