@@ -167,7 +167,7 @@ __device__ Item locate(uint32_t target, const PrefillParams& p, uint32_t lane) {
 //               (one box per 16-slot block run and 128-byte chunk), in two
 //               2-stage rings: a K stage is free once the S product of the
 //               tile two back is done, a V stage once that tile's PV is;
-//   warp 11     (FP8 K only) converts each E4M3 K tile, loaded into its own
+//   warp 11     (E4M3 K cache only) converts each E4M3 K tile, loaded into its own
 //               ring, into the f16 K tile (exact); with an E4M3 V cache,
 //               warp 10 likewise converts each V tile it loaded, one tile
 //               behind its loads;
@@ -175,8 +175,9 @@ __device__ Item locate(uint32_t target, const PrefillParams& p, uint32_t lane) {
 //               S = Q K^T (M 128, N 128, K = head_dim; BF16, or f16 Q scaled
 //               by a power of two per row against the f16 K) into one of
 //               two TMEM S buffers, Q read from tensor memory, then
-//               O += P_hi V + P_lo V (M 128, N = head_dim, K 128) into TMEM
-//               O, P from TMEM (written over its S buffer), V read as the
+//               O += P_hi V + P_lo V (M 128, N = head_dim, K 128; BF16
+//               parts, or f16 parts against the f16 V of an E4M3 V cache)
+//               into TMEM O, P from TMEM (written over its S buffer), V as the
 //               MN-major shared-memory operand (only K and V tiles are
 //               read from shared memory); this thread's issue-and-wait loop
 //               is the kernel's serial path;
@@ -630,7 +631,7 @@ __global__ void __launch_bounds__(tc_threads<kFp8>(), 1)
       // the last tile's V rows at or past k_hi were not loaded, or hold
       // positions past every query: zero them for the PV product
       const int32_t tile_base = (t_begin + i) * kTcBN;
-      // (E4M3 V: the converter warp zeroes those rows as it converts)
+      // (E4M3 V: warp 10 zeroes those rows as it converts the tile)
       const bool zero_v = !kFp8V && tile_base + kTcBN > k_hi;
       if (zero_v) {
         // V of this tile must have landed before its tail rows are zeroed
