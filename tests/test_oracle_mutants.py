@@ -44,6 +44,8 @@ MUTANTS = {
     "prefill_position_off_by_one": ("int64_t position = (int64_t)seq_lens[s] - n + j;",
                                     "int64_t position = (int64_t)seq_lens[s] - n + j + 1;"),
     "prefill_not_causal": ("max_blocks_per_seq, position + 1,", "max_blocks_per_seq, (int64_t)seq_lens[s],"),
+    "prefill_gqa_mapping": ("num_kv_heads, h / group, head_dim, block_size, inv_sqrt_d, k_scale, v_scale,",
+                            "num_kv_heads, h % num_kv_heads, head_dim, block_size, inv_sqrt_d, k_scale, v_scale,"),
     "prefill_v_with_k_scale": ("num_kv_heads, h / group, head_dim, block_size, inv_sqrt_d, k_scale, v_scale,",
                                "num_kv_heads, h / group, head_dim, block_size, inv_sqrt_d, k_scale, k_scale,"),
     "softmax_unnormalised": ("for (uint32_t d = 0; d < head_dim; ++d) out[d] = acc[d] / denom;",

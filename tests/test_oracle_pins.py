@@ -699,6 +699,49 @@ def test_fp8_kv_prefill_last_query_is_the_fp8_decode_of_its_row(oracle_lib):
         assert np.array_equal(out[qsl[s + 1] - 1], dec[s])
 
 
+def _prefill_any(oracle_lib, w, kc, vc, qsl, window, fp8, Hq, H, q, q_stride):
+    """The oracle prefill for any cache format (fp8: False, True or "kv"),
+    with the head counts and query rows given explicitly."""
+    kv = fp8 == "kv"
+    return oracle_lib.paged_prefill_attn(q, None if fp8 else kc, kc if fp8 else None, None if kv else vc,
+                                         w.block_tables.numpy(), w.seq_lens.numpy(), qsl, w.max_blocks_per_seq,
+                                         w.num_seqs, Hq, H, w.head_dim, w.block_size, w.inv_sqrt_d, w.k_scale,
+                                         q_stride, window, v_cache_fp8=vc if kv else None, v_scale=w.v_scale)
+
+
+def _cache_any(oracle_lib, w, fp8):
+    return _oracle_cache_fp8(oracle_lib, w) if fp8 == "kv" else _oracle_cache(oracle_lib, w, fp8)
+
+
+@pytest.mark.parametrize("fp8", [False, True, "kv"])
+def test_prefill_gqa_equals_mha_over_repeated_kv_heads(oracle_lib, fp8):
+    # query head h reads KV head h // g: repeating every KV head g times gives
+    # an MHA cache (Hq KV heads) on which the same queries give the same rows
+    lens, qlens = [37, 100, 16], [5, 30, 16]
+    w, qsl = _prefill_case(37, lens, qlens, fp8, Hq=8, H=2)
+    kc, vc = _cache_any(oracle_lib, w, fp8)
+    g = w.num_q_heads // w.num_kv_heads
+    q = _rows(w.q)
+    gqa = _prefill_any(oracle_lib, w, kc, vc, qsl, 9, fp8, 8, 2, q, 8 * w.head_dim)
+    kr, vr = (np.ascontiguousarray(np.repeat(c, g, axis=2)) for c in (kc, vc))
+    mha = _prefill_any(oracle_lib, w, kr, vr, qsl, 9, fp8, 8, 8, q, 8 * w.head_dim)
+    assert np.array_equal(gqa, mha)
+
+
+@pytest.mark.parametrize("fp8", [False, True, "kv"])
+def test_prefill_padded_query_rows_give_the_same_output(oracle_lib, fp8):
+    lens, qlens = [37, 100], [5, 30]
+    w, qsl = _prefill_case(38, lens, qlens, fp8)
+    kc, vc = _cache_any(oracle_lib, w, fp8)
+    q = _rows(w.q)
+    row = q.shape[1]
+    padded = np.full((q.shape[0], row + 40), 0x7FC0, np.uint16)   # NaN padding must never be read
+    padded[:, :row] = q
+    a = _prefill_any(oracle_lib, w, kc, vc, qsl, 0, fp8, w.num_q_heads, w.num_kv_heads, q, row)
+    b = _prefill_any(oracle_lib, w, kc, vc, qsl, 0, fp8, w.num_q_heads, w.num_kv_heads, padded, row + 40)
+    assert np.array_equal(a, b) and np.isfinite(a).all()
+
+
 def test_prefill_queries_before_position_zero_give_zeros(oracle_lib):
     lens, qlens = [3, 10], [5, 2]                # sequence 0 has more queries than positions
     w, qsl = _prefill_case(34, lens, qlens, False)
