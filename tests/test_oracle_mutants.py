@@ -22,6 +22,8 @@ MUTANTS = {
     "window_off_by_one": ("start = L - sliding_window;", "start = L - sliding_window + 1;"),
     "k_scale_dropped": ("return oracle_e4m3_to_f64(k_cache_fp8[idx]) * (double)k_scale;",
                         "return oracle_e4m3_to_f64(k_cache_fp8[idx]);"),
+    "e4m3_exponent_bias": ("v = ldexp(1.0 + m / 8.0, ef - 7);", "v = ldexp(1.0 + m / 8.0, ef - 8);"),
+    "e4m3_subnormal_scale": ("v = ldexp((double)m, -9);", "v = ldexp((double)m, -10);"),
     "e4m3_ties_away": ("double y = rint(ax / quantum) * quantum; /* at most 448",
                        "double y = round(ax / quantum) * quantum; /* at most 448"),
     "e4m3_no_saturation": ("if (ax >= 448.0) return (uint8_t)(sign | 0x7Eu);",
