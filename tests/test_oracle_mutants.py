@@ -50,6 +50,10 @@ MUTANTS = {
                             "num_kv_heads, h % num_kv_heads, head_dim, block_size, inv_sqrt_d, k_scale, v_scale,"),
     "prefill_v_with_k_scale": ("num_kv_heads, h / group, head_dim, block_size, inv_sqrt_d, k_scale, v_scale,",
                                "num_kv_heads, h / group, head_dim, block_size, inv_sqrt_d, k_scale, k_scale,"),
+    "score_scale_dropped": ("scores[p - start] = (double)inv_sqrt_d * dot;", "scores[p - start] = dot;"),
+    "rope_pairs_short_by_one": ("    uint32_t half = rotary_dim / 2;\n    for (uint32_t d = 0; d < head_dim; ++d) out[d] = y[d];",
+                                "    uint32_t half = rotary_dim / 2 - 1;\n    for (uint32_t d = 0; d < head_dim; ++d) out[d] = y[d];"),
+    "bf16_widen_shift": ("    uint32_t w = (uint32_t)bits << 16;", "    uint32_t w = (uint32_t)bits << 15;"),
     "softmax_unnormalised": ("for (uint32_t d = 0; d < head_dim; ++d) out[d] = acc[d] / denom;",
                              "for (uint32_t d = 0; d < head_dim; ++d) out[d] = acc[d];"),
 }
