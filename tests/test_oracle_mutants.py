@@ -30,6 +30,8 @@ MUTANTS = {
                            "if (ax >= 464.0) return 0x7Fu;"),
     "bf16_double_rounding": ("double n = rint(ax / quantum);",
                              "double n = rint((double)(float)ax / quantum);"),
+    "bf16_rows_at_packed_stride": ("value[(int64_t)t * value_stride + (int64_t)h * head_dim + d];",
+                                   "value[(int64_t)t * num_kv_heads * head_dim + (int64_t)h * head_dim + d];"),
     "slot_row": ("slots[i] = physical_block * (int64_t)block_size + (int64_t)(p % block_size);",
                  "slots[i] = physical_block * (int64_t)block_size + (int64_t)(i % block_size);"),
     "pool_head_major": ("return ((block * (int64_t)block_size + offset) * num_kv_heads + head) * (int64_t)head_dim + d;",
