@@ -1,7 +1,10 @@
-// Fused K path: RMSNorm -> RoPE -> BF16 paged write, one rounding.
+// Fused K path: RMSNorm -> RoPE -> paged write, one rounding.
 // [kv_cache.rs] `fused_k_norm_rope_cache_write_bf16`: K stays above BF16
 // precision through the norm and the rotation and is rounded once at the
-// cache write.
+// cache write. The same kernel serves the MRoPE variant
+// (`fused_k_norm_rope_cache_write_bf16_mrope`: pair i turns by the position
+// of stream i % 3) and the FP8-output variant
+// (`fused_k_norm_rope_cache_write_fp8`: E4M3 of the result times inv_scale).
 //
 // Precision design. The rotation of a pair (y_i, y_j) can cancel, so an
 // output element can be far smaller than its pair; to stay within 1 BF16 ulp
@@ -10,27 +13,33 @@
 //   - keeps u = x * w exact (BF16 x BF16 fits a binary32 significand) and
 //     applies the RMS factor r = 1/sqrt(mean(x^2) + eps) last, as a relative
 //     error only: o = r * (u_i cos - u_j sin);
-//   - carries the frequency theta^(-2i/R) as three binary32 parts (from a
-//     binary64 exp2), forms pos * freq as a sum of exact products, reduces it
-//     by pi/32 held in three parts, and evaluates sin and cos of the
-//     remainder (|r| <= pi/64) by short Taylor series in double-binary32
-//     arithmetic, combined with a table of sin/cos(m pi/32) held as (hi, lo)
-//     pairs (rope_tables.h): about 2^-44 absolute error;
+//   - reduces the angle pos * f_i modulo one turn exactly: the host passes,
+//     per rotation pair, G_i = frac(f_i / (2 pi)) as a 96-bit fixed-point
+//     fraction of a turn (f_i = theta^(-2i/R) in binary64, divided by 2 pi
+//     through the 256-bit constant 2^256 / (2 pi)), and the kernel forms
+//     pos * G_i mod 2^96 with integer multiplies, for any int32 position;
+//   - takes sin/cos of the nearest multiple of 2 pi / 2048 from a table of
+//     binary32 (hi, lo) pairs and finishes with the remainder r
+//     (|r| <= pi / 2048, converted to radians as a binary32 pair): the
+//     products with the table entries are formed exactly (FMA) and the
+//     short series of sin r and cos r - 1 enter as small corrections,
+//     largest last, for about 2^-43 absolute error;
 //   - forms u_i cos - u_j sin inside one FMA against the rounded second
 //     product, adding that product's exact error (FMA) afterwards, so the
 //     cancellation is exact and the result is accurate to ~2^-23 of itself.
-// The error-free transforms use __fmul_rn / __fadd_rn so that the compiler
+// Error-free transforms use __fmul_rn / __fadd_rn so that the compiler
 // cannot fuse them into FMAs.
 //
-// Work split: two 256-thread CTAs per SM (their phases interleave) take
-// passes of up to tokens_per_pass() tokens (all their heads); the frequency
-// ladder comes from the host with the launch. head_dim / 8 lanes per row and
-// 8 elements per lane: lane l < R/8 holds the rotation pairs (4l..4l+3,
-// R/2+4l..R/2+4l+3), the other lanes 8 pass-through elements; a thread keeps
-// up to 4 rows. Each pass
-// first issues every row load, then all threads build the pass's sin/cos
-// table in shared memory (once per token, shared by its heads) while the
-// loads are in flight, then normalises, rotates and stores every row.
+// Work split. A warp handles 256 / head_dim tokens at a time with
+// head_dim / 8 lanes per token. Lane l of a token owns unit l of every head
+// row of that token: when l < rotary_dim / 8 the rotation pairs 4l..4l+3
+// (elements 4l..4l+3 and R/2+4l..R/2+4l+3), otherwise 8 pass-through
+// elements (rotated by the identity, so that every lane runs the same code).
+// A lane therefore needs sin/cos of its own four pairs only: it computes
+// them once per token and uses them for every head, with no shared memory
+// and no barriers. Each warp walks (token group, group of kHeadsPerStep
+// heads) items and loads the next item's rows into registers before it
+// computes the current one, so loads are always in flight.
 #include <math.h>
 
 #include "internal.h"
@@ -44,138 +53,211 @@ struct Dd {
   float hi, lo;
 };
 
-__device__ __forceinline__ Dd two_sum(float a, float b) {
-  const float s = __fadd_rn(a, b);
-  const float bb = __fsub_rn(s, a);
-  const float e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
-  return {s, e};
-}
-
 // |a| >= |b| (or a == 0)
 __device__ __forceinline__ Dd fast_two_sum(float a, float b) {
   const float s = __fadd_rn(a, b);
   return {s, __fsub_rn(b, __fsub_rn(s, a))};
 }
 
-__device__ __forceinline__ Dd two_prod(float a, float b) {
-  const float p = __fmul_rn(a, b);
-  return {p, fmaf(a, b, -p)};
-}
-
-struct Freq {
-  float h, m, l;  // h + m + l = the binary64 frequency
-  float pad;
-  double d;
+// Per rotation pair i < rotary_dim / 2: frac(f_i / (2 pi)) * 2^96 as
+// {bits 0..31, 32..63, 64..95, unused}. Computed on the host per call and
+// passed by value.
+struct TurnTable {
+  uint4 g[128];
 };
 
-// theta^(-2i/R) for every rotation pair i < R/2 (R <= 256), computed on the
-// host per call (binary64 exp2/log2 are slow on this GPU) and passed by value.
-struct FreqTable {
-  Freq f[128];
-};
-
-// sin and cos of the remainder r = rh + rl (|r| <= ~pi/64), combined with
-// the table entry m: returns (sin, cos) of m*pi/32 + r as (hi, lo) pairs.
-__device__ __forceinline__ float4 sincos_from_remainder(float rh, float rl, int m, const float4* tab) {
-  // z = r^2
-  const float zh = __fmul_rn(rh, rh);
-  const float zl = fmaf(rh, rh, -zh) + 2.0f * rh * rl;
-  // sin r = r + r^3 * (-1/6 + z/120 - z^2/5040)
-  const float p = __fmul_rn(rh, zh);
-  const float pe = fmaf(rh, zh, -p) + (rh * zl + rl * zh);
-  const float c6h = -1.0f / 6.0f;
-  const float c6l = float(-1.0 / 6.0 - double(-1.0f / 6.0f));  // folded at compile time
-  const float poly = c6l + zh * (1.0f / 120.0f - zh * (1.0f / 5040.0f));
-  const Dd m1 = two_prod(p, c6h);
-  const float corr = m1.lo + (pe * c6h + p * poly);
-  Dd sr = fast_two_sum(rh, m1.hi);
-  sr.lo = sr.lo + (rl + corr);
-  // cos r = 1 + d, d = -z/2 + z^2/24 - z^3/720
-  const float dh = -0.5f * zh;
-  const float dl = -0.5f * zl + (zh * zh) * (1.0f / 24.0f - zh * (1.0f / 720.0f));
-  const float4 t = tab[m & 63];  // {sin_hi, sin_lo, cos_hi, cos_lo} of m*pi/32
-  // X + X*d + sign * Y*sin r
-  auto combine = [&](float xh, float xl, float yh, float yl, float sign) -> Dd {
-    const Dd t1 = two_prod(xh, dh);
-    const float t1l = t1.lo + (xh * dl + xl * dh);
-    const Dd t2 = two_prod(yh, sr.hi);
-    const float t2h = sign * t2.hi;
-    const float t2l = sign * (t2.lo + (yh * sr.lo + yl * sr.hi));
-    Dd x = two_sum(xh, t2h);
-    const Dd x2 = two_sum(x.hi, t1.hi);
-    const float lo = ((xl + x.lo) + (x2.lo + t1l)) + t2l;
-    return fast_two_sum(x2.hi, lo);
-  };
-  const Dd s = combine(t.x, t.y, t.z, t.w, 1.0f);
-  const Dd c = combine(t.z, t.w, t.x, t.y, -1.0f);
+// sin and cos, as (hi, lo) pairs {sin_hi, sin_lo, cos_hi, cos_lo}, of the
+// angle whose fraction of a turn is pos * G mod 1 (G in units of 2^-96 turn).
+__device__ __forceinline__ float4 turn_sincos(int32_t pos, uint4 g) {
+  // bits 32..95 of pos * G mod 2^96 (bits 0..31 are below the precision kept)
+  const uint32_t pu = uint32_t(pos);
+  const uint64_t mid = uint64_t(pu) * g.y + __umulhi(pu, g.x);
+  uint64_t w = ((uint64_t(uint32_t(mid >> 32) + pu * g.z)) << 32) | uint32_t(mid);
+  // a negative position was multiplied as pos + 2^32: take 2^32 * G back off
+  const uint64_t neg = uint64_t(int64_t(pos >> 31));
+  w -= ((uint64_t(g.y) << 32) | g.x) & neg;
+  const uint32_t w2 = uint32_t(w >> 32), w1 = uint32_t(w);
+  // nearest multiple m of 1/2048 turn, and the remainder
+  // (u - 2^20 + w1 / 2^32) * 2^-32 turn with |u - 2^20| <= 2^20
+  constexpr int kShift = 32 - kTurnTableBits;
+  const uint32_t wr = w2 + (1u << (kShift - 1));
+  const uint32_t m = wr >> kShift;
+  const uint32_t u = wr & ((1u << kShift) - 1);
+  // integers below 2^23 convert exactly through the 2^23 exponent pattern
+  const float th = __fsub_rn(__uint_as_float(0x4B000000u | u), float(8388608 + (1 << (kShift - 1))));
+  const float tl = __fmul_rn(__fsub_rn(__uint_as_float(0x4B000000u | (w1 >> 9)), 8388608.0f), 0x1p-23f);
+  // r = (th + tl) * 2 pi / 2^32 as rh + rl
+  const float rh = __fmul_rn(th, kTwoPiOver2p32Hi);
+  const float rl = fmaf(th, kTwoPiOver2p32Lo, fmaf(tl, kTwoPiOver2p32Hi, fmaf(th, kTwoPiOver2p32Hi, -rh)));
+  // {sin_hi, sin_lo, cos_hi, cos_lo} of 2 pi m / 2048
+  const float4 T = __ldg(reinterpret_cast<const float4*>(kSinCosTurn) + m);
+  // cos r = 1 + dh + dl (dh = -rh^2 / 2 exactly), sin r = rh + t
+  const float r2 = __fmul_rn(rh, rh);
+  const float r2e = fmaf(rh, rh, -r2);
+  const float dh = __fmul_rn(-0.5f, r2);
+  const float dl = fmaf(r2, __fmul_rn(r2, 1.0f / 24.0f), fmaf(-rh, rl, __fmul_rn(-0.5f, r2e)));
+  const float t = fmaf(__fmul_rn(rh, r2), -1.0f / 6.0f, rl);
+  // sin(A + r) = sin A (1 + d) + cos A (rh + t); |sin A| >= sin(2 pi / 2048)
+  // or sin A == 0, and |cos A * rh| <= pi / 2048, so fast_two_sum applies
+  const float p = __fmul_rn(T.z, rh);
+  Dd s = fast_two_sum(T.x, p);
+  float lo = fmaf(T.w, rh, fmaf(T.z, rh, -p));
+  lo = fmaf(T.x, dl, lo);
+  lo = __fadd_rn(__fadd_rn(lo, T.y), s.lo);
+  lo = fmaf(T.z, t, lo);
+  lo = fmaf(T.x, dh, lo);
+  s = fast_two_sum(s.hi, lo);
+  // cos(A + r) = cos A (1 + d) - sin A (rh + t)
+  const float q = __fmul_rn(T.x, rh);
+  Dd c = fast_two_sum(T.z, -q);
+  lo = fmaf(-T.y, rh, -fmaf(T.x, rh, -q));
+  lo = fmaf(T.z, dl, lo);
+  lo = __fadd_rn(__fadd_rn(lo, T.w), c.lo);
+  lo = fmaf(-T.x, t, lo);
+  lo = fmaf(T.z, dh, lo);
+  c = fast_two_sum(c.hi, lo);
   return make_float4(s.hi, s.lo, c.hi, c.lo);
 }
 
-// sin and cos of pos * freq as (hi, lo) pairs.
-__device__ __forceinline__ float4 rope_sincos(int32_t pos, const Freq& f, const float4* tab) {
-  if (pos > -65536 && pos < 65536) {
-    const float pf = float(pos);  // exact
-    const Dd a1 = two_prod(pf, f.h);
-    const Dd a2 = two_prod(pf, f.m);
-    const float a3 = __fmul_rn(pf, f.l);
-    const float k = rintf(__fmul_rn(a1.hi, k32OverPi));
-    const Dd q1 = two_prod(k, kPio32P1);
-    const Dd q2 = two_prod(k, kPio32P2);
-    const float q3 = __fmul_rn(k, kPio32P3);
-    float x = __fsub_rn(a1.hi, q1.hi);  // exact (Sterbenz)
-    Dd s1 = two_sum(x, a1.lo);
-    Dd s2 = two_sum(s1.hi, a2.hi);
-    Dd s3 = two_sum(s2.hi, -q1.lo);
-    Dd s4 = two_sum(s3.hi, -q2.hi);
-    const float lo = ((s1.lo + s2.lo) + (s3.lo + s4.lo)) + ((a2.lo + a3) - (q2.lo + q3));
-    const Dd r = fast_two_sum(s4.hi, lo);
-    return sincos_from_remainder(r.hi, r.lo, int(k), tab);
-  }
-  // Large positions: reduce in binary64.
-  const double a = double(pos) * f.d;
-  const double k = rint(a * (32.0 / 3.14159265358979323846));
-  double r = fma(-k, kPio32D1, a);
-  r = fma(-k, kPio32D2, r);
-  const float rh = float(r);
-  const float rl = float(r - double(rh));
-  const long long km = (long long)k;
-  return sincos_from_remainder(rh, rl, int(km & 63), tab);
+// Two binary32 values in one 64-bit register pair (the first in the low
+// half), operated on element-wise by the packed f32x2 instructions: one
+// issue slot for two elements.
+using F2 = unsigned long long;
+
+__device__ __forceinline__ F2 f2_make(float lo, float hi) {
+  F2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float2 f2_split(F2 v) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+  return r;
+}
+__device__ __forceinline__ F2 f2_mul(F2 a, F2 b) {
+  F2 d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ F2 f2_fma(F2 a, F2 b, F2 c) {
+  F2 d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ F2 f2_add(F2 a, F2 b) {
+  F2 d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ F2 f2_sub(F2 a, F2 b) {
+  F2 d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
 }
 
-// u_a * c + sign * u_b * s with c = (ch, cl), s = (sh, sl), accurate to about
-// 2^-23 of the result even when the two products cancel: p2 = RN(u_b * sh)
-// with its exact error e2 (FMA); u_a * ch - p2 is formed exactly inside one
-// FMA and rounded once; the small terms are added last.
-__device__ __forceinline__ float rotate(float ua, float ub, float ch, float cl, float sh, float sl,
-                                        float sign) {
+// The low (kHi false) or high BF16 halves of a and b multiplied exactly and
+// added to c with one rounding (mixed-precision FMA: no unpacking to binary32).
+template <bool kHi>
+__device__ __forceinline__ float fma_bf16(uint32_t a, uint32_t b, float c) {
+  float d;
+  if (kHi)
+    asm("{\n\t.reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
+        "fma.rn.f32.bf16 %0, ah, bh, %3;\n\t}"
+        : "=f"(d) : "r"(a), "r"(b), "f"(c));
+  else
+    asm("{\n\t.reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
+        "fma.rn.f32.bf16 %0, al, bl, %3;\n\t}"
+        : "=f"(d) : "r"(a), "r"(b), "f"(c));
+  return d;
+}
+
+// Sum of the squares of the 8 BF16 values in (a, b); each square is exact.
+__device__ __forceinline__ float sum_sq8(uint2 a, uint2 b) {
+  float s0 = fma_bf16<false>(a.x, a.x, 0.0f), s1 = fma_bf16<true>(a.x, a.x, 0.0f);
+  s0 = fma_bf16<false>(a.y, a.y, s0);
+  s1 = fma_bf16<true>(a.y, a.y, s1);
+  s0 = fma_bf16<false>(b.x, b.x, s0);
+  s1 = fma_bf16<true>(b.x, b.x, s1);
+  s0 = fma_bf16<false>(b.y, b.y, s0);
+  s1 = fma_bf16<true>(b.y, b.y, s1);
+  return __fadd_rn(s0, s1);
+}
+
+// x * w for a pair of BF16 values (the word's halves): exact in binary32.
+__device__ __forceinline__ F2 mul_bf16x2(uint32_t x, uint32_t w) {
+  return f2_make(fma_bf16<false>(x, w, -0.0f), fma_bf16<true>(x, w, -0.0f));
+}
+
+#ifndef FUSED_K_PACKED_ROTATE
+#define FUSED_K_PACKED_ROTATE 1
+#endif
+
+// Sine and cosine of two rotation pairs, each as a (hi, lo) binary32 pair,
+// packed pair by pair for the f32x2 rotation.
+struct PairSinCos {
+  F2 ch, cl, sh, nsh, sl;
+};
+
+// The rotation of two pairs at once: X holds their first elements, Y their
+// partners (rotary_dim / 2 further on). out_x = X cos - Y sin and
+// out_y = Y cos + X sin, each accurate to about 2^-23 of itself even when the
+// two products cancel: the product that is subtracted is rounded once and its
+// exact error (FMA against the negated sine) is added back with the low
+// parts of sin and cos, after the main difference has been formed exactly
+// inside one FMA and rounded once.
+__device__ __forceinline__ void rotate2(F2 X, F2 Y, const PairSinCos& c, F2& out_x, F2& out_y) {
+  const F2 nq = f2_mul(Y, c.nsh);             // -RN(Y sh)
+  const F2 e = f2_fma(Y, c.sh, nq);           // Y sh - RN(Y sh), exact
+  const F2 tx = f2_fma(X, c.ch, nq);          // X ch - RN(Y sh), one rounding
+  const F2 sx = f2_sub(f2_mul(X, c.cl), f2_mul(Y, c.sl));
+  out_x = f2_add(tx, f2_sub(sx, e));
+  const F2 q = f2_mul(X, c.sh);               // RN(X sh)
+  const F2 ne = f2_fma(X, c.nsh, q);          // RN(X sh) - X sh, exact
+  const F2 ty = f2_fma(Y, c.ch, q);           // Y ch + RN(X sh), one rounding
+  const F2 sy = f2_fma(Y, c.cl, f2_mul(X, c.sl));
+  out_y = f2_add(ty, f2_sub(sy, ne));
+}
+
+// The same two rotations one element at a time (scalar FMAs take the
+// negations as free operand modifiers: 6 FMA-pipe operations per output
+// against 7 packed).
+__device__ __forceinline__ float rotate1(float ua, float ub, float ch, float cl, float sh, float sl, float sign) {
   const float p2 = __fmul_rn(ub, sh);
   const float e2 = fmaf(ub, sh, -p2);
-  const float t0 = fmaf(ua, ch, sign * p2);  // ua*ch + sign*p2, one rounding
-  return t0 + (sign * e2 + (ua * cl + sign * (ub * sl)));
+  const float t0 = fmaf(ua, ch, sign * p2);  // ua ch + sign p2, one rounding
+  return __fadd_rn(t0, fmaf(sign * ub, sl, fmaf(ua, cl, sign * e2)));
 }
 
-__device__ __forceinline__ void unpack8(const uint32_t (&w)[4], float (&x)[8]) {
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    x[2 * j] = bf16_lo_to_f32(w[j]);
-    x[2 * j + 1] = bf16_hi_to_f32(w[j]);
-  }
+__device__ __forceinline__ void rotate2_scalar(F2 X, F2 Y, const PairSinCos& c, F2& out_x, F2& out_y) {
+  const float2 x = f2_split(X), y = f2_split(Y), ch = f2_split(c.ch), cl = f2_split(c.cl), sh = f2_split(c.sh),
+               sl = f2_split(c.sl);
+  out_x = f2_make(rotate1(x.x, y.x, ch.x, cl.x, sh.x, sl.x, -1.0f), rotate1(x.y, y.y, ch.y, cl.y, sh.y, sl.y, -1.0f));
+  out_y = f2_make(rotate1(y.x, x.x, ch.x, cl.x, sh.x, sl.x, 1.0f), rotate1(y.y, x.y, ch.y, cl.y, sh.y, sl.y, 1.0f));
 }
 
-constexpr int kThreads = 256;
-constexpr int kCtasPerSm = 2;  // two CTAs per SM interleave their load / table / row phases
-constexpr int kMaxRowsPerThread = 4;
-constexpr int kTableEntries = 2048;  // sin/cos entries per pass: tokens x rotary_dim/2
+#ifndef FUSED_K_THREADS
+#define FUSED_K_THREADS 256
+#endif
+#ifndef FUSED_K_CTAS
+#define FUSED_K_CTAS 2
+#endif
+#ifndef FUSED_K_HEADS
+#define FUSED_K_HEADS 4
+#endif
+constexpr int kThreads = FUSED_K_THREADS;
+constexpr int kWarps = kThreads / 32;
+constexpr int kCtasPerSm = FUSED_K_CTAS;
+constexpr int kHeadsPerStep = FUSED_K_HEADS;  // head rows a lane holds per item
 
-// Tokens per pass for a head_dim/rotary/heads shape: bounded by the table and
-// by 16 rows per thread.
-__host__ __device__ inline uint32_t tokens_per_pass(uint32_t head_dim, uint32_t rotary_dim, uint32_t num_kv_heads) {
-  const uint32_t rows_per_pass = (kThreads / (head_dim / 8)) * kMaxRowsPerThread;
-  uint32_t t = kTableEntries / (rotary_dim / 2);
-  const uint32_t by_rows = rows_per_pass / num_kv_heads;
-  if (by_rows < t) t = by_rows;
-  return t < 1 ? 1 : t;
-}
+// One item's inputs for this lane: its unit of kHeadsPerStep head rows of one
+// token, the token's slot and (on the token's first item) its positions.
+struct Item {
+  uint2 xa[kHeadsPerStep], xb[kHeadsPerStep];
+  int64_t slot;
+  int32_t pos[3];
+  uint32_t t, hg;
+  bool valid;
+};
 
 // kFp8Out: store E4M3(o * inv_scale) (saturating, RNE) instead of BF16(o).
 // kMrope: pair i takes its position from positions / pos_h / pos_w by i % 3.
@@ -185,136 +267,210 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) fused_k_norm_rope_kernel
     const int32_t* __restrict__ positions, const int32_t* __restrict__ pos_h,
     const int32_t* __restrict__ pos_w, void* __restrict__ k_cache,
     const int64_t* __restrict__ slot_mapping, uint32_t num_tokens, uint32_t num_kv_heads,
-    uint32_t rotary_dim, float rms_eps, const __grid_constant__ FreqTable ft, float inv_scale, uint32_t tok_pass) {
-  constexpr int kLanes = D / 8;              // lanes per row
-  constexpr int kRows = kThreads / kLanes;   // rows per sweep of the CTA
-  __shared__ Freq freq[128];
-  __shared__ float4 table[kTableEntries];
-  __shared__ float4 sincos_pio32[64];  // lanes index it by position: shared, not constant, memory
-  if (threadIdx.x < 64) sincos_pio32[threadIdx.x] = kSinCosPio32[threadIdx.x];
-
+    uint32_t rotary_dim, float rms_eps, const __grid_constant__ TurnTable tt, float inv_scale) {
+  constexpr uint32_t kLanes = D / 8;        // lanes per token
+  constexpr uint32_t kTokens = 32 / kLanes;  // tokens per warp step
+  const uint32_t lane = threadIdx.x & 31;
+  const uint32_t sub = lane / kLanes;        // token of the step
+  const uint32_t l = lane % kLanes;          // unit of the row
   const uint32_t half = rotary_dim / 2;
-  if (threadIdx.x < half) freq[threadIdx.x] = ft.f[threadIdx.x];  // visible after the pass's first barrier
+  const bool is_pair = l < rotary_dim / 8;
+  // element offsets of this lane's two groups of four
+  const uint32_t off_a = is_pair ? 4 * l : rotary_dim + 8 * (l - rotary_dim / 8);
+  const uint32_t off_b = is_pair ? half + 4 * l : off_a + 4;
+  const uint32_t head_groups = (num_kv_heads + kHeadsPerStep - 1) / kHeadsPerStep;
 
-  const uint32_t lane = threadIdx.x % kLanes;
-  const uint32_t row_in_sweep = threadIdx.x / kLanes;
-  const uint32_t pair_lanes = rotary_dim / 8;
-  const bool is_pair = lane < pair_lanes;
-  // element offsets of this lane's two groups of four (pair lanes) or one
-  // group of eight (pass-through lanes)
-  const uint32_t off_a = is_pair ? 4 * lane : rotary_dim + 8 * (lane - pair_lanes);
-  const uint32_t off_b = is_pair ? half + 4 * lane : off_a + 4;
+  // work of this warp: token steps gw, gw + W, ..., each in head_groups items
+  const uint32_t warps_total = gridDim.x * kWarps;
+  const uint32_t gw = blockIdx.x * kWarps + threadIdx.x / 32;
+  const uint32_t steps_total = (num_tokens + kTokens - 1) / kTokens;
+  const uint32_t my_steps = gw < steps_total ? (steps_total - gw + warps_total - 1) / warps_total : 0;
+  const uint32_t n_items = my_steps * head_groups;
 
-  float w[8];
-  {
-    const uint2 wa = *reinterpret_cast<const uint2*>(k_norm_weight + off_a);
-    const uint2 wb = *reinterpret_cast<const uint2*>(k_norm_weight + off_b);
-    const uint32_t ww[4] = {wa.x, wa.y, wb.x, wb.y};
-    unpack8(ww, w);
+  auto load_item = [&](uint32_t k, Item& it) {
+    const uint32_t step = gw + (k / head_groups) * warps_total;
+    it.hg = k % head_groups;
+    it.t = step * kTokens + sub;
+    it.valid = it.t < num_tokens;
+    it.slot = -1;
+#pragma unroll
+    for (int j = 0; j < kHeadsPerStep; ++j) it.xa[j] = it.xb[j] = make_uint2(0, 0);
+    if (!it.valid) return;
+    it.slot = __ldg(slot_mapping + it.t);
+    if (it.hg == 0) {
+      it.pos[0] = __ldg(positions + it.t);
+      if (kMrope) {
+        it.pos[1] = __ldg(pos_h + it.t);
+        it.pos[2] = __ldg(pos_w + it.t);
+      }
+    }
+    const uint16_t* src = k_in + (uint64_t(it.t) * num_kv_heads + it.hg * kHeadsPerStep) * D;
+#pragma unroll
+    for (int j = 0; j < kHeadsPerStep; ++j) {
+      if (it.hg * kHeadsPerStep + j < num_kv_heads) {
+        it.xa[j] = __ldcs(reinterpret_cast<const uint2*>(src + j * D + off_a));
+        it.xb[j] = __ldcs(reinterpret_cast<const uint2*>(src + j * D + off_b));
+      }
+    }
+  };
+
+  Item A, B;
+  if (n_items > 0) load_item(0, A);  // the first rows are on their way before the set-up below
+
+  __shared__ uint4 s_turn[128];  // turn fractions of the rotation pairs
+  for (uint32_t i = threadIdx.x; i < half; i += kThreads) s_turn[i] = tt.g[i];
+  // the norm weights of this lane's unit, as BF16 pairs
+  const uint2 wa = *reinterpret_cast<const uint2*>(k_norm_weight + off_a);
+  const uint2 wb = *reinterpret_cast<const uint2*>(k_norm_weight + off_b);
+  // sin/cos of this lane's pairs (4l, 4l+1) and (4l+2, 4l+3) for the current
+  // token; the identity for pass-through lanes
+  PairSinCos sc[2];
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    sc[k].ch = f2_make(1.0f, 1.0f);
+    sc[k].cl = sc[k].sh = sc[k].nsh = sc[k].sl = f2_make(0.0f, 0.0f);
   }
+  __syncthreads();  // s_turn written; no barrier follows
+  if (n_items == 0) return;
 
-  const uint32_t passes = (num_tokens + tok_pass - 1) / tok_pass;
-  for (uint32_t pass = blockIdx.x; pass < passes; pass += gridDim.x) {
-    const uint32_t t0 = pass * tok_pass;
-    const uint32_t ntok = num_tokens - t0 < tok_pass ? num_tokens - t0 : tok_pass;
-    const uint32_t nrows = ntok * num_kv_heads;
-
-    // 1. every load of the pass first: this thread's rows and their slots
-    uint2 xa[kMaxRowsPerThread], xb[kMaxRowsPerThread];
-    int64_t slot[kMaxRowsPerThread];
-    uint32_t tok_of[kMaxRowsPerThread], head_of[kMaxRowsPerThread];  // token in the pass, head
+  auto process = [&](const Item& it) {
+    if (it.hg == 0 && it.valid && is_pair) {
+      float4 v[4];
 #pragma unroll
-    for (int k = 0; k < kMaxRowsPerThread; ++k) {
-      const uint32_t row = row_in_sweep + k * kRows;
-      xa[k] = xb[k] = make_uint2(0, 0);
-      slot[k] = -1;
-      tok_of[k] = row / num_kv_heads;
-      head_of[k] = row - tok_of[k] * num_kv_heads;
-      if (row < nrows) {
-        const uint32_t t = t0 + tok_of[k], h = head_of[k];
-        const uint16_t* src = k_in + (uint64_t(t) * num_kv_heads + h) * D;
-        xa[k] = __ldcs(reinterpret_cast<const uint2*>(src + off_a));
-        xb[k] = __ldcs(reinterpret_cast<const uint2*>(src + off_b));
-        slot[k] = __ldg(slot_mapping + t);
+      for (int q = 0; q < 4; ++q) {
+        int32_t pos = it.pos[0];
+        if (kMrope) {
+          const uint32_t stream = (4 * l + q) % 3;
+          pos = stream == 0 ? it.pos[0] : (stream == 1 ? it.pos[1] : it.pos[2]);
+        }
+        v[q] = turn_sincos(pos, s_turn[4 * l + q]);  // {sin_hi, sin_lo, cos_hi, cos_lo}
+      }
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const float4 a0 = v[2 * k], a1 = v[2 * k + 1];
+        sc[k].ch = f2_make(a0.z, a1.z);
+        sc[k].cl = f2_make(a0.w, a1.w);
+        sc[k].sh = f2_make(a0.x, a1.x);
+        sc[k].nsh = f2_make(-a0.x, -a1.x);
+        sc[k].sl = f2_make(a0.y, a1.y);
+      }
+    }
+    int64_t slot = it.slot;
 #ifdef PAGEDKV_DEBUG_BOUNDS
-        if (slot[k] >= 0 && !dbg_slot_ok(slot[k])) slot[k] = -1;  // skipped like padding
+    if (it.valid && slot >= 0 && !dbg_slot_ok(slot)) slot = -1;  // skipped like padding
 #endif
-      }
+    // sums of squares of every row first, then their reductions over the
+    // token's lanes side by side, so that the shuffles do not wait on each
+    // other (rows past the last head are zeros and are not stored)
+    float ss[kHeadsPerStep];
+#pragma unroll
+    for (int j = 0; j < kHeadsPerStep; ++j) ss[j] = sum_sq8(it.xa[j], it.xb[j]);  // x^2 exact in binary32
+#pragma unroll
+    for (uint32_t o = kLanes / 2; o > 0; o >>= 1) {
+#pragma unroll
+      for (int j = 0; j < kHeadsPerStep; ++j) ss[j] += __shfl_xor_sync(0xffffffffu, ss[j], o);
     }
-    if (pass == blockIdx.x) __syncthreads();  // freq and sincos_pio32 written
-    // 2. sin/cos of every (token of the pass, frequency), by all threads.
-    // Pair i = 4 l + q (lane l, group q) sits at [token][q][l], so the 16
-    // lanes of a row read 16 consecutive entries (no bank conflicts).
-    const uint32_t quarter = half >> 2;  // rotary_dim is a multiple of 8
-    for (uint32_t e = threadIdx.x; e < ntok * half; e += kThreads) {
-      const uint32_t j = e / half, i = e % half;
-      const int32_t* pos_src = positions;
-      if (kMrope) pos_src = (i % 3 == 0) ? positions : (i % 3 == 1 ? pos_h : pos_w);
-      table[j * half + (i & 3) * quarter + (i >> 2)] = rope_sincos(__ldg(pos_src + t0 + j), freq[i], sincos_pio32);
-    }
-    __syncthreads();
-
-    // 3. normalise, rotate, round once and store every row
 #pragma unroll
-    for (int k = 0; k < kMaxRowsPerThread; ++k) {
-      const uint32_t row = row_in_sweep + k * kRows;
-      if (k * kRows >= nrows) break;  // uniform across the CTA
-      const bool active = row < nrows;
-      float x[8];
-      {
-        const uint32_t xw[4] = {xa[k].x, xa[k].y, xb[k].x, xb[k].y};
-        unpack8(xw, x);
-      }
-      float ss = 0.0f;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) ss = fmaf(x[j], x[j], ss);  // x^2 is exact in binary32
-#pragma unroll
-      for (int o = kLanes / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    for (int j = 0; j < kHeadsPerStep; ++j) {
+      const uint32_t h = it.hg * kHeadsPerStep + j;
+      if (!it.valid || slot < 0 || h >= num_kv_heads) continue;
       // 1/sqrt(mean + eps): a few-ulp binary32 factor, a relative error on the
       // whole row far below half a BF16 ulp
-      const float r = rsqrtf(__fadd_rn(ss * (1.0f / float(D)), rms_eps));
-      float u[8];
+      const float r = rsqrtf(__fadd_rn(ss[j] * (1.0f / float(D)), rms_eps));
+      // u = x * w (exact); X: elements 0..3 of the unit, Y: their partners 4..7
+      const F2 x01 = mul_bf16x2(it.xa[j].x, wa.x), x23 = mul_bf16x2(it.xa[j].y, wa.y);
+      const F2 y01 = mul_bf16x2(it.xb[j].x, wb.x), y23 = mul_bf16x2(it.xb[j].y, wb.y);
+      F2 o[4];  // elements (0,1), (2,3), (4,5), (6,7)
+#if FUSED_K_PACKED_ROTATE
+      rotate2(x01, y01, sc[0], o[0], o[2]);
+      rotate2(x23, y23, sc[1], o[1], o[3]);
+#else
+      rotate2_scalar(x01, y01, sc[0], o[0], o[2]);
+      rotate2_scalar(x23, y23, sc[1], o[1], o[3]);
+#endif
+      if constexpr (kFp8Out) {
+        // no BF16 rounding: the binary32 result times r * inv_scale, cast once
+        const float rs = __fmul_rn(r, inv_scale);
+        const F2 rs2 = f2_make(rs, rs);
+        uint32_t codes[2];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) u[j] = __fmul_rn(x[j], w[j]);  // exact
-      float out[8];
-      if (is_pair && active) {
-        const float4* tb = &table[tok_of[k] * half + lane];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float4 sc = tb[q * quarter];  // pair 4 lane + q: {sin_hi, sin_lo, cos_hi, cos_lo}
-          out[q] = rotate(u[q], u[4 + q], sc.z, sc.w, sc.x, sc.y, -1.0f);
-          out[4 + q] = rotate(u[4 + q], u[q], sc.z, sc.w, sc.x, sc.y, 1.0f);
+        for (int e = 0; e < 2; ++e) {
+          const float2 a0 = f2_split(f2_mul(o[2 * e], rs2)), a1 = f2_split(f2_mul(o[2 * e + 1], rs2));
+          codes[e] = uint32_t(f32x2_to_e4m3x2_satfinite(a0.x, a0.y)) |
+                     (uint32_t(f32x2_to_e4m3x2_satfinite(a1.x, a1.y)) << 16);
         }
+        uint8_t* dst = static_cast<uint8_t*>(k_cache) + (uint64_t(slot) * num_kv_heads + h) * D;
+        *reinterpret_cast<uint32_t*>(dst + off_a) = codes[0];
+        *reinterpret_cast<uint32_t*>(dst + off_b) = codes[1];
       } else {
+        const F2 r2 = f2_make(r, r);
+        uint32_t packed[4];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) out[j] = u[j];
-      }
-      if (active && slot[k] >= 0) {
-        if constexpr (kFp8Out) {
-          // no BF16 rounding: the binary32 result times inv_scale, cast once
-          const float rs = __fmul_rn(r, inv_scale);
-          uint32_t codes[2];
-#pragma unroll
-          for (int j = 0; j < 2; ++j)
-            codes[j] = uint32_t(f32x2_to_e4m3x2_satfinite(__fmul_rn(out[4 * j], rs), __fmul_rn(out[4 * j + 1], rs))) |
-                       (uint32_t(f32x2_to_e4m3x2_satfinite(__fmul_rn(out[4 * j + 2], rs),
-                                                           __fmul_rn(out[4 * j + 3], rs))) << 16);
-          uint8_t* dst = static_cast<uint8_t*>(k_cache) + (uint64_t(slot[k]) * num_kv_heads + head_of[k]) * D;
-          *reinterpret_cast<uint32_t*>(dst + off_a) = codes[0];
-          *reinterpret_cast<uint32_t*>(dst + off_b) = codes[1];
-        } else {
-          uint32_t packed[4];
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            packed[j] = f32x2_to_bf16x2(__fmul_rn(out[2 * j], r), __fmul_rn(out[2 * j + 1], r));
-          uint16_t* dst = static_cast<uint16_t*>(k_cache) + (uint64_t(slot[k]) * num_kv_heads + head_of[k]) * D;
-          *reinterpret_cast<uint2*>(dst + off_a) = make_uint2(packed[0], packed[1]);
-          *reinterpret_cast<uint2*>(dst + off_b) = make_uint2(packed[2], packed[3]);
+        for (int e = 0; e < 4; ++e) {
+          const float2 a0 = f2_split(f2_mul(o[e], r2));
+          packed[e] = f32x2_to_bf16x2(a0.x, a0.y);
         }
+        uint16_t* dst = static_cast<uint16_t*>(k_cache) + (uint64_t(slot) * num_kv_heads + h) * D;
+        *reinterpret_cast<uint2*>(dst + off_a) = make_uint2(packed[0], packed[1]);
+        *reinterpret_cast<uint2*>(dst + off_b) = make_uint2(packed[2], packed[3]);
       }
     }
-    __syncthreads();  // the next pass rewrites the table
+  };
+
+  // two item buffers in turn: the next item's loads are issued before the
+  // current item is computed
+  for (uint32_t k = 0;;) {
+    if (k + 1 < n_items) load_item(k + 1, B);
+    process(A);
+    if (++k >= n_items) break;
+    if (k + 1 < n_items) load_item(k + 1, A);
+    process(B);
+    if (++k >= n_items) break;
   }
+}
+
+// frac(f / (2 pi)) * 2^96 for a binary64 f > 0, least significant word first.
+// f = M * 2^(e - 53) with a 53-bit integer M, so f / (2 pi) * 2^96 =
+// X * 2^(e - 213) with X = M * floor(2^256 / (2 pi)); its fraction's 96 bits
+// are bits [213 - e, 309 - e) of X (the truncation of the constant moves them
+// by less than 2^-200).
+uint4 turn_fraction(double f) {
+  int e = 0;
+  const double fr = frexp(f, &e);
+  const uint64_t M = uint64_t(ldexp(fr, 53));
+  uint64_t X[5];
+  unsigned __int128 carry = 0;
+  for (int k = 0; k < 4; ++k) {
+    const unsigned __int128 prod = (unsigned __int128)M * kInv2Pi256[3 - k] + carry;
+    X[k] = uint64_t(prod);
+    carry = prod >> 64;
+  }
+  X[4] = uint64_t(carry);
+  auto word = [&](int bit) -> uint32_t {  // X's bits [bit, bit + 32); zero outside X
+    uint32_t v = 0;
+    for (int b = 0; b < 32; ++b) {
+      const int at = bit + b;
+      if (at >= 0 && at < 320 && ((X[at >> 6] >> (at & 63)) & 1u)) v |= 1u << b;
+    }
+    return v;
+  };
+  const int lo = 213 - e;
+  return make_uint4(word(lo), word(lo + 32), word(lo + 64), 0u);
+}
+
+// The turn fractions of theta^(-2i/R), i < R/2, for the last (theta, R) this
+// host thread launched with.
+const TurnTable& turn_table(float theta, uint32_t rotary_dim) {
+  thread_local TurnTable tt;
+  thread_local float cached_theta = 0.0f;
+  thread_local uint32_t cached_r = 0;
+  if (cached_r != rotary_dim || cached_theta != theta) {
+    const double c = -2.0 * log2(double(theta)) / double(rotary_dim);
+    for (uint32_t i = 0; i < 128; ++i) tt.g[i] = i < rotary_dim / 2 ? turn_fraction(exp2(c * double(i))) : uint4{};
+    cached_theta = theta;
+    cached_r = rotary_dim;
+  }
+  return tt;
 }
 
 }  // namespace
@@ -322,17 +478,17 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) fused_k_norm_rope_kernel
 template <int D>
 static void launch_d(bool fp8_out, bool mrope, unsigned blocks, cudaStream_t stream, const uint16_t* k_in,
                      const uint16_t* w, const int32_t* pos, const int32_t* pos_h, const int32_t* pos_w, void* cache,
-                     const int64_t* slots, uint32_t n, uint32_t H, uint32_t R, float eps, const FreqTable& ft,
-                     float inv_scale, uint32_t tok_pass) {
+                     const int64_t* slots, uint32_t n, uint32_t H, uint32_t R, float eps, const TurnTable& tt,
+                     float inv_scale) {
   if (fp8_out)
-    fused_k_norm_rope_kernel<D, true, false><<<blocks, kThreads, 0, stream>>>(
-        k_in, w, pos, pos_h, pos_w, cache, slots, n, H, R, eps, ft, inv_scale, tok_pass);
+    fused_k_norm_rope_kernel<D, true, false><<<blocks, kThreads, 0, stream>>>(k_in, w, pos, pos_h, pos_w, cache,
+                                                                              slots, n, H, R, eps, tt, inv_scale);
   else if (mrope)
-    fused_k_norm_rope_kernel<D, false, true><<<blocks, kThreads, 0, stream>>>(
-        k_in, w, pos, pos_h, pos_w, cache, slots, n, H, R, eps, ft, inv_scale, tok_pass);
+    fused_k_norm_rope_kernel<D, false, true><<<blocks, kThreads, 0, stream>>>(k_in, w, pos, pos_h, pos_w, cache,
+                                                                              slots, n, H, R, eps, tt, inv_scale);
   else
-    fused_k_norm_rope_kernel<D, false, false><<<blocks, kThreads, 0, stream>>>(
-        k_in, w, pos, pos_h, pos_w, cache, slots, n, H, R, eps, ft, inv_scale, tok_pass);
+    fused_k_norm_rope_kernel<D, false, false><<<blocks, kThreads, 0, stream>>>(k_in, w, pos, pos_h, pos_w, cache,
+                                                                               slots, n, H, R, eps, tt, inv_scale);
 }
 
 cudaError_t launch_fused_k_norm_rope(const uint16_t* k_in, const uint16_t* k_norm_weight,
@@ -342,35 +498,25 @@ cudaError_t launch_fused_k_norm_rope(const uint16_t* k_in, const uint16_t* k_nor
                                      uint32_t num_kv_heads, uint32_t head_dim, uint32_t rotary_dim,
                                      float rms_eps, float theta, cudaStream_t stream) {
   const DeviceInfo& dev = device_info();
-  const uint32_t tok_pass = tokens_per_pass(head_dim, rotary_dim, num_kv_heads);
-  const uint64_t passes = (uint64_t(num_tokens) + tok_pass - 1) / tok_pass;
+  const uint32_t tokens_per_step = 256 / head_dim;
+  const uint64_t steps = (uint64_t(num_tokens) + tokens_per_step - 1) / tokens_per_step;
   uint64_t blocks = uint64_t(dev.num_sms) * kCtasPerSm;  // persistent
-  if (passes < blocks) blocks = passes;
+  const uint64_t needed = (steps + kWarps - 1) / kWarps;   // one step per warp at least
+  if (needed < blocks) blocks = needed;
   const bool mrope = pos_h != nullptr;
-  // theta^(-2i/R) in binary64, split into three binary32 parts
-  FreqTable ft{};
-  const double c = -2.0 * log2(double(theta)) / double(rotary_dim);
-  for (uint32_t i = 0; i < rotary_dim / 2 && i < 128; ++i) {
-    const double f = exp2(c * double(i));
-    Freq& e = ft.f[i];
-    e.h = float(f);
-    e.m = float(f - double(e.h));
-    e.l = float(f - double(e.h) - double(e.m));
-    e.pad = 0.0f;
-    e.d = f;
-  }
+  const TurnTable& tt = turn_table(theta, rotary_dim);
   switch (head_dim) {
     case 64:
       launch_d<64>(fp8_out, mrope, unsigned(blocks), stream, k_in, k_norm_weight, positions, pos_h, pos_w, k_cache,
-                   slot_mapping, num_tokens, num_kv_heads, rotary_dim, rms_eps, ft, inv_scale, tok_pass);
+                   slot_mapping, num_tokens, num_kv_heads, rotary_dim, rms_eps, tt, inv_scale);
       break;
     case 128:
       launch_d<128>(fp8_out, mrope, unsigned(blocks), stream, k_in, k_norm_weight, positions, pos_h, pos_w, k_cache,
-                    slot_mapping, num_tokens, num_kv_heads, rotary_dim, rms_eps, ft, inv_scale, tok_pass);
+                    slot_mapping, num_tokens, num_kv_heads, rotary_dim, rms_eps, tt, inv_scale);
       break;
     case 256:
       launch_d<256>(fp8_out, mrope, unsigned(blocks), stream, k_in, k_norm_weight, positions, pos_h, pos_w, k_cache,
-                    slot_mapping, num_tokens, num_kv_heads, rotary_dim, rms_eps, ft, inv_scale, tok_pass);
+                    slot_mapping, num_tokens, num_kv_heads, rotary_dim, rms_eps, tt, inv_scale);
       break;
     default:
       return cudaErrorInvalidValue;
