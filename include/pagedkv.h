@@ -12,9 +12,11 @@
  * Conventions for every call
  *   - Pointers marked "device" are CUDA device (or managed) memory owned by
  *     the caller; the library never allocates, frees or keeps them, and never
- *     synchronises. Every call is asynchronous on `stream` (a cudaStream_t;
- *     NULL means the legacy default stream) and returns once the work is
- *     queued.
+ *     synchronises. Every call is asynchronous on `stream` and returns once
+ *     the work is queued. The stream is a cudaStream_t passed as void* (NULL
+ *     means the legacy default stream), so that this header and its callers
+ *     (C code, ctypes) need no CUDA header; the scope table's listing writes
+ *     it as cudaStream_t.
  *   - BF16 data are passed as their 16-bit patterns (kv_bf16_t), FP8 data as
  *     E4M3 ("FN": no infinities, max 448, NaN 0x7F/0xFF) codes (kv_e4m3_t).
  *   - Cache pools are [num_blocks, block_size, num_kv_heads, head_dim], row
@@ -56,7 +58,8 @@ enum kv_status {
     KV_ERR_INVALID_ARG = 1,  /* null pointer with work to do, bad shape or stride */
     KV_ERR_UNSUPPORTED = 2,  /* legal but outside what the kernels implement */
     KV_ERR_CUDA = 3,         /* a CUDA runtime or driver call failed */
-    KV_ERR_DEVICE = 4        /* a kernel reported a fault in device data or a wait timeout */
+    KV_ERR_DEVICE = 4        /* kv_get_device_error only: a kernel reported a fault in device
+                                data or a wait timeout since the last read */
 };
 
 /* Human-readable text of a status code (static storage). */
@@ -296,11 +299,12 @@ PAGEDKV_API int paged_prefill_attn_fp8(const kv_bf16_t *q, const kv_e4m3_t *k_ca
 /* ------------------------------------------------------------------------
  * FP8-K paged decode without any caller-provided memory. The source pages
  * have no counterpart of this call; it exists for callers that cannot give
- * the library a device allocation: host code running in a callback enqueued
- * with cudaLaunchHostFunc may not call the CUDA API (so it cannot
- * cudaMalloc a workspace), and applications whose device memory belongs to
- * another allocator (a framework memory pool, a serving engine with a fixed
- * memory budget) cannot set a raw buffer aside for a library.
+ * the library a device allocation: applications whose device memory belongs
+ * to another allocator (a framework memory pool, a serving engine that
+ * reserves all of HBM for its KV cache) cannot set a raw buffer aside for a
+ * library, and a cudaMalloc of their own would fail or break that
+ * allocator's accounting. Like every call here it uses the CUDA API, so it
+ * must not be made from a host function enqueued with cudaLaunchHostFunc.
  *
  * Same arguments, results and limits as paged_decode_attn_fp8k; the
  * split-KV scratch comes from a fixed 64 MiB array in the library's own
@@ -310,11 +314,13 @@ PAGEDKV_API int paged_prefill_attn_fp8(const kv_bf16_t *q, const kv_e4m3_t *k_ca
  * (kv_decode_workspace_bytes of the same arguments) exceeds 64 MiB.
  * The first call on a device, with that device current, looks up the
  * array's device address (cudaGetSymbolAddress) and caches it: make that
- * first call before any stream capture. All calls share the one array,
- * which keeps the previous call's contents; each call clears the counters
- * that must start at zero on its own stream first. Calls whose work may
- * overlap on the GPU (different streams, other devices' calls aside) race on
- * the array: order them.
+ * first call before any stream capture, and do not call it on a device
+ * after a cudaDeviceReset in the same process (the cached address belonged
+ * to the reset context). All calls share the one array, which keeps the
+ * previous call's contents; each call clears the counters that must start
+ * at zero on its own stream first. Calls whose work may overlap on the GPU
+ * (different streams, other devices' calls aside) race on the array: order
+ * them.
  * ---------------------------------------------------------------------- */
 PAGEDKV_API int paged_decode_attn_fp8k_static_scratch(
     const kv_bf16_t *q, const kv_e4m3_t *k_cache_fp8, const kv_bf16_t *v_cache, float *output,
@@ -327,6 +333,18 @@ PAGEDKV_API int paged_decode_attn_fp8k_static_scratch(
  * combine step need scratch). The caller allocates device memory of at
  * least kv_decode_workspace_bytes(...) for the largest decode it will run
  * and registers it for the current device; NULL (or 0 bytes) unregisters.
+ *
+ * kv_decode_workspace_bytes takes the decode's table geometry
+ * (max_blocks_per_seq, num_seqs, num_q_heads, num_kv_heads, head_dim,
+ * block_size: the same values the decode call gets) rather than a split
+ * count: the kernel chooses each launch's split size on the device from the
+ * actual sequence lengths, so a caller cannot know that count in advance.
+ * The size covers the worst case, a sequence as long as its table allows
+ * (max_blocks_per_seq * block_size positions) cut into the smallest split
+ * (256 positions): 256 + num_seqs * ceil(max_blocks_per_seq * block_size /
+ * 256) * num_q_heads * (head_dim + 2) * 4 bytes. A smaller registered
+ * workspace is still used, with coarser splits (or none below two splits'
+ * worth), and gives the same results.
  * Decode calls on that device use it in stream order, so decode calls that
  * may run concurrently on different streams need separate devices or must be
  * ordered by the caller. The library never frees it.
@@ -341,7 +359,12 @@ PAGEDKV_API int kv_set_decode_workspace(void *device_ptr, size_t bytes);
  * or table value they refuse to use, a pipeline wait that ran out of time)
  * skip the work, set a bit here and return instead of faulting or hanging.
  * kv_get_device_error synchronises the current device, returns the bits seen
- * since the last clear (0 = none) in *bits and clears them.
+ * since the last clear (0 = none) in *bits and clears them. Its status is
+ * KV_ERR_DEVICE when any bit was set, KV_OK when none was, KV_ERR_CUDA when
+ * the synchronisation or a read failed (*bits then unspecified) and
+ * KV_ERR_INVALID_ARG for a null bits pointer. The other calls never
+ * synchronise, so they cannot see these faults and never return
+ * KV_ERR_DEVICE.
  *   bit 0: a decode pipeline wait timed out
  *   bit 1: seq_lens[s] exceeded max_blocks_per_seq * block_size (clamped)
  *   bit 2: a prefill query_start_loc was decreasing, negative or past
@@ -365,6 +388,16 @@ PAGEDKV_API int kv_get_device_error(uint32_t *bits);
  * synchronises. The product build returns KV_ERR_UNSUPPORTED.
  * ---------------------------------------------------------------------- */
 PAGEDKV_API int kv_debug_set_pool(uint32_t num_blocks, uint32_t block_size);
+
+/* Bounds-checking build only: how long each pipeline wait of the paged
+ * decode kernels (a consumer waiting for a loaded tile, the loader waiting
+ * for a free stage) may take on the current device before the kernel gives
+ * up, sets bit 0 of the fault word and returns; 0 restores the default of
+ * 2 s, which the product build always uses. Whatever the limit, a decode CTA
+ * that gave up first waits (with the 2 s limit) until every copy it issued
+ * into its shared memory has landed, so that nothing is left in flight.
+ * The call synchronises. The product build returns KV_ERR_UNSUPPORTED. */
+PAGEDKV_API int kv_debug_set_wait_limit(uint64_t nanoseconds);
 
 /* Number of decode CTAs per SM and SM count the library launches with on the
  * current device, for benchmarks (optional outputs may be NULL). */

@@ -26,7 +26,8 @@ __all__ = [
     "paged_decode_attn_fp8k", "paged_decode_attn_fp8", "paged_prefill_attn_bf16", "paged_prefill_attn_fp8k",
     "paged_prefill_attn_fp8", "paged_decode_attn_fp8k_static_scratch",
     "kv_decode_workspace_bytes",
-    "kv_set_decode_workspace", "kv_get_device_error", "kv_device_info", "kv_debug_set_pool", "use_library",
+    "kv_set_decode_workspace", "kv_get_device_error", "kv_device_info", "kv_debug_set_pool",
+    "kv_debug_set_wait_limit", "use_library",
     "KV_OK", "KV_ERR_INVALID_ARG",
     "KV_ERR_UNSUPPORTED", "KV_ERR_CUDA", "KV_ERR_DEVICE",
 ]
@@ -77,6 +78,7 @@ _SIGNATURES = {
     "kv_get_device_error": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32)]),
     "kv_device_info": (ctypes.c_int, [ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)]),
     "kv_debug_set_pool": (ctypes.c_int, [_U32, _U32]),
+    "kv_debug_set_wait_limit": (ctypes.c_int, [ctypes.c_uint64]),
 }
 
 
@@ -300,6 +302,13 @@ def kv_debug_set_pool(num_blocks: int, block_size: int) -> None:
     _check("kv_debug_set_pool", lib().kv_debug_set_pool(num_blocks, block_size))
 
 
+def kv_debug_set_wait_limit(nanoseconds: int) -> None:
+    """Bounds-checking build only: the paged decode's pipeline wait limit on
+    the current device (0 restores the default 2 s). Raises PagedKVError
+    (KV_ERR_UNSUPPORTED) on the product build."""
+    _check("kv_debug_set_wait_limit", lib().kv_debug_set_wait_limit(nanoseconds))
+
+
 def kv_get_device_error() -> int:
     """Synchronise the current device and return (and clear) the kernels'
     fault bits: 1 = a pipeline wait timed out, 2 = a sequence length was
@@ -307,7 +316,9 @@ def kv_get_device_error() -> int:
     decreasing, negative or past num_q_tokens (that sequence skipped),
     8 = (bounds-checking build) a slot or block id outside the pool."""
     bits = ctypes.c_uint32(0)
-    _check("kv_get_device_error", lib().kv_get_device_error(ctypes.byref(bits)))
+    status = lib().kv_get_device_error(ctypes.byref(bits))
+    if status != KV_ERR_DEVICE:  # KV_ERR_DEVICE only says that some bit was set
+        _check("kv_get_device_error", status)
     return int(bits.value)
 
 

@@ -74,7 +74,7 @@ const char* kv_status_string(int status) {
     case KV_ERR_INVALID_ARG: return "invalid argument";
     case KV_ERR_UNSUPPORTED: return "unsupported shape, alignment or device";
     case KV_ERR_CUDA: return "CUDA error";
-    case KV_ERR_DEVICE: return "kernel reported a fault in device data";
+    case KV_ERR_DEVICE: return "a kernel reported a fault in device data or a wait timeout";
     default: return "unknown status";
   }
 }
@@ -395,7 +395,7 @@ int kv_get_device_error(uint32_t* bits) {
     return KV_ERR_CUDA;
   *bits |= d[0] | d[1] | d[2] | d[3];
 #endif
-  return KV_OK;
+  return *bits ? KV_ERR_DEVICE : KV_OK;
 }
 
 int kv_debug_set_pool(uint32_t num_blocks, uint32_t block_size) {
@@ -412,6 +412,17 @@ int kv_debug_set_pool(uint32_t num_blocks, uint32_t block_size) {
   (void)num_blocks;
   (void)block_size;
   return KV_ERR_UNSUPPORTED;  // only the bounds-checking build checks indices
+#endif
+}
+
+int kv_debug_set_wait_limit(uint64_t nanoseconds) {
+#ifdef PAGEDKV_DEBUG_BOUNDS
+  if (device_info().device < 0) return KV_ERR_CUDA;
+  const uint64_t ns = nanoseconds ? nanoseconds : kWaitLimitNs;
+  return from_cuda(debug_set_wait_limit_decode(ns));
+#else
+  (void)nanoseconds;
+  return KV_ERR_UNSUPPORTED;  // the product build's limit is fixed
 #endif
 }
 

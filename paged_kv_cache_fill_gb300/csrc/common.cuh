@@ -18,6 +18,10 @@ enum : uint32_t {
   kErrIndexOutOfPool = 1u << 3,  // bounds-checking build only
 };
 
+// How long a pipeline wait on an mbarrier may take before the kernel gives
+// up, records kErrWaitTimeout and leaves (2 s of %globaltimer).
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
 #ifdef PAGEDKV_DEBUG_BOUNDS
 // Bounds-checking build. Each translation unit holds the pool size the
 // caller set (kv_debug_set_pool; 0 blocks = unchecked) and its own fault
@@ -27,6 +31,13 @@ enum : uint32_t {
 static __device__ uint32_t g_dbg_pool_blocks;
 static __device__ uint64_t g_dbg_pool_slots;
 static __device__ uint32_t g_dbg_error;
+// The decode's pipeline wait limit, settable in this build only
+// (kv_debug_set_wait_limit), so that a test can make a wait run out.
+static __device__ uint64_t g_dbg_wait_limit_ns = kWaitLimitNs;
+
+__device__ __forceinline__ uint64_t pipeline_wait_limit() {
+  return *reinterpret_cast<volatile const uint64_t*>(&g_dbg_wait_limit_ns);
+}
 
 __device__ __forceinline__ bool dbg_block_ok(int64_t block) {
   const uint32_t n = g_dbg_pool_blocks;
@@ -56,7 +67,12 @@ __device__ __forceinline__ bool dbg_slot_ok(int64_t slot) {
     if (e != cudaSuccess) return e;                                                    \
     const uint32_t zero = 0;                                                           \
     return cudaMemcpyToSymbol(g_dbg_error, &zero, sizeof(zero));                       \
+  }                                                                                    \
+  cudaError_t debug_set_wait_limit_##unit(uint64_t ns) {                               \
+    return cudaMemcpyToSymbol(g_dbg_wait_limit_ns, &ns, sizeof(ns));                   \
   }
+#else
+__device__ __forceinline__ uint64_t pipeline_wait_limit() { return kWaitLimitNs; }
 #endif
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -103,7 +119,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // `limit_ns` of wall time (the hardware try_wait already suspends between
 // polls) and returns false so the caller can record the fault and leave.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
-                                          uint64_t limit_ns = 2000000000ull) {
+                                          uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {

@@ -225,6 +225,7 @@ __global__ void __launch_bounds__(32 * 9, 1)
 
   const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t num_consumers = p.heads_per_item * NT;
+  const uint64_t wait_ns = pipeline_wait_limit();  // fixed in the product build
 
   if (threadIdx.x == 0) {
     for (uint32_t s = 0; s < p.stages; ++s) {
@@ -269,6 +270,9 @@ __global__ void __launch_bounds__(32 * 9, 1)
     wk.load(0, p, split_tiles, lane);
     uint32_t stage = 0, phase = 0;
     bool ok = true;
+    // Stages whose last fill was issued with TMA (bit s) and the parity the
+    // consumers wait on for that fill: drained before the CTA exits.
+    uint32_t issued = 0, issued_parity = 0;
     // Items are handed out by an atomic counter in the workspace (each CTA
     // keeps the next item id in hand and asks for the one after while it
     // issues the current item), or statically without a workspace.
@@ -313,8 +317,9 @@ __global__ void __launch_bounds__(32 * 9, 1)
       if (tile_begin >= tile_end) {
         // no positions: one meta-only stage tells the consumers to write zeros
         if (lane == 0) {
-          if (!mbar_wait(&empty[stage], phase ^ 1)) ok = false;
+          if (!mbar_wait(&empty[stage], phase ^ 1, wait_ns)) ok = false;
           if (ok) {
+            issued &= ~(1u << stage);  // the stage's previous fill was taken, so it landed
             meta[stage] = StageMeta{int32_t(s), int32_t(hg), int32_t(split), 0, 0, 0,
                                     kFirst | kLast | kEmpty | base_flags, 0};
             mbar_arrive(&full[stage]);
@@ -337,8 +342,9 @@ __global__ void __launch_bounds__(32 * 9, 1)
         }
         const int32_t block_id = __shfl_sync(0xffffffffu, cached_block_id, lblock - cached_first_block);
         if (lane == 0) {
-          if (!mbar_wait(&empty[stage], phase ^ 1)) ok = false;
+          if (!mbar_wait(&empty[stage], phase ^ 1, wait_ns)) ok = false;
           if (ok) {
+            issued &= ~(1u << stage);
             int32_t flags = base_flags;
             if (tile == tile_begin) flags |= kFirst;
             if (tile == tile_end - 1) flags |= kLast;
@@ -360,6 +366,8 @@ __global__ void __launch_bounds__(32 * 9, 1)
             tma_load_3d(st, &tmap_k, 0, slot0, head0 * kKChunks, &full[stage]);
             tma_load_3d(st + p.k_bytes, &tmap_v, 0, slot0, head0 * kVChunks, &full[stage]);
             if (flags & kFirst) bulk_load(st + p.k_bytes + p.v_bytes, q_src, q_bytes, &full[stage]);
+            issued |= 1u << stage;
+            issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
           }
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -368,7 +376,8 @@ __global__ void __launch_bounds__(32 * 9, 1)
     }
     // sentinel: no more work
     if (ok && lane == 0) {
-      if (mbar_wait(&empty[stage], phase ^ 1)) {
+      if (mbar_wait(&empty[stage], phase ^ 1, wait_ns)) {
+        issued &= ~(1u << stage);
         meta[stage].flags = kSentinel;
         mbar_arrive(&full[stage]);
       } else {
@@ -376,6 +385,18 @@ __global__ void __launch_bounds__(32 * 9, 1)
       }
     }
     if (!__all_sync(0xffffffffu, ok) && lane == 0) atomicOr(&g_decode_error, kErrWaitTimeout);
+    // No copy may land in shared memory after the CTA exits: wait (bounded,
+    // with the fixed limit even where the pipeline's is shorter) until every
+    // TMA fill not yet known to have landed has completed. A bit is cleared
+    // when the producer next waits the stage's empty barrier out (the
+    // consumers took that fill). After a normal run the fills still marked
+    // are ones the consumers wait on too, so they have landed or are about
+    // to; the drain matters when a wait above, or a consumer's, gave up.
+    if (lane == 0) {
+      for (uint32_t st = 0; st < p.stages; ++st)
+        if ((issued >> st) & 1u)
+          if (!mbar_wait(&full[st], (issued_parity >> st) & 1u)) atomicOr(&g_decode_error, kErrWaitTimeout);
+    }
     // The last CTA to finish resets the counters for the next launch.
     if (dynamic && lane == 0) {
       __threadfence();
@@ -405,7 +426,8 @@ __global__ void __launch_bounds__(32 * 9, 1)
 
   uint32_t stage = 0, phase = 0;
   while (true) {
-    if (!mbar_wait(&full[stage], phase)) {
+    if (!mbar_wait(&full[stage], phase, wait_ns)) {
+      // the producer drains the copies it issued before the CTA exits
       if (lane == 0) atomicOr(&g_decode_error, kErrWaitTimeout);
       return;
     }

@@ -107,6 +107,7 @@ cudaError_t debug_read_and_clear_kv_write(uint32_t* bits);
 cudaError_t debug_read_and_clear_fused_k(uint32_t* bits);
 cudaError_t debug_read_and_clear_decode(uint32_t* bits);
 cudaError_t debug_read_and_clear_prefill(uint32_t* bits);
+cudaError_t debug_set_wait_limit_decode(uint64_t ns);
 #endif
 
 }  // namespace pagedkv

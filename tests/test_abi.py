@@ -163,15 +163,13 @@ def test_prefill_unsupported_shapes(pk, kind):
     assert _prefill(L, kind, mbps=1 << 27, bs=16) == UNS           # 2^31 positions per sequence
 
 
-def test_readme_example_calls_match_the_binding(pk):
-    """The README's call sequence cannot run without a GPU; parse it instead
-    and bind every pk.* call to the binding's signature."""
+def test_example_calls_match_the_binding(pk):
+    """The example call sequence (paged_kv_cache_fill_gb300/example.py) needs
+    a GPU to run; parse it instead and bind every pk.* call to the binding's
+    signature."""
     import ast
     import inspect
-    text = open(os.path.join(ROOT, "README.md")).read()
-    blocks = re.findall(r"```python\n(.*?)```", text, re.S)
-    assert blocks, "README has no python example"
-    tree = ast.parse(blocks[0])
+    tree = ast.parse(open(os.path.join(ROOT, "paged_kv_cache_fill_gb300", "example.py")).read())
     calls = [n for n in ast.walk(tree) if isinstance(n, ast.Call) and isinstance(n.func, ast.Attribute)
              and isinstance(n.func.value, ast.Name) and n.func.value.id == "pk"]
     assert len(calls) >= 5
@@ -186,6 +184,7 @@ def test_readme_example_calls_match_the_binding(pk):
 
 def test_product_build_has_no_bounds_checks(pk):
     assert pk.lib().kv_debug_set_pool(16, 16) == pk.KV_ERR_UNSUPPORTED
+    assert pk.lib().kv_debug_set_wait_limit(1000) == pk.KV_ERR_UNSUPPORTED
 
 
 def test_bounds_checking_build(pk):
@@ -218,6 +217,9 @@ def test_workspace_size_formula(pk):
     got = pk.kv_decode_workspace_bytes(512, 64, 32, 8, 128, 16)
     assert got == 256 + 64 * 32 * 32 * 130 * 4
     assert pk.kv_decode_workspace_bytes(1, 1, 4, 2, 64, 16) == 256 + 1 * 1 * 4 * 66 * 4
+    # the table geometry, not the lengths, sets the split count: 19 blocks of
+    # 16 positions (304) make 2 splits of 256
+    assert pk.kv_decode_workspace_bytes(19, 3, 8, 2, 128, 16) == 256 + 3 * 2 * 8 * 130 * 4
 
 
 def test_status_strings(pk):
