@@ -2,20 +2,25 @@
 // that cannot hand the library a device allocation.
 //
 // The regular decode takes its split-KV scratch from a buffer the caller
-// allocates and registers. Some callers cannot do that: code that runs in a
-// host callback enqueued with cudaLaunchHostFunc may not call the CUDA API at
-// all (so it cannot cudaMalloc), and applications whose device memory is owned
-// end to end by another allocator (a framework's memory pool, a serving engine
-// with a fixed memory budget) have no way to set a raw buffer aside for a
-// third-party library. This entry point needs no allocation from anyone: its
-// scratch is a fixed-size array in the library's own device memory.
+// allocates and registers. Some callers cannot do that: an application whose
+// device memory is owned end to end by another allocator (a framework's
+// memory pool, a serving engine that reserves all of HBM for its KV cache up
+// front) has no way to set a raw buffer aside for a third-party library, and
+// a cudaMalloc of its own would fail or break that allocator's accounting.
+// This entry point needs no allocation from anyone: its scratch is a
+// fixed-size array in the library's own device memory. (It is an ordinary
+// CUDA call like every other one here: it must not be made from a host
+// function enqueued with cudaLaunchHostFunc, where the CUDA API may not be
+// called.)
 //
 // The array is g_static_scratch below (kStaticScratchBytes = 64 MiB). Every
 // GPU that loads the library reserves it until the process exits. Host code
 // must not use the array's name as a device address, so the first call on
 // each device (with that device current) looks up the array's device address
 // with cudaGetSymbolAddress and caches it; make that first call before any
-// stream capture.
+// stream capture. A device reset (cudaDeviceReset) ends the context that
+// address belongs to: do not call this entry point on a device after
+// resetting it in the same process.
 #include <math.h>
 
 #include <mutex>
