@@ -163,7 +163,9 @@ WORKLOAD_OF_PART = {"fused_write": "fused", "bf16_prefill": "bf16_gqa4", "bf16_d
                     "fused_k_write_fp8": "fused", "fused_k_write_mrope": "fused",
                     "fp8_kv_prefill": "fp8k_long", "fp8_kv_decode_w0": "fp8k_long",
                     "fp8_kv_mixed_decode": "fp8k_mixed", "bf16_chunked_prefill": "bf16_gqa4",
-                    "fp8k_chunked_prefill": "fp8k_mixed", "fp8_kv_chunked_prefill": "fp8k_mixed"}
+                    "fp8k_chunked_prefill": "fp8k_mixed", "fp8_kv_chunked_prefill": "fp8k_mixed",
+                    "fused_write_65536": "fused_stream", "fused_k_write_65536": "fused_stream",
+                    "fused_k_write_fp8_65536": "fused_stream", "fused_k_write_mrope_65536": "fused_stream"}
 
 
 class GpuStep:
@@ -219,7 +221,8 @@ class GpuStep:
         # Each workload is set up in a method of its own, so every closure
         # binds its own shapes and buffers.
         want = WORKLOAD_OF_PART[self.only_part] if self.only_part else None
-        for name, setup in (("fused", self._setup_fused), ("bf16_gqa4", self._setup_bf16_gqa4),
+        for name, setup in (("fused", self._setup_fused), ("fused_stream", self._setup_fused_stream),
+                            ("bf16_gqa4", self._setup_bf16_gqa4),
                             ("fp8k_long", self._setup_fp8k_long), ("fp8k_mixed", self._setup_fp8k_mixed)):
             if want in (None, name):
                 setup()
@@ -288,6 +291,48 @@ class GpuStep:
         # positions (4, or 3 x 4) and the slot (8)
         self.extras += [dict(name="fused_k_write_fp8", fn=k_write_fp8, tokens=n, bytes=n * (2048 + 1024 + 4 + 8)),
                         dict(name="fused_k_write_mrope", fn=k_write_mrope, tokens=n,
+                             bytes=n * (2048 + 2048 + 12 + 8))]
+
+    def _setup_fused_stream(self):
+        """The fused K write and its siblings at a streaming size, beside the
+        step: 64 sequences x 1024 tokens (65,536 tokens; 134 MB of K and
+        134 MB of V rows in, the same out), the fused_write recipe otherwise.
+        The slots are filled once, untimed."""
+        torch, kvgen, pk, dev = self.torch, self.kvgen, self.pk, self.dev
+        w = kvgen.fused_write(device=dev, seqs=64, tokens_per_seq=1024)
+        H, D, bs, n = w.num_kv_heads, w.head_dim, w.block_size, w.num_tokens
+        tables = w.block_tables.to(dev)
+        slots = torch.empty(n, dtype=torch.int64, device=dev)
+        fill, _ = self._slots_calls(w, tables, slots)
+        fill()
+        kc = kvgen.poisoned_pool(w.num_blocks, bs, H, D, "bf16", dev)
+        vc = kvgen.poisoned_pool(w.num_blocks, bs, H, D, "bf16", dev)
+        kc8 = kvgen.poisoned_pool(w.num_blocks, bs, H, D, "fp8", dev)
+        wt, pos = w.extra["k_norm_weight"].to(dev), w.positions.to(dev)
+        key, value = w.key.contiguous(), w.value.contiguous()
+        g = torch.Generator().manual_seed(2024)
+        pos_h = torch.randint(0, 1 << 17, (n,), generator=g).to(torch.int32).to(dev)
+        pos_w = torch.randint(0, 512, (n,), generator=g).to(torch.int32).to(dev)
+
+        def k_write():
+            pk.kv_write_fused_k_norm_rope_bf16(key, wt, pos, kc, slots, n, H, D, 128, bs, 1e-6, 1e6)
+
+        def k_and_v_write():
+            k_write()
+            pk.kv_write_v_only(value, vc, slots, n, H, D, bs, H * D)
+
+        def k_write_fp8():
+            pk.kv_write_fused_k_norm_rope_fp8(key, wt, pos, kc8, slots, n, H, D, 128, bs, 1e-6, 1e6, 448.0 / 6.0)
+
+        def k_write_mrope():
+            pk.kv_write_fused_k_norm_rope_bf16_mrope(key, wt, pos, pos_h, pos_w, kc, slots, n, H, D, 128, bs,
+                                                     1e-6, 1e6)
+        self.extras += [dict(name="fused_write_65536", fn=k_and_v_write, tokens=n,
+                             bytes=n * (2048 + 2048 + 4 + 8 + 2048 + 2048 + 8)),
+                        dict(name="fused_k_write_65536", fn=k_write, tokens=n, bytes=n * (2048 + 2048 + 4 + 8)),
+                        dict(name="fused_k_write_fp8_65536", fn=k_write_fp8, tokens=n,
+                             bytes=n * (2048 + 1024 + 4 + 8)),
+                        dict(name="fused_k_write_mrope_65536", fn=k_write_mrope, tokens=n,
                              bytes=n * (2048 + 2048 + 12 + 8))]
 
     def _setup_bf16_gqa4(self):
@@ -558,35 +603,58 @@ class GpuStep:
             p["fn"]()
 
     def time_calls(self, reps: int) -> dict:
-        """Eager launches with CUDA events: each part's writes or decode, and
-        the per-sequence slot fills of all parts together ("slot_fill")."""
+        """Each part as the step runs it, from CUDA graphs of its own (so that
+        no host launch gap enters the time): its per-sequence slot fills
+        (together "slot_fill"), then its main calls, side by side where the
+        step runs them so. A 256 MiB buffer is rewritten before every timed
+        replay (outside the events), so no part finds its inputs in L2."""
         torch = self.torch
-        ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+        scrub = torch.empty(256 << 20, dtype=torch.uint8, device=self.dev)
+        side = [torch.cuda.Stream() for _ in range(8)]
+        cap = torch.cuda.Stream()
+
+        def graph_of(fns, parallel):
+            g = torch.cuda.CUDAGraph()
+            cap.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.graph(g, stream=cap):
+                if parallel and len(fns) > 1:
+                    for i, f in enumerate(fns):
+                        st = side[i % len(side)]
+                        st.wait_stream(cap)
+                        with torch.cuda.stream(st):
+                            f()
+                    for st in side[:len(fns)]:
+                        cap.wait_stream(st)
+                else:
+                    for f in fns:
+                        f()
+            torch.cuda.current_stream().wait_stream(cap)
+            return g
+
+        graphs = []
+        for p in self.parts:
+            if "fill_fn" in p:
+                graphs.append(("slot_fill", graph_of(p["fills"], True)))
+                mains = p.get("mains") or [p["main"]]
+                graphs.append((p["name"], graph_of(mains, True)))
+            else:
+                graphs.append((p["name"], graph_of([p["fn"]], False)))
+        torch.cuda.synchronize()
         rec = []
         for _ in range(reps):
-            for p in self.parts:
-                if "fill_fn" in p:
-                    a, b, c = ev(), ev(), ev()
-                    a.record()
-                    p["fill_fn"]()
-                    b.record()
-                    for f in (p.get("mains") or [p["main"]]):
-                        f()
-                    c.record()
-                    rec.append(("slot_fill", a, b))
-                    rec.append((p["name"], b, c))
-                else:
-                    a, b = ev(), ev()
-                    a.record()
-                    p["fn"]()
-                    b.record()
-                    rec.append((p["name"], a, b))
+            for name, g in graphs:
+                scrub.fill_(1)
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                g.replay()
+                b.record()
+                rec.append((name, a, b))
         torch.cuda.synchronize()
         out = {}
         for name, a, b in rec:
             out[name] = out.get(name, 0.0) + a.elapsed_time(b) / reps
+        del graphs
         return out
-
 
     def time_extras(self, reps: int) -> dict:
         """Eager launches of the calls outside the step, CUDA events around
@@ -766,8 +834,8 @@ def run_gpu(args):
             "algorithmic_bytes_per_step": int(step.total_bytes),
             "step_mode": "one CUDA-graph replay per step (the per-sequence slot fills run as 8 parallel graph "
                          "branches, the fused K and V-only writes side by side); per-call 'parts' timed "
-                         "from eager launches with CUDA events, the 196 per-sequence kv_fill_slots launches "
-                         "together as slot_fill",
+                         "from CUDA-graph replays of each part alone with CUDA events, L2 scrubbed before "
+                         "each, the 196 per-sequence kv_fill_slots launches together as slot_fill",
             "parts": parts,
             "next_rows": next_rows,
             "roofline": roofline,
@@ -849,15 +917,21 @@ def run_e2e(step, args, dev, world):
     in_ready = [torch.cuda.Event() for _ in range(2)]
     done = [torch.cuda.Event() for _ in range(2)]
     steps = max(1, min(args.steps, 5))
+    copy_marks = []  # (start, end) of every step's host->device copies, during the run
 
     def copy_in(k):
         b = k % 2
         if k >= 2:
             h2d_s.wait_event(done[b])  # step k - 2's kernels have read this set
+        a = torch.cuda.Event(enable_timing=True)
+        a.record(h2d_s)
         with torch.cuda.stream(h2d_s):
             for h, d in zip(host_in, dev_in[b]):
                 d.copy_(h, non_blocking=True)
         in_ready[b].record(h2d_s)
+        e = torch.cuda.Event(enable_timing=True)
+        e.record(h2d_s)
+        copy_marks.append((a, e))
 
     def run(n):
         start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -899,12 +973,18 @@ def run_e2e(step, args, dev, world):
         return t
 
     run(2)  # warm-up: both graphs and both buffer sets
+    copy_marks.clear()
     ms = run(steps) / steps
+    # the host->device copies of each step as they ran beside the kernels
+    h2d_run_ms = statistics.mean(a.elapsed_time(e) for a, e in copy_marks)
     alone = [copies_alone() for _ in range(2)]
     h2d_ms, d2h_ms = min(t[0] for t in alone), min(t[1] for t in alone)
     del twin_graph, twins
     link = host_link_gbs(compute)
-    link.update(step_h2d_gbs=round(h2d / (h2d_ms * 1e-3) / 1e9, 1), step_d2h_gbs=round(d2h / (d2h_ms * 1e-3) / 1e9, 1))
+    link.update(step_h2d_gbs=round(h2d / (h2d_ms * 1e-3) / 1e9, 1), step_d2h_gbs=round(d2h / (d2h_ms * 1e-3) / 1e9, 1),
+                step_h2d_ms_alone=round(h2d_ms, 3), step_d2h_ms_alone=round(d2h_ms, 3),
+                step_h2d_ms_during_run=round(h2d_run_ms, 3),
+                step_h2d_gbs_during_run=round(h2d / (h2d_run_ms * 1e-3) / 1e9, 1))
     # the step cannot end before its inputs have crossed the host link and
     # its outputs have come back: the step's own copies, timed alone, bound
     # the end-to-end rate

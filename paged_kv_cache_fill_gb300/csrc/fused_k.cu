@@ -188,10 +188,6 @@ __device__ __forceinline__ F2 mul_bf16x2(uint32_t x, uint32_t w) {
   return f2_make(fma_bf16<false>(x, w, -0.0f), fma_bf16<true>(x, w, -0.0f));
 }
 
-#ifndef FUSED_K_PACKED_ROTATE
-#define FUSED_K_PACKED_ROTATE 1
-#endif
-
 // Sine and cosine of two rotation pairs, each as a (hi, lo) binary32 pair,
 // packed pair by pair for the f32x2 rotation.
 struct PairSinCos {
@@ -218,36 +214,13 @@ __device__ __forceinline__ void rotate2(F2 X, F2 Y, const PairSinCos& c, F2& out
   out_y = f2_add(ty, f2_sub(sy, ne));
 }
 
-// The same two rotations one element at a time (scalar FMAs take the
-// negations as free operand modifiers: 6 FMA-pipe operations per output
-// against 7 packed).
-__device__ __forceinline__ float rotate1(float ua, float ub, float ch, float cl, float sh, float sl, float sign) {
-  const float p2 = __fmul_rn(ub, sh);
-  const float e2 = fmaf(ub, sh, -p2);
-  const float t0 = fmaf(ua, ch, sign * p2);  // ua ch + sign p2, one rounding
-  return __fadd_rn(t0, fmaf(sign * ub, sl, fmaf(ua, cl, sign * e2)));
-}
-
-__device__ __forceinline__ void rotate2_scalar(F2 X, F2 Y, const PairSinCos& c, F2& out_x, F2& out_y) {
-  const float2 x = f2_split(X), y = f2_split(Y), ch = f2_split(c.ch), cl = f2_split(c.cl), sh = f2_split(c.sh),
-               sl = f2_split(c.sl);
-  out_x = f2_make(rotate1(x.x, y.x, ch.x, cl.x, sh.x, sl.x, -1.0f), rotate1(x.y, y.y, ch.y, cl.y, sh.y, sl.y, -1.0f));
-  out_y = f2_make(rotate1(y.x, x.x, ch.x, cl.x, sh.x, sl.x, 1.0f), rotate1(y.y, x.y, ch.y, cl.y, sh.y, sl.y, 1.0f));
-}
-
-#ifndef FUSED_K_THREADS
-#define FUSED_K_THREADS 256
-#endif
-#ifndef FUSED_K_CTAS
-#define FUSED_K_CTAS 2
-#endif
-#ifndef FUSED_K_HEADS
-#define FUSED_K_HEADS 4
-#endif
-constexpr int kThreads = FUSED_K_THREADS;
+// Launch shape: persistent, two 256-thread CTAs per SM, four head rows per
+// lane per item (a sweep of threads, CTAs per SM and heads per item chose
+// it; eight heads per item spilled or cut the occupancy).
+constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kCtasPerSm = FUSED_K_CTAS;
-constexpr int kHeadsPerStep = FUSED_K_HEADS;  // head rows a lane holds per item
+constexpr int kCtasPerSm = 2;
+constexpr int kHeadsPerStep = 4;  // head rows a lane holds per item
 
 // One item's inputs for this lane: its unit of kHeadsPerStep head rows of one
 // token, the token's slot and (on the token's first item) its positions.
@@ -381,13 +354,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) fused_k_norm_rope_kernel
       const F2 x01 = mul_bf16x2(it.xa[j].x, wa.x), x23 = mul_bf16x2(it.xa[j].y, wa.y);
       const F2 y01 = mul_bf16x2(it.xb[j].x, wb.x), y23 = mul_bf16x2(it.xb[j].y, wb.y);
       F2 o[4];  // elements (0,1), (2,3), (4,5), (6,7)
-#if FUSED_K_PACKED_ROTATE
       rotate2(x01, y01, sc[0], o[0], o[2]);
       rotate2(x23, y23, sc[1], o[1], o[3]);
-#else
-      rotate2_scalar(x01, y01, sc[0], o[0], o[2]);
-      rotate2_scalar(x23, y23, sc[1], o[1], o[3]);
-#endif
       if constexpr (kFp8Out) {
         // no BF16 rounding: the binary32 result times r * inv_scale, cast once
         const float rs = __fmul_rn(r, inv_scale);
