@@ -214,9 +214,10 @@ PAGEDKV_API int kv_write_v_only(const kv_bf16_t *value, kv_bf16_t *v_cache, cons
  * Supported: head_dim in {64, 128, 256} (FP8: {128, 256}); block_size a power
  * of two in [16, 256]; g <= 16; q, caches and q_stride 16-byte aligned;
  * output 8-byte aligned. Anything else returns KV_ERR_UNSUPPORTED.
- * Long sequences are split across CTAs (flash-decoding) when a workspace was
- * registered with kv_set_decode_workspace; without one every (sequence, KV
- * head group) runs in one CTA (same result, less parallelism).
+ * With a workspace registered by kv_set_decode_workspace, the positions of
+ * all sequences are shared out equally among the CTAs and a sequence split
+ * between CTAs is merged afterwards (flash-decoding); without one every
+ * (sequence, KV head group) runs in one CTA (same result, less parallelism).
  * ---------------------------------------------------------------------- */
 PAGEDKV_API int paged_decode_attn_bf16(const kv_bf16_t *q, const kv_bf16_t *k_cache, const kv_bf16_t *v_cache,
                            float *output, const int32_t *block_tables, const int32_t *seq_lens,
@@ -337,14 +338,19 @@ PAGEDKV_API int paged_decode_attn_fp8k_static_scratch(
  * kv_decode_workspace_bytes takes the decode's table geometry
  * (max_blocks_per_seq, num_seqs, num_q_heads, num_kv_heads, head_dim,
  * block_size: the same values the decode call gets) rather than a split
- * count: the kernel chooses each launch's split size on the device from the
- * actual sequence lengths, so a caller cannot know that count in advance.
- * The size covers the worst case, a sequence as long as its table allows
- * (max_blocks_per_seq * block_size positions) cut into the smallest split
- * (256 positions): 256 + num_seqs * ceil(max_blocks_per_seq * block_size /
- * 256) * num_q_heads * (head_dim + 2) * 4 bytes. A smaller registered
- * workspace is still used, with coarser splits (or none below two splits'
- * worth), and gives the same results.
+ * count: the kernel cuts the tiles of all sequences (16 positions each),
+ * taken in sequence order, into equal chunks, about one per SM, sized on
+ * the device from the actual sequence lengths, and a sequence is split
+ * where a chunk boundary falls inside it; a caller cannot know those splits
+ * in advance. The size covers the worst case, a sequence as long as its
+ * table allows (T = ceil(max_blocks_per_seq * block_size / 16) tiles) cut
+ * by chunks of 16 tiles into P = (T <= 1 ? T : (T - 2) / 16 + 2) pieces
+ * (integer division): 256 bytes of header, then num_seqs * num_kv_heads
+ * 4-byte piece counts rounded up to a multiple of 256 bytes, then
+ * num_seqs * P * num_q_heads * (head_dim + 2) * 4 bytes of partials. A
+ * smaller registered workspace is still used, with longer chunks (or none
+ * where it holds fewer than two pieces per sequence), and gives the same
+ * results.
  * Decode calls on that device use it in stream order, so decode calls that
  * may run concurrently on different streams need separate devices or must be
  * ordered by the caller. The library never frees it.

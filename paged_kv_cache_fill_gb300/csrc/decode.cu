@@ -11,14 +11,20 @@
 // GB300 design (the pages launch one 256-thread block per (query head,
 // sequence); that re-reads each KV head's bytes once per query head of its
 // group, so it is not followed):
-//   * A work item is (sequence, group of HG KV heads, split of the sequence's
-//     16-token tiles). One persistent CTA per SM walks the items b, b+G, ...
+//   * The unit of work is a 16-token tile of one (sequence, group of HG KV
+//     heads). One persistent CTA per SM. With a workspace (split-KV), the
+//     tiles of all (sequence, head group) pairs form one stream, in sequence
+//     order, which is cut into equal chunks, about one per CTA (stream-K):
+//     every CTA gets the same number of tiles whatever the length mix, and a
+//     sequence is split only where a chunk boundary falls inside it. Without
+//     one, a CTA takes whole (sequence, head group) items b, b+G, ...
 //     Every KV byte is read exactly once per call.
-//   * Warp 0 is the producer: it walks the items and the block table and
+//   * Warp 0 is the producer: it walks its chunk's pieces (the part of one
+//     (sequence, head group) inside the chunk) and the block table, and
 //     issues TMA tiled loads of each 16-token tile of K and V for the HG
 //     heads (one 16-row x 128-byte box per head and 128-byte chunk, swizzled
-//     so that ldmatrix over 8 token rows is bank-conflict free) plus, on an
-//     item's first tile, a bulk copy of the item's query rows, into a ring of
+//     so that ldmatrix over 8 token rows is bank-conflict free) plus, on a
+//     piece's first tile, a bulk copy of its query rows, into a ring of
 //     stages guarded by full/empty mbarriers.
 //   * Warps 1..HG*NT are consumers, one per (KV head, 8-query-head tile). Per
 //     tile: S^T = K Q^T with mma.sync m16n8k16 (16 tokens x 8 query heads),
@@ -30,11 +36,11 @@
 //     gives each lane two tokens of two adjacent dims; P then enters as f16
 //     hi + lo parts scaled by 2^8 (keeping small weights out of the f16
 //     subnormal range), and v_scale / 2^8 is applied at the end.
-//   * Split-KV (flash-decoding): items of a sequence write unnormalised
-//     partial outputs with their running max and sum to a caller-provided
-//     workspace; a combine kernel merges them in fixed split order, so the
-//     result is deterministic. Sequences that fit one item are written
-//     directly.
+//   * Split-KV (flash-decoding): the pieces of a sequence cut by chunk
+//     boundaries write unnormalised partial outputs with their running max
+//     and sum to a caller-provided workspace; a combine kernel merges them in
+//     piece order, so the result is deterministic. A piece that holds a whole
+//     sequence is written directly.
 #include <cudaTypedefs.h>
 #include <math.h>
 
@@ -48,9 +54,10 @@ namespace {
 __device__ uint32_t g_decode_error;
 
 constexpr int kTile = 16;            // tokens per stage
-constexpr int kHeaderBytes = 256;    // workspace header (split size)
-constexpr int kItemsPerCtaTarget = 24;  // items per CTA the split size aims for
-constexpr int kMinSplitTiles = 16;      // smallest split: 256 positions
+constexpr int kHeaderBytes = 256;    // workspace header (work and done counters)
+constexpr int kChunksPerCta = 1;     // chunks of the tile stream per CTA
+constexpr int kMinChunkTiles = 4;    // smallest chunk: 64 positions
+constexpr int kSplitUnitTiles = 16;  // the workspace-size formula's split unit: 256 positions
 constexpr float kLog2e = 1.4426950408889634f;
 
 enum : int32_t {
@@ -72,14 +79,15 @@ struct DecodeParams {
   float* output;
   float* ws_o;          // [num_seqs, max_splits, Hq, D] partial outputs (unnormalised)
   float* ws_ml;         // [num_seqs, max_splits, Hq, 2] running max (log2 units) and sum
-  uint32_t* ws_header;  // [0] split size chosen by the kernel, [1] work counter, [2] done counter
+  uint32_t* ws_count;   // [num_seqs, num_head_groups] pieces of each (sequence, head group)
+  uint32_t* ws_header;  // [1] work counter, [2] done counter
   uint32_t max_blocks_per_seq, num_seqs, num_q_heads, num_kv_heads, block_size, block_shift;
   uint32_t group;       // query heads per KV head
   uint32_t heads_per_item;  // HG
   uint32_t num_head_groups;
   uint32_t q_stride, sliding_window;
   uint32_t max_splits;  // 0: no workspace, one item per (sequence, head group)
-  uint32_t min_split_tiles;
+  uint32_t min_chunk_tiles;  // chunks at least this long keep every sequence within max_splits pieces
   float score_scale;    // inv_sqrt_d * log2(e)   (times k_scale for FP8)
   float out_scale;      // FP8 V: v_scale / 2^8 (P enters the MMA scaled by 2^8)
   uint32_t stages, stage_bytes, k_bytes, v_bytes;  // shared-memory ring geometry
@@ -107,31 +115,24 @@ __device__ __forceinline__ SeqSpan seq_span(int32_t raw_len, const DecodeParams&
   return s;
 }
 
-__device__ __forceinline__ int32_t splits_of(int32_t ntiles, uint32_t split_tiles) {
-  const int64_t n = (int64_t(ntiles) + int64_t(split_tiles) - 1) / int64_t(split_tiles);
-  return n < 1 ? 1 : int32_t(n);
-}
-
-// The producer warp walks the item sequence 32 sequences at a time: each
-// lane holds one sequence's item count and the warp keeps an inclusive
-// prefix of the chunk.
+// The producer walks the tile stream 32 sequences at a time: each lane
+// holds one sequence's tile count (times the head groups) and the warp keeps
+// an inclusive prefix of the chunk.
 struct Walker {
-  uint32_t chunk_seq;     // first sequence of the cached chunk
-  uint64_t chunk_items;   // items before the chunk
-  uint32_t incl;          // inclusive prefix of item counts within the chunk (this lane)
-  uint32_t chunk_total;
-  int32_t raw_len;        // seq_lens of sequence chunk_seq + lane
+  uint32_t chunk_seq;    // first sequence of the cached chunk
+  uint64_t chunk_base;   // stream tiles before the chunk
+  uint64_t incl;         // inclusive prefix of stream tiles within the chunk (this lane)
+  uint64_t chunk_total;  // stream tiles of the chunk
+  int32_t raw_len;       // seq_lens of sequence chunk_seq + lane
 
-  __device__ void load(uint32_t first_seq, const DecodeParams& p, uint32_t split_tiles, uint32_t lane) {
+  __device__ void load(uint32_t first_seq, const DecodeParams& p, uint32_t lane) {
     chunk_seq = first_seq;
     const uint32_t s = first_seq + lane;
     raw_len = s < p.num_seqs ? __ldg(p.seq_lens + s) : 0;
-    uint32_t n = 0;
-    if (s < p.num_seqs) n = p.num_head_groups * uint32_t(splits_of(seq_span(raw_len, p).ntiles, split_tiles));
-    incl = n;
+    incl = s < p.num_seqs ? uint64_t(seq_span(raw_len, p).ntiles) * p.num_head_groups : 0;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+      const uint64_t v = __shfl_up_sync(0xffffffffu, incl, o);
       if (lane >= uint32_t(o)) incl += v;
     }
     chunk_total = __shfl_sync(0xffffffffu, incl, 31);
@@ -220,8 +221,7 @@ __global__ void __launch_bounds__(32 * 9, 1)
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.stages * p.stage_bytes);
   uint64_t* empty = full + p.stages;
   StageMeta* meta = reinterpret_cast<StageMeta*>(empty + p.stages);
-  __shared__ uint32_t s_split_tiles;
-  __shared__ uint64_t s_total;
+  __shared__ uint64_t s_chunk, s_total;
 
   const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t num_consumers = p.heads_per_item * NT;
@@ -237,8 +237,8 @@ __global__ void __launch_bounds__(32 * 9, 1)
   }
   __syncthreads();
 
-  // Split size: enough items for ~kItemsPerCtaTarget per CTA, never below
-  // the minimum split (or the larger minimum a small workspace imposes).
+  // Chunk size: the stream's tiles over kChunksPerCta chunks per CTA, never
+  // below the minimum chunk (or the larger one a small workspace imposes).
   if (p.max_splits > 0) {
     uint64_t local = 0;
     for (uint32_t s = threadIdx.x; s < p.num_seqs; s += blockDim.x)
@@ -248,74 +248,35 @@ __global__ void __launch_bounds__(32 * 9, 1)
     if (lane == 0 && local) atomicAdd(reinterpret_cast<unsigned long long*>(&s_total), local);
     __syncthreads();
     if (threadIdx.x == 0) {
-      const uint64_t stages_total = s_total * p.num_head_groups;
-      const uint64_t want = (stages_total + uint64_t(gridDim.x) * kItemsPerCtaTarget - 1) /
-                            (uint64_t(gridDim.x) * kItemsPerCtaTarget);
-      uint32_t t = want > p.min_split_tiles ? uint32_t(want) : p.min_split_tiles;
-      s_split_tiles = t;
-      if (blockIdx.x == 0) *p.ws_header = t;
+      s_total *= p.num_head_groups;
+      const uint64_t parts = uint64_t(gridDim.x) * kChunksPerCta;
+      const uint64_t want = (s_total + parts - 1) / parts;
+      s_chunk = want > p.min_chunk_tiles ? want : p.min_chunk_tiles;
     }
-  } else if (threadIdx.x == 0) {
-    s_split_tiles = 0x7fffffffu;
+    __syncthreads();
   }
-  __syncthreads();
-  const uint32_t split_tiles = s_split_tiles;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     tma_prefetch_desc(&tmap_k);
     tma_prefetch_desc(&tmap_v);
-    Walker wk;
-    wk.chunk_items = 0;
-    wk.load(0, p, split_tiles, lane);
     uint32_t stage = 0, phase = 0;
     bool ok = true;
     // Stages whose last fill was issued with TMA (bit s) and the parity the
     // consumers wait on for that fill: drained before the CTA exits.
     uint32_t issued = 0, issued_parity = 0;
-    // Items are handed out by an atomic counter in the workspace (each CTA
-    // keeps the next item id in hand and asks for the one after while it
-    // issues the current item), or statically without a workspace.
-    const bool dynamic = p.max_splits > 0;
-    uint32_t* const work = dynamic ? p.ws_header + 1 : nullptr;
-    auto grab = [&]() -> uint32_t { return lane == 0 ? atomicAdd(work, 1u) : 0u; };
-    uint64_t it = dynamic ? __shfl_sync(0xffffffffu, grab(), 0) : blockIdx.x;
-    uint64_t next = dynamic ? __shfl_sync(0xffffffffu, grab(), 0) : it + gridDim.x;
-    uint32_t pending = 0;
-    for (; ok; it = next, next = dynamic ? __shfl_sync(0xffffffffu, pending, 0) : next + gridDim.x) {
-      if (dynamic) pending = grab();  // consumed at the end of this iteration
-      // locate the item's sequence
-      while (wk.chunk_seq < p.num_seqs && it >= wk.chunk_items + wk.chunk_total) {
-        wk.chunk_items += wk.chunk_total;
-        wk.load(wk.chunk_seq + 32, p, split_tiles, lane);
-      }
-      if (wk.chunk_seq >= p.num_seqs) break;  // past the last item
-      const uint32_t rel = uint32_t(it - wk.chunk_items);
-      const uint32_t ballot = __ballot_sync(0xffffffffu, wk.incl > rel);
-      const uint32_t sl = __ffs(ballot) - 1;
-      const uint32_t s = wk.chunk_seq + sl;
-      const uint32_t incl_s = __shfl_sync(0xffffffffu, wk.incl, sl);
-      const int32_t raw_len = __shfl_sync(0xffffffffu, wk.raw_len, sl);
-      const SeqSpan span = seq_span(raw_len, p);
-      const uint32_t nsplit = uint32_t(splits_of(span.ntiles, split_tiles));
-      const uint32_t items_s = p.num_head_groups * nsplit;
-      const uint32_t j = rel - (incl_s - items_s);  // item index within the sequence
-      const uint32_t hg = j / nsplit, split = j % nsplit;
-      // 64-bit: without a workspace split_tiles is "unbounded" (0x7fffffff)
-      const int64_t tb64 = int64_t(span.t0) + int64_t(split) * int64_t(split_tiles);
-      int64_t te64 = tb64 + int64_t(split_tiles);
-      if (te64 > int64_t(span.t0) + span.ntiles) te64 = int64_t(span.t0) + span.ntiles;
-      const int32_t tile_begin = int32_t(tb64);
-      const int32_t tile_end = int32_t(te64);
-      const int32_t base_flags = (nsplit == 1 ? kSingle : 0);
+
+    // One piece: tiles [tile_begin, tile_end) of sequence s for head group
+    // hg, the split'th piece of that pair (no tiles: one meta-only stage
+    // tells the consumers to write zeros).
+    auto emit = [&](uint32_t s, uint32_t hg, uint32_t split, const SeqSpan& span, int32_t tile_begin,
+                    int32_t tile_end, int32_t base_flags) {
       const uint32_t heads_here = (hg + 1) * p.heads_per_item <= p.num_kv_heads
                                       ? p.heads_per_item
                                       : p.num_kv_heads - hg * p.heads_per_item;
       const uint32_t q_bytes = heads_here * p.group * D * 2;
       const uint16_t* q_src = p.q + uint64_t(s) * p.q_stride + uint64_t(hg) * p.heads_per_item * p.group * D;
-
       if (tile_begin >= tile_end) {
-        // no positions: one meta-only stage tells the consumers to write zeros
         if (lane == 0) {
           if (!mbar_wait(&empty[stage], phase ^ 1, wait_ns)) ok = false;
           if (ok) {
@@ -327,7 +288,7 @@ __global__ void __launch_bounds__(32 * 9, 1)
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (++stage == p.stages) { stage = 0; phase ^= 1; }
-        continue;
+        return;
       }
       const int32_t* table = p.block_tables + uint64_t(s) * p.max_blocks_per_seq;
       const int32_t tiles_per_block_shift = int32_t(p.block_shift) - 4;  // block_size >= 16
@@ -350,8 +311,8 @@ __global__ void __launch_bounds__(32 * 9, 1)
             if (tile == tile_end - 1) flags |= kLast;
             meta[stage] = StageMeta{int32_t(s), int32_t(hg), int32_t(split), tile, span.start,
                                     span.len, flags, 0};
-            // one box per tensor covers all heads of the item (chunks past the
-            // last head are zero-filled and still counted in the box bytes)
+            // one box per tensor covers all heads of the piece (chunks past
+            // the last head are zero-filled and still counted in the box bytes)
             const uint32_t bytes = p.k_bytes + p.v_bytes + ((flags & kFirst) ? q_bytes : 0u);
             mbar_arrive_expect_tx(&full[stage], bytes);
             uint8_t* st = smem + stage * p.stage_bytes;
@@ -372,6 +333,57 @@ __global__ void __launch_bounds__(32 * 9, 1)
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (++stage == p.stages) { stage = 0; phase ^= 1; }
+      }
+    };
+
+    if (p.max_splits > 0) {
+      // Stream-K: chunk k holds stream tiles [k C, (k + 1) C). CTA b takes
+      // chunk b; chunks past the grid (more than one per CTA) come from an
+      // atomic counter in the workspace header, in increasing order, so the
+      // walker only moves forward. The piece of (sequence, head group) range
+      // [a, b) that lies in chunk k is its piece k - floor(a / C).
+      const uint64_t C = s_chunk, total = s_total;
+      const uint64_t nchunks = (total + C - 1) / C;
+      uint32_t* const work = p.ws_header + 1;
+      Walker wk;
+      wk.chunk_base = 0;
+      wk.load(0, p, lane);
+      uint64_t k = blockIdx.x;
+      while (ok && k < nchunks) {
+        uint64_t g = k * C;
+        const uint64_t g1 = g + C < total ? g + C : total;
+        while (ok && g < g1) {
+          while (wk.chunk_seq < p.num_seqs && g >= wk.chunk_base + wk.chunk_total) {
+            wk.chunk_base += wk.chunk_total;
+            wk.load(wk.chunk_seq + 32, p, lane);
+          }
+          if (wk.chunk_seq >= p.num_seqs) break;  // not reached: g < total
+          const uint64_t rel = g - wk.chunk_base;
+          const uint32_t sl = __ffs(__ballot_sync(0xffffffffu, wk.incl > rel)) - 1;
+          const uint32_t s = wk.chunk_seq + sl;
+          const SeqSpan span = seq_span(__shfl_sync(0xffffffffu, wk.raw_len, sl), p);
+          const uint64_t nt = uint64_t(span.ntiles);  // > 0: the ballot skips empty sequences
+          const uint64_t seq_base = wk.chunk_base + __shfl_sync(0xffffffffu, wk.incl, sl) - nt * p.num_head_groups;
+          const uint32_t hg = uint32_t((g - seq_base) / nt);
+          const uint64_t a = seq_base + uint64_t(hg) * nt, b = a + nt;
+          const uint64_t e = b < g1 ? b : g1;
+          const uint32_t split = uint32_t(k - a / C);
+          // the piece that ends the pair records how many pieces it has
+          if (e == b && lane == 0) p.ws_count[uint64_t(s) * p.num_head_groups + hg] = split + 1;
+          emit(s, hg, split, span, span.t0 + int32_t(g - a), span.t0 + int32_t(e - a),
+               (g == a && e == b) ? kSingle : 0);
+          g = e;
+        }
+        if (nchunks <= gridDim.x) break;
+        k = gridDim.x + __shfl_sync(0xffffffffu, lane == 0 ? atomicAdd(work, 1u) : 0u, 0);
+      }
+    } else {
+      // no workspace: whole (sequence, head group) items, statically strided
+      const uint64_t items = uint64_t(p.num_seqs) * p.num_head_groups;
+      for (uint64_t it = blockIdx.x; it < items && ok; it += gridDim.x) {
+        const uint32_t s = uint32_t(it / p.num_head_groups), hg = uint32_t(it % p.num_head_groups);
+        const SeqSpan span = seq_span(__ldg(p.seq_lens + s), p);
+        emit(s, hg, 0, span, span.t0, span.t0 + span.ntiles, kSingle);
       }
     }
     // sentinel: no more work
@@ -398,7 +410,7 @@ __global__ void __launch_bounds__(32 * 9, 1)
           if (!mbar_wait(&full[st], (issued_parity >> st) & 1u)) atomicOr(&g_decode_error, kErrWaitTimeout);
     }
     // The last CTA to finish resets the counters for the next launch.
-    if (dynamic && lane == 0) {
+    if (p.max_splits > 0 && lane == 0) {
       __threadfence();
       if (atomicAdd(p.ws_header + 2, 1u) == gridDim.x - 1) {
         atomicExch(p.ws_header + 1, 0u);
@@ -676,11 +688,13 @@ __global__ void __launch_bounds__(32 * 9, 1)
   }
 }
 
-// Merge the split partials of every (sequence, query head) whose sequence
-// has more than one split: o = sum_i 2^(m_i - M) acc_i / sum_i 2^(m_i - M) l_i,
-// in split order. One CTA of D threads per (sequence, query head): the
-// splits' (m, l) are reduced across the threads, then each thread sums its
-// output element over the splits with independent (overlapping) loads.
+// Merge the partials of every (sequence, query head) whose sequence was cut
+// into more than one piece: o = sum_i 2^(m_i - M) acc_i / sum_i 2^(m_i - M) l_i,
+// in piece order. One CTA of D threads per (sequence, query head): the
+// pieces' (m, l) are reduced across the threads, then each thread sums its
+// output element over the pieces with independent (overlapping) loads. A
+// sequence with no positions has no piece in the tile stream: its output
+// row is written as zeros here.
 constexpr int kCombineMaxSplits = 1024;  // per pass through shared memory
 
 template <int D>
@@ -689,11 +703,15 @@ __global__ void __launch_bounds__(D) combine_kernel(const DecodeParams p) {
   __shared__ float s_red[D / 32];
   __shared__ float s_bcast;
   const uint32_t s = blockIdx.x, h = blockIdx.y;
-  const uint32_t split_tiles = *p.ws_header;
-  const SeqSpan span = seq_span(__ldg(p.seq_lens + s), p);
-  const int32_t nsplit = splits_of(span.ntiles, split_tiles);
-  if (nsplit <= 1) return;
   const uint32_t t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const SeqSpan span = seq_span(__ldg(p.seq_lens + s), p);
+  if (span.ntiles == 0) {
+    p.output[(uint64_t(s) * p.num_q_heads + h) * D + t] = 0.0f;
+    return;
+  }
+  const uint32_t hg = h / p.group / p.heads_per_item;
+  const int32_t nsplit = int32_t(__ldg(p.ws_count + uint64_t(s) * p.num_head_groups + hg));
+  if (nsplit <= 1) return;
   const uint64_t row0 = uint64_t(s) * p.max_splits * p.num_q_heads + h;  // split i at row0 + i*Hq
   auto block_reduce = [&](float v, bool is_max) -> float {
 #pragma unroll
@@ -851,12 +869,28 @@ int launch_decode_t(const DecodeArgs& a, cudaStream_t stream, const Geometry& ge
 
 }  // namespace
 
+namespace {
+
+// Pieces a sequence of up to max_tiles tiles can be cut into by chunks of
+// c tiles: a range [a, a + n) meets floor((a + n - 1) / c) - floor(a / c) + 1
+// chunks, at most ceil((n - 1) / c) + 1.
+uint64_t max_pieces(uint64_t max_tiles, uint64_t c) {
+  return max_tiles <= 1 ? max_tiles : (max_tiles - 2) / c + 2;
+}
+
+// The per-(sequence, head group) piece counts, ahead of the partials.
+uint64_t count_bytes(uint32_t num_seqs, uint32_t num_kv_heads) {
+  return (uint64_t(num_seqs) * num_kv_heads * 4 + kHeaderBytes - 1) / kHeaderBytes * kHeaderBytes;
+}
+
+}  // namespace
+
 size_t decode_workspace_bytes(uint32_t max_blocks_per_seq, uint32_t num_seqs, uint32_t num_q_heads,
                               uint32_t num_kv_heads, uint32_t head_dim, uint32_t block_size) {
-  (void)num_kv_heads;
   const uint64_t max_tiles = (uint64_t(max_blocks_per_seq) * block_size + kTile - 1) / kTile;
-  const uint64_t max_splits = (max_tiles + kMinSplitTiles - 1) / kMinSplitTiles;
-  return kHeaderBytes + uint64_t(num_seqs) * max_splits * num_q_heads * (uint64_t(head_dim) + 2) * 4;
+  const uint64_t max_splits = max_pieces(max_tiles, kSplitUnitTiles);
+  return kHeaderBytes + count_bytes(num_seqs, num_kv_heads) +
+         uint64_t(num_seqs) * max_splits * num_q_heads * (uint64_t(head_dim) + 2) * 4;
 }
 
 int launch_decode(const DecodeArgs& a, cudaStream_t stream) {
@@ -889,30 +923,32 @@ int launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   p.k_bytes = geo.k_bytes;
   p.v_bytes = geo.v_bytes;
 
-  // Split-KV when a workspace is registered and large enough for two or more
-  // splits: splits are at least kMinSplitTiles tiles, more if the workspace
-  // is smaller than the worst case needs.
+  // Split-KV (stream-K chunks) when a workspace is registered and holds the
+  // header, the piece counts and partials for the most pieces a sequence can
+  // be cut into: chunks are at least kMinChunkTiles long, longer if the
+  // workspace holds fewer pieces per sequence than that needs.
   const uint64_t max_tiles = (uint64_t(a.max_blocks_per_seq) * a.block_size + kTile - 1) / kTile;
+  const uint64_t fixed = kHeaderBytes + count_bytes(a.num_seqs, a.num_kv_heads);
   p.max_splits = 0;
-  p.min_split_tiles = 0x7fffffffu;
-  if (a.workspace && a.workspace_bytes > kHeaderBytes && max_tiles > kMinSplitTiles) {
+  p.min_chunk_tiles = 0;
+  if (a.workspace && a.workspace_bytes > fixed && max_tiles > 1) {
     const uint64_t per_split = uint64_t(a.num_seqs) * a.num_q_heads * (a.head_dim + 2) * 4;
-    const uint64_t fit = (a.workspace_bytes - kHeaderBytes) / per_split;
-    const uint64_t needed = (max_tiles + kMinSplitTiles - 1) / kMinSplitTiles;
-    uint64_t min_tiles = 0;
-    if (fit >= needed)
-      min_tiles = kMinSplitTiles;
+    const uint64_t fit = (a.workspace_bytes - fixed) / per_split;
+    uint64_t c = 0;
+    if (fit >= max_pieces(max_tiles, kMinChunkTiles))
+      c = kMinChunkTiles;
     else if (fit >= 2)
-      min_tiles = (max_tiles + fit - 1) / fit;
-    if (min_tiles) {
+      c = (max_tiles - 2) / (fit - 1) + 1;  // the least c with max_pieces(max_tiles, c) <= fit
+    if (c) {
       if (a.workspace_fresh &&
           cudaMemsetAsync(a.workspace, 0, kHeaderBytes, stream) != cudaSuccess)
         return KV_ERR_CUDA;
-      p.min_split_tiles = uint32_t(min_tiles);
-      p.max_splits = uint32_t((max_tiles + min_tiles - 1) / min_tiles);
+      p.min_chunk_tiles = uint32_t(c);
+      p.max_splits = uint32_t(max_pieces(max_tiles, c));
       uint8_t* ws = static_cast<uint8_t*>(a.workspace);
       p.ws_header = reinterpret_cast<uint32_t*>(ws);
-      p.ws_o = reinterpret_cast<float*>(ws + kHeaderBytes);
+      p.ws_count = reinterpret_cast<uint32_t*>(ws + kHeaderBytes);
+      p.ws_o = reinterpret_cast<float*>(ws + fixed);
       p.ws_ml = p.ws_o + uint64_t(a.num_seqs) * p.max_splits * a.num_q_heads * a.head_dim;
     }
   }

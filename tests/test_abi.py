@@ -213,13 +213,31 @@ def test_bounds_checking_build(pk):
 
 
 def test_workspace_size_formula(pk):
-    # header + num_seqs * ceil(ceil(mbps*bs/16)/16) splits * Hq * (D + 2) floats
+    # header + piece counts (num_seqs * num_kv_heads words, in 256-byte
+    # units) + num_seqs * P pieces * Hq * (D + 2) floats, where a sequence of
+    # T = ceil(mbps * bs / 16) tiles cut by 16-tile chunks makes at most
+    # P = (T - 2) // 16 + 2 pieces (T > 1)
     got = pk.kv_decode_workspace_bytes(512, 64, 32, 8, 128, 16)
-    assert got == 256 + 64 * 32 * 32 * 130 * 4
-    assert pk.kv_decode_workspace_bytes(1, 1, 4, 2, 64, 16) == 256 + 1 * 1 * 4 * 66 * 4
-    # the table geometry, not the lengths, sets the split count: 19 blocks of
-    # 16 positions (304) make 2 splits of 256
-    assert pk.kv_decode_workspace_bytes(19, 3, 8, 2, 128, 16) == 256 + 3 * 2 * 8 * 130 * 4
+    assert got == 256 + 2048 + 64 * 33 * 32 * 130 * 4
+    assert pk.kv_decode_workspace_bytes(1, 1, 4, 2, 64, 16) == 256 + 256 + 1 * 1 * 4 * 66 * 4
+    # the table geometry, not the lengths, sets the piece count: 19 blocks of
+    # 16 positions (19 tiles) can meet 3 chunks of 16 tiles
+    assert pk.kv_decode_workspace_bytes(19, 3, 8, 2, 128, 16) == 256 + 256 + 3 * 3 * 8 * 130 * 4
+    # 64-position blocks: 4 tiles each
+    assert pk.kv_decode_workspace_bytes(8, 100, 64, 8, 128, 64) == 256 + 3328 + 100 * 3 * 64 * 130 * 4
+
+
+def max_pieces(tiles, chunk):
+    """The most chunks of `chunk` tiles a run of `tiles` consecutive tiles,
+    starting anywhere, can meet (brute force over the start offset)."""
+    return max(((a + tiles - 1) // chunk - a // chunk + 1) if tiles else 0 for a in range(chunk))
+
+
+def test_piece_bound_is_tight():
+    # the workspace formula's P is the exact worst case of the chunk cut
+    for tiles in range(0, 200):
+        p = tiles if tiles <= 1 else (tiles - 2) // 16 + 2
+        assert p == max_pieces(tiles, 16), tiles
 
 
 def test_status_strings(pk):

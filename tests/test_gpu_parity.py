@@ -516,6 +516,37 @@ def test_decode_padded_q_stride_and_determinism():
     assert_decode_close(got1, _decode_ref(w, kr, vr, 0, False, q=qpad, q_stride=stride))
 
 
+@pytest.mark.parametrize("fp8", [False, True])
+def test_decode_stream_chunks(fp8):
+    """Split-KV cuts the tiles of all (sequence, head group) pairs, taken in
+    sequence order, into equal chunks. Here: sequences that straddle chunk
+    boundaries, empty sequences between them (their rows are written as
+    zeros by the combine), two head groups per sequence (16 KV heads), and
+    the same decode with workspaces that hold only 3 and 2 pieces per
+    sequence (longer chunks); every output against the oracle, and repeats
+    bit-identical."""
+    lens = [0, 5000, 3, 0, 777, 16, 17, 12000, 0, 1, 4097, 300]
+    Hq, H, D, bs = 64, 16, 128, 16
+    w = kvgen.custom(31, seq_lens=lens, num_q_heads=Hq, num_kv_heads=H, head_dim=D, block_size=bs, fp8=fp8)
+    kc, vc, kr, vr = _caches(w, fp8)
+    ref = _decode_ref(w, kr, vr, 0, fp8)
+    full = pk.kv_decode_workspace_bytes(w.max_blocks_per_seq, w.num_seqs, Hq, H, D, bs)
+    counts = -(-w.num_seqs * H * 4 // 256) * 256
+    per_piece = w.num_seqs * Hq * (D + 2) * 4
+    for pieces in (None, 3, 2):
+        _WORKSPACE.clear()
+        ws = torch.empty(full if pieces is None else 256 + counts + pieces * per_piece, dtype=torch.uint8,
+                         device=DEV)
+        pk.kv_set_decode_workspace(ws)
+        _WORKSPACE.append(ws)
+        got = _decode_gpu(w, kc, vc, 0, fp8)
+        assert_decode_close(got, ref, f"pieces {pieces}")
+        assert np.array_equal(got, _decode_gpu(w, kc, vc, 0, fp8)), f"pieces {pieces}: not deterministic"
+    for win in (1, 100, 4096):
+        assert_decode_close(_decode_gpu(w, kc, vc, win, fp8), _decode_ref(w, kr, vr, win, fp8), f"window {win}")
+    assert pk.kv_get_device_error() == 0
+
+
 def test_decode_clamps_overlong_sequence_and_flags_it():
     w = kvgen.custom(8, seq_lens=[40], num_q_heads=4, num_kv_heads=2, head_dim=128, block_size=16)
     kc, vc, kr, vr = _caches(w, False)
@@ -748,10 +779,10 @@ def _full_size(w, fp8, windows, sample_seqs, heads):
 
 @pytest.mark.parametrize("fp8", [False, True])
 def test_decode_one_very_long_sequence_every_head(fp8):
-    """A 262,144-position sequence beside a one-position one: ~1,000
-    split-KV partials for one (sequence, query head), the pool written in the
-    benchmark's 262,144-token chunks; every query head, with and without a
-    window."""
+    """A 262,144-position sequence beside a one-position one: the long one
+    is cut into a piece per SM (~150 split-KV partials per query head), the
+    pool written in the benchmark's 262,144-token chunks; every query head,
+    with and without a window."""
     w = kvgen.custom(240, device=DEV, seq_lens=[262144, 1], num_q_heads=32, num_kv_heads=8, head_dim=128,
                      block_size=16, fp8=fp8)
     _full_size(w, fp8, (0, 5000), [0, 1], tuple(range(32)))
