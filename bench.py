@@ -606,10 +606,11 @@ class GpuStep:
         """Each part as the step runs it, from CUDA graphs of its own (so that
         no host launch gap enters the time): its per-sequence slot fills
         (together "slot_fill"), then its main calls, side by side where the
-        step runs them so. A 256 MiB buffer is rewritten before every timed
-        replay (outside the events), so no part finds its inputs in L2."""
+        step runs them so. Before every timed replay (outside the events) L2
+        is flushed by reading a 256 MiB buffer (flush_l2), so no part finds
+        its inputs in L2."""
         torch = self.torch
-        scrub = torch.empty(256 << 20, dtype=torch.uint8, device=self.dev)
+        scrub = l2_flush_buffer(torch, self.dev)
         side = [torch.cuda.Stream() for _ in range(8)]
         cap = torch.cuda.Stream()
 
@@ -643,7 +644,7 @@ class GpuStep:
         rec = []
         for _ in range(reps):
             for name, g in graphs:
-                scrub.fill_(1)
+                flush_l2(scrub)
                 a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 a.record()
                 g.replay()
@@ -658,17 +659,16 @@ class GpuStep:
 
     def time_extras(self, reps: int) -> dict:
         """Eager launches of the calls outside the step, CUDA events around
-        each; a call's first run is untimed. Their inputs fit in L2, so a
-        256 MiB buffer is rewritten before every timed launch (outside the
-        events) to flush it."""
+        each; a call's first run is untimed. Their inputs fit in L2, so L2 is
+        flushed (flush_l2) before every timed launch, outside the events."""
         torch = self.torch
-        scrub = torch.empty(256 << 20, dtype=torch.uint8, device=self.dev)
+        scrub = l2_flush_buffer(torch, self.dev)
         out = {}
         for x in self.extras:
             x["fn"]()
             evs = []
             for i in range(reps):
-                scrub.fill_(i & 0xFF)
+                flush_l2(scrub)
                 a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 a.record()
                 x["fn"]()
@@ -677,6 +677,21 @@ class GpuStep:
             torch.cuda.synchronize()
             out[x["name"]] = sum(a.elapsed_time(b) for a, b in evs) / reps
         return out
+
+
+def l2_flush_buffer(torch, dev):
+    """A 256 MiB device buffer (twice L2's 129 MB) for flush_l2, written once."""
+    buf = torch.ones(256 << 20, dtype=torch.uint8, device=dev)
+    return buf.view(torch.int64)
+
+
+def flush_l2(buf):
+    """Evict everything from L2 by reading a buffer twice its size. A read
+    leaves L2 holding clean lines of this buffer: the dirty lines of earlier
+    work are written back here, before the timed region, rather than by the
+    next timed call (rewriting the buffer instead would leave ~129 MB of
+    dirty lines for that call to write back)."""
+    buf.sum()
 
 
 class Ranks:
