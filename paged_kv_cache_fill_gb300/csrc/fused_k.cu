@@ -119,42 +119,6 @@ __device__ __forceinline__ float4 turn_sincos(int32_t pos, uint4 g) {
   return make_float4(s.hi, s.lo, c.hi, c.lo);
 }
 
-// Two binary32 values in one 64-bit register pair (the first in the low
-// half), operated on element-wise by the packed f32x2 instructions: one
-// issue slot for two elements.
-using F2 = unsigned long long;
-
-__device__ __forceinline__ F2 f2_make(float lo, float hi) {
-  F2 r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-  return r;
-}
-__device__ __forceinline__ float2 f2_split(F2 v) {
-  float2 r;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
-  return r;
-}
-__device__ __forceinline__ F2 f2_mul(F2 a, F2 b) {
-  F2 d;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
-__device__ __forceinline__ F2 f2_fma(F2 a, F2 b, F2 c) {
-  F2 d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-  return d;
-}
-__device__ __forceinline__ F2 f2_add(F2 a, F2 b) {
-  F2 d;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
-__device__ __forceinline__ F2 f2_sub(F2 a, F2 b) {
-  F2 d;
-  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
-
 // The low (kHi false) or high BF16 halves of a and b multiplied exactly and
 // added to c with one rounding (mixed-precision FMA: no unpacking to binary32).
 template <bool kHi>

@@ -726,6 +726,431 @@ __global__ void __launch_bounds__(tc_threads<kFp8>(), 1)
   }
 }
 
+// ------------------------------------------------- the two-tile BF16 kernel
+// BF16 caches only. One CTA per (sequence, KV head, block of 256 rows): two
+// 128-row Q tiles, A (rows 0..127) and B (rows 128..255), share every K/V
+// tile the CTA loads. Each Q tile has its own S/P and O in tensor memory
+// (S_A [0, 128), O_A [128, 128 + D), S_B [256, 384), O_B [384, 384 + D)); Q
+// lives in shared memory (the S product's A operand). A tile's S product
+// writes the columns its P occupied, so it must wait until the tile's PV
+// product before it has finished (one thread's tcgen05.mma operations are
+// ordered only for the same accumulator); with one Q tile the tensor pipe
+// drained at every such hand-off. Here the other tile's products are queued
+// behind it: per K/V tile j the MMA thread issues PV_A(j), PV_B(j), then
+// S_A(j + 1) once PV_A(j) is done (PV_B(j) still running), then S_B(j + 1)
+// once PV_B(j) is (S_A(j + 1) running). 384 threads, three warpgroups:
+//   warpgroup 0 (registers cut to kTc2RegsLow with setmaxnreg):
+//     warp 0      TMA producer of 128-key K tiles, warp 2 of V tiles, each a
+//                 2-stage ring whose stage is free once the MMA thread's
+//                 commit after its last reader has arrived on its empty
+//                 barrier;
+//     warp 1      owns TMEM (all 512 columns) and issues every tcgen05.mma;
+//     warp 3      idle;
+//   warpgroups 1, 2 (registers raised to kTc2RegsHigh): the softmax of tile
+//     A and of tile B, one thread per row (TMEM lane) over all 128 keys of a
+//     tile, so no row is shared between threads; they also write the Q rows.
+constexpr int kTc2Rows = 256;
+constexpr uint32_t kTc2RegsLow = 64, kTc2RegsHigh = 216;  // 128 x 64 + 256 x 216 <= 384 x 168 at launch
+
+template <int D>
+struct Tc2Layout {  // byte offsets from the 1024-aligned shared base
+  static constexpr uint32_t kChunks = D / 64;
+  static constexpr uint32_t kQBytes = kChunks * kTcBM * 128;  // one Q tile [chunk][128 rows][128 B]
+  static constexpr uint32_t kQ0 = 0;
+  static constexpr uint32_t kKBytes = kChunks * kTcBN * 128;  // [chunk][128 keys][128 B]
+  static constexpr uint32_t kStage0 = 2 * kQBytes;
+  static constexpr uint32_t kStageBytes = 2 * kKBytes;        // K, then V
+  static constexpr uint32_t kBytes = kStage0 + kTcStages * kStageBytes;
+  static constexpr uint32_t kTmemCols = 512;
+  // tile t's S/P columns and O columns
+  static __device__ __forceinline__ constexpr uint32_t s_col(uint32_t t) { return t << 8; }
+  static __device__ __forceinline__ constexpr uint32_t o_col(uint32_t t) { return 128u + (t << 8); }
+};
+
+template <int D>
+__global__ void __launch_bounds__(32 * 12, 1)
+    prefill_tc2_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
+                       const PrefillParams p) {
+  using Lay = Tc2Layout<D>;
+  constexpr uint32_t kChunks = Lay::kChunks;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+  const uint32_t sbase = smem_u32(smem);
+  __shared__ uint64_t k_full[kTcStages], v_full[kTcStages], k_empty[kTcStages], v_empty[kTcStages];
+  __shared__ uint64_t s_full[2], p_full[2], o_full[2];  // per Q tile
+  __shared__ uint64_t q_full, mma_done;
+  __shared__ uint32_t tmem_base_s;
+  __shared__ Item s_item;
+
+  const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kTcStages; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&v_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+      mbar_init(&v_empty[s], 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&s_full[t], 1);
+      mbar_init(&p_full[t], kTcBM);
+      mbar_init(&o_full[t], 1);
+    }
+    mbar_init(&q_full, 2 * kTcBM);
+    mbar_init(&mma_done, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    const Item it = locate<kTc2Rows>(blockIdx.x, p, lane);
+    if (lane == 0) s_item = it;
+  }
+  __syncthreads();
+  const Item it = s_item;
+  if (it.seq < 0) return;
+  if (warp == 1) tmem_alloc(&tmem_base_s, Lay::kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_s;
+
+  const int32_t g = int32_t(p.group);
+  const bool two = it.rows > kTcBM;  // tile B holds rows
+  const int32_t pos_first = it.len - it.n + it.row0 / g;
+  const int32_t pos_last = it.len - it.n + (it.row0 + it.rows - 1) / g;
+  const int32_t k_hi = pos_last + 1;  // keys [k_lo, k_hi)
+  const int32_t W = int32_t(p.sliding_window);
+  int32_t k_lo = 0;
+  if (W > 0 && pos_first + 1 - W > 0) k_lo = pos_first + 1 - W;
+  const int32_t t_begin = k_lo / kTcBN;
+  const int32_t t_end = k_hi > 0 ? (k_hi + kTcBN - 1) / kTcBN : t_begin;
+  const int32_t T = t_end - t_begin;
+
+  if (warp < 4) {
+   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kTc2RegsLow));
+   if (warp == 0 || warp == 2) {
+    // ------------------------------------------------------------ producers
+    const bool is_k = warp == 0;
+    const CUtensorMap* map = is_k ? &tmap_k : &tmap_v;
+    uint64_t* full = is_k ? k_full : v_full;
+    uint64_t* empty = is_k ? k_empty : v_empty;
+    tma_prefetch_desc(map);
+    const int32_t* table = p.block_tables + uint64_t(it.seq) * p.max_blocks_per_seq;
+    bool ok = true;
+    int32_t issued = 0;
+    for (int32_t i = 0; i < T && ok; ++i) {
+      const uint32_t st = uint32_t(i) % kTcStages;
+      const int32_t key0 = (t_begin + i) * kTcBN + int32_t(lane) * kSub;
+      const bool mine = lane < uint32_t(kTcBN / kSub) && key0 < k_hi;
+      const int32_t block_id = mine ? __ldg(table + (key0 >> p.block_shift)) : 0;
+      // stage st was last filled for tile i - 2: free once its last reader is done
+      if (lane == 0 && i >= kTcStages && !mbar_wait(&empty[st], uint32_t((i - kTcStages) / kTcStages) & 1))
+        ok = false;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      const uint32_t loaded = __popc(__ballot_sync(0xffffffffu, mine));
+      if (lane == 0) mbar_arrive_expect_tx(&full[st], loaded * kChunks * (kSub * 128));
+      __syncwarp();
+      if (mine) {
+#ifdef PAGEDKV_DEBUG_BOUNDS
+        const int32_t slot0 =
+            ((dbg_block_ok(block_id) ? block_id : 0) << p.block_shift) + (key0 & int32_t(p.block_size - 1));
+#else
+        const int32_t slot0 = (block_id << p.block_shift) + (key0 & int32_t(p.block_size - 1));
+#endif
+        uint8_t* dst = smem + Lay::kStage0 + st * Lay::kStageBytes + (is_k ? 0u : Lay::kKBytes) + lane * (kSub * 128);
+        for (uint32_t c = 0; c < kChunks; ++c)
+          tma_load_3d(dst + c * (kTcBN * 128), map, 0, slot0, it.kv_head * kChunks + c, &full[st]);
+      }
+      issued = i + 1;
+    }
+    if (!ok) {
+      // a wait gave up: let this warp's loads still in flight land (bounded)
+      if (lane == 0) atomicOr(&g_prefill_error, kErrWaitTimeout);
+      for (int32_t j = issued > kTcStages ? issued - kTcStages : 0; j < issued; ++j)
+        mbar_wait(&full[uint32_t(j) % kTcStages], uint32_t(j / kTcStages) & 1);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issue
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = umma_idesc_bf16(kTcBM, kTcBN, false);
+      constexpr uint32_t idesc_o = umma_idesc_bf16(kTcBM, D, true);
+      const uint64_t k_desc0 = umma_desc_sw128(sbase + Lay::kStage0, 16, 1024);
+      const uint64_t v_desc0 = umma_desc_sw128(sbase + Lay::kStage0 + Lay::kKBytes, kTcBN * 128, 1024);
+      const uint64_t q_desc0 = umma_desc_sw128(sbase + Lay::kQ0, 16, 1024);
+      constexpr uint64_t kStageStep = Lay::kStageBytes >> 4;
+      constexpr uint64_t kQStep = Lay::kQBytes >> 4;
+      const uint32_t ntiles = two ? 2u : 1u;
+      bool ok = mbar_wait(&q_full, 0);
+      tc_fence_after();
+      // S_t(j) = Q_t K(j)^T into tile t's S columns
+      auto issue_s = [&](int32_t j, uint32_t t) {
+        const uint64_t kd = k_desc0 + uint64_t(uint32_t(j) % kTcStages) * kStageStep;
+        const uint64_t qd = q_desc0 + t * kQStep;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          // chunk kk / 4 is 128 rows of 128 B further; 16 dims are 32 B
+          const uint64_t off = uint64_t((kk >> 2) * (kTcBN * 128) + (kk & 3) * 32) >> 4;
+          umma_f16kind_ss(tmem + Lay::s_col(t), qd + off, kd + off, idesc_s, kk > 0);
+        }
+        umma_commit(&s_full[t]);
+      };
+      if (ok && T > 0) {
+        ok = mbar_wait(&k_full[0], 0);
+        tc_fence_after();
+        if (ok) {
+          for (uint32_t t = 0; t < ntiles; ++t) issue_s(0, t);
+          umma_commit(&k_empty[0]);
+        }
+      }
+      // Per K/V tile j: PV_A(j); S_A(j + 1) as soon as PV_A(j) is done; then
+      // PV_B(j) and S_B(j + 1) the same way. Each S product follows its own
+      // tile's PV directly, so a tile's loop (softmax, PV, S) is not held up
+      // by the other tile's PV product in the in-order pipe.
+      for (int32_t j = 0; j < T && ok; ++j) {
+        const uint32_t st = uint32_t(j) % kTcStages;
+        const bool more = j + 1 < T;
+        const uint32_t sn = uint32_t(j + 1) % kTcStages;
+        if (!mbar_wait(&v_full[st], uint32_t(j / kTcStages) & 1)) {
+          ok = false;
+          break;
+        }
+        const uint64_t vd = v_desc0 + st * kStageStep;
+        for (uint32_t t = 0; t < ntiles && ok; ++t) {
+          if (!mbar_wait(&p_full[t], uint32_t(j) & 1)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t pt = tmem + Lay::s_col(t);  // P of tile t: hi, then lo
+#pragma unroll
+          for (int kk = 0; kk < kTcBN / 16; ++kk) {
+            const uint64_t v_k = vd + uint64_t(kk * (16 * 128) >> 4);
+            umma_f16kind_tmem_a(tmem + Lay::o_col(t), pt + 8 * kk, v_k, idesc_o, j > 0 || kk > 0);
+            umma_f16kind_tmem_a(tmem + Lay::o_col(t), pt + kTcBN / 2 + 8 * kk, v_k, idesc_o, true);
+          }
+          umma_commit(&o_full[t]);
+          if (t + 1 == ntiles) umma_commit(&v_empty[st]);
+          if (more) {
+            // tile t's S columns hold P_t(j) until PV_t(j) is done
+            if (t == 0 && !mbar_wait(&k_full[sn], uint32_t((j + 1) / kTcStages) & 1)) {
+              ok = false;
+              break;
+            }
+            if (!mbar_wait(&o_full[t], uint32_t(j) & 1)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_s(j + 1, t);
+            if (t + 1 == ntiles) umma_commit(&k_empty[sn]);
+          }
+        }
+      }
+      if (!ok) atomicOr(&g_prefill_error, kErrWaitTimeout);
+      // every issued MMA has finished before TMEM is released
+      umma_commit(&mma_done);
+      mbar_wait(&mma_done, 0);
+    }
+    __syncwarp();
+   }
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kTc2RegsHigh));
+    // ------------------------------------------------------------ softmax
+    const uint32_t t = (warp - 4) >> 2;         // the Q tile
+    const uint32_t row = (warp & 3) * 32 + lane;  // the row within the tile = TMEM lane
+    const uint32_t lane_addr = ((warp & 3) * 32u) << 16;
+    const int32_t r = int32_t(t * kTcBM + row);  // the item's row
+    const bool valid = r < it.rows;
+    const int32_t grow = it.row0 + r;
+    const int32_t tok = grow / g, hh = grow % g;
+    const int32_t pos = valid ? it.len - it.n + tok : -1;  // -1: attends nothing
+    const int32_t lo = W > 0 ? pos + 1 - W : INT32_MIN;
+    // the Q row into the tile's shared-memory tile ([chunk][row][128 B],
+    // 128-byte swizzled), zeros past the item
+    {
+      const uint16_t* qr = valid ? p.q + uint64_t(it.qstart + tok) * p.q_stride + uint64_t(it.kv_head * g + hh) * D
+                                 : nullptr;
+      uint8_t* qt = smem + Lay::kQ0 + t * Lay::kQBytes;
+#pragma unroll
+      for (uint32_t u = 0; u < D / 8; ++u) {  // 16-byte unit u: chunk u / 8, unit u % 8 of its 128-byte row
+        const uint4 v = qr ? *reinterpret_cast<const uint4*>(qr + 8 * u) : make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(qt + (u >> 3) * (kTcBM * 128) + row * 128 + (((u & 7) ^ (row & 7)) << 4)) = v;
+      }
+    }
+    fence_async_smem();
+    mbar_arrive(&q_full);
+    if (t == 1 && !two) {
+      // no rows in tile B: nothing more to do
+    } else {
+      const uint32_t scol = tmem + lane_addr + Lay::s_col(t);
+      const uint32_t ocol = tmem + lane_addr + Lay::o_col(t);
+      float m_run = -INFINITY, l_run = 0.0f;
+      bool ok = true;
+      for (int32_t j = 0; j < T && ok; ++j) {
+        const uint32_t st = uint32_t(j) % kTcStages;
+        ok = __all_sync(0xffffffffu, mbar_wait(&s_full[t], uint32_t(j) & 1));
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t sv[kTcBN];
+#pragma unroll
+        for (int c = 0; c < kTcBN / 32; ++c)
+          tmem_ld32(scol + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&sv[32 * c]));
+        tmem_wait_ld();
+        float x[kTcBN];
+#pragma unroll
+        for (int k = 0; k < kTcBN; ++k) x[k] = __uint_as_float(sv[k]);
+        const int32_t key_base = (t_begin + j) * kTcBN;
+        if (key_base + kTcBN - 1 > pos || key_base < lo) {
+#pragma unroll
+          for (int k = 0; k < kTcBN; ++k)
+            if (key_base + k > pos || key_base + k < lo) x[k] = -INFINITY;
+        }
+        float xm8[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) xm8[q] = x[q];
+#pragma unroll
+        for (int k = 8; k < kTcBN; ++k) xm8[k & 7] = fmaxf(xm8[k & 7], x[k]);
+        const float xm = fmaxf(fmaxf(fmaxf(xm8[0], xm8[1]), fmaxf(xm8[2], xm8[3])),
+                               fmaxf(fmaxf(xm8[4], xm8[5]), fmaxf(xm8[6], xm8[7])));
+        // the row's reference max moves only when the tile max exceeds it
+        // by more than kRescaleLog2 (or on its first finite score)
+        const float tile_max = xm * p.score_scale;
+        const float mx = (m_run == -INFINITY || tile_max > m_run + kRescaleLog2) ? fmaxf(m_run, tile_max) : m_run;
+        const float mb = mx == -INFINITY ? 0.0f : mx;
+        // x * score_scale - mb and the row sum two keys per packed operation
+        const F2 sc2 = f2_make(p.score_scale, p.score_scale), nmb2 = f2_make(-mb, -mb);
+        F2 sum2[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+        for (int k = 0; k < kTcBN / 2; ++k) {
+          const float2 a = f2_split(f2_fma(f2_make(x[2 * k], x[2 * k + 1]), sc2, nmb2));
+          x[2 * k] = fast_exp2(a.x);
+          x[2 * k + 1] = fast_exp2(a.y);
+          sum2[k & 3] = f2_add(sum2[k & 3], f2_make(x[2 * k], x[2 * k + 1]));
+        }
+        const float2 s01 = f2_split(f2_add(f2_add(sum2[0], sum2[1]), f2_add(sum2[2], sum2[3])));
+        const float sum = s01.x + s01.y;
+        const float al = fast_exp2(m_run - mb);
+        const bool rescale = j > 0 && __any_sync(0xffffffffu, mx != m_run);
+        if (rescale) {
+          // O changes only once PV_t(j - 1) is done
+          ok = __all_sync(0xffffffffu, mbar_wait(&o_full[t], uint32_t(j - 1) & 1));
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll 1
+          for (uint32_t c0 = 0; c0 < uint32_t(D); c0 += 32) {
+            uint32_t ov[32];
+            tmem_ld32(ocol + c0, ov);
+            tmem_wait_ld();
+#pragma unroll
+            for (int k = 0; k < 32; ++k) ov[k] = __float_as_uint(__uint_as_float(ov[k]) * al);
+            tmem_st32(ocol + c0, ov);
+          }
+          tmem_wait_st();
+        }
+        l_run = l_run * al + sum;
+        m_run = mx;
+        // the last tile's V rows at or past k_hi: zeroed by tile A's warps
+        // before their P is published, so before either PV product reads them
+        const bool zero_v = t == 0 && key_base + kTcBN > k_hi;
+        if (zero_v) {
+          ok = __all_sync(0xffffffffu, mbar_wait(&v_full[st], (uint32_t(j) / kTcStages) & 1));
+          if (!ok) break;
+          const int32_t z0 = k_hi - key_base > 0 ? k_hi - key_base : 0;
+          uint8_t* vb = smem + Lay::kStage0 + st * Lay::kStageBytes + Lay::kKBytes;
+          const uint32_t units = uint32_t(kTcBN - z0) * kChunks * 8;
+          for (uint32_t e = row; e < units; e += kTcBM) {
+            const uint32_t rr = uint32_t(z0) + e / (kChunks * 8), rest = e % (kChunks * 8);
+            *reinterpret_cast<uint4*>(vb + (rest >> 3) * (kTcBN * 128) + rr * 128 + ((rest & 7) << 4)) =
+                make_uint4(0, 0, 0, 0);
+          }
+        }
+        // P hi / lo over the S columns (truncations, |P - hi - lo| < 2^-15 P):
+        // hi of keys 2m, 2m + 1 in column m, lo in column 64 + m
+#pragma unroll
+        for (int c = 0; c < kTcBN / 32; ++c) {
+          uint32_t hi[16], lw[16];
+#pragma unroll
+          for (int q = 0; q < 16; ++q) {
+            const float x0 = x[32 * c + 2 * q], x1 = x[32 * c + 2 * q + 1];
+            const uint32_t b0 = __float_as_uint(x0), b1 = __float_as_uint(x1);
+            hi[q] = __byte_perm(b0, b1, 0x7632u);
+            const float2 r = f2_split(f2_sub(f2_make(x0, x1), f2_make(__uint_as_float(b0 & 0xffff0000u),
+                                                                       __uint_as_float(b1 & 0xffff0000u))));
+            lw[q] = __byte_perm(__float_as_uint(r.x), __float_as_uint(r.y), 0x7632u);
+          }
+          tmem_st16(scol + 16 * c, hi);
+          tmem_st16(scol + kTcBN / 2 + 16 * c, lw);
+        }
+        tmem_wait_st();
+        if (zero_v) fence_async_smem();
+        tc_fence_before();
+        mbar_arrive(&p_full[t]);
+      }
+      if (!ok && lane == 0) atomicOr(&g_prefill_error, kErrWaitTimeout);
+      // ---- O / l to the output row
+      bool done = __all_sync(0xffffffffu, ok);
+      if (done && T > 0) {
+        done = __all_sync(0xffffffffu, mbar_wait(&o_full[t], uint32_t(T - 1) & 1));
+        tc_fence_after();
+      }
+      const float inv = l_run > 0.0f ? 1.0f / l_run : 0.0f;
+      float* o = valid ? p.output + (uint64_t(it.qstart + tok) * p.num_q_heads + uint64_t(it.kv_head * g + hh)) * D
+                       : nullptr;
+#pragma unroll 1
+      for (uint32_t c0 = 0; c0 < uint32_t(D); c0 += 32) {
+        uint32_t ov[32];
+        if (done && T > 0) {
+          tmem_ld32(ocol + c0, ov);
+          tmem_wait_ld();
+        }
+        if (o && done) {
+#pragma unroll
+          for (int k = 0; k < 32; k += 4) {
+            const float4 w4 = T > 0 ? make_float4(__uint_as_float(ov[k]) * inv, __uint_as_float(ov[k + 1]) * inv,
+                                                  __uint_as_float(ov[k + 2]) * inv, __uint_as_float(ov[k + 3]) * inv)
+                                    : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            *reinterpret_cast<float4*>(o + c0 + k) = w4;
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, Lay::kTmemCols);
+  }
+}
+
+template <int D>
+int launch_prefill_tc2(const PrefillArgs& a, cudaStream_t stream, PrefillParams& p) {
+  CUtensorMap mk, mv;
+  if (!encode_pool_map(&mk, a.k_cache, false, a.num_kv_heads, D, 1, 1) ||
+      !encode_pool_map(&mv, a.v_cache, false, a.num_kv_heads, D, 1, 1))
+    return KV_ERR_CUDA;
+  // grid: an upper bound of the item count, sum over sequences of
+  // ceil(n_s * group / 256) <= num_q_tokens * group / 256 + num_seqs
+  const uint64_t grid =
+      uint64_t(a.num_kv_heads) * ((uint64_t(a.num_q_tokens) * p.group + kTc2Rows - 1) / kTc2Rows + a.num_seqs);
+  if (grid == 0) return KV_OK;
+  if (grid > 0x7fffffffull) return KV_ERR_UNSUPPORTED;
+  // all 512 TMEM columns: no second CTA may be resident on an SM
+  constexpr int kNeed = int(1024 + Tc2Layout<D>::kBytes);
+  const int smem = kNeed > 120 * 1024 ? kNeed : 120 * 1024;
+  auto kern = prefill_tc2_kernel<D>;
+  static int set_bytes[64] = {0};
+  const int dev_id = device_info().device;
+  if (dev_id < 0 || dev_id >= 64) return KV_ERR_CUDA;
+  if (set_bytes[dev_id] < smem) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+      return KV_ERR_CUDA;
+    set_bytes[dev_id] = smem;
+  }
+  kern<<<unsigned(grid), 32 * 12, smem, stream>>>(mk, mv, p);
+  return cudaGetLastError() == cudaSuccess ? KV_OK : KV_ERR_CUDA;
+}
+
 template <int D, bool kFp8, bool kFp8V>
 int launch_prefill_tc(const PrefillArgs& a, cudaStream_t stream, PrefillParams& p) {
   CUtensorMap mk, mv;
@@ -779,8 +1204,8 @@ int launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   p.out_scale = a.fp8_v ? a.v_scale : 1.0f;
   const int key = (a.fp8_v ? 200 : a.fp8 ? 100 : 0) + int(a.head_dim);
   switch (key) {
-    case 64: return launch_prefill_tc<64, false, false>(a, stream, p);  // tcgen05 / TMEM
-    case 128: return launch_prefill_tc<128, false, false>(a, stream, p);
+    case 64: return launch_prefill_tc2<64>(a, stream, p);  // tcgen05 / TMEM, two Q tiles per CTA
+    case 128: return launch_prefill_tc2<128>(a, stream, p);
     case 228: return launch_prefill_tc<128, true, false>(a, stream, p);
     case 328: return launch_prefill_tc<128, true, true>(a, stream, p);
     default: return KV_ERR_UNSUPPORTED;
