@@ -211,7 +211,7 @@ PAGEDKV_API int kv_write_v_only(const kv_bf16_t *value, kv_bf16_t *v_cache, cons
  *   q       device bf16; q_stride (elements between sequences) >= num_q_heads * head_dim.
  *   output  device float32[num_seqs, num_q_heads, head_dim], written.
  *   seq_lens[s] <= max_blocks_per_seq * block_size.
- * Supported: head_dim in {64, 128, 256} (FP8: {128, 256}); block_size a power
+ * Supported: head_dim in {64, 128, 256}; block_size a power
  * of two in [16, 256]; g <= 16; q, caches and q_stride 16-byte aligned;
  * output 8-byte aligned. Anything else returns KV_ERR_UNSUPPORTED.
  * With a workspace registered by kv_set_decode_workspace, the positions of
@@ -265,7 +265,7 @@ PAGEDKV_API int paged_decode_attn_fp8(const kv_bf16_t *q, const kv_e4m3_t *k_cac
  *                    num_q_tokens (a violation sets bit 2 of the device
  *                    fault word and that sequence's rows are skipped).
  *   output           device float32[num_q_tokens, num_q_heads, head_dim].
- * Supported: head_dim 64 or 128 (FP8: 128); block_size a power of two in
+ * Supported: head_dim 64 or 128; block_size a power of two in
  * [16, 256]; q, caches, q_stride and output 16-byte aligned. No workspace
  * is used.
  * ---------------------------------------------------------------------- */

@@ -203,8 +203,7 @@ static int decode_common(const kv_bf16_t* q, const void* k_cache, const void* v_
   if (!isfinite(inv_sqrt_d)) return KV_ERR_INVALID_ARG;
   if (fp8 && (!(k_scale > 0.0f) || !isfinite(k_scale))) return KV_ERR_INVALID_ARG;
   if (fp8_v && (!(v_scale > 0.0f) || !isfinite(v_scale))) return KV_ERR_INVALID_ARG;
-  if (fp8 ? (head_dim != 128 && head_dim != 256) : (head_dim != 64 && head_dim != 128 && head_dim != 256))
-    return KV_ERR_UNSUPPORTED;
+  if (head_dim != 64 && head_dim != 128 && head_dim != 256) return KV_ERR_UNSUPPORTED;
   if (!is_pow2(block_size) || block_size < 16 || block_size > 256) return KV_ERR_UNSUPPORTED;
   if (num_q_heads / num_kv_heads > 16) return KV_ERR_UNSUPPORTED;
   if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || (q_stride * 2u) % 16)
@@ -297,7 +296,7 @@ static int prefill_common(const kv_bf16_t* q, const void* k_cache, const void* v
   if (!isfinite(inv_sqrt_d)) return KV_ERR_INVALID_ARG;
   if (fp8 && (!(k_scale > 0.0f) || !isfinite(k_scale))) return KV_ERR_INVALID_ARG;
   if (fp8_v && (!(v_scale > 0.0f) || !isfinite(v_scale))) return KV_ERR_INVALID_ARG;
-  if (fp8 ? head_dim != 128 : (head_dim != 64 && head_dim != 128)) return KV_ERR_UNSUPPORTED;
+  if (head_dim != 64 && head_dim != 128) return KV_ERR_UNSUPPORTED;
   if (!is_pow2(block_size) || block_size < 16 || block_size > 256) return KV_ERR_UNSUPPORTED;
   if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || (q_stride * 2u) % 16)
     return KV_ERR_UNSUPPORTED;

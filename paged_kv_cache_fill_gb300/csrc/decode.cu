@@ -139,6 +139,26 @@ struct Walker {
   }
 };
 
+// -------------------------------------------------------------- tile layout
+// Shared-memory address of 16-byte unit u of row `row` (a slot) in one head's
+// tile of a stage, whose head rows are RB bytes:
+//   RB a multiple of 128: [128-byte chunk][16 slots][128 B], 128-byte
+//     swizzle (unit u % 8 of chunk u / 8 sits at (u % 8) ^ (row % 8));
+//   RB = 64 (E4M3 rows of head_dim 64): [16 slots][64 B], 64-byte swizzle
+//     (unit u at u ^ ((row / 2) % 4)).
+// Both are what the TMA box of the matching tensor map writes (encode_pool_map)
+// into a 1024-byte-aligned tile, and both keep ldmatrix over 8 rows free of
+// bank conflicts.
+template <int RB>
+__device__ __forceinline__ uint32_t tile_addr(uint32_t head_base, uint32_t row, uint32_t u) {
+  if constexpr (RB == 64) {
+    return head_base + row * 64 + ((u ^ ((row >> 1) & 3)) << 4);
+  } else {
+    static_assert(RB % 128 == 0, "head rows of 64 bytes or whole 128-byte chunks");
+    return head_base + (u >> 3) * (kTile * 128) + row * 128 + (((u & 7) ^ (row & 7)) << 4);
+  }
+}
+
 // -------------------------------------------------------------- O^T += V^T P^T
 // One 16-token tile of the PV product for one warp: acc[i] holds the 16-dim
 // block i of O^T (8 query-head columns). B fragments (bh*, bl*) are the hi and
@@ -156,13 +176,12 @@ template <bool kFp8V, int D, bool kMask>
 __device__ __forceinline__ void pv_tile(float (&acc)[D / 16][4], uint32_t vbase, uint32_t row, uint32_t unit_lo,
                                         uint32_t bh0, uint32_t bh1, uint32_t bl0, uint32_t bl1, uint32_t vmask01,
                                         uint32_t vmask89) {
+  constexpr int kVRow = D * (kFp8V ? 1 : 2);  // bytes of one head's V row
   if constexpr (!kFp8V) {
     uint32_t a[D / 16][4];
 #pragma unroll
     for (int i = 0; i < D / 16; ++i) {
-      const uint32_t chunk = i >> 2;
-      const uint32_t unit = ((i & 3) << 1) + unit_lo;
-      ldmatrix_x4_trans(a[i], vbase + chunk * (kTile * 128) + row * 128 + ((unit ^ (row & 7)) << 4));
+      ldmatrix_x4_trans(a[i], tile_addr<kVRow>(vbase, row, 2 * i + unit_lo));
       if constexpr (kMask) {
         a[i][0] &= vmask01;
         a[i][1] &= vmask01;
@@ -177,10 +196,8 @@ __device__ __forceinline__ void pv_tile(float (&acc)[D / 16][4], uint32_t vbase,
   } else {
 #pragma unroll
     for (int jj = 0; jj < D / 32; ++jj) {
-      const uint32_t chunk = jj >> 2;
-      const uint32_t unit = ((jj & 3) << 1) + unit_lo;
       uint32_t r[4];
-      ldmatrix_x4_trans(r, vbase + chunk * (kTile * 128) + row * 128 + ((unit ^ (row & 7)) << 4));
+      ldmatrix_x4_trans(r, tile_addr<kVRow>(vbase, row, 2 * jj + unit_lo));
       uint32_t a[2][4];
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
@@ -212,8 +229,11 @@ template <bool kFp8, bool kFp8V, int D, int NT>
 __global__ void __launch_bounds__(32 * 9, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                   const DecodeParams p) {
-  constexpr int kKChunks = kFp8 ? D / 128 : D / 64;  // 128-byte chunks per K head row
-  constexpr int kVChunks = kFp8V ? D / 128 : D / 64;
+  constexpr int kKRow = D * (kFp8 ? 1 : 2), kVRow = D * (kFp8V ? 1 : 2);  // bytes of one head's row
+  // the tensor maps' third coordinate per head: 128-byte chunks, or one
+  // 64-byte row (encode_pool_map)
+  constexpr int kKCoord = kKRow >= 128 ? kKRow / 128 : 1;
+  constexpr int kVCoord = kVRow >= 128 ? kVRow / 128 : 1;
   static_assert(kFp8 || !kFp8V, "an FP8 V cache comes with an FP8 K cache");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -324,8 +344,8 @@ __global__ void __launch_bounds__(32 * 9, 1)
             const int32_t slot0 = (block_id << p.block_shift) + ((tile << 4) & int32_t(p.block_size - 1));
 #endif
             const int32_t head0 = int32_t(hg * p.heads_per_item);
-            tma_load_3d(st, &tmap_k, 0, slot0, head0 * kKChunks, &full[stage]);
-            tma_load_3d(st + p.k_bytes, &tmap_v, 0, slot0, head0 * kVChunks, &full[stage]);
+            tma_load_3d(st, &tmap_k, 0, slot0, head0 * kKCoord, &full[stage]);
+            tma_load_3d(st + p.k_bytes, &tmap_v, 0, slot0, head0 * kVCoord, &full[stage]);
             if (flags & kFirst) bulk_load(st + p.k_bytes + p.v_bytes, q_src, q_bytes, &full[stage]);
             issued |= 1u << stage;
             issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
@@ -505,28 +525,24 @@ __global__ void __launch_bounds__(32 * 9, 1)
     }
 
     if (head_ok && !(mt.flags & kEmpty)) {
-      const uint32_t kbase = smem_u32(st) + hl * (kKChunks * kTile * 128);
-      const uint32_t vbase = smem_u32(st + p.k_bytes) + hl * (kVChunks * kTile * 128);
+      const uint32_t kbase = smem_u32(st) + hl * (kTile * kKRow);
+      const uint32_t vbase = smem_u32(st + p.k_bytes) + hl * (kTile * kVRow);
       // ---- S^T = K Q^T (16 tokens x 8 query heads), even and odd k-steps in
       // two accumulators so that consecutive MMAs do not wait on each other
       float s[4] = {0.0f, 0.0f, 0.0f, 0.0f}, s2[4] = {0.0f, 0.0f, 0.0f, 0.0f};
       if constexpr (!kFp8) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t chunk = kk >> 2;
-          const uint32_t unit = ((kk & 3) << 1) + k_unit;
           uint32_t a[4];
-          ldmatrix_x4(a, kbase + chunk * (kTile * 128) + k_row * 128 + ((unit ^ (k_row & 7)) << 4));
+          ldmatrix_x4(a, tile_addr<kKRow>(kbase, k_row, 2 * kk + k_unit));
           if (kk & 1) mma_bf16(s2, a, qf[kk][0], qf[kk][1]);
           else mma_bf16(s, a, qf[kk][0], qf[kk][1]);
         }
       } else {
 #pragma unroll
         for (int jj = 0; jj < D / 32; ++jj) {
-          const uint32_t chunk = jj >> 2;
-          const uint32_t unit = ((jj & 3) << 1) + k_unit;
           uint32_t r[4];
-          ldmatrix_x4(r, kbase + chunk * (kTile * 128) + k_row * 128 + ((unit ^ (k_row & 7)) << 4));
+          ldmatrix_x4(r, tile_addr<kKRow>(kbase, k_row, 2 * jj + k_unit));
           uint32_t a0[4], a1[4];
           a0[0] = e4m3x2_to_f16x2(uint16_t(r[0]));
           a0[1] = e4m3x2_to_f16x2(uint16_t(r[1]));
@@ -791,6 +807,18 @@ bool encode_pool_map(CUtensorMap* map, const void* base, bool fp8, uint32_t num_
   auto encode = get_encode();
   if (!encode) return false;
   const uint32_t elem = fp8 ? 1 : 2;
+  if (head_dim * elem == 64) {
+    // E4M3 rows of head_dim 64: dim 0 a head's 64-byte row, dim 1 the slot,
+    // dim 2 the head (stride 64 bytes); box: one row x 16 slots x the item's
+    // heads, 64-byte swizzled ([head][slot][64 B] in shared memory)
+    cuuint64_t dims[3] = {64, cuuint64_t(1) << 31, num_kv_heads};
+    cuuint64_t strides[2] = {cuuint64_t(num_kv_heads) * 64, 64};
+    cuuint32_t box[3] = {64, kTile, box_chunks ? box_chunks : heads_per_item};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  }
   const uint32_t chunk_elems = 128 / elem;
   const uint32_t chunks_per_head = head_dim * elem / 128;
   cuuint64_t dims[3] = {chunk_elems, cuuint64_t(1) << 31, cuuint64_t(num_kv_heads) * chunks_per_head};
@@ -815,12 +843,11 @@ Geometry geometry(bool fp8, bool fp8_v, uint32_t head_dim, uint32_t num_kv_heads
   g.nt = (group + 7) / 8;
   uint32_t hg = 8 / g.nt;
   if (hg > num_kv_heads) hg = num_kv_heads;
-  const uint32_t kchunks = fp8 ? head_dim / 128 : head_dim / 64;
-  const uint32_t vchunks = fp8_v ? head_dim / 128 : head_dim / 64;
+  const uint32_t krow = head_dim * (fp8 ? 1 : 2), vrow = head_dim * (fp8_v ? 1 : 2);  // bytes per head row
   for (;; hg = (hg + 1) / 2) {
     g.heads_per_item = hg;
-    g.k_bytes = hg * kchunks * kTile * 128;
-    g.v_bytes = hg * vchunks * kTile * 128;
+    g.k_bytes = hg * kTile * krow;
+    g.v_bytes = hg * kTile * vrow;
     const uint32_t q_bytes = (hg * group * head_dim * 2 + 1023) / 1024 * 1024;
     g.stage_bytes = g.k_bytes + g.v_bytes + q_bytes;
     const uint32_t extra = 1024 + 64 * (2 * 8 + 32);  // alignment slack, barriers, meta
@@ -961,10 +988,14 @@ int launch_decode(const DecodeArgs& a, cudaStream_t stream) {
     case 22: return launch_decode_t<false, false, 128, 2>(a, stream, geo, p);
     case 41: return launch_decode_t<false, false, 256, 1>(a, stream, geo, p);
     case 42: return launch_decode_t<false, false, 256, 2>(a, stream, geo, p);
+    case 111: return launch_decode_t<true, false, 64, 1>(a, stream, geo, p);
+    case 112: return launch_decode_t<true, false, 64, 2>(a, stream, geo, p);
     case 121: return launch_decode_t<true, false, 128, 1>(a, stream, geo, p);
     case 122: return launch_decode_t<true, false, 128, 2>(a, stream, geo, p);
     case 141: return launch_decode_t<true, false, 256, 1>(a, stream, geo, p);
     case 142: return launch_decode_t<true, false, 256, 2>(a, stream, geo, p);
+    case 211: return launch_decode_t<true, true, 64, 1>(a, stream, geo, p);
+    case 212: return launch_decode_t<true, true, 64, 2>(a, stream, geo, p);
     case 221: return launch_decode_t<true, true, 128, 1>(a, stream, geo, p);
     case 222: return launch_decode_t<true, true, 128, 2>(a, stream, geo, p);
     case 241: return launch_decode_t<true, true, 256, 1>(a, stream, geo, p);

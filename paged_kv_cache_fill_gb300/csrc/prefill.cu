@@ -44,8 +44,9 @@ struct PrefillParams {
   uint32_t k_box_bytes, v_box_bytes, stage_bytes;
 };
 
-// An E4M3 tile [chunk of 128 dims][128 keys][128 B] -> the f16 tile [chunk of
-// 64 dims][128 keys][128 B], both 128-byte swizzled; rows at or past `live`
+// An E4M3 tile [chunk of 128 dims][128 keys][128 B] (head_dim 64: [128
+// keys][64 B], 64-byte swizzled) -> the f16 tile [chunk of 64 dims][128
+// keys][128 B], 128-byte swizzled; rows at or past `live`
 // become zeros. Exact (every E4M3 value is an f16 value). Lane l takes keys
 // l, l + 32 (first pass) and l + 64, l + 96 (second). Each pass loads its
 // two rows (16 x 16 B) before any store: the stores could alias the loads as
@@ -58,18 +59,25 @@ struct PrefillParams {
 template <int D>
 __device__ __noinline__ void e4m3_tile_to_f16(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst,
                                               int32_t live, uint32_t lane) {
+  constexpr uint32_t kUnits = D < 128 ? D / 16 : 8;  // 16-byte units of a source row per chunk
+  constexpr uint32_t kSrcChunks = (D + 127) / 128;
+  // unit u of key r in source chunk c8
+  auto src_unit = [&](uint32_t c8, uint32_t r, uint32_t u) -> const uint4* {
+    if constexpr (D == 64) return reinterpret_cast<const uint4*>(src + r * 64 + ((u ^ ((r >> 1) & 3)) << 4));
+    else return reinterpret_cast<const uint4*>(src + c8 * (128 * 128) + r * 128 + ((u ^ (r & 7)) << 4));
+  };
 #pragma unroll 1
   for (uint32_t r0 = 0; r0 < 128u; r0 += 64) {
 #pragma unroll
-    for (uint32_t c8 = 0; c8 < uint32_t(D / 128); ++c8) {
-      uint4 w[2][8];
+    for (uint32_t c8 = 0; c8 < kSrcChunks; ++c8) {
+      uint4 w[2][kUnits];
 #pragma unroll
       for (uint32_t k = 0; k < 2; ++k) {
         const uint32_t r = r0 + 32 * k + lane;
         const bool keep = int32_t(r) < live;
 #pragma unroll
-        for (uint32_t u = 0; u < 8; ++u) {
-          w[k][u] = *reinterpret_cast<const uint4*>(src + c8 * (128 * 128) + r * 128 + ((u ^ (r & 7)) << 4));
+        for (uint32_t u = 0; u < kUnits; ++u) {
+          w[k][u] = *src_unit(c8, r, u);
           if (!keep) w[k][u] = make_uint4(0u, 0u, 0u, 0u);
         }
       }
@@ -77,7 +85,7 @@ __device__ __noinline__ void e4m3_tile_to_f16(const uint8_t* __restrict__ src, u
       for (uint32_t k = 0; k < 2; ++k) {
         const uint32_t r = r0 + 32 * k + lane;
 #pragma unroll
-        for (uint32_t u = 0; u < 8; ++u) {  // 16 dims per 16-byte unit
+        for (uint32_t u = 0; u < kUnits; ++u) {  // 16 dims per 16-byte unit
           const uint32_t ws[4] = {w[k][u].x, w[k][u].y, w[k][u].z, w[k][u].w};
           uint32_t h[8];
 #pragma unroll
@@ -202,12 +210,15 @@ struct TcLayout {  // byte offsets from the 1024-aligned shared base
   static constexpr uint32_t kStage0 = 0;
   static constexpr uint32_t kKBytes = kChunks * kTcBN * 128;  // [chunk][128 keys][128 B]
   static constexpr uint32_t kStageBytes = 2 * kKBytes;        // K (f16 when FP8: converted), then V
-  // FP8 K as loaded: [chunk of 128 dims][128 keys][128 B], one ring of stages
-  static constexpr uint32_t kK8Chunks = D / 128;
-  static constexpr uint32_t kK8Bytes = kFp8 ? kK8Chunks * kTcBN * 128 : 0;
+  // FP8 K as loaded, one ring of stages: [chunk of 128 dims][128 keys][128 B]
+  // (128-byte swizzle), or for head_dim 64 [128 keys][64 B] (64-byte
+  // swizzle); kE4Row bytes of a key's row per chunk
+  static constexpr uint32_t kE4Row = D < 128 ? D : 128;
+  static constexpr uint32_t kK8Chunks = (D + 127) / 128;
+  static constexpr uint32_t kK8Bytes = kFp8 ? kK8Chunks * kTcBN * kE4Row : 0;
   static constexpr uint32_t kK80 = kStage0 + kTcStages * kStageBytes;
   // E4M3 V as loaded (same shape as the E4M3 K), one ring of stages
-  static constexpr uint32_t kV8Bytes = kFp8V ? kK8Chunks * kTcBN * 128 : 0;
+  static constexpr uint32_t kV8Bytes = kFp8V ? kK8Chunks * kTcBN * kE4Row : 0;
   static constexpr uint32_t kV80 = kK80 + kTcStages * kK8Bytes;
   static constexpr uint32_t kBytes = kV80 + kTcStages * kV8Bytes;
   // TMEM columns: two S buffers [0, 128), [128, 256), each overwritten by
@@ -352,7 +363,8 @@ __global__ void __launch_bounds__(tc_threads<kFp8>(), 1)
       if (!ok) break;
       const uint32_t loaded = __popc(__ballot_sync(0xffffffffu, mine));
       const uint32_t chunks = e4m3 ? Lay::kK8Chunks : kChunks;
-      if (lane == 0) mbar_arrive_expect_tx(&full[st], loaded * chunks * (kSub * 128));
+      const uint32_t row_bytes = e4m3 ? Lay::kE4Row : 128u;  // of a key's row per box
+      if (lane == 0) mbar_arrive_expect_tx(&full[st], loaded * chunks * (kSub * row_bytes));
       __syncwarp();
       if (mine) {
 #ifdef PAGEDKV_DEBUG_BOUNDS
@@ -364,9 +376,9 @@ __global__ void __launch_bounds__(tc_threads<kFp8>(), 1)
 #endif
         uint8_t* dst = smem + (e4m3 ? (is_k ? Lay::kK80 + st * Lay::kK8Bytes : Lay::kV80 + st * Lay::kV8Bytes)
                                     : Lay::kStage0 + st * Lay::kStageBytes + (is_k ? 0u : Lay::kKBytes)) +
-                       lane * (kSub * 128);
+                       lane * (kSub * row_bytes);
         for (uint32_t c = 0; c < chunks; ++c)
-          tma_load_3d(dst + c * (kTcBN * 128), map, 0, slot0, it.kv_head * chunks + c, &full[st]);
+          tma_load_3d(dst + c * (kTcBN * row_bytes), map, 0, slot0, it.kv_head * chunks + c, &full[st]);
       }
       issued = i + 1;
       if (self_converts && i >= 1) ok = convert_v(i - 1);
@@ -1206,7 +1218,9 @@ int launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   switch (key) {
     case 64: return launch_prefill_tc2<64>(a, stream, p);  // tcgen05 / TMEM, two Q tiles per CTA
     case 128: return launch_prefill_tc2<128>(a, stream, p);
+    case 164: return launch_prefill_tc<64, true, false>(a, stream, p);
     case 228: return launch_prefill_tc<128, true, false>(a, stream, p);
+    case 264: return launch_prefill_tc<64, true, true>(a, stream, p);
     case 328: return launch_prefill_tc<128, true, true>(a, stream, p);
     default: return KV_ERR_UNSUPPORTED;
   }

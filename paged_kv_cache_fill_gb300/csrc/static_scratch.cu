@@ -68,7 +68,7 @@ extern "C" int paged_decode_attn_fp8k_static_scratch(
   if (head_dim == 0 || block_size == 0) return KV_ERR_INVALID_ARG;
   if (uint64_t(q_stride) < uint64_t(num_q_heads) * head_dim) return KV_ERR_INVALID_ARG;
   if (!isfinite(inv_sqrt_d) || !(k_scale > 0.0f) || !isfinite(k_scale)) return KV_ERR_INVALID_ARG;
-  if (head_dim != 128 && head_dim != 256) return KV_ERR_UNSUPPORTED;
+  if (head_dim != 64 && head_dim != 128 && head_dim != 256) return KV_ERR_UNSUPPORTED;
   if (block_size < 16 || block_size > 256 || (block_size & (block_size - 1))) return KV_ERR_UNSUPPORTED;
   if (num_q_heads / num_kv_heads > 16) return KV_ERR_UNSUPPORTED;
   const auto misaligned = [](const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) != 0; };

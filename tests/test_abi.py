@@ -108,7 +108,7 @@ def test_unsupported_shapes(pk):
                                             a["D"], a["bs"], 0.1, 1.0, a["Hq"] * a["D"], 0, None)
         return L.paged_decode_attn_bf16(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, a["mbps"], 2, a["Hq"], a["H"],
                                         a["D"], a["bs"], 0.1, a["Hq"] * a["D"], 0, None)
-    assert dec(D=96) == UNS and dec(fp8=True, D=64) == UNS
+    assert dec(D=96) == UNS and dec(fp8=True, D=96) == UNS and dec(fp8=True, D=512) == UNS
     assert dec(bs=8) == UNS and dec(bs=24) == UNS and dec(bs=512) == UNS
     assert dec(Hq=64, H=2) == UNS            # group of 32 query heads
     misaligned = ctypes.c_void_p(0x10008)
@@ -153,8 +153,7 @@ def test_prefill_zero_work_and_invalid_arguments(pk, kind):
 def test_prefill_unsupported_shapes(pk, kind):
     L, UNS = pk.lib(), pk.KV_ERR_UNSUPPORTED
     assert _prefill(L, kind, D=96, q_stride=32 * 96) == UNS
-    if kind != "bf16":
-        assert _prefill(L, kind, D=64, q_stride=32 * 64) == UNS   # the FP8 prefills take head_dim 128
+    assert _prefill(L, kind, D=256, q_stride=32 * 256) == UNS    # the prefills take head_dim 64 and 128
     assert _prefill(L, kind, bs=8) == UNS and _prefill(L, kind, bs=24) == UNS and _prefill(L, kind, bs=512) == UNS
     misaligned = ctypes.c_void_p(0x10008)
     assert _prefill(L, kind, q=misaligned) == UNS and _prefill(L, kind, out=misaligned) == UNS

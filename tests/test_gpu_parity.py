@@ -481,6 +481,7 @@ CASES = [
     ([300, 77], 12, 1, 128, 256, (0, 50)),
     ([400, 90, 3], 6, 3, 64, 16, (0, 33)),
     ([129, 1500, 16], 32, 2, 128, 16, (0, 200)),     # the largest group (16): two 8-head tiles per KV head
+    ([129, 900, 17, 2000], 32, 2, 64, 16, (0, 100)),  # head_dim 64 with two 8-head tiles per KV head
 ]
 
 
@@ -489,8 +490,6 @@ CASES = [
 @pytest.mark.parametrize("split", [False, True])
 def test_decode_cases(fp8, case, split):
     lens, Hq, H, D, bs, windows = CASES[case]
-    if fp8 and D == 64:
-        pytest.skip("the FP8 decodes support head_dim 128 and 256")
     w = kvgen.custom(100 + case, seq_lens=lens, num_q_heads=Hq, num_kv_heads=H, head_dim=D, block_size=bs,
                      fp8=bool(fp8))
     kc, vc, kr, vr = _caches(w, fp8)
@@ -604,8 +603,6 @@ PREFILL_CASES = [
 @pytest.mark.parametrize("case", range(len(PREFILL_CASES)))
 def test_prefill_cases(fp8, case):
     lens, qlens, Hq, H, D, bs, windows = PREFILL_CASES[case]
-    if fp8 and D != 128:
-        pytest.skip("the FP8 prefills support head_dim 128")
     w = kvgen.custom(200 + case, seq_lens=lens, num_q_heads=Hq, num_kv_heads=H, head_dim=D, block_size=bs,
                      fp8=fp8, q_rows=max(sum(qlens), 1))
     kc, vc, kr, vr = _caches(w, fp8)
