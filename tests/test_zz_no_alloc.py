@@ -107,7 +107,7 @@ def test_static_scratch_decode_matches_the_oracle_and_the_registered_workspace_d
 
 
 def test_static_scratch_refuses_a_shape_larger_than_its_array():
-    # 64 sequences whose tables hold 65,536 positions each could need 272 MB
+    # 64 sequences whose tables hold 65,536 positions each could need 274 MB
     # of split-KV scratch: refused before anything is launched. Every buffer
     # is real and the lengths are zero, so that even a launch would only
     # write zeros to `out`.
