@@ -7,9 +7,9 @@ Cases:
            of them reports a wait that ran out (bit 0), then the default limit
            again and a decode checked against the oracle.
   bounds   a block table holding one block id outside the pool and the slots
-           it gives: slot filling, the BF16, FP8-K and fused K writes and the
-           BF16 decode, each checked against the oracle on everything the bad
-           index does not touch.
+           it gives: slot filling, the BF16, FP8-K and fused K writes, the
+           BF16 decode and the BF16 chunked prefill, each checked against the
+           oracle on everything the bad index does not touch.
 """
 import ctypes
 import json
@@ -179,6 +179,25 @@ def case_bounds():
     got = out.cpu().numpy()
     res["decode_untouched_finite"] = bool(np.isfinite(got[1:]).all())
     res["decode_untouched_abs_err"], res["decode_untouched_rel_err"] = decode_err(got[1:], ref[1:])
+
+    # BF16 chunked prefill over the same caches and the bad table: each
+    # sequence's last positions as queries; sequence 0's rows read block 0
+    # in place of the bad id, the others must match the oracle
+    qlens = [40, 20, 30]
+    qsl = np.concatenate([[0], np.cumsum(qlens)]).astype(np.int32)
+    n_q = int(qsl[-1])
+    qp = torch.randn((n_q, Hq * D), generator=torch.Generator().manual_seed(5)).to(torch.bfloat16)
+    outp = torch.empty((n_q, Hq, D), dtype=torch.float32, device=DEV)
+    pk.paged_prefill_attn_bf16(qp.to(DEV), kg, vg, outp, bad_tables.to(DEV), w.seq_lens.to(DEV),
+                               torch.from_numpy(qsl).to(DEV), w.max_blocks_per_seq, w.num_seqs, n_q, Hq, H, D, bs,
+                               w.inv_sqrt_d, Hq * D, 0)
+    res["prefill"] = device_error_status()
+    refp = oracle.paged_prefill_attn(u16(qp), krg, None, vrg, w.block_tables.numpy(), w.seq_lens.numpy(), qsl,
+                                     w.max_blocks_per_seq, w.num_seqs, Hq, H, D, bs, w.inv_sqrt_d, 1.0, Hq * D, 0)
+    gotp = outp.cpu().numpy()
+    res["prefill_untouched_finite"] = bool(np.isfinite(gotp[qlens[0]:]).all())
+    res["prefill_untouched_abs_err"], res["prefill_untouched_rel_err"] = decode_err(gotp[qlens[0]:],
+                                                                                    refp[qlens[0]:])
     pk.kv_debug_set_pool(0, 0)
     return res
 

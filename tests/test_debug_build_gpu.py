@@ -10,7 +10,8 @@ child process that loads that library alone (tests/debug_build_child.py).
   and the slots it gives. Slot filling flags it; the BF16, FP8-K and fused K
   writes skip those rows (every other pool byte equals the oracle's write of
   the remaining rows); the decode reads block 0 in place of the bad id, and
-  the sequences that do not use it match the oracle. Each step sets bit 3.
+  the sequences that do not use it match the oracle, and so does the BF16
+  chunked prefill's. Each step sets bit 3.
 Nothing here faults, traps or hangs a GPU: every wait is bounded, and no
 access leaves the buffers.
 """
@@ -63,7 +64,7 @@ def test_decode_wait_timeout_returns_flags_and_drains(debug_library):
 def test_out_of_pool_indices_are_flagged_and_skipped(debug_library):
     res = run_child("bounds", debug_library)
     assert res["clean"] == [KV_OK, 0]
-    for step in ("fill", "write_bf16", "write_fp8k", "write_fused", "decode"):
+    for step in ("fill", "write_bf16", "write_fp8k", "write_fused", "decode", "prefill"):
         assert res[step] == [KV_ERR_DEVICE, BIT_OUT_OF_POOL], (step, res[step])
     assert res["write_good"] == [KV_OK, 0]
     assert res["fill_slots_equal"]
@@ -71,3 +72,5 @@ def test_out_of_pool_indices_are_flagged_and_skipped(debug_library):
     assert res["write_fused_ulp"] <= 1
     assert res["decode_untouched_finite"]
     assert res["decode_untouched_abs_err"] <= 2e-3 and res["decode_untouched_rel_err"] <= 1e-2, res
+    assert res["prefill_untouched_finite"]
+    assert res["prefill_untouched_abs_err"] <= 2e-3 and res["prefill_untouched_rel_err"] <= 1e-2, res
