@@ -36,6 +36,7 @@ const DeviceInfo& device_info() {
   if (info.device != d) {
     cudaDeviceGetAttribute(&info.num_sms, cudaDevAttrMultiProcessorCount, d);
     cudaDeviceGetAttribute(&info.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, d);
+    cudaDeviceGetAttribute(&info.max_smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, d);
     cudaDeviceGetAttribute(&info.cc_major, cudaDevAttrComputeCapabilityMajor, d);
     cudaDeviceGetAttribute(&info.cc_minor, cudaDevAttrComputeCapabilityMinor, d);
     info.device = d;

@@ -225,8 +225,17 @@ __device__ __forceinline__ void pv_tile(float (&acc)[D / 16][4], uint32_t vbase,
 }
 
 // -------------------------------------------------------------- the kernel
+// The FP8 K+V variant does 1.5x the per-byte work of the others and is
+// bound by dependent-instruction latency: for head_dim up to 128 and one
+// 8-head tile per KV head it is built to run two CTAs per SM (registers for
+// two, a ring in half the shared memory) where the ring fits
+// (launch_decode); with head_dim 256 or two tiles the accumulators do not
+// fit two CTAs' registers.
+template <bool kFp8V, int D, int NT>
+constexpr bool two_ctas_per_sm() { return kFp8V && D <= 128 && NT == 1; }
+
 template <bool kFp8, bool kFp8V, int D, int NT>
-__global__ void __launch_bounds__(32 * 9, 1)
+__global__ void __launch_bounds__(32 * 9, two_ctas_per_sm<kFp8V, D, NT>() ? 2 : 1)
     decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                   const DecodeParams p) {
   constexpr int kKRow = D * (kFp8 ? 1 : 2), kVRow = D * (kFp8V ? 1 : 2);  // bytes of one head's row
@@ -836,6 +845,7 @@ namespace {
 
 struct Geometry {
   uint32_t heads_per_item, nt, stages, stage_bytes, k_bytes, v_bytes, smem_bytes;
+  uint32_t ctas_per_sm;  // set by launch_decode
 };
 
 Geometry geometry(bool fp8, bool fp8_v, uint32_t head_dim, uint32_t num_kv_heads, uint32_t group, int smem_max) {
@@ -884,7 +894,8 @@ int launch_decode_t(const DecodeArgs& a, cudaStream_t stream, const Geometry& ge
   }
   const DeviceInfo& dev = device_info();
   const uint32_t threads = 32 * (1 + geo.heads_per_item * geo.nt);
-  kern<<<dev.num_sms, threads, geo.smem_bytes, stream>>>(mk, mv, p);
+  if (geo.ctas_per_sm > 1 && !two_ctas_per_sm<kFp8V, D, NT>()) return KV_ERR_CUDA;  // not reached
+  kern<<<dev.num_sms * geo.ctas_per_sm, threads, geo.smem_bytes, stream>>>(mk, mv, p);
   if (cudaGetLastError() != cudaSuccess) return KV_ERR_CUDA;
   if (p.max_splits > 0) {
     dim3 grid(p.num_seqs, p.num_q_heads);
@@ -924,8 +935,22 @@ int launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   const DeviceInfo& dev = device_info();
   const uint32_t group = a.num_q_heads / a.num_kv_heads;
   const bool fp8_v = a.fp8 && a.fp8_v;
-  const Geometry geo = geometry(a.fp8, fp8_v, a.head_dim, a.num_kv_heads, group, dev.max_smem_optin);
+  Geometry geo = geometry(a.fp8, fp8_v, a.head_dim, a.num_kv_heads, group, dev.max_smem_optin);
   if (geo.stages < 2) return KV_ERR_UNSUPPORTED;
+  geo.ctas_per_sm = 1;
+  if (fp8_v && a.head_dim <= 128 && geo.nt == 1) {  // two_ctas_per_sm()
+    // two CTAs per SM when a ring of two or more stages with the same heads
+    // per item fits in half of the SM's shared memory (1 KB of it is
+    // reserved per CTA): 0.957 -> 0.883 ms on the mixed-length FP8 K+V
+    // decode, 1.344 -> 1.248 ms on 128 sequences of 32,768 positions; the
+    // other variants were 1-3% slower so
+    const Geometry half = geometry(a.fp8, fp8_v, a.head_dim, a.num_kv_heads, group,
+                                   dev.max_smem_sm / 2 - 1024 - 256);  // 256: the kernel's static shared memory
+    if (half.stages >= 2 && half.heads_per_item == geo.heads_per_item) {
+      geo = half;
+      geo.ctas_per_sm = 2;
+    }
+  }
 
   DecodeParams p{};
   p.q = a.q;

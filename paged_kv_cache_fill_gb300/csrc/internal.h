@@ -13,6 +13,7 @@ struct DeviceInfo {
   int device = -1;
   int num_sms = 0;
   int max_smem_optin = 0;  // bytes of shared memory a block may opt into
+  int max_smem_sm = 0;     // bytes of shared memory per SM (each resident block also reserves 1 KB)
   int cc_major = 0, cc_minor = 0;
 };
 
