@@ -12,9 +12,10 @@
 // sequence); that re-reads each KV head's bytes once per query head of its
 // group, so it is not followed):
 //   * The unit of work is a 16-token tile of one (sequence, group of HG KV
-//     heads). One persistent CTA per SM. With a workspace (split-KV), the
-//     tiles of all (sequence, head group) pairs form one stream, in sequence
-//     order, which is cut into equal chunks, about one per CTA (stream-K):
+//     heads). One persistent CTA per SM (two for the FP8 K+V variant where
+//     they fit). With a workspace (split-KV), the tiles of all (sequence,
+//     head group) pairs form one stream, in sequence order, which is cut
+//     into equal chunks, about one per CTA (stream-K):
 //     every CTA gets the same number of tiles whatever the length mix, and a
 //     sequence is split only where a chunk boundary falls inside it. Without
 //     one, a CTA takes whole (sequence, head group) items b, b+G, ...
