@@ -377,7 +377,8 @@ PAGEDKV_API int kv_set_decode_workspace(void *device_ptr, size_t bytes);
  *          num_q_tokens (that sequence skipped)
  *   bit 3: (bounds-checking build only) a slot or block id outside the pool
  *          set by kv_debug_set_pool
- *   (bit 0 also covers the prefill pipeline)
+ *   (bit 0 also covers the prefill pipeline and the fused K write's wait
+ *   for its shared-memory copy of the sin/cos table)
  * ---------------------------------------------------------------------- */
 PAGEDKV_API int kv_get_device_error(uint32_t *bits);
 

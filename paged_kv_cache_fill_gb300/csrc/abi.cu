@@ -383,11 +383,12 @@ int kv_set_decode_workspace(void* device_ptr, size_t bytes) {
 int kv_get_device_error(uint32_t* bits) {
   if (!bits) return KV_ERR_INVALID_ARG;
   if (cudaDeviceSynchronize() != cudaSuccess) return KV_ERR_CUDA;
-  uint32_t decode_bits = 0, prefill_bits = 0;
+  uint32_t decode_bits = 0, prefill_bits = 0, fused_bits = 0;
   if (read_and_clear_decode_error(&decode_bits) != cudaSuccess ||
-      read_and_clear_prefill_error(&prefill_bits) != cudaSuccess)
+      read_and_clear_prefill_error(&prefill_bits) != cudaSuccess ||
+      read_and_clear_fused_error(&fused_bits) != cudaSuccess)
     return KV_ERR_CUDA;
-  *bits = decode_bits | prefill_bits;
+  *bits = decode_bits | prefill_bits | fused_bits;
 #ifdef PAGEDKV_DEBUG_BOUNDS
   uint32_t d[4] = {0, 0, 0, 0};
   if (debug_read_and_clear_kv_write(&d[0]) != cudaSuccess || debug_read_and_clear_fused_k(&d[1]) != cudaSuccess ||

@@ -47,6 +47,8 @@
 
 namespace pagedkv {
 
+__device__ uint32_t g_fused_error;
+
 namespace {
 
 struct Dd {
@@ -67,8 +69,9 @@ struct TurnTable {
 };
 
 // sin and cos, as (hi, lo) pairs {sin_hi, sin_lo, cos_hi, cos_lo}, of the
-// angle whose fraction of a turn is pos * G mod 1 (G in units of 2^-96 turn).
-__device__ __forceinline__ float4 turn_sincos(int32_t pos, uint4 g) {
+// angle whose fraction of a turn is pos * G mod 1 (G in units of 2^-96 turn);
+// `table` is the CTA's shared-memory copy of kSinCosTurn.
+__device__ __forceinline__ float4 turn_sincos(int32_t pos, uint4 g, const float4* table) {
   // bits 32..95 of pos * G mod 2^96 (bits 0..31 are below the precision kept)
   const uint32_t pu = uint32_t(pos);
   const uint64_t mid = uint64_t(pu) * g.y + __umulhi(pu, g.x);
@@ -90,7 +93,7 @@ __device__ __forceinline__ float4 turn_sincos(int32_t pos, uint4 g) {
   const float rh = __fmul_rn(th, kTwoPiOver2p32Hi);
   const float rl = fmaf(th, kTwoPiOver2p32Lo, fmaf(tl, kTwoPiOver2p32Hi, fmaf(th, kTwoPiOver2p32Hi, -rh)));
   // {sin_hi, sin_lo, cos_hi, cos_lo} of 2 pi m / 2048
-  const float4 T = __ldg(reinterpret_cast<const float4*>(kSinCosTurn) + m);
+  const float4 T = table[m];
   // cos r = 1 + dh + dl (dh = -rh^2 / 2 exactly), sin r = rh + t
   const float r2 = __fmul_rn(rh, rh);
   const float r2e = fmaf(rh, rh, -r2);
@@ -255,6 +258,19 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) fused_k_norm_rope_kernel
   if (n_items > 0) load_item(0, A);  // the first rows are on their way before the set-up below
 
   __shared__ uint4 s_turn[128];  // turn fractions of the rotation pairs
+  // The sin/cos table in shared memory, one bulk copy per CTA issued now,
+  // beside the first rows. A warp's 32 lookups at unrelated indices cost a
+  // few shared-memory wavefronts here; read through L1 they touched ~32
+  // distinct lines each, which at 4096 tokens was ~2 us of every warp's
+  // first item.
+  __shared__ __align__(128) float4 s_table[sizeof(kSinCosTurn) / sizeof(float4)];
+  __shared__ uint64_t s_table_bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&s_table_bar, 1);
+    fence_mbar_init();
+    mbar_arrive_expect_tx(&s_table_bar, sizeof(kSinCosTurn));
+    bulk_load(s_table, kSinCosTurn, sizeof(kSinCosTurn), &s_table_bar);
+  }
   for (uint32_t i = threadIdx.x; i < half; i += kThreads) s_turn[i] = tt.g[i];
   // the norm weights of this lane's unit, as BF16 pairs
   const uint2 wa = *reinterpret_cast<const uint2*>(k_norm_weight + off_a);
@@ -267,7 +283,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) fused_k_norm_rope_kernel
     sc[k].ch = f2_make(1.0f, 1.0f);
     sc[k].cl = sc[k].sh = sc[k].nsh = sc[k].sl = f2_make(0.0f, 0.0f);
   }
-  __syncthreads();  // s_turn written; no barrier follows
+  __syncthreads();  // s_turn written (and the table's barrier initialised); no barrier follows
+  if (!mbar_wait(&s_table_bar, 0)) {
+    // the copy did not land in time: flag it and let it land (bounded)
+    // before the CTA can release its shared memory
+    if ((threadIdx.x & 31) == 0) atomicOr(&g_fused_error, kErrWaitTimeout);
+    mbar_wait(&s_table_bar, 0);
+    return;
+  }
   if (n_items == 0) return;
 
   auto process = [&](const Item& it) {
@@ -280,7 +303,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) fused_k_norm_rope_kernel
           const uint32_t stream = (4 * l + q) % 3;
           pos = stream == 0 ? it.pos[0] : (stream == 1 ? it.pos[1] : it.pos[2]);
         }
-        v[q] = turn_sincos(pos, s_turn[4 * l + q]);  // {sin_hi, sin_lo, cos_hi, cos_lo}
+        v[q] = turn_sincos(pos, s_turn[4 * l + q], s_table);  // {sin_hi, sin_lo, cos_hi, cos_lo}
       }
 #pragma unroll
       for (int k = 0; k < 2; ++k) {
@@ -454,6 +477,13 @@ cudaError_t launch_fused_k_norm_rope(const uint16_t* k_in, const uint16_t* k_nor
       return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
+}
+
+cudaError_t read_and_clear_fused_error(uint32_t* bits) {
+  uint32_t zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(bits, g_fused_error, sizeof(uint32_t));
+  if (e != cudaSuccess) return e;
+  return cudaMemcpyToSymbol(g_fused_error, &zero, sizeof(uint32_t));
 }
 
 #ifdef PAGEDKV_DEBUG_BOUNDS

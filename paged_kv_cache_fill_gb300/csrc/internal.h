@@ -98,6 +98,9 @@ int launch_decode(const DecodeArgs& a, cudaStream_t stream);
 // The decode kernels' device fault word (read and clear).
 cudaError_t read_and_clear_decode_error(uint32_t* bits);
 
+// The fused K write's device fault word (read and clear).
+cudaError_t read_and_clear_fused_error(uint32_t* bits);
+
 #ifdef PAGEDKV_DEBUG_BOUNDS
 // The bounds-checking build's per-unit pool size and fault word (common.cuh).
 cudaError_t debug_set_pool_kv_write(uint32_t num_blocks, uint32_t block_size);
