@@ -11,12 +11,18 @@
 // the decode: query head h reads KV head h / (num_q_heads / num_kv_heads).
 //
 // GB300 design (tcgen05 / TMEM). Rows are (query token, query head of the
-// KV head's group) pairs, token-major, so one CTA's 128 rows -- the M of one
-// tcgen05.mma -- share every K/V tile it loads. A CTA owns one (sequence, KV
-// head, block of 128 rows) item; items are laid out longest key range first
-// within a sequence, and the grid holds an upper bound of the item count
-// (CTAs past the last item exit at once). The kernel's own comment gives the
-// warp roles, the TMEM map and the barriers.
+// KV head's group) pairs, token-major, so a CTA's rows -- 128 per
+// tcgen05.mma (its M) -- share every K/V tile it loads. Two kernels:
+//   prefill_tc_kernel   one 128-row Q tile per CTA; any cache type; the FP8
+//                       calls run it (their E4M3 rings leave no room for a
+//                       second Q tile);
+//   prefill_tc2_kernel  two 128-row Q tiles per CTA, BF16 caches; the BF16
+//                       calls run it (one tile's products cover the other's
+//                       drain in the tensor pipe).
+// A CTA owns one (sequence, KV head, block of rows) item; items are laid out
+// longest key range first within a sequence, and the grid holds an upper
+// bound of the item count (CTAs past the last item exit at once). Each
+// kernel's own comment gives its warp roles, TMEM map and barriers.
 #include <math.h>
 
 #include "../../include/pagedkv.h"
