@@ -546,6 +546,24 @@ def test_decode_stream_chunks(fp8):
     assert pk.kv_get_device_error() == 0
 
 
+@pytest.mark.parametrize("fp8", [False, True])
+def test_decode_many_short_sequences(fp8):
+    """700 sequences of 0..60 positions (about one in six empty): each chunk
+    of the tile stream spans dozens of sequences, the producer's walk scans
+    sequence counts 32 at a time many times over, and the empty sequences'
+    rows are written as zeros; with and without split-KV and a window."""
+    g = np.random.default_rng(77)
+    lens = [int(x) if x > 9 else 0 for x in g.integers(0, 61, 700)]
+    w = kvgen.custom(32, seq_lens=lens, num_q_heads=16, num_kv_heads=4, head_dim=128, block_size=16, fp8=fp8)
+    kc, vc, kr, vr = _caches(w, fp8)
+    for split in (True, False):
+        with_workspace(w, split)
+        for win in (0, 7):
+            assert_decode_close(_decode_gpu(w, kc, vc, win, fp8), _decode_ref(w, kr, vr, win, fp8),
+                                f"split {split} window {win}")
+    assert pk.kv_get_device_error() == 0
+
+
 def test_decode_clamps_overlong_sequence_and_flags_it():
     w = kvgen.custom(8, seq_lens=[40], num_q_heads=4, num_kv_heads=2, head_dim=128, block_size=16)
     kc, vc, kr, vr = _caches(w, False)
