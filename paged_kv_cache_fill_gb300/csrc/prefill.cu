@@ -14,11 +14,11 @@
 // KV head's group) pairs, token-major, so a CTA's rows -- 128 per
 // tcgen05.mma (its M) -- share every K/V tile it loads. Two kernels:
 //   prefill_tc_kernel   one 128-row Q tile per CTA; any cache type; the FP8
-//                       calls run it (their E4M3 rings leave no room for a
-//                       second Q tile);
-//   prefill_tc2_kernel  two 128-row Q tiles per CTA, BF16 caches; the BF16
-//                       calls run it (one tile's products cover the other's
-//                       drain in the tensor pipe).
+//                       K+V call runs it (its E4M3 V ring leaves no room
+//                       for a second Q tile);
+//   prefill_tc2_kernel  two 128-row Q tiles per CTA, BF16 or E4M3-K caches;
+//                       the BF16 and FP8-K calls run it (one tile's products
+//                       cover the other's drain in the tensor pipe).
 // A CTA owns one (sequence, KV head, block of rows) item; items are laid out
 // longest key range first within a sequence, and the grid holds an upper
 // bound of the item count (CTAs past the last item exit at once). Each
@@ -744,8 +744,9 @@ __global__ void __launch_bounds__(tc_threads<kFp8>(), 1)
   }
 }
 
-// ------------------------------------------------- the two-tile BF16 kernel
-// BF16 caches only. One CTA per (sequence, KV head, block of 256 rows): two
+// ------------------------------------------------- the two-tile kernel
+// BF16 or E4M3-K / BF16-V caches (kFp8). One CTA per (sequence, KV head,
+// block of 256 rows): two
 // 128-row Q tiles, A (rows 0..127) and B (rows 128..255), share every K/V
 // tile the CTA loads. Each Q tile has its own S/P and O in tensor memory
 // (S_A [0, 128), O_A [128, 128 + D), S_B [256, 384), O_B [384, 384 + D)); Q
@@ -763,39 +764,50 @@ __global__ void __launch_bounds__(tc_threads<kFp8>(), 1)
 //                 commit after its last reader has arrived on its empty
 //                 barrier;
 //     warp 1      owns TMEM (all 512 columns) and issues every tcgen05.mma;
-//     warp 3      idle;
+//     warp 3      with an E4M3 K cache: turns each E4M3 K tile, loaded by
+//                 warp 0 into a ring of its own, into the f16 K stage the
+//                 S product reads (exact); otherwise idle;
 //   warpgroups 1, 2 (registers raised to kTc2RegsHigh): the softmax of tile
 //     A and of tile B, one thread per row (TMEM lane) over all 128 keys of a
-//     tile, so no row is shared between threads; they also write the Q rows.
+//     tile, so no row is shared between threads; they also write the Q rows
+//     (with an E4M3 K cache: as f16, the row scaled by a power of two that
+//     the row's score scale undoes, as in the one-tile kernel).
 constexpr int kTc2Rows = 256;
 constexpr uint32_t kTc2RegsLow = 64, kTc2RegsHigh = 216;  // 128 x 64 + 256 x 216 <= 384 x 168 at launch
 
-template <int D>
+template <int D, bool kFp8>
 struct Tc2Layout {  // byte offsets from the 1024-aligned shared base
   static constexpr uint32_t kChunks = D / 64;
   static constexpr uint32_t kQBytes = kChunks * kTcBM * 128;  // one Q tile [chunk][128 rows][128 B]
   static constexpr uint32_t kQ0 = 0;
   static constexpr uint32_t kKBytes = kChunks * kTcBN * 128;  // [chunk][128 keys][128 B]
   static constexpr uint32_t kStage0 = 2 * kQBytes;
-  static constexpr uint32_t kStageBytes = 2 * kKBytes;        // K, then V
-  static constexpr uint32_t kBytes = kStage0 + kTcStages * kStageBytes;
+  static constexpr uint32_t kStageBytes = 2 * kKBytes;        // K (f16 when converted), then V
+  // E4M3 K as loaded, one ring of stages: [chunk of 128 dims][128 keys][128
+  // B], or for head_dim 64 [128 keys][64 B] (kE4Row bytes of a key's row)
+  static constexpr uint32_t kE4Row = D < 128 ? D : 128;
+  static constexpr uint32_t kK8Chunks = (D + 127) / 128;
+  static constexpr uint32_t kK8Bytes = kFp8 ? kK8Chunks * kTcBN * kE4Row : 0;
+  static constexpr uint32_t kK80 = kStage0 + kTcStages * kStageBytes;
+  static constexpr uint32_t kBytes = kK80 + kTcStages * kK8Bytes;
   static constexpr uint32_t kTmemCols = 512;
   // tile t's S/P columns and O columns
   static __device__ __forceinline__ constexpr uint32_t s_col(uint32_t t) { return t << 8; }
   static __device__ __forceinline__ constexpr uint32_t o_col(uint32_t t) { return 128u + (t << 8); }
 };
 
-template <int D>
+template <int D, bool kFp8>
 __global__ void __launch_bounds__(32 * 12, 1)
     prefill_tc2_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                        const PrefillParams p) {
-  using Lay = Tc2Layout<D>;
+  using Lay = Tc2Layout<D, kFp8>;
   constexpr uint32_t kChunks = Lay::kChunks;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
   const uint32_t sbase = smem_u32(smem);
   __shared__ uint64_t k_full[kTcStages], v_full[kTcStages], k_empty[kTcStages], v_empty[kTcStages];
+  __shared__ uint64_t k8_full[kTcStages], k8_empty[kTcStages];  // E4M3 K: loaded, read by the converter
   __shared__ uint64_t s_full[2], p_full[2], o_full[2];  // per Q tile
   __shared__ uint64_t q_full, mma_done;
   __shared__ uint32_t tmem_base_s;
@@ -804,10 +816,12 @@ __global__ void __launch_bounds__(32 * 12, 1)
   const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kTcStages; ++s) {
-      mbar_init(&k_full[s], 1);
+      mbar_init(&k_full[s], kFp8 ? 32 : 1);  // E4M3 K: the converter warp's arrivals
       mbar_init(&v_full[s], 1);
       mbar_init(&k_empty[s], 1);
       mbar_init(&v_empty[s], 1);
+      mbar_init(&k8_full[s], 1);
+      mbar_init(&k8_empty[s], 32);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&s_full[t], 1);
@@ -848,9 +862,12 @@ __global__ void __launch_bounds__(32 * 12, 1)
    if (warp == 0 || warp == 2) {
     // ------------------------------------------------------------ producers
     const bool is_k = warp == 0;
+    const bool e4m3 = kFp8 && is_k;  // E4M3 K lands in its own ring, which the converter reads
     const CUtensorMap* map = is_k ? &tmap_k : &tmap_v;
-    uint64_t* full = is_k ? k_full : v_full;
-    uint64_t* empty = is_k ? k_empty : v_empty;
+    uint64_t* full = is_k ? (kFp8 ? k8_full : k_full) : v_full;
+    uint64_t* empty = is_k ? (kFp8 ? k8_empty : k_empty) : v_empty;
+    const uint32_t chunks = e4m3 ? Lay::kK8Chunks : kChunks;
+    const uint32_t row_bytes = e4m3 ? Lay::kE4Row : 128u;  // of a key's row per box
     tma_prefetch_desc(map);
     const int32_t* table = p.block_tables + uint64_t(it.seq) * p.max_blocks_per_seq;
     bool ok = true;
@@ -866,7 +883,7 @@ __global__ void __launch_bounds__(32 * 12, 1)
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       const uint32_t loaded = __popc(__ballot_sync(0xffffffffu, mine));
-      if (lane == 0) mbar_arrive_expect_tx(&full[st], loaded * kChunks * (kSub * 128));
+      if (lane == 0) mbar_arrive_expect_tx(&full[st], loaded * chunks * (kSub * row_bytes));
       __syncwarp();
       if (mine) {
 #ifdef PAGEDKV_DEBUG_BOUNDS
@@ -875,9 +892,11 @@ __global__ void __launch_bounds__(32 * 12, 1)
 #else
         const int32_t slot0 = (block_id << p.block_shift) + (key0 & int32_t(p.block_size - 1));
 #endif
-        uint8_t* dst = smem + Lay::kStage0 + st * Lay::kStageBytes + (is_k ? 0u : Lay::kKBytes) + lane * (kSub * 128);
-        for (uint32_t c = 0; c < kChunks; ++c)
-          tma_load_3d(dst + c * (kTcBN * 128), map, 0, slot0, it.kv_head * kChunks + c, &full[st]);
+        uint8_t* dst = smem + (e4m3 ? Lay::kK80 + st * Lay::kK8Bytes
+                                    : Lay::kStage0 + st * Lay::kStageBytes + (is_k ? 0u : Lay::kKBytes)) +
+                       lane * (kSub * row_bytes);
+        for (uint32_t c = 0; c < chunks; ++c)
+          tma_load_3d(dst + c * (kTcBN * row_bytes), map, 0, slot0, it.kv_head * chunks + c, &full[st]);
       }
       issued = i + 1;
     }
@@ -887,10 +906,61 @@ __global__ void __launch_bounds__(32 * 12, 1)
       for (int32_t j = issued > kTcStages ? issued - kTcStages : 0; j < issued; ++j)
         mbar_wait(&full[uint32_t(j) % kTcStages], uint32_t(j / kTcStages) & 1);
     }
-  } else if (warp == 1) {
+   } else if (kFp8 && warp == 3) {
+    // ------------------------------------------------------------ E4M3 -> f16
+    // Each loaded E4M3 K tile into the f16 K stage the S products read
+    // (exact: every E4M3 value is an f16 value). The f16 stage is free once
+    // both S products of the tile two back are done (k_empty), the E4M3
+    // stage once this warp has read it (k8_empty). Inline and one key row at
+    // a time: this warpgroup runs on kTc2RegsLow registers.
+    bool ok = true;
+    for (int32_t j = 0; j < T && ok; ++j) {
+      const uint32_t st = uint32_t(j) % kTcStages;
+      ok = __all_sync(0xffffffffu, mbar_wait(&k8_full[st], uint32_t(j / kTcStages) & 1));
+      if (ok && j >= kTcStages)
+        ok = __all_sync(0xffffffffu, mbar_wait(&k_empty[st], uint32_t((j - kTcStages) / kTcStages) & 1));
+      if (!ok) break;
+      const uint8_t* __restrict__ src = smem + Lay::kK80 + st * Lay::kK8Bytes;
+      uint8_t* __restrict__ dst = smem + Lay::kStage0 + st * Lay::kStageBytes;
+      constexpr uint32_t kUnits = Lay::kE4Row / 16;  // 16-byte units of a source row per chunk
+#pragma unroll 1
+      for (uint32_t r = lane; r < uint32_t(kTcBN); r += 32) {
+#pragma unroll
+        for (uint32_t c8 = 0; c8 < Lay::kK8Chunks; ++c8) {
+          uint4 w[kUnits];
+#pragma unroll
+          for (uint32_t u = 0; u < kUnits; ++u) {
+            const uint32_t off = D == 64 ? r * 64 + ((u ^ ((r >> 1) & 3)) << 4)
+                                         : c8 * (kTcBN * 128) + r * 128 + ((u ^ (r & 7)) << 4);
+            w[u] = *reinterpret_cast<const uint4*>(src + off);
+          }
+#pragma unroll
+          for (uint32_t u = 0; u < kUnits; ++u) {  // 16 dims: f16 chunk 2 c8 + u / 4, units 2 (u % 4), + 1
+            const uint32_t ws[4] = {w[u].x, w[u].y, w[u].z, w[u].w};
+            uint32_t h[8];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              h[2 * q] = e4m3x2_to_f16x2(uint16_t(ws[q]));
+              h[2 * q + 1] = e4m3x2_to_f16x2(uint16_t(ws[q] >> 16));
+            }
+            const uint32_t cf = 2 * c8 + (u >> 2), u0 = 2 * (u & 3);
+            uint8_t* drow = dst + cf * (kTcBN * 128) + r * 128;
+            *reinterpret_cast<uint4*>(drow + ((u0 ^ (r & 7)) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
+            *reinterpret_cast<uint4*>(drow + (((u0 + 1) ^ (r & 7)) << 4)) = make_uint4(h[4], h[5], h[6], h[7]);
+          }
+        }
+      }
+      fence_async_smem();
+      mbar_arrive(&k8_empty[st]);
+      mbar_arrive(&k_full[st]);
+    }
+    if (!ok && lane == 0) atomicOr(&g_prefill_error, kErrWaitTimeout);
+   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issue
     if (lane == 0) {
-      constexpr uint32_t idesc_s = umma_idesc_bf16(kTcBM, kTcBN, false);
+      // S: BF16 Q and K, or f16 Q rows scaled by powers of two against K converted to f16
+      constexpr uint32_t idesc_s =
+          kFp8 ? umma_idesc_f16(kTcBM, kTcBN, false) : umma_idesc_bf16(kTcBM, kTcBN, false);
       constexpr uint32_t idesc_o = umma_idesc_bf16(kTcBM, D, true);
       const uint64_t k_desc0 = umma_desc_sw128(sbase + Lay::kStage0, 16, 1024);
       const uint64_t v_desc0 = umma_desc_sw128(sbase + Lay::kStage0 + Lay::kKBytes, kTcBN * 128, 1024);
@@ -984,16 +1054,47 @@ __global__ void __launch_bounds__(32 * 12, 1)
     const int32_t pos = valid ? it.len - it.n + tok : -1;  // -1: attends nothing
     const int32_t lo = W > 0 ? pos + 1 - W : INT32_MIN;
     // the Q row into the tile's shared-memory tile ([chunk][row][128 B],
-    // 128-byte swizzled), zeros past the item
+    // 128-byte swizzled), zeros past the item. E4M3 K cache: the row as f16,
+    // times 2^e with e chosen so that its largest magnitude lies in
+    // [2^14, 2^15) (exact for BF16 values in range), and the row's score
+    // scale rs undoes 2^e.
+    float rs = p.score_scale;
     {
       const uint16_t* qr = valid ? p.q + uint64_t(it.qstart + tok) * p.q_stride + uint64_t(it.kv_head * g + hh) * D
                                  : nullptr;
       uint8_t* qt = smem + Lay::kQ0 + t * Lay::kQBytes;
+      uint4 qv[D / 8];
 #pragma unroll
-      for (uint32_t u = 0; u < D / 8; ++u) {  // 16-byte unit u: chunk u / 8, unit u % 8 of its 128-byte row
-        const uint4 v = qr ? *reinterpret_cast<const uint4*>(qr + 8 * u) : make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4*>(qt + (u >> 3) * (kTcBM * 128) + row * 128 + (((u & 7) ^ (row & 7)) << 4)) = v;
+      for (uint32_t u = 0; u < D / 8; ++u)
+        qv[u] = qr ? *reinterpret_cast<const uint4*>(qr + 8 * u) : make_uint4(0, 0, 0, 0);
+      if constexpr (kFp8) {
+        float amax = 0.0f;
+#pragma unroll
+        for (uint32_t u = 0; u < D / 8; ++u) {
+          const uint32_t w4[4] = {qv[u].x, qv[u].y, qv[u].z, qv[u].w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            amax = fmaxf(amax, fmaxf(fabsf(bf16_lo_to_f32(w4[q])), fabsf(bf16_hi_to_f32(w4[q]))));
+        }
+        int e = 0;
+        if (amax > 0.0f && amax < INFINITY) {
+          int ex;
+          frexpf(amax, &ex);
+          e = 15 - ex;
+        }
+        const float sc = ldexpf(1.0f, e);
+        rs = p.score_scale * ldexpf(1.0f, -e);
+#pragma unroll
+        for (uint32_t u = 0; u < D / 8; ++u) {
+          uint32_t w4[4] = {qv[u].x, qv[u].y, qv[u].z, qv[u].w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) w4[q] = f32x2_to_f16x2(bf16_lo_to_f32(w4[q]) * sc, bf16_hi_to_f32(w4[q]) * sc);
+          qv[u] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+        }
       }
+#pragma unroll
+      for (uint32_t u = 0; u < D / 8; ++u)  // 16-byte unit u: chunk u / 8, unit u % 8 of its 128-byte row
+        *reinterpret_cast<uint4*>(qt + (u >> 3) * (kTcBM * 128) + row * 128 + (((u & 7) ^ (row & 7)) << 4)) = qv[u];
     }
     fence_async_smem();
     mbar_arrive(&q_full);
@@ -1032,11 +1133,11 @@ __global__ void __launch_bounds__(32 * 12, 1)
                                fmaxf(fmaxf(xm8[4], xm8[5]), fmaxf(xm8[6], xm8[7])));
         // the row's reference max moves only when the tile max exceeds it
         // by more than kRescaleLog2 (or on its first finite score)
-        const float tile_max = xm * p.score_scale;
+        const float tile_max = xm * rs;
         const float mx = (m_run == -INFINITY || tile_max > m_run + kRescaleLog2) ? fmaxf(m_run, tile_max) : m_run;
         const float mb = mx == -INFINITY ? 0.0f : mx;
         // x * score_scale - mb and the row sum two keys per packed operation
-        const F2 sc2 = f2_make(p.score_scale, p.score_scale), nmb2 = f2_make(-mb, -mb);
+        const F2 sc2 = f2_make(rs, rs), nmb2 = f2_make(-mb, -mb);
         F2 sum2[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
         for (int k = 0; k < kTcBN / 2; ++k) {
@@ -1141,10 +1242,10 @@ __global__ void __launch_bounds__(32 * 12, 1)
   }
 }
 
-template <int D>
+template <int D, bool kFp8>
 int launch_prefill_tc2(const PrefillArgs& a, cudaStream_t stream, PrefillParams& p) {
   CUtensorMap mk, mv;
-  if (!encode_pool_map(&mk, a.k_cache, false, a.num_kv_heads, D, 1, 1) ||
+  if (!encode_pool_map(&mk, a.k_cache, kFp8, a.num_kv_heads, D, 1, 1) ||
       !encode_pool_map(&mv, a.v_cache, false, a.num_kv_heads, D, 1, 1))
     return KV_ERR_CUDA;
   // grid: an upper bound of the item count, sum over sequences of
@@ -1154,9 +1255,9 @@ int launch_prefill_tc2(const PrefillArgs& a, cudaStream_t stream, PrefillParams&
   if (grid == 0) return KV_OK;
   if (grid > 0x7fffffffull) return KV_ERR_UNSUPPORTED;
   // all 512 TMEM columns: no second CTA may be resident on an SM
-  constexpr int kNeed = int(1024 + Tc2Layout<D>::kBytes);
+  constexpr int kNeed = int(1024 + Tc2Layout<D, kFp8>::kBytes);
   const int smem = kNeed > 120 * 1024 ? kNeed : 120 * 1024;
-  auto kern = prefill_tc2_kernel<D>;
+  auto kern = prefill_tc2_kernel<D, kFp8>;
   static int set_bytes[64] = {0};
   const int dev_id = device_info().device;
   if (dev_id < 0 || dev_id >= 64) return KV_ERR_CUDA;
@@ -1222,10 +1323,10 @@ int launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   p.out_scale = a.fp8_v ? a.v_scale : 1.0f;
   const int key = (a.fp8_v ? 200 : a.fp8 ? 100 : 0) + int(a.head_dim);
   switch (key) {
-    case 64: return launch_prefill_tc2<64>(a, stream, p);  // tcgen05 / TMEM, two Q tiles per CTA
-    case 128: return launch_prefill_tc2<128>(a, stream, p);
-    case 164: return launch_prefill_tc<64, true, false>(a, stream, p);
-    case 228: return launch_prefill_tc<128, true, false>(a, stream, p);
+    case 64: return launch_prefill_tc2<64, false>(a, stream, p);  // tcgen05 / TMEM, two Q tiles per CTA
+    case 128: return launch_prefill_tc2<128, false>(a, stream, p);
+    case 164: return launch_prefill_tc2<64, true>(a, stream, p);
+    case 228: return launch_prefill_tc2<128, true>(a, stream, p);
     case 264: return launch_prefill_tc<64, true, true>(a, stream, p);
     case 328: return launch_prefill_tc<128, true, true>(a, stream, p);
     default: return KV_ERR_UNSUPPORTED;
