@@ -14,11 +14,10 @@
 // KV head's group) pairs, token-major, so a CTA's rows -- 128 per
 // tcgen05.mma (its M) -- share every K/V tile it loads. Two kernels:
 //   prefill_tc_kernel   one 128-row Q tile per CTA; any cache type; the FP8
-//                       K+V call runs it (its E4M3 V ring leaves no room
-//                       for a second Q tile);
-//   prefill_tc2_kernel  two 128-row Q tiles per CTA, BF16 or E4M3-K caches;
-//                       the BF16 and FP8-K calls run it (one tile's products
-//                       cover the other's drain in the tensor pipe).
+//                       K+V call at head_dim 64 runs it;
+//   prefill_tc2_kernel  two 128-row Q tiles per CTA (one tile's products
+//                       cover the other's drain in the tensor pipe); every
+//                       other call runs it.
 // A CTA owns one (sequence, KV head, block of rows) item; items are laid out
 // longest key range first within a sequence, and the grid holds an upper
 // bound of the item count (CTAs past the last item exit at once). Each
@@ -745,8 +744,8 @@ __global__ void __launch_bounds__(tc_threads<kFp8>(), 1)
 }
 
 // ------------------------------------------------- the two-tile kernel
-// BF16 or E4M3-K / BF16-V caches (kFp8). One CTA per (sequence, KV head,
-// block of 256 rows): two
+// BF16, E4M3-K / BF16-V (kFp8) or, for head_dim 128, E4M3 K and V (kFp8V)
+// caches. One CTA per (sequence, KV head, block of 256 rows): two
 // 128-row Q tiles, A (rows 0..127) and B (rows 128..255), share every K/V
 // tile the CTA loads. Each Q tile has its own S/P and O in tensor memory
 // (S_A [0, 128), O_A [128, 128 + D), S_B [256, 384), O_B [384, 384 + D)); Q
@@ -762,7 +761,11 @@ __global__ void __launch_bounds__(tc_threads<kFp8>(), 1)
 //     warp 0      TMA producer of 128-key K tiles, warp 2 of V tiles, each a
 //                 2-stage ring whose stage is free once the MMA thread's
 //                 commit after its last reader has arrived on its empty
-//                 barrier;
+//                 barrier; with an E4M3 V cache warp 2 loads each V tile
+//                 into the upper half of its f16 stage and converts it in
+//                 place before it loads the next (E4M3 row r lies where
+//                 the f16 tile's second chunk puts row r, and a lane reads
+//                 the whole row before it writes);
 //     warp 1      owns TMEM (all 512 columns) and issues every tcgen05.mma;
 //     warp 3      with an E4M3 K cache: turns each E4M3 K tile, loaded by
 //                 warp 0 into a ring of its own, into the f16 K stage the
@@ -776,7 +779,7 @@ constexpr int kTc2Rows = 256;
 constexpr uint32_t kTc2RegsLow = 64, kTc2RegsHigh = 216;  // 128 x 64 + 256 x 216 <= 384 x 168 at launch
 
 template <int D, bool kFp8>
-struct Tc2Layout {  // byte offsets from the 1024-aligned shared base
+struct Tc2Layout {  // (an E4M3 V tile lands inside its f16 V stage: no ring of its own)  // byte offsets from the 1024-aligned shared base
   static constexpr uint32_t kChunks = D / 64;
   static constexpr uint32_t kQBytes = kChunks * kTcBM * 128;  // one Q tile [chunk][128 rows][128 B]
   static constexpr uint32_t kQ0 = 0;
@@ -796,10 +799,12 @@ struct Tc2Layout {  // byte offsets from the 1024-aligned shared base
   static __device__ __forceinline__ constexpr uint32_t o_col(uint32_t t) { return 128u + (t << 8); }
 };
 
-template <int D, bool kFp8>
+template <int D, bool kFp8, bool kFp8V>
 __global__ void __launch_bounds__(32 * 12, 1)
     prefill_tc2_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                        const PrefillParams p) {
+  static_assert(kFp8 || !kFp8V, "an E4M3 V cache comes with an E4M3 K cache");
+  static_assert(!kFp8V || D == 128, "the in-place V conversion needs the 128-dim layout");
   using Lay = Tc2Layout<D, kFp8>;
   constexpr uint32_t kChunks = Lay::kChunks;
   extern __shared__ uint8_t smem_raw[];
@@ -808,6 +813,7 @@ __global__ void __launch_bounds__(32 * 12, 1)
   const uint32_t sbase = smem_u32(smem);
   __shared__ uint64_t k_full[kTcStages], v_full[kTcStages], k_empty[kTcStages], v_empty[kTcStages];
   __shared__ uint64_t k8_full[kTcStages], k8_empty[kTcStages];  // E4M3 K: loaded, read by the converter
+  __shared__ uint64_t v8_full[kTcStages];                        // E4M3 V: loaded
   __shared__ uint64_t s_full[2], p_full[2], o_full[2];  // per Q tile
   __shared__ uint64_t q_full, mma_done;
   __shared__ uint32_t tmem_base_s;
@@ -817,11 +823,12 @@ __global__ void __launch_bounds__(32 * 12, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kTcStages; ++s) {
       mbar_init(&k_full[s], kFp8 ? 32 : 1);  // E4M3 K: the converter warp's arrivals
-      mbar_init(&v_full[s], 1);
+      mbar_init(&v_full[s], kFp8V ? 32 : 1);  // E4M3 V: warp 2's arrivals once converted
       mbar_init(&k_empty[s], 1);
       mbar_init(&v_empty[s], 1);
       mbar_init(&k8_full[s], 1);
       mbar_init(&k8_empty[s], 32);
+      mbar_init(&v8_full[s], 1);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&s_full[t], 1);
@@ -862,17 +869,57 @@ __global__ void __launch_bounds__(32 * 12, 1)
    if (warp == 0 || warp == 2) {
     // ------------------------------------------------------------ producers
     const bool is_k = warp == 0;
-    const bool e4m3 = kFp8 && is_k;  // E4M3 K lands in its own ring, which the converter reads
+    const bool e4m3 = is_k ? kFp8 : kFp8V;  // this tensor's cache holds E4M3 codes
+    const bool self_converts = kFp8V && !is_k;
     const CUtensorMap* map = is_k ? &tmap_k : &tmap_v;
-    uint64_t* full = is_k ? (kFp8 ? k8_full : k_full) : v_full;
+    uint64_t* full = is_k ? (kFp8 ? k8_full : k_full) : (kFp8V ? v8_full : v_full);
     uint64_t* empty = is_k ? (kFp8 ? k8_empty : k_empty) : v_empty;
     const uint32_t chunks = e4m3 ? Lay::kK8Chunks : kChunks;
     const uint32_t row_bytes = e4m3 ? Lay::kE4Row : 128u;  // of a key's row per box
+    // E4M3 V tile j -> its f16 stage, in place; rows at or past the item's
+    // last key (not loaded, or positions past every query) become zeros
+    auto convert_v = [&](int32_t j) -> bool {
+      const uint32_t sj = uint32_t(j) % kTcStages;
+      if (!__all_sync(0xffffffffu, mbar_wait(&v8_full[sj], uint32_t(j / kTcStages) & 1))) return false;
+      uint8_t* vt = smem + Lay::kStage0 + sj * Lay::kStageBytes + Lay::kKBytes;  // [chunk][128 keys][128 B]
+      const int32_t live = k_hi - (t_begin + j) * kTcBN;
+#pragma unroll 1
+      for (uint32_t r = lane; r < uint32_t(kTcBN); r += 32) {
+        uint8_t* row1 = vt + kTcBN * 128 + r * 128;  // the E4M3 row, and the f16 tile's chunk 1 row r
+        uint4 w[8];
+#pragma unroll
+        for (uint32_t u = 0; u < 8; ++u) w[u] = *reinterpret_cast<const uint4*>(row1 + ((u ^ (r & 7)) << 4));
+        if (int32_t(r) >= live) {
+#pragma unroll
+          for (uint32_t u = 0; u < 8; ++u) w[u] = make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (uint32_t u = 0; u < 8; ++u) {  // dims 16 u ..: f16 chunk u / 4, units 2 (u % 4) and + 1
+          const uint32_t ws[4] = {w[u].x, w[u].y, w[u].z, w[u].w};
+          uint32_t h[8];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            h[2 * q] = e4m3x2_to_f16x2(uint16_t(ws[q]));
+            h[2 * q + 1] = e4m3x2_to_f16x2(uint16_t(ws[q] >> 16));
+          }
+          const uint32_t u0 = 2 * (u & 3);
+          uint8_t* drow = vt + (u >> 2) * (kTcBN * 128) + r * 128;
+          *reinterpret_cast<uint4*>(drow + ((u0 ^ (r & 7)) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
+          *reinterpret_cast<uint4*>(drow + (((u0 + 1) ^ (r & 7)) << 4)) = make_uint4(h[4], h[5], h[6], h[7]);
+        }
+      }
+      fence_async_smem();
+      mbar_arrive(&v_full[sj]);
+      return true;
+    };
     tma_prefetch_desc(map);
     const int32_t* table = p.block_tables + uint64_t(it.seq) * p.max_blocks_per_seq;
     bool ok = true;
     int32_t issued = 0;
     for (int32_t i = 0; i < T && ok; ++i) {
+      // E4M3 V: the tile before this one is converted as soon as it has
+      // landed, before this tile's stage is waited for (PV two tiles back)
+      if (self_converts && i >= 1 && !(ok = convert_v(i - 1))) break;
       const uint32_t st = uint32_t(i) % kTcStages;
       const int32_t key0 = (t_begin + i) * kTcBN + int32_t(lane) * kSub;
       const bool mine = lane < uint32_t(kTcBN / kSub) && key0 < k_hi;
@@ -892,14 +939,17 @@ __global__ void __launch_bounds__(32 * 12, 1)
 #else
         const int32_t slot0 = (block_id << p.block_shift) + (key0 & int32_t(p.block_size - 1));
 #endif
-        uint8_t* dst = smem + (e4m3 ? Lay::kK80 + st * Lay::kK8Bytes
-                                    : Lay::kStage0 + st * Lay::kStageBytes + (is_k ? 0u : Lay::kKBytes)) +
+        // E4M3 K: its own ring; E4M3 V: the upper half of its f16 stage
+        uint8_t* dst = smem + (is_k ? (e4m3 ? Lay::kK80 + st * Lay::kK8Bytes : Lay::kStage0 + st * Lay::kStageBytes)
+                                    : Lay::kStage0 + st * Lay::kStageBytes + Lay::kKBytes +
+                                          (e4m3 ? kTcBN * 128u : 0u)) +
                        lane * (kSub * row_bytes);
         for (uint32_t c = 0; c < chunks; ++c)
           tma_load_3d(dst + c * (kTcBN * row_bytes), map, 0, slot0, it.kv_head * chunks + c, &full[st]);
       }
       issued = i + 1;
     }
+    if (self_converts && ok && T > 0) ok = convert_v(T - 1);
     if (!ok) {
       // a wait gave up: let this warp's loads still in flight land (bounded)
       if (lane == 0) atomicOr(&g_prefill_error, kErrWaitTimeout);
@@ -961,7 +1011,8 @@ __global__ void __launch_bounds__(32 * 12, 1)
       // S: BF16 Q and K, or f16 Q rows scaled by powers of two against K converted to f16
       constexpr uint32_t idesc_s =
           kFp8 ? umma_idesc_f16(kTcBM, kTcBN, false) : umma_idesc_bf16(kTcBM, kTcBN, false);
-      constexpr uint32_t idesc_o = umma_idesc_bf16(kTcBM, D, true);
+      // PV: BF16 P parts x BF16 V, or f16 P parts x V converted to f16
+      constexpr uint32_t idesc_o = kFp8V ? umma_idesc_f16(kTcBM, D, true) : umma_idesc_bf16(kTcBM, D, true);
       const uint64_t k_desc0 = umma_desc_sw128(sbase + Lay::kStage0, 16, 1024);
       const uint64_t v_desc0 = umma_desc_sw128(sbase + Lay::kStage0 + Lay::kKBytes, kTcBN * 128, 1024);
       const uint64_t q_desc0 = umma_desc_sw128(sbase + Lay::kQ0, 16, 1024);
@@ -1136,8 +1187,12 @@ __global__ void __launch_bounds__(32 * 12, 1)
         const float tile_max = xm * rs;
         const float mx = (m_run == -INFINITY || tile_max > m_run + kRescaleLog2) ? fmaxf(m_run, tile_max) : m_run;
         const float mb = mx == -INFINITY ? 0.0f : mx;
-        // x * score_scale - mb and the row sum two keys per packed operation
-        const F2 sc2 = f2_make(rs, rs), nmb2 = f2_make(-mb, -mb);
+        // E4M3 V: the weights are formed as 2^7 P (<= 2^15), so that their f16
+        // parts stay above the f16 subnormal range down to P = 2^-21; the sum l
+        // takes the same factor
+        const float mbp = kFp8V ? mb - 7.0f : mb;
+        // x * score_scale - mbp and the row sum two keys per packed operation
+        const F2 sc2 = f2_make(rs, rs), nmb2 = f2_make(-mbp, -mbp);
         F2 sum2[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
         for (int k = 0; k < kTcBN / 2; ++k) {
@@ -1170,7 +1225,7 @@ __global__ void __launch_bounds__(32 * 12, 1)
         m_run = mx;
         // the last tile's V rows at or past k_hi: zeroed by tile A's warps
         // before their P is published, so before either PV product reads them
-        const bool zero_v = t == 0 && key_base + kTcBN > k_hi;
+        const bool zero_v = !kFp8V && t == 0 && key_base + kTcBN > k_hi;  // (E4M3 V: zeroed as converted)
         if (zero_v) {
           ok = __all_sync(0xffffffffu, mbar_wait(&v_full[st], (uint32_t(j) / kTcStages) & 1));
           if (!ok) break;
@@ -1191,11 +1246,20 @@ __global__ void __launch_bounds__(32 * 12, 1)
 #pragma unroll
           for (int q = 0; q < 16; ++q) {
             const float x0 = x[32 * c + 2 * q], x1 = x[32 * c + 2 * q + 1];
-            const uint32_t b0 = __float_as_uint(x0), b1 = __float_as_uint(x1);
-            hi[q] = __byte_perm(b0, b1, 0x7632u);
-            const float2 r = f2_split(f2_sub(f2_make(x0, x1), f2_make(__uint_as_float(b0 & 0xffff0000u),
-                                                                       __uint_as_float(b1 & 0xffff0000u))));
-            lw[q] = __byte_perm(__float_as_uint(r.x), __float_as_uint(r.y), 0x7632u);
+            if constexpr (kFp8V) {
+              // f16 parts: hi the weight truncated to 11 significant bits, lo
+              // the exact remainder rounded to f16 (|P - hi - lo| <= max(2^-21 P, 2^-24))
+              const float h0 = __uint_as_float(__float_as_uint(x0) & 0xffffe000u);
+              const float h1 = __uint_as_float(__float_as_uint(x1) & 0xffffe000u);
+              hi[q] = f32x2_to_f16x2(h0, h1);
+              lw[q] = f32x2_to_f16x2(x0 - h0, x1 - h1);
+            } else {
+              const uint32_t b0 = __float_as_uint(x0), b1 = __float_as_uint(x1);
+              hi[q] = __byte_perm(b0, b1, 0x7632u);
+              const float2 r = f2_split(f2_sub(f2_make(x0, x1), f2_make(__uint_as_float(b0 & 0xffff0000u),
+                                                                         __uint_as_float(b1 & 0xffff0000u))));
+              lw[q] = __byte_perm(__float_as_uint(r.x), __float_as_uint(r.y), 0x7632u);
+            }
           }
           tmem_st16(scol + 16 * c, hi);
           tmem_st16(scol + kTcBN / 2 + 16 * c, lw);
@@ -1212,7 +1276,8 @@ __global__ void __launch_bounds__(32 * 12, 1)
         done = __all_sync(0xffffffffu, mbar_wait(&o_full[t], uint32_t(T - 1) & 1));
         tc_fence_after();
       }
-      const float inv = l_run > 0.0f ? 1.0f / l_run : 0.0f;
+      // (E4M3 V: the PV product summed codes; v_scale dequantises them)
+      const float inv = l_run > 0.0f ? (kFp8V ? p.out_scale : 1.0f) / l_run : 0.0f;
       float* o = valid ? p.output + (uint64_t(it.qstart + tok) * p.num_q_heads + uint64_t(it.kv_head * g + hh)) * D
                        : nullptr;
 #pragma unroll 1
@@ -1242,11 +1307,11 @@ __global__ void __launch_bounds__(32 * 12, 1)
   }
 }
 
-template <int D, bool kFp8>
+template <int D, bool kFp8, bool kFp8V>
 int launch_prefill_tc2(const PrefillArgs& a, cudaStream_t stream, PrefillParams& p) {
   CUtensorMap mk, mv;
   if (!encode_pool_map(&mk, a.k_cache, kFp8, a.num_kv_heads, D, 1, 1) ||
-      !encode_pool_map(&mv, a.v_cache, false, a.num_kv_heads, D, 1, 1))
+      !encode_pool_map(&mv, a.v_cache, kFp8V, a.num_kv_heads, D, 1, 1))
     return KV_ERR_CUDA;
   // grid: an upper bound of the item count, sum over sequences of
   // ceil(n_s * group / 256) <= num_q_tokens * group / 256 + num_seqs
@@ -1257,7 +1322,7 @@ int launch_prefill_tc2(const PrefillArgs& a, cudaStream_t stream, PrefillParams&
   // all 512 TMEM columns: no second CTA may be resident on an SM
   constexpr int kNeed = int(1024 + Tc2Layout<D, kFp8>::kBytes);
   const int smem = kNeed > 120 * 1024 ? kNeed : 120 * 1024;
-  auto kern = prefill_tc2_kernel<D, kFp8>;
+  auto kern = prefill_tc2_kernel<D, kFp8, kFp8V>;
   static int set_bytes[64] = {0};
   const int dev_id = device_info().device;
   if (dev_id < 0 || dev_id >= 64) return KV_ERR_CUDA;
@@ -1323,12 +1388,12 @@ int launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   p.out_scale = a.fp8_v ? a.v_scale : 1.0f;
   const int key = (a.fp8_v ? 200 : a.fp8 ? 100 : 0) + int(a.head_dim);
   switch (key) {
-    case 64: return launch_prefill_tc2<64, false>(a, stream, p);  // tcgen05 / TMEM, two Q tiles per CTA
-    case 128: return launch_prefill_tc2<128, false>(a, stream, p);
-    case 164: return launch_prefill_tc2<64, true>(a, stream, p);
-    case 228: return launch_prefill_tc2<128, true>(a, stream, p);
+    case 64: return launch_prefill_tc2<64, false, false>(a, stream, p);  // tcgen05 / TMEM, two Q tiles per CTA
+    case 128: return launch_prefill_tc2<128, false, false>(a, stream, p);
+    case 164: return launch_prefill_tc2<64, true, false>(a, stream, p);
+    case 228: return launch_prefill_tc2<128, true, false>(a, stream, p);
     case 264: return launch_prefill_tc<64, true, true>(a, stream, p);
-    case 328: return launch_prefill_tc<128, true, true>(a, stream, p);
+    case 328: return launch_prefill_tc2<128, true, true>(a, stream, p);
     default: return KV_ERR_UNSUPPORTED;
   }
 }
