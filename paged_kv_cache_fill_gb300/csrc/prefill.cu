@@ -753,10 +753,12 @@ __global__ void __launch_bounds__(tc_threads<kFp8>(), 1)
 // writes the columns its P occupied, so it must wait until the tile's PV
 // product before it has finished (one thread's tcgen05.mma operations are
 // ordered only for the same accumulator); with one Q tile the tensor pipe
-// drained at every such hand-off. Here the other tile's products are queued
-// behind it: per K/V tile j the MMA thread issues PV_A(j), PV_B(j), then
-// S_A(j + 1) once PV_A(j) is done (PV_B(j) still running), then S_B(j + 1)
-// once PV_B(j) is (S_A(j + 1) running). 384 threads, three warpgroups:
+// idled through that hand-off and the softmax that follows. Here per K/V
+// tile j the MMA thread issues PV_A(j), S_A(j + 1) as soon as PV_A(j) is
+// done, then PV_B(j), and S_B(j + 1) as soon as PV_B(j) is done: while one
+// tile's softmax runs, the other tile's products keep the pipe busy, and a
+// tile's S product never waits behind the other tile's PV product (that
+// order measured slower). 384 threads, three warpgroups:
 //   warpgroup 0 (registers cut to kTc2RegsLow with setmaxnreg):
 //     warp 0      TMA producer of 128-key K tiles, warp 2 of V tiles, each a
 //                 2-stage ring whose stage is free once the MMA thread's
@@ -779,7 +781,8 @@ constexpr int kTc2Rows = 256;
 constexpr uint32_t kTc2RegsLow = 64, kTc2RegsHigh = 216;  // 128 x 64 + 256 x 216 <= 384 x 168 at launch
 
 template <int D, bool kFp8>
-struct Tc2Layout {  // (an E4M3 V tile lands inside its f16 V stage: no ring of its own)  // byte offsets from the 1024-aligned shared base
+struct Tc2Layout {  // byte offsets from the 1024-aligned shared base; an E4M3 V tile lands
+                    // inside its f16 V stage and needs no ring of its own
   static constexpr uint32_t kChunks = D / 64;
   static constexpr uint32_t kQBytes = kChunks * kTcBM * 128;  // one Q tile [chunk][128 rows][128 B]
   static constexpr uint32_t kQ0 = 0;
