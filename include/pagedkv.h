@@ -265,6 +265,13 @@ PAGEDKV_API int paged_decode_attn_fp8(const kv_bf16_t *q, const kv_e4m3_t *k_cac
  *                    num_q_tokens (a violation sets bit 2 of the device
  *                    fault word and that sequence's rows are skipped).
  *   output           device float32[num_q_tokens, num_q_heads, head_dim].
+ * Precision: scores and sums in fp32; the PV product takes the softmax
+ * weights as f16 (one rounding, relative error at most 2^-11; the FP8 K and
+ * V call at head_dim 64 takes them as two f16 parts) against V as f16: E4M3
+ * codes exactly, BF16 values as v * 2^-8 rounded to f16, exact for
+ * 2^-6 <= |v| < 2^24 and within 2^-17 below. BF16 V values of magnitude
+ * 2^24 or more are outside the supported range (the outputs that weigh them
+ * are not finite).
  * Supported: head_dim 64 or 128; block_size a power of two in
  * [16, 256]; q, caches, q_stride and output 16-byte aligned. No workspace
  * is used.
@@ -288,7 +295,7 @@ PAGEDKV_API int paged_prefill_attn_fp8k(const kv_bf16_t *q, const kv_e4m3_t *k_c
 /* Multi-token paged attention over an FP8 K and V cache (the cache that
  * kv_write_fp8 fills and paged_decode_attn_fp8 reads): as
  * paged_prefill_attn_fp8k, with v_p = E4M3 code * v_scale (v_scale finite and
- * > 0) read from a uint8 V pool. head_dim 128. */
+ * > 0) read from a uint8 V pool. head_dim 64 or 128. */
 PAGEDKV_API int paged_prefill_attn_fp8(const kv_bf16_t *q, const kv_e4m3_t *k_cache_fp8,
                                        const kv_e4m3_t *v_cache_fp8, float *output, const int32_t *block_tables,
                                        const int32_t *seq_lens, const int32_t *query_start_loc,

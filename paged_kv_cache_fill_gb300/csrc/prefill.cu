@@ -18,10 +18,11 @@
 //   prefill_tc2_kernel  two 128-row Q tiles per CTA (one tile's products
 //                       cover the other's drain in the tensor pipe); every
 //                       other call runs it.
-// A CTA owns one (sequence, KV head, block of rows) item; items are laid out
-// longest key range first within a sequence, and the grid holds an upper
-// bound of the item count (CTAs past the last item exit at once). Each
-// kernel's own comment gives its warp roles, TMEM map and barriers.
+// A CTA owns one (sequence, KV head, block of rows) item; items run
+// longest key range first across all sequences (by a length class of each
+// sequence's key range), and the grid holds an upper bound of the item count
+// (CTAs past the last item exit at once). Each kernel's own comment gives
+// its warp roles, TMEM map and barriers.
 #include <math.h>
 
 #include "../../include/pagedkv.h"
@@ -34,6 +35,7 @@ __device__ uint32_t g_prefill_error;
 namespace {
 
 constexpr int kSub = 16;                // keys per TMA box
+constexpr int kTcBM = 128, kTcBN = 128, kTcStages = 2;  // rows per Q tile, keys per K/V tile, ring stages
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct PrefillParams {
@@ -119,24 +121,95 @@ __device__ __forceinline__ uint32_t row_blocks(int64_t n, uint32_t group) {
   return uint32_t((n * group + BM - 1) / BM);
 }
 
-// The item of CTA `target` (seq < 0: none), items of BM rows. Run by one warp.
+// Items run longest key range first across all sequences (a CTA launched
+// late then runs a short item, so the last wave ends evenly): the order is
+// by length class of the sequence's key range, descending, then by
+// sequence, then by row block (the last block, with the most keys, first).
+// Classes are log-linear in 128-key tiles, eight per octave, so items of one
+// class differ in length by at most 1/8.
+constexpr uint32_t kLenClasses = 128;
+
+__device__ __forceinline__ uint32_t len_class(uint64_t tiles) {
+  if (tiles == 0) return 0;
+  const uint32_t msb = 63 - __clzll(tiles);
+  const uint32_t frac = uint32_t(msb >= 3 ? tiles >> (msb - 3) : tiles << (3 - msb)) & 7u;
+  const uint32_t c = msb * 8 + frac;
+  return c < kLenClasses ? c : kLenClasses - 1;
+}
+
+// Sequence s's share of the item list: its query tokens n, its items (row
+// blocks x KV heads) and the length class of its queries' key range.
+// A bad query layout counts as no queries (flagged once, by the caller's
+// first pass).
 template <int BM>
-__device__ Item locate(uint32_t target, const PrefillParams& p, uint32_t lane) {
+__device__ __forceinline__ uint32_t seq_items(const PrefillParams& p, uint32_t s, bool flag, int64_t& n,
+                                              uint32_t& cls) {
+  n = 0;
+  cls = 0;
+  if (s >= p.num_seqs) return 0;
+  const int32_t a = __ldg(p.qsl + s), b = __ldg(p.qsl + s + 1);
+  n = int64_t(b) - a;
+  if (a < 0 || n < 0 || uint32_t(b) > p.num_q_tokens) {
+    if (flag) atomicOr(&g_prefill_error, kErrQueryLayout);
+    n = 0;
+  }
+  int64_t L = __ldg(p.seq_lens + s);
+  const int64_t cap = int64_t(p.max_blocks_per_seq) << p.block_shift;
+  L = L < 0 ? 0 : (L > cap ? cap : L);
+  int64_t k_lo = 0;
+  if (p.sliding_window > 0 && L - n + 1 - int64_t(p.sliding_window) > 0) k_lo = L - n + 1 - p.sliding_window;
+  const int64_t tiles = (L + kTcBN - 1) / kTcBN - k_lo / kTcBN;
+  cls = len_class(tiles > 0 ? uint64_t(tiles) : 0);
+  return row_blocks<BM>(n, p.group) * p.num_kv_heads;
+}
+
+// The item of CTA `target` (seq < 0: none), items of BM rows. Run by one
+// warp; `hist` is kLenClasses words of scratch shared memory.
+template <int BM>
+__device__ Item locate(uint32_t target, const PrefillParams& p, uint32_t lane, uint32_t* hist) {
   Item it{};
   it.seq = -1;
-  uint64_t base = 0;
+  for (uint32_t c = lane; c < kLenClasses; c += 32) hist[c] = 0;
+  __syncwarp();
+  // items per length class
+  for (uint32_t s = lane; s < p.num_seqs; s += 32) {
+    int64_t n;
+    uint32_t cls;
+    const uint32_t items = seq_items<BM>(p, s, true, n, cls);
+    if (items) atomicAdd(&hist[cls], items);
+  }
+  __syncwarp();
+  // the class that holds item `target`, longest class first (lane l of a
+  // round takes class c0 + 31 - l)
+  uint64_t before = 0;
+  int32_t cls_t = -1;
+  for (int32_t c0 = int32_t(kLenClasses) - 32; c0 >= 0 && cls_t < 0; c0 -= 32) {
+    const uint32_t cnt = hist[uint32_t(c0) + 31 - lane];
+    uint32_t incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= uint32_t(o)) incl += v;
+    }
+    const uint32_t total = __shfl_sync(0xffffffffu, incl, 31);
+    if (uint64_t(target) < before + total) {
+      const uint32_t rel = uint32_t(target - before);
+      const uint32_t sl = __ffs(__ballot_sync(0xffffffffu, incl > rel)) - 1;
+      cls_t = c0 + 31 - int32_t(sl);
+      before += __shfl_sync(0xffffffffu, incl, sl) - __shfl_sync(0xffffffffu, cnt, sl);
+    } else {
+      before += total;
+    }
+  }
+  if (cls_t < 0) return it;
+  // the sequence of that class, in sequence order, that holds it
+  uint64_t rel = uint64_t(target) - before;
   for (uint32_t s0 = 0; s0 < p.num_seqs; s0 += 32) {
     const uint32_t s = s0 + lane;
-    int64_t n = 0;
-    if (s < p.num_seqs) {
-      const int32_t a = __ldg(p.qsl + s), b = __ldg(p.qsl + s + 1);
-      n = int64_t(b) - a;
-      if (a < 0 || n < 0 || uint32_t(b) > p.num_q_tokens) {
-        atomicOr(&g_prefill_error, kErrQueryLayout);
-        n = 0;
-      }
-    }
-    const uint32_t items = row_blocks<BM>(n, p.group) * p.num_kv_heads;
+    int64_t n;
+    uint32_t cls;
+    uint32_t items = seq_items<BM>(p, s, false, n, cls);
+    if (int32_t(cls) != cls_t) items = 0;
     uint32_t incl = items;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -144,10 +217,10 @@ __device__ Item locate(uint32_t target, const PrefillParams& p, uint32_t lane) {
       if (lane >= uint32_t(o)) incl += v;
     }
     const uint32_t total = __shfl_sync(0xffffffffu, incl, 31);
-    if (uint64_t(target) < base + total) {
-      const uint32_t rel = uint32_t(target - base);
-      const uint32_t sl = __ffs(__ballot_sync(0xffffffffu, incl > rel)) - 1;
-      const uint32_t local = rel - (__shfl_sync(0xffffffffu, incl, sl) - __shfl_sync(0xffffffffu, items, sl));
+    if (rel < total) {
+      const uint32_t sl = __ffs(__ballot_sync(0xffffffffu, incl > uint32_t(rel))) - 1;
+      const uint32_t local =
+          uint32_t(rel) - (__shfl_sync(0xffffffffu, incl, sl) - __shfl_sync(0xffffffffu, items, sl));
       const int64_t ns = __shfl_sync(0xffffffffu, n, sl);
       const uint32_t nblk = row_blocks<BM>(ns, p.group);
       const uint32_t blk = nblk - 1 - local / p.num_kv_heads;  // longest key range first
@@ -168,7 +241,7 @@ __device__ Item locate(uint32_t target, const PrefillParams& p, uint32_t lane) {
       it.len = L;
       return it;
     }
-    base += total;
+    rel -= total;
   }
   return it;
 }
@@ -203,7 +276,6 @@ __device__ Item locate(uint32_t target, const PrefillParams& p, uint32_t lane) {
 //               (the PV MMA reads its A operand from tensor memory, sparing
 //               shared-memory bandwidth), and at the end O / l to the output.
 // S of tile i + 1 is computed while the softmax works on tile i.
-constexpr int kTcBM = 128, kTcBN = 128, kTcStages = 2;
 constexpr uint32_t kVWarp = 10, kConvWarp = 11;  // V producer (and E4M3 V converter); FP8 K converter
 template <bool kFp8>
 constexpr int tc_threads() { return 32 * (kFp8 ? 12 : 11); }
@@ -285,7 +357,7 @@ __global__ void __launch_bounds__(tc_threads<kFp8>(), 1)
     fence_mbar_init();
   }
   if (warp == 0) {
-    const Item it = locate<kTcBM>(blockIdx.x, p, lane);
+    const Item it = locate<kTcBM>(blockIdx.x, p, lane, reinterpret_cast<uint32_t*>(smem));  // (free until the Q rows)
     if (lane == 0) s_item = it;
   }
   __syncthreads();
@@ -758,7 +830,12 @@ __global__ void __launch_bounds__(tc_threads<kFp8>(), 1)
 // done, then PV_B(j), and S_B(j + 1) as soon as PV_B(j) is done: while one
 // tile's softmax runs, the other tile's products keep the pipe busy, and a
 // tile's S product never waits behind the other tile's PV product (that
-// order measured slower). 384 threads, three warpgroups:
+// order measured slower).
+// The PV product is one f16 x f16 product: the weights as one f16 rounding
+// of 2^7 P (relative error <= 2^-11), every V tile converted to f16 in
+// shared memory before it (E4M3 codes exactly; BF16 values times 2^-8,
+// exact for 2^-6 <= |v| < 2^24, which the output scale undoes). 384
+// threads, three warpgroups:
 //   warpgroup 0 (registers cut to kTc2RegsLow with setmaxnreg):
 //     warp 0      TMA producer of 128-key K tiles, warp 2 of V tiles, each a
 //                 2-stage ring whose stage is free once the MMA thread's
@@ -776,7 +853,11 @@ __global__ void __launch_bounds__(tc_threads<kFp8>(), 1)
 //     A and of tile B, one thread per row (TMEM lane) over all 128 keys of a
 //     tile, so no row is shared between threads; they also write the Q rows
 //     (with an E4M3 K cache: as f16, the row scaled by a power of two that
-//     the row's score scale undoes, as in the one-tile kernel).
+//     the row's score scale undoes, as in the one-tile kernel) and, with a
+//     BF16 V cache, convert V tile j + 1 in place (each warpgroup half of
+//     it) right after publishing their P of tile j, off the path of that
+//     tile's PV product (one warp converting a whole tile per cycle became
+//     the serial path).
 constexpr int kTc2Rows = 256;
 constexpr uint32_t kTc2RegsLow = 64, kTc2RegsHigh = 216;  // 128 x 64 + 256 x 216 <= 384 x 168 at launch
 
@@ -826,7 +907,7 @@ __global__ void __launch_bounds__(32 * 12, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kTcStages; ++s) {
       mbar_init(&k_full[s], kFp8 ? 32 : 1);  // E4M3 K: the converter warp's arrivals
-      mbar_init(&v_full[s], kFp8V ? 32 : 1);  // E4M3 V: warp 2's arrivals once converted
+      mbar_init(&v_full[s], kFp8V ? 32 : 8);  // once the tile is f16: warp 2's lanes, or the softmax warps
       mbar_init(&k_empty[s], 1);
       mbar_init(&v_empty[s], 1);
       mbar_init(&k8_full[s], 1);
@@ -843,7 +924,7 @@ __global__ void __launch_bounds__(32 * 12, 1)
     fence_mbar_init();
   }
   if (warp == 0) {
-    const Item it = locate<kTc2Rows>(blockIdx.x, p, lane);
+    const Item it = locate<kTc2Rows>(blockIdx.x, p, lane, reinterpret_cast<uint32_t*>(smem));  // (free until the Q rows)
     if (lane == 0) s_item = it;
   }
   __syncthreads();
@@ -875,7 +956,7 @@ __global__ void __launch_bounds__(32 * 12, 1)
     const bool e4m3 = is_k ? kFp8 : kFp8V;  // this tensor's cache holds E4M3 codes
     const bool self_converts = kFp8V && !is_k;
     const CUtensorMap* map = is_k ? &tmap_k : &tmap_v;
-    uint64_t* full = is_k ? (kFp8 ? k8_full : k_full) : (kFp8V ? v8_full : v_full);
+    uint64_t* full = is_k ? (kFp8 ? k8_full : k_full) : v8_full;  // V: converted before v_full
     uint64_t* empty = is_k ? (kFp8 ? k8_empty : k_empty) : v_empty;
     const uint32_t chunks = e4m3 ? Lay::kK8Chunks : kChunks;
     const uint32_t row_bytes = e4m3 ? Lay::kE4Row : 128u;  // of a key's row per box
@@ -1014,8 +1095,8 @@ __global__ void __launch_bounds__(32 * 12, 1)
       // S: BF16 Q and K, or f16 Q rows scaled by powers of two against K converted to f16
       constexpr uint32_t idesc_s =
           kFp8 ? umma_idesc_f16(kTcBM, kTcBN, false) : umma_idesc_bf16(kTcBM, kTcBN, false);
-      // PV: BF16 P parts x BF16 V, or f16 P parts x V converted to f16
-      constexpr uint32_t idesc_o = kFp8V ? umma_idesc_f16(kTcBM, D, true) : umma_idesc_bf16(kTcBM, D, true);
+      // PV: f16 P x V converted to f16
+      constexpr uint32_t idesc_o = umma_idesc_f16(kTcBM, D, true);
       const uint64_t k_desc0 = umma_desc_sw128(sbase + Lay::kStage0, 16, 1024);
       const uint64_t v_desc0 = umma_desc_sw128(sbase + Lay::kStage0 + Lay::kKBytes, kTcBN * 128, 1024);
       const uint64_t q_desc0 = umma_desc_sw128(sbase + Lay::kQ0, 16, 1024);
@@ -1063,12 +1144,11 @@ __global__ void __launch_bounds__(32 * 12, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t pt = tmem + Lay::s_col(t);  // P of tile t: hi, then lo
+          const uint32_t pt = tmem + Lay::s_col(t);  // P of tile t: keys 2m, 2m + 1 in column m
 #pragma unroll
           for (int kk = 0; kk < kTcBN / 16; ++kk) {
             const uint64_t v_k = vd + uint64_t(kk * (16 * 128) >> 4);
             umma_f16kind_tmem_a(tmem + Lay::o_col(t), pt + 8 * kk, v_k, idesc_o, j > 0 || kk > 0);
-            umma_f16kind_tmem_a(tmem + Lay::o_col(t), pt + kTcBN / 2 + 8 * kk, v_k, idesc_o, true);
           }
           umma_commit(&o_full[t]);
           if (t + 1 == ntiles) umma_commit(&v_empty[st]);
@@ -1157,10 +1237,61 @@ __global__ void __launch_bounds__(32 * 12, 1)
     } else {
       const uint32_t scol = tmem + lane_addr + Lay::s_col(t);
       const uint32_t ocol = tmem + lane_addr + Lay::o_col(t);
+      // BF16 V tile j -> f16 in place, this warpgroup's half of it (tile A's
+      // warps take both halves when tile B holds no rows): each value times
+      // 2^-8, rounded to f16 (exact for 2^-6 <= |v| < 2^24, within 2^-17
+      // absolute below; the output scale undoes 2^-8). Rows at or past the
+      // item's last key (not loaded, or positions past every query) become
+      // zeros. Elementwise, so the swizzle does not matter: 16-byte unit e of
+      // the tile ([chunk][128 keys][128 B]) holds key row (e / 8) % 128, and
+      // a warp's access covers 32 consecutive units.
+      auto convert_v_half = [&](int32_t j, uint32_t h) -> bool {
+        constexpr uint32_t kHalf = uint32_t(kTcBN) * kChunks * 4;  // units per half
+        constexpr uint32_t kPer = kHalf / kTcBM;                    // per thread
+        const uint32_t sj = uint32_t(j) % kTcStages;
+        if (!__all_sync(0xffffffffu, mbar_wait(&v8_full[sj], uint32_t(j / kTcStages) & 1))) return false;
+        uint4* units = reinterpret_cast<uint4*>(smem + Lay::kStage0 + sj * Lay::kStageBytes + Lay::kKBytes);
+        const int32_t live = k_hi - (t_begin + j) * kTcBN;
+        const F2 down = f2_make(0.00390625f, 0.00390625f);
+        constexpr uint32_t kPass = kPer < 4 ? kPer : 4;  // units per pass
+#pragma unroll 1
+        for (uint32_t u0 = 0; u0 < kPer; u0 += kPass) {
+          uint4 w[kPass];
+#pragma unroll
+          for (uint32_t u = 0; u < kPass; ++u) w[u] = units[h * kHalf + (u0 + u) * kTcBM + row];
+#pragma unroll
+          for (uint32_t u = 0; u < kPass; ++u) {
+            uint32_t ws[4] = {w[u].x, w[u].y, w[u].z, w[u].w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const float2 f = f2_split(
+                  f2_mul(f2_make(__uint_as_float(ws[q] << 16), __uint_as_float(ws[q] & 0xffff0000u)), down));
+              ws[q] = f32x2_to_f16x2(f.x, f.y);
+            }
+            w[u] = make_uint4(ws[0], ws[1], ws[2], ws[3]);
+          }
+          if (live < kTcBN) {  // the item's last tile
+#pragma unroll
+            for (uint32_t u = 0; u < kPass; ++u)
+              if (int32_t(((h * kHalf + (u0 + u) * kTcBM + row) >> 3) % uint32_t(kTcBN)) >= live)
+                w[u] = make_uint4(0, 0, 0, 0);
+          }
+#pragma unroll
+          for (uint32_t u = 0; u < kPass; ++u) units[h * kHalf + (u0 + u) * kTcBM + row] = w[u];
+        }
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&v_full[sj]);
+        return true;
+      };
+      auto convert_v = [&](int32_t j) -> bool {
+        if constexpr (kFp8V) return true;  // E4M3 V: converted by the V producer warp
+        if (!convert_v_half(j, t)) return false;
+        return two || convert_v_half(j, 1);
+      };
       float m_run = -INFINITY, l_run = 0.0f;
-      bool ok = true;
+      bool ok = T == 0 || convert_v(0);
       for (int32_t j = 0; j < T && ok; ++j) {
-        const uint32_t st = uint32_t(j) % kTcStages;
         ok = __all_sync(0xffffffffu, mbar_wait(&s_full[t], uint32_t(j) & 1));
         if (!ok) break;
         tc_fence_after();
@@ -1190,20 +1321,28 @@ __global__ void __launch_bounds__(32 * 12, 1)
         const float tile_max = xm * rs;
         const float mx = (m_run == -INFINITY || tile_max > m_run + kRescaleLog2) ? fmaxf(m_run, tile_max) : m_run;
         const float mb = mx == -INFINITY ? 0.0f : mx;
-        // E4M3 V: the weights are formed as 2^7 P (<= 2^15), so that their f16
-        // parts stay above the f16 subnormal range down to P = 2^-21; the sum l
-        // takes the same factor
-        const float mbp = kFp8V ? mb - 7.0f : mb;
-        // x * score_scale - mbp and the row sum two keys per packed operation
+        // the weights are formed as 2^7 P (<= 2^15), so that they stay above
+        // f16's subnormal range down to P = 2^-21; the sum l takes the same
+        // factor
+        const float mbp = mb - 7.0f;
+        // x * score_scale - mbp and the row sum two keys per packed operation;
+        // each pair of weights goes to f16 as soon as it is formed (|P - P16|
+        // <= 2^-11 P above 2^-21 P, the weights being 2^7 P), so that only the
+        // 64 packed words stay live
         const F2 sc2 = f2_make(rs, rs), nmb2 = f2_make(-mbp, -mbp);
         F2 sum2[4] = {0ull, 0ull, 0ull, 0ull};
+        uint32_t pw[kTcBN / 2];
 #pragma unroll
         for (int k = 0; k < kTcBN / 2; ++k) {
           const float2 a = f2_split(f2_fma(f2_make(x[2 * k], x[2 * k + 1]), sc2, nmb2));
-          x[2 * k] = fast_exp2(a.x);
-          x[2 * k + 1] = fast_exp2(a.y);
-          sum2[k & 3] = f2_add(sum2[k & 3], f2_make(x[2 * k], x[2 * k + 1]));
+          const float e0 = fast_exp2(a.x), e1 = fast_exp2(a.y);
+          sum2[k & 3] = f2_add(sum2[k & 3], f2_make(e0, e1));
+          pw[k] = f32x2_to_f16x2(e0, e1);
         }
+        // P over the S columns, keys 2m, 2m + 1 in column m (the V rows of
+        // keys at or past k_hi were zeroed as the tile was converted)
+#pragma unroll
+        for (int c = 0; c < kTcBN / 32; ++c) tmem_st16(scol + 16 * c, *reinterpret_cast<uint32_t(*)[16]>(&pw[16 * c]));
         const float2 s01 = f2_split(f2_add(f2_add(sum2[0], sum2[1]), f2_add(sum2[2], sum2[3])));
         const float sum = s01.x + s01.y;
         const float al = fast_exp2(m_run - mb);
@@ -1222,55 +1361,14 @@ __global__ void __launch_bounds__(32 * 12, 1)
             for (int k = 0; k < 32; ++k) ov[k] = __float_as_uint(__uint_as_float(ov[k]) * al);
             tmem_st32(ocol + c0, ov);
           }
-          tmem_wait_st();
         }
         l_run = l_run * al + sum;
         m_run = mx;
-        // the last tile's V rows at or past k_hi: zeroed by tile A's warps
-        // before their P is published, so before either PV product reads them
-        const bool zero_v = !kFp8V && t == 0 && key_base + kTcBN > k_hi;  // (E4M3 V: zeroed as converted)
-        if (zero_v) {
-          ok = __all_sync(0xffffffffu, mbar_wait(&v_full[st], (uint32_t(j) / kTcStages) & 1));
-          if (!ok) break;
-          const int32_t z0 = k_hi - key_base > 0 ? k_hi - key_base : 0;
-          uint8_t* vb = smem + Lay::kStage0 + st * Lay::kStageBytes + Lay::kKBytes;
-          const uint32_t units = uint32_t(kTcBN - z0) * kChunks * 8;
-          for (uint32_t e = row; e < units; e += kTcBM) {
-            const uint32_t rr = uint32_t(z0) + e / (kChunks * 8), rest = e % (kChunks * 8);
-            *reinterpret_cast<uint4*>(vb + (rest >> 3) * (kTcBN * 128) + rr * 128 + ((rest & 7) << 4)) =
-                make_uint4(0, 0, 0, 0);
-          }
-        }
-        // P hi / lo over the S columns (truncations, |P - hi - lo| < 2^-15 P):
-        // hi of keys 2m, 2m + 1 in column m, lo in column 64 + m
-#pragma unroll
-        for (int c = 0; c < kTcBN / 32; ++c) {
-          uint32_t hi[16], lw[16];
-#pragma unroll
-          for (int q = 0; q < 16; ++q) {
-            const float x0 = x[32 * c + 2 * q], x1 = x[32 * c + 2 * q + 1];
-            if constexpr (kFp8V) {
-              // f16 parts: hi the weight truncated to 11 significant bits, lo
-              // the exact remainder rounded to f16 (|P - hi - lo| <= max(2^-21 P, 2^-24))
-              const float h0 = __uint_as_float(__float_as_uint(x0) & 0xffffe000u);
-              const float h1 = __uint_as_float(__float_as_uint(x1) & 0xffffe000u);
-              hi[q] = f32x2_to_f16x2(h0, h1);
-              lw[q] = f32x2_to_f16x2(x0 - h0, x1 - h1);
-            } else {
-              const uint32_t b0 = __float_as_uint(x0), b1 = __float_as_uint(x1);
-              hi[q] = __byte_perm(b0, b1, 0x7632u);
-              const float2 r = f2_split(f2_sub(f2_make(x0, x1), f2_make(__uint_as_float(b0 & 0xffff0000u),
-                                                                         __uint_as_float(b1 & 0xffff0000u))));
-              lw[q] = __byte_perm(__float_as_uint(r.x), __float_as_uint(r.y), 0x7632u);
-            }
-          }
-          tmem_st16(scol + 16 * c, hi);
-          tmem_st16(scol + kTcBN / 2 + 16 * c, lw);
-        }
         tmem_wait_st();
-        if (zero_v) fence_async_smem();
         tc_fence_before();
         mbar_arrive(&p_full[t]);
+        // the next V tile, off the path of this tile's PV product
+        if (j + 1 < T) ok = convert_v(j + 1);
       }
       if (!ok && lane == 0) atomicOr(&g_prefill_error, kErrWaitTimeout);
       // ---- O / l to the output row
@@ -1279,8 +1377,9 @@ __global__ void __launch_bounds__(32 * 12, 1)
         done = __all_sync(0xffffffffu, mbar_wait(&o_full[t], uint32_t(T - 1) & 1));
         tc_fence_after();
       }
-      // (E4M3 V: the PV product summed codes; v_scale dequantises them)
-      const float inv = l_run > 0.0f ? (kFp8V ? p.out_scale : 1.0f) / l_run : 0.0f;
+      // the PV product summed E4M3 codes (v_scale dequantises them) or BF16
+      // values times 2^-8
+      const float inv = l_run > 0.0f ? (kFp8V ? p.out_scale : 256.0f) / l_run : 0.0f;
       float* o = valid ? p.output + (uint64_t(it.qstart + tok) * p.num_q_heads + uint64_t(it.kv_head * g + hh)) * D
                        : nullptr;
 #pragma unroll 1
