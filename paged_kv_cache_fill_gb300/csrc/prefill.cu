@@ -859,7 +859,7 @@ __global__ void __launch_bounds__(tc_threads<kFp8>(), 1)
 //     tile's PV product (one warp converting a whole tile per cycle became
 //     the serial path).
 constexpr int kTc2Rows = 256;
-constexpr uint32_t kTc2RegsLow = 64, kTc2RegsHigh = 216;  // 128 x 64 + 256 x 216 <= 384 x 168 at launch
+constexpr uint32_t kTc2RegsLow = 96, kTc2RegsHigh = 192;  // 128 x 96 + 256 x 192 <= 384 x 168 at launch
 
 template <int D, bool kFp8>
 struct Tc2Layout {  // byte offsets from the 1024-aligned shared base; an E4M3 V tile lands
@@ -1286,8 +1286,11 @@ __global__ void __launch_bounds__(32 * 12, 1)
       };
       auto convert_v = [&](int32_t j) -> bool {
         if constexpr (kFp8V) return true;  // E4M3 V: converted by the V producer warp
-        if (!convert_v_half(j, t)) return false;
-        return two || convert_v_half(j, 1);
+        const uint32_t h1 = two ? t + 1 : 2u;
+#pragma unroll 1
+        for (uint32_t h = two ? t : 0u; h < h1; ++h)
+          if (!convert_v_half(j, h)) return false;
+        return true;
       };
       float m_run = -INFINITY, l_run = 0.0f;
       bool ok = T == 0 || convert_v(0);
@@ -1327,22 +1330,26 @@ __global__ void __launch_bounds__(32 * 12, 1)
         const float mbp = mb - 7.0f;
         // x * score_scale - mbp and the row sum two keys per packed operation;
         // each pair of weights goes to f16 as soon as it is formed (|P - P16|
-        // <= 2^-11 P above 2^-21 P, the weights being 2^7 P), so that only the
-        // 64 packed words stay live
+        // <= 2^-11 P above 2^-21 P, the weights being 2^7 P), so that few
+        // packed words stay live
         const F2 sc2 = f2_make(rs, rs), nmb2 = f2_make(-mbp, -mbp);
         F2 sum2[4] = {0ull, 0ull, 0ull, 0ull};
-        uint32_t pw[kTcBN / 2];
+        // P over the S columns, keys 2m, 2m + 1 in column m, 32 keys at a
+        // time (the V rows of keys at or past k_hi were zeroed as the tile
+        // was converted)
 #pragma unroll
-        for (int k = 0; k < kTcBN / 2; ++k) {
-          const float2 a = f2_split(f2_fma(f2_make(x[2 * k], x[2 * k + 1]), sc2, nmb2));
-          const float e0 = fast_exp2(a.x), e1 = fast_exp2(a.y);
-          sum2[k & 3] = f2_add(sum2[k & 3], f2_make(e0, e1));
-          pw[k] = f32x2_to_f16x2(e0, e1);
+        for (int c = 0; c < kTcBN / 32; ++c) {
+          uint32_t pw[16];
+#pragma unroll
+          for (int q = 0; q < 16; ++q) {
+            const int k = 16 * c + q;
+            const float2 a = f2_split(f2_fma(f2_make(x[2 * k], x[2 * k + 1]), sc2, nmb2));
+            const float e0 = fast_exp2(a.x), e1 = fast_exp2(a.y);
+            sum2[q & 3] = f2_add(sum2[q & 3], f2_make(e0, e1));
+            pw[q] = f32x2_to_f16x2(e0, e1);
+          }
+          tmem_st16(scol + 16 * c, pw);
         }
-        // P over the S columns, keys 2m, 2m + 1 in column m (the V rows of
-        // keys at or past k_hi were zeroed as the tile was converted)
-#pragma unroll
-        for (int c = 0; c < kTcBN / 32; ++c) tmem_st16(scol + 16 * c, *reinterpret_cast<uint32_t(*)[16]>(&pw[16 * c]));
         const float2 s01 = f2_split(f2_add(f2_add(sum2[0], sum2[1]), f2_add(sum2[2], sum2[3])));
         const float sum = s01.x + s01.y;
         const float al = fast_exp2(m_run - mb);
