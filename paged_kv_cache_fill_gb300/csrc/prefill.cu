@@ -836,7 +836,7 @@ __global__ void __launch_bounds__(tc_threads<kFp8>(), 1)
 // shared memory before it (E4M3 codes exactly; BF16 values times 2^-8,
 // exact for 2^-6 <= |v| < 2^24, which the output scale undoes). 384
 // threads, three warpgroups:
-//   warpgroup 0 (registers cut to kTc2RegsLow with setmaxnreg):
+//   warpgroup 0 (registers cut to tc2_regs_low() with setmaxnreg):
 //     warp 0      TMA producer of 128-key K tiles, warp 2 of V tiles, each a
 //                 2-stage ring whose stage is free once the MMA thread's
 //                 commit after its last reader has arrived on its empty
@@ -849,7 +849,7 @@ __global__ void __launch_bounds__(tc_threads<kFp8>(), 1)
 //     warp 3      with an E4M3 K cache: turns each E4M3 K tile, loaded by
 //                 warp 0 into a ring of its own, into the f16 K stage the
 //                 S product reads (exact); otherwise idle;
-//   warpgroups 1, 2 (registers raised to kTc2RegsHigh): the softmax of tile
+//   warpgroups 1, 2 (registers raised to tc2_regs_high()): the softmax of tile
 //     A and of tile B, one thread per row (TMEM lane) over all 128 keys of a
 //     tile, so no row is shared between threads; they also write the Q rows
 //     (with an E4M3 K cache: as f16, the row scaled by a power of two that
@@ -857,9 +857,20 @@ __global__ void __launch_bounds__(tc_threads<kFp8>(), 1)
 //     BF16 V cache, convert V tile j + 1 in place (each warpgroup half of
 //     it) right after publishing their P of tile j, off the path of that
 //     tile's PV product (one warp converting a whole tile per cycle became
-//     the serial path).
+//     the serial path). At the end each thread stages its O / l row in the
+//     then free Q tiles and K/V stages and stores it with one bulk copy
+//     (direct stores of a row per thread wrote 16 bytes per 32-byte sector
+//     and took ~3 us per CTA).
 constexpr int kTc2Rows = 256;
-constexpr uint32_t kTc2RegsLow = 96, kTc2RegsHigh = 192;  // 128 x 96 + 256 x 192 <= 384 x 168 at launch
+// registers per thread of warpgroup 0 and of the softmax warpgroups after
+// setmaxnreg (per variant, the split that ptxas fits without spills or the
+// faster one measured): 128 x low + 256 x high <= 384 x 168 at launch
+template <bool kFp8V>
+__host__ __device__ constexpr uint32_t tc2_regs_low() { return kFp8V ? 72u : 96u; }
+template <bool kFp8V>
+__host__ __device__ constexpr uint32_t tc2_regs_high() { return kFp8V ? 208u : 192u; }
+static_assert(128 * tc2_regs_low<false>() + 256 * tc2_regs_high<false>() <= 384 * 168, "register split");
+static_assert(128 * tc2_regs_low<true>() + 256 * tc2_regs_high<true>() <= 384 * 168, "register split");
 
 template <int D, bool kFp8>
 struct Tc2Layout {  // byte offsets from the 1024-aligned shared base; an E4M3 V tile lands
@@ -949,7 +960,7 @@ __global__ void __launch_bounds__(32 * 12, 1)
   const int32_t T = t_end - t_begin;
 
   if (warp < 4) {
-   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kTc2RegsLow));
+   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(tc2_regs_low<kFp8V>()));
    if (warp == 0 || warp == 2) {
     // ------------------------------------------------------------ producers
     const bool is_k = warp == 0;
@@ -1046,7 +1057,7 @@ __global__ void __launch_bounds__(32 * 12, 1)
     // (exact: every E4M3 value is an f16 value). The f16 stage is free once
     // both S products of the tile two back are done (k_empty), the E4M3
     // stage once this warp has read it (k8_empty). Inline and one key row at
-    // a time: this warpgroup runs on kTc2RegsLow registers.
+    // a time: this warpgroup runs on tc2_regs_low() registers.
     bool ok = true;
     for (int32_t j = 0; j < T && ok; ++j) {
       const uint32_t st = uint32_t(j) % kTcStages;
@@ -1176,7 +1187,7 @@ __global__ void __launch_bounds__(32 * 12, 1)
     __syncwarp();
    }
   } else {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kTc2RegsHigh));
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(tc2_regs_high<kFp8V>()));
     // ------------------------------------------------------------ softmax
     const uint32_t t = (warp - 4) >> 2;         // the Q tile
     const uint32_t row = (warp & 3) * 32 + lane;  // the row within the tile = TMEM lane
@@ -1379,31 +1390,41 @@ __global__ void __launch_bounds__(32 * 12, 1)
       }
       if (!ok && lane == 0) atomicOr(&g_prefill_error, kErrWaitTimeout);
       // ---- O / l to the output row
-      bool done = __all_sync(0xffffffffu, ok);
-      if (done && T > 0) {
-        done = __all_sync(0xffffffffu, mbar_wait(&o_full[t], uint32_t(T - 1) & 1));
-        tc_fence_after();
-      }
       // the PV product summed E4M3 codes (v_scale dequantises them) or BF16
       // values times 2^-8
       const float inv = l_run > 0.0f ? (kFp8V ? p.out_scale : 256.0f) / l_run : 0.0f;
       float* o = valid ? p.output + (uint64_t(it.qstart + tok) * p.num_q_heads + uint64_t(it.kv_head * g + hh)) * D
                        : nullptr;
+      bool done = __all_sync(0xffffffffu, ok);
+      if (T == 0) {  // no key for any query of the item: zeros
+        if (o && done)
+          for (uint32_t c = 0; c < uint32_t(D); c += 4) *reinterpret_cast<float4*>(o + c) = make_float4(0, 0, 0, 0);
+      } else if (done) {
+        // once every product is done, the Q tiles and the K/V stages are free:
+        // the row is staged there (rows D * 4 + 16 bytes apart, so that the
+        // warp's 16-byte stores fall in distinct banks) and goes out as one
+        // bulk copy
+        done = __all_sync(0xffffffffu, mbar_wait(&mma_done, 0));
+        tc_fence_after();
+        constexpr uint32_t kRowStride = D * 4 + 16;
+        static_assert(2 * kTcBM * kRowStride <= Lay::kStage0 + kTcStages * Lay::kStageBytes,
+                      "the staged O rows fit in the Q tiles and the K/V stages");
+        float* stage = reinterpret_cast<float*>(smem + (t * kTcBM + row) * kRowStride);
 #pragma unroll 1
-      for (uint32_t c0 = 0; c0 < uint32_t(D); c0 += 32) {
-        uint32_t ov[32];
-        if (done && T > 0) {
+        for (uint32_t c0 = 0; c0 < uint32_t(D) && done; c0 += 32) {
+          uint32_t ov[32];
           tmem_ld32(ocol + c0, ov);
           tmem_wait_ld();
+#pragma unroll
+          for (int k = 0; k < 32; k += 4)
+            *reinterpret_cast<float4*>(stage + c0 + k) =
+                make_float4(__uint_as_float(ov[k]) * inv, __uint_as_float(ov[k + 1]) * inv,
+                            __uint_as_float(ov[k + 2]) * inv, __uint_as_float(ov[k + 3]) * inv);
         }
         if (o && done) {
-#pragma unroll
-          for (int k = 0; k < 32; k += 4) {
-            const float4 w4 = T > 0 ? make_float4(__uint_as_float(ov[k]) * inv, __uint_as_float(ov[k + 1]) * inv,
-                                                  __uint_as_float(ov[k + 2]) * inv, __uint_as_float(ov[k + 3]) * inv)
-                                    : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-            *reinterpret_cast<float4*>(o + c0 + k) = w4;
-          }
+          fence_async_smem();
+          bulk_store(o, stage, D * 4);
+          bulk_store_wait_read();
         }
       }
     }
