@@ -270,8 +270,8 @@ PAGEDKV_API int paged_decode_attn_fp8(const kv_bf16_t *q, const kv_e4m3_t *k_cac
  * V call at head_dim 64 takes them as two f16 parts) against V as f16: E4M3
  * codes exactly, BF16 values as v * 2^-8 rounded to f16, exact for
  * 2^-6 <= |v| < 2^24 and within 2^-17 below. BF16 V values of magnitude
- * 2^24 or more are outside the supported range (the outputs that weigh them
- * are not finite).
+ * 2^24 or more are outside the supported range: the outputs of every query
+ * whose keys share a 128-key tile with one are not finite.
  * Supported: head_dim 64 or 128; block_size a power of two in
  * [16, 256]; q, caches, q_stride and output 16-byte aligned. No workspace
  * is used.

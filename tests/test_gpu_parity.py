@@ -632,6 +632,36 @@ def test_prefill_cases(fp8, case):
     assert pk.kv_get_device_error() == 0
 
 
+@pytest.mark.parametrize("fp8", [False, True])
+@pytest.mark.parametrize("log2_scale", [20, -12])
+def test_prefill_bf16_v_range(fp8, log2_scale):
+    """BF16 V enters the chunked prefill's PV product as v * 2^-8 rounded to
+    f16: exact for 2^-6 <= |v| < 2^24, within 2^-17 (absolute) below. V
+    scaled by 2^20 (|v| up to ~2^22.5) must give the unit-scale result
+    times 2^20 within the usual bound; V scaled by 2^-12 (every |v| below
+    2^-6) must stay within 2^-17 per value plus the weights' f16 rounding
+    (2^-11 relative) of the oracle's output."""
+    lens, qlens, Hq, H, D, bs, _ = PREFILL_CASES[1]
+    w = kvgen.custom(240 + (log2_scale > 0), seq_lens=lens, num_q_heads=Hq, num_kv_heads=H, head_dim=D,
+                     block_size=bs, fp8=fp8, q_rows=sum(qlens))
+    scale = 2.0 ** log2_scale
+    w.value = (w.value.float() * scale).to(torch.bfloat16)   # exact: a power of two
+    vmax = float(w.value.float().abs().max())
+    assert (vmax < 2.0 ** 24) if log2_scale > 0 else (vmax < 2.0 ** -6)
+    kc, vc, kr, vr = _caches(w, fp8)
+    qsl = np.concatenate([[0], np.cumsum(qlens)]).astype(np.int32)
+    for win in (0, 256):
+        got = _prefill_gpu(w, kc, vc, qsl, win, fp8)
+        ref = _prefill_ref(w, kr, vr, qsl, win, fp8)
+        if log2_scale > 0:
+            assert_decode_close(got / scale, ref / scale, f"V x 2^{log2_scale}, window {win}")
+        else:
+            assert np.isfinite(got).all()
+            err = np.abs(got.astype(np.float64) - ref)
+            assert err.max() <= 2.0 ** -17 + 2.0 ** -11 * vmax, f"V x 2^{log2_scale}: max abs err {err.max():.3e}"
+    assert pk.kv_get_device_error() == 0
+
+
 def test_prefill_one_query_per_sequence_matches_the_decode():
     w = kvgen.custom(230, seq_lens=[4000, 17, 900, 1], num_q_heads=32, num_kv_heads=8, head_dim=128, block_size=16)
     kc, vc, kr, vr = _caches(w, False)
