@@ -266,9 +266,8 @@ PAGEDKV_API int paged_decode_attn_fp8(const kv_bf16_t *q, const kv_e4m3_t *k_cac
  *                    fault word and that sequence's rows are skipped).
  *   output           device float32[num_q_tokens, num_q_heads, head_dim].
  * Precision: scores and sums in fp32; the PV product takes the softmax
- * weights as f16 (one rounding, relative error at most 2^-11; the FP8 K and
- * V call at head_dim 64 takes them as two f16 parts) against V as f16: E4M3
- * codes exactly, BF16 values as v * 2^-8 rounded to f16, exact for
+ * weights as f16 (one rounding, relative error at most 2^-11) against V as
+ * f16: E4M3 codes exactly, BF16 values as v * 2^-8 rounded to f16, exact for
  * 2^-6 <= |v| < 2^24 and within 2^-17 below. BF16 V values of magnitude
  * 2^24 or more are outside the supported range: the outputs of every query
  * whose keys share a 128-key tile with one are not finite.

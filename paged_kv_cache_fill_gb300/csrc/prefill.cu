@@ -1,5 +1,5 @@
-// Multi-token (chunked-prefill) paged attention over a BF16 or FP8-E4M3-K /
-// BF16-V paged cache.
+// Multi-token (chunked-prefill) paged attention over a BF16, an FP8-E4M3-K /
+// BF16-V or an FP8-E4M3 K and V paged cache.
 //
 // [kv_cache.rs] "Batched prefill variants (N tokens)" (a heading only), read
 // as: sequence s brings n_s = query_start_loc[s+1] - query_start_loc[s]
@@ -12,16 +12,13 @@
 //
 // GB300 design (tcgen05 / TMEM). Rows are (query token, query head of the
 // KV head's group) pairs, token-major, so a CTA's rows -- 128 per
-// tcgen05.mma (its M) -- share every K/V tile it loads. Two kernels:
-//   prefill_tc_kernel   one 128-row Q tile per CTA; any cache type; the FP8
-//                       K+V call at head_dim 64 runs it;
-//   prefill_tc2_kernel  two 128-row Q tiles per CTA (one tile's products
-//                       cover the other's drain in the tensor pipe); every
-//                       other call runs it.
-// A CTA owns one (sequence, KV head, block of rows) item; items run
+// tcgen05.mma (its M) -- share every K/V tile it loads. One kernel,
+// prefill_tc2_kernel, with two 128-row Q tiles per CTA (one tile's
+// products cover the other's drain in the tensor pipe), runs every call.
+// A CTA owns one (sequence, KV head, block of 256 rows) item; items run
 // longest key range first across all sequences (by a length class of each
 // sequence's key range), and the grid holds an upper bound of the item count
-// (CTAs past the last item exit at once). Each kernel's own comment gives
+// (CTAs past the last item exit at once). The kernel's own comment gives
 // its warp roles, TMEM map and barriers.
 #include <math.h>
 
@@ -48,7 +45,6 @@ struct PrefillParams {
   uint32_t block_size, block_shift, q_stride, sliding_window;
   float score_scale;  // inv_sqrt_d * log2(e) (times k_scale for FP8)
   float out_scale;    // E4M3 V: v_scale (the V codes enter the PV product as they are)
-  uint32_t k_box_bytes, v_box_bytes, stage_bytes;
 };
 
 // An E4M3 tile [chunk of 128 dims][128 keys][128 B] (head_dim 64: [128
@@ -60,9 +56,10 @@ struct PrefillParams {
 // far as the compiler knows, so interleaving them would serialise every
 // load behind the previous unit's stores. A dead row's codes are replaced by
 // zeros as loaded (E4M3 0 is f16 0), which costs far fewer instructions than
-// selecting every converted word. Not inlined and the passes not unrolled:
-// the K and V converting warps then run one short body, where two inlined,
-// unrolled copies left the kernel's warps stalled on instruction fetch.
+// selecting every converted word. Not inlined and the passes not unrolled,
+// so that the converting warp runs one short body (inlined, unrolled
+// converter copies in several warps have stalled a kernel's warps on
+// instruction fetch).
 template <int D>
 __device__ __noinline__ void e4m3_tile_to_f16(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst,
                                               int32_t live, uint32_t lane) {
@@ -246,578 +243,10 @@ __device__ Item locate(uint32_t target, const PrefillParams& p, uint32_t lane, u
   return it;
 }
 
-// ---------------------------------------------------------------- the kernel
-// One CTA per (sequence, KV head, block of 128 rows), 352 threads (384 with
-// an E4M3 K cache):
-//   warps 0, 10 TMA producers of 128-key K and V tiles, each [chunk][key][128 B]
-//               (one box per 16-slot block run and 128-byte chunk), in two
-//               2-stage rings: a K stage is free once the S product of the
-//               tile two back is done, a V stage once that tile's PV is;
-//   warp 11     (E4M3 K cache only) converts each E4M3 K tile, loaded into its own
-//               ring, into the f16 K tile (exact); with an E4M3 V cache,
-//               warp 10 likewise converts each V tile it loaded, one tile
-//               behind its loads;
-//   warp 1      owns TMEM and issues every tcgen05.mma from one thread:
-//               S = Q K^T (M 128, N 128, K = head_dim; BF16, or f16 Q scaled
-//               by a power of two per row against the f16 K) into one of
-//               two TMEM S buffers, Q read from tensor memory, then
-//               O += P_hi V + P_lo V (M 128, N = head_dim, K 128; BF16
-//               parts, or f16 parts against the f16 V of an E4M3 V cache)
-//               into TMEM O, P from TMEM (written over its S buffer), V as the
-//               MN-major shared-memory operand (only K and V tiles are
-//               read from shared memory); this thread's issue-and-wait loop
-//               is the kernel's serial path;
-//   warps 2..9  softmax, two threads per row = TMEM lane (warp w owns lanes
-//               32 (w % 4) ..; warps 2..5 the first half of a tile's keys and
-//               of O's columns, warps 6..9 the second): Q rows into tensor
-//               memory, then per tile S via tcgen05.ld, masks, base-2 online
-//               softmax (the pair swaps partial row maxima), O rescale in
-//               TMEM when a row's reference max moved, P hi / lo into TMEM
-//               (the PV MMA reads its A operand from tensor memory, sparing
-//               shared-memory bandwidth), and at the end O / l to the output.
-// S of tile i + 1 is computed while the softmax works on tile i.
-constexpr uint32_t kVWarp = 10, kConvWarp = 11;  // V producer (and E4M3 V converter); FP8 K converter
-template <bool kFp8>
-constexpr int tc_threads() { return 32 * (kFp8 ? 12 : 11); }
 constexpr float kRescaleLog2 = 8.0f;  // reference-max slack of the online softmax (base 2)
 
-template <int D, bool kFp8, bool kFp8V = false>
-struct TcLayout {  // byte offsets from the 1024-aligned shared base
-  static constexpr uint32_t kChunks = D / 64;
-  static constexpr uint32_t kStage0 = 0;
-  static constexpr uint32_t kKBytes = kChunks * kTcBN * 128;  // [chunk][128 keys][128 B]
-  static constexpr uint32_t kStageBytes = 2 * kKBytes;        // K (f16 when FP8: converted), then V
-  // FP8 K as loaded, one ring of stages: [chunk of 128 dims][128 keys][128 B]
-  // (128-byte swizzle), or for head_dim 64 [128 keys][64 B] (64-byte
-  // swizzle); kE4Row bytes of a key's row per chunk
-  static constexpr uint32_t kE4Row = D < 128 ? D : 128;
-  static constexpr uint32_t kK8Chunks = (D + 127) / 128;
-  static constexpr uint32_t kK8Bytes = kFp8 ? kK8Chunks * kTcBN * kE4Row : 0;
-  static constexpr uint32_t kK80 = kStage0 + kTcStages * kStageBytes;
-  // E4M3 V as loaded (same shape as the E4M3 K), one ring of stages
-  static constexpr uint32_t kV8Bytes = kFp8V ? kK8Chunks * kTcBN * kE4Row : 0;
-  static constexpr uint32_t kV80 = kK80 + kTcStages * kK8Bytes;
-  static constexpr uint32_t kBytes = kV80 + kTcStages * kV8Bytes;
-  // TMEM columns: two S buffers [0, 128), [128, 256), each overwritten by
-  // its tile's P once read (hi [+0, +64), lo [+64, +128): 128 keys, 2 per
-  // column); Q [256, 256 + D / 2) (the S product's A operand, 2 dims per
-  // column); O [384, 384 + D)
-  static constexpr uint32_t kTmemCols = 512;
-  static constexpr uint32_t kQCol = 256;
-  static constexpr uint32_t kOCol = 384;
-  static constexpr uint32_t kSBufs = 2;
-};
-
-template <int D, bool kFp8, bool kFp8V>
-__global__ void __launch_bounds__(tc_threads<kFp8>(), 1)
-    prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
-                      const PrefillParams p) {
-  static_assert(kFp8 || !kFp8V, "an E4M3 V cache comes with an E4M3 K cache");
-  using Lay = TcLayout<D, kFp8, kFp8V>;
-  constexpr uint32_t kChunks = Lay::kChunks;
-  extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw_addr = smem_u32(smem_raw);
-  uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
-  const uint32_t sbase = smem_u32(smem);
-  __shared__ uint64_t k_full[kTcStages], v_full[kTcStages];
-  __shared__ uint64_t k8_full[kTcStages], k8_empty[kTcStages];  // FP8 K: loaded, converted
-  __shared__ uint64_t v8_full[kTcStages];                       // FP8 V: loaded
-  __shared__ float s_qamax[2][kTcBM];                           // FP8: [half][row] partial max |q|
-  __shared__ uint64_t qamax_bar[4];
-  __shared__ uint64_t s_full[Lay::kSBufs], p_full[Lay::kSBufs], o_full[Lay::kSBufs];  // per S/P buffer
-  __shared__ uint64_t q_full, mma_done;
-  __shared__ uint32_t tmem_base_s;
-  __shared__ Item s_item;
-  __shared__ float s_xchg[2][2][kTcBM];  // [tile parity][half][row] partial row maxima
-  __shared__ float s_lsum[2][kTcBM];     // [half][row] partial row sums, at the end
-  __shared__ uint64_t xchg_bar[4][2], lsum_bar[4];  // per TMEM lane quarter: the pair of warps
-
-  const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < kTcStages; ++s) {
-      mbar_init(&k_full[s], kFp8 ? 32 : 1);  // FP8: the converter warp's arrivals
-      mbar_init(&v_full[s], kFp8V ? 32 : 1);  // FP8 V: warp 10's arrivals once converted
-      mbar_init(&k8_full[s], 1);
-      mbar_init(&k8_empty[s], 32);
-      mbar_init(&v8_full[s], 1);
-    }
-    for (uint32_t b = 0; b < Lay::kSBufs; ++b) {
-      mbar_init(&s_full[b], 1);
-      mbar_init(&p_full[b], 256);
-      mbar_init(&o_full[b], 1);
-    }
-    mbar_init(&q_full, 256);
-    for (int qd = 0; qd < 4; ++qd) {
-      mbar_init(&xchg_bar[qd][0], 64);
-      mbar_init(&xchg_bar[qd][1], 64);
-      mbar_init(&lsum_bar[qd], 64);
-      mbar_init(&qamax_bar[qd], 64);
-    }
-    mbar_init(&mma_done, 1);
-    fence_mbar_init();
-  }
-  if (warp == 0) {
-    const Item it = locate<kTcBM>(blockIdx.x, p, lane, reinterpret_cast<uint32_t*>(smem));  // (free until the Q rows)
-    if (lane == 0) s_item = it;
-  }
-  __syncthreads();
-  const Item it = s_item;
-  if (it.seq < 0) return;
-  if (warp == 1) tmem_alloc(&tmem_base_s, Lay::kTmemCols);
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = tmem_base_s;
-
-  const int32_t g = int32_t(p.group);
-  const int32_t pos_first = it.len - it.n + it.row0 / g;
-  const int32_t pos_last = it.len - it.n + (it.row0 + it.rows - 1) / g;
-  const int32_t k_hi = pos_last + 1;  // keys [k_lo, k_hi)
-  const int32_t W = int32_t(p.sliding_window);
-  int32_t k_lo = 0;
-  if (W > 0 && pos_first + 1 - W > 0) k_lo = pos_first + 1 - W;
-  const int32_t t_begin = k_lo / kTcBN;
-  const int32_t t_end = k_hi > 0 ? (k_hi + kTcBN - 1) / kTcBN : t_begin;
-  const int32_t T = t_end - t_begin;
-
-  if (warp == 0 || warp == kVWarp) {
-    // ------------------------------------------------------------ producers
-    // warp 0 loads K, warp 10 V, each into its own 2-stage ring. A K stage
-    // is free once the S product of the tile two back is done (s_full of its
-    // S buffer), a V stage once that tile's PV product is done (o_full): the
-    // MMA thread commits nothing extra for the producers. With two S buffers
-    // the same barrier completes next for tile i itself, which needs this
-    // load first, so the parity of the wait is unambiguous. FP8 K lands in
-    // a ring of its own, free once the converter warp has read it. E4M3 V
-    // lands in a ring of its own too, which warp 10 converts itself one tile
-    // behind its loads: a stage of it is free again by the time warp 10
-    // loads into it, the f16 V stage once the PV product two tiles back is
-    // done.
-    const bool is_k = warp == 0;
-    const bool e4m3 = is_k ? kFp8 : kFp8V;  // this tensor's cache holds E4M3 codes
-    const CUtensorMap* map = is_k ? &tmap_k : &tmap_v;
-    uint64_t* full = is_k ? (kFp8 ? k8_full : k_full) : (kFp8V ? v8_full : v_full);
-    static_assert(kTcStages == 2, "stage reuse waits on tile i - 2");
-    tma_prefetch_desc(map);
-    const int32_t* table = p.block_tables + uint64_t(it.seq) * p.max_blocks_per_seq;
-    // E4M3 V tile j -> the f16 V stage the PV product reads; rows past the
-    // item's last key (not loaded, or positions past every query) as zeros
-    auto convert_v = [&](int32_t j) -> bool {
-      if constexpr (kFp8V) {
-        const uint32_t sj = uint32_t(j) % kTcStages;
-        bool good = __all_sync(0xffffffffu, mbar_wait(&v8_full[sj], uint32_t(j / kTcStages) & 1));
-        if (good && j >= kTcStages)
-          good = __all_sync(0xffffffffu, mbar_wait(&o_full[(j - kTcStages) % Lay::kSBufs],
-                                                   uint32_t((j - kTcStages) / Lay::kSBufs) & 1));
-        if (!good) return false;
-        const int32_t left = k_hi - (t_begin + j) * kTcBN;
-        e4m3_tile_to_f16<D>(smem + Lay::kV80 + sj * Lay::kV8Bytes,
-                            smem + Lay::kStage0 + sj * Lay::kStageBytes + Lay::kKBytes,
-                            left < 0 ? 0 : (left > kTcBN ? kTcBN : left), lane);
-        fence_async_smem();
-        mbar_arrive(&v_full[sj]);
-        return true;
-      } else {
-        return j < 0;  // not reached: only an E4M3 V cache converts
-      }
-    };
-    const bool self_converts = kFp8V && !is_k;
-    bool ok = true;
-    int32_t issued = 0;  // tiles whose loads this warp has issued
-    for (int32_t i = 0; i < T && ok; ++i) {
-      const uint32_t st = uint32_t(i) % kTcStages;
-      const int32_t key0 = (t_begin + i) * kTcBN + int32_t(lane) * kSub;
-      const bool mine = lane < uint32_t(kTcBN / kSub) && key0 < k_hi;
-      const int32_t block_id = mine ? __ldg(table + (key0 >> p.block_shift)) : 0;
-      if (lane == 0 && i >= kTcStages && !self_converts) {
-        const int32_t j = i - kTcStages;
-        const bool freed = e4m3 ? mbar_wait(&k8_empty[st], uint32_t(j / kTcStages) & 1)
-                                : mbar_wait(&(is_k ? s_full : o_full)[j % Lay::kSBufs],
-                                            uint32_t(j / Lay::kSBufs) & 1);
-        if (!freed) ok = false;
-      }
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
-      const uint32_t loaded = __popc(__ballot_sync(0xffffffffu, mine));
-      const uint32_t chunks = e4m3 ? Lay::kK8Chunks : kChunks;
-      const uint32_t row_bytes = e4m3 ? Lay::kE4Row : 128u;  // of a key's row per box
-      if (lane == 0) mbar_arrive_expect_tx(&full[st], loaded * chunks * (kSub * row_bytes));
-      __syncwarp();
-      if (mine) {
-#ifdef PAGEDKV_DEBUG_BOUNDS
-        // a block id outside the pool is flagged and block 0 read instead
-        const int32_t slot0 =
-            ((dbg_block_ok(block_id) ? block_id : 0) << p.block_shift) + (key0 & int32_t(p.block_size - 1));
-#else
-        const int32_t slot0 = (block_id << p.block_shift) + (key0 & int32_t(p.block_size - 1));
-#endif
-        uint8_t* dst = smem + (e4m3 ? (is_k ? Lay::kK80 + st * Lay::kK8Bytes : Lay::kV80 + st * Lay::kV8Bytes)
-                                    : Lay::kStage0 + st * Lay::kStageBytes + (is_k ? 0u : Lay::kKBytes)) +
-                       lane * (kSub * row_bytes);
-        for (uint32_t c = 0; c < chunks; ++c)
-          tma_load_3d(dst + c * (kTcBN * row_bytes), map, 0, slot0, it.kv_head * chunks + c, &full[st]);
-      }
-      issued = i + 1;
-      if (self_converts && i >= 1) ok = convert_v(i - 1);
-    }
-    if (self_converts && ok && T > 0) ok = convert_v(T - 1);
-    if (!ok) {
-      // a wait gave up: let this warp's loads still in flight (at most the
-      // last two tiles, one per stage) land, bounded, before the CTA can
-      // exit, so no copy writes into shared memory the CTA has released
-      if (lane == 0) atomicOr(&g_prefill_error, kErrWaitTimeout);
-      for (int32_t j = issued > kTcStages ? issued - kTcStages : 0; j < issued; ++j)
-        mbar_wait(&full[uint32_t(j) % kTcStages], uint32_t(j / kTcStages) & 1);
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issue
-    if (lane == 0) {
-      // S: BF16 Q and K, or (FP8 cache) f16 Q scaled per row against K converted exactly to f16
-      constexpr uint32_t idesc_s =
-          kFp8 ? umma_idesc_f16(kTcBM, kTcBN, false) : umma_idesc_bf16(kTcBM, kTcBN, false);
-      // PV: BF16 P parts x BF16 V, or (E4M3 V) f16 P parts x V converted exactly to f16
-      constexpr uint32_t idesc_o = kFp8V ? umma_idesc_f16(kTcBM, D, true) : umma_idesc_bf16(kTcBM, D, true);
-      // Descriptors are built once: a k-step or a stage moves only the start
-      // address field (bits 0-13, in 16-byte units), so each MMA adds a small
-      // constant. One thread issues every MMA, so its instruction count per
-      // MMA sets the issue rate.
-      const uint64_t k_desc0 = umma_desc_sw128(sbase + Lay::kStage0, 16, 1024);
-      const uint64_t v_desc0 = umma_desc_sw128(sbase + Lay::kStage0 + Lay::kKBytes, kTcBN * 128, 1024);
-      constexpr uint64_t kStageStep = Lay::kStageBytes >> 4;
-      const uint32_t tmem_o = tmem + Lay::kOCol;
-      bool ok = mbar_wait(&q_full, 0);
-      tc_fence_after();
-      auto issue_s = [&](int32_t i) -> bool {
-        const uint32_t st = uint32_t(i) % kTcStages, b = uint32_t(i) % Lay::kSBufs;
-        if (!mbar_wait(&k_full[st], (i / kTcStages) & 1)) return false;
-        // buffer b holds tile i - 2's P until its PV is done
-        if (i >= int32_t(Lay::kSBufs) && !mbar_wait(&o_full[b], uint32_t((i - Lay::kSBufs) / Lay::kSBufs) & 1))
-          return false;
-        tc_fence_after();
-        const uint64_t kd = k_desc0 + st * kStageStep;
-        const uint32_t tmem_s = tmem + b * kTcBN;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          // Q: 8 TMEM columns per 16 dims; K: chunk kk / 4 is kTcBN rows of 128 B further
-          const uint64_t off_k = uint64_t((kk >> 2) * (kTcBN * 128) + (kk & 3) * 32) >> 4;
-          umma_f16kind_tmem_a(tmem_s, tmem + Lay::kQCol + 8 * kk, kd + off_k, idesc_s, kk > 0);
-        }
-        umma_commit(&s_full[b]);
-        return true;
-      };
-      if (ok && T > 0) ok = issue_s(0);
-      for (int32_t i = 0; i < T && ok; ++i) {
-        if (i + 1 < T && !issue_s(i + 1)) {
-          ok = false;
-          break;
-        }
-        // per-buffer: the softmax cannot get a phase ahead on buffer i % 2
-        // before PV i, which reads it, has been issued
-        if (!mbar_wait(&p_full[i % Lay::kSBufs], uint32_t(i / Lay::kSBufs) & 1)) {
-          ok = false;
-          break;
-        }
-        const uint32_t st = uint32_t(i) % kTcStages, pb = uint32_t(i) % Lay::kSBufs;
-        if (!mbar_wait(&v_full[st], (i / kTcStages) & 1)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint64_t vd = v_desc0 + st * kStageStep;
-        const uint32_t pt = tmem + pb * kTcBN;  // P of this tile, in its S buffer: hi, then lo
-#pragma unroll
-        for (int kk = 0; kk < kTcBN / 16; ++kk) {
-          const uint64_t v_k = vd + uint64_t(kk * (16 * 128) >> 4);
-          umma_f16kind_tmem_a(tmem_o, pt + 8 * kk, v_k, idesc_o, i > 0 || kk > 0);
-          umma_f16kind_tmem_a(tmem_o, pt + kTcBN / 2 + 8 * kk, v_k, idesc_o, true);
-        }
-        umma_commit(&o_full[pb]);
-      }
-      if (!ok) atomicOr(&g_prefill_error, kErrWaitTimeout);
-      // every issued MMA has finished before TMEM is released
-      umma_commit(&mma_done);
-      mbar_wait(&mma_done, 0);
-    }
-    __syncwarp();
-  } else if (kFp8 && warp == kConvWarp) {
-   if constexpr (kFp8) {  // (warp 11 exists only with an E4M3 K cache)
-    // ------------------------------------------------------------ E4M3 -> f16
-    // One warp turns each loaded E4M3 K tile into the f16 [chunk][key][128 B]
-    // tile the S product reads. Exact: every E4M3 value is an f16 value. A
-    // f16 K stage is free once the S product two tiles back is done; an E4M3
-    // stage once its rows are read.
-    bool ok = true;
-    for (int32_t i = 0; i < T && ok; ++i) {
-      const uint32_t st = uint32_t(i) % kTcStages;
-      ok = __all_sync(0xffffffffu, mbar_wait(&k8_full[st], uint32_t(i / kTcStages) & 1));
-      if (ok && i >= kTcStages)
-        ok = __all_sync(0xffffffffu, mbar_wait(&s_full[(i - kTcStages) % Lay::kSBufs],
-                                               uint32_t((i - kTcStages) / Lay::kSBufs) & 1));
-      if (!ok) break;
-      e4m3_tile_to_f16<D>(smem + Lay::kK80 + st * Lay::kK8Bytes, smem + Lay::kStage0 + st * Lay::kStageBytes,
-                          kTcBN, lane);
-      fence_async_smem();
-      mbar_arrive(&k8_empty[st]);
-      mbar_arrive(&k_full[st]);
-    }
-    if (!ok && lane == 0) atomicOr(&g_prefill_error, kErrWaitTimeout);
-   }
-  } else {
-    // ------------------------------------------------------------ softmax
-    // two threads per row: warps 2..5 take keys 0..31 of each tile and O
-    // columns [0, D/2), warps 6..9 keys 32..63 and [D/2, D); the two warps
-    // of a TMEM lane quarter swap their partial row max (and, at the end,
-    // their partial sums) through shared memory and a 64-arrival mbarrier
-    constexpr int kHalfKeys = kTcBN / 2;
-    constexpr uint32_t kHalfD = D / 2;
-    const uint32_t quad = warp & 3;             // TMEM lanes 32 quad .. 32 quad + 31
-    const uint32_t half = (warp - 2) >> 2;      // 0: warps 2..5, 1: warps 6..9
-    const uint32_t row = quad * 32 + lane;      // the item's row = TMEM lane
-    const uint32_t lane_addr = (quad * 32u) << 16;
-    const bool valid = int32_t(row) < it.rows;
-    const int32_t grow = it.row0 + int32_t(row);
-    const int32_t t = grow / g, hh = grow % g;
-    const int32_t pos = valid ? it.len - it.n + t : -1;  // -1: attends nothing
-    const int32_t lo = W > 0 ? pos + 1 - W : INT32_MIN;
-    // this thread's half of the Q row into its TMEM lane (dims 2c and 2c + 1
-    // in column c, the lower in the low half: a bf16 pair of the row as it
-    // lies in memory), zeros past the item
-    const uint16_t* qr = valid ? p.q + uint64_t(it.qstart + t) * p.q_stride + uint64_t(it.kv_head * g + hh) * D
-                               : nullptr;
-    float rs = p.score_scale;  // the row's score scale (FP8: the row's power-of-two Q scale undone)
-    bool ok = true;
-    uint32_t qw[D / 4];        // this half's D / 2 dims, two per word
-    if constexpr (!kFp8) {
-#pragma unroll
-      for (uint32_t uh = 0; uh < D / 16; ++uh) {
-        const uint4 v = qr ? *reinterpret_cast<const uint4*>(qr + 8 * (half * (D / 16) + uh)) : make_uint4(0, 0, 0, 0);
-        qw[4 * uh] = v.x;
-        qw[4 * uh + 1] = v.y;
-        qw[4 * uh + 2] = v.z;
-        qw[4 * uh + 3] = v.w;
-      }
-    } else {
-      // f16 Q for the f16 S product: the row times 2^e, e chosen so that its
-      // largest magnitude lies in [2^14, 2^15) (the two halves swap maxima)
-      float qv[D / 2];
-      float amax = 0.0f;
-#pragma unroll
-      for (uint32_t uh = 0; uh < D / 16; ++uh) {
-        const uint4 v = qr ? *reinterpret_cast<const uint4*>(qr + 8 * (half * (D / 16) + uh)) : make_uint4(0, 0, 0, 0);
-        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          qv[8 * uh + 2 * j] = bf16_lo_to_f32(w4[j]);
-          qv[8 * uh + 2 * j + 1] = bf16_hi_to_f32(w4[j]);
-          amax = fmaxf(amax, fmaxf(fabsf(qv[8 * uh + 2 * j]), fabsf(qv[8 * uh + 2 * j + 1])));
-        }
-      }
-      s_qamax[half][row] = amax;
-      mbar_arrive(&qamax_bar[quad]);
-      ok = __all_sync(0xffffffffu, mbar_wait(&qamax_bar[quad], 0));
-      amax = fmaxf(amax, s_qamax[half ^ 1][row]);
-      int e = 0;
-      if (amax > 0.0f && amax < INFINITY) {
-        int ex;
-        frexpf(amax, &ex);
-        e = 15 - ex;
-      }
-      const float sc = ldexpf(1.0f, e);
-      rs = p.score_scale * ldexpf(1.0f, -e);
-#pragma unroll
-      for (uint32_t w = 0; w < D / 4; ++w) qw[w] = f32x2_to_f16x2(qv[2 * w] * sc, qv[2 * w + 1] * sc);
-    }
-    const uint32_t q_col = tmem + lane_addr + Lay::kQCol + half * (D / 4);
-    if constexpr (D == 128) {
-      tmem_st32(q_col, qw);
-    } else {
-      static_assert(D == 64, "head_dim 64 or 128");
-      tmem_st16(q_col, qw);
-    }
-    tmem_wait_st();
-    tc_fence_before();
-    mbar_arrive(&q_full);
-
-    float m_run = -INFINITY, l_run = 0.0f;
-    for (int32_t i = 0; i < T && ok; ++i) {
-      const uint32_t b = uint32_t(i) % Lay::kSBufs, st = uint32_t(i) % kTcStages, xb = uint32_t(i) & 1;
-      ok = __all_sync(0xffffffffu, mbar_wait(&s_full[b], uint32_t(i / Lay::kSBufs) & 1));
-      if (!ok) break;
-      tc_fence_after();
-      uint32_t sv[kHalfKeys];
-#pragma unroll
-      for (int c = 0; c < kHalfKeys / 32; ++c)
-        tmem_ld32(tmem + lane_addr + b * kTcBN + half * kHalfKeys + 32 * c,
-                  *reinterpret_cast<uint32_t(*)[32]>(&sv[32 * c]));
-      tmem_wait_ld();
-      // raw scores; max and exponent work on s * score_scale (score_scale > 0)
-      float x[kHalfKeys];
-#pragma unroll
-      for (int j = 0; j < kHalfKeys; ++j) x[j] = __uint_as_float(sv[j]);
-      const int32_t key_base = (t_begin + i) * kTcBN + int32_t(half) * kHalfKeys;
-      if (key_base + kHalfKeys - 1 > pos || key_base < lo) {
-#pragma unroll
-        for (int j = 0; j < kHalfKeys; ++j)
-          if (key_base + j > pos || key_base + j < lo) x[j] = -INFINITY;
-      }
-      float xm8[8];
-#pragma unroll
-      for (int q = 0; q < 8; ++q) xm8[q] = x[q];
-#pragma unroll
-      for (int j = 8; j < kHalfKeys; ++j) xm8[j & 7] = fmaxf(xm8[j & 7], x[j]);
-      float xm = fmaxf(fmaxf(fmaxf(xm8[0], xm8[1]), fmaxf(xm8[2], xm8[3])),
-                       fmaxf(fmaxf(xm8[4], xm8[5]), fmaxf(xm8[6], xm8[7])));
-      // the row's other half: partial maxima swap through a per-tile-parity
-      // slot and the quarter's mbarrier (bounded wait)
-      s_xchg[xb][half][row] = xm;
-      mbar_arrive(&xchg_bar[quad][xb]);
-      ok = __all_sync(0xffffffffu, mbar_wait(&xchg_bar[quad][xb], (uint32_t(i) >> 1) & 1));
-      if (!ok) break;
-      xm = fmaxf(xm, s_xchg[xb][half ^ 1][row]);
-      // The row's reference max moves only when the tile max exceeds it by
-      // more than kRescaleLog2 (or on its first finite score): softmax does
-      // not depend on the reference, the weights stay below 2^kRescaleLog2,
-      // and the O rescale -- which must wait for the previous PV -- is rare.
-      const float tile_max = xm * rs;
-      const float mx = (m_run == -INFINITY || tile_max > m_run + kRescaleLog2) ? fmaxf(m_run, tile_max) : m_run;
-      const float mb = mx == -INFINITY ? 0.0f : mx;  // a row with nothing attended yet stays at zero
-      // E4M3 V: the weights are formed as 2^7 P (<= 2^15), so that their f16
-      // parts stay above the f16 subnormal range down to P = 2^-21; the sum l
-      // takes the same factor
-      const float mbp = kFp8V ? mb - 7.0f : mb;
-      float sum8[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-      for (int j = 0; j < kHalfKeys; ++j) {
-        x[j] = fast_exp2(fmaf(x[j], rs, -mbp));
-        sum8[j & 7] += x[j];
-      }
-      const float sum = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
-      const float al = fast_exp2(m_run - mb);  // 1 when the max did not move, 0 before the first key
-      // both warps of a quarter see the same rows and maxima: the same choice
-      const bool rescale = i > 0 && __any_sync(0xffffffffu, mx != m_run);
-      // O changes only when every PV so far is done (tile i - 1's)
-      if (rescale) {
-        ok = __all_sync(0xffffffffu,
-                        mbar_wait(&o_full[(i - 1) % Lay::kSBufs], uint32_t((i - 1) / Lay::kSBufs) & 1));
-        if (!ok) break;
-        tc_fence_after();
-      }
-      if (rescale) {
-#pragma unroll
-        for (uint32_t c0 = 0; c0 < kHalfD; c0 += 32) {
-          uint32_t ov[32];
-          const uint32_t col = tmem + lane_addr + Lay::kOCol + half * kHalfD + c0;
-          tmem_ld32(col, ov);
-          tmem_wait_ld();
-#pragma unroll
-          for (int j = 0; j < 32; ++j) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * al);
-          tmem_st32(col, ov);
-        }
-        tmem_wait_st();
-      }
-      l_run = l_run * al + sum;
-      m_run = mx;
-      // the last tile's V rows at or past k_hi were not loaded, or hold
-      // positions past every query: zero them for the PV product
-      const int32_t tile_base = (t_begin + i) * kTcBN;
-      // (E4M3 V: warp 10 zeroes those rows as it converts the tile)
-      const bool zero_v = !kFp8V && tile_base + kTcBN > k_hi;
-      if (zero_v) {
-        // V of this tile must have landed before its tail rows are zeroed
-        ok = __all_sync(0xffffffffu, mbar_wait(&v_full[st], (uint32_t(i) / kTcStages) & 1));
-        if (!ok) break;
-        const int32_t z0 = k_hi - tile_base > 0 ? k_hi - tile_base : 0;
-        uint8_t* vb = smem + Lay::kStage0 + st * Lay::kStageBytes + Lay::kKBytes;
-        const uint32_t units = uint32_t(kTcBN - z0) * kChunks * 8;
-        for (uint32_t e = threadIdx.x - 64; e < units; e += 256) {
-          const uint32_t r = uint32_t(z0) + e / (kChunks * 8), rest = e % (kChunks * 8);
-          *reinterpret_cast<uint4*>(vb + (rest >> 3) * (kTcBN * 128) + r * 128 + ((rest & 7) << 4)) =
-              make_uint4(0, 0, 0, 0);
-        }
-      }
-      // this thread's keys of the P hi / lo rows, into the tile's S buffer in
-      // TMEM (two keys per column; both halves of the row have read their S
-      // values before either passed the max swap). BF16 V: hi is the
-      // weight's top 16 bits and lo the top 16 bits of the (exact) remainder,
-      // both truncations, so |P - hi - lo| < 2^-15 P. E4M3 V: f16 parts, hi
-      // the weight truncated to 11 significant bits and lo the exact
-      // remainder rounded to f16, so |P - hi - lo| <= max(2^-21 P, 2^-24)
-      // (the absolute term where lo or hi falls into f16's subnormals); the
-      // row's largest weight is at least 2^7, so either is far below the
-      // row sum's rounding
-#pragma unroll
-      for (int c = 0; c < kHalfKeys / 64; ++c) {
-        uint32_t hi[32], lw[32];
-#pragma unroll
-        for (int q = 0; q < 32; ++q) {
-          const float x0 = x[64 * c + 2 * q], x1 = x[64 * c + 2 * q + 1];
-          if constexpr (kFp8V) {
-            const float h0 = __uint_as_float(__float_as_uint(x0) & 0xffffe000u);
-            const float h1 = __uint_as_float(__float_as_uint(x1) & 0xffffe000u);
-            hi[q] = f32x2_to_f16x2(h0, h1);
-            lw[q] = f32x2_to_f16x2(x0 - h0, x1 - h1);
-          } else {
-            const uint32_t b0 = __float_as_uint(x0), b1 = __float_as_uint(x1);
-            hi[q] = __byte_perm(b0, b1, 0x7632u);
-            const float r0 = x0 - __uint_as_float(b0 & 0xffff0000u);
-            const float r1 = x1 - __uint_as_float(b1 & 0xffff0000u);
-            lw[q] = __byte_perm(__float_as_uint(r0), __float_as_uint(r1), 0x7632u);
-          }
-        }
-        const uint32_t pt = tmem + lane_addr + b * kTcBN + half * (kHalfKeys / 2) + 32 * c;
-        tmem_st32(pt, hi);
-        tmem_st32(pt + kTcBN / 2, lw);
-      }
-      tmem_wait_st();
-      if (zero_v) fence_async_smem();  // the zeroed V rows, for the MMA
-      tc_fence_before();
-      mbar_arrive(&p_full[b]);
-    }
-    if (!ok && lane == 0) atomicOr(&g_prefill_error, kErrWaitTimeout);
-    // ---- O / l to the output row (each thread its half of the columns)
-    s_lsum[half][row] = l_run;
-    mbar_arrive(&lsum_bar[quad]);
-    bool done = __all_sync(0xffffffffu, ok && mbar_wait(&lsum_bar[quad], 0));
-    const float l_row = l_run + s_lsum[half ^ 1][row];
-    if (done && T > 0) {
-      done = __all_sync(0xffffffffu,
-                        mbar_wait(&o_full[(T - 1) % Lay::kSBufs], uint32_t((T - 1) / Lay::kSBufs) & 1));
-      tc_fence_after();
-    }
-    // (E4M3 V: the PV product summed codes; v_scale dequantises them)
-    const float inv = l_row > 0.0f ? (kFp8V ? p.out_scale : 1.0f) / l_row : 0.0f;
-    float* o = valid ? p.output + (uint64_t(it.qstart + t) * p.num_q_heads + uint64_t(it.kv_head * g + hh)) * D +
-                           half * kHalfD
-                     : nullptr;
-#pragma unroll
-    for (uint32_t c0 = 0; c0 < kHalfD; c0 += 32) {
-      uint32_t ov[32];
-      if (done && T > 0) {
-        tmem_ld32(tmem + lane_addr + Lay::kOCol + half * kHalfD + c0, ov);
-        tmem_wait_ld();
-      }
-      if (o && done) {
-#pragma unroll
-        for (int j = 0; j < 32; j += 4) {
-          const float4 w4 = T > 0 ? make_float4(__uint_as_float(ov[j]) * inv, __uint_as_float(ov[j + 1]) * inv,
-                                                __uint_as_float(ov[j + 2]) * inv, __uint_as_float(ov[j + 3]) * inv)
-                                  : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-          *reinterpret_cast<float4*>(o + c0 + j) = w4;
-        }
-      }
-    }
-  }
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem, Lay::kTmemCols);
-  }
-}
-
 // ------------------------------------------------- the two-tile kernel
-// BF16, E4M3-K / BF16-V (kFp8) or, for head_dim 128, E4M3 K and V (kFp8V)
-// caches. One CTA per (sequence, KV head, block of 256 rows): two
+// BF16, E4M3-K / BF16-V (kFp8) or E4M3 K and V (kFp8V) caches. One CTA per (sequence, KV head, block of 256 rows): two
 // 128-row Q tiles, A (rows 0..127) and B (rows 128..255), share every K/V
 // tile the CTA loads. Each Q tile has its own S/P and O in tensor memory
 // (S_A [0, 128), O_A [128, 128 + D), S_B [256, 384), O_B [384, 384 + D)); Q
@@ -840,11 +269,13 @@ __global__ void __launch_bounds__(tc_threads<kFp8>(), 1)
 //     warp 0      TMA producer of 128-key K tiles, warp 2 of V tiles, each a
 //                 2-stage ring whose stage is free once the MMA thread's
 //                 commit after its last reader has arrived on its empty
-//                 barrier; with an E4M3 V cache warp 2 loads each V tile
-//                 into the upper half of its f16 stage and converts it in
-//                 place before it loads the next (E4M3 row r lies where
-//                 the f16 tile's second chunk puts row r, and a lane reads
-//                 the whole row before it writes);
+//                 barrier; with an E4M3 V cache warp 2 converts each V
+//                 tile into its f16 stage before it loads the next: at
+//                 head_dim 128 in place, the tile loaded into the upper
+//                 half of its f16 stage (E4M3 row r lies where the f16
+//                 tile's second chunk puts row r, and a lane reads the
+//                 whole row before it writes), at head_dim 64 from a ring
+//                 of its own;
 //     warp 1      owns TMEM (all 512 columns) and issues every tcgen05.mma;
 //     warp 3      with an E4M3 K cache: turns each E4M3 K tile, loaded by
 //                 warp 0 into a ring of its own, into the f16 K stage the
@@ -853,7 +284,7 @@ __global__ void __launch_bounds__(tc_threads<kFp8>(), 1)
 //     A and of tile B, one thread per row (TMEM lane) over all 128 keys of a
 //     tile, so no row is shared between threads; they also write the Q rows
 //     (with an E4M3 K cache: as f16, the row scaled by a power of two that
-//     the row's score scale undoes, as in the one-tile kernel) and, with a
+//     the row's score scale undoes) and, with a
 //     BF16 V cache, convert V tile j + 1 in place (each warpgroup half of
 //     it) right after publishing their P of tile j, off the path of that
 //     tile's PV product (one warp converting a whole tile per cycle became
@@ -872,9 +303,8 @@ __host__ __device__ constexpr uint32_t tc2_regs_high() { return kFp8V ? 208u : 1
 static_assert(128 * tc2_regs_low<false>() + 256 * tc2_regs_high<false>() <= 384 * 168, "register split");
 static_assert(128 * tc2_regs_low<true>() + 256 * tc2_regs_high<true>() <= 384 * 168, "register split");
 
-template <int D, bool kFp8>
-struct Tc2Layout {  // byte offsets from the 1024-aligned shared base; an E4M3 V tile lands
-                    // inside its f16 V stage and needs no ring of its own
+template <int D, bool kFp8, bool kFp8V>
+struct Tc2Layout {  // byte offsets from the 1024-aligned shared base
   static constexpr uint32_t kChunks = D / 64;
   static constexpr uint32_t kQBytes = kChunks * kTcBM * 128;  // one Q tile [chunk][128 rows][128 B]
   static constexpr uint32_t kQ0 = 0;
@@ -887,7 +317,13 @@ struct Tc2Layout {  // byte offsets from the 1024-aligned shared base; an E4M3 V
   static constexpr uint32_t kK8Chunks = (D + 127) / 128;
   static constexpr uint32_t kK8Bytes = kFp8 ? kK8Chunks * kTcBN * kE4Row : 0;
   static constexpr uint32_t kK80 = kStage0 + kTcStages * kStageBytes;
-  static constexpr uint32_t kBytes = kK80 + kTcStages * kK8Bytes;
+  // E4M3 V as loaded: at head_dim 128 a V tile lands inside its f16 V stage
+  // (converted in place, no ring of its own: the shared memory is full);
+  // at head_dim 64 in a ring of its own, [128 keys][64 B]
+  static constexpr bool kV8Ring = kFp8V && D == 64;
+  static constexpr uint32_t kV8Bytes = kV8Ring ? kTcBN * kE4Row : 0;
+  static constexpr uint32_t kV80 = kK80 + kTcStages * kK8Bytes;
+  static constexpr uint32_t kBytes = kV80 + kTcStages * kV8Bytes;
   static constexpr uint32_t kTmemCols = 512;
   // tile t's S/P columns and O columns
   static __device__ __forceinline__ constexpr uint32_t s_col(uint32_t t) { return t << 8; }
@@ -899,8 +335,7 @@ __global__ void __launch_bounds__(32 * 12, 1)
     prefill_tc2_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                        const PrefillParams p) {
   static_assert(kFp8 || !kFp8V, "an E4M3 V cache comes with an E4M3 K cache");
-  static_assert(!kFp8V || D == 128, "the in-place V conversion needs the 128-dim layout");
-  using Lay = Tc2Layout<D, kFp8>;
+  using Lay = Tc2Layout<D, kFp8, kFp8V>;
   constexpr uint32_t kChunks = Lay::kChunks;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -971,36 +406,41 @@ __global__ void __launch_bounds__(32 * 12, 1)
     uint64_t* empty = is_k ? (kFp8 ? k8_empty : k_empty) : v_empty;
     const uint32_t chunks = e4m3 ? Lay::kK8Chunks : kChunks;
     const uint32_t row_bytes = e4m3 ? Lay::kE4Row : 128u;  // of a key's row per box
-    // E4M3 V tile j -> its f16 stage, in place; rows at or past the item's
-    // last key (not loaded, or positions past every query) become zeros
+    // E4M3 V tile j -> its f16 stage (in place at head_dim 128, from its own
+    // ring at head_dim 64); rows at or past the item's last key (not
+    // loaded, or positions past every query) become zeros
     auto convert_v = [&](int32_t j) -> bool {
       const uint32_t sj = uint32_t(j) % kTcStages;
       if (!__all_sync(0xffffffffu, mbar_wait(&v8_full[sj], uint32_t(j / kTcStages) & 1))) return false;
       uint8_t* vt = smem + Lay::kStage0 + sj * Lay::kStageBytes + Lay::kKBytes;  // [chunk][128 keys][128 B]
       const int32_t live = k_hi - (t_begin + j) * kTcBN;
+      if constexpr (Lay::kV8Ring) {
+        e4m3_tile_to_f16<D>(smem + Lay::kV80 + sj * Lay::kV8Bytes, vt, live, lane);
+      } else {
 #pragma unroll 1
-      for (uint32_t r = lane; r < uint32_t(kTcBN); r += 32) {
-        uint8_t* row1 = vt + kTcBN * 128 + r * 128;  // the E4M3 row, and the f16 tile's chunk 1 row r
-        uint4 w[8];
+        for (uint32_t r = lane; r < uint32_t(kTcBN); r += 32) {
+          uint8_t* row1 = vt + kTcBN * 128 + r * 128;  // the E4M3 row, and the f16 tile's chunk 1 row r
+          uint4 w[8];
 #pragma unroll
-        for (uint32_t u = 0; u < 8; ++u) w[u] = *reinterpret_cast<const uint4*>(row1 + ((u ^ (r & 7)) << 4));
-        if (int32_t(r) >= live) {
+          for (uint32_t u = 0; u < 8; ++u) w[u] = *reinterpret_cast<const uint4*>(row1 + ((u ^ (r & 7)) << 4));
+          if (int32_t(r) >= live) {
 #pragma unroll
-          for (uint32_t u = 0; u < 8; ++u) w[u] = make_uint4(0u, 0u, 0u, 0u);
-        }
-#pragma unroll
-        for (uint32_t u = 0; u < 8; ++u) {  // dims 16 u ..: f16 chunk u / 4, units 2 (u % 4) and + 1
-          const uint32_t ws[4] = {w[u].x, w[u].y, w[u].z, w[u].w};
-          uint32_t h[8];
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            h[2 * q] = e4m3x2_to_f16x2(uint16_t(ws[q]));
-            h[2 * q + 1] = e4m3x2_to_f16x2(uint16_t(ws[q] >> 16));
+            for (uint32_t u = 0; u < 8; ++u) w[u] = make_uint4(0u, 0u, 0u, 0u);
           }
-          const uint32_t u0 = 2 * (u & 3);
-          uint8_t* drow = vt + (u >> 2) * (kTcBN * 128) + r * 128;
-          *reinterpret_cast<uint4*>(drow + ((u0 ^ (r & 7)) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
-          *reinterpret_cast<uint4*>(drow + (((u0 + 1) ^ (r & 7)) << 4)) = make_uint4(h[4], h[5], h[6], h[7]);
+#pragma unroll
+          for (uint32_t u = 0; u < 8; ++u) {  // dims 16 u ..: f16 chunk u / 4, units 2 (u % 4) and + 1
+            const uint32_t ws[4] = {w[u].x, w[u].y, w[u].z, w[u].w};
+            uint32_t h[8];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              h[2 * q] = e4m3x2_to_f16x2(uint16_t(ws[q]));
+              h[2 * q + 1] = e4m3x2_to_f16x2(uint16_t(ws[q] >> 16));
+            }
+            const uint32_t u0 = 2 * (u & 3);
+            uint8_t* drow = vt + (u >> 2) * (kTcBN * 128) + r * 128;
+            *reinterpret_cast<uint4*>(drow + ((u0 ^ (r & 7)) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
+            *reinterpret_cast<uint4*>(drow + (((u0 + 1) ^ (r & 7)) << 4)) = make_uint4(h[4], h[5], h[6], h[7]);
+          }
         }
       }
       fence_async_smem();
@@ -1035,10 +475,13 @@ __global__ void __launch_bounds__(32 * 12, 1)
         const int32_t slot0 = (block_id << p.block_shift) + (key0 & int32_t(p.block_size - 1));
 #endif
         // E4M3 K: its own ring; E4M3 V: the upper half of its f16 stage
-        uint8_t* dst = smem + (is_k ? (e4m3 ? Lay::kK80 + st * Lay::kK8Bytes : Lay::kStage0 + st * Lay::kStageBytes)
-                                    : Lay::kStage0 + st * Lay::kStageBytes + Lay::kKBytes +
-                                          (e4m3 ? kTcBN * 128u : 0u)) +
-                       lane * (kSub * row_bytes);
+        // (head_dim 128) or its own ring (head_dim 64)
+        uint8_t* dst =
+            smem +
+            (is_k ? (e4m3 ? Lay::kK80 + st * Lay::kK8Bytes : Lay::kStage0 + st * Lay::kStageBytes)
+                  : (Lay::kV8Ring ? Lay::kV80 + st * Lay::kV8Bytes
+                                  : Lay::kStage0 + st * Lay::kStageBytes + Lay::kKBytes + (e4m3 ? kTcBN * 128u : 0u))) +
+            lane * (kSub * row_bytes);
         for (uint32_t c = 0; c < chunks; ++c)
           tma_load_3d(dst + c * (kTcBN * row_bytes), map, 0, slot0, it.kv_head * chunks + c, &full[st]);
       }
@@ -1450,7 +893,7 @@ int launch_prefill_tc2(const PrefillArgs& a, cudaStream_t stream, PrefillParams&
   if (grid == 0) return KV_OK;
   if (grid > 0x7fffffffull) return KV_ERR_UNSUPPORTED;
   // all 512 TMEM columns: no second CTA may be resident on an SM
-  constexpr int kNeed = int(1024 + Tc2Layout<D, kFp8>::kBytes);
+  constexpr int kNeed = int(1024 + Tc2Layout<D, kFp8, kFp8V>::kBytes);
   const int smem = kNeed > 120 * 1024 ? kNeed : 120 * 1024;
   auto kern = prefill_tc2_kernel<D, kFp8, kFp8V>;
   static int set_bytes[64] = {0};
@@ -1462,36 +905,6 @@ int launch_prefill_tc2(const PrefillArgs& a, cudaStream_t stream, PrefillParams&
     set_bytes[dev_id] = smem;
   }
   kern<<<unsigned(grid), 32 * 12, smem, stream>>>(mk, mv, p);
-  return cudaGetLastError() == cudaSuccess ? KV_OK : KV_ERR_CUDA;
-}
-
-template <int D, bool kFp8, bool kFp8V>
-int launch_prefill_tc(const PrefillArgs& a, cudaStream_t stream, PrefillParams& p) {
-  CUtensorMap mk, mv;
-  // one 128-byte chunk per box: each box lands in its chunk's [128 keys] tile
-  if (!encode_pool_map(&mk, a.k_cache, kFp8, a.num_kv_heads, D, 1, 1) ||
-      !encode_pool_map(&mv, a.v_cache, kFp8V, a.num_kv_heads, D, 1, 1))
-    return KV_ERR_CUDA;
-  // grid: an upper bound of the item count, sum over sequences of
-  // ceil(n_s * group / 128) <= num_q_tokens * group / 128 + num_seqs
-  const uint64_t grid =
-      uint64_t(a.num_kv_heads) * ((uint64_t(a.num_q_tokens) * p.group + kTcBM - 1) / kTcBM + a.num_seqs);
-  if (grid == 0) return KV_OK;
-  if (grid > 0x7fffffffull) return KV_ERR_UNSUPPORTED;
-  // The kernel takes all 512 TMEM columns: ask for enough shared memory that
-  // no second CTA of it is resident on an SM (it would wait in tcgen05.alloc)
-  constexpr int kNeed = int(1024 + TcLayout<D, kFp8, kFp8V>::kBytes);
-  const int smem = kNeed > 120 * 1024 ? kNeed : 120 * 1024;
-  auto kern = prefill_tc_kernel<D, kFp8, kFp8V>;
-  static int set_bytes[64] = {0};
-  const int dev_id = device_info().device;
-  if (dev_id < 0 || dev_id >= 64) return KV_ERR_CUDA;
-  if (set_bytes[dev_id] < smem) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-      return KV_ERR_CUDA;
-    set_bytes[dev_id] = smem;
-  }
-  kern<<<unsigned(grid), tc_threads<kFp8>(), smem, stream>>>(mk, mv, p);
   return cudaGetLastError() == cudaSuccess ? KV_OK : KV_ERR_CUDA;
 }
 
@@ -1522,7 +935,7 @@ int launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
     case 128: return launch_prefill_tc2<128, false, false>(a, stream, p);
     case 164: return launch_prefill_tc2<64, true, false>(a, stream, p);
     case 228: return launch_prefill_tc2<128, true, false>(a, stream, p);
-    case 264: return launch_prefill_tc<64, true, true>(a, stream, p);
+    case 264: return launch_prefill_tc2<64, true, true>(a, stream, p);
     case 328: return launch_prefill_tc2<128, true, true>(a, stream, p);
     default: return KV_ERR_UNSUPPORTED;
   }
