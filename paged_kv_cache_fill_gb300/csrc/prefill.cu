@@ -246,9 +246,9 @@ __device__ Item locate(uint32_t target, const PrefillParams& p, uint32_t lane, u
 constexpr float kRescaleLog2 = 8.0f;  // reference-max slack of the online softmax (base 2)
 
 // ------------------------------------------------- the two-tile kernel
-// BF16, E4M3-K / BF16-V (kFp8) or E4M3 K and V (kFp8V) caches. One CTA per (sequence, KV head, block of 256 rows): two
-// 128-row Q tiles, A (rows 0..127) and B (rows 128..255), share every K/V
-// tile the CTA loads. Each Q tile has its own S/P and O in tensor memory
+// BF16, E4M3-K / BF16-V (kFp8) or E4M3 K and V (kFp8V) caches. One CTA
+// per (sequence, KV head, block of 256 rows): two 128-row Q tiles, A (rows
+// 0..127) and B (rows 128..255), share every K/V tile the CTA loads. Each Q tile has its own S/P and O in tensor memory
 // (S_A [0, 128), O_A [128, 128 + D), S_B [256, 384), O_B [384, 384 + D)); Q
 // lives in shared memory (the S product's A operand). A tile's S product
 // writes the columns its P occupied, so it must wait until the tile's PV
