@@ -716,77 +716,52 @@ __global__ void __launch_bounds__(32 * 9, two_ctas_per_sm<kFp8V, D, NT>() ? 2 : 
 
 // Merge the partials of every (sequence, query head) whose sequence was cut
 // into more than one piece: o = sum_i 2^(m_i - M) acc_i / sum_i 2^(m_i - M) l_i,
-// in piece order. One CTA of D threads per (sequence, query head): the
-// pieces' (m, l) are reduced across the threads, then each thread sums its
-// output element over the pieces with independent (overlapping) loads. A
-// sequence with no positions has no piece in the tile stream: its output
-// row is written as zeros here.
-constexpr int kCombineMaxSplits = 1024;  // per pass through shared memory
+// in piece order, in one pass: M is the running max of the pieces' maxima,
+// and the sums so far are scaled by 2^(M_old - M_new) when it moves. One
+// warp per (sequence, query head), lane k holding dims k, k + 32, ...: the
+// piece count, then each piece's (m, l) and the lane's dims of its partial
+// output, whose loads do not depend on one another. A sequence with no
+// positions has no piece in the tile stream: its output row is written as
+// zeros here.
+constexpr uint32_t kCombineWarps = 8;  // per CTA
 
 template <int D>
-__global__ void __launch_bounds__(D) combine_kernel(const DecodeParams p) {
-  __shared__ float s_w[kCombineMaxSplits];
-  __shared__ float s_red[D / 32];
-  __shared__ float s_bcast;
-  const uint32_t s = blockIdx.x, h = blockIdx.y;
-  const uint32_t t = threadIdx.x, lane = t & 31, warp = t >> 5;
+__global__ void __launch_bounds__(32 * kCombineWarps) combine_kernel(const DecodeParams p) {
+  const uint32_t lane = threadIdx.x & 31;
+  const uint64_t item = uint64_t(blockIdx.x) * kCombineWarps + (threadIdx.x >> 5);  // s * Hq + h
+  if (item >= uint64_t(p.num_seqs) * p.num_q_heads) return;
+  const uint32_t s = uint32_t(item / p.num_q_heads), h = uint32_t(item % p.num_q_heads);
+  float* out = p.output + item * D;
   const SeqSpan span = seq_span(__ldg(p.seq_lens + s), p);
   if (span.ntiles == 0) {
-    p.output[(uint64_t(s) * p.num_q_heads + h) * D + t] = 0.0f;
+#pragma unroll
+    for (uint32_t k = 0; k < D / 32; ++k) out[lane + 32 * k] = 0.0f;
     return;
   }
   const uint32_t hg = h / p.group / p.heads_per_item;
   const int32_t nsplit = int32_t(__ldg(p.ws_count + uint64_t(s) * p.num_head_groups + hg));
   if (nsplit <= 1) return;
-  const uint64_t row0 = uint64_t(s) * p.max_splits * p.num_q_heads + h;  // split i at row0 + i*Hq
-  auto block_reduce = [&](float v, bool is_max) -> float {
+  const uint64_t row0 = uint64_t(s) * p.max_splits * p.num_q_heads + h;  // piece i at row0 + i * Hq
+  float M = -INFINITY, den = 0.0f, acc[D / 32];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float u = __shfl_xor_sync(0xffffffffu, v, o);
-      v = is_max ? fmaxf(v, u) : v + u;
-    }
-    if (lane == 0) s_red[warp] = v;
-    __syncthreads();
-    if (t == 0) {
-      float r = s_red[0];
-      for (int w = 1; w < D / 32; ++w) r = is_max ? fmaxf(r, s_red[w]) : r + s_red[w];
-      s_bcast = r;
-    }
-    __syncthreads();
-    const float r = s_bcast;
-    __syncthreads();
-    return r;
-  };
-  // global max of the splits' running maxima
-  float m = -INFINITY;
-  for (int32_t i = t; i < nsplit; i += D)
-    m = fmaxf(m, p.ws_ml[(row0 + uint64_t(i) * p.num_q_heads) * 2]);
-  const float M = block_reduce(m, true);
-  float num = 0.0f, den_part = 0.0f;
-  for (int32_t base = 0; base < nsplit; base += kCombineMaxSplits) {
-    const int32_t n = nsplit - base < kCombineMaxSplits ? nsplit - base : kCombineMaxSplits;
-    for (int32_t i = t; i < n; i += D) {
-      const float2 ml = *reinterpret_cast<const float2*>(p.ws_ml + (row0 + uint64_t(base + i) * p.num_q_heads) * 2);
-      const float w = fast_exp2(ml.x - M);
-      s_w[i] = w;
-      den_part += w * ml.y;
-    }
-    __syncthreads();
-    const float* src = p.ws_o + (row0 + uint64_t(base) * p.num_q_heads) * D + t;
-    const uint64_t step = uint64_t(p.num_q_heads) * D;
-    int32_t i = 0;
-    for (; i + 8 <= n; i += 8) {
-      float v[8];
+  for (uint32_t k = 0; k < D / 32; ++k) acc[k] = 0.0f;
+#pragma unroll 4
+  for (int32_t i = 0; i < nsplit; ++i) {
+    const uint64_t row = row0 + uint64_t(i) * p.num_q_heads;
+    const float2 ml = *reinterpret_cast<const float2*>(p.ws_ml + row * 2);
+    float v[D / 32];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) v[u] = src[uint64_t(i + u) * step];
+    for (uint32_t k = 0; k < D / 32; ++k) v[k] = p.ws_o[row * D + lane + 32 * k];
+    const float Mn = fmaxf(M, ml.x);
+    const float a = M == -INFINITY ? 0.0f : fast_exp2(M - Mn);
+    const float w = ml.x == -INFINITY ? 0.0f : fast_exp2(ml.x - Mn);
+    den = den * a + w * ml.y;
 #pragma unroll
-      for (int u = 0; u < 8; ++u) num += s_w[i + u] * v[u];
-    }
-    for (; i < n; ++i) num += s_w[i] * src[uint64_t(i) * step];
-    __syncthreads();
+    for (uint32_t k = 0; k < D / 32; ++k) acc[k] = acc[k] * a + w * v[k];
+    M = Mn;
   }
-  const float den = block_reduce(den_part, false);
-  p.output[(uint64_t(s) * p.num_q_heads + h) * D + t] = num / den;
+#pragma unroll
+  for (uint32_t k = 0; k < D / 32; ++k) out[lane + 32 * k] = acc[k] / den;
 }
 
 // ---------------------------------------------------------------- host side
@@ -899,8 +874,8 @@ int launch_decode_t(const DecodeArgs& a, cudaStream_t stream, const Geometry& ge
   kern<<<dev.num_sms * geo.ctas_per_sm, threads, geo.smem_bytes, stream>>>(mk, mv, p);
   if (cudaGetLastError() != cudaSuccess) return KV_ERR_CUDA;
   if (p.max_splits > 0) {
-    dim3 grid(p.num_seqs, p.num_q_heads);
-    combine_kernel<D><<<grid, D, 0, stream>>>(p);
+    const uint64_t items = uint64_t(p.num_seqs) * p.num_q_heads;
+    combine_kernel<D><<<unsigned((items + kCombineWarps - 1) / kCombineWarps), 32 * kCombineWarps, 0, stream>>>(p);
     if (cudaGetLastError() != cudaSuccess) return KV_ERR_CUDA;
   }
   return KV_OK;
