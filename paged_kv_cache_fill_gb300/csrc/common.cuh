@@ -229,6 +229,14 @@ __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence:
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
+// max(a, b, c) in one instruction (three-input max.f32; NaN inputs are
+// ignored as fmaxf ignores them)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 // Bulk copy of `bytes` (a multiple of 16; both addresses 16-byte aligned)
 // from this CTA's shared memory to global memory, in this thread's bulk
 // group; bulk_store_wait_read() returns once every such copy the thread

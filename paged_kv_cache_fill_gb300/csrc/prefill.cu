@@ -766,13 +766,19 @@ __global__ void __launch_bounds__(32 * 12, 1)
           for (int k = 0; k < kTcBN; ++k)
             if (key_base + k > pos || key_base + k < lo) x[k] = -INFINITY;
         }
+        // the tile max: eight partial maxima, two scores into each per
+        // three-input max
         float xm8[8];
 #pragma unroll
         for (int q = 0; q < 8; ++q) xm8[q] = x[q];
 #pragma unroll
-        for (int k = 8; k < kTcBN; ++k) xm8[k & 7] = fmaxf(xm8[k & 7], x[k]);
-        const float xm = fmaxf(fmaxf(fmaxf(xm8[0], xm8[1]), fmaxf(xm8[2], xm8[3])),
-                               fmaxf(fmaxf(xm8[4], xm8[5]), fmaxf(xm8[6], xm8[7])));
+        for (int k = 8; k + 8 < kTcBN; k += 16) {
+#pragma unroll
+          for (int q = 0; q < 8; ++q) xm8[q] = fmax3(xm8[q], x[k + q], x[k + 8 + q]);
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) xm8[q] = fmaxf(xm8[q], x[kTcBN - 8 + q]);
+        const float xm = fmax3(fmax3(xm8[0], xm8[1], xm8[2]), fmax3(xm8[3], xm8[4], xm8[5]), fmaxf(xm8[6], xm8[7]));
         // the row's reference max moves only when the tile max exceeds it
         // by more than kRescaleLog2 (or on its first finite score)
         const float tile_max = xm * rs;
