@@ -662,6 +662,27 @@ def test_prefill_bf16_v_range(fp8, log2_scale):
     assert pk.kv_get_device_error() == 0
 
 
+@pytest.mark.parametrize("fp8", [False, True])
+def test_prefill_many_sequences_of_spread_lengths(fp8):
+    """120 sequences with lengths log-uniform in [1, 3000] and 1..32 queries
+    each (GQA 4: single-Q-tile items, the last tile of most), so that the
+    items spread over many length classes and the kernel's longest-first
+    order across sequences must still reach every item once; with and
+    without a window."""
+    rng = np.random.default_rng(77)
+    lens = np.maximum(1, np.round(np.exp(rng.uniform(0, np.log(3000), 120)))).astype(int).tolist()
+    qlens = [int(min(L, rng.integers(1, 33))) for L in lens]
+    w = kvgen.custom(250 + bool(fp8), seq_lens=lens, num_q_heads=16, num_kv_heads=4, head_dim=128,
+                     block_size=16, fp8=fp8, q_rows=sum(qlens))
+    kc, vc, kr, vr = _caches(w, fp8)
+    qsl = np.concatenate([[0], np.cumsum(qlens)]).astype(np.int32)
+    for win in (0, 100):
+        got = _prefill_gpu(w, kc, vc, qsl, win, fp8)
+        ref = _prefill_ref(w, kr, vr, qsl, win, fp8)
+        assert_decode_close(got, ref, f"many sequences, window {win}")
+    assert pk.kv_get_device_error() == 0
+
+
 def test_prefill_one_query_per_sequence_matches_the_decode():
     w = kvgen.custom(230, seq_lens=[4000, 17, 900, 1], num_q_heads=32, num_kv_heads=8, head_dim=128, block_size=16)
     kc, vc, kr, vr = _caches(w, False)
