@@ -279,16 +279,18 @@ constexpr float kRescaleLog2 = 8.0f;  // reference-max slack of the online softm
 //     warp 1      owns TMEM (all 512 columns) and issues every tcgen05.mma;
 //     warp 3      with an E4M3 K cache: turns each E4M3 K tile, loaded by
 //                 warp 0 into a ring of its own, into the f16 K stage the
-//                 S product reads (exact); otherwise idle;
+//                 S product reads (exact); with a BF16 K cache: converts
+//                 the second half of each BF16 V tile (below);
 //   warpgroups 1, 2 (registers raised to tc2_regs_high()): the softmax of tile
 //     A and of tile B, one thread per row (TMEM lane) over all 128 keys of a
 //     tile, so no row is shared between threads; they also write the Q rows
 //     (with an E4M3 K cache: as f16, the row scaled by a power of two that
 //     the row's score scale undoes) and, with a
-//     BF16 V cache, convert V tile j + 1 in place (each warpgroup half of
-//     it) right after publishing their P of tile j, off the path of that
-//     tile's PV product (one warp converting a whole tile per cycle became
-//     the serial path). At the end each thread stages its O / l row in the
+//     BF16 V cache, convert V tile j + 1 in place right after publishing
+//     their P of tile j, off the path of that tile's PV product (each
+//     warpgroup half of it with an E4M3 K cache; with a BF16 K cache a
+//     quarter each, warp 3 the other half: one warp converting a whole
+//     tile per cycle became the serial path). At the end each thread stages its O / l row in the
 //     then free Q tiles and K/V stages and stores it with one bulk copy
 //     (direct stores of a row per thread wrote 16 bytes per 32-byte sector
 //     and took ~3 us per CTA).
@@ -353,7 +355,9 @@ __global__ void __launch_bounds__(32 * 12, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kTcStages; ++s) {
       mbar_init(&k_full[s], kFp8 ? 32 : 1);  // E4M3 K: the converter warp's arrivals
-      mbar_init(&v_full[s], kFp8V ? 32 : 8);  // once the tile is f16: warp 2's lanes, or the softmax warps
+      // once the tile is f16: E4M3 V, warp 2's lanes; BF16 V, the eight
+      // softmax warps (and warp 3 with a BF16 K cache)
+      mbar_init(&v_full[s], kFp8V ? 32 : (kFp8 ? 8 : 9));
       mbar_init(&k_empty[s], 1);
       mbar_init(&v_empty[s], 1);
       mbar_init(&k8_full[s], 1);
@@ -494,6 +498,49 @@ __global__ void __launch_bounds__(32 * 12, 1)
       for (int32_t j = issued > kTcStages ? issued - kTcStages : 0; j < issued; ++j)
         mbar_wait(&full[uint32_t(j) % kTcStages], uint32_t(j / kTcStages) & 1);
     }
+   } else if (!kFp8 && warp == 3) {
+    // ------------------------------------------------------------ BF16 V
+    // With a BF16 K cache this warp is free: it turns the second half of
+    // each BF16 V tile into f16 (the same rounding as the softmax warps'
+    // quarters, below), leaving the softmax warps a quarter each.
+    bool ok = true;
+    const F2 down = f2_make(0.00390625f, 0.00390625f);
+    constexpr uint32_t kHalf = uint32_t(kTcBN) * kChunks * 4;
+    for (int32_t j = 0; j < T && ok; ++j) {
+      const uint32_t sj = uint32_t(j) % kTcStages;
+      ok = __all_sync(0xffffffffu, mbar_wait(&v8_full[sj], uint32_t(j / kTcStages) & 1));
+      if (!ok) break;
+      uint4* units = reinterpret_cast<uint4*>(smem + Lay::kStage0 + sj * Lay::kStageBytes + Lay::kKBytes);
+      const int32_t live = k_hi - (t_begin + j) * kTcBN;
+#pragma unroll 1
+      for (uint32_t e0 = kHalf; e0 < 2 * kHalf; e0 += 8 * 32) {
+        uint4 w[8];
+#pragma unroll
+        for (uint32_t u = 0; u < 8; ++u) w[u] = units[e0 + 32 * u + lane];
+#pragma unroll
+        for (uint32_t u = 0; u < 8; ++u) {
+          uint32_t ws[4] = {w[u].x, w[u].y, w[u].z, w[u].w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float2 f = f2_split(
+                f2_mul(f2_make(__uint_as_float(ws[q] << 16), __uint_as_float(ws[q] & 0xffff0000u)), down));
+            ws[q] = f32x2_to_f16x2(f.x, f.y);
+          }
+          w[u] = make_uint4(ws[0], ws[1], ws[2], ws[3]);
+        }
+        if (live < kTcBN) {
+#pragma unroll
+          for (uint32_t u = 0; u < 8; ++u)
+            if (int32_t(((e0 + 32 * u + lane) >> 3) % uint32_t(kTcBN)) >= live) w[u] = make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (uint32_t u = 0; u < 8; ++u) units[e0 + 32 * u + lane] = w[u];
+      }
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&v_full[sj]);
+    }
+    if (!ok && lane == 0) atomicOr(&g_prefill_error, kErrWaitTimeout);
    } else if (kFp8 && warp == 3) {
     // ------------------------------------------------------------ E4M3 -> f16
     // Each loaded E4M3 K tile into the f16 K stage the S products read
@@ -691,8 +738,10 @@ __global__ void __launch_bounds__(32 * 12, 1)
     } else {
       const uint32_t scol = tmem + lane_addr + Lay::s_col(t);
       const uint32_t ocol = tmem + lane_addr + Lay::o_col(t);
-      // BF16 V tile j -> f16 in place, this warpgroup's half of it (tile A's
-      // warps take both halves when tile B holds no rows): each value times
+      // BF16 V tile j -> f16 in place, part h of it: each warpgroup one part
+      // (tile A's both when tile B holds no rows), a half of the tile with an
+      // E4M3 K cache, a quarter with a BF16 K cache, where warp 3 takes the
+      // second half: each value times
       // 2^-8, rounded to f16 (exact for 2^-6 <= |v| < 2^24, within 2^-17
       // absolute below; the output scale undoes 2^-8). Rows at or past the
       // item's last key (not loaded, or positions past every query) become
@@ -700,8 +749,8 @@ __global__ void __launch_bounds__(32 * 12, 1)
       // the tile ([chunk][128 keys][128 B]) holds key row (e / 8) % 128, and
       // a warp's access covers 32 consecutive units.
       auto convert_v_half = [&](int32_t j, uint32_t h) -> bool {
-        constexpr uint32_t kHalf = uint32_t(kTcBN) * kChunks * 4;  // units per half
-        constexpr uint32_t kPer = kHalf / kTcBM;                    // per thread
+        constexpr uint32_t kHalf = uint32_t(kTcBN) * kChunks * (kFp8 ? 4 : 2);  // units per part
+        constexpr uint32_t kPer = kHalf / kTcBM;                                 // per thread
         const uint32_t sj = uint32_t(j) % kTcStages;
         if (!__all_sync(0xffffffffu, mbar_wait(&v8_full[sj], uint32_t(j / kTcStages) & 1))) return false;
         uint4* units = reinterpret_cast<uint4*>(smem + Lay::kStage0 + sj * Lay::kStageBytes + Lay::kKBytes);
